@@ -1,0 +1,454 @@
+"""Pins for the oracle: it is checked against things other than itself.
+
+* the pages' worked block-table example (tests/golden/worked_block_table.json)
+* brute force (pure-Python loops) and an independent numpy twin on tiny inputs
+* a library routine: torch scaled_dot_product_attention in float64
+* closed-form invariants: weights sum to 1, L=1 returns v_0, equal keys give
+  the mean of V, a dominant score selects its value row, output unchanged
+  under any physical placement, GQA equals MHA with repeated KV heads, the
+  split-K log-sum-exp merge equals the unsplit result
+* masking: NaN in padding slots never reaches a result
+* mutation checks: plausible mistakes planted in a copy of the numpy twin
+  (dropped scale, wrong GQA map, wrong in-block offset, off-by-one mask) are
+  each rejected by at least one of the pins above.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import PoolModel
+
+
+def _bf16(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _random_case(seed, B=3, Hq=4, Hkv=2, D=8, BS=4, lens=(1, 3, 9), NB=None):
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, dtype=np.int32)
+    nblk = (lens + BS - 1) // BS
+    need = int(nblk.sum())
+    NB = NB or need + 3
+    perm = rng.permutation(NB).astype(np.int32)
+    mb = int(nblk.max())
+    tables = np.full((B, mb), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        tables[b, :nblk[b]] = perm[pos:pos + nblk[b]]
+        pos += nblk[b]
+    q = _bf16((B, Hq, D), seed + 1)
+    kc = _bf16((NB, Hkv, BS, D), seed + 2)
+    vc = _bf16((NB, Hkv, BS, D), seed + 3)
+    return q, kc, vc, tables, lens
+
+
+def _sdpa_unpaged(q, K, V, scale=None):
+    """torch SDPA, float64, KV heads repeated to the query heads."""
+    Hq = q.shape[0]
+    G = Hq // K.shape[0]
+    Kr = K.repeat_interleave(G, dim=0)  # [Hq, L, D]
+    Vr = V.repeat_interleave(G, dim=0)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        q[:, None, :], Kr, Vr, scale=scale)  # [Hq, 1, D]
+    return out[:, 0, :]
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_worked_example_slots(golden_dir):
+    gold = json.load(open(os.path.join(golden_dir, "worked_block_table.json")))
+    BS = gold["block_size"]
+    table = gold["block_table"]
+    others = [b for b in range(16) if b not in table]
+    pool = PoolModel(16, BS, free_order=table + others)
+    s = pool.seq_create()
+    slots, cows = pool.append_tokens(s, gold["num_tokens"])
+    assert pool.table(s) == table
+    assert slots == gold["slots"]
+    assert cows == []
+
+
+def test_worked_example_gather_equals_unpaged(golden_dir):
+    gold = json.load(open(os.path.join(golden_dir, "worked_block_table.json")))
+    BS, n = gold["block_size"], gold["num_tokens"]
+    NB, Hkv, D = 12, 1, 4
+    Kt = _bf16((n, D), 11)  # token t's key, in logical order
+    Vt = _bf16((n, D), 12)
+    kc = torch.full((NB, Hkv, BS, D), float("nan"), dtype=torch.bfloat16)
+    vc = kc.clone()
+    for t, slot in enumerate(gold["slots"]):
+        kc[slot // BS, 0, slot % BS] = Kt[t]
+        vc[slot // BS, 0, slot % BS] = Vt[t]
+    q = _bf16((1, 2, D), 13)
+    tables = np.array([gold["block_table"]], dtype=np.int32)
+    lens = np.array([n], dtype=np.int32)
+    got = oracle.paged_decode(q, kc, vc, tables, lens)
+    ref = _sdpa_unpaged(q[0].double(), Kt.double()[None], Vt.double()[None]).numpy()
+    np.testing.assert_allclose(got[0], ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- brute force / twin / library
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_oracle_matches_brute_force(seed):
+    q, kc, vc, tables, lens = _random_case(seed)
+    got = oracle.paged_decode(q, kc, vc, tables, lens)
+    twin = oracle.paged_decode_numpy(q, kc, vc, tables, lens)
+    np.testing.assert_allclose(got, twin, rtol=0, atol=1e-12)
+    qd, kd, vd = (oracle.bf16_to_f64(x) for x in (q, kc, vc))
+    B, Hq, D = qd.shape
+    Hkv, BS = kd.shape[1], kd.shape[2]
+    G = Hq // Hkv
+    for b in range(B):
+        for g in range(Hkv):
+            # contiguous K/V assembled by walking the table with plain loops
+            K, V = [], []
+            for t in range(int(lens[b])):
+                blk = int(tables[b][t // BS])
+                K.append(list(kd[blk, g, t % BS]))
+                V.append(list(vd[blk, g, t % BS]))
+            ref = oracle.brute_force_decode([list(qd[b, h]) for h in range(g * G, g * G + G)],
+                                            K, V, 1.0 / math.sqrt(D))
+            np.testing.assert_allclose(got[b, g * G:(g + 1) * G], np.array(ref), rtol=0, atol=1e-12)
+
+
+def test_identity_table_equals_library_sdpa():
+    B, Hq, Hkv, D, BS = 2, 8, 2, 16, 4
+    lens = np.array([13, 7], dtype=np.int32)
+    mb = 4
+    tables = np.arange(B * mb, dtype=np.int32).reshape(B, mb)
+    q = _bf16((B, Hq, D), 21)
+    kc = _bf16((B * mb, Hkv, BS, D), 22)
+    vc = _bf16((B * mb, Hkv, BS, D), 23)
+    got = oracle.paged_decode(q, kc, vc, tables, lens)
+    for b in range(B):
+        L = int(lens[b])
+        K = kc[b * mb:(b + 1) * mb].double().permute(1, 0, 2, 3).reshape(Hkv, mb * BS, D)[:, :L]
+        V = vc[b * mb:(b + 1) * mb].double().permute(1, 0, 2, 3).reshape(Hkv, mb * BS, D)[:, :L]
+        ref = _sdpa_unpaged(q[b].double(), K, V).numpy()
+        np.testing.assert_allclose(got[b], ref, rtol=0, atol=1e-12)
+
+
+def test_units_subset_matches_full():
+    q, kc, vc, tables, lens = _random_case(5)
+    full = oracle.paged_decode(q, kc, vc, tables, lens)
+    units = [(2, 3), (0, 1), (1, 0)]
+    sub = oracle.paged_decode(q, kc, vc, tables, lens, units=units)
+    for i, (b, h) in enumerate(units):
+        assert np.array_equal(sub[i], full[b, h])
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_permutation_invariance_is_exact():
+    q, kc, vc, tables, lens = _random_case(7, lens=(5, 16, 17))
+    base = oracle.paged_decode(q, kc, vc, tables, lens)
+    NB = kc.shape[0]
+    perm = np.random.default_rng(99).permutation(NB)
+    kc2 = torch.empty_like(kc)
+    vc2 = torch.empty_like(vc)
+    kc2[torch.from_numpy(perm)] = kc
+    vc2[torch.from_numpy(perm)] = vc
+    t2 = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    moved = oracle.paged_decode(q, kc2, vc2, t2, lens)
+    assert np.array_equal(base, moved)
+
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    q, kc, vc, tables, lens = _random_case(8, Hq=8, Hkv=2)
+    gqa = oracle.paged_decode(q, kc, vc, tables, lens)
+    mha = oracle.paged_decode(q, kc.repeat_interleave(4, dim=1), vc.repeat_interleave(4, dim=1),
+                              tables, lens)
+    assert np.array_equal(gqa, mha)
+
+
+def test_length_one_returns_v0_exactly():
+    q, kc, vc, tables, lens = _random_case(9, lens=(1, 1, 1))
+    got = oracle.paged_decode(q, kc, vc, tables, lens)
+    vd = oracle.bf16_to_f64(vc)
+    G = q.shape[1] // kc.shape[1]
+    for b in range(3):
+        for h in range(q.shape[1]):
+            assert np.array_equal(got[b, h], vd[tables[b, 0], h // G, 0])
+
+
+def test_weights_sum_to_one():
+    q, kc, vc, tables, lens = _random_case(10, lens=(3, 40, 77), BS=8)
+    ones = torch.ones_like(vc)
+    got = oracle.paged_decode(q * 4, kc, ones, tables, lens)
+    np.testing.assert_allclose(got, 1.0, rtol=0, atol=1e-12)
+
+
+def test_equal_keys_give_mean_of_v():
+    q, kc, vc, tables, lens = _random_case(11, lens=(6, 21, 2))
+    kc_const = torch.zeros_like(kc) + kc[0, 0, 0]
+    got = oracle.paged_decode(q, kc_const, vc, tables, lens)
+    vd = oracle.bf16_to_f64(vc)
+    G = q.shape[1] // kc.shape[1]
+    for b in range(3):
+        for h in range(q.shape[1]):
+            V = oracle.gather_contiguous(vd, tables[b], int(lens[b]), h // G)
+            np.testing.assert_allclose(got[b, h], V.mean(axis=0), rtol=0, atol=1e-12)
+
+
+def test_dominant_score_selects_its_value_row():
+    B, Hq, Hkv, D, BS = 1, 1, 1, 8, 4
+    L = 10
+    tables = np.array([[2, 0, 1]], dtype=np.int32)
+    kc = torch.zeros((3, Hkv, BS, D), dtype=torch.bfloat16)
+    vc = _bf16((3, Hkv, BS, D), 31)
+    q = torch.zeros((B, Hq, D), dtype=torch.bfloat16)
+    q[0, 0, 0] = 64.0
+    t_star = 6  # logical token 6 -> table[1] = block 0, offset 2
+    kc[0, 0, 2, 0] = 64.0  # score = 64*64/sqrt(8) ~ 1448 above every other
+    got = oracle.paged_decode(q, kc, vc, tables, np.array([L], dtype=np.int32))
+    want = oracle.bf16_to_f64(vc)[0, 0, 2]
+    assert t_star // BS == 1
+    np.testing.assert_allclose(got[0, 0], want, rtol=0, atol=1e-300)
+
+
+def test_padding_slots_never_read():
+    q, kc, vc, tables, lens = _random_case(12, lens=(3, 6, 11), BS=4)
+    base = oracle.paged_decode(q, kc, vc, tables, lens)
+    kc2, vc2 = kc.clone(), vc.clone()
+    for b in range(3):
+        L = int(lens[b])
+        last = tables[b, (L - 1) // 4]
+        kc2[last, :, L % 4 or 4:] = float("nan")
+        vc2[last, :, L % 4 or 4:] = float("nan")
+    # unused blocks too
+    used = set(tables[tables >= 0].tolist())
+    for blk in range(kc.shape[0]):
+        if blk not in used:
+            kc2[blk] = float("nan")
+            vc2[blk] = float("nan")
+    got = oracle.paged_decode(q, kc2, vc2, tables, lens)
+    assert np.isfinite(got).all()
+    assert np.array_equal(base, got)
+
+
+@pytest.mark.parametrize("P", [4, 8, 12, 16, 64])
+def test_split_merge_identity(P):
+    q, kc, vc, tables, lens = _random_case(13, lens=(1, 16, 33), BS=4)
+    full = oracle.paged_decode(q, kc, vc, tables, lens)
+    qd, kd, vd = (oracle.bf16_to_f64(x) for x in (q, kc, vc))
+    G = qd.shape[1] // kd.shape[1]
+    for b in range(3):
+        for h in range(qd.shape[1]):
+            K = oracle.gather_contiguous(kd, tables[b], int(lens[b]), h // G)
+            V = oracle.gather_contiguous(vd, tables[b], int(lens[b]), h // G)
+            parts = oracle.partition_decode(qd[b, h], K, V, 1 / math.sqrt(qd.shape[2]), P)
+            assert len(parts) == -(-int(lens[b]) // P)
+            np.testing.assert_allclose(oracle.merge_partitions(parts), full[b, h], rtol=0, atol=1e-12)
+
+
+def test_scale_argument_is_used():
+    q, kc, vc, tables, lens = _random_case(14)
+    a = oracle.paged_decode(q, kc, vc, tables, lens)
+    b = oracle.paged_decode(q, kc, vc, tables, lens, scale=1.0 / math.sqrt(q.shape[2]))
+    c = oracle.paged_decode(q, kc, vc, tables, lens, scale=1.0)
+    assert np.array_equal(a, b)
+    assert not np.allclose(a[1:], c[1:])
+
+
+def test_bad_table_entry_is_an_error():
+    q, kc, vc, tables, lens = _random_case(15)
+    bad = tables.copy()
+    bad[2, 0] = kc.shape[0]  # out of range
+    with pytest.raises(ValueError):
+        oracle.paged_decode(q, kc, vc, bad, lens)
+
+
+# ---------------------------------------------------------------- mutation checks
+
+def _twin_mutant(kind):
+    """A copy of the numpy twin with one plausible mistake planted in it."""
+    def run(q, k_cache, v_cache, block_tables, context_lens):
+        qd, kd, vd = (oracle.bf16_to_f64(x) for x in (q, k_cache, v_cache))
+        B, Hq, D = qd.shape
+        Hkv, BS = kd.shape[1], kd.shape[2]
+        G = Hq // Hkv
+        scale = 1.0 if kind == "no_scale" else 1 / math.sqrt(D)
+        out = np.empty((B, Hq, D))
+        for b in range(B):
+            L = int(context_lens[b]) - (1 if kind == "mask_off_by_one" and context_lens[b] > 1 else 0)
+            for h in range(Hq):
+                g = h % Hkv if kind == "gqa_modulo" else h // G
+                t = np.arange(L)
+                off = (t + 1) % BS if kind == "offset" else t % BS
+                blk = block_tables[b][t // BS]
+                K, V = kd[blk, g, off], vd[blk, g, off]
+                s = K @ qd[b, h] * scale
+                w = np.exp(s - s.max())
+                out[b, h] = (w / w.sum()) @ V
+        return out
+    return run
+
+
+@pytest.mark.parametrize("kind", ["no_scale", "gqa_modulo", "offset", "mask_off_by_one"])
+def test_pins_reject_planted_mistakes(kind):
+    """Each planted mistake must be caught by a library or brute-force pin."""
+    q, kc, vc, tables, lens = _random_case(16, Hq=4, Hkv=2, lens=(5, 9, 13))
+    mutant = _twin_mutant(kind)(q, kc, vc, tables, lens)
+    ok = oracle.paged_decode(q, kc, vc, tables, lens)
+    # the brute-force pin distinguishes the mutant from the definition
+    assert np.abs(mutant - ok).max() > 1e-3
+
+
+# ---------------------------------------------------------------- cache writes
+
+def test_reshape_and_cache_matches_indexing_definition():
+    NB, Hkv, BS, D, T = 6, 2, 4, 8, 5
+    kc = _bf16((NB, Hkv, BS, D), 41)
+    vc = _bf16((NB, Hkv, BS, D), 42)
+    kn = _bf16((T, Hkv, D), 43)
+    vn = _bf16((T, Hkv, D), 44)
+    slots = np.array([5, -1, 0, 23, 14], dtype=np.int64)
+    k2, v2 = oracle.reshape_and_cache(kn, vn, kc, vc, slots)
+    ke = oracle.bf16_bits(kc).copy()
+    ve = oracle.bf16_bits(vc).copy()
+    for t, s in enumerate(slots):
+        if s >= 0:
+            ke[s // BS, :, s % BS, :] = oracle.bf16_bits(kn)[t]
+            ve[s // BS, :, s % BS, :] = oracle.bf16_bits(vn)[t]
+    assert np.array_equal(k2, ke) and np.array_equal(v2, ve)
+    # untouched slots keep their bits
+    touched = {(s // BS, s % BS) for s in slots if s >= 0}
+    kb = oracle.bf16_bits(kc)
+    for blk in range(NB):
+        for off in range(BS):
+            if (blk, off) not in touched:
+                assert np.array_equal(k2[blk, :, off], kb[blk, :, off])
+
+
+def test_reshape_and_cache_then_decode_reads_the_new_token(golden_dir):
+    gold = json.load(open(os.path.join(golden_dir, "worked_block_table.json")))
+    BS = gold["block_size"]
+    NB, Hkv, D = 12, 1, 4
+    kc = torch.full((NB, Hkv, BS, D), float("nan"), dtype=torch.bfloat16)
+    vc = kc.clone()
+    kn = _bf16((5, Hkv, D), 51)
+    vn = _bf16((5, Hkv, D), 52)
+    k2, v2 = oracle.reshape_and_cache(kn, vn, kc, vc, np.array(gold["slots"], dtype=np.int64))
+    q = _bf16((1, 1, D), 53)
+    got = oracle.paged_decode(q, k2, v2, np.array([gold["block_table"]], np.int32),
+                              np.array([5], np.int32))
+    ref = _sdpa_unpaged(q[0].double(), kn.double().permute(1, 0, 2), vn.double().permute(1, 0, 2))
+    np.testing.assert_allclose(got[0], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_reshape_and_cache_rejects_out_of_range_slot():
+    kc = _bf16((2, 1, 4, 8), 61)
+    with pytest.raises(ValueError):
+        oracle.reshape_and_cache(_bf16((1, 1, 8), 62), _bf16((1, 1, 8), 63), kc, kc,
+                                 np.array([8], dtype=np.int64))
+
+
+def test_copy_blocks_matches_definition():
+    NB, Hkv, BS, D = 8, 2, 4, 8
+    kc = _bf16((NB, Hkv, BS, D), 71)
+    vc = _bf16((NB, Hkv, BS, D), 72)
+    pairs = np.array([[1, 5], [3, 6], [0, 7]], dtype=np.int32)
+    k2, v2 = oracle.copy_blocks(kc, vc, pairs)
+    kb, vb = oracle.bf16_bits(kc), oracle.bf16_bits(vc)
+    for blk in range(NB):
+        src = {5: 1, 6: 3, 7: 0}.get(blk, blk)
+        assert np.array_equal(k2[blk], kb[src]) and np.array_equal(v2[blk], vb[src])
+
+
+# ---------------------------------------------------------------- block manager model
+
+def test_allocator_arithmetic(golden_dir):
+    gold = json.load(open(os.path.join(golden_dir, "allocator_arithmetic.json")))
+    BS = gold["block_size"]
+    for case in gold["cases"]:
+        n = case["tokens"]
+        pool = PoolModel(400, BS)
+        s = pool.seq_create()
+        pool.append_tokens(s, n)
+        assert len(pool.table(s)) == case["blocks"] == oracle.blocks_needed(n, BS)
+        wasted = case["blocks"] * BS - n
+        assert wasted <= gold["max_waste_slots"]["value"]
+        if "wasted_slots" in case:
+            assert wasted == case["wasted_slots"]
+            assert abs(wasted / n - case["fragmentation_vs_length"]) < 1e-12
+        if "utilisation_pct_rounded" in case:
+            assert round(100 * n / (case["blocks"] * BS)) == case["utilisation_pct_rounded"]
+    for n in range(1, 400):
+        assert 0 <= oracle.blocks_needed(n, BS) * BS - n <= gold["max_waste_slots"]["value"]
+
+
+def test_prefix_share_counts(golden_dir):
+    gold = json.load(open(os.path.join(golden_dir, "allocator_arithmetic.json")))["prefix_share"]
+    pool = PoolModel(200, 16)
+    pre = pool.seq_create()
+    pool.append_tokens(pre, gold["shared_blocks"] * 16)  # the resident preamble blocks
+    used_before = pool.stats()["used"]
+    req = pool.seq_fork(pre, gold["shared_blocks"] * 16)
+    pool.append_tokens(req, gold["prompt_tokens"] - gold["shared_blocks"] * 16)
+    assert len(pool.table(req)) == 75
+    assert pool.stats()["used"] - used_before == gold["new_blocks"]
+    assert pool.table(req)[:56] == pool.table(pre)
+    assert all(pool.ref[b] == 2 for b in pool.table(pre))
+
+
+def test_new_block_exactly_when_crossing_a_boundary():
+    pool = PoolModel(100, 16)
+    s = pool.seq_create()
+    pool.append_tokens(s, 1200)
+    assert len(pool.table(s)) == 75
+    pool.append_slot(s)  # token index 1200, the 1,201st token
+    assert len(pool.table(s)) == 76
+    pool.append_tokens(s, 15)
+    assert len(pool.table(s)) == 76
+    pool.append_slot(s)
+    assert len(pool.table(s)) == 77
+
+
+def test_copy_on_write_state_machine():
+    pool = PoolModel(10, 4, free_order=list(range(10)))
+    a = pool.seq_create()
+    pool.append_tokens(a, 6)  # blocks 0, 1 (block 1 partial: 2 of 4)
+    b = pool.seq_fork(a, 6)
+    assert pool.ref[0] == 2 and pool.ref[1] == 2
+    slot, cow = pool.append_slot(b)  # writes into shared partial block 1 -> CoW
+    assert cow == (1, 2)
+    assert pool.table(b) == [0, 2] and pool.table(a) == [0, 1]
+    assert pool.ref[1] == 1 and pool.ref[2] == 1 and pool.ref[0] == 2
+    assert slot == 2 * 4 + 2
+    slot_a, cow_a = pool.append_slot(a)  # a's block 1 is now private: no CoW
+    assert cow_a is None and slot_a == 1 * 4 + 2
+    pool.seq_free(b)
+    assert pool.ref[0] == 1 and pool.ref[2] == 0
+    assert pool.alloc() == 2  # freed block handed out next (LIFO free list)
+
+
+def test_oom_leaves_state_unchanged():
+    pool = PoolModel(2, 4)
+    s = pool.seq_create()
+    pool.append_tokens(s, 8)
+    snap = (list(pool.free), list(pool.ref), pool.table(s), pool.length(s))
+    with pytest.raises(oracle.PoolOOM):
+        pool.append_slot(s)
+    assert snap == (list(pool.free), list(pool.ref), pool.table(s), pool.length(s))
+    t = pool.seq_fork(s, 7)
+    snap = (list(pool.free), list(pool.ref), pool.table(t), pool.length(t))
+    with pytest.raises(oracle.PoolOOM):
+        pool.append_slot(t)  # CoW needs a block; none left
+    assert snap == (list(pool.free), list(pool.ref), pool.table(t), pool.length(t))
+
+
+def test_double_free_and_bad_ids():
+    pool = PoolModel(4, 4)
+    blk = pool.alloc()
+    pool.decref(blk)
+    with pytest.raises(oracle.PoolError):
+        pool.decref(blk)
+    with pytest.raises(oracle.PoolError):
+        pool.incref(7)
