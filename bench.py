@@ -1,0 +1,480 @@
+"""Benchmark: one paged decode step of a Llama-3.1-8B-class layer on GB300.
+
+A step is one pass of the whole hot path over one batch: the copy-on-write
+block copies the pool asked for (none in this workload), the KV write of one
+new token per sequence through the slot mapping, and paged decode attention
+over the updated cache (split-K partitions + merge where a sequence spans
+more than one partition).
+
+Workload (default): 64 sequences, 32 query / 8 KV heads, head dim 128, bf16,
+block size 16, context lengths uniform in [128, 2048] (+1 appended token),
+physical blocks shuffled across a pool 1.25x the need. Synthetic seeded data,
+q/K/V ~ N(0, 1). The KV pool is replicated 3 times (each copy larger than
+the 129 MB L2) and consecutive steps rotate through the copies, so every
+step streams its K/V from HBM.
+
+Metric: algorithmic bytes per step / step time (GB/s), with the fraction of
+the measured HBM peak and steps/s alongside. Algorithmic bytes: every cached
+K/V byte of every sequence once (GQA packing), q in and out, block-table
+entries and lengths, plus the KV write's bytes.
+
+``--impl reference`` times the float64 CPU oracle (the reference arm) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attention KV HBM GB/s (% of GB300 peak) and decode steps/s"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- bytes
+
+def decode_bytes(lens, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int = 16) -> int:
+    """Algorithmic bytes of one decode: K+V of every cached token once per KV head,
+    q in and out, table entries, lengths."""
+    lens = np.asarray(lens, dtype=np.int64)
+    B = len(lens)
+    kv = int(lens.sum()) * num_kv_heads * head_dim * 2 * 2
+    qo = B * num_q_heads * head_dim * 2 * 2
+    tables = int(((lens + block_size - 1) // block_size).sum()) * 4 + 4 * B
+    return kv + qo + tables
+
+
+def append_bytes(num_tokens: int, num_kv_heads: int, head_dim: int) -> int:
+    """KV write: read the new K/V rows, write them into the cache, read the slots."""
+    return num_tokens * num_kv_heads * head_dim * 2 * 2 * 2 + 8 * num_tokens
+
+
+def cow_bytes(num_pairs: int, num_kv_heads: int, head_dim: int, block_size: int = 16) -> int:
+    """Block copy: read and write a whole block of K and of V per pair."""
+    return num_pairs * 2 * num_kv_heads * block_size * head_dim * 2 * 2
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the GPU is loaded."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.proc = None
+        self.path = None
+        try:
+            import tempfile
+
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class StepPlan:
+    """Pre-marshalled C-ABI calls for one step on one KV-pool copy."""
+
+    def __init__(self, pk, lib, dec_params, ws_ptr, ws_bytes, rc_args, cow_args, stream):
+        self.pk, self.lib = pk, lib
+        self.dec = dec_params
+        self.ws_ptr, self.ws_bytes = ws_ptr, ws_bytes
+        self.rc_args = rc_args
+        self.cow_args = cow_args
+        self.stream = stream
+
+    def run(self, ev_dec=None):
+        lib = self.lib
+        if self.cow_args is not None:
+            st = lib.pa_copy_blocks(*self.cow_args, self.stream)
+            if st:
+                raise RuntimeError(f"pa_copy_blocks failed: {st}")
+        st = lib.pa_reshape_and_cache(*self.rc_args, self.stream)
+        if st:
+            raise RuntimeError(f"pa_reshape_and_cache failed: {st}")
+        if ev_dec is not None:
+            ev_dec[0].record()
+        st = lib.pa_decode(ctypes.byref(self.dec), self.ws_ptr, self.ws_bytes, self.stream)
+        if st:
+            raise RuntimeError(f"pa_decode failed: {st}")
+        if ev_dec is not None:
+            ev_dec[1].record()
+
+
+def setup_workload(r: workloads.Recipe, device, n_copies: int):
+    import torch
+
+    import paged_kv_cache_92_gb300 as pk
+
+    pool = pk.Pool(r.num_blocks, r.block_size, free_order=r.free_order)
+    seqs = workloads.drive_prefill(pool, r)
+    slots, cows = workloads.drive_step_append(pool, seqs, r)
+    tables = workloads.tables_of(pool, seqs)
+    lens = (r.lens0 + r.append).astype(np.int32)
+    pool.close()
+    q, kn, vn, kc, vc = workloads.step_tensors(r, str(device))
+    copies = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(n_copies - 1)]
+    return dict(tables=tables, lens=lens, slots=slots, cows=cows, q=q, kn=kn, vn=vn,
+                copies=copies)
+
+
+def make_plans(pk, W, device, partition_tokens=0):
+    import torch
+
+    lib = pk.load()
+    stream = torch.cuda.current_stream().cuda_stream or None
+    tables_d = torch.from_numpy(W["tables"]).to(device)
+    lens_d = torch.from_numpy(W["lens"]).to(device)
+    slots_d = torch.from_numpy(W["slots"]).to(device)
+    cows_d = torch.from_numpy(W["cows"]).to(device) if len(W["cows"]) else None
+    out = torch.empty_like(W["q"])
+    keep = [tables_d, lens_d, slots_d, cows_d, out]
+    plans = []
+    ws = None
+    for kc, vc in W["copies"]:
+        p = pk.make_decode_params(W["q"], out, kc, vc, tables_d, lens_d,
+                                  max_context_len=int(W["lens"].max()),
+                                  partition_tokens=partition_tokens)
+        need = pk.pa_decode_workspace_size(p)
+        if ws is None and need:
+            ws = torch.empty(need, dtype=torch.uint8, device=device)
+            keep.append(ws)
+        NB, Hkv, BS, D = kc.shape
+        rc_args = (W["kn"].data_ptr(), W["vn"].data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                   slots_d.data_ptr(), W["kn"].shape[0], Hkv, D, BS, NB)
+        cow_args = None
+        if cows_d is not None:
+            cow_args = (kc.data_ptr(), vc.data_ptr(), cows_d.data_ptr(), cows_d.shape[0], Hkv, D,
+                        BS, NB)
+        plans.append(StepPlan(pk, lib, p, ws.data_ptr() if ws is not None else None,
+                              ws.numel() if ws is not None else 0, rc_args, cow_args, stream))
+    return plans, out, keep
+
+
+def run_ours(args, rank: int, world: int) -> dict:
+    import torch
+
+    import paged_kv_cache_92_gb300 as pk
+
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    pk.load()
+    r = workloads.llama8b_layer()
+    W = setup_workload(r, device, n_copies=3)
+    plans, out, keep = make_plans(pk, W, device)
+    lens = W["lens"]
+    dec_b = decode_bytes(lens, r.num_q_heads, r.num_kv_heads, r.head_dim)
+    step_b = dec_b + append_bytes(len(W["slots"]), r.num_kv_heads, r.head_dim) + \
+        cow_bytes(len(W["cows"]), r.num_kv_heads, r.head_dim)
+    pool_copy_bytes = 2 * W["copies"][0][0].numel() * 2
+    n_split = int((lens > 512).sum())
+    launches_per_step = 1 + 1 + (1 if int(lens.max()) > 512 else 0) + (1 if len(W["cows"]) else 0)
+
+    stream = torch.cuda.current_stream()
+    # warm-up (untimed), then a sustained untimed loop under the clock sampler
+    for i in range(args.warmup):
+        plans[i % len(plans)].run()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    t_sustain = time.time()
+    i = 0
+    while time.time() - t_sustain < args.sustain_s:
+        for _ in range(64):
+            plans[i % len(plans)].run()
+            i += 1
+        torch.cuda.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        plans[k % len(plans)].run(evs[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_b * args.steps / (elapsed_ms * 1e-3) / 1e9
+
+    peaks = measured_peaks()
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    achieved = dec_b / (dec_avg_ms * 1e-3) / 1e9
+
+    # end to end through the public Python API: pinned host inputs -> device,
+    # step, result -> pinned host, every step
+    e2e = run_e2e(pk, W, r, device, args.steps, args.warmup, step_b)
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/K/V, uniform context lengths; no weights needed)",
+        "pct_of_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "steps_per_s": round(1000.0 / ms_per_step, 1),
+        "config": {
+            "workload": "llama8b_layer_decode_b64: 64 seqs, 32 q / 8 KV heads, head_dim 128, "
+                        "bf16, block 16, L~U[128,2048]+1 appended token, shuffled 1.25x pool",
+            "num_seqs": r.num_seqs, "num_q_heads": r.num_q_heads, "num_kv_heads": r.num_kv_heads,
+            "head_dim": r.head_dim, "block_size": r.block_size,
+            "total_context_tokens": int(lens.sum()), "seqs_split_k": n_split,
+            "algorithmic_bytes_per_step": step_b, "decode_bytes_per_step": dec_b,
+            "l2": f"inputs larger than L2: {len(W['copies'])} rotating KV pool copies of "
+                  f"{pool_copy_bytes / 1e6:.0f} MB each (L2 129 MB)",
+            "parallelism": "replicas only" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "pa_decode (decode kernel + split-K merge)",
+            "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "peak_source": f"{peaks['source']} hbm_gbs", "avg_launch_ms": round(dec_avg_ms, 5),
+        },
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(r, W, budget_s=args.cpu_baseline_s)
+    return res
+
+
+def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int) -> dict:
+    import torch
+
+    host = {k: W[k] for k in ("tables", "lens", "slots")}
+    pin = {
+        "q": W["q"].cpu().pin_memory(), "kn": W["kn"].cpu().pin_memory(),
+        "vn": W["vn"].cpu().pin_memory(),
+        "tables": torch.from_numpy(host["tables"]).pin_memory(),
+        "lens": torch.from_numpy(host["lens"]).pin_memory(),
+        "slots": torch.from_numpy(host["slots"]).pin_memory(),
+    }
+    if len(W["cows"]):
+        pin["cows"] = torch.from_numpy(W["cows"]).pin_memory()
+    dev = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
+    out_d = torch.empty_like(W["q"])
+    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = out_h.numel() * out_h.element_size()
+    ws = {}
+    max_ctx = int(host["lens"].max())
+
+    def step(i):
+        kc, vc = W["copies"][i % len(W["copies"])]
+        for k in pin:
+            dev[k].copy_(pin[k], non_blocking=True)
+        if "cows" in dev:
+            pk.pa_copy_blocks(kc, vc, dev["cows"])
+        pk.pa_reshape_and_cache(dev["kn"], dev["vn"], kc, vc, dev["slots"])
+        if "ws" not in ws:
+            p = pk.make_decode_params(dev["q"], out_d, kc, vc, dev["tables"], dev["lens"], max_ctx)
+            n = pk.pa_decode_workspace_size(p)
+            ws["ws"] = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None
+        pk.pa_decode(dev["q"], kc, vc, dev["tables"], dev["lens"], max_ctx, out=out_d,
+                     workspace=ws["ws"])
+        out_h.copy_(out_d, non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(i)
+        torch.cuda.current_stream().synchronize()  # the host reads the result every step
+    dt = time.perf_counter() - t0
+    return {"value": round(step_b * steps / dt / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(dt * 1e3 / steps, 4)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def _oracle_sample_inputs(r: workloads.Recipe):
+    """Host layout and contents for the oracle (its own pool model)."""
+    import oracle
+
+    model = oracle.PoolModel(r.num_blocks, r.block_size, free_order=r.free_order)
+    seqs = workloads.drive_prefill(model, r)
+    slots, cows = workloads.drive_step_append(model, seqs, r)
+    tables = workloads.tables_of(model, seqs)
+    lens = (r.lens0 + r.append).astype(np.int32)
+    q, kn, vn, kc, vc = workloads.step_tensors(r, "cpu")
+    return tables, lens, q, kc, vc
+
+
+def cpu_baseline(r: workloads.Recipe, W=None, budget_s: float = 10.0) -> dict:
+    """The float64 oracle on this host's cores over a bounded sample of the
+    workload: whole sequences (all query heads), one after another, until the
+    time budget is spent. Value in GB/s of algorithmic decode bytes."""
+    import oracle
+
+    tables, lens, q, kc, vc = _oracle_sample_inputs(r)
+    qb, kb, vb = oracle.bf16_bits(q), oracle.bf16_bits(kc), oracle.bf16_bits(vc)
+    done_bytes, n_seqs = 0, 0
+    t0 = time.perf_counter()
+    b = 0
+    while time.perf_counter() - t0 < budget_s and n_seqs < 4 * r.num_seqs:
+        units = [(b, h) for h in range(r.num_q_heads)]
+        oracle.paged_decode(qb, kb, vb, tables, lens, units=units)
+        done_bytes += decode_bytes(lens[b:b + 1], r.num_q_heads, r.num_kv_heads, r.head_dim)
+        n_seqs += 1
+        b = (b + 1) % r.num_seqs
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"float64 C oracle decode of {n_seqs} whole sequences (all {r.num_q_heads} "
+                      f"query heads) of the same workload, {dt:.1f} s"}
+
+
+def run_reference(args) -> dict:
+    import oracle
+
+    r = workloads.llama8b_layer()
+    tables, lens, q, kc, vc = _oracle_sample_inputs(r)
+    qb, kb, vb = oracle.bf16_bits(q), oracle.bf16_bits(kc), oracle.bf16_bits(vc)
+    per_step = 2  # sequences per step (all heads): keeps a step well under a second
+
+    def step(i):
+        seqs = [(i * per_step + j) % r.num_seqs for j in range(per_step)]
+        units = [(b, h) for b in seqs for h in range(r.num_q_heads)]
+        oracle.paged_decode(qb, kb, vb, tables, lens, units=units)
+        return decode_bytes(lens[seqs], r.num_q_heads, r.num_kv_heads, r.head_dim)
+
+    for i in range(args.warmup):
+        step(i)
+    total = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        total += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    sample = (f"each step: float64 C oracle decode of {per_step} whole sequences (all "
+              f"{r.num_q_heads} query heads) of the llama8b_layer_decode_b64 workload")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/K/V)",
+        "config": {"workload": "llama8b_layer_decode_b64 (sampled)", "num_seqs": r.num_seqs,
+                   "num_q_heads": r.num_q_heads, "num_kv_heads": r.num_kv_heads,
+                   "head_dim": r.head_dim, "block_size": r.block_size},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sustain-s", type=float, default=1.0,
+                    help="untimed loaded seconds before the timed region (clock sampling)")
+    ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,241 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: paged KV-cache decode attention for
+ * GB300 (sm_103a), its companion cache kernels, and a host-side block pool.
+ *
+ * Sources for what each call computes:
+ *  [P1] "How Paged Attention and Continuous Batching Actually Work"
+ *       (netraruntime.com): §Paged attention: virtual memory for the KV cache
+ *       (16-token blocks, free list, block table, the indexing rule: divide
+ *       for the logical block, look up the physical block, multiply out, add
+ *       the offset); §One step, end to end (write KV through the slot
+ *       mapping, allocate_slots).
+ *  [P2] "Paged Attention as a Memory Manager" (praveentn.live): §How the
+ *       Kernel Executes Paged Attention (score_i = q.k_i / sqrt(d_k), the
+ *       per-block loop: read the table entry, load the block, dot products,
+ *       mask padding, running max and sum, weighted sum of V); §Prefix
+ *       Caching and Copy-on-Write (refcounts; allocate, copy, decrement,
+ *       update the table).
+ *  [P3] PagedAttention architecture walk-through (aicassindra.com):
+ *       §The architecture: every piece explained (entry i of the block table
+ *       backs tokens [16i, 16i+15]; every 16th token takes a fresh block;
+ *       a write to a shared block triggers copy-on-write).
+ *  [P4] "PagedAttention and continuous batching" (ai-knowledge-tree):
+ *       §Block table example; §Attention kernel modification (K/V loaded
+ *       block by block through the table, running softmax across blocks).
+ *
+ * Data layout (the pages fix none; this library's choice):
+ *   k_cache, v_cache  bf16 [num_blocks][num_kv_heads][block_size][head_dim]
+ *                     (one (block, KV head) tile is block_size*head_dim*2
+ *                     contiguous bytes: 4 KiB at block 16, head dim 128)
+ *   q, out            bf16 [num_seqs][num_q_heads][head_dim]
+ *   block_tables      int32 [num_seqs][max_blocks_per_seq]; entry j of row b
+ *                     is the physical block of logical tokens
+ *                     [j*block_size, (j+1)*block_size); entries past
+ *                     ceil(len/block_size) are never read
+ *   context_lens      int32 [num_seqs], the number of cached tokens of each
+ *                     sequence including the one written this step
+ *   slot_mapping      int64 [num_tokens]; slot = block*block_size + offset
+ *   GQA               query head h reads KV head h / (num_q_heads/num_kv_heads)
+ *
+ * Conventions for every device call:
+ *  - All array pointers are caller-owned DEVICE memory, 16-byte aligned,
+ *    dense (no strides). The library never allocates device memory and never
+ *    synchronises the stream (except pa_device_errors).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    failing check returns PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED and
+ *    launches nothing. A launch failure returns PA_ERR_CUDA.
+ *  - Values that live only on the device (table entries, lengths, slots) are
+ *    checked inside the kernels: an out-of-range value is never dereferenced
+ *    (the access is clamped or skipped), a sticky device error bit is set,
+ *    and the affected output is unspecified. pa_device_errors() reads the
+ *    bits. No kernel faults or hangs on bad device-side values.
+ *  - pa_last_error() returns a thread-local message for the last failing
+ *    call on that thread.
+ *
+ * Supported shapes: block_size 16; head_dim 64 or 128; num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8}. Anything else returns PA_ERR_UNSUPPORTED.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* a host-checkable argument is wrong */
+  PA_ERR_UNSUPPORTED = 2,  /* valid, but a shape this build does not implement */
+  PA_ERR_OOM = 3,          /* block pool exhausted; pool state unchanged */
+  PA_ERR_REFCOUNT = 4,     /* refcount underflow / block not allocated */
+  PA_ERR_BOUNDS = 5,       /* an id or index out of range */
+  PA_ERR_CUDA = 6          /* a CUDA runtime call or launch failed */
+} pa_status;
+
+/* Device error bits reported by pa_device_errors(). */
+#define PA_DEVERR_TABLE_ENTRY 0x1u   /* block table entry outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT_LEN 0x2u   /* context_len > max_context_len or > table capacity */
+#define PA_DEVERR_SLOT 0x4u          /* slot_mapping entry >= num_blocks*block_size */
+#define PA_DEVERR_COPY_PAIR 0x8u     /* copy_blocks pair outside [0, num_blocks) */
+#define PA_DEVERR_TIMEOUT 0x10u      /* an mbarrier wait hit its iteration limit */
+
+const char* pa_status_string(pa_status s);
+const char* pa_last_error(void);
+int32_t pa_version(void);
+
+/* Sticky device error bits accumulated by every kernel of this library on the
+ * current device since the last call. Synchronises `stream`, returns the bits
+ * in *flags and clears them. */
+pa_status pa_device_errors(pa_stream_t stream, uint32_t* flags);
+
+/* ------------------------------------------------------------------------
+ * pa_decode -- paged decode attention [P2 §How the Kernel Executes Paged
+ * Attention; P4 §Attention kernel modification].
+ *
+ * For every sequence b and query head h (KV head g = h / G):
+ *   K_b, V_b = rows t = 0..L_b-1 of the cache, row t read from physical block
+ *              block_tables[b][t / block_size] at offset t % block_size [P1]
+ *   s_t      = scale * (q[b][h] . K_b[t])
+ *   out[b][h]= sum_t softmax(s)_t * V_b[t]                (bf16, round to nearest even)
+ * computed with fp32 accumulation and a running (online) softmax. Sequences
+ * longer than `partition_tokens` are split into partitions of that many
+ * tokens; each partition yields (max, sum, weighted sum) and a second kernel
+ * merges them by log-sum-exp (flash-decoding split; not on the pages).
+ * Rows with L_b <= 0 are written as zeros.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void* q;               /* bf16 [num_seqs][num_q_heads][head_dim] */
+  void* out;                   /* bf16 [num_seqs][num_q_heads][head_dim] */
+  const void* k_cache;         /* bf16 [num_blocks][num_kv_heads][block_size][head_dim] */
+  const void* v_cache;         /* same layout as k_cache */
+  const int32_t* block_tables; /* int32 [num_seqs][max_blocks_per_seq] */
+  const int32_t* context_lens; /* int32 [num_seqs] */
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_context_len;     /* host-known upper bound of every context_lens[b] (>= 1) */
+  float scale;                 /* softmax scale, normally 1/sqrt(head_dim) */
+  int32_t partition_tokens;    /* split-K partition length; 0 = 512; else a multiple of
+                                  block_size in [block_size, 4096] */
+} pa_decode_params;
+
+/* Bytes of device workspace pa_decode needs for these parameters (0 when no
+ * sequence can span more than one partition). Returns 0 for invalid params. */
+size_t pa_decode_workspace_size(const pa_decode_params* p);
+
+/* Enqueue the decode. `workspace` is caller-owned device memory of at least
+ * pa_decode_workspace_size(p) bytes (may be NULL when that size is 0); it
+ * holds split-K partials and is fully rewritten by every call, so two calls
+ * in flight at once must not share it. */
+pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace_bytes,
+                    pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_reshape_and_cache -- write each new token's K/V row into its slot
+ * [P1 §One step, end to end: "gather and write KV through the slot-mapping
+ * formula"; P3 §The architecture: the forward pass appends the new token's
+ * K/V into the right physical block].
+ *   for t in [0, num_tokens): slot = slot_mapping[t]; if slot < 0: skip
+ *     k_cache[slot / block_size][h][slot % block_size][:] = k_new[t][h][:]  (every KV head h)
+ *     v_cache[...]                                         = v_new[t][h][:]
+ * Bit-exact copies. k_new/v_new: bf16 [num_tokens][num_kv_heads][head_dim].
+ * Two tokens with the same slot race (unspecified which one lands).
+ * ---------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,
+                               void* v_cache, const int64_t* slot_mapping, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_copy_blocks -- the data half of copy-on-write [P2 §Prefix Caching and
+ * Copy-on-Write: "allocates a fresh physical block, copies the existing
+ * content"]. For each pair i: block pairs[i][1] of both caches becomes a
+ * bit-exact copy of block pairs[i][0] (all KV heads, all slots).
+ * pairs: int32 [num_pairs][2] (src, dst), device memory. Destinations must
+ * be pairwise distinct and disjoint from the sources (what the pool's
+ * copy-on-write produces); overlapping pairs give unspecified contents.
+ * ---------------------------------------------------------------------- */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_blocks, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Host block pool [P1 §Paged attention; P2 §Prefix Caching and Copy-on-Write;
+ * P3 §The architecture]. All memory here is host memory owned by the pool.
+ * Not thread-safe: one pool per thread, or external locking.
+ *
+ * Free list: a stack. free_order[0] (or block 0 when free_order is NULL) is
+ * handed out first; a block whose refcount drops to zero is pushed on top
+ * and handed out next. Every failing call leaves the pool unchanged.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_pool pa_pool;
+
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t free_blocks;
+  int32_t used_blocks;   /* refcount >= 1 */
+  int32_t shared_blocks; /* refcount >= 2 */
+  int32_t max_refcount;
+  int32_t live_seqs;
+} pa_pool_stats_t;
+
+/* free_order: host int32 [num_blocks], a permutation of 0..num_blocks-1, or NULL. */
+pa_status pa_pool_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order,
+                         pa_pool** out);
+void pa_pool_destroy(pa_pool* pool);
+/* Pop one block (refcount 1). PA_ERR_OOM when empty. */
+pa_status pa_pool_alloc(pa_pool* pool, int32_t* block);
+pa_status pa_pool_incref(pa_pool* pool, int32_t block);
+/* Refcount - 1; pushed back on the free list at 0. PA_ERR_REFCOUNT if not allocated. */
+pa_status pa_pool_decref(pa_pool* pool, int32_t block);
+/* Refcount of `block` (0 = free), or -1 for an out-of-range id. */
+int32_t pa_pool_refcount(const pa_pool* pool, int32_t block);
+pa_status pa_pool_stats(const pa_pool* pool, pa_pool_stats_t* stats);
+
+/* Sequences: each owns a block table and a length. */
+pa_status pa_seq_create(pa_pool* pool, int32_t* seq);
+/* Release every block of the sequence (in logical order) and retire the id. */
+pa_status pa_seq_free(pa_pool* pool, int32_t seq);
+/* New sequence sharing the parent's first ceil(num_tokens/block_size) blocks
+ * (each refcount + 1), length num_tokens <= parent length. */
+pa_status pa_seq_fork(pa_pool* pool, int32_t parent, int32_t num_tokens, int32_t* child);
+/* Reserve the slot of the sequence's next token (allocate_slots for one
+ * token). If the length is a multiple of block_size a fresh block is
+ * appended to the table. Otherwise, if the target block is shared
+ * (refcount > 1), copy-on-write: a fresh block replaces it in this table, the
+ * old block's refcount drops by one, and (src, dst) is returned in cow_pair
+ * with *has_cow = 1 -- the caller must run pa_copy_blocks on that pair before
+ * writing the token. *slot = table[len / bs] * bs + len % bs. */
+pa_status pa_seq_append_slot(pa_pool* pool, int32_t seq, int64_t* slot, int32_t cow_pair[2],
+                             int32_t* has_cow);
+/* Append n tokens; slots (nullable, [n]) and cow_pairs (nullable, [n][2])
+ * receive the results, *num_cow (nullable) the number of pairs. All or
+ * nothing: on PA_ERR_OOM the pool is unchanged. */
+pa_status pa_seq_append_tokens(pa_pool* pool, int32_t seq, int32_t n, int64_t* slots,
+                               int32_t* cow_pairs, int32_t* num_cow);
+pa_status pa_seq_length(const pa_pool* pool, int32_t seq, int32_t* length);
+/* Copy the sequence's table into out[0..cap); *n_blocks = its block count. */
+pa_status pa_seq_table(const pa_pool* pool, int32_t seq, int32_t* out, int32_t cap,
+                       int32_t* n_blocks);
+/* Pack the tables and lengths of seqs[0..n) into host arrays
+ * tables[n][max_blocks] (unused entries -1) and lens[n], ready to upload. */
+pa_status pa_pool_export(const pa_pool* pool, const int32_t* seqs, int32_t n, int32_t max_blocks,
+                         int32_t* tables, int32_t* lens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

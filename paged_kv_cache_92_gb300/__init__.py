@@ -1,0 +1,345 @@
+"""Python binding of libpagedkv.so: paged KV-cache decode attention on GB300.
+
+Argument marshalling only. Every step of the data path runs in the CUDA
+kernels of ``libpagedkv.so`` (see ``include/pagedkv.h``); torch supplies
+device memory and streams. There is no CPU fallback: if the library has not
+been built, every call raises.
+
+Names follow the C ABI: ``pa_decode``, ``pa_decode_workspace_size``,
+``pa_reshape_and_cache``, ``pa_copy_blocks``, ``pa_device_errors`` and the
+``pa_pool_*`` / ``pa_seq_*`` block-pool calls (wrapped by ``Pool``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+PA_OK = 0
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OOM",
+                4: "PA_ERR_REFCOUNT", 5: "PA_ERR_BOUNDS", 6: "PA_ERR_CUDA"}
+DEVERR_TABLE_ENTRY = 0x1
+DEVERR_CONTEXT_LEN = 0x2
+DEVERR_SLOT = 0x4
+DEVERR_COPY_PAIR = 0x8
+DEVERR_TIMEOUT = 0x10
+
+EXPORTED_SYMBOLS = [
+    "pa_status_string", "pa_last_error", "pa_version", "pa_device_errors",
+    "pa_decode_workspace_size", "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_pool_create", "pa_pool_destroy", "pa_pool_alloc", "pa_pool_incref", "pa_pool_decref",
+    "pa_pool_refcount", "pa_pool_stats", "pa_seq_create", "pa_seq_free", "pa_seq_fork",
+    "pa_seq_append_slot", "pa_seq_append_tokens", "pa_seq_length", "pa_seq_table",
+    "pa_pool_export",
+]
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {detail}")
+
+
+class PoolOOM(PagedKVError):
+    pass
+
+
+class DecodeParams(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("block_tables", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
+        ("max_blocks_per_seq", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("partition_tokens", ctypes.c_int32),
+    ]
+
+
+class PoolStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("num_blocks", "block_size", "free_blocks", "used_blocks", "shared_blocks",
+                 "max_refcount", "live_seqs")]
+
+
+_lib = None
+
+
+def load():
+    """Load libpagedkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: run paged_kv_cache_92_gb300.build.build() "
+                          "(or __graft_entry__.build()) first; there is no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    P = ctypes.POINTER
+    sigs = {
+        "pa_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "pa_last_error": ([], ctypes.c_char_p),
+        "pa_version": ([], i32),
+        "pa_device_errors": ([vp, P(ctypes.c_uint32)], ctypes.c_int),
+        "pa_decode_workspace_size": ([P(DecodeParams)], sz),
+        "pa_decode": ([P(DecodeParams), vp, sz, vp], ctypes.c_int),
+        "pa_reshape_and_cache": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
+        "pa_copy_blocks": ([vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
+        "pa_pool_create": ([i32, i32, vp, P(vp)], ctypes.c_int),
+        "pa_pool_destroy": ([vp], None),
+        "pa_pool_alloc": ([vp, P(i32)], ctypes.c_int),
+        "pa_pool_incref": ([vp, i32], ctypes.c_int),
+        "pa_pool_decref": ([vp, i32], ctypes.c_int),
+        "pa_pool_refcount": ([vp, i32], i32),
+        "pa_pool_stats": ([vp, P(PoolStats)], ctypes.c_int),
+        "pa_seq_create": ([vp, P(i32)], ctypes.c_int),
+        "pa_seq_free": ([vp, i32], ctypes.c_int),
+        "pa_seq_fork": ([vp, i32, i32, P(i32)], ctypes.c_int),
+        "pa_seq_append_slot": ([vp, i32, P(i64), P(i32), P(i32)], ctypes.c_int),
+        "pa_seq_append_tokens": ([vp, i32, i32, vp, vp, P(i32)], ctypes.c_int),
+        "pa_seq_length": ([vp, i32, P(i32)], ctypes.c_int),
+        "pa_seq_table": ([vp, i32, vp, i32, P(i32)], ctypes.c_int),
+        "pa_pool_export": ([vp, vp, i32, i32, vp, vp], ctypes.c_int),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != PA_OK:
+        detail = load().pa_last_error().decode(errors="replace")
+        cls = PoolOOM if status == 3 else PagedKVError
+        raise cls(status, where, detail)
+
+
+# --------------------------------------------------------------------------
+# device calls (torch tensors in, marshalled to raw pointers)
+# --------------------------------------------------------------------------
+
+def _dev_ptr(t, dtype, name: str) -> int:
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
+                       max_context_len: int, scale: Optional[float] = None,
+                       partition_tokens: int = 0) -> DecodeParams:
+    import torch
+
+    B, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("shape mismatch between q / out / k_cache / v_cache")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    p = DecodeParams()
+    p.q = _dev_ptr(q, torch.bfloat16, "q")
+    p.out = _dev_ptr(out, torch.bfloat16, "out")
+    p.k_cache = _dev_ptr(k_cache, torch.bfloat16, "k_cache")
+    p.v_cache = _dev_ptr(v_cache, torch.bfloat16, "v_cache")
+    p.block_tables = _dev_ptr(block_tables, torch.int32, "block_tables")
+    p.context_lens = _dev_ptr(context_lens, torch.int32, "context_lens")
+    p.max_blocks_per_seq = block_tables.shape[1]
+    p.num_seqs, p.num_q_heads, p.num_kv_heads = B, Hq, Hkv
+    p.head_dim, p.block_size, p.num_blocks = D, BS, NB
+    p.max_context_len = int(max_context_len)
+    p.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
+    p.partition_tokens = int(partition_tokens)
+    return p
+
+
+def pa_decode_workspace_size(params: DecodeParams) -> int:
+    return int(load().pa_decode_workspace_size(ctypes.byref(params)))
+
+
+def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+              scale: Optional[float] = None, partition_tokens: int = 0, out=None,
+              workspace=None, stream=None):
+    """Paged decode attention; returns ``out`` (bf16 [B][Hq][d]).
+
+    ``workspace`` is a uint8 CUDA tensor of at least
+    ``pa_decode_workspace_size`` bytes; allocated here when omitted.
+    """
+    import torch
+
+    lib = load()
+    if out is None:
+        out = torch.empty_like(q)
+    p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
+                           max_context_len, scale, partition_tokens)
+    need = int(lib.pa_decode_workspace_size(ctypes.byref(p)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev_ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(lib.pa_decode(ctypes.byref(p), ws_ptr, ws_bytes, _stream_handle(stream)), "pa_decode")
+    return out
+
+
+def pa_reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    import torch
+
+    T, Hkv, D = k_new.shape
+    NB, Hkv2, BS, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or tuple(v_new.shape) != tuple(k_new.shape) \
+            or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(slot_mapping.shape) != (T,):
+        raise ValueError("shape mismatch in pa_reshape_and_cache")
+    lib = load()
+    _check(lib.pa_reshape_and_cache(
+        _dev_ptr(k_new, torch.bfloat16, "k_new"), _dev_ptr(v_new, torch.bfloat16, "v_new"),
+        _dev_ptr(k_cache, torch.bfloat16, "k_cache"), _dev_ptr(v_cache, torch.bfloat16, "v_cache"),
+        _dev_ptr(slot_mapping, torch.int64, "slot_mapping"), T, Hkv, D, BS, NB,
+        _stream_handle(stream)), "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
+    import torch
+
+    NB, Hkv, BS, D = k_cache.shape
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int32 [n][2]")
+    lib = load()
+    _check(lib.pa_copy_blocks(
+        _dev_ptr(k_cache, torch.bfloat16, "k_cache"), _dev_ptr(v_cache, torch.bfloat16, "v_cache"),
+        _dev_ptr(pairs, torch.int32, "pairs"), pairs.shape[0], Hkv, D, BS, NB,
+        _stream_handle(stream)), "pa_copy_blocks")
+
+
+def pa_device_errors(stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    _check(load().pa_device_errors(_stream_handle(stream), ctypes.byref(flags)), "pa_device_errors")
+    return int(flags.value)
+
+
+# --------------------------------------------------------------------------
+# host block pool
+# --------------------------------------------------------------------------
+
+class Pool:
+    """Host block pool (``pa_pool_*`` / ``pa_seq_*``). Free list is a stack seeded
+    from ``free_order`` (first element handed out first)."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16,
+                 free_order: Optional[Sequence[int]] = None):
+        self._lib = load()
+        self._h = ctypes.c_void_p()
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+        _check(self._lib.pa_pool_create(num_blocks, block_size,
+                                        None if order is None else order.ctypes.data,
+                                        ctypes.byref(self._h)), "pa_pool_create")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.pa_pool_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self) -> int:
+        b = ctypes.c_int32()
+        _check(self._lib.pa_pool_alloc(self._h, ctypes.byref(b)), "pa_pool_alloc")
+        return b.value
+
+    def incref(self, blk: int) -> None:
+        _check(self._lib.pa_pool_incref(self._h, blk), "pa_pool_incref")
+
+    def decref(self, blk: int) -> None:
+        _check(self._lib.pa_pool_decref(self._h, blk), "pa_pool_decref")
+
+    def refcount(self, blk: int) -> int:
+        return int(self._lib.pa_pool_refcount(self._h, blk))
+
+    def stats(self) -> dict:
+        st = PoolStats()
+        _check(self._lib.pa_pool_stats(self._h, ctypes.byref(st)), "pa_pool_stats")
+        return {n: getattr(st, n) for n, _ in PoolStats._fields_}
+
+    def seq_create(self) -> int:
+        s = ctypes.c_int32()
+        _check(self._lib.pa_seq_create(self._h, ctypes.byref(s)), "pa_seq_create")
+        return s.value
+
+    def seq_free(self, seq: int) -> None:
+        _check(self._lib.pa_seq_free(self._h, seq), "pa_seq_free")
+
+    def seq_fork(self, parent: int, num_tokens: int) -> int:
+        c = ctypes.c_int32()
+        _check(self._lib.pa_seq_fork(self._h, parent, num_tokens, ctypes.byref(c)), "pa_seq_fork")
+        return c.value
+
+    def append_slot(self, seq: int) -> Tuple[int, Optional[Tuple[int, int]]]:
+        slot = ctypes.c_int64()
+        pair = (ctypes.c_int32 * 2)()
+        has = ctypes.c_int32()
+        _check(self._lib.pa_seq_append_slot(self._h, seq, ctypes.byref(slot), pair,
+                                            ctypes.byref(has)), "pa_seq_append_slot")
+        return slot.value, ((pair[0], pair[1]) if has.value else None)
+
+    def append_tokens(self, seq: int, n: int, want_slots: bool = True):
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int32)
+        ncow = ctypes.c_int32()
+        _check(self._lib.pa_seq_append_tokens(
+            self._h, seq, n, slots.ctypes.data if want_slots else None, pairs.ctypes.data,
+            ctypes.byref(ncow)), "pa_seq_append_tokens")
+        return (slots[:n].tolist() if want_slots else None,
+                [tuple(int(x) for x in r) for r in pairs[:ncow.value]])
+
+    def length(self, seq: int) -> int:
+        n = ctypes.c_int32()
+        _check(self._lib.pa_seq_length(self._h, seq, ctypes.byref(n)), "pa_seq_length")
+        return n.value
+
+    def table(self, seq: int) -> List[int]:
+        n = ctypes.c_int32()
+        _check(self._lib.pa_seq_table(self._h, seq, None, 0, ctypes.byref(n)), "pa_seq_table")
+        buf = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(self._lib.pa_seq_table(self._h, seq, buf.ctypes.data, buf.shape[0],
+                                      ctypes.byref(n)), "pa_seq_table")
+        return buf[:n.value].tolist()
+
+    def export(self, seqs: Sequence[int], max_blocks: int):
+        s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        tables = np.empty((len(s), max_blocks), dtype=np.int32)
+        lens = np.empty(len(s), dtype=np.int32)
+        _check(self._lib.pa_pool_export(self._h, s.ctypes.data, len(s), max_blocks,
+                                        tables.ctypes.data, lens.ctypes.data), "pa_pool_export")
+        return tables, lens

@@ -1,0 +1,219 @@
+// C ABI entry points of libpagedkv.so: host-side argument validation, launch
+// policy (split-K partition count, workspace carve-up) and status reporting.
+// Every check here runs before anything is launched.
+#include <cuda_runtime_api.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+thread_local char g_msg[512] = "";
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int resolve_partition_tokens(const pa_decode_params* p) {
+  return p->partition_tokens == 0 ? kDefaultPartitionTokens : p->partition_tokens;
+}
+
+// Full host validation of decode params. Returns PA_OK or an error (message set).
+pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
+  if (!p) return set_error(PA_ERR_INVALID_ARG, "pa_decode: params is NULL");
+  if (p->num_seqs < 0 || p->num_seqs > 65535)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: num_seqs must be in [0, 65535]");
+  if (p->num_q_heads < 1 || p->num_kv_heads < 1 || p->num_q_heads % p->num_kv_heads != 0)
+    return set_error(PA_ERR_INVALID_ARG,
+                     "pa_decode: num_q_heads must be a positive multiple of num_kv_heads");
+  if (p->num_kv_heads > 65535)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: num_kv_heads must be <= 65535");
+  if (p->block_size != kBlockSize)
+    return set_error(PA_ERR_UNSUPPORTED, "pa_decode: only block_size 16 is built");
+  if (p->head_dim != 64 && p->head_dim != 128)
+    return set_error(PA_ERR_UNSUPPORTED, "pa_decode: head_dim must be 64 or 128");
+  const int g = p->num_q_heads / p->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8)
+    return set_error(PA_ERR_UNSUPPORTED, "pa_decode: query heads per KV head must be 1, 2, 4 or 8");
+  if (p->num_blocks < 1) return set_error(PA_ERR_INVALID_ARG, "pa_decode: num_blocks < 1");
+  if (p->max_blocks_per_seq < 1)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq < 1");
+  if (p->max_context_len < 1)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_context_len < 1");
+  if (int64_t(p->max_blocks_per_seq) * kBlockSize > INT32_MAX)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq too large");
+  const int pt = resolve_partition_tokens(p);
+  if (pt < kBlockSize || pt > kMaxPartitionTokens || pt % kBlockSize != 0)
+    return set_error(PA_ERR_INVALID_ARG,
+                     "pa_decode: partition_tokens must be 0 or a multiple of 16 in [16, 4096]");
+  if (!(p->scale > 0.0f) || p->scale != p->scale)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: scale must be a positive finite number");
+  if (need_pointers && p->num_seqs > 0) {
+    if (!p->q || !p->out || !p->k_cache || !p->v_cache || !p->block_tables || !p->context_lens)
+      return set_error(PA_ERR_INVALID_ARG, "pa_decode: a required pointer is NULL");
+    if (!aligned16(p->q) || !aligned16(p->out) || !aligned16(p->k_cache) ||
+        !aligned16(p->v_cache))
+      return set_error(PA_ERR_INVALID_ARG,
+                       "pa_decode: q, out, k_cache and v_cache must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(p->block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(p->context_lens) & 3u))
+      return set_error(PA_ERR_INVALID_ARG, "pa_decode: int32 arrays must be 4-byte aligned");
+  }
+  return PA_OK;
+}
+
+int num_partitions_for(const pa_decode_params* p) {
+  const int pt = resolve_partition_tokens(p);
+  int64_t cap = int64_t(p->max_blocks_per_seq) * kBlockSize;
+  int64_t mx = p->max_context_len < cap ? p->max_context_len : cap;
+  return int((mx + pt - 1) / pt);
+}
+}  // namespace
+
+pa_status set_error(pa_status s, const char* msg) {
+  if (s != PA_OK) std::snprintf(g_msg, sizeof(g_msg), "%s", msg);
+  return s;
+}
+
+pa_status set_cuda_error(const char* where, int err) {
+  std::snprintf(g_msg, sizeof(g_msg), "%s: %s", where,
+                cudaGetErrorString(static_cast<cudaError_t>(err)));
+  return PA_ERR_CUDA;
+}
+
+size_t decode_workspace_layout(const pa_decode_params* p, int num_partitions, size_t* off_m,
+                               size_t* off_l, size_t* off_acc) {
+  if (num_partitions <= 1) {
+    *off_m = *off_l = *off_acc = 0;
+    return 0;
+  }
+  const size_t rows = size_t(p->num_seqs) * p->num_q_heads * num_partitions;
+  *off_m = 0;
+  *off_l = round_up(rows * sizeof(float), 256);
+  *off_acc = *off_l + round_up(rows * sizeof(float), 256);
+  return *off_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+}
+
+}  // namespace pa
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_OOM: return "PA_ERR_OOM";
+    case PA_ERR_REFCOUNT: return "PA_ERR_REFCOUNT";
+    case PA_ERR_BOUNDS: return "PA_ERR_BOUNDS";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+const char* pa_last_error(void) { return pa::g_msg; }
+
+int32_t pa_version(void) { return 1; }
+
+pa_status pa_device_errors(pa_stream_t stream, uint32_t* flags) {
+  if (!flags) return pa::set_error(PA_ERR_INVALID_ARG, "pa_device_errors: flags is NULL");
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return pa::set_cuda_error("pa_device_errors: stream sync", int(e));
+  uint32_t a = 0, b = 0;
+  int r = pa::read_and_clear_decode_errors(&a);
+  if (r != 0) return pa::set_cuda_error("pa_device_errors: read", r);
+  r = pa::read_and_clear_cache_errors(&b);
+  if (r != 0) return pa::set_cuda_error("pa_device_errors: read", r);
+  *flags = a | b;
+  return PA_OK;
+}
+
+size_t pa_decode_workspace_size(const pa_decode_params* p) {
+  if (pa::check_decode(p, false) != PA_OK) return 0;
+  size_t a, b, c;
+  return pa::decode_workspace_layout(p, pa::num_partitions_for(p), &a, &b, &c);
+}
+
+pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace_bytes,
+                    pa_stream_t stream) {
+  pa_status st = pa::check_decode(p, true);
+  if (st != PA_OK) return st;
+  if (p->num_seqs == 0) return PA_OK;
+  const int np = pa::num_partitions_for(p);
+  size_t om, ol, oa;
+  const size_t need = pa::decode_workspace_layout(p, np, &om, &ol, &oa);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need)
+      return pa::set_error(PA_ERR_INVALID_ARG,
+                           "pa_decode: workspace smaller than pa_decode_workspace_size()");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return pa::set_error(PA_ERR_INVALID_ARG, "pa_decode: workspace must be 256-byte aligned");
+  }
+  pa::DecodeLaunch L;
+  L.p = p;
+  L.partition_tokens = p->partition_tokens == 0 ? pa::kDefaultPartitionTokens : p->partition_tokens;
+  L.num_partitions = np;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  L.part_m = need ? reinterpret_cast<float*>(ws + om) : nullptr;
+  L.part_l = need ? reinterpret_cast<float*>(ws + ol) : nullptr;
+  L.part_acc = need ? reinterpret_cast<float*>(ws + oa) : nullptr;
+  const int e = pa::launch_decode(L, stream);
+  if (e != 0) return pa::set_cuda_error("pa_decode: launch", e);
+  return PA_OK;
+}
+
+pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,
+                               void* v_cache, const int64_t* slot_mapping, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, pa_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1)
+    return pa::set_error(PA_ERR_INVALID_ARG,
+                         "pa_reshape_and_cache: num_tokens >= 0, num_kv_heads >= 1, num_blocks >= 1");
+  if (block_size != pa::kBlockSize)
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache: only block_size 16 is built");
+  if (head_dim < 8 || head_dim % 8 != 0 || head_dim > 1024)
+    return pa::set_error(PA_ERR_UNSUPPORTED,
+                         "pa_reshape_and_cache: head_dim must be a multiple of 8 in [8, 1024]");
+  if (num_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping)
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: a required pointer is NULL");
+  if (!pa::aligned16(k_new) || !pa::aligned16(v_new) || !pa::aligned16(k_cache) ||
+      !pa::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: misaligned pointer");
+  // one thread per 16-byte chunk, 256 per CTA: keep the grid within gridDim.x
+  if (int64_t(num_tokens) * num_kv_heads * (head_dim / 8) > (int64_t(1) << 38))
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: too many tokens");
+  const int e = pa::launch_reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping,
+                                             num_tokens, num_kv_heads, head_dim, num_blocks, stream);
+  if (e != 0) return pa::set_cuda_error("pa_reshape_and_cache: launch", e);
+  return PA_OK;
+}
+
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_blocks, pa_stream_t stream) {
+  if (num_pairs < 0 || num_pairs > 65535 || num_kv_heads < 1 || num_blocks < 1)
+    return pa::set_error(PA_ERR_INVALID_ARG,
+                         "pa_copy_blocks: num_pairs in [0, 65535], num_kv_heads >= 1, num_blocks >= 1");
+  if (block_size != pa::kBlockSize)
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks: only block_size 16 is built");
+  if (head_dim < 8 || head_dim % 8 != 0 || head_dim > 1024)
+    return pa::set_error(PA_ERR_UNSUPPORTED,
+                         "pa_copy_blocks: head_dim must be a multiple of 8 in [8, 1024]");
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !pairs)
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: a required pointer is NULL");
+  if (!pa::aligned16(k_cache) || !pa::aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(pairs) & 3u))
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: misaligned pointer");
+  const int e = pa::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_kv_heads, head_dim,
+                                       num_blocks, stream);
+  if (e != 0) return pa::set_cuda_error("pa_copy_blocks: launch", e);
+  return PA_OK;
+}
+
+}  // extern "C"

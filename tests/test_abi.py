@@ -1,0 +1,99 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol that
+include/pagedkv.h declares, and rejects bad host-side arguments before any
+launch (no GPU is touched by these calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_cache_92_gb300 import build
+
+    build.build()
+    import paged_kv_cache_92_gb300 as pk
+
+    pk.load()
+    return pk
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = set(re.findall(r"\b(pa_[a-z_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_expected_calls(pk):
+    declared = _declared_functions()
+    assert set(declared) == set(pk.EXPORTED_SYMBOLS)
+    for name in ("pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_pool_create",
+                 "pa_seq_append_slot"):
+        assert name in declared
+
+
+def test_library_exports_every_declared_symbol(pk):
+    lib = ctypes.CDLL(pk.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert pk.load().pa_version() == 1
+
+
+def test_status_strings(pk):
+    lib = pk.load()
+    for code, name in pk.STATUS_NAMES.items():
+        assert lib.pa_status_string(code).decode() == name
+
+
+def _params(pk, **kw):
+    p = pk.DecodeParams()
+    base = dict(max_blocks_per_seq=4, num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                block_size=16, num_blocks=8, max_context_len=64, scale=0.088, partition_tokens=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), 2),
+    (dict(block_size=32), 2),
+    (dict(num_q_heads=12, num_kv_heads=1), 2),
+    (dict(num_q_heads=6, num_kv_heads=4), 1),
+    (dict(max_context_len=0), 1),
+    (dict(partition_tokens=24), 1),
+    (dict(partition_tokens=8192), 1),
+    (dict(scale=0.0), 1),
+    (dict(num_seqs=70000), 1),
+    (dict(), 1),  # valid shapes, NULL pointers
+])
+def test_decode_rejects_bad_arguments_on_the_host(pk, kw, status):
+    lib = pk.load()
+    p = _params(pk, **kw)
+    assert lib.pa_decode(ctypes.byref(p), None, 0, None) == status
+    assert lib.pa_last_error()
+
+
+def test_decode_workspace_size(pk):
+    lib = pk.load()
+    # max context 64 <= one 512-token partition: no workspace
+    assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk))) == 0
+    p = _params(pk, max_context_len=2048, max_blocks_per_seq=128)
+    rows = 2 * 8 * 4  # seqs * q heads * partitions
+    want = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == want
+    assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk, head_dim=96))) == 0
+
+
+def test_cache_ops_reject_bad_arguments_on_the_host(pk):
+    lib = pk.load()
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, 32, 10, None) == 2
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, 16, 10, None) == 1
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 0, 8, 128, 16, 10, None) == 0
+    assert lib.pa_copy_blocks(None, None, None, 2, 8, 128, 16, 10, None) == 1
+    assert lib.pa_copy_blocks(None, None, None, 0, 8, 128, 16, 10, None) == 0
+    assert lib.pa_copy_blocks(None, None, None, 70000, 8, 128, 16, 10, None) == 1

@@ -1,0 +1,309 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Bit-exact: KV write through the slot mapping and the copy-on-write block
+copy (whole caches compared). Decode attention: max-abs <= 2e-2 and
+mean-abs <= 2e-3 (bf16 inputs, fp32 accumulation). Padding slots hold NaN
+in every case, so a masked slot that leaks into a result fails the
+finiteness check.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import torch
+
+    from paged_kv_cache_92_gb300 import build
+
+    build.build()
+    import paged_kv_cache_92_gb300 as pk
+
+    pk.load()
+    assert torch.cuda.is_available()
+    return pk
+
+
+def _check_errors(pk):
+    assert pk.pa_device_errors() == 0
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_tiny_workload_full(pk):
+    """4 sequences {1,5,17,33}, 4/1 heads, d=64: decode, append, decode again."""
+    import torch
+
+    r = workloads.tiny()
+    case = harness.build_case(r)
+    # decode before the append, over the pre-step lengths
+    kc, vc = case.k_cache, case.v_cache
+    out0 = pk.pa_decode(case.q, kc, vc, torch.from_numpy(case.tables0).cuda(),
+                        torch.from_numpy(case.lens0).cuda(), max_context_len=33)
+    ref0 = oracle.paged_decode(case.q.cpu(), kc.cpu(), vc.cpu(), case.tables0, case.lens0)
+    harness.assert_close(harness.bf16_tensor_to_f64(out0), ref0)
+    # the step: append one token per sequence (no boundary crossed), decode over {2,6,18,34}
+    assert case.cows.shape[0] == 0
+    assert list(case.lens) == [2, 6, 18, 34]
+    out, kg, vg = harness.run_step_gpu(case)
+    ref, ko, vo = harness.run_step_oracle(case)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    _check_errors(pk)
+
+
+def test_llama8b_layer_full(pk):
+    case = harness.build_case(workloads.llama8b_layer())
+    out, kg, vg = harness.run_step_gpu(case)
+    ref, ko, vo = harness.run_step_oracle(case)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    _check_errors(pk)
+
+
+def test_llama8b_high_concurrency_full(pk):
+    r = workloads.llama8b_high_concurrency()
+    case = harness.build_case(r)
+    # new blocks were allocated exactly for the sequences sitting on a boundary
+    grew = (case.tables >= 0).sum(1) - (case.tables0 >= 0).sum(1)
+    assert np.array_equal(grew, (r.lens0 % 16 == 0).astype(int))
+    out, kg, vg = harness.run_step_gpu(case)
+    ref, ko, vo = harness.run_step_oracle(case)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    _check_errors(pk)
+
+
+@pytest.mark.parametrize("batch", [8, 32])
+def test_llama70b_long_context(pk, batch):
+    """64/8 heads, L ~ U[8192, 32768]: split-K over 512-token partitions + merge."""
+    r = workloads.llama70b_long(batch=batch)
+    case = harness.build_case(r)
+    out, kg, vg = harness.run_step_gpu(case)
+    B, Hq = r.num_seqs, r.num_q_heads
+    if batch == 8:
+        units = None
+    else:
+        units = harness.sample_units(B, Hq, 192, seed=batch,
+                                     must=[(int(np.argmax(case.lens)), 0),
+                                           (int(np.argmin(case.lens)), Hq - 1)])
+    ref, ko, vo = harness.run_step_oracle(case, units=units)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
+    got = harness.bf16_tensor_to_f64(out)
+    if units is not None:
+        got = np.stack([got[b, h] for b, h in units])
+    harness.assert_close(got, ref)
+    _check_errors(pk)
+
+
+def test_shared_prefix_copy_on_write(pk):
+    r = workloads.shared_prefix()
+    case = harness.build_case(r)
+    assert case.cows.shape == (32, 2)
+    assert len(set(case.cows[:, 0].tolist())) == 1  # all copies come from the last shared block
+    out, kg, vg = harness.run_step_gpu(case)
+    ref, ko, vo = harness.run_step_oracle(case)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    _check_errors(pk)
+
+
+# ---------------------------------------------------------------- edge cases
+
+def _direct_case(lens, Hq, Hkv, D, seed, extra_blocks=3, reverse=False, identity=False):
+    import torch
+
+    lens = np.asarray(lens, dtype=np.int64)
+    need = int(((lens + 15) // 16).sum())
+    NB = need + extra_blocks
+    rng = np.random.default_rng(seed)
+    if identity:
+        order = np.arange(NB, dtype=np.int32)
+    elif reverse:
+        order = np.arange(NB, dtype=np.int32)[::-1].copy()
+    else:
+        order = rng.permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, 16)
+    q = workloads.bf16_normal((len(lens), Hq, D), seed + 1, "cuda")
+    kc = workloads.bf16_normal((NB, Hkv, 16, D), seed + 2, "cuda")
+    vc = workloads.bf16_normal((NB, Hkv, 16, D), seed + 3, "cuda")
+    workloads.fill_padding_nan(kc, tables, lens, 16)
+    workloads.fill_padding_nan(vc, tables, lens, 16)
+    return q, kc, vc, tables, lens.astype(np.int32), torch
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("partition", [0, 16, 64, 4096])
+def test_edge_lengths(pk, D, G, partition):
+    lens = [1, 15, 16, 17, 511, 512, 513, 1024, 1025, 4097]
+    Hkv = 2
+    q, kc, vc, tables, lens, torch = _direct_case(lens, G * Hkv, Hkv, D, seed=D * 10 + G)
+    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=int(lens.max()), partition_tokens=partition)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    _check_errors(pk)
+
+
+@pytest.mark.parametrize("partition", [0, 16])
+def test_length_one_returns_v0_bit_exact(pk, partition):
+    q, kc, vc, tables, lens, torch = _direct_case([1] * 6, 8, 2, 128, seed=5)
+    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=1, partition_tokens=partition)
+    torch.cuda.synchronize()
+    vh = vc.cpu()
+    for b in range(6):
+        for h in range(8):
+            assert torch.equal(out[b, h].cpu(), vh[tables[b, 0], h // 4, 0])
+
+
+def test_physical_placement_does_not_change_a_bit(pk):
+    lens = [37, 300, 1, 900, 16, 513]
+    outs = []
+    for kind in ("random", "reverse", "identity"):
+        q, kc, vc, tables, lens_a, torch = _direct_case(
+            lens, 32, 8, 128, seed=77, extra_blocks=0,
+            reverse=(kind == "reverse"), identity=(kind == "identity"))
+        # same logical contents under every placement: rebuild the caches from logical order
+        base_q, base_kc, base_vc, base_tables, _, _ = _direct_case(lens, 32, 8, 128, seed=77,
+                                                                    extra_blocks=0)
+        kc2 = torch.empty_like(base_kc)
+        vc2 = torch.empty_like(base_vc)
+        kc2[torch.from_numpy(tables[tables >= 0]).long().cuda()] = \
+            base_kc[torch.from_numpy(base_tables[base_tables >= 0]).long().cuda()]
+        vc2[torch.from_numpy(tables[tables >= 0]).long().cuda()] = \
+            base_vc[torch.from_numpy(base_tables[base_tables >= 0]).long().cuda()]
+        out = pk.pa_decode(base_q, kc2, vc2, torch.from_numpy(tables).cuda(),
+                           torch.from_numpy(lens_a).cuda(), max_context_len=900)
+        outs.append(out.cpu())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_split_and_unsplit_agree(pk):
+    q, kc, vc, tables, lens, torch = _direct_case([700, 2049, 3000], 32, 8, 128, seed=9)
+    bt, cl = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+    a = pk.pa_decode(q, kc, vc, bt, cl, max_context_len=3000, partition_tokens=4096)
+    b = pk.pa_decode(q, kc, vc, bt, cl, max_context_len=3000, partition_tokens=128)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(a), ref)
+    harness.assert_close(harness.bf16_tensor_to_f64(b), ref)
+
+
+def test_zero_length_rows_are_zero(pk):
+    q, kc, vc, tables, lens, torch = _direct_case([5, 20, 3], 8, 2, 128, seed=11)
+    lens2 = lens.copy()
+    lens2[1] = 0
+    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens2).cuda(),
+                       max_context_len=20)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out[1]).item() == 0
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    got = harness.bf16_tensor_to_f64(out)
+    harness.assert_close(got[[0, 2]], ref[[0, 2]])
+
+
+def test_empty_batch_and_empty_writes(pk):
+    import torch
+
+    q = torch.empty((0, 8, 128), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((4, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    out = pk.pa_decode(q, kc, kc, torch.empty((0, 1), dtype=torch.int32, device="cuda"),
+                       torch.empty((0,), dtype=torch.int32, device="cuda"), max_context_len=1)
+    assert out.shape == (0, 8, 128)
+    pk.pa_reshape_and_cache(torch.empty((0, 2, 128), dtype=torch.bfloat16, device="cuda"),
+                            torch.empty((0, 2, 128), dtype=torch.bfloat16, device="cuda"), kc, kc,
+                            torch.empty((0,), dtype=torch.int64, device="cuda"))
+    pk.pa_copy_blocks(kc, kc, torch.empty((0, 2), dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    _check_errors(pk)
+
+
+def test_reshape_and_cache_skips_negative_slots_bit_exact(pk):
+    import torch
+
+    NB, Hkv, D = 12, 8, 128
+    kc = workloads.bf16_normal((NB, Hkv, 16, D), 1, "cuda")
+    vc = workloads.bf16_normal((NB, Hkv, 16, D), 2, "cuda")
+    kn = workloads.bf16_normal((7, Hkv, D), 3, "cuda")
+    vn = workloads.bf16_normal((7, Hkv, D), 4, "cuda")
+    slots = np.array([0, -1, 191, 17, -5, 100, 16], dtype=np.int64)
+    k2, v2 = kc.clone(), vc.clone()
+    pk.pa_reshape_and_cache(kn, vn, k2, v2, torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    ko, vo = oracle.reshape_and_cache(kn.cpu(), vn.cpu(), kc.cpu(), vc.cpu(), slots)
+    assert np.array_equal(oracle.bf16_bits(k2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(v2.cpu()), vo)
+
+
+def test_copy_blocks_bit_exact_and_untouched_blocks(pk):
+    import torch
+
+    NB, Hkv, D = 20, 8, 128
+    kc = workloads.bf16_normal((NB, Hkv, 16, D), 5, "cuda")
+    vc = workloads.bf16_normal((NB, Hkv, 16, D), 6, "cuda")
+    pairs = np.array([[3, 11], [3, 12], [0, 19], [7, 2]], dtype=np.int32)
+    k2, v2 = kc.clone(), vc.clone()
+    pk.pa_copy_blocks(k2, v2, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    ko, vo = oracle.copy_blocks(kc.cpu(), vc.cpu(), pairs)
+    assert np.array_equal(oracle.bf16_bits(k2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(v2.cpu()), vo)
+
+
+# ---------------------------------------------------------------- device-side range checks
+
+def test_bad_device_values_set_error_bits_without_faulting(pk):
+    import torch
+
+    q, kc, vc, tables, lens, _ = _direct_case([40, 7], 8, 2, 128, seed=13)
+    assert pk.pa_device_errors() == 0
+    bad = tables.copy()
+    bad[0, 1] = kc.shape[0] + 1000  # past the pool
+    pk.pa_decode(q, kc, vc, torch.from_numpy(bad).cuda(), torch.from_numpy(lens).cuda(),
+                 max_context_len=40)
+    assert pk.pa_device_errors() & pk.DEVERR_TABLE_ENTRY
+    long = lens.copy()
+    long[1] = 41  # above the host-promised maximum
+    pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(long).cuda(),
+                 max_context_len=40)
+    assert pk.pa_device_errors() & pk.DEVERR_CONTEXT_LEN
+    kn = workloads.bf16_normal((1, 2, 128), 1, "cuda")
+    pk.pa_reshape_and_cache(kn, kn, kc.clone(), vc.clone(),
+                            torch.tensor([kc.shape[0] * 16], dtype=torch.int64, device="cuda"))
+    assert pk.pa_device_errors() & pk.DEVERR_SLOT
+    pk.pa_copy_blocks(kc.clone(), vc.clone(),
+                      torch.tensor([[0, kc.shape[0]]], dtype=torch.int32, device="cuda"))
+    assert pk.pa_device_errors() & pk.DEVERR_COPY_PAIR
+    # the context is still healthy
+    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=40)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert pk.pa_device_errors() == 0
+
+
+def test_scale_is_applied(pk):
+    q, kc, vc, tables, lens, torch = _direct_case([33, 70], 8, 2, 64, seed=17)
+    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=70, scale=0.3)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens, scale=0.3)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert not math.isclose(0.3, 1 / 8)

@@ -192,3 +192,76 @@ def fill_padding_nan(cache, tables: np.ndarray, lens: np.ndarray, bs: int) -> No
 
 def lengths_after_append(r: Recipe) -> np.ndarray:
     return r.lens0 + r.append
+
+
+# --------------------------------------------------------------------------
+# Driving a pool through a recipe. The pool object does all block-manager
+# arithmetic; these helpers only issue the recipe's operations in order, so
+# the product pool and the oracle's model each produce their own tables.
+# Both expose seq_create / seq_fork / append_tokens / append_slot / table.
+# --------------------------------------------------------------------------
+
+def drive_prefill(pool, r: Recipe) -> List[int]:
+    """Create every sequence of the recipe with its pre-step length."""
+    if r.diverge_seqs is None:
+        seqs = []
+        for b in range(r.num_seqs):
+            s = pool.seq_create()
+            pool.append_tokens(s, int(r.lens0[b]))
+            seqs.append(s)
+        return seqs
+    div = set(int(x) for x in r.diverge_seqs)
+    root = pool.seq_create()
+    pool.append_tokens(root, r.shared_prefix_tokens)
+    seqs = [root]
+    for b in range(1, r.num_seqs):
+        n = int(r.lens0[b]) if b in div else r.shared_prefix_tokens
+        seqs.append(pool.seq_fork(root, n))
+    for b in range(r.num_seqs):
+        if b not in div:
+            pool.append_tokens(seqs[b], int(r.lens0[b]) - r.shared_prefix_tokens)
+    return seqs
+
+
+def drive_step_append(pool, seqs: List[int], r: Recipe):
+    """Reserve this step's slot for every sequence (``r.append`` tokens each).
+
+    Returns (slot_mapping int64 [B * append], cow_pairs int32 [P][2]).
+    """
+    slots, cows = [], []
+    for s in seqs:
+        for _ in range(r.append):
+            slot, cow = pool.append_slot(s)
+            slots.append(slot)
+            if cow is not None:
+                cows.append(cow)
+    return (np.asarray(slots, dtype=np.int64),
+            np.asarray(cows, dtype=np.int32).reshape(-1, 2))
+
+
+def tables_of(pool, seqs: List[int], max_blocks: Optional[int] = None) -> np.ndarray:
+    rows = [pool.table(s) for s in seqs]
+    mb = max(len(t) for t in rows) if max_blocks is None else max_blocks
+    out = np.full((len(seqs), mb), -1, dtype=np.int32)
+    for i, t in enumerate(rows):
+        out[i, :len(t)] = t
+    return out
+
+
+def step_tensors(r: Recipe, device: str = "cpu", seed_offset: int = 0):
+    """Random tensor contents of one step: q, k_new, v_new, k_cache, v_cache (bf16)."""
+    import torch
+
+    s = r.seed * 1000 + seed_offset
+    B, Hq, Hkv, D, BS = r.num_seqs, r.num_q_heads, r.num_kv_heads, r.head_dim, r.block_size
+    q = bf16_normal((B, Hq, D), s + 1, device)
+    k_new = bf16_normal((B * r.append, Hkv, D), s + 2, device)
+    v_new = bf16_normal((B * r.append, Hkv, D), s + 3, device)
+    k_cache = torch.empty((r.num_blocks, Hkv, BS, D), dtype=torch.bfloat16, device=device)
+    v_cache = torch.empty_like(k_cache)
+    chunk = max(1, (1 << 26) // (Hkv * BS * D))  # ~64M elements per draw
+    for i, c in enumerate((k_cache, v_cache)):
+        for j, start in enumerate(range(0, r.num_blocks, chunk)):
+            stop = min(r.num_blocks, start + chunk)
+            c[start:stop] = bf16_normal((stop - start, Hkv, BS, D), s + 10 + 7919 * i + 31 * j, device)
+    return q, k_new, v_new, k_cache, v_cache
