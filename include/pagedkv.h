@@ -142,6 +142,28 @@ pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace
                     pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_decode_noalloc -- the same decode as pa_decode, for callers that cannot
+ * allocate device memory at decode time. The pages have no counterpart: it
+ * exists because an engine that hands all free HBM to its KV block pool at
+ * start-up has nothing left for a workspace, and a serving loop cannot take
+ * cudaMalloc's implicit device synchronisation.
+ *
+ * The split-K partials go to a fixed device array inside the library
+ * (PA_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library until
+ * the process exits). Nothing is allocated or freed by the call.
+ *  - Shapes whose partials need more than that (num_seqs * num_q_heads *
+ *    partitions * (head_dim + 2) * 4 bytes, each of the three parts rounded up
+ *    to 256 bytes) are rejected with PA_ERR_INVALID_ARG.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its partials in
+ *    it. Calls whose kernels overlap on the GPU (different streams, no
+ *    ordering between them) race on it and give unspecified results.
+ * ---------------------------------------------------------------------- */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+pa_status pa_decode_noalloc(const pa_decode_params* p, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * pa_reshape_and_cache -- write each new token's K/V row into its slot
  * [P1 §One step, end to end: "gather and write KV through the slot-mapping
  * formula"; P3 §The architecture: the forward pass appends the new token's

@@ -32,7 +32,8 @@ DEVERR_TIMEOUT = 0x10
 
 EXPORTED_SYMBOLS = [
     "pa_status_string", "pa_last_error", "pa_version", "pa_device_errors",
-    "pa_decode_workspace_size", "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_reshape_and_cache",
+    "pa_copy_blocks",
     "pa_pool_create", "pa_pool_destroy", "pa_pool_alloc", "pa_pool_incref", "pa_pool_decref",
     "pa_pool_refcount", "pa_pool_stats", "pa_seq_create", "pa_seq_free", "pa_seq_fork",
     "pa_seq_append_slot", "pa_seq_append_tokens", "pa_seq_length", "pa_seq_table",
@@ -90,6 +91,7 @@ def load():
         "pa_device_errors": ([vp, P(ctypes.c_uint32)], ctypes.c_int),
         "pa_decode_workspace_size": ([P(DecodeParams)], sz),
         "pa_decode": ([P(DecodeParams), vp, sz, vp], ctypes.c_int),
+        "pa_decode_noalloc": ([P(DecodeParams), vp], ctypes.c_int),
         "pa_reshape_and_cache": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
         "pa_copy_blocks": ([vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
         "pa_pool_create": ([i32, i32, vp, P(vp)], ctypes.c_int),
@@ -203,6 +205,27 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
     ws_ptr = _dev_ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(lib.pa_decode(ctypes.byref(p), ws_ptr, ws_bytes, _stream_handle(stream)), "pa_decode")
+    return out
+
+
+def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+                      scale: Optional[float] = None, partition_tokens: int = 0, out=None,
+                      stream=None):
+    """Same decode as ``pa_decode`` without any workspace: for callers that
+    cannot allocate device memory at decode time (all free HBM already handed
+    to the KV pool, or no room for cudaMalloc's synchronisation in the serving
+    loop). The split-K partials live in a fixed 16 MiB device array inside the
+    library; larger needs are rejected. ``out`` must be given by such callers;
+    when omitted it is allocated here for convenience. Calls that overlap on
+    the GPU share that array and race."""
+    import torch
+
+    lib = load()
+    if out is None:
+        out = torch.empty_like(q)
+    p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
+                           max_context_len, scale, partition_tokens)
+    _check(lib.pa_decode_noalloc(ctypes.byref(p), _stream_handle(stream)), "pa_decode_noalloc")
     return out
 
 

@@ -166,6 +166,37 @@ pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace
   return PA_OK;
 }
 
+pa_status pa_decode_noalloc(const pa_decode_params* p, pa_stream_t stream) {
+  pa_status st = pa::check_decode(p, true);
+  if (st != PA_OK) return st;
+  if (p->num_seqs == 0) return PA_OK;
+  const int np = pa::num_partitions_for(p);
+  size_t om, ol, oa;
+  const size_t need = pa::decode_workspace_layout(p, np, &om, &ol, &oa);
+  if (need > pa::kNoAllocScratchBytes)
+    return pa::set_error(PA_ERR_INVALID_ARG,
+                         "pa_decode_noalloc: these shapes need more split-K scratch than the "
+                         "library's fixed PA_NOALLOC_SCRATCH_BYTES; use pa_decode with a workspace "
+                         "or a larger partition_tokens");
+  pa::DecodeLaunch L;
+  L.p = p;
+  L.partition_tokens = p->partition_tokens == 0 ? pa::kDefaultPartitionTokens : p->partition_tokens;
+  L.num_partitions = np;
+  L.part_m = L.part_l = L.part_acc = nullptr;
+  if (need > 0) {
+    void* scratch = nullptr;
+    const int e = pa::decode_scratch_address(&scratch);
+    if (e != 0) return pa::set_cuda_error("pa_decode_noalloc: scratch lookup", e);
+    unsigned char* ws = static_cast<unsigned char*>(scratch);
+    L.part_m = reinterpret_cast<float*>(ws + om);
+    L.part_l = reinterpret_cast<float*>(ws + ol);
+    L.part_acc = reinterpret_cast<float*>(ws + oa);
+  }
+  const int e = pa::launch_decode(L, stream);
+  if (e != 0) return pa::set_cuda_error("pa_decode_noalloc: launch", e);
+  return PA_OK;
+}
+
 pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,
                                void* v_cache, const int64_t* slot_mapping, int32_t num_tokens,
                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,

@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -456,6 +457,45 @@ int launch_decode(const DecodeLaunch& Lc, void* stream) {
     case 128: return dispatch_group<128>(Lc, s);
     default: return int(cudaErrorInvalidValue);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Decode without any caller-provided workspace.
+//
+// Some callers cannot allocate device memory when they decode: an engine that
+// carved all free HBM into its KV block pool at start-up has nothing left to
+// hand out, and a serving loop that must not stall cannot afford cudaMalloc's
+// implicit synchronisation. For them the split-K partials live in this
+// file-scope device array instead of a workspace. Every GPU that loads the
+// library holds the array until the process exits.
+//
+// Host code cannot pass the array's name to a kernel (on the host it is only
+// a stand-in, not a device address), so its device address is looked up with
+// cudaGetSymbolAddress once per device, with that device current, on the
+// first call made on that device, and cached.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+int decode_scratch_address(void** addr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return int(e);
+  if (dev < 0 || dev >= kMaxDevices) return int(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return int(e);
+    g_scratch_addr[dev] = p;
+  }
+  *addr = g_scratch_addr[dev];
+  return int(cudaSuccess);
 }
 
 int read_and_clear_decode_errors(uint32_t* flags) {

@@ -41,6 +41,11 @@ int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32
 
 // Device error words, one per kernel translation unit: read and clear.
 int read_and_clear_decode_errors(uint32_t* flags);
+
+// Size of the library-owned device scratch used by pa_decode_noalloc.
+constexpr size_t kNoAllocScratchBytes = PA_NOALLOC_SCRATCH_BYTES;
+// Device address of that scratch on the current device (looked up on first use).
+int decode_scratch_address(void** addr);
 int read_and_clear_cache_errors(uint32_t* flags);
 
 }  // namespace pa
