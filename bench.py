@@ -178,7 +178,7 @@ def setup_workload(r: workloads.Recipe, device, n_copies: int):
                 copies=copies)
 
 
-def make_plans(pk, W, device, partition_tokens=0):
+def make_plans(pk, W, device, partition_tokens=0, variant=0):
     import torch
 
     lib = pk.load()
@@ -194,7 +194,7 @@ def make_plans(pk, W, device, partition_tokens=0):
     for kc, vc in W["copies"]:
         p = pk.make_decode_params(W["q"], out, kc, vc, tables_d, lens_d,
                                   max_context_len=int(W["lens"].max()),
-                                  partition_tokens=partition_tokens)
+                                  partition_tokens=partition_tokens, variant=variant)
         need = pk.pa_decode_workspace_size(p)
         if ws is None and need:
             ws = torch.empty(need, dtype=torch.uint8, device=device)
@@ -222,7 +222,7 @@ def run_ours(args, rank: int, world: int) -> dict:
     pk.load()
     r = workloads.llama8b_layer()
     W = setup_workload(r, device, n_copies=3)
-    plans, out, keep = make_plans(pk, W, device)
+    plans, out, keep = make_plans(pk, W, device, variant=args.variant)
     lens = W["lens"]
     dec_b = decode_bytes(lens, r.num_q_heads, r.num_kv_heads, r.head_dim)
     step_b = dec_b + append_bytes(len(W["slots"]), r.num_kv_heads, r.head_dim) + \
@@ -274,7 +274,7 @@ def run_ours(args, rank: int, world: int) -> dict:
 
     # end to end through the public Python API: pinned host inputs -> device,
     # step, result -> pinned host, every step
-    e2e = run_e2e(pk, W, r, device, args.steps, args.warmup, step_b)
+    e2e = run_e2e(pk, W, r, device, args.steps, args.warmup, step_b, args.variant)
 
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -295,7 +295,9 @@ def run_ours(args, rank: int, world: int) -> dict:
             "parallelism": "replicas only" if world > 1 else "single GPU",
         },
         "roofline": {
-            "bound": "hbm", "kernel": "pa_decode (decode kernel + split-K merge)",
+            "bound": "hbm",
+            "kernel": ("pa_decode: " + ("tensor-core" if args.variant == 0 else "CUDA-core")
+                       + " decode kernel + split-K merge"),
             "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
             "peak_source": f"{peaks['source']} hbm_gbs", "avg_launch_ms": round(dec_avg_ms, 5),
@@ -309,7 +311,7 @@ def run_ours(args, rank: int, world: int) -> dict:
     return res
 
 
-def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int) -> dict:
+def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int = 0) -> dict:
     import torch
 
     host = {k: W[k] for k in ("tables", "lens", "slots")}
@@ -338,11 +340,12 @@ def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int) -> dict:
             pk.pa_copy_blocks(kc, vc, dev["cows"])
         pk.pa_reshape_and_cache(dev["kn"], dev["vn"], kc, vc, dev["slots"])
         if "ws" not in ws:
-            p = pk.make_decode_params(dev["q"], out_d, kc, vc, dev["tables"], dev["lens"], max_ctx)
+            p = pk.make_decode_params(dev["q"], out_d, kc, vc, dev["tables"], dev["lens"], max_ctx,
+                                      variant=variant)
             n = pk.pa_decode_workspace_size(p)
             ws["ws"] = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None
         pk.pa_decode(dev["q"], kc, vc, dev["tables"], dev["lens"], max_ctx, out=out_d,
-                     workspace=ws["ws"])
+                     workspace=ws["ws"], variant=variant)
         out_h.copy_(out_d, non_blocking=True)
 
     for i in range(warmup):
@@ -449,6 +452,8 @@ def main(argv=None) -> int:
                     help="untimed loaded seconds before the timed region (clock sampling)")
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", type=int, default=0, choices=[0, 1],
+                    help="decode kernel: 0 tensor-core (default), 1 CUDA-core")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

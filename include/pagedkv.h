@@ -128,16 +128,23 @@ typedef struct {
   float scale;                 /* softmax scale, normally 1/sqrt(head_dim) */
   int32_t partition_tokens;    /* split-K partition length; 0 = 512; else a multiple of
                                   block_size in [block_size, 4096] */
+  int32_t variant;             /* PA_DECODE_TENSOR_CORE (default) or PA_DECODE_CUDA_CORE */
 } pa_decode_params;
 
-/* Bytes of device workspace pa_decode needs for these parameters (0 when no
- * sequence can span more than one partition). Returns 0 for invalid params. */
+/* Decode kernel variants; both compute the same function. */
+#define PA_DECODE_TENSOR_CORE 0 /* tcgen05 MMAs, TMEM accumulators, tensor-map TMA ring */
+#define PA_DECODE_CUDA_CORE 1   /* fp32 FMAs on CUDA cores, 1-D bulk-copy rings */
+
+/* Bytes of device workspace pa_decode needs for these parameters: a 256-byte
+ * header (the tensor-core kernel's work counter) plus the split-K partials
+ * when a sequence can span more than one partition. Returns 0 for invalid
+ * params. */
 size_t pa_decode_workspace_size(const pa_decode_params* p);
 
 /* Enqueue the decode. `workspace` is caller-owned device memory of at least
- * pa_decode_workspace_size(p) bytes (may be NULL when that size is 0); it
- * holds split-K partials and is fully rewritten by every call, so two calls
- * in flight at once must not share it. */
+ * pa_decode_workspace_size(p) bytes, 256-byte aligned. Every call clears the
+ * header and rewrites the partials before reading them, so its contents on
+ * entry do not matter; two calls in flight at once must not share it. */
 pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace_bytes,
                     pa_stream_t stream);
 

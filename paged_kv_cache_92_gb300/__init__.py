@@ -61,7 +61,12 @@ class DecodeParams(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("num_blocks", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
         ("scale", ctypes.c_float), ("partition_tokens", ctypes.c_int32),
+        ("variant", ctypes.c_int32),
     ]
+
+
+DECODE_TENSOR_CORE = 0
+DECODE_CUDA_CORE = 1
 
 
 class PoolStats(ctypes.Structure):
@@ -155,7 +160,7 @@ def _stream_handle(stream) -> Optional[int]:
 
 def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
                        max_context_len: int, scale: Optional[float] = None,
-                       partition_tokens: int = 0) -> DecodeParams:
+                       partition_tokens: int = 0, variant: int = DECODE_TENSOR_CORE) -> DecodeParams:
     import torch
 
     B, Hq, D = q.shape
@@ -177,6 +182,7 @@ def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
     p.max_context_len = int(max_context_len)
     p.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
     p.partition_tokens = int(partition_tokens)
+    p.variant = int(variant)
     return p
 
 
@@ -186,7 +192,7 @@ def pa_decode_workspace_size(params: DecodeParams) -> int:
 
 def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
               scale: Optional[float] = None, partition_tokens: int = 0, out=None,
-              workspace=None, stream=None):
+              workspace=None, stream=None, variant: int = DECODE_TENSOR_CORE):
     """Paged decode attention; returns ``out`` (bf16 [B][Hq][d]).
 
     ``workspace`` is a uint8 CUDA tensor of at least
@@ -198,7 +204,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
     if out is None:
         out = torch.empty_like(q)
     p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
-                           max_context_len, scale, partition_tokens)
+                           max_context_len, scale, partition_tokens, variant)
     need = int(lib.pa_decode_workspace_size(ctypes.byref(p)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -210,7 +216,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
 
 def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
                       scale: Optional[float] = None, partition_tokens: int = 0, out=None,
-                      stream=None):
+                      stream=None, variant: int = DECODE_TENSOR_CORE):
     """Same decode as ``pa_decode`` without any workspace: for callers that
     cannot allocate device memory at decode time (all free HBM already handed
     to the KV pool, or no room for cudaMalloc's synchronisation in the serving
@@ -224,7 +230,7 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_conte
     if out is None:
         out = torch.empty_like(q)
     p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
-                           max_context_len, scale, partition_tokens)
+                           max_context_len, scale, partition_tokens, variant)
     _check(lib.pa_decode_noalloc(ctypes.byref(p), _stream_handle(stream)), "pa_decode_noalloc")
     return out
 

@@ -50,6 +50,11 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
   if (pt < kBlockSize || pt > kMaxPartitionTokens || pt % kBlockSize != 0)
     return set_error(PA_ERR_INVALID_ARG,
                      "pa_decode: partition_tokens must be 0 or a multiple of 16 in [16, 4096]");
+  if (p->variant != PA_DECODE_TENSOR_CORE && p->variant != PA_DECODE_CUDA_CORE)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: variant must be 0 (tensor core) or 1 (CUDA core)");
+  if (int64_t(p->num_blocks) * p->num_kv_heads * kBlockSize >= (int64_t(1) << 31) - 16 ||
+      int64_t(p->num_seqs) * p->num_q_heads >= (int64_t(1) << 31) - 16)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: cache or query rows exceed 2^31");
   if (!(p->scale > 0.0f) || p->scale != p->scale)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: scale must be a positive finite number");
   if (need_pointers && p->num_seqs > 0) {
@@ -87,15 +92,47 @@ pa_status set_cuda_error(const char* where, int err) {
 
 size_t decode_workspace_layout(const pa_decode_params* p, int num_partitions, size_t* off_m,
                                size_t* off_l, size_t* off_acc) {
+  // [0, 256): work counter of the tensor-core kernel; then split-K partials.
   if (num_partitions <= 1) {
-    *off_m = *off_l = *off_acc = 0;
-    return 0;
+    *off_m = *off_l = *off_acc = kWorkspaceHeaderBytes;
+    return kWorkspaceHeaderBytes;
   }
   const size_t rows = size_t(p->num_seqs) * p->num_q_heads * num_partitions;
-  *off_m = 0;
-  *off_l = round_up(rows * sizeof(float), 256);
+  *off_m = kWorkspaceHeaderBytes;
+  *off_l = *off_m + round_up(rows * sizeof(float), 256);
   *off_acc = *off_l + round_up(rows * sizeof(float), 256);
   return *off_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+}
+
+// Clear the work counter, launch the selected decode kernel, then the merge.
+static pa_status run_decode(const pa_decode_params* p, unsigned char* ws, int np, size_t om,
+                            size_t ol, size_t oa, pa_stream_t stream, const char* who) {
+  DecodeLaunch L;
+  L.p = p;
+  L.partition_tokens = resolve_partition_tokens(p);
+  L.num_partitions = np;
+  L.counters = reinterpret_cast<unsigned int*>(ws);
+  L.part_m = np > 1 ? reinterpret_cast<float*>(ws + om) : nullptr;
+  L.part_l = np > 1 ? reinterpret_cast<float*>(ws + ol) : nullptr;
+  L.part_acc = np > 1 ? reinterpret_cast<float*>(ws + oa) : nullptr;
+  char where[96];
+  int e = 0;
+  if (p->variant == PA_DECODE_TENSOR_CORE) {
+    e = int(cudaMemsetAsync(ws, 0, 16, stream));
+    if (e) {
+      std::snprintf(where, sizeof(where), "%s: clear work counter", who);
+      return set_cuda_error(where, e);
+    }
+    e = launch_decode_tc(L, stream);
+  } else {
+    e = launch_decode(L, stream);
+  }
+  if (!e) e = launch_merge(L, stream);
+  if (e) {
+    std::snprintf(where, sizeof(where), "%s: launch", who);
+    return set_cuda_error(where, e);
+  }
+  return PA_OK;
 }
 
 }  // namespace pa
@@ -123,12 +160,12 @@ pa_status pa_device_errors(pa_stream_t stream, uint32_t* flags) {
   if (!flags) return pa::set_error(PA_ERR_INVALID_ARG, "pa_device_errors: flags is NULL");
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return pa::set_cuda_error("pa_device_errors: stream sync", int(e));
-  uint32_t a = 0, b = 0;
+  uint32_t a = 0, b = 0, c = 0;
   int r = pa::read_and_clear_decode_errors(&a);
+  if (r == 0) r = pa::read_and_clear_decode_tc_errors(&c);
+  if (r == 0) r = pa::read_and_clear_cache_errors(&b);
   if (r != 0) return pa::set_cuda_error("pa_device_errors: read", r);
-  r = pa::read_and_clear_cache_errors(&b);
-  if (r != 0) return pa::set_cuda_error("pa_device_errors: read", r);
-  *flags = a | b;
+  *flags = a | b | c;
   return PA_OK;
 }
 
@@ -146,24 +183,13 @@ pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace
   const int np = pa::num_partitions_for(p);
   size_t om, ol, oa;
   const size_t need = pa::decode_workspace_layout(p, np, &om, &ol, &oa);
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need)
-      return pa::set_error(PA_ERR_INVALID_ARG,
-                           "pa_decode: workspace smaller than pa_decode_workspace_size()");
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-      return pa::set_error(PA_ERR_INVALID_ARG, "pa_decode: workspace must be 256-byte aligned");
-  }
-  pa::DecodeLaunch L;
-  L.p = p;
-  L.partition_tokens = p->partition_tokens == 0 ? pa::kDefaultPartitionTokens : p->partition_tokens;
-  L.num_partitions = np;
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  L.part_m = need ? reinterpret_cast<float*>(ws + om) : nullptr;
-  L.part_l = need ? reinterpret_cast<float*>(ws + ol) : nullptr;
-  L.part_acc = need ? reinterpret_cast<float*>(ws + oa) : nullptr;
-  const int e = pa::launch_decode(L, stream);
-  if (e != 0) return pa::set_cuda_error("pa_decode: launch", e);
-  return PA_OK;
+  if (!workspace || workspace_bytes < need)
+    return pa::set_error(PA_ERR_INVALID_ARG,
+                         "pa_decode: workspace smaller than pa_decode_workspace_size()");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_decode: workspace must be 256-byte aligned");
+  return pa::run_decode(p, static_cast<unsigned char*>(workspace), np, om, ol, oa, stream,
+                        "pa_decode");
 }
 
 pa_status pa_decode_noalloc(const pa_decode_params* p, pa_stream_t stream) {
@@ -178,23 +204,13 @@ pa_status pa_decode_noalloc(const pa_decode_params* p, pa_stream_t stream) {
                          "pa_decode_noalloc: these shapes need more split-K scratch than the "
                          "library's fixed PA_NOALLOC_SCRATCH_BYTES; use pa_decode with a workspace "
                          "or a larger partition_tokens");
-  pa::DecodeLaunch L;
-  L.p = p;
-  L.partition_tokens = p->partition_tokens == 0 ? pa::kDefaultPartitionTokens : p->partition_tokens;
-  L.num_partitions = np;
-  L.part_m = L.part_l = L.part_acc = nullptr;
-  if (need > 0) {
-    void* scratch = nullptr;
-    const int e = pa::decode_scratch_address(&scratch);
-    if (e != 0) return pa::set_cuda_error("pa_decode_noalloc: scratch lookup", e);
-    unsigned char* ws = static_cast<unsigned char*>(scratch);
-    L.part_m = reinterpret_cast<float*>(ws + om);
-    L.part_l = reinterpret_cast<float*>(ws + ol);
-    L.part_acc = reinterpret_cast<float*>(ws + oa);
-  }
-  const int e = pa::launch_decode(L, stream);
-  if (e != 0) return pa::set_cuda_error("pa_decode_noalloc: launch", e);
-  return PA_OK;
+  void* scratch = nullptr;
+  const int e = pa::decode_scratch_address(&scratch);
+  if (e != 0) return pa::set_cuda_error("pa_decode_noalloc: scratch lookup", e);
+  // run_decode clears the work counter at the head of the shared array before
+  // every launch; the partials are fully rewritten before they are read.
+  return pa::run_decode(p, static_cast<unsigned char*>(scratch), np, om, ol, oa, stream,
+                        "pa_decode_noalloc");
 }
 
 pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,

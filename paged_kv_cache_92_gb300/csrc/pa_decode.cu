@@ -424,17 +424,18 @@ int launch_decode_t(const DecodeLaunch& Lc, cudaStream_t stream) {
       p->block_tables, p->context_lens, p->max_blocks_per_seq, p->num_kv_heads, p->num_blocks,
       p->max_context_len, scale_log2, Lc.partition_tokens, Lc.num_partitions, Lc.part_m, Lc.part_l,
       Lc.part_acc);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return int(e);
-  if (Lc.num_partitions > 1) {
-    dim3 mgrid((p->num_q_heads + 3) / 4, p->num_seqs);
-    merge_partitions_kernel<D><<<mgrid, 128, 0, stream>>>(
-        static_cast<__nv_bfloat16*>(p->out), Lc.part_m, Lc.part_l, Lc.part_acc, p->context_lens,
-        p->num_q_heads, p->max_blocks_per_seq, p->max_context_len, Lc.partition_tokens,
-        Lc.num_partitions);
-    e = cudaGetLastError();
-  }
-  return int(e);
+  return int(cudaGetLastError());
+}
+
+template <int D>
+int launch_merge_t(const DecodeLaunch& Lc, cudaStream_t stream) {
+  const pa_decode_params* p = Lc.p;
+  dim3 mgrid((p->num_q_heads + 3) / 4, p->num_seqs);
+  merge_partitions_kernel<D><<<mgrid, 128, 0, stream>>>(
+      static_cast<__nv_bfloat16*>(p->out), Lc.part_m, Lc.part_l, Lc.part_acc, p->context_lens,
+      p->num_q_heads, p->max_blocks_per_seq, p->max_context_len, Lc.partition_tokens,
+      Lc.num_partitions);
+  return int(cudaGetLastError());
 }
 
 template <int D>
@@ -496,6 +497,16 @@ int decode_scratch_address(void** addr) {
   }
   *addr = g_scratch_addr[dev];
   return int(cudaSuccess);
+}
+
+int launch_merge(const DecodeLaunch& Lc, void* stream) {
+  if (Lc.num_partitions <= 1) return int(cudaSuccess);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (Lc.p->head_dim) {
+    case 64: return launch_merge_t<64>(Lc, s);
+    case 128: return launch_merge_t<128>(Lc, s);
+    default: return int(cudaErrorInvalidValue);
+  }
 }
 
 int read_and_clear_decode_errors(uint32_t* flags) {

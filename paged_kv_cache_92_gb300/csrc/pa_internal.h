@@ -25,14 +25,20 @@ struct DecodeLaunch {
   float* part_m;       // [num_seqs][num_q_heads][num_partitions]
   float* part_l;       // same
   float* part_acc;     // [num_seqs][num_q_heads][num_partitions][head_dim]
+  unsigned int* counters;  // work counter of the tensor-core kernel (zero at launch)
 };
 
-// Workspace carve-up for split-K partials. Returns total bytes.
+// Bytes at the start of every decode workspace holding the work counter.
+constexpr size_t kWorkspaceHeaderBytes = 256;
+
+// Workspace carve-up: counter header, then split-K partials. Returns total bytes.
 size_t decode_workspace_layout(const pa_decode_params* p, int num_partitions, size_t* off_m,
                                size_t* off_l, size_t* off_acc);
 
 // Kernel launchers (pa_decode.cu / pa_cache.cu). Return a cudaError_t as int.
-int launch_decode(const DecodeLaunch& L, void* stream);
+int launch_decode(const DecodeLaunch& L, void* stream);      // CUDA-core decode kernel
+int launch_decode_tc(const DecodeLaunch& L, void* stream);   // tensor-core decode kernel
+int launch_merge(const DecodeLaunch& L, void* stream);       // split-K merge (if needed)
 int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
                              int32_t head_dim, int32_t num_blocks, void* stream);
@@ -41,6 +47,7 @@ int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32
 
 // Device error words, one per kernel translation unit: read and clear.
 int read_and_clear_decode_errors(uint32_t* flags);
+int read_and_clear_decode_tc_errors(uint32_t* flags);
 
 // Size of the library-owned device scratch used by pa_decode_noalloc.
 constexpr size_t kNoAllocScratchBytes = PA_NOALLOC_SCRATCH_BYTES;

@@ -58,7 +58,7 @@ def build_case(r: workloads.Recipe, device: str = "cuda") -> Case:
                 slm, cwm, q, kn, vn, kc, vc)
 
 
-def run_step_gpu(case: Case, partition_tokens: int = 0):
+def run_step_gpu(case: Case, partition_tokens: int = 0, variant: int = 0):
     """The hot path on the GPU: copy_blocks -> reshape_and_cache -> decode."""
     import torch
 
@@ -71,7 +71,7 @@ def run_step_gpu(case: Case, partition_tokens: int = 0):
     pk.pa_reshape_and_cache(case.k_new, case.v_new, kc, vc, torch.from_numpy(case.slots).to(dev))
     out = pk.pa_decode(case.q, kc, vc, torch.from_numpy(case.tables).to(dev),
                        torch.from_numpy(case.lens).to(dev), max_context_len=int(case.lens.max()),
-                       partition_tokens=partition_tokens)
+                       partition_tokens=partition_tokens, variant=variant)
     torch.cuda.synchronize()
     return out, kc, vc
 

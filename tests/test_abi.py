@@ -69,6 +69,8 @@ def _params(pk, **kw):
     (dict(partition_tokens=8192), 1),
     (dict(scale=0.0), 1),
     (dict(num_seqs=70000), 1),
+    (dict(variant=2), 1),
+    (dict(num_blocks=1 << 24, num_kv_heads=8), 1),  # cache rows past 2^31
     (dict(), 1),  # valid shapes, NULL pointers
 ])
 def test_decode_rejects_bad_arguments_on_the_host(pk, kw, status):
@@ -80,11 +82,11 @@ def test_decode_rejects_bad_arguments_on_the_host(pk, kw, status):
 
 def test_decode_workspace_size(pk):
     lib = pk.load()
-    # max context 64 <= one 512-token partition: no workspace
-    assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk))) == 0
+    # max context 64 <= one 512-token partition: only the 256-byte counter header
+    assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk))) == 256
     p = _params(pk, max_context_len=2048, max_blocks_per_seq=128)
     rows = 2 * 8 * 4  # seqs * q heads * partitions
-    want = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256
+    want = 256 + 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == want
     assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk, head_dim=96))) == 0
 

@@ -17,6 +17,8 @@ from tests import harness
 
 pytestmark = pytest.mark.gpu
 
+VARIANTS = pytest.mark.parametrize("variant", [0, 1], ids=["tensor_core", "cuda_core"])
+
 
 @pytest.fixture(scope="module")
 def pk():
@@ -38,7 +40,8 @@ def _check_errors(pk):
 
 # ---------------------------------------------------------------- the five workloads
 
-def test_tiny_workload_full(pk):
+@VARIANTS
+def test_tiny_workload_full(pk, variant):
     """4 sequences {1,5,17,33}, 4/1 heads, d=64: decode, append, decode again."""
     import torch
 
@@ -47,13 +50,13 @@ def test_tiny_workload_full(pk):
     # decode before the append, over the pre-step lengths
     kc, vc = case.k_cache, case.v_cache
     out0 = pk.pa_decode(case.q, kc, vc, torch.from_numpy(case.tables0).cuda(),
-                        torch.from_numpy(case.lens0).cuda(), max_context_len=33)
+                        torch.from_numpy(case.lens0).cuda(), max_context_len=33, variant=variant)
     ref0 = oracle.paged_decode(case.q.cpu(), kc.cpu(), vc.cpu(), case.tables0, case.lens0)
     harness.assert_close(harness.bf16_tensor_to_f64(out0), ref0)
     # the step: append one token per sequence (no boundary crossed), decode over {2,6,18,34}
     assert case.cows.shape[0] == 0
     assert list(case.lens) == [2, 6, 18, 34]
-    out, kg, vg = harness.run_step_gpu(case)
+    out, kg, vg = harness.run_step_gpu(case, variant=variant)
     ref, ko, vo = harness.run_step_oracle(case)
     assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
     assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
@@ -61,9 +64,10 @@ def test_tiny_workload_full(pk):
     _check_errors(pk)
 
 
-def test_llama8b_layer_full(pk):
+@VARIANTS
+def test_llama8b_layer_full(pk, variant):
     case = harness.build_case(workloads.llama8b_layer())
-    out, kg, vg = harness.run_step_gpu(case)
+    out, kg, vg = harness.run_step_gpu(case, variant=variant)
     ref, ko, vo = harness.run_step_oracle(case)
     assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
     assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
@@ -71,13 +75,14 @@ def test_llama8b_layer_full(pk):
     _check_errors(pk)
 
 
-def test_llama8b_high_concurrency_full(pk):
+@VARIANTS
+def test_llama8b_high_concurrency_full(pk, variant):
     r = workloads.llama8b_high_concurrency()
     case = harness.build_case(r)
     # new blocks were allocated exactly for the sequences sitting on a boundary
     grew = (case.tables >= 0).sum(1) - (case.tables0 >= 0).sum(1)
     assert np.array_equal(grew, (r.lens0 % 16 == 0).astype(int))
-    out, kg, vg = harness.run_step_gpu(case)
+    out, kg, vg = harness.run_step_gpu(case, variant=variant)
     ref, ko, vo = harness.run_step_oracle(case)
     assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
     assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
@@ -85,12 +90,13 @@ def test_llama8b_high_concurrency_full(pk):
     _check_errors(pk)
 
 
+@VARIANTS
 @pytest.mark.parametrize("batch", [8, 32])
-def test_llama70b_long_context(pk, batch):
+def test_llama70b_long_context(pk, batch, variant):
     """64/8 heads, L ~ U[8192, 32768]: split-K over 512-token partitions + merge."""
     r = workloads.llama70b_long(batch=batch)
     case = harness.build_case(r)
-    out, kg, vg = harness.run_step_gpu(case)
+    out, kg, vg = harness.run_step_gpu(case, variant=variant)
     B, Hq = r.num_seqs, r.num_q_heads
     if batch == 8:
         units = None
@@ -108,12 +114,13 @@ def test_llama70b_long_context(pk, batch):
     _check_errors(pk)
 
 
-def test_shared_prefix_copy_on_write(pk):
+@VARIANTS
+def test_shared_prefix_copy_on_write(pk, variant):
     r = workloads.shared_prefix()
     case = harness.build_case(r)
     assert case.cows.shape == (32, 2)
     assert len(set(case.cows[:, 0].tolist())) == 1  # all copies come from the last shared block
-    out, kg, vg = harness.run_step_gpu(case)
+    out, kg, vg = harness.run_step_gpu(case, variant=variant)
     ref, ko, vo = harness.run_step_oracle(case)
     assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
     assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
@@ -145,26 +152,29 @@ def _direct_case(lens, Hq, Hkv, D, seed, extra_blocks=3, reverse=False, identity
     return q, kc, vc, tables, lens.astype(np.int32), torch
 
 
+@VARIANTS
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-@pytest.mark.parametrize("partition", [0, 16, 64, 4096])
-def test_edge_lengths(pk, D, G, partition):
+@pytest.mark.parametrize("partition", [0, 16, 80, 4096])
+def test_edge_lengths(pk, D, G, partition, variant):
     lens = [1, 15, 16, 17, 511, 512, 513, 1024, 1025, 4097]
     Hkv = 2
     q, kc, vc, tables, lens, torch = _direct_case(lens, G * Hkv, Hkv, D, seed=D * 10 + G)
     out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
-                       max_context_len=int(lens.max()), partition_tokens=partition)
+                       max_context_len=int(lens.max()), partition_tokens=partition,
+                       variant=variant)
     torch.cuda.synchronize()
     ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
     harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
     _check_errors(pk)
 
 
+@VARIANTS
 @pytest.mark.parametrize("partition", [0, 16])
-def test_length_one_returns_v0_bit_exact(pk, partition):
+def test_length_one_returns_v0_bit_exact(pk, partition, variant):
     q, kc, vc, tables, lens, torch = _direct_case([1] * 6, 8, 2, 128, seed=5)
     out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
-                       max_context_len=1, partition_tokens=partition)
+                       max_context_len=1, partition_tokens=partition, variant=variant)
     torch.cuda.synchronize()
     vh = vc.cpu()
     for b in range(6):
@@ -172,7 +182,8 @@ def test_length_one_returns_v0_bit_exact(pk, partition):
             assert torch.equal(out[b, h].cpu(), vh[tables[b, 0], h // 4, 0])
 
 
-def test_physical_placement_does_not_change_a_bit(pk):
+@VARIANTS
+def test_physical_placement_does_not_change_a_bit(pk, variant):
     lens = [37, 300, 1, 900, 16, 513]
     outs = []
     for kind in ("random", "reverse", "identity"):
@@ -189,28 +200,33 @@ def test_physical_placement_does_not_change_a_bit(pk):
         vc2[torch.from_numpy(tables[tables >= 0]).long().cuda()] = \
             base_vc[torch.from_numpy(base_tables[base_tables >= 0]).long().cuda()]
         out = pk.pa_decode(base_q, kc2, vc2, torch.from_numpy(tables).cuda(),
-                           torch.from_numpy(lens_a).cuda(), max_context_len=900)
+                           torch.from_numpy(lens_a).cuda(), max_context_len=900, variant=variant)
         outs.append(out.cpu())
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
-def test_split_and_unsplit_agree(pk):
+@VARIANTS
+def test_split_and_unsplit_agree(pk, variant):
     q, kc, vc, tables, lens, torch = _direct_case([700, 2049, 3000], 32, 8, 128, seed=9)
     bt, cl = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
-    a = pk.pa_decode(q, kc, vc, bt, cl, max_context_len=3000, partition_tokens=4096)
-    b = pk.pa_decode(q, kc, vc, bt, cl, max_context_len=3000, partition_tokens=128)
+    a = pk.pa_decode(q, kc, vc, bt, cl, max_context_len=3000, partition_tokens=4096,
+                     variant=variant)
+    b = pk.pa_decode(q, kc, vc, bt, cl, max_context_len=3000, partition_tokens=128,
+                     variant=variant)
     torch.cuda.synchronize()
     ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
     harness.assert_close(harness.bf16_tensor_to_f64(a), ref)
     harness.assert_close(harness.bf16_tensor_to_f64(b), ref)
 
 
-def test_zero_length_rows_are_zero(pk):
+@VARIANTS
+def test_zero_length_rows_are_zero(pk, variant):
     q, kc, vc, tables, lens, torch = _direct_case([5, 20, 3], 8, 2, 128, seed=11)
     lens2 = lens.copy()
     lens2[1] = 0
-    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens2).cuda(),
-                       max_context_len=20)
+    out = torch.full_like(q, 7.0)
+    pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens2).cuda(),
+                 max_context_len=20, out=out, variant=variant)
     torch.cuda.synchronize()
     assert torch.count_nonzero(out[1]).item() == 0
     ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
@@ -268,7 +284,8 @@ def test_copy_blocks_bit_exact_and_untouched_blocks(pk):
 
 # ---------------------------------------------------------------- device-side range checks
 
-def test_bad_device_values_set_error_bits_without_faulting(pk):
+@VARIANTS
+def test_bad_device_values_set_error_bits_without_faulting(pk, variant):
     import torch
 
     q, kc, vc, tables, lens, _ = _direct_case([40, 7], 8, 2, 128, seed=13)
@@ -276,12 +293,12 @@ def test_bad_device_values_set_error_bits_without_faulting(pk):
     bad = tables.copy()
     bad[0, 1] = kc.shape[0] + 1000  # past the pool
     pk.pa_decode(q, kc, vc, torch.from_numpy(bad).cuda(), torch.from_numpy(lens).cuda(),
-                 max_context_len=40)
+                 max_context_len=40, variant=variant)
     assert pk.pa_device_errors() & pk.DEVERR_TABLE_ENTRY
     long = lens.copy()
     long[1] = 41  # above the host-promised maximum
     pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(long).cuda(),
-                 max_context_len=40)
+                 max_context_len=40, variant=variant)
     assert pk.pa_device_errors() & pk.DEVERR_CONTEXT_LEN
     kn = workloads.bf16_normal((1, 2, 128), 1, "cuda")
     pk.pa_reshape_and_cache(kn, kn, kc.clone(), vc.clone(),
@@ -292,17 +309,18 @@ def test_bad_device_values_set_error_bits_without_faulting(pk):
     assert pk.pa_device_errors() & pk.DEVERR_COPY_PAIR
     # the context is still healthy
     out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
-                       max_context_len=40)
+                       max_context_len=40, variant=variant)
     torch.cuda.synchronize()
     ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
     harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
     assert pk.pa_device_errors() == 0
 
 
-def test_scale_is_applied(pk):
+@VARIANTS
+def test_scale_is_applied(pk, variant):
     q, kc, vc, tables, lens, torch = _direct_case([33, 70], 8, 2, 64, seed=17)
     out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
-                       max_context_len=70, scale=0.3)
+                       max_context_len=70, scale=0.3, variant=variant)
     torch.cuda.synchronize()
     ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens, scale=0.3)
     harness.assert_close(harness.bf16_tensor_to_f64(out), ref)

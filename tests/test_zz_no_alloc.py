@@ -56,7 +56,7 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row(pk):
     for q, kc, vc, bt, cl, mx, tables, lens in cases:
         ref_out = pk.pa_decode(q, kc, vc, bt, cl, max_context_len=mx)
         p = pk.make_decode_params(q, torch.empty_like(q), kc, vc, bt, cl, max_context_len=mx)
-        assert pk.pa_decode_workspace_size(p) > 0  # this case does use split-K scratch
+        assert pk.pa_decode_workspace_size(p) > 256  # split-K partials beyond the counter header
         out = torch.empty_like(q)
         p = pk.make_decode_params(q, out, kc, vc, bt, cl, max_context_len=mx)
         stream = torch.cuda.current_stream().cuda_stream or None
