@@ -131,20 +131,24 @@ typedef struct {
   int32_t variant;             /* PA_DECODE_TENSOR_CORE (default) or PA_DECODE_CUDA_CORE */
 } pa_decode_params;
 
-/* Decode kernel variants; both compute the same function. */
+/* Decode kernel variants; both compute the same function. The tensor-core
+ * kernel handles num_kv_heads in {1, 2, 4, 8}, num_q_heads <= 64 and up to
+ * 16384 sequences per call; other shapes run on the CUDA-core kernel
+ * whatever `variant` says. */
 #define PA_DECODE_TENSOR_CORE 0 /* tcgen05 MMAs, TMEM accumulators, tensor-map TMA ring */
 #define PA_DECODE_CUDA_CORE 1   /* fp32 FMAs on CUDA cores, 1-D bulk-copy rings */
 
-/* Bytes of device workspace pa_decode needs for these parameters: a 256-byte
- * header (the tensor-core kernel's work counter) plus the split-K partials
- * when a sequence can span more than one partition. Returns 0 for invalid
+/* Bytes of device workspace pa_decode needs for these parameters on the
+ * current device: a 256-byte header, then the larger of the two kernels'
+ * needs -- the CUDA-core kernel's per-partition partials, or the tensor-core
+ * kernel's work plan and per-(sequence, SM) partials. Returns 0 for invalid
  * params. */
 size_t pa_decode_workspace_size(const pa_decode_params* p);
 
 /* Enqueue the decode. `workspace` is caller-owned device memory of at least
- * pa_decode_workspace_size(p) bytes, 256-byte aligned. Every call clears the
- * header and rewrites the partials before reading them, so its contents on
- * entry do not matter; two calls in flight at once must not share it. */
+ * pa_decode_workspace_size(p) bytes, 256-byte aligned. Every call writes what
+ * it later reads there, so its contents on entry do not matter; two calls in
+ * flight at once must not share it. */
 pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace_bytes,
                     pa_stream_t stream);
 
@@ -158,9 +162,8 @@ pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace
  * The split-K partials go to a fixed device array inside the library
  * (PA_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library until
  * the process exits). Nothing is allocated or freed by the call.
- *  - Shapes whose partials need more than that (num_seqs * num_q_heads *
- *    partitions * (head_dim + 2) * 4 bytes, each of the three parts rounded up
- *    to 256 bytes) are rejected with PA_ERR_INVALID_ARG.
+ *  - Shapes whose workspace (pa_decode_workspace_size) exceeds that are
+ *    rejected with PA_ERR_INVALID_ARG.
  *  - The first call on a device looks up the array's device address with that
  *    device current; make that first call before any stream capture.
  *  - Every call on a device shares the one array and leaves its partials in

@@ -90,44 +90,56 @@ pa_status set_cuda_error(const char* where, int err) {
   return PA_ERR_CUDA;
 }
 
-size_t decode_workspace_layout(const pa_decode_params* p, int num_partitions, size_t* off_m,
-                               size_t* off_l, size_t* off_acc) {
-  // [0, 256): work counter of the tensor-core kernel; then split-K partials.
-  if (num_partitions <= 1) {
-    *off_m = *off_l = *off_acc = kWorkspaceHeaderBytes;
-    return kWorkspaceHeaderBytes;
+WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_partitions,
+                                        int grid) {
+  WorkspaceLayout w{};
+  const size_t H = kWorkspaceHeaderBytes;
+  // CUDA-core kernel: per-partition partials (only when a sequence can split)
+  size_t simt_end = H;
+  if (num_partitions > 1) {
+    const size_t rows = size_t(p->num_seqs) * p->num_q_heads * num_partitions;
+    w.simt_m = H;
+    w.simt_l = w.simt_m + round_up(rows * sizeof(float), 256);
+    w.simt_acc = w.simt_l + round_up(rows * sizeof(float), 256);
+    simt_end = w.simt_acc + round_up(rows * p->head_dim * sizeof(float), 256);
   }
-  const size_t rows = size_t(p->num_seqs) * p->num_q_heads * num_partitions;
-  *off_m = kWorkspaceHeaderBytes;
-  *off_l = *off_m + round_up(rows * sizeof(float), 256);
-  *off_acc = *off_l + round_up(rows * sizeof(float), 256);
-  return *off_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+  // tensor-core kernel: stream-K plan, then one partial per (sequence, CTA) segment
+  const size_t segs = size_t(p->num_seqs) + size_t(grid > 0 ? grid : 256);
+  const size_t rows = segs * p->num_q_heads;
+  w.tc_plan = H;
+  w.tc_m = w.tc_plan + round_up((size_t(p->num_seqs) + 2) * sizeof(int), 256);
+  w.tc_l = w.tc_m + round_up(rows * sizeof(float), 256);
+  w.tc_acc = w.tc_l + round_up(rows * sizeof(float), 256);
+  const size_t tc_end = w.tc_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+  w.total = simt_end > tc_end ? simt_end : tc_end;
+  return w;
 }
 
-// Clear the work counter, launch the selected decode kernel, then the merge.
-static pa_status run_decode(const pa_decode_params* p, unsigned char* ws, int np, size_t om,
-                            size_t ol, size_t oa, pa_stream_t stream, const char* who) {
+// Launch the selected decode kernel and its merge.
+static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
+                            const WorkspaceLayout& w, int np, int grid, pa_stream_t stream,
+                            const char* who) {
   DecodeLaunch L;
   L.p = p;
   L.partition_tokens = resolve_partition_tokens(p);
   L.num_partitions = np;
-  L.counters = reinterpret_cast<unsigned int*>(ws);
-  L.part_m = np > 1 ? reinterpret_cast<float*>(ws + om) : nullptr;
-  L.part_l = np > 1 ? reinterpret_cast<float*>(ws + ol) : nullptr;
-  L.part_acc = np > 1 ? reinterpret_cast<float*>(ws + oa) : nullptr;
+  L.grid = grid;
   char where[96];
   int e = 0;
-  if (p->variant == PA_DECODE_TENSOR_CORE) {
-    e = int(cudaMemsetAsync(ws, 0, 16, stream));
-    if (e) {
-      std::snprintf(where, sizeof(where), "%s: clear work counter", who);
-      return set_cuda_error(where, e);
-    }
+  if (p->variant == PA_DECODE_TENSOR_CORE && tc_supports(p) && grid > 0) {
+    L.plan = reinterpret_cast<int*>(ws + w.tc_plan);
+    L.part_m = reinterpret_cast<float*>(ws + w.tc_m);
+    L.part_l = reinterpret_cast<float*>(ws + w.tc_l);
+    L.part_acc = reinterpret_cast<float*>(ws + w.tc_acc);
     e = launch_decode_tc(L, stream);
   } else {
+    L.plan = nullptr;
+    L.part_m = np > 1 ? reinterpret_cast<float*>(ws + w.simt_m) : nullptr;
+    L.part_l = np > 1 ? reinterpret_cast<float*>(ws + w.simt_l) : nullptr;
+    L.part_acc = np > 1 ? reinterpret_cast<float*>(ws + w.simt_acc) : nullptr;
     e = launch_decode(L, stream);
+    if (!e) e = launch_merge(L, stream);
   }
-  if (!e) e = launch_merge(L, stream);
   if (e) {
     std::snprintf(where, sizeof(where), "%s: launch", who);
     return set_cuda_error(where, e);
@@ -171,8 +183,7 @@ pa_status pa_device_errors(pa_stream_t stream, uint32_t* flags) {
 
 size_t pa_decode_workspace_size(const pa_decode_params* p) {
   if (pa::check_decode(p, false) != PA_OK) return 0;
-  size_t a, b, c;
-  return pa::decode_workspace_layout(p, pa::num_partitions_for(p), &a, &b, &c);
+  return pa::decode_workspace_layout(p, pa::num_partitions_for(p), pa::tc_grid()).total;
 }
 
 pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace_bytes,
@@ -181,14 +192,14 @@ pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace
   if (st != PA_OK) return st;
   if (p->num_seqs == 0) return PA_OK;
   const int np = pa::num_partitions_for(p);
-  size_t om, ol, oa;
-  const size_t need = pa::decode_workspace_layout(p, np, &om, &ol, &oa);
-  if (!workspace || workspace_bytes < need)
+  const int grid = pa::tc_grid();
+  const pa::WorkspaceLayout w = pa::decode_workspace_layout(p, np, grid);
+  if (!workspace || workspace_bytes < w.total)
     return pa::set_error(PA_ERR_INVALID_ARG,
                          "pa_decode: workspace smaller than pa_decode_workspace_size()");
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return pa::set_error(PA_ERR_INVALID_ARG, "pa_decode: workspace must be 256-byte aligned");
-  return pa::run_decode(p, static_cast<unsigned char*>(workspace), np, om, ol, oa, stream,
+  return pa::run_decode(p, static_cast<unsigned char*>(workspace), w, np, grid, stream,
                         "pa_decode");
 }
 
@@ -197,9 +208,9 @@ pa_status pa_decode_noalloc(const pa_decode_params* p, pa_stream_t stream) {
   if (st != PA_OK) return st;
   if (p->num_seqs == 0) return PA_OK;
   const int np = pa::num_partitions_for(p);
-  size_t om, ol, oa;
-  const size_t need = pa::decode_workspace_layout(p, np, &om, &ol, &oa);
-  if (need > pa::kNoAllocScratchBytes)
+  const int grid = pa::tc_grid();
+  const pa::WorkspaceLayout w = pa::decode_workspace_layout(p, np, grid);
+  if (w.total > pa::kNoAllocScratchBytes)
     return pa::set_error(PA_ERR_INVALID_ARG,
                          "pa_decode_noalloc: these shapes need more split-K scratch than the "
                          "library's fixed PA_NOALLOC_SCRATCH_BYTES; use pa_decode with a workspace "
@@ -207,9 +218,9 @@ pa_status pa_decode_noalloc(const pa_decode_params* p, pa_stream_t stream) {
   void* scratch = nullptr;
   const int e = pa::decode_scratch_address(&scratch);
   if (e != 0) return pa::set_cuda_error("pa_decode_noalloc: scratch lookup", e);
-  // run_decode clears the work counter at the head of the shared array before
-  // every launch; the partials are fully rewritten before they are read.
-  return pa::run_decode(p, static_cast<unsigned char*>(scratch), np, om, ol, oa, stream,
+  // Nothing in the array needs to start at zero: every call writes its plan
+  // and partials before reading them.
+  return pa::run_decode(p, static_cast<unsigned char*>(scratch), w, np, grid, stream,
                         "pa_decode_noalloc");
 }
 

@@ -4,36 +4,41 @@
 // Manager", §How the Kernel Executes Paged Attention; "PagedAttention and
 // continuous batching", §Attention kernel modification): per (sequence,
 // query head), softmax(scale * q.K^T) V over the cached tokens, K/V gathered
-// block by block through the block table, a running softmax across blocks,
-// padding slots of the last block masked.
+// block by block through the block table, a running softmax carried across
+// blocks, padding slots of the last block masked.
 //
-// Why tensor cores: with the query heads of one KV group packed, the score
-// step is a small dense contraction [keys x d] x [d x G] and the value step
-// [d x keys] x [keys x G]. Done in fp32 on CUDA cores they cost ~1000
-// instructions per 8 KiB (block, KV head) tile, which left the CUDA-core
-// kernel issue-bound at ~57 % of HBM bandwidth. On tcgen05 the same tile is
-// two MMA instructions.
+// Data movement. A chunk is one paged block with ALL its KV heads: in the
+// [block][kv head][16][d] cache that is 16*Hkv contiguous rows, so K and V
+// each arrive as two 128-byte-swizzled tensor-map TMA boxes of 16*Hkv rows
+// (16 KiB at Hkv = 8). For Hkv < 8 a chunk takes 8/Hkv blocks so that it
+// always has 128 rows: row = (block u, KV head h, key). Large boxes matter:
+// one issuing thread per SM keeps HBM busy with 16 KiB boxes, not with the
+// 2 KiB a (block, head) tile would give.
 //
-// Structure (one persistent CTA per SM, 5 warps):
-//  * Warp 4 -- producer. Takes work items (sequence, KV head, partition)
-//    from a global counter, reads the partition's block-table slice once
-//    (range-checked), and streams K and V in chunks of 8 blocks = 128 keys
-//    into a 3-stage shared-memory ring with tensor-map TMA (128-byte
-//    swizzle; blocks past the item are loaded from an out-of-range row and
-//    arrive as zeros). The item's query rows come with its first chunk.
-//  * Warps 0-3 -- consumers, one thread per key of the chunk:
-//      S^T[128 keys][16] = K[128][d] . Q^T  (tcgen05.mma, M=128, N=16, fp32 in TMEM)
-//      running max / sum per head, P = exp2(S*scale*log2e - m) as bf16 in smem
-//      O^T[d][16]      = V^T[d][128] . P^T   (tcgen05.mma, V read MN-major)
-//      acc[h] = acc[h] * alpha[h] + O^T[dim][h]   (thread = head dimension)
-//    The G real heads of the KV group use columns 0..G-1; the padded columns
-//    are never read back.
-//  * Results: one partition -> bf16 output; several -> fp32 partials merged
-//    by the log-sum-exp merge kernel.
+// Math. The chunk is the M=128 side of two tcgen05 MMAs whose N side is
+// every query head of the sequence (Hq padded to a multiple of 16):
+//   S^T[128 rows][N] = Kchunk . Q^T                 (fp32 in TMEM)
+//   O^T[d][N]       += V^Tchunk . P^T                (V read MN-major)
+// Row r only uses the G columns of its own KV head (GQA: query head n reads
+// KV head n / G), and P^T is block-diagonal (P^T[r][n] = 0 unless n / G is
+// r's head), so the second MMA sums each query head over its own KV head's
+// keys only. The unused products are free: the tensor pipe runs at a few
+// percent here. Softmax runs on CUDA cores, one thread per row.
 //
-// Every mbarrier wait is bounded; a wait that runs out sets PA_DEVERR_TIMEOUT
-// and the CTA winds down (uniformly, through its named barriers), drains its
-// outstanding copies and MMAs with bounded waits, frees TMEM and exits.
+// Scheduling (stream-K). The blocks of all sequences form one stream; CTA c
+// takes the c-th contiguous 1/grid of it. A (sequence, CTA) segment that
+// holds a whole sequence writes the bf16 output directly; otherwise it writes
+// fp32 (max, sum, weighted sum) partials to slot (sequence + CTA), unique
+// along the stream, and the merge kernel combines them by log-sum-exp.
+//
+// Roles: warp 4 produces (TMA into a ring of ST chunk slots; block-table
+// windows and the next sequence's length prefetched into registers); warps
+// 0-3 consume, pipelined one chunk deep: chunk c+1's scores (S double-
+// buffered in TMEM) and chunk c's value product run on the tensor core while
+// the CUDA cores do chunk c's softmax; chunk c's O^T is folded into the
+// accumulators at the start of chunk c+1, before P is rewritten. Every mbarrier
+// wait is bounded; a wait that runs out sets PA_DEVERR_TIMEOUT and the CTA
+// winds down through its named barriers, drains, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -51,258 +56,390 @@ namespace {
 __device__ unsigned int g_tc_errors;
 
 constexpr int BS = kBlockSize;
-constexpr int CHB = 8;         // blocks per chunk
-constexpr int CHK = CHB * BS;  // keys per chunk = MMA M
-constexpr int NQ = 16;         // MMA N: query heads of a KV group, padded
-constexpr int NCONS = 4;       // consumer warps
-constexpr int NTHREADS = (NCONS + 1) * 32;
+constexpr int ROWS = 128;      // rows of a chunk = MMA M
+constexpr int NCONS = 4;       // softmax (consumer) warps 0-3
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int NTHREADS = 6 * 32;
 constexpr int kCons = NCONS * 32;
-constexpr int TMEM_COLS = 32;  // S^T in columns 0..15, O^T in 16..31
-constexpr int MAX_ITEM_BLOCKS = kMaxPartitionTokens / BS;
+constexpr int kGroups = ROWS / BS;  // 16-row groups per chunk: (block, KV head)
+constexpr int kMaxDynSmem = 232448;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum : int { F_FIRST = 1, F_LAST = 2, F_SPLIT = 4, F_ZERO = 8, F_END = 16 };
+enum : int { F_FIRST = 1, F_LAST = 2, F_WHOLE = 4, F_END = 8 };
 
 struct __align__(16) ChunkMeta {
-  int b, g, p, flags;
-  int tok0;     // first token of the chunk
-  int tok_end;  // one past the item's last token
-  int nblk;     // blocks of the chunk that hold cache data
+  int b;      // sequence
+  int seg;    // partial slot when the sequence spans several CTAs
+  int flags;
+  int tok0;   // first token of the chunk
+  int L;      // context length (clamped)
+  int nblk;   // blocks of the chunk holding cache data (the others read as zeros)
   int qslot;
+  int pad;
 };
 
-template <int D>
+template <int D, int N>
 struct TcCfg {
-  static constexpr int HALVES = D / 64;               // 128-byte swizzle atoms per row
-  static constexpr int HALF_BYTES = CHK * 128;        // [128 rows][64 bf16]
+  static constexpr int HALVES = D / 64;            // 128-byte swizzle atoms per row
+  static constexpr int HALF_BYTES = ROWS * 128;    // [128 rows][64 bf16]
   static constexpr int K_BYTES = HALVES * HALF_BYTES;
-  static constexpr int SLOT_BYTES = 2 * K_BYTES;      // K then V
-  static constexpr int ST = (D == 128) ? 3 : 5;
-  static constexpr int QH_BYTES = NQ * 128;           // [16 rows][64 bf16]
+  static constexpr int SLOT_BYTES = 2 * K_BYTES;   // K then V
+  static constexpr int QH_BYTES = N * 128;         // [N rows][64 bf16]
   static constexpr int Q_BYTES = HALVES * QH_BYTES;
-  static constexpr int P_BYTES = 2 * NQ * 128;        // P^T [16][128 keys]: 2 atoms of 64 keys
-  static constexpr int BOX_BYTES = BS * 128;          // one TMA box: 16 rows x 64 bf16
-  static constexpr uint32_t CHUNK_TX = CHB * 2 * HALVES * BOX_BYTES;
-  static constexpr uint32_t Q_TX = HALVES * QH_BYTES;
+  static constexpr int PH_BYTES = N * 128;         // P^T [N rows][64 keys]
+  static constexpr int P_BYTES = 2 * PH_BYTES;     // 128 keys
+  static constexpr int MISC_BYTES = 4096;
+  static constexpr int ST_FIT =
+      (kMaxDynSmem - 1024 - 2 * Q_BYTES - P_BYTES - MISC_BYTES) / SLOT_BYTES;
+  static constexpr int ST = ST_FIT > 4 ? 4 : ST_FIT;
+  static_assert(ST >= 2, "at least a double-buffered ring");
   static constexpr int OFF_RING = 0;
-  static constexpr int OFF_Q = OFF_RING + ST * SLOT_BYTES;
+  static constexpr int OFF_Q = ST * SLOT_BYTES;
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_BARS = OFF_P + P_BYTES;
-  static constexpr int NBARS = 2 * ST + 5;  // full[ST] empty[ST] qempty[2] s o drain
-  static constexpr int OFF_META = (OFF_BARS + NBARS * 8 + 15) / 16 * 16;
-  static constexpr int OFF_TAB = OFF_META + ST * int(sizeof(ChunkMeta));
-  static constexpr int OFF_RED = OFF_TAB + MAX_ITEM_BLOCKS * 4;
-  static constexpr int OFF_RED2 = OFF_RED + NCONS * NQ * 4;
-  static constexpr int OFF_MISC = OFF_RED2 + NCONS * NQ * 4;
-  static constexpr int SMEM = OFF_MISC + 32 + 1024;  // + alignment slack
-  static constexpr uint32_t IDESC_S = dev::idesc_bf16_f32(CHK, NQ, false, false);
-  static constexpr uint32_t IDESC_PV = dev::idesc_bf16_f32(128, NQ, true, false);
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static constexpr int OFF_MISC = OFF_P + P_BYTES;
+  // full[ST] empty[ST] qempty[2] s[2] o p drain
+  static constexpr int NBARS = 2 * ST + 7;
+  static constexpr int OFF_BARS = OFF_MISC;
+  static constexpr int OFF_META = OFF_BARS + (NBARS * 8 + 15) / 16 * 16;
+  static constexpr int OFF_RED = OFF_META + ST * int(sizeof(ChunkMeta));  // [2][8 groups][8]
+  static constexpr int OFF_RED2 = OFF_RED + 2 * kGroups * 8 * 4;
+  static constexpr int OFF_ALPHA = OFF_RED2 + kGroups * 8 * 4;  // [2][64], by chunk parity
+  static constexpr int OFF_LS = OFF_ALPHA + 2 * 64 * 4;
+  static constexpr int OFF_MS = OFF_LS + 64 * 4;
+  static constexpr int OFF_WORDS = OFF_MS + 64 * 4;
+  static constexpr int SMEM = OFF_WORDS + 64 + 1024;  // + alignment slack
+  static_assert(OFF_WORDS + 64 <= OFF_MISC + MISC_BYTES, "misc area");
+  static_assert(SMEM <= kMaxDynSmem, "shared memory budget");
+  static constexpr int TMEM_COLS = 4 * N;  // S double buffer [0, 2N), O at [2N, 3N)
+  static constexpr uint32_t IDESC_S = dev::idesc_bf16_f32(ROWS, N, false, false);
+  static constexpr uint32_t IDESC_PV = dev::idesc_bf16_f32(ROWS, N, true, false);
+  static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
+  static constexpr uint32_t Q_TX = Q_BYTES;
 };
 
 struct TcParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   __nv_bfloat16* out;
-  float* part_m;
-  float* part_l;
-  float* part_acc;
-  unsigned int* counters;
-  int max_blocks_per_seq, num_seqs, num_kv_heads, num_q_heads, group, num_blocks;
-  int max_context_len, partition_tokens, num_partitions, total_items, oob_row;
+  float* part_m;    // [segments][Hq]
+  float* part_l;    // [segments][Hq]
+  float* part_acc;  // [segments][Hq][D]
+  int* ws_plan;     // [0] = blocks per CTA, [1 .. B+1] = block prefix of the sequences
+  int max_blocks_per_seq, num_seqs, num_kv_heads, num_q_heads, num_blocks, cap, oob_row;
   float scale_log2;
 };
 
-// Byte offset of P^T[h][key] in the K-major, 128B-swizzled B-operand layout.
-__device__ __forceinline__ uint32_t p_offset(int h, int key) {
+// Byte offset of P^T[n][key] in the K-major, 128B-swizzled B-operand layout
+// (two 64-key atoms of [N rows][128 B]).
+template <int N>
+__device__ __forceinline__ uint32_t p_offset(int n, int key) {
   const int half = key >> 6, kin = key & 63;
-  const int r = h & 7, grp = h >> 3;
-  return uint32_t(half * 2048 + grp * 1024 + r * 128 + (((kin >> 3) ^ r) << 4) + (kin & 7) * 2);
+  const int r = n & 7, grp = n >> 3;
+  return uint32_t(half * (N * 128) + grp * 1024 + r * 128 + (((kin >> 3) ^ r) << 4) +
+                  (kin & 7) * 2);
 }
 
-template <int D, int G>
-__device__ __forceinline__ void consumer_loop(const TcParams& P, unsigned char* ring,
-                                              unsigned char* qbuf, unsigned char* pbuf,
-                                              uint64_t* full, uint64_t* empty, uint64_t* qempty,
-                                              uint64_t* bar_s, uint64_t* bar_o,
-                                              const ChunkMeta* meta, float* red, float* red2,
-                                              uint32_t tmem, volatile int* abort_flag,
-                                              int* consumed_out) {
-  using C = TcCfg<D>;
-  const int ctid = threadIdx.x;  // 0..127: key of the chunk, and head dimension
-  const int cw = ctid >> 5, lane = ctid & 31;
-  const uint32_t t_lane = uint32_t(cw * 32) << 16;
-  const uint32_t tS = tmem + t_lane, tO = tmem + t_lane + 16;
-  float m_run[G], l_part[G], acc[G];
+// S^T = Kchunk . Q^T for one chunk (single thread): D/16 MMAs of K = 16.
+template <int D, int N>
+__device__ __forceinline__ void issue_scores(uint32_t tmem_col, const unsigned char* kv,
+                                             const unsigned char* q) {
+  using C = TcCfg<D, N>;
+  const uint32_t kb = dev::smem_addr(kv);
+  const uint32_t qb = dev::smem_addr(q);
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m_run[h] = -INFINITY;
-    l_part[h] = 0.0f;
-    acc[h] = 0.0f;
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t hf = kk >> 2, off = uint32_t(kk & 3) * 32;
+    dev::mma_bf16(tmem_col,
+                  dev::smem_desc(kb + hf * C::HALF_BYTES + off, 16, 1024, dev::kSwizzle128B),
+                  dev::smem_desc(qb + hf * C::QH_BYTES + off, 16, 1024, dev::kSwizzle128B),
+                  C::IDESC_S, kk > 0);
   }
-  int chunk_seq = 0;
-  int mma_chunks = 0;
-  bool carry_ok = true;
+}
+
+// ---------------------------------------------------------------------------
+// MMA warp (one thread): per chunk, S^T = K.Q^T into S[chunk & 1] as soon as
+// the chunk has landed, and O^T = V^T.P^T once the softmax warps have written
+// P for it. Scores run one chunk ahead of the value product.
+// ---------------------------------------------------------------------------
+template <int D, int N>
+__device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbuf,
+                                         unsigned char* pbuf, uint64_t* full, uint64_t* empty,
+                                         uint64_t* qempty, uint64_t* bar_s, uint64_t* bar_o,
+                                         uint64_t* bar_p, uint64_t* drain, const ChunkMeta* meta,
+                                         uint32_t tmem, volatile int* abort_flag) {
+  using C = TcCfg<D, N>;
+  // D = 64: the second 64-row half of M re-reads the first (LBO 0); those
+  // TMEM lanes are never read back.
+  const uint32_t lbo = C::HALVES == 2 ? uint32_t(C::HALF_BYTES) : 0u;
+  const uint32_t pbs = dev::smem_addr(pbuf);
+  // Event loop: issue whichever is ready first -- the scores of the next
+  // ring position once its data has landed (at most one position ahead of
+  // the value products), or the value product of position c once the softmax
+  // warps have written its P. Every ring position before the end sentinel
+  // is a real chunk, so position = chunk index.
+  int c = 0;           // position whose value product is next
+  int s_pos = 0;       // next position to issue scores for
+  int end_pos = -1;    // position of the end sentinel, once seen
+  bool ok = true;
+  uint64_t t_progress = dev::global_timer_ns();
   for (;;) {
-    const int slot = chunk_seq % C::ST;
-    const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
-    bool ok = __all_sync(0xffffffffu, dev::mbar_wait(&full[slot], ph));
-    const ChunkMeta m = meta[slot];
-    if (!dev::named_barrier_and(1, kCons, ok && carry_ok && *abort_flag == 0)) {
-      if (ctid == 0) {
-        atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
-        *abort_flag = 1;
+    bool progress = false;
+    if (end_pos < 0 && s_pos <= c + 1 &&
+        dev::mbar_test(&full[s_pos % C::ST], uint32_t(s_pos / C::ST) & 1u)) {
+      const int sl = s_pos % C::ST;
+      const ChunkMeta mn = meta[sl];
+      if (mn.flags & F_END) {
+        end_pos = s_pos;
+      } else {
+        dev::tc_fence_after();
+        issue_scores<D, N>(tmem + (s_pos & 1) * N, ring + size_t(sl) * C::SLOT_BYTES,
+                           qbuf + mn.qslot * C::Q_BYTES);
+        dev::mma_commit(&bar_s[s_pos & 1]);
+        if (mn.flags & F_LAST) dev::mma_commit(&qempty[mn.qslot]);
       }
-      break;
+      ++s_pos;
+      progress = true;
     }
-    if (m.flags & F_END) break;
-    if (m.flags & F_ZERO) {
-      if (ctid < D) {
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          P.out[(size_t(m.b) * P.num_q_heads + m.g * G + h) * D + ctid] = __float2bfloat16_rn(0.f);
-      }
-      if (ctid == 0) dev::mbar_arrive(&empty[slot]);
-      ++chunk_seq;
-      continue;
-    }
-    unsigned char* kv = ring + size_t(slot) * C::SLOT_BYTES;
-
-    // ---- S^T = K . Q^T  (one thread issues; fp32 result in TMEM columns 0..15)
-    if (ctid == 0) {
+    if (c < s_pos && c != end_pos && dev::mbar_test(bar_p, uint32_t(c) & 1u)) {
+      const int sl = c % C::ST;
       dev::tc_fence_after();
-      const uint32_t kb = dev::smem_addr(kv);
-      const uint32_t qb = dev::smem_addr(qbuf + m.qslot * C::Q_BYTES);
+      const uint32_t vb = dev::smem_addr(ring + size_t(sl) * C::SLOT_BYTES + C::K_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t hf = kk >> 2, off = uint32_t(kk & 3) * 32;
-        dev::mma_bf16(tmem, dev::smem_desc(kb + hf * C::HALF_BYTES + off, 16, 1024, dev::kSwizzle128B),
-                      dev::smem_desc(qb + hf * C::QH_BYTES + off, 16, 1024, dev::kSwizzle128B),
-                      C::IDESC_S, kk > 0);
-      }
-      dev::mma_commit(bar_s);
-      if (m.flags & F_LAST) dev::mma_commit(&qempty[m.qslot]);
-    }
-    ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_s, uint32_t(mma_chunks) & 1u));
-    dev::tc_fence_after();
-    float s[16];
-    dev::tmem_ld16(tS, s);
-
-    // ---- running softmax over this chunk (thread = key)
-    const int t = m.tok0 + ctid;
-    const bool valid = t < m.tok_end;
-    float x[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      x[h] = valid ? s[h] * P.scale_log2 : -INFINITY;
-      float v = x[h];
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-      if (lane == 0) red[cw * NQ + h] = v;
-    }
-    ok = dev::named_barrier_and(1, kCons, ok);
-    float alpha[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float cmax = red[h];
-#pragma unroll
-      for (int w = 1; w < NCONS; ++w) cmax = fmaxf(cmax, red[w * NQ + h]);
-      const float m_new = fmaxf(m_run[h], cmax);
-      alpha[h] = dev::fast_exp2(m_run[h] - m_new);
-      m_run[h] = m_new;
-      const float p = dev::fast_exp2(x[h] - m_new);
-      l_part[h] = fmaf(l_part[h], alpha[h], p);
-      *reinterpret_cast<__nv_bfloat16*>(pbuf + p_offset(h, ctid)) = __float2bfloat16_rn(p);
-    }
-    // A masked key inside a block that was loaded (the sequence's last,
-    // partial block) may hold anything, NaN included: clear its V row so that
-    // 0 * V stays 0 in the MMA.
-    if (!valid && (ctid >> 4) < m.nblk) {
-#pragma unroll
-      for (int hf = 0; hf < C::HALVES; ++hf) {
-        uint4* row = reinterpret_cast<uint4*>(kv + C::K_BYTES + hf * C::HALF_BYTES + ctid * 128);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    dev::fence_async_smem();
-    dev::tc_fence_before();
-    ok = dev::named_barrier_and(1, kCons, ok);
-
-    // ---- O^T = V^T . P^T  (V read MN-major; fresh accumulation each chunk)
-    if (ctid == 0) {
-      dev::tc_fence_after();
-      const uint32_t vb = dev::smem_addr(kv + C::K_BYTES);
-      const uint32_t pb = dev::smem_addr(pbuf);
-      // D = 64: the second 64-row half of M re-reads the first (LBO 0); its
-      // TMEM lanes are never read back.
-      const uint32_t lbo = C::HALVES == 2 ? uint32_t(C::HALF_BYTES) : 0u;
-#pragma unroll
-      for (int kk = 0; kk < CHK / 16; ++kk) {
-        dev::mma_bf16(tmem + 16, dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
-                      dev::smem_desc(pb + (kk >> 2) * C::QH_BYTES + (kk & 3) * 32, 16, 1024,
+      for (int kk = 0; kk < ROWS / 16; ++kk) {
+        dev::mma_bf16(tmem + 2 * N,
+                      dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
+                      dev::smem_desc(pbs + (kk >> 2) * C::PH_BYTES + (kk & 3) * 32, 16, 1024,
                                      dev::kSwizzle128B),
                       C::IDESC_PV, kk > 0);
       }
       dev::mma_commit(bar_o);
-      dev::mma_commit(&empty[slot]);
+      dev::mma_commit(&empty[sl]);
+      ++c;
+      progress = true;
     }
-    ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(mma_chunks) & 1u)) && ok;
-    dev::tc_fence_after();
-    float o[16];
-    dev::tmem_ld16(tO, o);
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = fmaf(acc[h], alpha[h], o[h]);
-    dev::tc_fence_before();
-    ++mma_chunks;
-    ++chunk_seq;
+    if (c == end_pos) break;
+    if (progress) {
+      t_progress = dev::global_timer_ns();
+      continue;
+    }
+    if (*abort_flag) break;
+    if (dev::global_timer_ns() - t_progress > dev::kWaitNsLimit) {
+      ok = false;
+      break;
+    }
+    __nanosleep(20);
+  }
+  if (!ok) {
+    atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  }
+  // every MMA this thread issued completes before TMEM can be released
+  dev::mma_commit(drain);
+  (void)dev::mbar_wait(drain, 0);
+}
 
-    if (m.flags & F_LAST) {
+// ---------------------------------------------------------------------------
+// Softmax warps 0-3: thread = row of the chunk (scores), = head dimension
+// (output). Chunk r: read S, running max (half-warp + shared-memory exchange
+// across the chunk's groups of the same KV head), fold chunk r-1's O^T into
+// the accumulators, write P and signal the MMA warp.
+// ---------------------------------------------------------------------------
+template <int D, int G, int N>
+struct Softmax {
+  using C = TcCfg<D, N>;
+  static constexpr int LDC = 2 * G <= 8 ? 8 : 16;  // score columns a warp reads (two heads)
+
+  __device__ __forceinline__ static void run(const TcParams& P, unsigned char* ring,
+                                             unsigned char* pbuf, uint64_t* full,
+                                             uint64_t* bar_s, uint64_t* bar_o, uint64_t* bar_p,
+                                             const ChunkMeta* meta, float* red, float* red2,
+                                             float* alpha_s, float* l_s, float* m_s,
+                                             uint32_t tmem, volatile int* abort_flag,
+                                             int* consumed_out) {
+    const int ctid = threadIdx.x;
+    const int cw = ctid >> 5, lane = ctid & 31;
+    const int H = P.num_kv_heads;
+    const int Hq = P.num_q_heads;
+    const int U = kGroups / H;
+    const int grp = ctid >> 4;  // (block u, KV head h) group of this row
+    const int u = grp / H, h = grp - (grp / H) * H;
+    const int key = ctid & 15;
+    const int h0 = (2 * cw) % H;  // the warp's first head
+    const int col0 = H >= 2 ? h0 * G : 0;
+    const bool upper = H >= 2 && lane >= 16;  // this lane's head is the warp's second
+    const uint32_t t_lane = uint32_t(cw * 32) << 16;
+    const uint32_t tO = tmem + t_lane + 2 * N;
+
+    float m_run[G], l_part[G];
+    float acc[N];
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float v = l_part[h];
+    for (int j = 0; j < G; ++j) {
+      m_run[j] = -INFINITY;
+      l_part[j] = 0.0f;
+    }
 #pragma unroll
-        for (int o2 = 16; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
-        if (lane == 0) red2[cw * NQ + h] = v;
+    for (int n = 0; n < N; ++n) acc[n] = 0.0f;
+    int c = 0;          // ring position
+    int r = 0;          // real chunks handled
+    bool pend = false;  // chunk r-1's O^T not yet folded into acc
+    bool ok = true;
+
+    for (;;) {
+      const int slot = c % C::ST;
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&full[slot], uint32_t(c / C::ST) & 1u)) && ok;
+      const ChunkMeta m = meta[slot];
+      // every exit below is taken by all 128 threads together (named barriers follow)
+      if (!dev::named_barrier_and(1, kCons, ok && *abort_flag == 0)) {
+        ok = false;
+        break;
       }
-      ok = dev::named_barrier_and(1, kCons, ok);
-      if (ctid < D) {
+      if (m.flags & F_END) break;
+      const int buf = r & 1;
+      float* redb = red + buf * (kGroups * 8);
+
+      // ---- scores of this chunk -> registers
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(r >> 1) & 1u)) && ok;
+      dev::tc_fence_after();
+      float s[LDC];
+      if constexpr (LDC == 8) {
+        dev::tmem_ld8(tmem + t_lane + buf * N + col0, s);
+      } else {
+        dev::tmem_ld16(tmem + t_lane + buf * N + col0, s);
+      }
+
+      // ---- running softmax: row = (block u, head h, key)
+      const int t = m.tok0 + u * BS + key;
+      const bool valid = u < m.nblk && t < m.L;
+      float x[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float l = red2[h];
+      for (int j = 0; j < G; ++j) {
+        const float sj = upper ? s[(LDC >= 2 * G ? G : 0) + j] : s[j];
+        x[j] = valid ? sj * P.scale_log2 : -INFINITY;
+        float v = x[j];
 #pragma unroll
-          for (int w = 1; w < NCONS; ++w) l += red2[w * NQ + h];
-          const size_t row = size_t(m.b) * P.num_q_heads + m.g * G + h;
-          if (!(m.flags & F_SPLIT)) {
-            P.out[row * D + ctid] = __float2bfloat16_rn(acc[h] * __frcp_rn(l));
+        for (int o = 8; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (key == 0) redb[grp * 8 + j] = v;
+      }
+      if (!dev::named_barrier_and(1, kCons, ok && *abort_flag == 0)) {
+        ok = false;
+        break;
+      }
+
+      // ---- fold chunk r-1's O^T (its value MMA must be done before P is rewritten)
+      if (pend) {
+        ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(r - 1) & 1u)) && ok;
+        dev::tc_fence_after();
+        float o[N];
+        dev::tmem_ld_cols<N>(tO, o);
+        const float* al = alpha_s + ((r - 1) & 1) * 64;
+#pragma unroll
+        for (int n = 0; n < N; ++n) acc[n] = fmaf(acc[n], al[n], o[n]);
+        pend = false;
+      }
+
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float cmax = -INFINITY;
+        for (int uu = 0; uu < U; ++uu) cmax = fmaxf(cmax, redb[(uu * H + h) * 8 + j]);
+        const float m_new = fmaxf(m_run[j], cmax);
+        const float alpha = dev::fast_exp2(m_run[j] - m_new);
+        m_run[j] = m_new;
+        const float p = dev::fast_exp2(x[j] - m_new);
+        l_part[j] = fmaf(l_part[j], alpha, p);
+        const int n = h * G + j;
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + p_offset<N>(n, ctid)) = __float2bfloat16_rn(p);
+        if (u == 0 && key == 0) alpha_s[buf * 64 + n] = alpha;
+      }
+      // A masked row inside a loaded block (the sequence's last, partial
+      // block) may hold anything, NaN included: clear its V row so 0 * V = 0.
+      if (!valid && u < m.nblk) {
+        unsigned char* kv = ring + size_t(slot) * C::SLOT_BYTES;
+#pragma unroll
+        for (int hf = 0; hf < C::HALVES; ++hf) {
+          uint4* row = reinterpret_cast<uint4*>(kv + C::K_BYTES + hf * C::HALF_BYTES + ctid * 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      dev::fence_async_smem();
+      dev::tc_fence_before();
+      dev::mbar_arrive(bar_p);  // P(r) written, S(r) and O(r-1) read
+
+      if (m.flags & F_LAST) {
+        // per query head: softmax denominator over all rows of its KV head
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          float v = l_part[j];
+#pragma unroll
+          for (int o2 = 8; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+          if (key == 0) red2[grp * 8 + j] = v;
+        }
+        ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(r) & 1u)) && ok;
+        dev::tc_fence_after();
+        float o[N];
+        dev::tmem_ld_cols<N>(tO, o);
+        dev::named_barrier(1, kCons);  // every alpha and l of this chunk is written
+        {
+          const float* al = alpha_s + buf * 64;
+#pragma unroll
+          for (int n = 0; n < N; ++n) acc[n] = fmaf(acc[n], al[n], o[n]);
+        }
+        if (u == 0 && key == 0) {
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            float l = 0.0f;
+            for (int uu = 0; uu < U; ++uu) l += red2[(uu * H + h) * 8 + j];
+            l_s[h * G + j] = l;
+            m_s[h * G + j] = m_run[j];
+          }
+        }
+        dev::named_barrier(1, kCons);
+        if (ctid < D) {
+          if (m.flags & F_WHOLE) {
+            __nv_bfloat16* o_row = P.out + size_t(m.b) * Hq * D + ctid;
+#pragma unroll
+            for (int n = 0; n < N; ++n)
+              if (n < Hq) o_row[size_t(n) * D] = __float2bfloat16_rn(acc[n] * __frcp_rn(l_s[n]));
           } else {
-            const size_t prow = row * P.num_partitions + m.p;
-            P.part_acc[prow * D + ctid] = acc[h];
-            if (ctid == 0) {
-              P.part_m[prow] = m_run[h];
-              P.part_l[prow] = l;
+            float* a_row = P.part_acc + size_t(m.seg) * Hq * D + ctid;
+#pragma unroll
+            for (int n = 0; n < N; ++n)
+              if (n < Hq) a_row[size_t(n) * D] = acc[n];
+            if (ctid < Hq) {
+              P.part_m[size_t(m.seg) * Hq + ctid] = m_s[ctid];
+              P.part_l[size_t(m.seg) * Hq + ctid] = l_s[ctid];
             }
           }
         }
-      }
+        dev::tc_fence_before();
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        m_run[h] = -INFINITY;
-        l_part[h] = 0.0f;
-        acc[h] = 0.0f;
+        for (int j = 0; j < G; ++j) {
+          m_run[j] = -INFINITY;
+          l_part[j] = 0.0f;
+        }
+#pragma unroll
+        for (int n = 0; n < N; ++n) acc[n] = 0.0f;
+      } else {
+        pend = true;
       }
+      ++r;
+      ++c;
     }
-    carry_ok = ok;
+    if (!ok && ctid == 0) {
+      atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    if (ctid == 0) *consumed_out = c;
   }
-  if (ctid == 0) *consumed_out = chunk_seq;
-}
+};
 
-template <int D, int G>
+template <int D, int G, int N>
 __global__ void __launch_bounds__(NTHREADS, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, const TcParams P) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, N>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -313,46 +450,108 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + C::ST;
   uint64_t* qempty = bars + 2 * C::ST;
-  uint64_t* bar_s = bars + 2 * C::ST + 2;
-  uint64_t* bar_o = bar_s + 1;
-  uint64_t* drain = bar_s + 2;
+  uint64_t* bar_s = bars + 2 * C::ST + 2;  // [2] scores ready
+  uint64_t* bar_o = bar_s + 2;              // value product ready
+  uint64_t* bar_p = bar_o + 1;              // P written by all 128 softmax threads
+  uint64_t* drain = bar_p + 1;
   ChunkMeta* meta = reinterpret_cast<ChunkMeta*>(smem + C::OFF_META);
-  int32_t* tab = reinterpret_cast<int32_t*>(smem + C::OFF_TAB);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* red2 = reinterpret_cast<float*>(smem + C::OFF_RED2);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  int* consumed = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
-  int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 12);
+  float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
+  float* l_s = reinterpret_cast<float*>(smem + C::OFF_LS);
+  float* m_s = reinterpret_cast<float*>(smem + C::OFF_MS);
+  int* words = reinterpret_cast<int*>(smem + C::OFF_WORDS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&words[0]);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&words[1]);
+  int* consumed = &words[2];
+  int* issued = &words[3];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const int B = P.num_seqs;
+  const int H = P.num_kv_heads;
 
   if (tid == 0) {
     for (int i = 0; i < C::ST; ++i) {
       dev::mbar_init(&full[i], 1);
       dev::mbar_init(&empty[i], 1);
     }
-    dev::mbar_init(&qempty[0], 1);
-    dev::mbar_init(&qempty[1], 1);
-    dev::mbar_init(bar_s, 1);
+    for (int i = 0; i < 2; ++i) {
+      dev::mbar_init(&qempty[i], 1);
+      dev::mbar_init(&bar_s[i], 1);
+    }
     dev::mbar_init(bar_o, 1);
+    dev::mbar_init(bar_p, kCons);
     dev::mbar_init(drain, 1);
     *abort_flag = 0;
     *consumed = 0;
     *issued = 0;
     dev::fence_barrier_init();
   }
+  // P^T is block-diagonal: the entries off the diagonal stay zero for good.
   for (int i = tid; i < C::P_BYTES / 16; i += NTHREADS)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
-  if (warp == 0) dev::tmem_alloc(tmem_slot, TMEM_COLS);
+
+  // ---- stream-K plan (uses the still-empty ring as scratch): block counts of
+  // the sequences, their exclusive prefix, this CTA's range of the stream.
+  int* pre = reinterpret_cast<int*>(ring);
+  {
+    const int seg = (B + NTHREADS - 1) / NTHREADS;
+    const int b0 = min(B, tid * seg), b1 = min(B, b0 + seg);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      int L = P.context_lens[b];
+      if (L > P.cap) {
+        if (blockIdx.x == 0) atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
+        L = P.cap;
+      }
+      local += L > 0 ? (L + BS - 1) / BS : 0;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) reinterpret_cast<int*>(red)[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += reinterpret_cast<int*>(red)[w];
+    for (int b = b0; b < b1; ++b) {
+      pre[b] = run;
+      const int L = min(P.context_lens[b], P.cap);
+      run += L > 0 ? (L + BS - 1) / BS : 0;
+    }
+    if (tid == NTHREADS - 1) pre[B] = run;
+  }
+  __syncthreads();
+  const int total = pre[B];
+  const int R = total > 0 ? (total + int(gridDim.x) - 1) / int(gridDim.x) : 1;
+  const int u0 = min(total, int(blockIdx.x) * R);
+  const int u1 = min(total, u0 + R);
+  int b_start = 0;
+  if (u0 < u1) {
+    int lo = 0, hi = B;  // largest b with pre[b] <= u0: the sequence holding block u0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] <= u0) lo = mid; else hi = mid;
+    }
+    b_start = lo;
+  }
+  const int off_start = u0 < u1 ? u0 - pre[b_start] : 0;
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= B; i += NTHREADS) P.ws_plan[1 + i] = pre[i];
+    if (tid == 0) P.ws_plan[0] = R;
+  }
+  for (int i = tid; i < 128; i += NTHREADS) alpha_s[i] = 1.0f;  // padded columns stay 1
+  if (warp == 0) dev::tmem_alloc(tmem_slot, C::TMEM_COLS);
   dev::fence_async_smem();
   dev::tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // the ring is free for TMA from here on
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == NCONS) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       dev::prefetch_tmap(&tm_k);
@@ -360,108 +559,98 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       dev::prefetch_tmap(&tm_q);
     }
     const uint64_t pol = dev::l2_evict_first_policy();
-    const int PT = P.partition_tokens;
-    const int bh = P.num_seqs * P.num_kv_heads;
-    int chunk_seq = 0, item_seq = 0;
+    const int U = kGroups / H;   // blocks per chunk
+    const int grows = BS * H;    // rows of one block (all KV heads)
+    int chunk_seq = 0, seg_seq = 0;
     bool ok = true;
-    while (ok) {
+    // block-table window: lane j holds the entry of block first_block + j
+    auto load_window = [&](int b, int first_block) {
+      const int j = first_block + lane;
+      return (b < B && j < P.max_blocks_per_seq)
+                 ? P.block_tables[size_t(b) * P.max_blocks_per_seq + j] : -1;
+    };
+    int b = b_start, off = off_start, unit = u0;
+    int win = load_window(b, off);
+    int L_cur = b < B ? min(P.context_lens[b], P.cap) : 0;
+    while (ok && unit < u1) {
       if (*abort_flag) break;
-      int w = 0;
-      if (lane == 0) w = int(atomicAdd(P.counters, 1u));
-      w = __shfl_sync(0xffffffffu, w, 0);
-      if (w >= P.total_items) break;
-      const int p = w / bh;
-      const int rem = w - p * bh;
-      const int b = rem / P.num_kv_heads;
-      const int g = rem - b * P.num_kv_heads;
-      int L = P.context_lens[b];
-      const int cap = min(P.max_blocks_per_seq * BS, P.max_context_len);
-      if (L > cap) {
-        if (lane == 0 && p == 0 && g == 0) atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
-        L = cap;
-      }
-      if (L <= 0) {
-        if (p != 0) continue;
-        const int slot = chunk_seq % C::ST;
-        const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
-        if (lane == 0) {
-          ok = dev::mbar_wait(&empty[slot], ph ^ 1u);
-          ChunkMeta m{};
-          m.b = b;
-          m.g = g;
-          m.p = 0;
-          m.flags = F_ZERO;
-          meta[slot] = m;
-          dev::mbar_arrive(&full[slot]);
-        }
-        ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
-        ++chunk_seq;
+      const int nb = L_cur > 0 ? (L_cur + BS - 1) / BS : 0;
+      if (nb == 0) {  // empty sequence: nothing of it in the stream
+        ++b;
+        win = load_window(b, 0);
+        L_cur = b < B ? min(P.context_lens[b], P.cap) : 0;
         continue;
       }
-      const int np = (L + PT - 1) / PT;
-      if (p >= np) continue;
-      const int tok0 = p * PT;
-      const int tok1 = min(L, tok0 + PT);
-      const int nblk = (tok1 - tok0 + BS - 1) / BS;
-      const int lb0 = tok0 / BS;
-      __syncwarp();
-      const int32_t* trow = P.block_tables + size_t(b) * P.max_blocks_per_seq + lb0;
-      for (int j = lane; j < nblk; j += 32) {
-        const int32_t e = trow[j];
-        int row = P.oob_row;
-        if (e < 0 || e >= P.num_blocks) {
-          atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
-        } else {
-          row = (e * P.num_kv_heads + g) * BS;
-        }
-        tab[j] = row;
-      }
-      __syncwarp();
-      const int qs = item_seq & 1;
-      const int nch = (nblk + CHB - 1) / CHB;
+      const int seg_nb = min(nb - off, u1 - unit);
+      const bool whole = off == 0 && seg_nb == nb;
+      // prefetched for later: the next sequence's length and first window,
+      // this segment's second window
+      const int L_nxt = b + 1 < B ? min(P.context_lens[b + 1], P.cap) : 0;
+      const int win_nxt_seq = load_window(b + 1, 0);
+      int win_nxt = seg_nb > 32 ? load_window(b, off + 32) : -1;
+      const int qs = seg_seq & 1;
+      const int nch = (seg_nb + U - 1) / U;
       for (int c = 0; c < nch; ++c) {
+        const int jb = c * U;  // first block of the chunk within the segment
+        if (jb > 0 && (jb & 31) == 0) {
+          win = win_nxt;
+          win_nxt = jb + 32 < seg_nb ? load_window(b, off + jb + 32) : -1;
+        }
         const int slot = chunk_seq % C::ST;
         const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
         if (lane == 0) {
-          ok = dev::mbar_wait(&empty[slot], ph ^ 1u);
-          if (ok && c == 0) ok = dev::mbar_wait(&qempty[qs], (uint32_t(item_seq >> 1) & 1u) ^ 1u);
+          ok = dev::mbar_wait_sleep(&empty[slot], ph ^ 1u, 64);
+          if (ok && c == 0)
+            ok = dev::mbar_wait_sleep(&qempty[qs], (uint32_t(seg_seq >> 1) & 1u) ^ 1u, 64);
           if (ok) {
             ChunkMeta m;
             m.b = b;
-            m.g = g;
-            m.p = p;
-            m.flags = (c == 0 ? F_FIRST : 0) | (c == nch - 1 ? F_LAST : 0) | (L > PT ? F_SPLIT : 0);
-            m.tok0 = tok0 + c * CHK;
-            m.tok_end = tok1;
-            m.nblk = min(CHB, nblk - c * CHB);
+            m.seg = b + int(blockIdx.x);
+            m.flags = (c == 0 ? F_FIRST : 0) | (c == nch - 1 ? F_LAST : 0) | (whole ? F_WHOLE : 0);
+            m.tok0 = (off + jb) * BS;
+            m.L = L_cur;
+            m.nblk = min(U, seg_nb - jb);
             m.qslot = qs;
+            m.pad = 0;
             meta[slot] = m;
             dev::mbar_arrive_expect_tx(&full[slot], C::CHUNK_TX + (c == 0 ? C::Q_TX : 0u));
           }
         }
         ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
         if (!ok) break;
+        // lanes 0..U-1: one block (all KV heads) each
+        const int e = __shfl_sync(0xffffffffu, win, (jb & 31) + (lane % U));
         unsigned char* kdst = ring + size_t(slot) * C::SLOT_BYTES;
-        if (lane < CHB) {
-          const int j = c * CHB + lane;
-          const int row = j < nblk ? tab[j] : P.oob_row;
+        if (lane < U) {
+          int row = P.oob_row;
+          if (jb + lane < seg_nb) {
+            if (e >= 0 && e < P.num_blocks) {
+              row = e * grows;
+            } else {
+              atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+            }
+          }
 #pragma unroll
           for (int hf = 0; hf < C::HALVES; ++hf) {
-            unsigned char* d = kdst + hf * C::HALF_BYTES + lane * C::BOX_BYTES;
+            unsigned char* d = kdst + hf * C::HALF_BYTES + lane * grows * 128;
             dev::tma_load_2d(d, &tm_k, hf * 64, row, &full[slot], pol);
             dev::tma_load_2d(d + C::K_BYTES, &tm_v, hf * 64, row, &full[slot], pol);
           }
-        } else if (lane == CHB && c == 0) {
-          const int qrow = b * P.num_q_heads + g * P.group;
+        } else if (lane == 8 && c == 0) {
 #pragma unroll
           for (int hf = 0; hf < C::HALVES; ++hf)
-            dev::tma_load_2d(qbuf + qs * C::Q_BYTES + hf * C::QH_BYTES, &tm_q, hf * 64, qrow,
-                             &full[slot], pol);
+            dev::tma_load_2d(qbuf + qs * C::Q_BYTES + hf * C::QH_BYTES, &tm_q, hf * 64,
+                             b * P.num_q_heads, &full[slot], pol);
         }
         ++chunk_seq;
         if (lane == 0) *issued = chunk_seq;
       }
-      ++item_seq;
+      ++seg_seq;
+      unit += seg_nb;
+      ++b;
+      off = 0;
+      win = win_nxt_seq;
+      L_cur = L_nxt;
     }
     // end of work: a sentinel chunk tells the consumers to stop
     if (lane == 0) {
@@ -477,19 +666,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         *abort_flag = 1;
       }
     }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0)
+      mma_loop<D, N>(ring, qbuf, pbuf, full, empty, qempty, bar_s, bar_o, bar_p, drain, meta,
+                     tmem, abort_flag);
   } else {
-    // ------------------------------------------------------------ consumers
-    consumer_loop<D, G>(P, ring, qbuf, pbuf, full, empty, qempty, bar_s, bar_o, meta, red, red2,
-                        tmem, abort_flag, consumed);
+    // ------------------------------------------------------------ softmax
+    Softmax<D, G, N>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2, alpha_s,
+                          l_s, m_s, tmem, abort_flag, consumed);
   }
 
   __syncthreads();
   if (*abort_flag && tid == 0) {
-    // Wind down after a stalled wait: let every MMA issued so far finish and
-    // every bulk copy issued but not consumed land (each wait bounded)
-    // before TMEM and shared memory are released.
-    dev::mma_commit(drain);
-    (void)dev::mbar_wait(drain, 0);
+    // Wind down after a stalled wait: every bulk copy issued but not consumed
+    // lands (each wait bounded) before shared memory is released. (The MMA
+    // warp has already waited for its own MMAs.)
     for (int c = *consumed; c < *issued; ++c)
       (void)dev::mbar_wait(&full[c % C::ST], uint32_t(c / C::ST) & 1u);
   }
@@ -497,8 +689,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (warp == 0) {
     dev::tc_fence_after();
-    dev::tmem_dealloc(tmem, TMEM_COLS);
+    dev::tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+// Log-sum-exp merge of the partials of sequences that span several CTAs, and
+// zero rows for empty sequences. One warp per (sequence, query head).
+template <int D>
+__global__ void __launch_bounds__(128)
+    merge_segments_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ part_m,
+                          const float* __restrict__ part_l, const float* __restrict__ part_acc,
+                          const int* __restrict__ ws_plan, int num_q_heads) {
+  constexpr int VPL = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 4 + warp;
+  const int b = blockIdx.y;
+  if (n >= num_q_heads) return;
+  const int R = ws_plan[0];
+  const int pre0 = ws_plan[1 + b], pre1 = ws_plan[2 + b];
+  __nv_bfloat16* o = out + (size_t(b) * num_q_heads + n) * D + lane * VPL;
+  if (pre1 <= pre0) {  // empty sequence
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(0.0f);
+    return;
+  }
+  const int c0 = pre0 / R, c1 = (pre1 - 1) / R;
+  if (c0 == c1) return;  // written whole by the decode kernel
+  float M = -INFINITY;
+  for (int c = c0; c <= c1; ++c) M = fmaxf(M, part_m[size_t(b + c) * num_q_heads + n]);
+  float acc[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) acc[j] = 0.0f;
+  float den = 0.0f;
+  for (int c = c0; c <= c1; ++c) {
+    const size_t sidx = size_t(b + c) * num_q_heads + n;
+    const float wt = dev::fast_exp2(part_m[sidx] - M);
+    den = fmaf(wt, part_l[sidx], den);
+    const float* src = part_acc + sidx * D + lane * VPL;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) acc[j] = fmaf(wt, src[j], acc[j]);
+  }
+  const float inv = __frcp_rn(den);
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(acc[j] * inv);
 }
 
 // ---------------------------------------------------------------- host side
@@ -520,14 +753,14 @@ int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return g_encode ? 0 : int(cudaErrorNotSupported);
 }
 
-// 2-D bf16 tensor [rows][cols] (row pitch cols*2 bytes), box 16 rows x 64 cols, 128B swizzle,
-// out-of-range elements read as zero.
-int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+// 2-D bf16 tensor [rows][cols] (row pitch cols*2 bytes), box box_rows x 64 cols,
+// 128B swizzle, out-of-range elements read as zero.
+int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   if (encode_fn(&enc)) return int(cudaErrorNotSupported);
   cuuint64_t gdim[2] = {cols, rows};
   cuuint64_t gstride[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -535,7 +768,75 @@ int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
   return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
 }
 
-int sm_count() {
+template <int D, int G, int N>
+int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
+  using C = TcCfg<D, N>;
+  const pa_decode_params* p = Lc.p;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, G, N>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return int(e);
+    configured = true;
+  }
+  const int H = p->num_kv_heads;
+  CUtensorMap tk, tv, tq;
+  const uint64_t cache_rows = uint64_t(p->num_blocks) * H * BS;
+  int r = make_map(&tk, p->k_cache, cache_rows, D, uint32_t(BS * H));
+  if (!r) r = make_map(&tv, p->v_cache, cache_rows, D, uint32_t(BS * H));
+  if (!r) r = make_map(&tq, p->q, uint64_t(p->num_seqs) * p->num_q_heads, D, uint32_t(N));
+  if (r) return r;
+  TcParams P;
+  P.block_tables = p->block_tables;
+  P.context_lens = p->context_lens;
+  P.out = static_cast<__nv_bfloat16*>(p->out);
+  P.part_m = Lc.part_m;
+  P.part_l = Lc.part_l;
+  P.part_acc = Lc.part_acc;
+  P.ws_plan = Lc.plan;
+  P.max_blocks_per_seq = p->max_blocks_per_seq;
+  P.num_seqs = p->num_seqs;
+  P.num_kv_heads = H;
+  P.num_q_heads = p->num_q_heads;
+  P.num_blocks = p->num_blocks;
+  P.cap = min(p->max_blocks_per_seq * BS, p->max_context_len);
+  P.oob_row = int(cache_rows);
+  P.scale_log2 = p->scale * kLog2e;
+  paged_decode_tc_kernel<D, G, N><<<Lc.grid, NTHREADS, C::SMEM, stream>>>(tk, tv, tq, P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return int(e);
+  dim3 mgrid((p->num_q_heads + 3) / 4, p->num_seqs);
+  merge_segments_kernel<D><<<mgrid, 128, 0, stream>>>(P.out, P.part_m, P.part_l, P.part_acc,
+                                                      P.ws_plan, p->num_q_heads);
+  return int(cudaGetLastError());
+}
+
+template <int D>
+int dispatch_tc(const DecodeLaunch& Lc, cudaStream_t s) {
+  const int G = Lc.p->num_q_heads / Lc.p->num_kv_heads;
+  const int hq = Lc.p->num_q_heads;
+  const int N = hq <= 16 ? 16 : (hq <= 32 ? 32 : 64);
+  switch (G * 100 + N) {
+    case 116: return launch_tc_t<D, 1, 16>(Lc, s);
+    case 216: return launch_tc_t<D, 2, 16>(Lc, s);
+    case 416: return launch_tc_t<D, 4, 16>(Lc, s);
+    case 432: return launch_tc_t<D, 4, 32>(Lc, s);
+    case 816: return launch_tc_t<D, 8, 16>(Lc, s);
+    case 832: return launch_tc_t<D, 8, 32>(Lc, s);
+    case 864: return launch_tc_t<D, 8, 64>(Lc, s);
+    default: return int(cudaErrorInvalidValue);
+  }
+}
+
+}  // namespace
+
+bool tc_supports(const pa_decode_params* p) {
+  const int H = p->num_kv_heads;
+  return (H == 1 || H == 2 || H == 4 || H == 8) && p->num_q_heads <= 64 &&
+         p->num_seqs <= kTcMaxSeqs;
+}
+
+int tc_grid() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (!g_sm_count[dev]) {
@@ -545,63 +846,6 @@ int sm_count() {
   }
   return g_sm_count[dev];
 }
-
-template <int D, int G>
-int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
-  using C = TcCfg<D>;
-  const pa_decode_params* p = Lc.p;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return int(e);
-    configured = true;
-  }
-  CUtensorMap tk, tv, tq;
-  const uint64_t cache_rows = uint64_t(p->num_blocks) * p->num_kv_heads * BS;
-  int r = make_map(&tk, p->k_cache, cache_rows, D);
-  if (!r) r = make_map(&tv, p->v_cache, cache_rows, D);
-  if (!r) r = make_map(&tq, p->q, uint64_t(p->num_seqs) * p->num_q_heads, D);
-  if (r) return r;
-  TcParams P;
-  P.block_tables = p->block_tables;
-  P.context_lens = p->context_lens;
-  P.out = static_cast<__nv_bfloat16*>(p->out);
-  P.part_m = Lc.part_m;
-  P.part_l = Lc.part_l;
-  P.part_acc = Lc.part_acc;
-  P.counters = Lc.counters;
-  P.max_blocks_per_seq = p->max_blocks_per_seq;
-  P.num_seqs = p->num_seqs;
-  P.num_kv_heads = p->num_kv_heads;
-  P.num_q_heads = p->num_q_heads;
-  P.group = G;
-  P.num_blocks = p->num_blocks;
-  P.max_context_len = p->max_context_len;
-  P.partition_tokens = Lc.partition_tokens;
-  P.num_partitions = Lc.num_partitions;
-  P.total_items = Lc.num_partitions * p->num_seqs * p->num_kv_heads;
-  P.oob_row = int(cache_rows);
-  P.scale_log2 = p->scale * kLog2e;
-  int sms = sm_count();
-  if (sms <= 0) return int(cudaErrorInvalidDevice);
-  const int grid = P.total_items < sms ? P.total_items : sms;
-  paged_decode_tc_kernel<D, G><<<grid, NTHREADS, C::SMEM, stream>>>(tk, tv, tq, P);
-  return int(cudaGetLastError());
-}
-
-template <int D>
-int dispatch_tc(const DecodeLaunch& Lc, cudaStream_t s) {
-  switch (Lc.p->num_q_heads / Lc.p->num_kv_heads) {
-    case 1: return launch_tc_t<D, 1>(Lc, s);
-    case 2: return launch_tc_t<D, 2>(Lc, s);
-    case 4: return launch_tc_t<D, 4>(Lc, s);
-    case 8: return launch_tc_t<D, 8>(Lc, s);
-    default: return int(cudaErrorInvalidValue);
-  }
-}
-
-}  // namespace
 
 int launch_decode_tc(const DecodeLaunch& Lc, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);

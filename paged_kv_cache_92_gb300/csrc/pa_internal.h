@@ -16,24 +16,38 @@ pa_status set_cuda_error(const char* where, int cuda_err);
 constexpr int kBlockSize = 16;
 constexpr int kDefaultPartitionTokens = 512;
 constexpr int kMaxPartitionTokens = 4096;
+// The tensor-core decode kernel plans its stream-K split in shared memory
+// (one int per sequence); larger batches run on the CUDA-core kernel.
+constexpr int kTcMaxSeqs = 16384;
 
 // Resolved decode launch parameters (host validated).
 struct DecodeLaunch {
   const pa_decode_params* p;
-  int partition_tokens;
-  int num_partitions;  // max over sequences, from max_context_len
-  float* part_m;       // [num_seqs][num_q_heads][num_partitions]
-  float* part_l;       // same
-  float* part_acc;     // [num_seqs][num_q_heads][num_partitions][head_dim]
-  unsigned int* counters;  // work counter of the tensor-core kernel (zero at launch)
+  int partition_tokens;  // CUDA-core kernel: split-K partition length
+  int num_partitions;    // CUDA-core kernel: max partitions over sequences
+  int grid;              // tensor-core kernel: persistent CTAs (one per SM)
+  float* part_m;         // partial maxima (layout depends on the kernel)
+  float* part_l;         // partial sums
+  float* part_acc;       // partial weighted sums
+  int* plan;             // tensor-core kernel: stream-K plan for its merge
 };
 
-// Bytes at the start of every decode workspace holding the work counter.
+// Bytes at the start of every decode workspace (reserved).
 constexpr size_t kWorkspaceHeaderBytes = 256;
 
-// Workspace carve-up: counter header, then split-K partials. Returns total bytes.
-size_t decode_workspace_layout(const pa_decode_params* p, int num_partitions, size_t* off_m,
-                               size_t* off_l, size_t* off_acc);
+// Workspace carve-up. Both kernels start after the header; a call uses one.
+struct WorkspaceLayout {
+  size_t total;
+  size_t simt_m, simt_l, simt_acc;    // [seqs][q heads][partitions](+[dim])
+  size_t tc_plan, tc_m, tc_l, tc_acc; // plan, then [seqs + grid][q heads](+[dim])
+};
+WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_partitions,
+                                        int tc_grid);
+
+// Tensor-core kernel: shapes it handles, and its grid (SM count of the current
+// device, or 0 if that cannot be queried).
+bool tc_supports(const pa_decode_params* p);
+int tc_grid();
 
 // Kernel launchers (pa_decode.cu / pa_cache.cu). Return a cudaError_t as int.
 int launch_decode(const DecodeLaunch& L, void* stream);      // CUDA-core decode kernel

@@ -80,14 +80,32 @@ def test_decode_rejects_bad_arguments_on_the_host(pk, kw, status):
     assert lib.pa_last_error()
 
 
+def _ru(x):
+    return (x + 255) // 256 * 256
+
+
+def _expected_ws(B, Hq, D, parts, grid):
+    simt = 0
+    if parts > 1:
+        rows = B * Hq * parts
+        simt = 2 * _ru(rows * 4) + _ru(rows * D * 4)
+    rows = (B + grid) * Hq
+    tc = _ru((B + 2) * 4) + 2 * _ru(rows * 4) + _ru(rows * D * 4)
+    return 256 + max(simt, tc)
+
+
 def test_decode_workspace_size(pk):
+    """Header + the larger of the CUDA-core per-partition partials and the
+    tensor-core plan + per-(sequence, SM) partials. Without a GPU the SM count
+    used for sizing is 256."""
     lib = pk.load()
-    # max context 64 <= one 512-token partition: only the 256-byte counter header
-    assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk))) == 256
+    got = lib.pa_decode_workspace_size(ctypes.byref(_params(pk)))
+    assert got == _expected_ws(2, 8, 128, 1, 256)
     p = _params(pk, max_context_len=2048, max_blocks_per_seq=128)
-    rows = 2 * 8 * 4  # seqs * q heads * partitions
-    want = 256 + 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256
-    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == want
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(2, 8, 128, 4, 256)
+    p = _params(pk, num_seqs=64, num_q_heads=32, num_kv_heads=8, max_context_len=32768,
+                max_blocks_per_seq=2048)
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 64, 256)
     assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk, head_dim=96))) == 0
 
 

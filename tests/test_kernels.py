@@ -325,3 +325,21 @@ def test_scale_is_applied(pk, variant):
     ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens, scale=0.3)
     harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
     assert not math.isclose(0.3, 1 / 8)
+
+
+def test_batch_beyond_the_tensor_core_plan_runs_and_matches(pk):
+    """More sequences than the tensor-core kernel plans in shared memory: the
+    call still succeeds (CUDA-core kernel) and matches the oracle."""
+    import torch
+
+    rng = np.random.default_rng(21)
+    lens = rng.integers(1, 40, size=2100)
+    q, kc, vc, tables, lens, _ = _direct_case(lens, 8, 2, 64, seed=23)
+    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=int(lens.max()), partition_tokens=16, variant=0)
+    torch.cuda.synchronize()
+    units = harness.sample_units(len(lens), 8, 300, seed=5)
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens, units=units)
+    got = harness.bf16_tensor_to_f64(out)
+    harness.assert_close(np.stack([got[b, h] for b, h in units]), ref)
+    _check_errors(pk)
