@@ -65,6 +65,9 @@ constexpr int kCons = NCONS * 32;
 constexpr int kGroups = ROWS / BS;  // 16-row groups per chunk: (block, KV head)
 constexpr int kMaxDynSmem = 232448;
 constexpr float kLog2e = 1.4426950408889634f;
+// The softmax reference maximum moves only when a score exceeds it by more
+// than this (log2 units, a factor of 256); values of P stay <= 256.
+constexpr float kRescaleLog2 = 8.0f;
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_WHOLE = 4, F_END = 8 };
 
@@ -203,6 +206,8 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
     }
     if (c < s_pos && c != end_pos && dev::mbar_test(bar_p, uint32_t(c) & 1u)) {
       const int sl = c % C::ST;
+      // O accumulates over a segment's chunks; its first chunk starts afresh
+      const bool fresh = (meta[sl].flags & F_FIRST) != 0;
       dev::tc_fence_after();
       const uint32_t vb = dev::smem_addr(ring + size_t(sl) * C::SLOT_BYTES + C::K_BYTES);
 #pragma unroll
@@ -211,7 +216,7 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
                       dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
                       dev::smem_desc(pbs + (kk >> 2) * C::PH_BYTES + (kk & 3) * 32, 16, 1024,
                                      dev::kSwizzle128B),
-                      C::IDESC_PV, kk > 0);
+                      C::IDESC_PV, kk > 0 || !fresh);
       }
       dev::mma_commit(bar_o);
       dev::mma_commit(&empty[sl]);
@@ -271,18 +276,17 @@ struct Softmax {
     const uint32_t t_lane = uint32_t(cw * 32) << 16;
     const uint32_t tO = tmem + t_lane + 2 * N;
 
-    float m_run[G], l_part[G];
-    float acc[N];
+    // Reference maximum per query head (log2 domain) and this row's share of
+    // the softmax sum relative to it. O^T accumulates in TMEM relative to the
+    // same reference; the reference is raised (and O^T, l rescaled) only when
+    // a chunk's maximum exceeds it by more than kRescaleLog2.
+    float m_ref[G], l_part[G];
 #pragma unroll
     for (int j = 0; j < G; ++j) {
-      m_run[j] = -INFINITY;
+      m_ref[j] = -INFINITY;
       l_part[j] = 0.0f;
     }
-#pragma unroll
-    for (int n = 0; n < N; ++n) acc[n] = 0.0f;
-    int c = 0;          // ring position
-    int r = 0;          // real chunks handled
-    bool pend = false;  // chunk r-1's O^T not yet folded into acc
+    int c = 0;  // ring position = chunk index
     bool ok = true;
 
     for (;;) {
@@ -295,11 +299,11 @@ struct Softmax {
         break;
       }
       if (m.flags & F_END) break;
-      const int buf = r & 1;
-      float* redb = red + buf * (kGroups * 8);
+      const int buf = c & 1;
+      const bool first = (m.flags & F_FIRST) != 0;
 
       // ---- scores of this chunk -> registers
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(r >> 1) & 1u)) && ok;
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(c >> 1) & 1u)) && ok;
       dev::tc_fence_after();
       float s[LDC];
       if constexpr (LDC == 8) {
@@ -308,10 +312,10 @@ struct Softmax {
         dev::tmem_ld16(tmem + t_lane + buf * N + col0, s);
       }
 
-      // ---- running softmax: row = (block u, head h, key)
+      // ---- chunk maximum per query head: row = (block u, head h, key)
       const int t = m.tok0 + u * BS + key;
       const bool valid = u < m.nblk && t < m.L;
-      float x[G];
+      float x[G], cm[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const float sj = upper ? s[(LDC >= 2 * G ? G : 0) + j] : s[j];
@@ -319,37 +323,59 @@ struct Softmax {
         float v = x[j];
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-        if (key == 0) redb[grp * 8 + j] = v;
+        cm[j] = v;
       }
-      if (!dev::named_barrier_and(1, kCons, ok && *abort_flag == 0)) {
-        ok = false;
-        break;
-      }
-
-      // ---- fold chunk r-1's O^T (its value MMA must be done before P is rewritten)
-      if (pend) {
-        ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(r - 1) & 1u)) && ok;
-        dev::tc_fence_after();
-        float o[N];
-        dev::tmem_ld_cols<N>(tO, o);
-        const float* al = alpha_s + ((r - 1) & 1) * 64;
+      if (U > 1) {  // the head's rows span several 16-row groups of the chunk
+        if (key == 0) {
 #pragma unroll
-        for (int n = 0; n < N; ++n) acc[n] = fmaf(acc[n], al[n], o[n]);
-        pend = false;
+          for (int j = 0; j < G; ++j) red[grp * 8 + j] = cm[j];
+        }
+        dev::named_barrier(1, kCons);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          float v = -INFINITY;
+          for (int uu = 0; uu < U; ++uu) v = fmaxf(v, red[(uu * H + h) * 8 + j]);
+          cm[j] = v;
+        }
       }
+      bool need = false;
+#pragma unroll
+      for (int j = 0; j < G; ++j) need |= cm[j] > m_ref[j] + kRescaleLog2;
+
+      // ---- raise the reference where needed; rescale l and (in TMEM) O^T
+      bool waited_prev = false;
+      if (dev::named_barrier_or(1, kCons, need)) {
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float nr = cm[j] > m_ref[j] + kRescaleLog2 ? cm[j] : m_ref[j];
+          const float f = dev::fast_exp2(m_ref[j] - nr);  // 0 from -inf, 1 if unchanged
+          l_part[j] *= f;
+          m_ref[j] = nr;
+          if (u == 0 && key == 0) alpha_s[h * G + j] = f;
+        }
+        if (!first) {
+          // chunk c-1's value product must be in O^T before it is scaled
+          ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(c - 1) & 1u)) && ok;
+          waited_prev = true;
+          dev::named_barrier(1, kCons);  // every factor is written
+          dev::tc_fence_after();
+          float o[N];
+          dev::tmem_ld_cols<N>(tO, o);
+#pragma unroll
+          for (int n = 0; n < N; ++n) o[n] *= alpha_s[n];
+          dev::tmem_st_cols<N>(tO, o);
+        }
+      }
+      // P of chunk c-1 must have been consumed before P is rewritten
+      if (!first && !waited_prev)
+        ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(c - 1) & 1u)) && ok;
 
 #pragma unroll
       for (int j = 0; j < G; ++j) {
-        float cmax = -INFINITY;
-        for (int uu = 0; uu < U; ++uu) cmax = fmaxf(cmax, redb[(uu * H + h) * 8 + j]);
-        const float m_new = fmaxf(m_run[j], cmax);
-        const float alpha = dev::fast_exp2(m_run[j] - m_new);
-        m_run[j] = m_new;
-        const float p = dev::fast_exp2(x[j] - m_new);
-        l_part[j] = fmaf(l_part[j], alpha, p);
-        const int n = h * G + j;
-        *reinterpret_cast<__nv_bfloat16*>(pbuf + p_offset<N>(n, ctid)) = __float2bfloat16_rn(p);
-        if (u == 0 && key == 0) alpha_s[buf * 64 + n] = alpha;
+        const float p = dev::fast_exp2(x[j] - m_ref[j]);
+        l_part[j] += p;
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + p_offset<N>(h * G + j, ctid)) =
+            __float2bfloat16_rn(p);
       }
       // A masked row inside a loaded block (the sequence's last, partial
       // block) may hold anything, NaN included: clear its V row so 0 * V = 0.
@@ -364,7 +390,7 @@ struct Softmax {
       }
       dev::fence_async_smem();
       dev::tc_fence_before();
-      dev::mbar_arrive(bar_p);  // P(r) written, S(r) and O(r-1) read
+      dev::mbar_arrive(bar_p);  // P(c) written; S(c) read; O^T rescaled
 
       if (m.flags & F_LAST) {
         // per query head: softmax denominator over all rows of its KV head
@@ -375,37 +401,32 @@ struct Softmax {
           for (int o2 = 8; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
           if (key == 0) red2[grp * 8 + j] = v;
         }
-        ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(r) & 1u)) && ok;
-        dev::tc_fence_after();
-        float o[N];
-        dev::tmem_ld_cols<N>(tO, o);
-        dev::named_barrier(1, kCons);  // every alpha and l of this chunk is written
-        {
-          const float* al = alpha_s + buf * 64;
-#pragma unroll
-          for (int n = 0; n < N; ++n) acc[n] = fmaf(acc[n], al[n], o[n]);
-        }
+        dev::named_barrier(1, kCons);
         if (u == 0 && key == 0) {
 #pragma unroll
           for (int j = 0; j < G; ++j) {
             float l = 0.0f;
             for (int uu = 0; uu < U; ++uu) l += red2[(uu * H + h) * 8 + j];
             l_s[h * G + j] = l;
-            m_s[h * G + j] = m_run[j];
+            m_s[h * G + j] = m_ref[j];
           }
         }
-        dev::named_barrier(1, kCons);
+        ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(c) & 1u)) && ok;
+        dev::tc_fence_after();
+        float o[N];
+        dev::tmem_ld_cols<N>(tO, o);
+        dev::named_barrier(1, kCons);  // l_s, m_s written
         if (ctid < D) {
           if (m.flags & F_WHOLE) {
             __nv_bfloat16* o_row = P.out + size_t(m.b) * Hq * D + ctid;
 #pragma unroll
             for (int n = 0; n < N; ++n)
-              if (n < Hq) o_row[size_t(n) * D] = __float2bfloat16_rn(acc[n] * __frcp_rn(l_s[n]));
+              if (n < Hq) o_row[size_t(n) * D] = __float2bfloat16_rn(o[n] * __frcp_rn(l_s[n]));
           } else {
             float* a_row = P.part_acc + size_t(m.seg) * Hq * D + ctid;
 #pragma unroll
             for (int n = 0; n < N; ++n)
-              if (n < Hq) a_row[size_t(n) * D] = acc[n];
+              if (n < Hq) a_row[size_t(n) * D] = o[n];
             if (ctid < Hq) {
               P.part_m[size_t(m.seg) * Hq + ctid] = m_s[ctid];
               P.part_l[size_t(m.seg) * Hq + ctid] = l_s[ctid];
@@ -415,15 +436,10 @@ struct Softmax {
         dev::tc_fence_before();
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-          m_run[j] = -INFINITY;
+          m_ref[j] = -INFINITY;
           l_part[j] = 0.0f;
         }
-#pragma unroll
-        for (int n = 0; n < N; ++n) acc[n] = 0.0f;
-      } else {
-        pend = true;
       }
-      ++r;
       ++c;
     }
     if (!ok && ctid == 0) {

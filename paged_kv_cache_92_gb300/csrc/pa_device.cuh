@@ -280,6 +280,42 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NC]) {
   for (int i = 0; i < NC; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Store NC consecutive 32-bit columns of this thread's TMEM lane (x16 stores).
+template <int NC>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float (&v)[NC]) {
+  static_assert(NC % 16 == 0, "multiple of 16 columns");
+#pragma unroll
+  for (int c = 0; c < NC; c += 16) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr + uint32_t(c)),
+        "r"(__float_as_uint(v[c + 0])), "r"(__float_as_uint(v[c + 1])),
+        "r"(__float_as_uint(v[c + 2])), "r"(__float_as_uint(v[c + 3])),
+        "r"(__float_as_uint(v[c + 4])), "r"(__float_as_uint(v[c + 5])),
+        "r"(__float_as_uint(v[c + 6])), "r"(__float_as_uint(v[c + 7])),
+        "r"(__float_as_uint(v[c + 8])), "r"(__float_as_uint(v[c + 9])),
+        "r"(__float_as_uint(v[c + 10])), "r"(__float_as_uint(v[c + 11])),
+        "r"(__float_as_uint(v[c + 12])), "r"(__float_as_uint(v[c + 13])),
+        "r"(__float_as_uint(v[c + 14])), "r"(__float_as_uint(v[c + 15]))
+        : "memory");
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Named barrier that ORs a predicate across `count` threads.
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(out)
+      : "r"(uint32_t(pred)), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+
 // Named barrier over `count` threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
   uint32_t out;
