@@ -178,7 +178,7 @@ def setup_workload(r: workloads.Recipe, device, n_copies: int):
                 copies=copies)
 
 
-def make_plans(pk, W, device, partition_tokens=0, variant=0):
+def make_plans(pk, W, device, partition_tokens=0, variant=0, overlap=True):
     import torch
 
     lib = pk.load()
@@ -194,7 +194,8 @@ def make_plans(pk, W, device, partition_tokens=0, variant=0):
     for kc, vc in W["copies"]:
         p = pk.make_decode_params(W["q"], out, kc, vc, tables_d, lens_d,
                                   max_context_len=int(W["lens"].max()),
-                                  partition_tokens=partition_tokens, variant=variant)
+                                  partition_tokens=partition_tokens, variant=variant,
+                                  overlap_prologue=overlap)
         need = pk.pa_decode_workspace_size(p)
         if ws is None and need:
             ws = torch.empty(need, dtype=torch.uint8, device=device)
@@ -222,7 +223,8 @@ def run_ours(args, rank: int, world: int) -> dict:
     pk.load()
     r = workloads.llama8b_layer()
     W = setup_workload(r, device, n_copies=3)
-    plans, out, keep = make_plans(pk, W, device, variant=args.variant)
+    plans, out, keep = make_plans(pk, W, device, variant=args.variant,
+                                  overlap=not args.no_overlap)
     lens = W["lens"]
     dec_b = decode_bytes(lens, r.num_q_heads, r.num_kv_heads, r.head_dim)
     step_b = dec_b + append_bytes(len(W["slots"]), r.num_kv_heads, r.head_dim) + \
@@ -274,7 +276,8 @@ def run_ours(args, rank: int, world: int) -> dict:
 
     # end to end through the public Python API: pinned host inputs -> device,
     # step, result -> pinned host, every step
-    e2e = run_e2e(pk, W, r, device, args.steps, args.warmup, step_b, args.variant)
+    e2e = run_e2e(pk, W, r, device, args.steps, args.warmup, step_b, args.variant,
+                  overlap=not args.no_overlap)
 
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -311,7 +314,8 @@ def run_ours(args, rank: int, world: int) -> dict:
     return res
 
 
-def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int = 0) -> dict:
+def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int = 0,
+            overlap: bool = True) -> dict:
     import torch
 
     host = {k: W[k] for k in ("tables", "lens", "slots")}
@@ -344,8 +348,9 @@ def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int
                                       variant=variant)
             n = pk.pa_decode_workspace_size(p)
             ws["ws"] = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None
+        # tables and lengths arrived before the first kernel of the step
         pk.pa_decode(dev["q"], kc, vc, dev["tables"], dev["lens"], max_ctx, out=out_d,
-                     workspace=ws["ws"], variant=variant)
+                     workspace=ws["ws"], variant=variant, overlap_prologue=overlap)
         out_h.copy_(out_d, non_blocking=True)
 
     for i in range(warmup):
@@ -452,6 +457,9 @@ def main(argv=None) -> int:
                     help="untimed loaded seconds before the timed region (clock sampling)")
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch the decode in plain stream order instead of overlapping its "
+                         "set-up with the KV write")
     ap.add_argument("--variant", type=int, default=0, choices=[0, 1],
                     help="decode kernel: 0 tensor-core (default), 1 CUDA-core")
     args = ap.parse_args(argv)

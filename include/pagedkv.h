@@ -129,6 +129,12 @@ typedef struct {
   int32_t partition_tokens;    /* split-K partition length; 0 = 512; else a multiple of
                                   block_size in [block_size, 4096] */
   int32_t variant;             /* PA_DECODE_TENSOR_CORE (default) or PA_DECODE_CUDA_CORE */
+  int32_t overlap_prologue;    /* nonzero: context_lens and block_tables were final before the
+                                  previous kernel on `stream` began (e.g. uploaded once per step),
+                                  so the tensor-core kernel may read them -- and plan its work --
+                                  while that kernel still runs (programmatic dependent launch).
+                                  q, the caches and every output are touched only after the
+                                  previous kernel has completed. 0 = plain stream order. */
 } pa_decode_params;
 
 /* Decode kernel variants; both compute the same function. The tensor-core

@@ -61,7 +61,7 @@ class DecodeParams(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("num_blocks", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
         ("scale", ctypes.c_float), ("partition_tokens", ctypes.c_int32),
-        ("variant", ctypes.c_int32),
+        ("variant", ctypes.c_int32), ("overlap_prologue", ctypes.c_int32),
     ]
 
 
@@ -160,7 +160,8 @@ def _stream_handle(stream) -> Optional[int]:
 
 def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
                        max_context_len: int, scale: Optional[float] = None,
-                       partition_tokens: int = 0, variant: int = DECODE_TENSOR_CORE) -> DecodeParams:
+                       partition_tokens: int = 0, variant: int = DECODE_TENSOR_CORE,
+                       overlap_prologue: bool = False) -> DecodeParams:
     import torch
 
     B, Hq, D = q.shape
@@ -183,6 +184,7 @@ def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
     p.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
     p.partition_tokens = int(partition_tokens)
     p.variant = int(variant)
+    p.overlap_prologue = int(bool(overlap_prologue))
     return p
 
 
@@ -192,7 +194,8 @@ def pa_decode_workspace_size(params: DecodeParams) -> int:
 
 def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
               scale: Optional[float] = None, partition_tokens: int = 0, out=None,
-              workspace=None, stream=None, variant: int = DECODE_TENSOR_CORE):
+              workspace=None, stream=None, variant: int = DECODE_TENSOR_CORE,
+              overlap_prologue: bool = False):
     """Paged decode attention; returns ``out`` (bf16 [B][Hq][d]).
 
     ``workspace`` is a uint8 CUDA tensor of at least
@@ -204,7 +207,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
     if out is None:
         out = torch.empty_like(q)
     p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
-                           max_context_len, scale, partition_tokens, variant)
+                           max_context_len, scale, partition_tokens, variant, overlap_prologue)
     need = int(lib.pa_decode_workspace_size(ctypes.byref(p)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

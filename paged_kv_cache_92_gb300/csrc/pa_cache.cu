@@ -11,6 +11,7 @@
 
 #include <cstdint>
 
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -26,6 +27,9 @@ __global__ void __launch_bounds__(256)
                              uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                              const int64_t* __restrict__ slot_mapping, int64_t num_chunks,
                              int num_kv_heads, int chunks_per_row, int64_t num_slots) {
+  // a decode launched as a programmatic dependent may start its set-up now;
+  // it waits for this kernel before it reads the cache
+  dev::griddep_launch_dependents();
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= num_chunks) return;
   const int c = int(idx % chunks_per_row);

@@ -101,8 +101,8 @@ struct TcCfg {
   static constexpr int OFF_Q = ST * SLOT_BYTES;
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_MISC = OFF_P + P_BYTES;
-  // full[ST] empty[ST] qempty[2] s[2] o p drain
-  static constexpr int NBARS = 2 * ST + 7;
+  // full[ST] empty[ST] qempty[2] s[3] o p drain
+  static constexpr int NBARS = 2 * ST + 8;
   static constexpr int OFF_BARS = OFF_MISC;
   static constexpr int OFF_META = OFF_BARS + (NBARS * 8 + 15) / 16 * 16;
   static constexpr int OFF_RED = OFF_META + ST * int(sizeof(ChunkMeta));  // [2][8 groups][8]
@@ -114,7 +114,8 @@ struct TcCfg {
   static constexpr int SMEM = OFF_WORDS + 64 + 1024;  // + alignment slack
   static_assert(OFF_WORDS + 64 <= OFF_MISC + MISC_BYTES, "misc area");
   static_assert(SMEM <= kMaxDynSmem, "shared memory budget");
-  static constexpr int TMEM_COLS = 4 * N;  // S double buffer [0, 2N), O at [2N, 3N)
+  static constexpr int TMEM_COLS = 4 * N;  // S triple buffer [0, 3N), O at [3N, 4N)
+  static constexpr int kSBufs = 3;
   static constexpr uint32_t IDESC_S = dev::idesc_bf16_f32(ROWS, N, false, false);
   static constexpr uint32_t IDESC_PV = dev::idesc_bf16_f32(ROWS, N, true, false);
   static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
@@ -188,22 +189,7 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
   uint64_t t_progress = dev::global_timer_ns();
   for (;;) {
     bool progress = false;
-    if (end_pos < 0 && s_pos <= c + 1 &&
-        dev::mbar_test(&full[s_pos % C::ST], uint32_t(s_pos / C::ST) & 1u)) {
-      const int sl = s_pos % C::ST;
-      const ChunkMeta mn = meta[sl];
-      if (mn.flags & F_END) {
-        end_pos = s_pos;
-      } else {
-        dev::tc_fence_after();
-        issue_scores<D, N>(tmem + (s_pos & 1) * N, ring + size_t(sl) * C::SLOT_BYTES,
-                           qbuf + mn.qslot * C::Q_BYTES);
-        dev::mma_commit(&bar_s[s_pos & 1]);
-        if (mn.flags & F_LAST) dev::mma_commit(&qempty[mn.qslot]);
-      }
-      ++s_pos;
-      progress = true;
-    }
+    // value product first: it frees a ring slot for the producer
     if (c < s_pos && c != end_pos && dev::mbar_test(bar_p, uint32_t(c) & 1u)) {
       const int sl = c % C::ST;
       // O accumulates over a segment's chunks; its first chunk starts afresh
@@ -212,7 +198,7 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       const uint32_t vb = dev::smem_addr(ring + size_t(sl) * C::SLOT_BYTES + C::K_BYTES);
 #pragma unroll
       for (int kk = 0; kk < ROWS / 16; ++kk) {
-        dev::mma_bf16(tmem + 2 * N,
+        dev::mma_bf16(tmem + C::kSBufs * N,
                       dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
                       dev::smem_desc(pbs + (kk >> 2) * C::PH_BYTES + (kk & 3) * 32, 16, 1024,
                                      dev::kSwizzle128B),
@@ -221,6 +207,25 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       dev::mma_commit(bar_o);
       dev::mma_commit(&empty[sl]);
       ++c;
+      progress = true;
+    }
+    // scores of the next positions as soon as their data has landed, up to
+    // two positions ahead of the value products (S is triple-buffered)
+    if (end_pos < 0 && s_pos <= c + 2 &&
+        dev::mbar_test(&full[s_pos % C::ST], uint32_t(s_pos / C::ST) & 1u)) {
+      const int sl = s_pos % C::ST;
+      const ChunkMeta mn = meta[sl];
+      if (mn.flags & F_END) {
+        end_pos = s_pos;
+      } else {
+        const int sb = s_pos % C::kSBufs;
+        dev::tc_fence_after();
+        issue_scores<D, N>(tmem + sb * N, ring + size_t(sl) * C::SLOT_BYTES,
+                           qbuf + mn.qslot * C::Q_BYTES);
+        dev::mma_commit(&bar_s[sb]);
+        if (mn.flags & F_LAST) dev::mma_commit(&qempty[mn.qslot]);
+      }
+      ++s_pos;
       progress = true;
     }
     if (c == end_pos) break;
@@ -274,7 +279,7 @@ struct Softmax {
     const int col0 = H >= 2 ? h0 * G : 0;
     const bool upper = H >= 2 && lane >= 16;  // this lane's head is the warp's second
     const uint32_t t_lane = uint32_t(cw * 32) << 16;
-    const uint32_t tO = tmem + t_lane + 2 * N;
+    const uint32_t tO = tmem + t_lane + C::kSBufs * N;
 
     // Reference maximum per query head (log2 domain) and this row's share of
     // the softmax sum relative to it. O^T accumulates in TMEM relative to the
@@ -299,11 +304,11 @@ struct Softmax {
         break;
       }
       if (m.flags & F_END) break;
-      const int buf = c & 1;
+      const int buf = c % C::kSBufs;
       const bool first = (m.flags & F_FIRST) != 0;
 
       // ---- scores of this chunk -> registers
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(c >> 1) & 1u)) && ok;
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(c / C::kSBufs) & 1u)) && ok;
       dev::tc_fence_after();
       float s[LDC];
       if constexpr (LDC == 8) {
@@ -466,8 +471,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + C::ST;
   uint64_t* qempty = bars + 2 * C::ST;
-  uint64_t* bar_s = bars + 2 * C::ST + 2;  // [2] scores ready
-  uint64_t* bar_o = bar_s + 2;              // value product ready
+  uint64_t* bar_s = bars + 2 * C::ST + 2;  // [3] scores ready
+  uint64_t* bar_o = bar_s + 3;              // value product ready
   uint64_t* bar_p = bar_o + 1;              // P written by all 128 softmax threads
   uint64_t* drain = bar_p + 1;
   ChunkMeta* meta = reinterpret_cast<ChunkMeta*>(smem + C::OFF_META);
@@ -492,10 +497,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       dev::mbar_init(&full[i], 1);
       dev::mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      dev::mbar_init(&qempty[i], 1);
-      dev::mbar_init(&bar_s[i], 1);
-    }
+    for (int i = 0; i < 2; ++i) dev::mbar_init(&qempty[i], 1);
+    for (int i = 0; i < 3; ++i) dev::mbar_init(&bar_s[i], 1);
     dev::mbar_init(bar_o, 1);
     dev::mbar_init(bar_p, kCons);
     dev::mbar_init(drain, 1);
@@ -555,12 +558,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     b_start = lo;
   }
   const int off_start = u0 < u1 ? u0 - pre[b_start] : 0;
-  if (blockIdx.x == 0) {
+  // the merge kernel (a programmatic dependent) may launch; it waits for us
+  if (tid == 0) dev::griddep_launch_dependents();
+  for (int i = tid; i < 128; i += NTHREADS) alpha_s[i] = 1.0f;  // padded columns stay 1
+  if (warp == 0) dev::tmem_alloc(tmem_slot, C::TMEM_COLS);
+  // Everything above read only context_lens (and shared memory). When this
+  // kernel overlaps the previous one, that is all it may touch before
+  // waiting; the producer also fetches its first block-table window first.
+  int win0 = -1, len0 = 0;
+  if (warp == kProducerWarp && u0 < u1) {
+    const int j = off_start + lane;
+    win0 = j < P.max_blocks_per_seq
+               ? P.block_tables[size_t(b_start) * P.max_blocks_per_seq + j] : -1;
+    len0 = min(P.context_lens[b_start], P.cap);
+  }
+  dev::griddep_wait();
+  if (blockIdx.x == 0) {  // the stream-K plan, for the merge kernel
     for (int i = tid; i <= B; i += NTHREADS) P.ws_plan[1 + i] = pre[i];
     if (tid == 0) P.ws_plan[0] = R;
   }
-  for (int i = tid; i < 128; i += NTHREADS) alpha_s[i] = 1.0f;  // padded columns stay 1
-  if (warp == 0) dev::tmem_alloc(tmem_slot, C::TMEM_COLS);
   dev::fence_async_smem();
   dev::tc_fence_before();
   __syncthreads();  // the ring is free for TMA from here on
@@ -586,8 +602,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                  ? P.block_tables[size_t(b) * P.max_blocks_per_seq + j] : -1;
     };
     int b = b_start, off = off_start, unit = u0;
-    int win = load_window(b, off);
-    int L_cur = b < B ? min(P.context_lens[b], P.cap) : 0;
+    int win = win0;
+    int L_cur = len0;
     while (ok && unit < u1) {
       if (*abort_flag) break;
       const int nb = L_cur > 0 ? (L_cur + BS - 1) / BS : 0;
@@ -717,6 +733,7 @@ __global__ void __launch_bounds__(128)
                           const float* __restrict__ part_l, const float* __restrict__ part_acc,
                           const int* __restrict__ ws_plan, int num_q_heads) {
   constexpr int VPL = D / 32;
+  dev::griddep_wait();  // launched as a programmatic dependent of the decode
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 4 + warp;
   const int b = blockIdx.y;
@@ -818,13 +835,33 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.cap = min(p->max_blocks_per_seq * BS, p->max_context_len);
   P.oob_row = int(cache_rows);
   P.scale_log2 = p->scale * kLog2e;
-  paged_decode_tc_kernel<D, G, N><<<Lc.grid, NTHREADS, C::SMEM, stream>>>(tk, tv, tq, P);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Lc.grid);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // overlap the set-up with the previous kernel only when the caller says
+  // context_lens and block_tables were final before that kernel began
+  attr[0].val.programmaticStreamSerializationAllowed = p->overlap_prologue ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<D, G, N>, tk, tv, tq, P);
   if (e != cudaSuccess) return int(e);
-  dim3 mgrid((p->num_q_heads + 3) / 4, p->num_seqs);
-  merge_segments_kernel<D><<<mgrid, 128, 0, stream>>>(P.out, P.part_m, P.part_l, P.part_acc,
-                                                      P.ws_plan, p->num_q_heads);
-  return int(cudaGetLastError());
+  // the merge launches while the decode drains and waits for it on the device
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3((p->num_q_heads + 3) / 4, p->num_seqs);
+  mcfg.blockDim = dim3(128);
+  mcfg.stream = stream;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  e = cudaLaunchKernelEx(&mcfg, merge_segments_kernel<D>, P.out,
+                         static_cast<const float*>(P.part_m), static_cast<const float*>(P.part_l),
+                         static_cast<const float*>(P.part_acc),
+                         static_cast<const int*>(P.ws_plan), p->num_q_heads);
+  return int(e);
 }
 
 template <int D>

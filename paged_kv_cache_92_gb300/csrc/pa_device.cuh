@@ -91,6 +91,15 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
   return false;
 }
 
+// Programmatic dependent launch. launch_dependents: the next kernel on the
+// stream (if launched as a programmatic dependent) may start now. wait: block
+// until the preceding kernel has completed and its memory is visible (a no-op
+// when this kernel was launched normally).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // L2 policy for data that is streamed once (K/V tiles).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;

@@ -58,7 +58,8 @@ def build_case(r: workloads.Recipe, device: str = "cuda") -> Case:
                 slm, cwm, q, kn, vn, kc, vc)
 
 
-def run_step_gpu(case: Case, partition_tokens: int = 0, variant: int = 0):
+def run_step_gpu(case: Case, partition_tokens: int = 0, variant: int = 0,
+                 overlap_prologue: bool = False):
     """The hot path on the GPU: copy_blocks -> reshape_and_cache -> decode."""
     import torch
 
@@ -66,12 +67,16 @@ def run_step_gpu(case: Case, partition_tokens: int = 0, variant: int = 0):
 
     dev = case.q.device
     kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    # tables and lengths are uploaded before the first kernel of the step, as
+    # overlap_prologue requires
+    tables = torch.from_numpy(case.tables).to(dev)
+    lens = torch.from_numpy(case.lens).to(dev)
     if len(case.cows):
         pk.pa_copy_blocks(kc, vc, torch.from_numpy(case.cows).to(dev))
     pk.pa_reshape_and_cache(case.k_new, case.v_new, kc, vc, torch.from_numpy(case.slots).to(dev))
-    out = pk.pa_decode(case.q, kc, vc, torch.from_numpy(case.tables).to(dev),
-                       torch.from_numpy(case.lens).to(dev), max_context_len=int(case.lens.max()),
-                       partition_tokens=partition_tokens, variant=variant)
+    out = pk.pa_decode(case.q, kc, vc, tables, lens, max_context_len=int(case.lens.max()),
+                       partition_tokens=partition_tokens, variant=variant,
+                       overlap_prologue=overlap_prologue)
     torch.cuda.synchronize()
     return out, kc, vc
 

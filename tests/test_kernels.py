@@ -343,3 +343,49 @@ def test_batch_beyond_the_tensor_core_plan_runs_and_matches(pk):
     got = harness.bf16_tensor_to_f64(out)
     harness.assert_close(np.stack([got[b, h] for b, h in units]), ref)
     _check_errors(pk)
+
+
+# ---------------------------------------------------------------- overlapped set-up
+
+def test_overlapped_prologue_is_bit_identical_to_stream_order(pk):
+    """overlap_prologue lets the decode plan its work while the KV write is
+    still running (programmatic dependent launch). It must read the cache only
+    after the write: the new token of every sequence is in the result, and the
+    output equals the plain stream-ordered launch bit for bit, step after step."""
+    import torch
+
+    case = harness.build_case(workloads.llama8b_layer(), "cuda")
+    want, _, _ = harness.run_step_gpu(case)
+    for _ in range(3):
+        got, _, _ = harness.run_step_gpu(case, overlap_prologue=True)
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    units = harness.sample_units(case.q.shape[0], case.q.shape[1], 64, seed=3)
+    ref, _, _ = harness.run_step_oracle(case, units=units)
+    g = harness.bf16_tensor_to_f64(want)
+    harness.assert_close(np.stack([g[b, h] for b, h in units]), ref)
+    _check_errors(pk)
+
+
+def test_overlapped_decodes_back_to_back_keep_their_partials(pk):
+    """Two overlapped decodes in a row on one workspace (two layers of a
+    step): the second must not write its plan or partials before the first
+    one's merge has read them."""
+    import torch
+
+    case = harness.build_case(workloads.llama8b_layer(), "cuda")
+    tables = torch.from_numpy(case.tables).cuda()
+    lens = torch.from_numpy(case.lens).cuda()
+    q2 = workloads.bf16_normal(tuple(case.q.shape), 99, "cuda")
+    mx = int(case.lens.max())
+    p = pk.make_decode_params(case.q, torch.empty_like(case.q), case.k_cache, case.v_cache,
+                              tables, lens, max_context_len=mx, overlap_prologue=True)
+    ws = torch.empty(pk.pa_decode_workspace_size(p), dtype=torch.uint8, device="cuda")
+    plain = [pk.pa_decode(q, case.k_cache, case.v_cache, tables, lens, max_context_len=mx,
+                          workspace=ws) for q in (case.q, q2)]
+    for _ in range(3):
+        got = [pk.pa_decode(q, case.k_cache, case.v_cache, tables, lens, max_context_len=mx,
+                            workspace=ws, overlap_prologue=True) for q in (case.q, q2)]
+        torch.cuda.synchronize()
+        for a, b in zip(got, plain):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    _check_errors(pk)
