@@ -135,13 +135,15 @@ class ClockSampler:
 class StepPlan:
     """Pre-marshalled C-ABI calls for one step on one KV-pool copy."""
 
-    def __init__(self, pk, lib, dec_params, ws_ptr, ws_bytes, rc_args, cow_args, stream):
+    def __init__(self, pk, lib, dec_params, ws_ptr, ws_bytes, rc_args, cow_args, stream,
+                 append=None):
         self.pk, self.lib = pk, lib
         self.dec = dec_params
         self.ws_ptr, self.ws_bytes = ws_ptr, ws_bytes
         self.rc_args = rc_args
         self.cow_args = cow_args
         self.stream = stream
+        self.append = append  # AppendParams: KV write fused into the decode launch
 
     def run(self, ev_dec=None):
         lib = self.lib
@@ -149,14 +151,19 @@ class StepPlan:
             st = lib.pa_copy_blocks(*self.cow_args, self.stream)
             if st:
                 raise RuntimeError(f"pa_copy_blocks failed: {st}")
-        st = lib.pa_reshape_and_cache(*self.rc_args, self.stream)
-        if st:
-            raise RuntimeError(f"pa_reshape_and_cache failed: {st}")
+        if self.append is None:
+            st = lib.pa_reshape_and_cache(*self.rc_args, self.stream)
+            if st:
+                raise RuntimeError(f"pa_reshape_and_cache failed: {st}")
         if ev_dec is not None:
             ev_dec[0].record()
-        st = lib.pa_decode(ctypes.byref(self.dec), self.ws_ptr, self.ws_bytes, self.stream)
+        if self.append is None:
+            st = lib.pa_decode(ctypes.byref(self.dec), self.ws_ptr, self.ws_bytes, self.stream)
+        else:
+            st = lib.pa_append_decode(ctypes.byref(self.dec), ctypes.byref(self.append),
+                                      self.ws_ptr, self.ws_bytes, self.stream)
         if st:
-            raise RuntimeError(f"pa_decode failed: {st}")
+            raise RuntimeError(f"decode failed: {st}: {lib.pa_last_error()}")
         if ev_dec is not None:
             ev_dec[1].record()
 
@@ -178,7 +185,20 @@ def setup_workload(r: workloads.Recipe, device, n_copies: int):
                 copies=copies)
 
 
-def make_plans(pk, W, device, partition_tokens=0, variant=0, overlap=True):
+def count_launches(variant: int, fused: bool, max_len: int, num_cow: int) -> int:
+    """Kernels one step launches: copy-on-write copy (if any pairs), the KV
+    write (unless fused into the tensor-core decode), the decode, the merge
+    (always for the tensor-core kernel; for the CUDA-core kernel only when a
+    sequence spans several 512-token partitions)."""
+    n = 1 if num_cow else 0
+    if variant == 0:
+        n += (0 if fused else 1) + 2
+    else:
+        n += 1 + 1 + (1 if max_len > 512 else 0)
+    return n
+
+
+def make_plans(pk, W, device, partition_tokens=0, variant=0, overlap=True, fused=True):
     import torch
 
     lib = pk.load()
@@ -207,8 +227,10 @@ def make_plans(pk, W, device, partition_tokens=0, variant=0, overlap=True):
         if cows_d is not None:
             cow_args = (kc.data_ptr(), vc.data_ptr(), cows_d.data_ptr(), cows_d.shape[0], Hkv, D,
                         BS, NB)
+        app = pk.make_append_params(W["kn"], W["vn"], slots_d, kc, vc) if fused else None
         plans.append(StepPlan(pk, lib, p, ws.data_ptr() if ws is not None else None,
-                              ws.numel() if ws is not None else 0, rc_args, cow_args, stream))
+                              ws.numel() if ws is not None else 0, rc_args, cow_args, stream,
+                              append=app))
     return plans, out, keep
 
 
@@ -223,15 +245,18 @@ def run_ours(args, rank: int, world: int) -> dict:
     pk.load()
     r = workloads.llama8b_layer()
     W = setup_workload(r, device, n_copies=3)
+    fused = not args.separate_append
     plans, out, keep = make_plans(pk, W, device, variant=args.variant,
-                                  overlap=not args.no_overlap)
+                                  overlap=not args.no_overlap, fused=fused)
     lens = W["lens"]
     dec_b = decode_bytes(lens, r.num_q_heads, r.num_kv_heads, r.head_dim)
-    step_b = dec_b + append_bytes(len(W["slots"]), r.num_kv_heads, r.head_dim) + \
-        cow_bytes(len(W["cows"]), r.num_kv_heads, r.head_dim)
+    app_b = append_bytes(len(W["slots"]), r.num_kv_heads, r.head_dim)
+    step_b = dec_b + app_b + cow_bytes(len(W["cows"]), r.num_kv_heads, r.head_dim)
+    # bytes of the timed launch: the decode, plus the KV write when it is fused in
+    roof_b = dec_b + (app_b if fused else 0)
     pool_copy_bytes = 2 * W["copies"][0][0].numel() * 2
     n_split = int((lens > 512).sum())
-    launches_per_step = 1 + 1 + (1 if int(lens.max()) > 512 else 0) + (1 if len(W["cows"]) else 0)
+    launches_per_step = count_launches(args.variant, fused, int(lens.max()), len(W["cows"]))
 
     stream = torch.cuda.current_stream()
     # warm-up (untimed), then a sustained untimed loop under the clock sampler
@@ -277,12 +302,12 @@ def run_ours(args, rank: int, world: int) -> dict:
 
     peaks = measured_peaks()
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
-    achieved = dec_b / (dec_avg_ms * 1e-3) / 1e9
+    achieved = roof_b / (dec_avg_ms * 1e-3) / 1e9
 
     # end to end through the public Python API: pinned host inputs -> device,
     # step, result -> pinned host, every step
     e2e = run_e2e(pk, W, r, device, args.steps, args.warmup, step_b, args.variant,
-                  overlap=not args.no_overlap)
+                  overlap=not args.no_overlap, fused=fused)
 
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -304,8 +329,11 @@ def run_ours(args, rank: int, world: int) -> dict:
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": ("pa_decode: " + ("tensor-core" if args.variant == 0 else "CUDA-core")
-                       + " decode kernel + split-K merge"),
+            "kernel": (("pa_append_decode: " if fused else "pa_decode: ")
+                       + ("tensor-core" if args.variant == 0 else "CUDA-core")
+                       + (" decode kernel with the KV write fused in" if fused else
+                          " decode kernel") + " + split-K merge"),
+            "bytes_per_launch": roof_b,
             "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
             "peak_source": f"{peaks['source']} hbm_gbs", "avg_launch_ms": round(dec_avg_ms, 5),
@@ -317,13 +345,13 @@ def run_ours(args, rank: int, world: int) -> dict:
     }
     if not args.no_workloads:
         res["other_workloads"] = measure_other_workloads(pk, device, variant=args.variant,
-                                                         overlap=not args.no_overlap)
+                                                         overlap=not args.no_overlap, fused=fused)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(r, W, budget_s=args.cpu_baseline_s)
     return res
 
 
-def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True,
+def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True, fused: bool = True,
                             steps: int = 200, warmup: int = 10) -> dict:
     """The decode on the other workload shapes, measured after the main timed
     region: decode-only GB/s from CUDA events around each decode, and the
@@ -342,7 +370,7 @@ def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True,
     stream = torch.cuda.current_stream()
     for name, r in recipes:
         W = setup_workload(r, device, n_copies=2)
-        plans, _, keep = make_plans(pk, W, device, variant=variant, overlap=overlap)
+        plans, _, keep = make_plans(pk, W, device, variant=variant, overlap=overlap, fused=fused)
         lens = W["lens"]
         dec_b = decode_bytes(lens, r.num_q_heads, r.num_kv_heads, r.head_dim)
         step_b = dec_b + append_bytes(len(W["slots"]), r.num_kv_heads, r.head_dim) + \
@@ -377,7 +405,7 @@ def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True,
 
 
 def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int = 0,
-            overlap: bool = True) -> dict:
+            overlap: bool = True, fused: bool = True) -> dict:
     import torch
 
     host = {k: W[k] for k in ("tables", "lens", "slots")}
@@ -404,15 +432,21 @@ def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int
             dev[k].copy_(pin[k], non_blocking=True)
         if "cows" in dev:
             pk.pa_copy_blocks(kc, vc, dev["cows"])
-        pk.pa_reshape_and_cache(dev["kn"], dev["vn"], kc, vc, dev["slots"])
+        if not fused:
+            pk.pa_reshape_and_cache(dev["kn"], dev["vn"], kc, vc, dev["slots"])
         if "ws" not in ws:
             p = pk.make_decode_params(dev["q"], out_d, kc, vc, dev["tables"], dev["lens"], max_ctx,
                                       variant=variant)
             n = pk.pa_decode_workspace_size(p)
             ws["ws"] = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None
         # tables and lengths arrived before the first kernel of the step
-        pk.pa_decode(dev["q"], kc, vc, dev["tables"], dev["lens"], max_ctx, out=out_d,
-                     workspace=ws["ws"], variant=variant, overlap_prologue=overlap)
+        if fused:
+            pk.pa_append_decode(dev["q"], kc, vc, dev["tables"], dev["lens"], max_ctx,
+                                dev["kn"], dev["vn"], dev["slots"], out=out_d,
+                                workspace=ws["ws"], variant=variant, overlap_prologue=overlap)
+        else:
+            pk.pa_decode(dev["q"], kc, vc, dev["tables"], dev["lens"], max_ctx, out=out_d,
+                         workspace=ws["ws"], variant=variant, overlap_prologue=overlap)
         out_h.copy_(out_d, non_blocking=True)
 
     for i in range(warmup):
@@ -521,6 +555,9 @@ def main(argv=None) -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the decode measurements on the other workload shapes")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="launch the KV write as its own kernel instead of fusing it into the "
+                         "decode (pa_reshape_and_cache + pa_decode)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch the decode in plain stream order instead of overlapping its "
                          "set-up with the KV write")

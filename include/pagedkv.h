@@ -85,6 +85,8 @@ typedef enum {
 #define PA_DEVERR_SLOT 0x4u          /* slot_mapping entry >= num_blocks*block_size */
 #define PA_DEVERR_COPY_PAIR 0x8u     /* copy_blocks pair outside [0, num_blocks) */
 #define PA_DEVERR_TIMEOUT 0x10u      /* an mbarrier wait hit its iteration limit */
+#define PA_DEVERR_APPEND_SLOT 0x20u  /* pa_append_decode: slot_mapping[b] is not the slot of
+                                        token context_lens[b]-1 of sequence b (not written) */
 
 const char* pa_status_string(pa_status s);
 const char* pa_last_error(void);
@@ -194,6 +196,40 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cac
                                void* v_cache, const int64_t* slot_mapping, int32_t num_tokens,
                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                int32_t num_blocks, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_append_decode -- one decode step's KV write and attention in one
+ * launch: the effect of
+ *   pa_reshape_and_cache(a->k_new, a->v_new, k_cache, v_cache,
+ *                        a->slot_mapping, num_seqs, ...)
+ *   pa_decode(p, ...)
+ * [P1 §One step, end to end: the forward pass writes the new token's KV
+ * through the slot mapping, then attention reads the paged cache].
+ * Token b is sequence b's new token: k_new/v_new are bf16
+ * [num_seqs][num_kv_heads][head_dim], slot_mapping is int64 [num_seqs], and
+ * p->context_lens already counts the new token. The write of sequence b is
+ * done by the part of the decode that reads b's last block, just before that
+ * block is loaded, so
+ *  - slot_mapping[b] must be the slot of token context_lens[b]-1 of b, i.e.
+ *    block_tables[b][(L-1)/16]*16 + (L-1)%16. Any other non-negative value
+ *    sets PA_DEVERR_APPEND_SLOT and is not written; a negative value writes
+ *    nothing (padding); sequences of length 0 write nothing.
+ *  - the written block must not be read by another sequence of the batch,
+ *    which copy-on-write guarantees (a shared block is copied before a write).
+ * a->k_cache / a->v_cache must equal p->k_cache / p->v_cache (the caches are
+ * written through these). Same workspace as pa_decode. The CUDA-core variant
+ * and shapes the tensor-core kernel does not cover run the KV-write kernel
+ * and then the decode, with the same result.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void* k_new;            /* bf16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned */
+  const void* v_new;            /* same */
+  const int64_t* slot_mapping;  /* int64 [num_seqs] */
+  void* k_cache;                /* == p->k_cache, written */
+  void* v_cache;                /* == p->v_cache, written */
+} pa_append_params;
+pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a, void* workspace,
+                           size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_copy_blocks -- the data half of copy-on-write [P2 §Prefix Caching and

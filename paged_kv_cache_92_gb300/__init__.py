@@ -29,10 +29,12 @@ DEVERR_CONTEXT_LEN = 0x2
 DEVERR_SLOT = 0x4
 DEVERR_COPY_PAIR = 0x8
 DEVERR_TIMEOUT = 0x10
+DEVERR_APPEND_SLOT = 0x20
 
 EXPORTED_SYMBOLS = [
     "pa_status_string", "pa_last_error", "pa_version", "pa_device_errors",
-    "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_reshape_and_cache",
+    "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_append_decode",
+    "pa_reshape_and_cache",
     "pa_copy_blocks",
     "pa_pool_create", "pa_pool_destroy", "pa_pool_alloc", "pa_pool_incref", "pa_pool_decref",
     "pa_pool_refcount", "pa_pool_stats", "pa_seq_create", "pa_seq_free", "pa_seq_fork",
@@ -69,6 +71,14 @@ DECODE_TENSOR_CORE = 0
 DECODE_CUDA_CORE = 1
 
 
+class AppendParams(ctypes.Structure):
+    _fields_ = [
+        ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("slot_mapping", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+    ]
+
+
 class PoolStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("num_blocks", "block_size", "free_blocks", "used_blocks", "shared_blocks",
@@ -97,6 +107,7 @@ def load():
         "pa_decode_workspace_size": ([P(DecodeParams)], sz),
         "pa_decode": ([P(DecodeParams), vp, sz, vp], ctypes.c_int),
         "pa_decode_noalloc": ([P(DecodeParams), vp], ctypes.c_int),
+        "pa_append_decode": ([P(DecodeParams), P(AppendParams), vp, sz, vp], ctypes.c_int),
         "pa_reshape_and_cache": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
         "pa_copy_blocks": ([vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
         "pa_pool_create": ([i32, i32, vp, P(vp)], ctypes.c_int),
@@ -214,6 +225,50 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
     ws_ptr = _dev_ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(lib.pa_decode(ctypes.byref(p), ws_ptr, ws_bytes, _stream_handle(stream)), "pa_decode")
+    return out
+
+
+def make_append_params(k_new, v_new, slot_mapping, k_cache, v_cache) -> AppendParams:
+    import torch
+
+    B, Hkv, D = k_new.shape
+    if tuple(v_new.shape) != (B, Hkv, D) or tuple(slot_mapping.shape) != (B,) \
+            or tuple(k_cache.shape[1:2]) != (Hkv,) or k_cache.shape[3] != D:
+        raise ValueError("k_new/v_new must be [num_seqs][num_kv_heads][head_dim] matching the "
+                         "cache, slot_mapping [num_seqs]")
+    a = AppendParams()
+    a.k_new = _dev_ptr(k_new, torch.bfloat16, "k_new")
+    a.v_new = _dev_ptr(v_new, torch.bfloat16, "v_new")
+    a.slot_mapping = _dev_ptr(slot_mapping, torch.int64, "slot_mapping")
+    a.k_cache = _dev_ptr(k_cache, torch.bfloat16, "k_cache")
+    a.v_cache = _dev_ptr(v_cache, torch.bfloat16, "v_cache")
+    return a
+
+
+def pa_append_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+                     k_new, v_new, slot_mapping, scale: Optional[float] = None,
+                     partition_tokens: int = 0, out=None, workspace=None, stream=None,
+                     variant: int = DECODE_TENSOR_CORE, overlap_prologue: bool = False):
+    """One decode step in one launch: write token b's K/V (``k_new[b]``,
+    ``v_new[b]``) at ``slot_mapping[b]`` -- which must be the slot of token
+    ``context_lens[b] - 1`` of sequence b -- then paged decode attention over
+    the updated caches. Same result as ``pa_reshape_and_cache`` followed by
+    ``pa_decode``; returns ``out``."""
+    import torch
+
+    lib = load()
+    if out is None:
+        out = torch.empty_like(q)
+    p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
+                           max_context_len, scale, partition_tokens, variant, overlap_prologue)
+    a = make_append_params(k_new, v_new, slot_mapping, k_cache, v_cache)
+    need = int(lib.pa_decode_workspace_size(ctypes.byref(p)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev_ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(lib.pa_append_decode(ctypes.byref(p), ctypes.byref(a), ws_ptr, ws_bytes,
+                                _stream_handle(stream)), "pa_append_decode")
     return out
 
 

@@ -118,9 +118,10 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
 // Launch the selected decode kernel and its merge.
 static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
                             const WorkspaceLayout& w, int np, int grid, pa_stream_t stream,
-                            const char* who) {
+                            const char* who, const pa_append_params* append = nullptr) {
   DecodeLaunch L;
   L.p = p;
+  L.append = append;
   L.partition_tokens = resolve_partition_tokens(p);
   L.num_partitions = np;
   L.grid = grid;
@@ -133,6 +134,21 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
     L.part_acc = reinterpret_cast<float*>(ws + w.tc_acc);
     e = launch_decode_tc(L, stream);
   } else {
+    if (append) {  // the same effect in two launches
+      AppendCheck chk;
+      chk.block_tables = p->block_tables;
+      chk.context_lens = p->context_lens;
+      chk.max_blocks_per_seq = p->max_blocks_per_seq;
+      chk.cap = p->max_blocks_per_seq * kBlockSize < p->max_context_len
+                    ? p->max_blocks_per_seq * kBlockSize : p->max_context_len;
+      e = launch_reshape_and_cache(append->k_new, append->v_new, append->k_cache,
+                                   append->v_cache, append->slot_mapping, p->num_seqs,
+                                   p->num_kv_heads, p->head_dim, p->num_blocks, stream, chk);
+    }
+    if (e) {
+      std::snprintf(where, sizeof(where), "%s: launch", who);
+      return set_cuda_error(where, e);
+    }
     L.plan = nullptr;
     L.part_m = np > 1 ? reinterpret_cast<float*>(ws + w.simt_m) : nullptr;
     L.part_l = np > 1 ? reinterpret_cast<float*>(ws + w.simt_l) : nullptr;
@@ -222,6 +238,32 @@ pa_status pa_decode_noalloc(const pa_decode_params* p, pa_stream_t stream) {
   // and partials before reading them.
   return pa::run_decode(p, static_cast<unsigned char*>(scratch), w, np, grid, stream,
                         "pa_decode_noalloc");
+}
+
+pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
+                           void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = pa::check_decode(p, true);
+  if (st != PA_OK) return st;
+  if (!a) return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: append params are NULL");
+  if (p->num_seqs == 0) return PA_OK;
+  if (!a->k_new || !a->v_new || !a->slot_mapping || !a->k_cache || !a->v_cache)
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: a required pointer is NULL");
+  if (a->k_cache != p->k_cache || a->v_cache != p->v_cache)
+    return pa::set_error(PA_ERR_INVALID_ARG,
+                         "pa_append_decode: append k_cache/v_cache must be the decode's caches");
+  if (!pa::aligned16(a->k_new) || !pa::aligned16(a->v_new) ||
+      (reinterpret_cast<uintptr_t>(a->slot_mapping) & 7u))
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: misaligned pointer");
+  const int np = pa::num_partitions_for(p);
+  const int grid = pa::tc_grid();
+  const pa::WorkspaceLayout w = pa::decode_workspace_layout(p, np, grid);
+  if (!workspace || workspace_bytes < w.total)
+    return pa::set_error(PA_ERR_INVALID_ARG,
+                         "pa_append_decode: workspace smaller than pa_decode_workspace_size()");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: workspace must be 256-byte aligned");
+  return pa::run_decode(p, static_cast<unsigned char*>(workspace), w, np, grid, stream,
+                        "pa_append_decode", a);
 }
 
 pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,

@@ -26,7 +26,8 @@ __global__ void __launch_bounds__(256)
     reshape_and_cache_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                              uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                              const int64_t* __restrict__ slot_mapping, int64_t num_chunks,
-                             int num_kv_heads, int chunks_per_row, int64_t num_slots) {
+                             int num_kv_heads, int chunks_per_row, int64_t num_slots,
+                             AppendCheck check) {
   // a decode launched as a programmatic dependent may start its set-up now;
   // it waits for this kernel before it reads the cache
   dev::griddep_launch_dependents();
@@ -41,6 +42,15 @@ __global__ void __launch_bounds__(256)
   if (slot >= num_slots) {
     atomicOr(&g_cache_errors, PA_DEVERR_SLOT);
     return;
+  }
+  if (check.block_tables) {  // decode step: only the slot of the sequence's last token
+    const int L = min(check.context_lens[t], check.cap);
+    if (L <= 0) return;
+    const int e = check.block_tables[t * check.max_blocks_per_seq + (L - 1) / BS];
+    if (slot != int64_t(e) * BS + (L - 1) % BS) {
+      if (h == 0 && c == 0) atomicOr(&g_cache_errors, PA_DEVERR_APPEND_SLOT);
+      return;
+    }
   }
   const int64_t blk = slot / BS;
   const int64_t off = slot % BS;
@@ -72,7 +82,8 @@ __global__ void __launch_bounds__(256)
 
 int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
-                             int32_t head_dim, int32_t num_blocks, void* stream) {
+                             int32_t head_dim, int32_t num_blocks, void* stream,
+                             const AppendCheck& check) {
   const int chunks_per_row = head_dim * 2 / 16;
   const int64_t num_chunks = int64_t(num_tokens) * num_kv_heads * chunks_per_row;
   if (num_chunks == 0) return int(cudaSuccess);
@@ -81,7 +92,7 @@ int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache
   reshape_and_cache_kernel<<<unsigned(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_chunks,
-      num_kv_heads, chunks_per_row, int64_t(num_blocks) * BS);
+      num_kv_heads, chunks_per_row, int64_t(num_blocks) * BS, check);
   return int(cudaGetLastError());
 }
 

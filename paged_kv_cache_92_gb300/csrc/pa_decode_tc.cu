@@ -130,6 +130,12 @@ struct TcParams {
   float* part_l;    // [segments][Hq]
   float* part_acc;  // [segments][Hq][D]
   int* ws_plan;     // [0] = blocks per CTA, [1 .. B+1] = block prefix of the sequences
+  // fused KV append (null k_new: none): token b goes to slot_mapping[b]
+  const uint4* k_new;
+  const uint4* v_new;
+  const int64_t* slot_mapping;
+  uint4* k_cache_w;
+  uint4* v_cache_w;
   int max_blocks_per_seq, num_seqs, num_kv_heads, num_q_heads, num_blocks, cap, oob_row;
   float scale_log2;
 };
@@ -601,6 +607,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return (b < B && j < P.max_blocks_per_seq)
                  ? P.block_tables[size_t(b) * P.max_blocks_per_seq + j] : -1;
     };
+    // Fused KV append: sequence b's new token (its last, token L-1) is
+    // written by the piece that reads b's last block, before that block's
+    // copy is issued. Generic-proxy stores, then a proxy fence so the TMA
+    // (async proxy) that follows reads the new row.
+    auto append_token = [&](int b, int L) {
+      const int64_t slot = P.slot_mapping[b];
+      if (slot < 0) return;  // padding token
+      if (slot >= int64_t(P.num_blocks) * BS) {
+        if (lane == 0) atomicOr(&g_tc_errors, PA_DEVERR_SLOT);
+        return;
+      }
+      const int last = L - 1;
+      const int e = P.block_tables[size_t(b) * P.max_blocks_per_seq + last / BS];
+      if (e < 0 || e >= P.num_blocks || slot != int64_t(e) * BS + last % BS) {
+        if (lane == 0) atomicOr(&g_tc_errors, PA_DEVERR_APPEND_SLOT);
+        return;
+      }
+      constexpr int CPR = D / 8;  // 16-byte chunks of one row
+      const int n = H * CPR;
+      for (int i = lane; i < n; i += 32) {
+        const int hh = i / CPR, ch = i - (i / CPR) * CPR;
+        const size_t src = size_t(b) * n + i;
+        const size_t dst = ((size_t(e) * H + hh) * BS + last % BS) * CPR + ch;
+        const uint4 kv = P.k_new[src];
+        const uint4 vv = P.v_new[src];
+        P.k_cache_w[dst] = kv;
+        P.v_cache_w[dst] = vv;
+      }
+      dev::fence_async_global();
+    };
     int b = b_start, off = off_start, unit = u0;
     int win = win0;
     int L_cur = len0;
@@ -615,6 +651,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const int seg_nb = min(nb - off, u1 - unit);
       const bool whole = off == 0 && seg_nb == nb;
+      if (P.k_new != nullptr && off + seg_nb == nb) {  // this piece holds the last block
+        append_token(b, L_cur);
+        __syncwarp();
+        dev::fence_async_global();
+      }
       // prefetched for later: the next sequence's length and first window,
       // this segment's second window
       const int L_nxt = b + 1 < B ? min(P.context_lens[b + 1], P.cap) : 0;
@@ -827,6 +868,12 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.part_l = Lc.part_l;
   P.part_acc = Lc.part_acc;
   P.ws_plan = Lc.plan;
+  const pa_append_params* a = Lc.append;
+  P.k_new = a ? static_cast<const uint4*>(a->k_new) : nullptr;
+  P.v_new = a ? static_cast<const uint4*>(a->v_new) : nullptr;
+  P.slot_mapping = a ? a->slot_mapping : nullptr;
+  P.k_cache_w = a ? static_cast<uint4*>(a->k_cache) : nullptr;
+  P.v_cache_w = a ? static_cast<uint4*>(a->v_cache) : nullptr;
   P.max_blocks_per_seq = p->max_blocks_per_seq;
   P.num_seqs = p->num_seqs;
   P.num_kv_heads = H;

@@ -346,6 +346,11 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's generic-proxy global accesses before its later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 }  // namespace dev
 }  // namespace pa

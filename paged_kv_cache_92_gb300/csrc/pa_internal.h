@@ -30,6 +30,7 @@ struct DecodeLaunch {
   float* part_l;         // partial sums
   float* part_acc;       // partial weighted sums
   int* plan;             // tensor-core kernel: stream-K plan for its merge
+  const pa_append_params* append;  // non-null: write each sequence's new token first
 };
 
 // Bytes at the start of every decode workspace (reserved).
@@ -53,9 +54,20 @@ int tc_grid();
 int launch_decode(const DecodeLaunch& L, void* stream);      // CUDA-core decode kernel
 int launch_decode_tc(const DecodeLaunch& L, void* stream);   // tensor-core decode kernel
 int launch_merge(const DecodeLaunch& L, void* stream);       // split-K merge (if needed)
+// Decode-step check (block_tables non-null): token t is sequence t's newest
+// token; it is written only if slot_mapping[t] is the slot of token
+// min(context_lens[t], cap) - 1 of sequence t (else PA_DEVERR_APPEND_SLOT),
+// and not at all for an empty sequence.
+struct AppendCheck {
+  const int32_t* block_tables = nullptr;
+  const int32_t* context_lens = nullptr;
+  int max_blocks_per_seq = 0;
+  int cap = 0;
+};
 int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
-                             int32_t head_dim, int32_t num_blocks, void* stream);
+                             int32_t head_dim, int32_t num_blocks, void* stream,
+                             const AppendCheck& check = AppendCheck());
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
                        int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, void* stream);
 

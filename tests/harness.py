@@ -59,8 +59,9 @@ def build_case(r: workloads.Recipe, device: str = "cuda") -> Case:
 
 
 def run_step_gpu(case: Case, partition_tokens: int = 0, variant: int = 0,
-                 overlap_prologue: bool = False):
-    """The hot path on the GPU: copy_blocks -> reshape_and_cache -> decode."""
+                 overlap_prologue: bool = False, fused_append: bool = False):
+    """The hot path on the GPU: copy_blocks -> reshape_and_cache -> decode
+    (or copy_blocks -> pa_append_decode, the KV write fused into the decode)."""
     import torch
 
     import paged_kv_cache_92_gb300 as pk
@@ -73,12 +74,28 @@ def run_step_gpu(case: Case, partition_tokens: int = 0, variant: int = 0,
     lens = torch.from_numpy(case.lens).to(dev)
     if len(case.cows):
         pk.pa_copy_blocks(kc, vc, torch.from_numpy(case.cows).to(dev))
-    pk.pa_reshape_and_cache(case.k_new, case.v_new, kc, vc, torch.from_numpy(case.slots).to(dev))
-    out = pk.pa_decode(case.q, kc, vc, tables, lens, max_context_len=int(case.lens.max()),
-                       partition_tokens=partition_tokens, variant=variant,
-                       overlap_prologue=overlap_prologue)
+    slots = torch.from_numpy(case.slots).to(dev)
+    if fused_append:
+        out = pk.pa_append_decode(case.q, kc, vc, tables, lens, int(case.lens.max()),
+                                  case.k_new, case.v_new, slots,
+                                  partition_tokens=partition_tokens, variant=variant,
+                                  overlap_prologue=overlap_prologue)
+    else:
+        pk.pa_reshape_and_cache(case.k_new, case.v_new, kc, vc, slots)
+        out = pk.pa_decode(case.q, kc, vc, tables, lens, max_context_len=int(case.lens.max()),
+                           partition_tokens=partition_tokens, variant=variant,
+                           overlap_prologue=overlap_prologue)
     torch.cuda.synchronize()
     return out, kc, vc
+
+
+def oracle_caches(case: Case):
+    """The oracle's caches after the step's copy-on-write and KV write (bits)."""
+    kc = oracle.bf16_bits(case.k_cache.cpu())
+    vc = oracle.bf16_bits(case.v_cache.cpu())
+    if len(case.cows):
+        kc, vc = oracle.copy_blocks(kc, vc, case.cows)
+    return oracle.reshape_and_cache(case.k_new.cpu(), case.v_new.cpu(), kc, vc, case.slots)
 
 
 def run_step_oracle(case: Case, units=None):

@@ -117,3 +117,28 @@ def test_cache_ops_reject_bad_arguments_on_the_host(pk):
     assert lib.pa_copy_blocks(None, None, None, 2, 8, 128, 16, 10, None) == 1
     assert lib.pa_copy_blocks(None, None, None, 0, 8, 128, 16, 10, None) == 0
     assert lib.pa_copy_blocks(None, None, None, 70000, 8, 128, 16, 10, None) == 1
+
+
+def test_append_decode_rejects_bad_arguments_on_the_host(pk):
+    """pa_append_decode validates its append arguments before any launch (no
+    pointer is dereferenced on the host)."""
+    lib = pk.load()
+    p = _params(pk)
+    fake = 1 << 20  # 16-byte aligned, never dereferenced by the host checks
+    p.q = p.out = p.k_cache = p.v_cache = fake
+    p.block_tables = p.context_lens = fake
+    assert lib.pa_append_decode(ctypes.byref(p), None, None, 0, None) == 1
+    a = pk.AppendParams()
+    assert lib.pa_append_decode(ctypes.byref(p), ctypes.byref(a), None, 0, None) == 1  # NULLs
+    a.k_new = a.v_new = a.slot_mapping = fake
+    a.k_cache, a.v_cache = fake + 256, fake  # not the decode's cache
+    assert lib.pa_append_decode(ctypes.byref(p), ctypes.byref(a), None, 0, None) == 1
+    assert b"decode's caches" in lib.pa_last_error()
+    a.k_cache = fake
+    a.k_new = fake + 8  # misaligned
+    assert lib.pa_append_decode(ctypes.byref(p), ctypes.byref(a), None, 0, None) == 1
+    a.k_new = fake
+    assert lib.pa_append_decode(ctypes.byref(p), ctypes.byref(a), None, 0, None) == 1  # no workspace
+    assert b"workspace" in lib.pa_last_error()
+    p.head_dim = 96
+    assert lib.pa_append_decode(ctypes.byref(p), ctypes.byref(a), None, 0, None) == 2

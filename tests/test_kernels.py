@@ -389,3 +389,72 @@ def test_overlapped_decodes_back_to_back_keep_their_partials(pk):
         for a, b in zip(got, plain):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     _check_errors(pk)
+
+
+# ---------------------------------------------------------------- fused KV append
+
+FUSED_CASES = {
+    "tiny": workloads.tiny,
+    "llama8b_layer": workloads.llama8b_layer,
+    "llama8b_high_concurrency": workloads.llama8b_high_concurrency,
+    "llama70b_long_b8": lambda: workloads.llama70b_long(batch=8),
+    "shared_prefix": workloads.shared_prefix,
+}
+
+
+@VARIANTS
+@pytest.mark.parametrize("name", list(FUSED_CASES))
+def test_fused_append_decode_matches_oracle_and_separate_launches(pk, name, variant):
+    """pa_append_decode (KV write inside the decode) against the oracle's KV
+    write + decode, and bit for bit against pa_reshape_and_cache + pa_decode."""
+    import torch
+
+    case = harness.build_case(FUSED_CASES[name]())
+    got, kg, vg = harness.run_step_gpu(case, variant=variant, fused_append=True,
+                                       overlap_prologue=True)
+    ko, vo = harness.oracle_caches(case)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
+    B, Hq = case.q.shape[0], case.q.shape[1]
+    units = harness.sample_units(B, Hq, min(B * Hq, 96), seed=7,
+                                 must=[(int(np.argmax(case.lens)), Hq - 1)])
+    ref = oracle.paged_decode(case.q.cpu(), ko, vo, case.tables, case.lens, units=units)
+    g = harness.bf16_tensor_to_f64(got)
+    harness.assert_close(np.stack([g[b, h] for b, h in units]), ref)
+    want, _, _ = harness.run_step_gpu(case, variant=variant)
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    _check_errors(pk)
+
+
+@VARIANTS
+def test_fused_append_slot_rules(pk, variant):
+    """Sequence 0 appends at its last token's slot (written); sequence 1 has a
+    negative slot (nothing written); sequence 2 names a slot that is not its
+    last token's (error bit, nothing written); sequence 3 is empty (nothing
+    written, zero output)."""
+    import torch
+
+    lens = np.array([41, 8, 17, 0])
+    q, kc, vc, tables, lens, _ = _direct_case(lens, 8, 2, 128, seed=31)
+    last = [(int(tables[b, (lens[b] - 1) // 16]) * 16 + (lens[b] - 1) % 16) if lens[b] else -1
+            for b in range(4)]
+    spare = (kc.shape[0] - 1) * 16  # a slot of an unused block
+    slots = np.array([last[0], -1, last[2] + 1, spare], dtype=np.int64)
+    kn = workloads.bf16_normal((4, 2, 128), 41, "cuda")
+    vn = workloads.bf16_normal((4, 2, 128), 42, "cuda")
+    k2, v2 = kc.clone(), vc.clone()
+    out = pk.pa_append_decode(q, k2, v2, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
+                              torch.from_numpy(slots).cuda(), variant=variant)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() == pk.DEVERR_APPEND_SLOT
+    only0 = np.array([last[0], -1, -1, -1], dtype=np.int64)
+    ko, vo = oracle.reshape_and_cache(kn.cpu(), vn.cpu(), oracle.bf16_bits(kc.cpu()),
+                                      oracle.bf16_bits(vc.cpu()), only0)
+    assert np.array_equal(oracle.bf16_bits(k2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(v2.cpu()), vo)
+    units = [(b, h) for b in range(3) for h in range(8)]  # the oracle has no empty sequence
+    ref = oracle.paged_decode(q.cpu(), ko, vo, tables, lens, units=units)
+    got = harness.bf16_tensor_to_f64(out)
+    harness.assert_close(got[:3].reshape(24, -1), ref)
+    assert not got[3].any()
