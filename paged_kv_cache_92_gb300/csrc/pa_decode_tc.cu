@@ -564,8 +564,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     b_start = lo;
   }
   const int off_start = u0 < u1 ? u0 - pre[b_start] : 0;
-  // the merge kernel (a programmatic dependent) may launch; it waits for us
-  if (tid == 0) dev::griddep_launch_dependents();
   for (int i = tid; i < 128; i += NTHREADS) alpha_s[i] = 1.0f;  // padded columns stay 1
   if (warp == 0) dev::tmem_alloc(tmem_slot, C::TMEM_COLS);
   // Everything above read only context_lens (and shared memory). When this
@@ -760,6 +758,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   dev::tc_fence_before();
   __syncthreads();
+  // The merge kernel (a programmatic dependent) can do nothing before this
+  // grid ends: let it launch as the CTAs finish, not earlier, so its waiting
+  // CTAs never share an SM with a running decode CTA.
+  if (tid == 0) dev::griddep_launch_dependents();
   if (warp == 0) {
     dev::tc_fence_after();
     dev::tmem_dealloc(tmem, C::TMEM_COLS);
@@ -767,13 +769,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // Log-sum-exp merge of the partials of sequences that span several CTAs, and
-// zero rows for empty sequences. One warp per (sequence, query head).
+// zero rows for empty sequences. One warp per (sequence, query head). The
+// lanes read the pieces' (max, sum) pairs side by side while the rows of the
+// first kPrefetch pieces are already in flight, so a typical merge costs one
+// memory round trip.
+template <int VPL>
+struct Row {
+  float v[VPL];
+  __device__ void load(const float* src) {
+    if constexpr (VPL == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(src);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      v[0] = t.x; v[1] = t.y;
+    }
+  }
+  __device__ void madd_into(float* acc, float w) const {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) acc[j] = fmaf(w, v[j], acc[j]);
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(128)
     merge_segments_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ part_m,
                           const float* __restrict__ part_l, const float* __restrict__ part_acc,
                           const int* __restrict__ ws_plan, int num_q_heads) {
   constexpr int VPL = D / 32;
+  constexpr int kPrefetch = 16;
+  // The next kernel on the stream may start its own set-up now (it waits
+  // for this grid before it touches memory this grid writes).
+  dev::griddep_launch_dependents();
   dev::griddep_wait();  // launched as a programmatic dependent of the decode
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 4 + warp;
@@ -789,20 +816,60 @@ __global__ void __launch_bounds__(128)
   }
   const int c0 = pre0 / R, c1 = (pre1 - 1) / R;
   if (c0 == c1) return;  // written whole by the decode kernel
-  float M = -INFINITY;
-  for (int c = c0; c <= c1; ++c) M = fmaxf(M, part_m[size_t(b + c) * num_q_heads + n]);
+  const int nseg = c1 - c0 + 1;
+  // piece k of the sequence sits in partial slot (b + c0 + k)
+  const size_t slot0 = size_t(b + c0) * num_q_heads + n;
+  const size_t stride = size_t(num_q_heads);
+  const float* src0 = part_acc + slot0 * D + lane * VPL;
+  Row<VPL> pf[kPrefetch];
+#pragma unroll
+  for (int k = 0; k < kPrefetch; ++k)
+    if (k < nseg) pf[k].load(src0 + size_t(k) * stride * D);
+  float m_first = -INFINITY, l_first = 0.0f;  // this lane's piece among the first 32
+  if (lane < nseg) {
+    m_first = part_m[slot0 + lane * stride];
+    l_first = part_l[slot0 + lane * stride];
+  }
+  float M = m_first;
+  for (int k = 32 + lane; k < nseg; k += 32) M = fmaxf(M, part_m[slot0 + k * stride]);
+#pragma unroll
+  for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
   float acc[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) acc[j] = 0.0f;
   float den = 0.0f;
-  for (int c = c0; c <= c1; ++c) {
-    const size_t sidx = size_t(b + c) * num_q_heads + n;
-    const float wt = dev::fast_exp2(part_m[sidx] - M);
-    den = fmaf(wt, part_l[sidx], den);
-    const float* src = part_acc + sidx * D + lane * VPL;
+  for (int base = 0; base < nseg; base += 32) {
+    float w = 0.0f;
+    if (base + lane < nseg) {
+      const float mk = base == 0 ? m_first : part_m[slot0 + (base + lane) * stride];
+      const float lk = base == 0 ? l_first : part_l[slot0 + (base + lane) * stride];
+      w = dev::fast_exp2(mk - M);
+      den = fmaf(w, lk, den);
+    }
+    const int cnt = min(32, nseg - base);
+    int k0 = 0;
+    if (base == 0) {
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) acc[j] = fmaf(wt, src[j], acc[j]);
+      for (int k = 0; k < kPrefetch; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        if (k < cnt) pf[k].madd_into(acc, wk);
+      }
+      k0 = kPrefetch;
+    }
+    for (int k = k0; k < cnt; k += 8) {
+      Row<VPL> r[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (k + j < cnt) r[j].load(src0 + size_t(base + k + j) * stride * D);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, (k + j) & 31);
+        if (k + j < cnt) r[j].madd_into(acc, wj);
+      }
+    }
   }
+#pragma unroll
+  for (int o2 = 16; o2 >= 1; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
   const float inv = __frcp_rn(den);
 #pragma unroll
   for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(acc[j] * inv);
