@@ -69,6 +69,30 @@ def cow_bytes(num_pairs: int, num_kv_heads: int, head_dim: int, block_size: int 
     return num_pairs * 2 * num_kv_heads * block_size * head_dim * 2 * 2
 
 
+def profiled_traffic(summary: str = "pa_decode_tc_llama8b_b64.md"):
+    """DRAM bytes (read + write) of one decode launch from the committed ncu
+    summary, or None when the kernel sources have changed since that capture
+    (the summary records a sha256 prefix of each source file)."""
+    import hashlib
+    import re
+
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    h = re.search(r"source_sha256_prefix:\s*(.+)", text)
+    if not m or not h:
+        return None
+    csrc = os.path.join(ROOT, "paged_kv_cache_92_gb300", "csrc")
+    for item in h.group(1).split():
+        name, want = item.split("=")
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:len(want)] != want:
+                return None
+    return int(m.group(1))
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -335,7 +359,8 @@ def run_ours(args, rank: int, world: int) -> dict:
                           " decode kernel") + " + split-K merge"),
             "bytes_per_launch": roof_b,
             "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": profiled_traffic() if args.variant == 0 and fused else None,
             "peak_source": f"{peaks['source']} hbm_gbs", "avg_launch_ms": round(dec_avg_ms, 5),
             "timed_launches": len(dec_ms),
         },
