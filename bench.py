@@ -431,63 +431,48 @@ def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True, 
 
 def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int = 0,
             overlap: bool = True, fused: bool = True) -> dict:
+    """The same step end to end through ``pa_step_host``: each step is one C
+    call that copies the packed inputs (q, new K/V, slots, tables, lengths,
+    copy-on-write pairs) from pinned host memory to the device, runs the
+    step, copies the output back to pinned host memory and synchronises."""
     import torch
 
-    host = {k: W[k] for k in ("tables", "lens", "slots")}
-    pin = {
-        "q": W["q"].cpu().pin_memory(), "kn": W["kn"].cpu().pin_memory(),
-        "vn": W["vn"].cpu().pin_memory(),
-        "tables": torch.from_numpy(host["tables"]).pin_memory(),
-        "lens": torch.from_numpy(host["lens"]).pin_memory(),
-        "slots": torch.from_numpy(host["slots"]).pin_memory(),
-    }
-    if len(W["cows"]):
-        pin["cows"] = torch.from_numpy(W["cows"]).pin_memory()
-    dev = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
-    out_d = torch.empty_like(W["q"])
-    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in pin.values())
-    d2h = out_h.numel() * out_h.element_size()
-    ws = {}
-    max_ctx = int(host["lens"].max())
+    lib = pk.load()
+    B, Hq, D = W["q"].shape
+    params = []
+    host_in = None
+    for kc, vc in W["copies"]:
+        p = pk.make_step_host_params(kc, vc, B, Hq, W["tables"].shape[1], int(W["lens"].max()),
+                                     num_cow_pairs=len(W["cows"]), variant=variant)
+        if host_in is None:
+            host_in = pk.pack_step_inputs(p, W["q"].cpu(), W["kn"].cpu(), W["vn"].cpu(),
+                                          W["slots"], W["tables"], W["lens"],
+                                          W["cows"] if len(W["cows"]) else None)
+        params.append(p)
+    host_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    for p in params:
+        p.host_in, p.host_out = host_in.data_ptr(), host_out.data_ptr()
+    ws = torch.empty(pk.pa_step_host_workspace_size(params[0]), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream().cuda_stream or None
+    refs = [ctypes.byref(p) for p in params]
 
     def step(i):
-        kc, vc = W["copies"][i % len(W["copies"])]
-        for k in pin:
-            dev[k].copy_(pin[k], non_blocking=True)
-        if "cows" in dev:
-            pk.pa_copy_blocks(kc, vc, dev["cows"])
-        if not fused:
-            pk.pa_reshape_and_cache(dev["kn"], dev["vn"], kc, vc, dev["slots"])
-        if "ws" not in ws:
-            p = pk.make_decode_params(dev["q"], out_d, kc, vc, dev["tables"], dev["lens"], max_ctx,
-                                      variant=variant)
-            n = pk.pa_decode_workspace_size(p)
-            ws["ws"] = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None
-        # tables and lengths arrived before the first kernel of the step
-        if fused:
-            pk.pa_append_decode(dev["q"], kc, vc, dev["tables"], dev["lens"], max_ctx,
-                                dev["kn"], dev["vn"], dev["slots"], out=out_d,
-                                workspace=ws["ws"], variant=variant, overlap_prologue=overlap)
-        else:
-            pk.pa_decode(dev["q"], kc, vc, dev["tables"], dev["lens"], max_ctx, out=out_d,
-                         workspace=ws["ws"], variant=variant, overlap_prologue=overlap)
-        out_h.copy_(out_d, non_blocking=True)
+        st = lib.pa_step_host(refs[i % len(refs)], ws.data_ptr(), ws.numel(), stream)
+        if st:
+            raise RuntimeError(f"pa_step_host failed: {st}: {lib.pa_last_error()}")
 
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
-        step(i)
-        torch.cuda.current_stream().synchronize()  # the host reads the result every step
+        step(i)  # returns once the output is in host memory
     dt = time.perf_counter() - t0
     return {"value": round(step_b * steps / dt / 1e9, 2), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": round(dt * 1e3 / steps, 4)}
-
-
-# ----------------------------------------------------------------------------- oracle arm
+            "h2d_bytes_per_step": int(host_in.numel()), "d2h_bytes_per_step": int(host_out.numel() * 2),
+            "ms_per_step": round(dt / steps * 1e3, 4),
+            "api": "pa_step_host (one C call per step: H2D of the packed inputs, copy-on-write, "
+                   "fused KV write + decode + merge, D2H of the output, stream sync)"}
 
 def _oracle_sample_inputs(r: workloads.Recipe):
     """Host layout and contents for the oracle (its own pool model)."""

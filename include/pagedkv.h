@@ -232,6 +232,64 @@ pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
                            size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_step_host -- one whole decode step driven from host memory, for a host
+ * that builds each step's batch (the scheduler of [P1 §One step, end to
+ * end]) and reads the result back: copy-on-write copies, the KV write of
+ * one new token per sequence and paged decode attention, with the inputs
+ * taken from one packed host buffer and the output returned to host memory.
+ *
+ * The call enqueues on `stream`
+ *   1. one host->device copy of the packed inputs into the workspace,
+ *   2. pa_copy_blocks (if num_cow_pairs > 0), then pa_append_decode on the
+ *      staged inputs and the device-resident caches,
+ *   3. one device->host copy of the output,
+ * and synchronises the stream before it returns (the output is in host_out).
+ *
+ * Packed input (host memory; pinned memory lets the copy run at full speed):
+ * sections at the byte offsets pa_step_host_layout reports, each 256-byte
+ * aligned, in this order:
+ *   q             bf16  [num_seqs][num_q_heads][head_dim]
+ *   k_new, v_new  bf16  [num_seqs][num_kv_heads][head_dim]
+ *   slot_mapping  int64 [num_seqs]          (rules of pa_append_decode)
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens  int32 [num_seqs]          (counting the new token)
+ *   cow_pairs     int32 [num_cow_pairs][2]  (rules of pa_copy_blocks)
+ * host_out: bf16 [num_seqs][num_q_heads][head_dim], host memory.
+ * The workspace (device memory, 256-byte aligned, at least
+ * pa_step_host_workspace_size bytes) holds the staged inputs, the staged
+ * output and the decode workspace; nothing in it needs initialising.
+ * Errors: host-checkable arguments as pa_decode (no copy is issued);
+ * PA_ERR_CUDA when a copy, a launch or the synchronisation fails.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  uint64_t q, k_new, v_new, slot_mapping, block_tables, context_lens, cow_pairs;
+  uint64_t total;  /* bytes of the whole packed input */
+} pa_step_layout;
+
+typedef struct {
+  const void* host_in;        /* packed inputs (see above) */
+  void* host_out;             /* bf16 [num_seqs][num_q_heads][head_dim] */
+  void* k_cache;              /* device caches, layout of pa_decode; written */
+  void* v_cache;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t max_context_len;    /* host-known upper bound of every context length */
+  int32_t num_cow_pairs;
+  float scale;
+  int32_t variant;            /* PA_DECODE_TENSOR_CORE or PA_DECODE_CUDA_CORE */
+} pa_step_host_params;
+
+pa_status pa_step_host_layout(const pa_step_host_params* p, pa_step_layout* out);
+size_t pa_step_host_workspace_size(const pa_step_host_params* p); /* 0 if p is invalid */
+pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * pa_copy_blocks -- the data half of copy-on-write [P2 §Prefix Caching and
  * Copy-on-Write: "allocates a fresh physical block, copies the existing
  * content"]. For each pair i: block pairs[i][1] of both caches becomes a

@@ -34,6 +34,7 @@ DEVERR_APPEND_SLOT = 0x20
 EXPORTED_SYMBOLS = [
     "pa_status_string", "pa_last_error", "pa_version", "pa_device_errors",
     "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_append_decode",
+    "pa_step_host_layout", "pa_step_host_workspace_size", "pa_step_host",
     "pa_reshape_and_cache",
     "pa_copy_blocks",
     "pa_pool_create", "pa_pool_destroy", "pa_pool_alloc", "pa_pool_incref", "pa_pool_decref",
@@ -79,6 +80,24 @@ class AppendParams(ctypes.Structure):
     ]
 
 
+class StepLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in
+                ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
+                 "cow_pairs", "total")]
+
+
+class StepHostParams(ctypes.Structure):
+    _fields_ = [
+        ("host_in", ctypes.c_void_p), ("host_out", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("num_seqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
+        ("num_cow_pairs", ctypes.c_int32), ("scale", ctypes.c_float), ("variant", ctypes.c_int32),
+    ]
+
+
 class PoolStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("num_blocks", "block_size", "free_blocks", "used_blocks", "shared_blocks",
@@ -108,6 +127,9 @@ def load():
         "pa_decode": ([P(DecodeParams), vp, sz, vp], ctypes.c_int),
         "pa_decode_noalloc": ([P(DecodeParams), vp], ctypes.c_int),
         "pa_append_decode": ([P(DecodeParams), P(AppendParams), vp, sz, vp], ctypes.c_int),
+        "pa_step_host_layout": ([P(StepHostParams), P(StepLayout)], ctypes.c_int),
+        "pa_step_host_workspace_size": ([P(StepHostParams)], sz),
+        "pa_step_host": ([P(StepHostParams), vp, sz, vp], ctypes.c_int),
         "pa_reshape_and_cache": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
         "pa_copy_blocks": ([vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
         "pa_pool_create": ([i32, i32, vp, P(vp)], ctypes.c_int),
@@ -270,6 +292,77 @@ def pa_append_decode(q, k_cache, v_cache, block_tables, context_lens, max_contex
     _check(lib.pa_append_decode(ctypes.byref(p), ctypes.byref(a), ws_ptr, ws_bytes,
                                 _stream_handle(stream)), "pa_append_decode")
     return out
+
+
+def make_step_host_params(k_cache, v_cache, num_seqs: int, num_q_heads: int,
+                          max_blocks_per_seq: int, max_context_len: int, num_cow_pairs: int = 0,
+                          scale: Optional[float] = None,
+                          variant: int = DECODE_TENSOR_CORE) -> StepHostParams:
+    """Shape half of a host-driven step; host_in / host_out are set by the caller
+    (or by ``pa_step_host``)."""
+    import torch
+
+    NB, Hkv, BS, D = k_cache.shape
+    p = StepHostParams()
+    p.k_cache = _dev_ptr(k_cache, torch.bfloat16, "k_cache")
+    p.v_cache = _dev_ptr(v_cache, torch.bfloat16, "v_cache")
+    p.num_seqs, p.num_q_heads, p.num_kv_heads, p.head_dim = num_seqs, num_q_heads, Hkv, D
+    p.block_size, p.num_blocks = BS, NB
+    p.max_blocks_per_seq, p.max_context_len = max_blocks_per_seq, int(max_context_len)
+    p.num_cow_pairs = num_cow_pairs
+    p.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
+    p.variant = int(variant)
+    return p
+
+
+def pa_step_host_layout(params: StepHostParams) -> StepLayout:
+    out = StepLayout()
+    _check(load().pa_step_host_layout(ctypes.byref(params), ctypes.byref(out)),
+           "pa_step_host_layout")
+    return out
+
+
+def pa_step_host_workspace_size(params: StepHostParams) -> int:
+    return int(load().pa_step_host_workspace_size(ctypes.byref(params)))
+
+
+def pack_step_inputs(params: StepHostParams, q, k_new, v_new, slot_mapping, block_tables,
+                     context_lens, cow_pairs=None, pin: bool = True):
+    """Marshal one step's host inputs into the packed buffer of ``pa_step_host``
+    (a uint8 CPU tensor; pinned unless ``pin`` is False)."""
+    import torch
+
+    L = pa_step_host_layout(params)
+    buf = torch.zeros(int(L.total), dtype=torch.uint8, pin_memory=pin)
+    parts = [(L.q, q, torch.bfloat16), (L.k_new, k_new, torch.bfloat16),
+             (L.v_new, v_new, torch.bfloat16), (L.slot_mapping, slot_mapping, torch.int64),
+             (L.block_tables, block_tables, torch.int32), (L.context_lens, context_lens, torch.int32)]
+    if params.num_cow_pairs:
+        parts.append((L.cow_pairs, cow_pairs, torch.int32))
+    for off, t, dt in parts:
+        t = torch.as_tensor(t).to("cpu", dt).contiguous().view(torch.uint8).reshape(-1)
+        buf[int(off):int(off) + t.numel()] = t
+    return buf
+
+
+def pa_step_host(params: StepHostParams, host_in, host_out, workspace, stream=None) -> None:
+    """One whole step from host memory (see the C header): ``host_in`` is a
+    uint8 CPU tensor packed by ``pa_step_host_layout`` (pinned for speed),
+    ``host_out`` a bf16 CPU tensor [num_seqs][num_q_heads][head_dim],
+    ``workspace`` a uint8 CUDA tensor. Returns when host_out holds the result."""
+    import torch
+
+    if host_in.device.type != "cpu" or host_out.device.type != "cpu":
+        raise ValueError("host_in and host_out must be host (CPU) tensors")
+    if not host_in.is_contiguous() or not host_out.is_contiguous():
+        raise ValueError("host_in and host_out must be contiguous")
+    if host_out.dtype != torch.bfloat16 or host_in.dtype != torch.uint8:
+        raise ValueError("host_in must be uint8, host_out bf16")
+    params.host_in = host_in.data_ptr()
+    params.host_out = host_out.data_ptr()
+    ws = _dev_ptr(workspace, torch.uint8, "workspace")
+    _check(load().pa_step_host(ctypes.byref(params), ws, workspace.numel(),
+                               _stream_handle(stream)), "pa_step_host")
 
 
 def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,

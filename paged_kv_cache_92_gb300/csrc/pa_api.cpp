@@ -163,6 +163,75 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
   return PA_OK;
 }
 
+// ---- host-driven step: packed input layout and the decode params over it
+
+static pa_status check_step(const pa_step_host_params* p) {
+  if (!p) return set_error(PA_ERR_INVALID_ARG, "pa_step_host: params is NULL");
+  if (p->num_seqs < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->head_dim < 1 ||
+      p->max_blocks_per_seq < 1)
+    return set_error(PA_ERR_INVALID_ARG, "pa_step_host: counts must be positive");
+  if (p->num_cow_pairs < 0 || p->num_cow_pairs > 65535)
+    return set_error(PA_ERR_INVALID_ARG, "pa_step_host: num_cow_pairs must be in [0, 65535]");
+  return PA_OK;
+}
+
+static void step_layout(const pa_step_host_params* p, pa_step_layout* L) {
+  const size_t B = size_t(p->num_seqs), D = size_t(p->head_dim);
+  size_t off = 0;
+  auto put = [&](uint64_t& field, size_t bytes) {
+    field = off;
+    off = round_up(off + bytes, 256);
+  };
+  put(L->q, B * p->num_q_heads * D * 2);
+  put(L->k_new, B * p->num_kv_heads * D * 2);
+  put(L->v_new, B * p->num_kv_heads * D * 2);
+  put(L->slot_mapping, B * sizeof(int64_t));
+  put(L->block_tables, B * size_t(p->max_blocks_per_seq) * sizeof(int32_t));
+  put(L->context_lens, B * sizeof(int32_t));
+  put(L->cow_pairs, size_t(p->num_cow_pairs) * 2 * sizeof(int32_t));
+  L->total = off;
+}
+
+// Workspace of a host-driven step: staged input, staged output, decode workspace.
+struct StepSpace {
+  pa_step_layout in;
+  size_t out_off, dec_off, total;
+};
+
+static void step_decode_params(const pa_step_host_params* p, unsigned char* ws,
+                               const StepSpace& sp, pa_decode_params* d) {
+  std::memset(d, 0, sizeof(*d));
+  d->q = ws ? ws + sp.in.q : nullptr;
+  d->out = ws ? ws + sp.out_off : nullptr;
+  d->k_cache = p->k_cache;
+  d->v_cache = p->v_cache;
+  d->block_tables = ws ? reinterpret_cast<const int32_t*>(ws + sp.in.block_tables) : nullptr;
+  d->context_lens = ws ? reinterpret_cast<const int32_t*>(ws + sp.in.context_lens) : nullptr;
+  d->max_blocks_per_seq = p->max_blocks_per_seq;
+  d->num_seqs = p->num_seqs;
+  d->num_q_heads = p->num_q_heads;
+  d->num_kv_heads = p->num_kv_heads;
+  d->head_dim = p->head_dim;
+  d->block_size = p->block_size;
+  d->num_blocks = p->num_blocks;
+  d->max_context_len = p->max_context_len;
+  d->scale = p->scale;
+  d->partition_tokens = 0;
+  d->variant = p->variant;
+  d->overlap_prologue = 0;
+}
+
+static StepSpace step_space(const pa_step_host_params* p, const pa_decode_params& d, int np,
+                            int grid) {
+  StepSpace sp;
+  step_layout(p, &sp.in);
+  sp.out_off = sp.in.total;
+  const size_t out_bytes = size_t(p->num_seqs) * p->num_q_heads * p->head_dim * 2;
+  sp.dec_off = round_up(sp.out_off + out_bytes, 256);
+  sp.total = sp.dec_off + decode_workspace_layout(&d, np, grid).total;
+  return sp;
+}
+
 }  // namespace pa
 
 extern "C" {
@@ -264,6 +333,75 @@ pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
     return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: workspace must be 256-byte aligned");
   return pa::run_decode(p, static_cast<unsigned char*>(workspace), w, np, grid, stream,
                         "pa_append_decode", a);
+}
+
+pa_status pa_step_host_layout(const pa_step_host_params* p, pa_step_layout* out) {
+  pa_status st = pa::check_step(p);
+  if (st != PA_OK) return st;
+  if (!out) return pa::set_error(PA_ERR_INVALID_ARG, "pa_step_host_layout: out is NULL");
+  pa::step_layout(p, out);
+  return PA_OK;
+}
+
+size_t pa_step_host_workspace_size(const pa_step_host_params* p) {
+  if (pa::check_step(p) != PA_OK) return 0;
+  pa_decode_params d;
+  pa::step_decode_params(p, nullptr, pa::StepSpace{}, &d);
+  if (pa::check_decode(&d, false) != PA_OK) return 0;
+  return pa::step_space(p, d, pa::num_partitions_for(&d), pa::tc_grid()).total;
+}
+
+pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream) {
+  pa_status st = pa::check_step(p);
+  if (st != PA_OK) return st;
+  if (!p->host_in || !p->host_out || !p->k_cache || !p->v_cache)
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_step_host: a required pointer is NULL");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_step_host: workspace must be 256-byte aligned");
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  pa_decode_params d;
+  pa::step_decode_params(p, nullptr, pa::StepSpace{}, &d);
+  st = pa::check_decode(&d, false);
+  if (st != PA_OK) return st;
+  const int np = pa::num_partitions_for(&d);
+  const int grid = pa::tc_grid();
+  const pa::StepSpace sp = pa::step_space(p, d, np, grid);
+  if (workspace_bytes < sp.total)
+    return pa::set_error(PA_ERR_INVALID_ARG,
+                         "pa_step_host: workspace smaller than pa_step_host_workspace_size()");
+  if (p->num_seqs == 0 && p->num_cow_pairs == 0) return PA_OK;
+  pa::step_decode_params(p, ws, sp, &d);
+  st = pa::check_decode(&d, true);
+  if (st != PA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(ws, p->host_in, sp.in.total, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: input copy", int(e));
+  if (p->num_cow_pairs > 0) {
+    const int r = pa::launch_copy_blocks(p->k_cache, p->v_cache,
+                                         reinterpret_cast<const int32_t*>(ws + sp.in.cow_pairs),
+                                         p->num_cow_pairs, p->num_kv_heads, p->head_dim,
+                                         p->num_blocks, stream);
+    if (r != 0) return pa::set_cuda_error("pa_step_host: copy_blocks launch", r);
+  }
+  if (p->num_seqs > 0) {
+    pa_append_params a;
+    a.k_new = ws + sp.in.k_new;
+    a.v_new = ws + sp.in.v_new;
+    a.slot_mapping = reinterpret_cast<const int64_t*>(ws + sp.in.slot_mapping);
+    a.k_cache = p->k_cache;
+    a.v_cache = p->v_cache;
+    const pa::WorkspaceLayout w = pa::decode_workspace_layout(&d, np, grid);
+    st = pa::run_decode(&d, ws + sp.dec_off, w, np, grid, stream, "pa_step_host", &a);
+    if (st != PA_OK) return st;
+    e = cudaMemcpyAsync(p->host_out, ws + sp.out_off,
+                        size_t(p->num_seqs) * p->num_q_heads * p->head_dim * 2,
+                        cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: output copy", int(e));
+  }
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: synchronize", int(e));
+  return PA_OK;
 }
 
 pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,

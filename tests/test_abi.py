@@ -142,3 +142,31 @@ def test_append_decode_rejects_bad_arguments_on_the_host(pk):
     assert b"workspace" in lib.pa_last_error()
     p.head_dim = 96
     assert lib.pa_append_decode(ctypes.byref(p), ctypes.byref(a), None, 0, None) == 2
+
+
+def test_step_host_layout_and_workspace(pk):
+    """The packed-input layout of pa_step_host: sections in header order, each
+    256-byte aligned and exactly large enough; the workspace holds the staged
+    input, the staged output and a decode workspace."""
+    lib = pk.load()
+    p = pk.StepHostParams()
+    p.num_seqs, p.num_q_heads, p.num_kv_heads, p.head_dim = 3, 8, 2, 128
+    p.block_size, p.num_blocks, p.max_blocks_per_seq, p.max_context_len = 16, 10, 5, 80
+    p.num_cow_pairs, p.scale = 2, 0.088
+    L = pk.StepLayout()
+    assert lib.pa_step_host_layout(ctypes.byref(p), ctypes.byref(L)) == 0
+    sizes = [3 * 8 * 128 * 2, 3 * 2 * 128 * 2, 3 * 2 * 128 * 2, 3 * 8, 3 * 5 * 4, 3 * 4, 2 * 8]
+    offs = [L.q, L.k_new, L.v_new, L.slot_mapping, L.block_tables, L.context_lens, L.cow_pairs]
+    assert offs[0] == 0
+    for i in range(len(offs)):
+        assert offs[i] % 256 == 0
+        end = offs[i + 1] if i + 1 < len(offs) else L.total
+        assert end == _ru(offs[i] + sizes[i])
+    dec = _params(pk, num_seqs=3, num_q_heads=8, num_kv_heads=2, max_blocks_per_seq=5,
+                  max_context_len=80, num_blocks=10)
+    want = _ru(L.total + 3 * 8 * 128 * 2) + lib.pa_decode_workspace_size(ctypes.byref(dec))
+    assert lib.pa_step_host_workspace_size(ctypes.byref(p)) == want
+    assert lib.pa_step_host(ctypes.byref(p), None, 0, None) == 1  # NULL buffers
+    p.num_cow_pairs = 70000
+    assert lib.pa_step_host_layout(ctypes.byref(p), ctypes.byref(L)) == 1
+    assert lib.pa_step_host_workspace_size(ctypes.byref(p)) == 0

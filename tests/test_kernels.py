@@ -458,3 +458,33 @@ def test_fused_append_slot_rules(pk, variant):
     got = harness.bf16_tensor_to_f64(out)
     harness.assert_close(got[:3].reshape(24, -1), ref)
     assert not got[3].any()
+
+
+# ---------------------------------------------------------------- host-driven step
+
+@VARIANTS
+@pytest.mark.parametrize("name", ["tiny", "llama8b_layer", "shared_prefix"])
+def test_step_host_matches_device_step(pk, name, variant):
+    """pa_step_host (packed host inputs in, host output back, one call) gives
+    the device-side step's output and caches bit for bit; the caches also
+    match the oracle's copy-on-write + KV write."""
+    import torch
+
+    case = harness.build_case(FUSED_CASES[name]())
+    want, kw, vw = harness.run_step_gpu(case, variant=variant, fused_append=True)
+    kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    B, Hq, D = case.q.shape
+    p = pk.make_step_host_params(kc, vc, B, Hq, case.tables.shape[1], int(case.lens.max()),
+                                 num_cow_pairs=len(case.cows), variant=variant)
+    host_in = pk.pack_step_inputs(p, case.q.cpu(), case.k_new.cpu(), case.v_new.cpu(), case.slots,
+                                  case.tables, case.lens, case.cows if len(case.cows) else None)
+    host_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    ws = torch.empty(pk.pa_step_host_workspace_size(p), dtype=torch.uint8, device="cuda")
+    pk.pa_step_host(p, host_in, host_out, ws)
+    assert torch.equal(host_out.view(torch.int16), want.cpu().view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kw.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vw.view(torch.int16))
+    ko, vo = harness.oracle_caches(case)
+    assert np.array_equal(oracle.bf16_bits(kc.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc.cpu()), vo)
+    _check_errors(pk)
