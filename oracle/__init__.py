@@ -62,6 +62,16 @@ def _load():
         lib.oracle_copy_blocks.argtypes = [p, p, p, i32, i32, i32, i32, i32]
         lib.oracle_copy_blocks.restype = ctypes.c_int
         lib.oracle_num_threads.restype = ctypes.c_int
+        u8 = ctypes.c_uint8
+        lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_from_float.restype = u8
+        lib.oracle_e4m3_to_double.argtypes = [u8]
+        lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_reshape_and_cache_fp8.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32]
+        lib.oracle_reshape_and_cache_fp8.restype = ctypes.c_int
+        lib.oracle_paged_decode_fp8.argtypes = [p, p, p, p, p, p, i32, p, i32, i32, i32, i32,
+                                                i32, i32, ctypes.c_double, p, i64, p, p]
+        lib.oracle_paged_decode_fp8.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -239,6 +249,87 @@ def copy_blocks(k_cache, v_cache, pairs) -> Tuple[np.ndarray, np.ndarray]:
     if rc != 0:
         raise ValueError(f"oracle_copy_blocks failed with code {rc}")
     return kc, vc
+
+
+# --------------------------------------------------------------------------
+# 8-bit (FP8 E4M3) KV cache: K [block][head][offset][d], V [block][head][d][offset]
+# --------------------------------------------------------------------------
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Exact value of E4M3 codes (NaN for the two NaN codes)."""
+    lib = _load()
+    table = np.array([lib.oracle_e4m3_to_double(c) for c in range(256)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_from_f32(x) -> np.ndarray:
+    """float32 -> E4M3 codes, round to nearest even, saturating (element by element)."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float32)
+    return np.array([lib.oracle_e4m3_from_float(float(v)) for v in a.reshape(-1)],
+                    dtype=np.uint8).reshape(a.shape)
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale, v_scale
+                          ) -> Tuple[np.ndarray, np.ndarray]:
+    """Quantising KV write into an E4M3 cache. Returns new (k_cache, v_cache) uint8 arrays."""
+    lib = _load()
+    kn, vn = bf16_bits(k_new), bf16_bits(v_new)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8).copy()
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8).copy()
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    NB, Hkv, BS, D = kc.shape
+    rc = lib.oracle_reshape_and_cache_fp8(_ptr(kn), _ptr(vn), _ptr(kc), _ptr(vc), _ptr(sm),
+                                          _ptr(ks), _ptr(vs), sm.shape[0], Hkv, D, BS, NB)
+    if rc != 0:
+        raise ValueError(f"oracle_reshape_and_cache_fp8 failed with code {rc}")
+    return kc, vc
+
+
+def paged_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                     scale: Optional[float] = None, units=None):
+    """Decode over an E4M3 cache: K/V dequantised exactly (code value x head scale)."""
+    lib = _load()
+    qb = bf16_bits(q)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, Hq, D = qb.shape
+    NB, Hkv, BS, D2 = kc.shape
+    if D2 != D or vc.shape != kc.shape:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if units is None:
+        u, n = None, B * Hq
+        out = np.empty((B, Hq, D), dtype=np.float64)
+    else:
+        u = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
+        n = u.shape[0]
+        out = np.empty((n, D), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    rc = lib.oracle_paged_decode_fp8(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
+                                     bt.shape[1], _ptr(cl), B, Hq, Hkv, D, BS, NB, float(scale),
+                                     None if u is None else _ptr(u), n, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_decode_fp8 failed with code {rc}")
+    return out
+
+
+def copy_blocks_fp8(k_cache, v_cache, pairs) -> Tuple[np.ndarray, np.ndarray]:
+    """Block copy of an E4M3 cache (a byte copy of whole blocks, as for bf16)."""
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    NB, Hkv, BS, D = kc.shape
+    k2, v2 = copy_blocks(kc.view(np.uint16), vc.view(np.uint16), pairs)
+    return k2.view(np.uint8).reshape(kc.shape), v2.view(np.uint8).reshape(vc.shape)
 
 
 # --------------------------------------------------------------------------

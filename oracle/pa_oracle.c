@@ -33,6 +33,19 @@
  *
  * bf16 values are widened to double exactly (the bf16 bit pattern is the
  * top half of an IEEE float).
+ *
+ * 8-bit KV cache ("PagedAttention" glossary page, §What paging costs: paging
+ * combines with 8-bit KV quantisation, which halves the bytes per block).
+ * The pages fix no format; this oracle follows the reading the library
+ * implements: FP8 E4M3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits, subnormals, no infinities, S.1111.111 is NaN, largest finite 448)
+ * with one dequantisation scale per KV head for K and one for V:
+ *  - write: code = E4M3(x / scale[h]), the division in float32 and the
+ *    conversion round-to-nearest-even, saturating finite values (and
+ *    infinities) to +-448, NaN to 0x7F;
+ *  - read: value = decode(code) * scale[h], in double;
+ *  - layout: K as the bf16 cache, [block][head][offset][d]; V transposed
+ *    inside each (block, head) tile, [block][head][d][offset].
  */
 #include <math.h>
 #include <stdint.h>
@@ -51,6 +64,50 @@ static double bf16_bits_to_double(uint16_t bits) {
   return (double)f;
 }
 
+/* E4M3 code -> value (exact in double). */
+static double e4m3_to_double(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9); /* subnormal: m/8 * 2^(1-7) */
+  else
+    v = ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* float32 -> E4M3, round to nearest even, saturating to the largest finite
+ * value; NaN -> 0x7F. Works on the exact value of the float. */
+static uint8_t e4m3_from_float(float xf) {
+  const double x = (double)xf;
+  if (x != x) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E;
+  /* candidates on the grid of this binade: the spacing is 2^(e-3) for a
+   * normal value with exponent e, 2^-9 below 2^-6 */
+  int e;
+  (void)frexp(a, &e); /* a = f * 2^e, f in [0.5, 1) -> a in [2^(e-1), 2^e) */
+  const int ue = e - 1; /* unbiased exponent of a */
+  const double spacing = ue < -6 ? ldexp(1.0, -9) : ldexp(1.0, ue - 3);
+  const double k = a / spacing; /* exact: a power-of-two division */
+  double r = floor(k);
+  const double frac = k - r;
+  if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  const double v = r * spacing; /* the rounded magnitude */
+  if (v >= 448.0 + 32.0) return sign | 0x7E; /* would be 480: saturate */
+  /* encode v */
+  if (v < ldexp(1.0, -6)) return sign | (uint8_t)(v / ldexp(1.0, -9)); /* subnormal (or 0) */
+  int ve;
+  (void)frexp(v, &ve);
+  const int vue = ve - 1;
+  const int man = (int)(v / ldexp(1.0, vue - 3)) - 8;
+  return sign | (uint8_t)(((vue + 7) << 3) | man);
+}
+
+uint8_t oracle_e4m3_from_float(float x) { return e4m3_from_float(x); }
+double oracle_e4m3_to_double(uint8_t c) { return e4m3_to_double(c); }
+
 /* Address of (physical block, kv head, offset in block) in a cache array. */
 static size_t cache_row(int64_t blk, int32_t kv_head, int32_t off, int32_t num_kv_heads,
                         int32_t block_size, int32_t head_dim) {
@@ -63,7 +120,27 @@ static size_t cache_row(int64_t blk, int32_t kv_head, int32_t off, int32_t num_k
  * out_row: head_dim doubles. lse_out (nullable): log sum_i exp(score_i).
  * Returns ORACLE_OK or an error code.
  */
-static int decode_one(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+/* Element c of row (blk, head, off) of K and of V, as double, for a bf16
+ * cache (fp8 == 0) or an E4M3 cache with per-head scales (fp8 == 1). */
+static void kv_element(const void* k_cache, const void* v_cache, int fp8, const float* k_scale,
+                       const float* v_scale, int64_t blk, int32_t g, int32_t off, int32_t c,
+                       int32_t num_kv_heads, int32_t block_size, int32_t head_dim, double* k,
+                       double* v) {
+  const size_t row = cache_row(blk, g, off, num_kv_heads, block_size, head_dim);
+  if (!fp8) {
+    *k = bf16_bits_to_double(((const uint16_t*)k_cache)[row + c]);
+    *v = bf16_bits_to_double(((const uint16_t*)v_cache)[row + c]);
+    return;
+  }
+  /* V is transposed inside its (block, head) tile: [d][offset] */
+  const size_t tile = ((size_t)blk * num_kv_heads + g) * (size_t)block_size * head_dim;
+  *k = e4m3_to_double(((const uint8_t*)k_cache)[row + c]) * (double)k_scale[g];
+  *v = e4m3_to_double(((const uint8_t*)v_cache)[tile + (size_t)c * block_size + off]) *
+       (double)v_scale[g];
+}
+
+static int decode_one(const uint16_t* q, const void* k_cache, const void* v_cache, int fp8,
+                      const float* k_scale, const float* v_scale,
                       const int32_t* block_tables, int32_t max_blocks_per_seq,
                       const int32_t* context_lens, int32_t num_q_heads, int32_t num_kv_heads,
                       int32_t head_dim, int32_t block_size, int32_t num_blocks, double scale,
@@ -91,11 +168,9 @@ static int decode_one(const uint16_t* q, const uint16_t* k_cache, const uint16_t
       rc = ORACLE_OUT_OF_RANGE;
       break;
     }
-    const size_t row = cache_row(blk, g, off, num_kv_heads, block_size, head_dim);
-    for (int32_t c = 0; c < head_dim; ++c) {
-      K[(size_t)t * head_dim + c] = bf16_bits_to_double(k_cache[row + c]);
-      V[(size_t)t * head_dim + c] = bf16_bits_to_double(v_cache[row + c]);
-    }
+    for (int32_t c = 0; c < head_dim; ++c)
+      kv_element(k_cache, v_cache, fp8, k_scale, v_scale, blk, g, off, c, num_kv_heads,
+                 block_size, head_dim, &K[(size_t)t * head_dim + c], &V[(size_t)t * head_dim + c]);
   }
   if (rc == ORACLE_OK) {
     const uint16_t* qrow = q + ((size_t)b * num_q_heads + h) * head_dim;
@@ -140,7 +215,8 @@ static int decode_one(const uint16_t* q, const uint16_t* k_cache, const uint16_t
  *   lse          double [n_units] (nullable)
  * OpenMP parallelises over units; each unit is computed independently.
  */
-int oracle_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+static int paged_decode(const uint16_t* q, const void* k_cache, const void* v_cache, int fp8,
+                        const float* k_scale, const float* v_scale,
                         const int32_t* block_tables, int32_t max_blocks_per_seq,
                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
@@ -163,15 +239,42 @@ int oracle_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16
     }
     int r = ORACLE_BAD_ARG;
     if (b >= 0 && b < num_seqs && h >= 0 && h < num_q_heads)
-      r = decode_one(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, b, h,
-                     out + (size_t)u * head_dim, lse ? lse + u : NULL);
+      r = decode_one(q, k_cache, v_cache, fp8, k_scale, v_scale, block_tables,
+                     max_blocks_per_seq, context_lens, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, scale, b, h, out + (size_t)u * head_dim,
+                     lse ? lse + u : NULL);
     if (r != ORACLE_OK) {
 #pragma omp critical
       rc = r;
     }
   }
   return rc;
+}
+
+int oracle_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int32_t num_blocks, double scale, const int32_t* units, int64_t n_units,
+                        double* out, double* lse) {
+  return paged_decode(q, k_cache, v_cache, 0, NULL, NULL, block_tables, max_blocks_per_seq,
+                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, scale, units, n_units, out, lse);
+}
+
+/* The same decode over an E4M3 cache (k/v_cache uint8, layouts above) with
+ * per-KV-head scales k_scale, v_scale (float [num_kv_heads]). */
+int oracle_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                            const float* k_scale, const float* v_scale,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, double scale, const int32_t* units,
+                            int64_t n_units, double* out, double* lse) {
+  if (!k_scale || !v_scale) return ORACLE_BAD_ARG;
+  return paged_decode(q, k_cache, v_cache, 1, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, scale, units, n_units, out, lse);
 }
 
 /*
@@ -194,6 +297,38 @@ int oracle_reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new, uint1
       const size_t dst = cache_row(blk, h, off, num_kv_heads, block_size, head_dim);
       memcpy(k_cache + dst, k_new + src, sizeof(uint16_t) * (size_t)head_dim);
       memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)head_dim);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * KV write into an E4M3 cache: token t's row of KV head h is quantised with
+ * that head's scale (code = E4M3(float32(x) / scale[h])) and stored at
+ * (slot / BS, h, slot % BS) -- K as a row, V as a column of its transposed
+ * (block, head) tile. A negative slot means "no write".
+ */
+int oracle_reshape_and_cache_fp8(const uint16_t* k_new, const uint16_t* v_new, uint8_t* k_cache,
+                                 uint8_t* v_cache, const int64_t* slot_mapping,
+                                 const float* k_scale, const float* v_scale, int32_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int32_t num_blocks) {
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= (int64_t)num_blocks * block_size) return ORACLE_OUT_OF_RANGE;
+    const int64_t blk = slot / block_size;
+    const int32_t off = (int32_t)(slot % block_size);
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      const size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+      const size_t row = cache_row(blk, h, off, num_kv_heads, block_size, head_dim);
+      const size_t tile = ((size_t)blk * num_kv_heads + h) * (size_t)block_size * head_dim;
+      for (int32_t c = 0; c < head_dim; ++c) {
+        const float kx = (float)bf16_bits_to_double(k_new[src + c]) / k_scale[h];
+        const float vx = (float)bf16_bits_to_double(v_new[src + c]) / v_scale[h];
+        k_cache[row + c] = e4m3_from_float(kx);
+        v_cache[tile + (size_t)c * block_size + off] = e4m3_from_float(vx);
+      }
     }
   }
   return ORACLE_OK;

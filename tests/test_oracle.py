@@ -452,3 +452,136 @@ def test_double_free_and_bad_ids():
         pool.decref(blk)
     with pytest.raises(oracle.PoolError):
         pool.incref(7)
+
+
+# ---------------------------------------------------------------- 8-bit (E4M3) KV cache
+# The pages only say that 8-bit KV quantisation halves the bytes per block
+# ("PagedAttention" glossary page, §What paging costs); the format pinned here
+# is the library's reading: OCP FP8 E4M3 with per-KV-head scales.
+
+E4M3 = getattr(torch, "float8_e4m3fn", None)
+needs_torch_fp8 = pytest.mark.skipif(E4M3 is None, reason="torch without float8_e4m3fn")
+
+
+def test_e4m3_decode_landmarks():
+    """Values the E4M3 definition fixes: zero, the smallest subnormal and normal,
+    one, the largest finite value, exactly two NaN codes, sign symmetry, and a
+    strictly increasing positive range."""
+    t = oracle.e4m3_to_f64(np.arange(256))
+    assert t[0x00] == 0.0 and np.signbit(t[0x80])
+    assert t[0x01] == 2.0 ** -9 and t[0x07] == 7 * 2.0 ** -9
+    assert t[0x08] == 2.0 ** -6 and t[0x38] == 1.0 and t[0x7E] == 448.0
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF]) and np.isnan(t).sum() == 2
+    assert np.all(np.diff(t[:0x7F]) > 0)
+    assert np.array_equal(t[0x80:0xFF], -t[0x00:0x7F])
+    # eight evenly spaced values per binade above the subnormals
+    for e in range(-6, 9):
+        vals = t[(e + 7) * 8:(e + 7) * 8 + (8 if e < 8 else 7)]  # the last code is NaN
+        assert np.allclose(np.diff(vals), 2.0 ** (e - 3)) and vals[0] == 2.0 ** e
+
+
+@needs_torch_fp8
+def test_e4m3_decode_matches_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    want = codes.view(E4M3).to(torch.float64).numpy()
+    got = oracle.e4m3_to_f64(np.arange(256))
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+
+
+@needs_torch_fp8
+def test_e4m3_encoder_matches_torch_in_range_and_saturates():
+    """Round to nearest even, compared with torch's float32 -> float8_e4m3fn cast
+    on random values, exact ties and subnormals (|x| < 448, where the two agree
+    by definition); beyond 448 the encoder saturates (torch does not)."""
+    rng = np.random.default_rng(11)
+    grid = oracle.e4m3_to_f64(np.arange(0x7F))
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)  # exact ties (representable)
+    x = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * 30,
+        (rng.standard_normal(2000) * 2.0 ** -8).astype(np.float32),
+        mids, -mids, np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(0)),
+        grid[:0x7F].astype(np.float32),
+    ])
+    x = x[np.abs(x) < 448]
+    want = torch.from_numpy(x).to(E4M3).view(torch.uint8).numpy()
+    got = oracle.e4m3_from_f32(x)
+    assert np.array_equal(got, want)
+    sat = oracle.e4m3_from_f32(np.array([448.0, 463.9, 464.0, 1e6, np.inf, -500.0, -np.inf],
+                                        dtype=np.float32))
+    assert list(sat) == [0x7E] * 5 + [0xFE] * 2
+    assert oracle.e4m3_from_f32(np.array([np.nan], dtype=np.float32))[0] == 0x7F
+
+
+def _fp8_case(seed, B=3, Hq=8, Hkv=2, D=16, BS=4, lens=(1, 6, 11), scales=(0.5, 2.0)):
+    q, kc, vc, tables, lens = _random_case(seed, B=B, Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens)
+    ks = np.array([scales[0] * (h + 1) for h in range(Hkv)], dtype=np.float32)
+    vs = np.array([scales[1] / (h + 1) for h in range(Hkv)], dtype=np.float32)
+    # fill the whole pool through the quantising write, one slot per token
+    NB = kc.shape[0]
+    slots = np.arange(NB * BS, dtype=np.int64)
+    kn = _bf16((NB * BS, Hkv, D), seed + 7)
+    vn = _bf16((NB * BS, Hkv, D), seed + 8)
+    k8, v8 = oracle.reshape_and_cache_fp8(kn, vn, np.zeros((NB, Hkv, BS, D), np.uint8),
+                                          np.zeros((NB, Hkv, BS, D), np.uint8), slots, ks, vs)
+    return q, k8, v8, ks, vs, tables, lens, kn, vn
+
+
+@needs_torch_fp8
+def test_fp8_write_quantises_per_head_and_transposes_v():
+    """code = E4M3(float32(x) / scale[h]) (torch's cast, in range here); K rows
+    at (block, head, offset), V stored as column `offset` of the (block, head)
+    tile [d][offset]; negative slots write nothing."""
+    q, k8, v8, ks, vs, tables, lens, kn, vn = _fp8_case(21)
+    NB, Hkv, BS, D = k8.shape
+    kx = torch.from_numpy(oracle.bf16_to_f64(kn).astype(np.float32)) / torch.from_numpy(ks)[:, None]
+    vx = torch.from_numpy(oracle.bf16_to_f64(vn).astype(np.float32)) / torch.from_numpy(vs)[:, None]
+    kcode = kx.to(E4M3).view(torch.uint8).numpy()  # [slot][h][d]
+    vcode = vx.to(E4M3).view(torch.uint8).numpy()
+    for slot in (0, 5, NB * BS - 1):
+        blk, off = divmod(slot, BS)
+        for h in range(Hkv):
+            assert np.array_equal(k8[blk, h, off, :], kcode[slot, h])
+            assert np.array_equal(v8.reshape(NB, Hkv, D, BS)[blk, h, :, off], vcode[slot, h])
+    k2, v2 = oracle.reshape_and_cache_fp8(kn[:2], vn[:2], k8, v8, np.array([-1, -7]), ks, vs)
+    assert np.array_equal(k2, k8) and np.array_equal(v2, v8)
+
+
+def test_fp8_decode_equals_bf16_oracle_on_the_dequantised_cache():
+    """With power-of-two scales every dequantised value (code value x scale) is
+    exactly a bf16 value, so the 8-bit decode must equal the bf16 oracle run
+    on a bf16 cache holding those values (V transposed back)."""
+    q, k8, v8, ks, vs, tables, lens, _, _ = _fp8_case(22, scales=(0.25, 4.0))
+    ks = np.array([0.25, 0.5], dtype=np.float32)
+    vs = np.array([4.0, 2.0], dtype=np.float32)
+    NB, Hkv, BS, D = k8.shape
+    kd = oracle.e4m3_to_f64(k8) * ks[None, :, None, None]
+    vd = (oracle.e4m3_to_f64(v8).reshape(NB, Hkv, D, BS) * vs[None, :, None, None]).transpose(0, 1, 3, 2)
+    kb = torch.from_numpy(np.ascontiguousarray(kd)).to(torch.bfloat16)
+    vb = torch.from_numpy(np.ascontiguousarray(vd)).to(torch.bfloat16)
+    assert np.array_equal(oracle.bf16_to_f64(kb), kd) and np.array_equal(oracle.bf16_to_f64(vb), vd)
+    want = oracle.paged_decode(q, kb, vb, tables, lens)
+    got = oracle.paged_decode_fp8(q, k8, v8, ks, vs, tables, lens)
+    assert np.abs(got - want).max() < 1e-12
+
+
+def test_fp8_decode_scales_act_as_the_definition_says():
+    """k_scale multiplies every score of its head (so doubling it equals
+    doubling the softmax scale for those heads' queries) and v_scale scales
+    the output linearly."""
+    q, k8, v8, ks, vs, tables, lens, _, _ = _fp8_case(23)
+    base = oracle.paged_decode_fp8(q, k8, v8, ks, vs, tables, lens)
+    two_k = oracle.paged_decode_fp8(q, k8, v8, ks * 2, vs, tables, lens)
+    D = q.shape[2]
+    twice_scale = oracle.paged_decode_fp8(q, k8, v8, ks, vs, tables, lens, scale=2 / math.sqrt(D))
+    assert np.abs(two_k - twice_scale).max() < 1e-12
+    assert np.abs(two_k - base).max() > 1e-3
+    three_v = oracle.paged_decode_fp8(q, k8, v8, ks, vs * 3, tables, lens)
+    assert np.abs(three_v - 3 * base).max() < 1e-12
+
+
+def test_fp8_copy_blocks_is_a_byte_copy():
+    _, k8, v8, *_ = _fp8_case(24)
+    k2, v2 = oracle.copy_blocks_fp8(k8, v8, [[1, 4], [2, 0]])
+    assert np.array_equal(k2[4], k8[1]) and np.array_equal(v2[0], v8[2])
+    assert np.array_equal(k2[3], k8[3])
