@@ -137,12 +137,31 @@ typedef struct {
                                   while that kernel still runs (programmatic dependent launch).
                                   q, the caches and every output are touched only after the
                                   previous kernel has completed. 0 = plain stream order. */
+  int32_t kv_dtype;            /* PA_KV_BF16 (0, default) or PA_KV_FP8_E4M3 (1) */
+  const float* k_scale;        /* PA_KV_FP8_E4M3 only: device float [num_kv_heads], the
+                                  dequantisation scale of each KV head's K (value = code * scale) */
+  const float* v_scale;        /* the same for V */
 } pa_decode_params;
 
 /* Decode kernel variants; both compute the same function. The tensor-core
  * kernel handles num_kv_heads in {1, 2, 4, 8}, num_q_heads <= 64 and up to
  * 16384 sequences per call; other shapes run on the CUDA-core kernel
  * whatever `variant` says. */
+/* Cache element types. PA_KV_FP8_E4M3 -- the 8-bit KV cache ("PagedAttention"
+ * glossary page, §What paging costs: 8-bit KV quantisation halves the bytes per
+ * block; the format is this library's reading): OCP E4M3 codes (uint8) with one
+ * dequantisation scale per KV head for K and for V.
+ *   k_cache  uint8 [num_blocks][num_kv_heads][block_size][head_dim]
+ *   v_cache  uint8 [num_blocks][num_kv_heads][head_dim][block_size]  (V^T per tile)
+ * Written by pa_reshape_and_cache_fp8, copied by pa_copy_blocks_fp8. The decode
+ * computes on the tensor cores (variant PA_DECODE_TENSOR_CORE, head_dim 128; the
+ * rest of the tensor-core shape rules apply, other shapes return
+ * PA_ERR_UNSUPPORTED) with the queries and the softmax weights each split into
+ * two E4M3 terms, so the result is within the bf16 tolerance of the exact decode
+ * over the dequantised cache. */
+#define PA_KV_BF16 0
+#define PA_KV_FP8_E4M3 1
+
 #define PA_DECODE_TENSOR_CORE 0 /* tcgen05 MMAs, TMEM accumulators, tensor-map TMA ring */
 #define PA_DECODE_CUDA_CORE 1   /* fp32 FMAs on CUDA cores, 1-D bulk-copy rings */
 
@@ -288,6 +307,29 @@ pa_status pa_step_host_layout(const pa_step_host_params* p, pa_step_layout* out)
 size_t pa_step_host_workspace_size(const pa_step_host_params* p); /* 0 if p is invalid */
 pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t workspace_bytes,
                        pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_reshape_and_cache_fp8 -- the KV write into an 8-bit (PA_KV_FP8_E4M3)
+ * cache: for token t and KV head h,
+ *   code = E4M3(float32(x) / scale[h])   (round to nearest even; finite values
+ *                                         beyond +-448 saturate)
+ * K codes go to row (slot / block_size, h, slot % block_size); V codes to
+ * column slot % block_size of the tile [h][d][offset] of block slot /
+ * block_size. k_scale, v_scale: device float [num_kv_heads]. Otherwise as
+ * pa_reshape_and_cache (negative slots skipped, out-of-range slots set
+ * PA_DEVERR_SLOT). head_dim a multiple of 8.
+ * ---------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                   void* v_cache, const int64_t* slot_mapping,
+                                   const float* k_scale, const float* v_scale,
+                                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t num_blocks, pa_stream_t stream);
+
+/* pa_copy_blocks for an 8-bit cache: the same whole-block copy of both caches
+ * (block_size * head_dim bytes per KV head). */
+pa_status pa_copy_blocks_fp8(void* k_cache, void* v_cache, const int32_t* pairs,
+                             int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_copy_blocks -- the data half of copy-on-write [P2 §Prefix Caching and

@@ -303,7 +303,7 @@ def paged_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, contex
     cl = np.ascontiguousarray(context_lens, dtype=np.int32)
     B, Hq, D = qb.shape
     NB, Hkv, BS, D2 = kc.shape
-    if D2 != D or vc.shape != kc.shape:
+    if D2 != D or vc.size != kc.size:  # V^T tiles: [NB][Hkv][D][BS], the same bytes
         raise ValueError("shape mismatch")
     if scale is None:
         scale = 1.0 / math.sqrt(D)

@@ -31,11 +31,14 @@ DEVERR_COPY_PAIR = 0x8
 DEVERR_TIMEOUT = 0x10
 DEVERR_APPEND_SLOT = 0x20
 
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+
 EXPORTED_SYMBOLS = [
     "pa_status_string", "pa_last_error", "pa_version", "pa_device_errors",
     "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_append_decode",
     "pa_step_host_layout", "pa_step_host_workspace_size", "pa_step_host",
-    "pa_reshape_and_cache",
+    "pa_reshape_and_cache", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8",
     "pa_copy_blocks",
     "pa_pool_create", "pa_pool_destroy", "pa_pool_alloc", "pa_pool_incref", "pa_pool_decref",
     "pa_pool_refcount", "pa_pool_stats", "pa_seq_create", "pa_seq_free", "pa_seq_fork",
@@ -65,6 +68,7 @@ class DecodeParams(ctypes.Structure):
         ("num_blocks", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
         ("scale", ctypes.c_float), ("partition_tokens", ctypes.c_int32),
         ("variant", ctypes.c_int32), ("overlap_prologue", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -132,6 +136,9 @@ def load():
         "pa_step_host": ([P(StepHostParams), vp, sz, vp], ctypes.c_int),
         "pa_reshape_and_cache": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
         "pa_copy_blocks": ([vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
+        "pa_reshape_and_cache_fp8": ([vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp],
+                                     ctypes.c_int),
+        "pa_copy_blocks_fp8": ([vp, vp, vp, i32, i32, i32, i32, i32, vp], ctypes.c_int),
         "pa_pool_create": ([i32, i32, vp, P(vp)], ctypes.c_int),
         "pa_pool_destroy": ([vp], None),
         "pa_pool_alloc": ([vp, P(i32)], ctypes.c_int),
@@ -194,20 +201,33 @@ def _stream_handle(stream) -> Optional[int]:
 def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
                        max_context_len: int, scale: Optional[float] = None,
                        partition_tokens: int = 0, variant: int = DECODE_TENSOR_CORE,
-                       overlap_prologue: bool = False) -> DecodeParams:
+                       overlap_prologue: bool = False, k_scale=None,
+                       v_scale=None) -> DecodeParams:
+    """Marshal a pa_decode call. bf16 caches [NB][Hkv][BS][D]; uint8 caches are
+    the 8-bit E4M3 cache (K [NB][Hkv][BS][D], V^T [NB][Hkv][D][BS]) and need
+    k_scale / v_scale, float32 CUDA tensors [Hkv]."""
     import torch
 
     B, Hq, D = q.shape
+    fp8 = k_cache.dtype == torch.uint8
     NB, Hkv, BS, D2 = k_cache.shape
-    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, Hq, D):
+    v_want = (NB, Hkv, D2, BS) if fp8 else tuple(k_cache.shape)
+    if D2 != D or tuple(v_cache.shape) != v_want or tuple(out.shape) != (B, Hq, D):
         raise ValueError("shape mismatch between q / out / k_cache / v_cache")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
     p = DecodeParams()
     p.q = _dev_ptr(q, torch.bfloat16, "q")
     p.out = _dev_ptr(out, torch.bfloat16, "out")
-    p.k_cache = _dev_ptr(k_cache, torch.bfloat16, "k_cache")
-    p.v_cache = _dev_ptr(v_cache, torch.bfloat16, "v_cache")
+    cache_dtype = torch.uint8 if fp8 else torch.bfloat16
+    p.k_cache = _dev_ptr(k_cache, cache_dtype, "k_cache")
+    p.v_cache = _dev_ptr(v_cache, cache_dtype, "v_cache")
+    if fp8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("the 8-bit cache needs k_scale and v_scale")
+        p.kv_dtype = KV_FP8_E4M3
+        p.k_scale = _dev_ptr(k_scale, torch.float32, "k_scale")
+        p.v_scale = _dev_ptr(v_scale, torch.float32, "v_scale")
     p.block_tables = _dev_ptr(block_tables, torch.int32, "block_tables")
     p.context_lens = _dev_ptr(context_lens, torch.int32, "context_lens")
     p.max_blocks_per_seq = block_tables.shape[1]
@@ -228,7 +248,7 @@ def pa_decode_workspace_size(params: DecodeParams) -> int:
 def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
               scale: Optional[float] = None, partition_tokens: int = 0, out=None,
               workspace=None, stream=None, variant: int = DECODE_TENSOR_CORE,
-              overlap_prologue: bool = False):
+              overlap_prologue: bool = False, k_scale=None, v_scale=None):
     """Paged decode attention; returns ``out`` (bf16 [B][Hq][d]).
 
     ``workspace`` is a uint8 CUDA tensor of at least
@@ -240,7 +260,8 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
     if out is None:
         out = torch.empty_like(q)
     p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
-                           max_context_len, scale, partition_tokens, variant, overlap_prologue)
+                           max_context_len, scale, partition_tokens, variant, overlap_prologue,
+                           k_scale, v_scale)
     need = int(lib.pa_decode_workspace_size(ctypes.byref(p)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -413,6 +434,38 @@ def pa_copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
         _dev_ptr(k_cache, torch.bfloat16, "k_cache"), _dev_ptr(v_cache, torch.bfloat16, "v_cache"),
         _dev_ptr(pairs, torch.int32, "pairs"), pairs.shape[0], Hkv, D, BS, NB,
         _stream_handle(stream)), "pa_copy_blocks")
+
+
+def pa_reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale, v_scale,
+                             stream=None) -> None:
+    """KV write into the 8-bit cache (uint8 K [NB][Hkv][BS][D], V^T [NB][Hkv][D][BS])."""
+    import torch
+
+    T, Hkv, D = k_new.shape
+    NB, Hkv2, BS, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or tuple(v_new.shape) != tuple(k_new.shape) \
+            or tuple(v_cache.shape) != (NB, Hkv, D, BS) or tuple(slot_mapping.shape) != (T,):
+        raise ValueError("shape mismatch in pa_reshape_and_cache_fp8")
+    lib = load()
+    _check(lib.pa_reshape_and_cache_fp8(
+        _dev_ptr(k_new, torch.bfloat16, "k_new"), _dev_ptr(v_new, torch.bfloat16, "v_new"),
+        _dev_ptr(k_cache, torch.uint8, "k_cache"), _dev_ptr(v_cache, torch.uint8, "v_cache"),
+        _dev_ptr(slot_mapping, torch.int64, "slot_mapping"),
+        _dev_ptr(k_scale, torch.float32, "k_scale"), _dev_ptr(v_scale, torch.float32, "v_scale"),
+        T, Hkv, D, BS, NB, _stream_handle(stream)), "pa_reshape_and_cache_fp8")
+
+
+def pa_copy_blocks_fp8(k_cache, v_cache, pairs, stream=None) -> None:
+    import torch
+
+    NB, Hkv, BS, D = k_cache.shape
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int32 [n][2]")
+    lib = load()
+    _check(lib.pa_copy_blocks_fp8(
+        _dev_ptr(k_cache, torch.uint8, "k_cache"), _dev_ptr(v_cache, torch.uint8, "v_cache"),
+        _dev_ptr(pairs, torch.int32, "pairs"), pairs.shape[0], Hkv, D, BS, NB,
+        _stream_handle(stream)), "pa_copy_blocks_fp8")
 
 
 def pa_device_errors(stream=None) -> int:

@@ -57,6 +57,19 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: cache or query rows exceed 2^31");
   if (!(p->scale > 0.0f) || p->scale != p->scale)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: scale must be a positive finite number");
+  if (p->kv_dtype != PA_KV_BF16 && p->kv_dtype != PA_KV_FP8_E4M3)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: kv_dtype must be PA_KV_BF16 or PA_KV_FP8_E4M3");
+  if (p->kv_dtype == PA_KV_FP8_E4M3) {
+    if (p->head_dim != 128 || p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p))
+      return set_error(PA_ERR_UNSUPPORTED,
+                       "pa_decode: the 8-bit cache runs on the tensor-core kernel with head_dim "
+                       "128, num_kv_heads 1/2/4/8, num_q_heads <= 64");
+    if (need_pointers && p->num_seqs > 0 &&
+        (!p->k_scale || !p->v_scale || (reinterpret_cast<uintptr_t>(p->k_scale) & 3u) ||
+         (reinterpret_cast<uintptr_t>(p->v_scale) & 3u)))
+      return set_error(PA_ERR_INVALID_ARG,
+                       "pa_decode: the 8-bit cache needs k_scale and v_scale (float arrays)");
+  }
   if (need_pointers && p->num_seqs > 0) {
     if (!p->q || !p->out || !p->k_cache || !p->v_cache || !p->block_tables || !p->context_lens)
       return set_error(PA_ERR_INVALID_ARG, "pa_decode: a required pointer is NULL");
@@ -110,7 +123,13 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
   w.tc_m = w.tc_plan + round_up((size_t(p->num_seqs) + 2) * sizeof(int), 256);
   w.tc_l = w.tc_m + round_up(rows * sizeof(float), 256);
   w.tc_acc = w.tc_l + round_up(rows * sizeof(float), 256);
-  const size_t tc_end = w.tc_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+  size_t tc_end = w.tc_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+  if (p->kv_dtype == PA_KV_FP8_E4M3) {  // split queries [B][2N][D] bytes and [B][N] floats
+    const size_t n_pad = size_t(tc_n_pad(p->num_q_heads));
+    w.tc_q8 = tc_end;
+    w.tc_qa = w.tc_q8 + round_up(size_t(p->num_seqs) * 2 * n_pad * p->head_dim, 256);
+    tc_end = w.tc_qa + round_up(size_t(p->num_seqs) * n_pad * sizeof(float), 256);
+  }
   w.total = simt_end > tc_end ? simt_end : tc_end;
   return w;
 }
@@ -129,10 +148,15 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
   int e = 0;
   if (p->variant == PA_DECODE_TENSOR_CORE && tc_supports(p) && grid > 0) {
     L.plan = reinterpret_cast<int*>(ws + w.tc_plan);
+    L.q8 = p->kv_dtype == PA_KV_FP8_E4M3 ? ws + w.tc_q8 : nullptr;
+    L.q_inv_alpha =
+        p->kv_dtype == PA_KV_FP8_E4M3 ? reinterpret_cast<float*>(ws + w.tc_qa) : nullptr;
     L.part_m = reinterpret_cast<float*>(ws + w.tc_m);
     L.part_l = reinterpret_cast<float*>(ws + w.tc_l);
     L.part_acc = reinterpret_cast<float*>(ws + w.tc_acc);
     e = launch_decode_tc(L, stream);
+  } else if (p->kv_dtype == PA_KV_FP8_E4M3) {
+    return set_error(PA_ERR_UNSUPPORTED, "the 8-bit cache needs the tensor-core kernel");
   } else {
     if (append) {  // the same effect in two launches
       AppendCheck chk;
@@ -257,12 +281,13 @@ pa_status pa_device_errors(pa_stream_t stream, uint32_t* flags) {
   if (!flags) return pa::set_error(PA_ERR_INVALID_ARG, "pa_device_errors: flags is NULL");
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return pa::set_cuda_error("pa_device_errors: stream sync", int(e));
-  uint32_t a = 0, b = 0, c = 0;
+  uint32_t a = 0, b = 0, c = 0, d = 0;
   int r = pa::read_and_clear_decode_errors(&a);
   if (r == 0) r = pa::read_and_clear_decode_tc_errors(&c);
   if (r == 0) r = pa::read_and_clear_cache_errors(&b);
+  if (r == 0) r = pa::read_and_clear_fp8_errors(&d);
   if (r != 0) return pa::set_cuda_error("pa_device_errors: read", r);
-  *flags = a | b | c;
+  *flags = a | b | c | d;
   return PA_OK;
 }
 
@@ -314,6 +339,10 @@ pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
   pa_status st = pa::check_decode(p, true);
   if (st != PA_OK) return st;
   if (!a) return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: append params are NULL");
+  if (p->kv_dtype != PA_KV_BF16)
+    return pa::set_error(PA_ERR_UNSUPPORTED,
+                         "pa_append_decode: bf16 caches only (use pa_reshape_and_cache_fp8 and "
+                         "pa_decode for the 8-bit cache)");
   if (p->num_seqs == 0) return PA_OK;
   if (!a->k_new || !a->v_new || !a->slot_mapping || !a->k_cache || !a->v_cache)
     return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: a required pointer is NULL");
@@ -429,6 +458,46 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cac
                                              num_tokens, num_kv_heads, head_dim, num_blocks, stream);
   if (e != 0) return pa::set_cuda_error("pa_reshape_and_cache: launch", e);
   return PA_OK;
+}
+
+pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                   void* v_cache, const int64_t* slot_mapping,
+                                   const float* k_scale, const float* v_scale,
+                                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t num_blocks, pa_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1)
+    return pa::set_error(PA_ERR_INVALID_ARG,
+                         "pa_reshape_and_cache_fp8: num_tokens >= 0, num_kv_heads >= 1, "
+                         "num_blocks >= 1");
+  if (block_size != pa::kBlockSize)
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache_fp8: only block_size 16");
+  if (head_dim < 8 || head_dim % 8 != 0 || head_dim > 1024)
+    return pa::set_error(PA_ERR_UNSUPPORTED,
+                         "pa_reshape_and_cache_fp8: head_dim must be a multiple of 8 in [8, 1024]");
+  if (num_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping || !k_scale || !v_scale)
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache_fp8: a required pointer is NULL");
+  if (!pa::aligned16(k_new) || !pa::aligned16(v_new) || !pa::aligned16(k_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache_fp8: misaligned pointer");
+  if (int64_t(num_tokens) * num_kv_heads * (head_dim / 8) > (int64_t(1) << 38))
+    return pa::set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache_fp8: too many tokens");
+  const int e = pa::launch_reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping,
+                                                 k_scale, v_scale, num_tokens, num_kv_heads,
+                                                 head_dim, num_blocks, stream);
+  if (e != 0) return pa::set_cuda_error("pa_reshape_and_cache_fp8: launch", e);
+  return PA_OK;
+}
+
+pa_status pa_copy_blocks_fp8(void* k_cache, void* v_cache, const int32_t* pairs,
+                             int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks, pa_stream_t stream) {
+  if (head_dim % 16 != 0)
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: head_dim must be a multiple of 16");
+  // one byte per element: the same bytes as a bf16 block of head_dim / 2
+  return pa_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_kv_heads, head_dim / 2, block_size,
+                        num_blocks, stream);
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,

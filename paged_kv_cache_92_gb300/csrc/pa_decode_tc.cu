@@ -82,20 +82,27 @@ struct __align__(16) ChunkMeta {
   int pad;
 };
 
-template <int D, int N>
+// F8: the 8-bit (E4M3) cache. K rows are D bytes (one 128-byte atom at
+// D = 128); V^T comes as one [D][16 keys] tile per (block, KV head), side by
+// side; Q and P are each split into an E4M3 hi and lo term.
+template <int D, int N, bool F8 = false>
 struct TcCfg {
-  static constexpr int HALVES = D / 64;            // 128-byte swizzle atoms per row
-  static constexpr int HALF_BYTES = ROWS * 128;    // [128 rows][64 bf16]
+  static constexpr int HALVES = F8 ? 1 : D / 64;   // 128-byte swizzle atoms per K row
+  static constexpr int HALF_BYTES = ROWS * 128;    // [128 rows][64 bf16] or [128 rows][128 e4m3]
   static constexpr int K_BYTES = HALVES * HALF_BYTES;
-  static constexpr int SLOT_BYTES = 2 * K_BYTES;   // K then V
-  static constexpr int QH_BYTES = N * 128;         // [N rows][64 bf16]
-  static constexpr int Q_BYTES = HALVES * QH_BYTES;
-  static constexpr int PH_BYTES = N * 128;         // P^T [N rows][64 keys]
-  static constexpr int P_BYTES = 2 * PH_BYTES;     // 128 keys
+  static constexpr int VT_TILE = D * BS;           // F8: one [D][16] V^T tile, bytes
+  static constexpr int V_BYTES = F8 ? kGroups * VT_TILE : K_BYTES;
+  static constexpr int SLOT_BYTES = K_BYTES + V_BYTES;  // K then V
+  static constexpr int QH_BYTES = N * 128;         // [N rows][64 bf16] or [N rows][128 e4m3]
+  static constexpr int Q_BYTES = F8 ? 2 * QH_BYTES : HALVES * QH_BYTES;  // F8: hi, lo
+  static constexpr int PH_BYTES = N * 128;         // P^T [N rows][64 keys] or [N rows][128 keys]
+  static constexpr int P_BYTES = 2 * PH_BYTES;     // bf16: 128 keys; F8: hi and lo
   static constexpr int MISC_BYTES = 4096;
   static constexpr int ST_FIT =
       (kMaxDynSmem - 1024 - 2 * Q_BYTES - P_BYTES - MISC_BYTES) / SLOT_BYTES;
-  static constexpr int ST = ST_FIT > 4 ? 4 : ST_FIT;
+  static constexpr int ST_CAP = F8 ? 6 : 4;
+  static constexpr int ST = ST_FIT > ST_CAP ? ST_CAP : ST_FIT;
+  static_assert(!F8 || D == 128, "the 8-bit cache is built for head_dim 128");
   static_assert(ST >= 2, "at least a double-buffered ring");
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_Q = ST * SLOT_BYTES;
@@ -111,15 +118,19 @@ struct TcCfg {
   static constexpr int OFF_LS = OFF_ALPHA + 2 * 64 * 4;
   static constexpr int OFF_MS = OFF_LS + 64 * 4;
   static constexpr int OFF_WORDS = OFF_MS + 64 * 4;
-  static constexpr int SMEM = OFF_WORDS + 64 + 1024;  // + alignment slack
-  static_assert(OFF_WORDS + 64 <= OFF_MISC + MISC_BYTES, "misc area");
+  static constexpr int OFF_QALPHA = OFF_WORDS + 64;       // F8: [2 q slots][64] 1/alpha
+  static constexpr int OFF_KVSCALE = OFF_QALPHA + 2 * 64 * 4;  // F8: k_scale[8], v_scale[8]
+  static constexpr int SMEM = OFF_KVSCALE + 64 + 1024;  // + alignment slack
+  static_assert(OFF_KVSCALE + 64 <= OFF_MISC + MISC_BYTES, "misc area");
   static_assert(SMEM <= kMaxDynSmem, "shared memory budget");
   static constexpr int TMEM_COLS = 4 * N;  // S triple buffer [0, 3N), O at [3N, 4N)
   static constexpr int kSBufs = 3;
-  static constexpr uint32_t IDESC_S = dev::idesc_bf16_f32(ROWS, N, false, false);
-  static constexpr uint32_t IDESC_PV = dev::idesc_bf16_f32(ROWS, N, true, false);
+  static constexpr uint32_t IDESC_S =
+      F8 ? dev::idesc_e4m3_f32(ROWS, N) : dev::idesc_bf16_f32(ROWS, N, false, false);
+  static constexpr uint32_t IDESC_PV =
+      F8 ? dev::idesc_e4m3_f32(ROWS, N) : dev::idesc_bf16_f32(ROWS, N, true, false);
   static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
-  static constexpr uint32_t Q_TX = Q_BYTES;
+  static constexpr uint32_t Q_TX = Q_BYTES + (F8 ? N * 4 : 0);  // F8: + 1/alpha per column
 };
 
 struct TcParams {
@@ -136,7 +147,14 @@ struct TcParams {
   const int64_t* slot_mapping;
   uint4* k_cache_w;
   uint4* v_cache_w;
+  // 8-bit cache: per-KV-head dequantisation scales, and per (sequence, query
+  // head) 1/alpha of the split queries ([B][N] floats)
+  const float* k_scale;
+  const float* v_scale;
+  const float* q_inv_alpha;
   int max_blocks_per_seq, num_seqs, num_kv_heads, num_q_heads, num_blocks, cap, oob_row;
+  int oob_row_v;   // 8-bit cache: first row past the V^T tensor map
+  int q_rows;      // rows of one sequence's queries in the Q tensor map
   float scale_log2;
 };
 
@@ -150,20 +168,41 @@ __device__ __forceinline__ uint32_t p_offset(int n, int key) {
                   (kin & 7) * 2);
 }
 
-// S^T = Kchunk . Q^T for one chunk (single thread): D/16 MMAs of K = 16.
-template <int D, int N>
+// Byte offset of the E4M3 P^T[n][key] in the K-major, 128B-swizzled B-operand
+// layout [N rows][128 keys] (one atom per row).
+__device__ __forceinline__ uint32_t p8_offset(int n, int key) {
+  const int r = n & 7, grp = n >> 3;
+  return uint32_t(grp * 1024 + r * 128 + (((key >> 4) ^ r) << 4) + (key & 15));
+}
+
+// S^T = Kchunk . Q^T for one chunk (single thread). bf16: D/16 MMAs of K = 16.
+// E4M3: D/32 MMAs of K = 32 for each of the two query terms (hi, then lo),
+// accumulating into the same scores.
+template <int D, int N, bool F8>
 __device__ __forceinline__ void issue_scores(uint32_t tmem_col, const unsigned char* kv,
                                              const unsigned char* q) {
-  using C = TcCfg<D, N>;
+  using C = TcCfg<D, N, F8>;
   const uint32_t kb = dev::smem_addr(kv);
   const uint32_t qb = dev::smem_addr(q);
+  if constexpr (F8) {
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t hf = kk >> 2, off = uint32_t(kk & 3) * 32;
-    dev::mma_bf16(tmem_col,
-                  dev::smem_desc(kb + hf * C::HALF_BYTES + off, 16, 1024, dev::kSwizzle128B),
-                  dev::smem_desc(qb + hf * C::QH_BYTES + off, 16, 1024, dev::kSwizzle128B),
-                  C::IDESC_S, kk > 0);
+    for (int kk = 0; kk < D / 32; ++kk) {
+      const uint64_t a = dev::smem_desc(kb + kk * 32, 16, 1024, dev::kSwizzle128B);
+      dev::mma_e4m3(tmem_col, a, dev::smem_desc(qb + kk * 32, 16, 1024, dev::kSwizzle128B),
+                    C::IDESC_S, kk > 0);
+      dev::mma_e4m3(tmem_col, a,
+                    dev::smem_desc(qb + C::QH_BYTES + kk * 32, 16, 1024, dev::kSwizzle128B),
+                    C::IDESC_S, true);
+    }
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t hf = kk >> 2, off = uint32_t(kk & 3) * 32;
+      dev::mma_bf16(tmem_col,
+                    dev::smem_desc(kb + hf * C::HALF_BYTES + off, 16, 1024, dev::kSwizzle128B),
+                    dev::smem_desc(qb + hf * C::QH_BYTES + off, 16, 1024, dev::kSwizzle128B),
+                    C::IDESC_S, kk > 0);
+    }
   }
 }
 
@@ -172,13 +211,13 @@ __device__ __forceinline__ void issue_scores(uint32_t tmem_col, const unsigned c
 // the chunk has landed, and O^T = V^T.P^T once the softmax warps have written
 // P for it. Scores run one chunk ahead of the value product.
 // ---------------------------------------------------------------------------
-template <int D, int N>
+template <int D, int N, bool F8>
 __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbuf,
                                          unsigned char* pbuf, uint64_t* full, uint64_t* empty,
                                          uint64_t* qempty, uint64_t* bar_s, uint64_t* bar_o,
                                          uint64_t* bar_p, uint64_t* drain, const ChunkMeta* meta,
                                          uint32_t tmem, volatile int* abort_flag) {
-  using C = TcCfg<D, N>;
+  using C = TcCfg<D, N, F8>;
   // D = 64: the second 64-row half of M re-reads the first (LBO 0); those
   // TMEM lanes are never read back.
   const uint32_t lbo = C::HALVES == 2 ? uint32_t(C::HALF_BYTES) : 0u;
@@ -202,13 +241,30 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       const bool fresh = (meta[sl].flags & F_FIRST) != 0;
       dev::tc_fence_after();
       const uint32_t vb = dev::smem_addr(ring + size_t(sl) * C::SLOT_BYTES + C::K_BYTES);
+      if constexpr (F8) {
+        // V^T K-major without swizzle: 8-row x 16-byte core matrices, the
+        // next 8 rows of d 128 B on (SBO), the next 16 keys one [D][16]
+        // tile on (LBO); 32 keys per MMA, each against P's hi and lo terms
 #pragma unroll
-      for (int kk = 0; kk < ROWS / 16; ++kk) {
-        dev::mma_bf16(tmem + C::kSBufs * N,
-                      dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
-                      dev::smem_desc(pbs + (kk >> 2) * C::PH_BYTES + (kk & 3) * 32, 16, 1024,
-                                     dev::kSwizzle128B),
-                      C::IDESC_PV, kk > 0 || !fresh);
+        for (int kk = 0; kk < ROWS / 32; ++kk) {
+          const uint64_t a =
+              dev::smem_desc(vb + kk * 2 * C::VT_TILE, C::VT_TILE, 128, dev::kSwizzleNone);
+          dev::mma_e4m3(tmem + C::kSBufs * N, a,
+                        dev::smem_desc(pbs + kk * 32, 16, 1024, dev::kSwizzle128B), C::IDESC_PV,
+                        kk > 0 || !fresh);
+          dev::mma_e4m3(tmem + C::kSBufs * N, a,
+                        dev::smem_desc(pbs + C::PH_BYTES + kk * 32, 16, 1024, dev::kSwizzle128B),
+                        C::IDESC_PV, true);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < ROWS / 16; ++kk) {
+          dev::mma_bf16(tmem + C::kSBufs * N,
+                        dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
+                        dev::smem_desc(pbs + (kk >> 2) * C::PH_BYTES + (kk & 3) * 32, 16, 1024,
+                                       dev::kSwizzle128B),
+                        C::IDESC_PV, kk > 0 || !fresh);
+        }
       }
       dev::mma_commit(bar_o);
       dev::mma_commit(&empty[sl]);
@@ -226,8 +282,8 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       } else {
         const int sb = s_pos % C::kSBufs;
         dev::tc_fence_after();
-        issue_scores<D, N>(tmem + sb * N, ring + size_t(sl) * C::SLOT_BYTES,
-                           qbuf + mn.qslot * C::Q_BYTES);
+        issue_scores<D, N, F8>(tmem + sb * N, ring + size_t(sl) * C::SLOT_BYTES,
+                               qbuf + mn.qslot * C::Q_BYTES);
         dev::mma_commit(&bar_s[sb]);
         if (mn.flags & F_LAST) dev::mma_commit(&qempty[mn.qslot]);
       }
@@ -261,9 +317,9 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
 // across the chunk's groups of the same KV head), fold chunk r-1's O^T into
 // the accumulators, write P and signal the MMA warp.
 // ---------------------------------------------------------------------------
-template <int D, int G, int N>
+template <int D, int G, int N, bool F8>
 struct Softmax {
-  using C = TcCfg<D, N>;
+  using C = TcCfg<D, N, F8>;
   static constexpr int LDC = 2 * G <= 8 ? 8 : 16;  // score columns a warp reads (two heads)
 
   __device__ __forceinline__ static void run(const TcParams& P, unsigned char* ring,
@@ -271,6 +327,7 @@ struct Softmax {
                                              uint64_t* bar_s, uint64_t* bar_o, uint64_t* bar_p,
                                              const ChunkMeta* meta, float* red, float* red2,
                                              float* alpha_s, float* l_s, float* m_s,
+                                             const float* qalpha, const float* kvscale,
                                              uint32_t tmem, volatile int* abort_flag,
                                              int* consumed_out) {
     const int ctid = threadIdx.x;
@@ -330,7 +387,10 @@ struct Softmax {
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const float sj = upper ? s[(LDC >= 2 * G ? G : 0) + j] : s[j];
-        x[j] = valid ? sj * P.scale_log2 : -INFINITY;
+        float f = P.scale_log2;
+        if constexpr (F8)  // the head's K scale and the query term's 1/alpha
+          f *= kvscale[h] * qalpha[m.qslot * 64 + h * G + j];
+        x[j] = valid ? sj * f : -INFINITY;
         float v = x[j];
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -384,19 +444,37 @@ struct Softmax {
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const float p = dev::fast_exp2(x[j] - m_ref[j]);
-        l_part[j] += p;
-        *reinterpret_cast<__nv_bfloat16*>(pbuf + p_offset<N>(h * G + j, ctid)) =
-            __float2bfloat16_rn(p);
+        if constexpr (F8) {
+          // P as two E4M3 terms; the sum uses exactly what the MMA multiplies
+          const uint8_t ph = dev::to_e4m3(p);
+          const float phf = dev::from_e4m3(ph);
+          const uint8_t pl = dev::to_e4m3(p - phf);
+          l_part[j] += phf + dev::from_e4m3(pl);
+          const uint32_t o = p8_offset(h * G + j, ctid);
+          pbuf[o] = ph;
+          pbuf[C::PH_BYTES + o] = pl;
+        } else {
+          l_part[j] += p;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + p_offset<N>(h * G + j, ctid)) =
+              __float2bfloat16_rn(p);
+        }
       }
       // A masked row inside a loaded block (the sequence's last, partial
       // block) may hold anything, NaN included: clear its V row so 0 * V = 0.
       if (!valid && u < m.nblk) {
         unsigned char* kv = ring + size_t(slot) * C::SLOT_BYTES;
+        if constexpr (F8) {  // the key is column `key` of its [D][16] V^T tile
+          unsigned char* tile = kv + C::K_BYTES + grp * C::VT_TILE + key;
+#pragma unroll 16
+          for (int d = 0; d < D; ++d) tile[d * BS] = 0;
+        } else {
 #pragma unroll
-        for (int hf = 0; hf < C::HALVES; ++hf) {
-          uint4* row = reinterpret_cast<uint4*>(kv + C::K_BYTES + hf * C::HALF_BYTES + ctid * 128);
+          for (int hf = 0; hf < C::HALVES; ++hf) {
+            uint4* row =
+                reinterpret_cast<uint4*>(kv + C::K_BYTES + hf * C::HALF_BYTES + ctid * 128);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < 8; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
       }
       dev::fence_async_smem();
@@ -426,6 +504,10 @@ struct Softmax {
         dev::tc_fence_after();
         float o[N];
         dev::tmem_ld_cols<N>(tO, o);
+        if constexpr (F8) {  // the V scale of each query head's KV head
+#pragma unroll
+          for (int n = 0; n < N; ++n) o[n] *= kvscale[8 + (n < Hq ? n / G : 0)];
+        }
         dev::named_barrier(1, kCons);  // l_s, m_s written
         if (ctid < D) {
           if (m.flags & F_WHOLE) {
@@ -461,12 +543,12 @@ struct Softmax {
   }
 };
 
-template <int D, int G, int N>
+template <int D, int G, int N, bool F8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, const TcParams P) {
-  using C = TcCfg<D, N>;
+  using C = TcCfg<D, N, F8>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -488,6 +570,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   float* l_s = reinterpret_cast<float*>(smem + C::OFF_LS);
   float* m_s = reinterpret_cast<float*>(smem + C::OFF_MS);
   int* words = reinterpret_cast<int*>(smem + C::OFF_WORDS);
+  float* qalpha = reinterpret_cast<float*>(smem + C::OFF_QALPHA);    // F8
+  float* kvscale = reinterpret_cast<float*>(smem + C::OFF_KVSCALE);  // F8
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&words[0]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&words[1]);
   int* consumed = &words[2];
@@ -565,6 +649,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   const int off_start = u0 < u1 ? u0 - pre[b_start] : 0;
   for (int i = tid; i < 128; i += NTHREADS) alpha_s[i] = 1.0f;  // padded columns stay 1
+
   if (warp == 0) dev::tmem_alloc(tmem_slot, C::TMEM_COLS);
   // Everything above read only context_lens (and shared memory). When this
   // kernel overlaps the previous one, that is all it may touch before
@@ -577,6 +662,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     len0 = min(P.context_lens[b_start], P.cap);
   }
   dev::griddep_wait();
+  if constexpr (F8) {  // per-KV-head scales: k_scale in [0, 8), v_scale in [8, 16)
+    if (tid < 16) kvscale[tid] = (tid & 7) < H ? (tid < 8 ? P.k_scale : P.v_scale)[tid & 7] : 1.0f;
+  }
   if (blockIdx.x == 0) {  // the stream-K plan, for the merge kernel
     for (int i = tid; i <= B; i += NTHREADS) P.ws_plan[1 + i] = pre[i];
     if (tid == 0) P.ws_plan[0] = R;
@@ -649,10 +737,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const int seg_nb = min(nb - off, u1 - unit);
       const bool whole = off == 0 && seg_nb == nb;
-      if (P.k_new != nullptr && off + seg_nb == nb) {  // this piece holds the last block
-        append_token(b, L_cur);
-        __syncwarp();
-        dev::fence_async_global();
+      if constexpr (!F8) {
+        if (P.k_new != nullptr && off + seg_nb == nb) {  // this piece holds the last block
+          append_token(b, L_cur);
+          __syncwarp();
+          dev::fence_async_global();
+        }
       }
       // prefetched for later: the next sequence's length and first window,
       // this segment's second window
@@ -692,26 +782,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // lanes 0..U-1: one block (all KV heads) each
         const int e = __shfl_sync(0xffffffffu, win, (jb & 31) + (lane % U));
         unsigned char* kdst = ring + size_t(slot) * C::SLOT_BYTES;
-        if (lane < U) {
-          int row = P.oob_row;
-          if (jb + lane < seg_nb) {
-            if (e >= 0 && e < P.num_blocks) {
-              row = e * grows;
-            } else {
-              atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+        if constexpr (F8) {
+          // lane j < 8 also brings the V^T tile of (block j / H, KV head j % H)
+          const int uv = min(lane / H, U - 1);
+          const int ev = __shfl_sync(0xffffffffu, win, (jb & 31) + uv);
+          if (lane < U) {
+            int row = P.oob_row;
+            if (jb + lane < seg_nb) {
+              if (e >= 0 && e < P.num_blocks) {
+                row = e * grows;
+              } else {
+                atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+              }
             }
+            dev::tma_load_2d(kdst + lane * grows * 128, &tm_k, 0, row, &full[slot], pol);
           }
-#pragma unroll
-          for (int hf = 0; hf < C::HALVES; ++hf) {
-            unsigned char* d = kdst + hf * C::HALF_BYTES + lane * grows * 128;
-            dev::tma_load_2d(d, &tm_k, hf * 64, row, &full[slot], pol);
-            dev::tma_load_2d(d + C::K_BYTES, &tm_v, hf * 64, row, &full[slot], pol);
+          if (lane < kGroups) {
+            int row = P.oob_row_v;
+            if (jb + uv < seg_nb && ev >= 0 && ev < P.num_blocks)
+              row = (ev * H + (lane - uv * H)) * D;
+            dev::tma_load_2d(kdst + C::K_BYTES + lane * C::VT_TILE, &tm_v, 0, row, &full[slot],
+                             pol);
+          } else if (lane == 8 && c == 0) {
+            dev::tma_load_2d(qbuf + qs * C::Q_BYTES, &tm_q, 0, b * P.q_rows, &full[slot], pol);
+            dev::bulk_load(qalpha + qs * 64, P.q_inv_alpha + size_t(b) * N, N * 4, &full[slot],
+                           pol);
           }
-        } else if (lane == 8 && c == 0) {
+        } else {
+          if (lane < U) {
+            int row = P.oob_row;
+            if (jb + lane < seg_nb) {
+              if (e >= 0 && e < P.num_blocks) {
+                row = e * grows;
+              } else {
+                atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+              }
+            }
 #pragma unroll
-          for (int hf = 0; hf < C::HALVES; ++hf)
-            dev::tma_load_2d(qbuf + qs * C::Q_BYTES + hf * C::QH_BYTES, &tm_q, hf * 64,
-                             b * P.num_q_heads, &full[slot], pol);
+            for (int hf = 0; hf < C::HALVES; ++hf) {
+              unsigned char* d = kdst + hf * C::HALF_BYTES + lane * grows * 128;
+              dev::tma_load_2d(d, &tm_k, hf * 64, row, &full[slot], pol);
+              dev::tma_load_2d(d + C::K_BYTES, &tm_v, hf * 64, row, &full[slot], pol);
+            }
+          } else if (lane == 8 && c == 0) {
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf)
+              dev::tma_load_2d(qbuf + qs * C::Q_BYTES + hf * C::QH_BYTES, &tm_q, hf * 64,
+                               b * P.q_rows, &full[slot], pol);
+          }
         }
         ++chunk_seq;
         if (lane == 0) *issued = chunk_seq;
@@ -740,12 +858,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0)
-      mma_loop<D, N>(ring, qbuf, pbuf, full, empty, qempty, bar_s, bar_o, bar_p, drain, meta,
-                     tmem, abort_flag);
+      mma_loop<D, N, F8>(ring, qbuf, pbuf, full, empty, qempty, bar_s, bar_o, bar_p, drain,
+                         meta, tmem, abort_flag);
   } else {
     // ------------------------------------------------------------ softmax
-    Softmax<D, G, N>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2, alpha_s,
-                          l_s, m_s, tmem, abort_flag, consumed);
+    Softmax<D, G, N, F8>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2,
+                              alpha_s, l_s, m_s, qalpha, kvscale, tmem, abort_flag, consumed);
   }
 
   __syncthreads();
@@ -909,13 +1027,29 @@ int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uin
   return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
 }
 
-template <int D, int G, int N>
+// 2-D byte tensor [rows][cols] (row pitch cols bytes), box box_rows x
+// box_cols, the given swizzle, out-of-range elements read as zero.
+int make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (encode_fn(&enc)) return int(cudaErrorNotSupported);
+  cuuint64_t gdim[2] = {cols, rows};
+  cuuint64_t gstride[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
+}
+
+template <int D, int G, int N, bool F8>
 int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
-  using C = TcCfg<D, N>;
+  using C = TcCfg<D, N, F8>;
   const pa_decode_params* p = Lc.p;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, G, N>,
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, G, N, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return int(e);
     configured = true;
@@ -923,9 +1057,26 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   const int H = p->num_kv_heads;
   CUtensorMap tk, tv, tq;
   const uint64_t cache_rows = uint64_t(p->num_blocks) * H * BS;
-  int r = make_map(&tk, p->k_cache, cache_rows, D, uint32_t(BS * H));
-  if (!r) r = make_map(&tv, p->v_cache, cache_rows, D, uint32_t(BS * H));
-  if (!r) r = make_map(&tq, p->q, uint64_t(p->num_seqs) * p->num_q_heads, D, uint32_t(N));
+  int r = 0;
+  if constexpr (F8) {
+    // K rows of D bytes; V^T rows of 16 bytes, one [D][16] tile per (block,
+    // head); the split queries, 2N rows of D bytes per sequence
+    r = make_map_u8(&tk, p->k_cache, cache_rows, D, D, uint32_t(BS * H),
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r)
+      r = make_map_u8(&tv, p->v_cache, uint64_t(p->num_blocks) * H * D, BS, BS, uint32_t(D),
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!r)
+      r = make_map_u8(&tq, Lc.q8, uint64_t(p->num_seqs) * 2 * N, D, D, uint32_t(2 * N),
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r)
+      r = launch_quantize_q(p->q, Lc.q8, Lc.q_inv_alpha, p->num_seqs, p->num_q_heads, N, D,
+                            stream);
+  } else {
+    r = make_map(&tk, p->k_cache, cache_rows, D, uint32_t(BS * H));
+    if (!r) r = make_map(&tv, p->v_cache, cache_rows, D, uint32_t(BS * H));
+    if (!r) r = make_map(&tq, p->q, uint64_t(p->num_seqs) * p->num_q_heads, D, uint32_t(N));
+  }
   if (r) return r;
   TcParams P;
   P.block_tables = p->block_tables;
@@ -941,6 +1092,11 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.slot_mapping = a ? a->slot_mapping : nullptr;
   P.k_cache_w = a ? static_cast<uint4*>(a->k_cache) : nullptr;
   P.v_cache_w = a ? static_cast<uint4*>(a->v_cache) : nullptr;
+  P.k_scale = p->k_scale;
+  P.v_scale = p->v_scale;
+  P.q_inv_alpha = Lc.q_inv_alpha;
+  P.oob_row_v = int(uint64_t(p->num_blocks) * H * D);
+  P.q_rows = F8 ? 2 * N : p->num_q_heads;
   P.max_blocks_per_seq = p->max_blocks_per_seq;
   P.num_seqs = p->num_seqs;
   P.num_kv_heads = H;
@@ -961,7 +1117,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   // overlap the set-up with the previous kernel only when the caller says
   // context_lens and block_tables were final before that kernel began
   attr[0].val.programmaticStreamSerializationAllowed = p->overlap_prologue ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<D, G, N>, tk, tv, tq, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<D, G, N, F8>, tk, tv, tq, P);
   if (e != cudaSuccess) return int(e);
   // the merge launches while the decode drains and waits for it on the device
   cudaLaunchConfig_t mcfg = {};
@@ -978,19 +1134,18 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   return int(e);
 }
 
-template <int D>
+template <int D, bool F8>
 int dispatch_tc(const DecodeLaunch& Lc, cudaStream_t s) {
   const int G = Lc.p->num_q_heads / Lc.p->num_kv_heads;
-  const int hq = Lc.p->num_q_heads;
-  const int N = hq <= 16 ? 16 : (hq <= 32 ? 32 : 64);
+  const int N = tc_n_pad(Lc.p->num_q_heads);
   switch (G * 100 + N) {
-    case 116: return launch_tc_t<D, 1, 16>(Lc, s);
-    case 216: return launch_tc_t<D, 2, 16>(Lc, s);
-    case 416: return launch_tc_t<D, 4, 16>(Lc, s);
-    case 432: return launch_tc_t<D, 4, 32>(Lc, s);
-    case 816: return launch_tc_t<D, 8, 16>(Lc, s);
-    case 832: return launch_tc_t<D, 8, 32>(Lc, s);
-    case 864: return launch_tc_t<D, 8, 64>(Lc, s);
+    case 116: return launch_tc_t<D, 1, 16, F8>(Lc, s);
+    case 216: return launch_tc_t<D, 2, 16, F8>(Lc, s);
+    case 416: return launch_tc_t<D, 4, 16, F8>(Lc, s);
+    case 432: return launch_tc_t<D, 4, 32, F8>(Lc, s);
+    case 816: return launch_tc_t<D, 8, 16, F8>(Lc, s);
+    case 832: return launch_tc_t<D, 8, 32, F8>(Lc, s);
+    case 864: return launch_tc_t<D, 8, 64, F8>(Lc, s);
     default: return int(cudaErrorInvalidValue);
   }
 }
@@ -1016,9 +1171,11 @@ int tc_grid() {
 
 int launch_decode_tc(const DecodeLaunch& Lc, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Lc.p->kv_dtype == PA_KV_FP8_E4M3)
+    return Lc.p->head_dim == 128 ? dispatch_tc<128, true>(Lc, s) : int(cudaErrorInvalidValue);
   switch (Lc.p->head_dim) {
-    case 64: return dispatch_tc<64>(Lc, s);
-    case 128: return dispatch_tc<128>(Lc, s);
+    case 64: return dispatch_tc<64, false>(Lc, s);
+    case 128: return dispatch_tc<128, false>(Lc, s);
     default: return int(cudaErrorInvalidValue);
   }
 }

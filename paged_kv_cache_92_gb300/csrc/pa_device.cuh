@@ -2,12 +2,23 @@
 // (TMA without a tensor map), bounded waits, bf16 unpacking.
 #pragma once
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 namespace pa {
 namespace dev {
+
+// float -> E4M3 (round to nearest even, saturating finite) and back (exact).
+__device__ __forceinline__ uint8_t to_e4m3(float x) {
+  return uint8_t(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float from_e4m3(uint8_t c) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t(c), __NV_E4M3);
+  return __half2float(__half(h));
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -197,6 +208,7 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1, swizzle mode.
+constexpr uint64_t kSwizzleNone = 0;
 constexpr uint64_t kSwizzle128B = 2;
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint64_t swizzle) {
@@ -220,6 +232,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | (uint32_t(b_mn_major) << 16) // B major
          | (uint32_t(N >> 3) << 17)     // N / 8
          | (uint32_t(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0),
+// both K-major, and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                      // D format: f32
+         | (0u << 7)                    // A format: e4m3
+         | (0u << 10)                   // B format: e4m3
+         | (uint32_t(N >> 3) << 17)     // N / 8
+         | (uint32_t(M >> 4) << 24);    // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem], E4M3 operands (K = 32 per instruction);
+// issued by a single thread.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
+      : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; issued by a single thread.

@@ -1,0 +1,170 @@
+// 8-bit (FP8 E4M3) KV cache support for sm_103a: the quantising KV write and
+// the split of the bf16 queries into two E4M3 terms for the tensor cores.
+//
+// The pages say only that paging combines with 8-bit KV quantisation, which
+// halves the bytes per block ("PagedAttention" glossary page, §What paging
+// costs). The format is this library's reading:
+//  - OCP E4M3 codes, one dequantisation scale per KV head for K and for V;
+//  - write: code = E4M3(float32(x) / scale[h]), round to nearest even,
+//    saturating to +-448 (the CUDA conversion intrinsic with satfinite);
+//  - layout: K [block][head][offset][d] like the bf16 cache; V transposed
+//    inside each (block, head) tile, [block][head][d][offset], so that the
+//    value product reads V^T K-major (keys contiguous) on the tensor cores.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__device__ unsigned int g_fp8_errors;
+
+constexpr int BS = kBlockSize;
+
+using dev::from_e4m3;
+using dev::to_e4m3;
+
+// One thread per 8 elements (one 16-byte chunk of the bf16 input) of one
+// (token, KV head) row, for K and V.
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                 uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                                 const int64_t* __restrict__ slot_mapping,
+                                 const float* __restrict__ k_scale,
+                                 const float* __restrict__ v_scale, int64_t num_chunks,
+                                 int num_kv_heads, int head_dim, int64_t num_slots) {
+  dev::griddep_launch_dependents();
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= num_chunks) return;
+  const int cpr = head_dim / 8;
+  const int c = int(idx % cpr);
+  const int64_t row = idx / cpr;  // t * num_kv_heads + h
+  const int h = int(row % num_kv_heads);
+  const int64_t t = row / num_kv_heads;
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0) return;  // padding token: no write
+  if (slot >= num_slots) {
+    if (h == 0 && c == 0) atomicOr(&g_fp8_errors, PA_DEVERR_SLOT);
+    return;
+  }
+  const int64_t blk = slot / BS;
+  const int off = int(slot % BS);
+  const float ks = k_scale[h], vs = v_scale[h];
+  const uint4 kr = k_new[idx], vr = v_new[idx];
+  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kr);
+  const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vr);
+  uint8_t kq[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) kq[i] = to_e4m3(__fdiv_rn(__bfloat162float(kb[i]), ks));
+  const int64_t tile = (blk * num_kv_heads + h) * int64_t(BS) * head_dim;
+  // K row: 8 contiguous bytes
+  uint2 kw;
+  kw.x = uint32_t(kq[0]) | uint32_t(kq[1]) << 8 | uint32_t(kq[2]) << 16 | uint32_t(kq[3]) << 24;
+  kw.y = uint32_t(kq[4]) | uint32_t(kq[5]) << 8 | uint32_t(kq[6]) << 16 | uint32_t(kq[7]) << 24;
+  *reinterpret_cast<uint2*>(k_cache + tile + int64_t(off) * head_dim + c * 8) = kw;
+  // V column: element d of the row goes to byte d * BS + off of the tile
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    v_cache[tile + int64_t(c * 8 + i) * BS + off] = to_e4m3(__fdiv_rn(__bfloat162float(vb[i]), vs));
+}
+
+// Queries for the E4M3 tensor-core decode. For every (sequence b, query head
+// n) the row is scaled by a power of two alpha (its largest magnitude lands
+// in [64, 128)), split into hi = E4M3(q * alpha) and lo = E4M3(q * alpha - hi),
+// which together carry about 8 significant bits (the scores use hi + lo), and
+// 1/alpha is kept for the softmax. Output rows: q8[b][n] = hi, q8[b][N + n] =
+// lo, zero for n >= Hq; inv_alpha[b][n] (1 for n >= Hq). One warp per (b, n).
+__global__ void __launch_bounds__(128)
+    quantize_q_kernel(const __nv_bfloat16* __restrict__ q, uint8_t* __restrict__ q8,
+                      float* __restrict__ inv_alpha, int num_seqs, int num_q_heads, int N,
+                      int head_dim) {
+  dev::griddep_launch_dependents();
+  dev::griddep_wait();  // q may come from the previous kernel
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t gw = int64_t(blockIdx.x) * 4 + warp;
+  if (gw >= int64_t(num_seqs) * N) return;
+  const int b = int(gw / N), n = int(gw % N);
+  const int per = head_dim / 32;  // elements per lane (4 at head_dim 128)
+  uint8_t* hi_row = q8 + (int64_t(b) * 2 * N + n) * head_dim;
+  uint8_t* lo_row = q8 + (int64_t(b) * 2 * N + N + n) * head_dim;
+  if (n >= num_q_heads) {
+    for (int i = 0; i < per; ++i) {
+      hi_row[lane * per + i] = 0;
+      lo_row[lane * per + i] = 0;
+    }
+    if (lane == 0) inv_alpha[int64_t(b) * N + n] = 1.0f;
+    return;
+  }
+  const __nv_bfloat16* src = q + (int64_t(b) * num_q_heads + n) * head_dim + lane * per;
+  float v[4];
+  float amax = 0.0f;
+  for (int i = 0; i < per; ++i) {
+    v[i] = __bfloat162float(src[i]);
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int e = 0;
+  if (amax > 0.0f) (void)frexpf(amax, &e);  // amax < 2^e
+  e = max(e, -100);
+  const float alpha = ldexpf(1.0f, 7 - e);  // a power of two: exact
+  for (int i = 0; i < per; ++i) {
+    const float y = v[i] * alpha;
+    const uint8_t h = to_e4m3(y);
+    hi_row[lane * per + i] = h;
+    lo_row[lane * per + i] = to_e4m3(y - from_e4m3(h));
+  }
+  if (lane == 0) inv_alpha[int64_t(b) * N + n] = ldexpf(1.0f, e - 7);
+}
+
+}  // namespace
+
+int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                 void* v_cache, const int64_t* slot_mapping, const float* k_scale,
+                                 const float* v_scale, int32_t num_tokens, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t num_blocks, void* stream) {
+  const int64_t num_chunks = int64_t(num_tokens) * num_kv_heads * (head_dim / 8);
+  if (num_chunks == 0) return int(cudaSuccess);
+  const int threads = 256;
+  const int64_t blocks = (num_chunks + threads - 1) / threads;
+  reshape_and_cache_fp8_kernel<<<unsigned(blocks), threads, 0,
+                                 static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), slot_mapping, k_scale,
+      v_scale, num_chunks, num_kv_heads, head_dim, int64_t(num_blocks) * BS);
+  return int(cudaGetLastError());
+}
+
+int launch_quantize_q(const void* q, void* q8, float* inv_alpha, int32_t num_seqs,
+                      int32_t num_q_heads, int32_t n_pad, int32_t head_dim, void* stream) {
+  const int64_t warps = int64_t(num_seqs) * n_pad;
+  if (warps == 0) return int(cudaSuccess);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((warps + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return int(cudaLaunchKernelEx(&cfg, quantize_q_kernel, static_cast<const __nv_bfloat16*>(q),
+                                static_cast<uint8_t*>(q8), inv_alpha, int(num_seqs),
+                                int(num_q_heads), int(n_pad), int(head_dim)));
+}
+
+int read_and_clear_fp8_errors(uint32_t* flags) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_fp8_errors, sizeof(v));
+  if (e != cudaSuccess) return int(e);
+  e = cudaMemcpyToSymbol(g_fp8_errors, &zero, sizeof(zero));
+  *flags = v;
+  return int(e);
+}
+
+}  // namespace pa

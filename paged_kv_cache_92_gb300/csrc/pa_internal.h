@@ -31,7 +31,14 @@ struct DecodeLaunch {
   float* part_acc;       // partial weighted sums
   int* plan;             // tensor-core kernel: stream-K plan for its merge
   const pa_append_params* append;  // non-null: write each sequence's new token first
+  unsigned char* q8;     // 8-bit cache: split queries [B][2N][D] (workspace)
+  float* q_inv_alpha;    // 8-bit cache: [B][N] (workspace)
 };
+
+// Query heads padded to the tensor-core N (16, 32 or 64).
+inline int tc_n_pad(int num_q_heads) {
+  return num_q_heads <= 16 ? 16 : (num_q_heads <= 32 ? 32 : 64);
+}
 
 // Bytes at the start of every decode workspace (reserved).
 constexpr size_t kWorkspaceHeaderBytes = 256;
@@ -41,6 +48,7 @@ struct WorkspaceLayout {
   size_t total;
   size_t simt_m, simt_l, simt_acc;    // [seqs][q heads][partitions](+[dim])
   size_t tc_plan, tc_m, tc_l, tc_acc; // plan, then [seqs + grid][q heads](+[dim])
+  size_t tc_q8, tc_qa;                // 8-bit cache: split queries, their 1/alpha
 };
 WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_partitions,
                                         int tc_grid);
@@ -68,6 +76,14 @@ int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
                              int32_t head_dim, int32_t num_blocks, void* stream,
                              const AppendCheck& check = AppendCheck());
+// 8-bit cache (pa_fp8.cu)
+int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                 void* v_cache, const int64_t* slot_mapping, const float* k_scale,
+                                 const float* v_scale, int32_t num_tokens, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t num_blocks, void* stream);
+int launch_quantize_q(const void* q, void* q8, float* inv_alpha, int32_t num_seqs,
+                      int32_t num_q_heads, int32_t n_pad, int32_t head_dim, void* stream);
+int read_and_clear_fp8_errors(uint32_t* flags);
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
                        int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, void* stream);
 

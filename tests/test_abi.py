@@ -24,7 +24,7 @@ def pk():
 def _declared_functions():
     src = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = set(re.findall(r"\b(pa_[a-z_]+)\s*\(", src))
+    names = set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", src))
     return sorted(names)
 
 

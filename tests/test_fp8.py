@@ -1,0 +1,218 @@
+"""GPU parity of the 8-bit (E4M3) KV cache against the float64 oracle.
+
+Bit-exact: the quantising KV write (whole caches compared, including exact
+rounding ties and saturation) and the block copy. Decode: max-abs <= 2e-2 and
+mean-abs <= 2e-3 against the exact attention over the dequantised cache (the
+oracle decodes every code exactly and multiplies by its head's scale in
+float64). Padding slots hold E4M3 NaN codes, so a masked slot that leaks into
+a result fails the finiteness check.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+NAN8 = 0x7F
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import torch
+
+    from paged_kv_cache_92_gb300 import build
+
+    build.build()
+    import paged_kv_cache_92_gb300 as pk
+
+    pk.load()
+    assert torch.cuda.is_available()
+    return pk
+
+
+def _scales(Hkv, seed, base):
+    rng = np.random.default_rng(seed)
+    return (base * np.exp(rng.uniform(-0.5, 0.5, size=Hkv))).astype(np.float32)
+
+
+def _fp8_case(pk, lens, Hq, Hkv, seed, extra_blocks=3):
+    """Random tables; every slot of the pool written through
+    pa_reshape_and_cache_fp8 (bf16 N(0,1) rows, per-head scales); padding
+    slots of each sequence's last block then set to the NaN code."""
+    import torch
+
+    D = 128
+    lens = np.asarray(lens, dtype=np.int64)
+    need = int(((lens + 15) // 16).sum())
+    NB = need + extra_blocks
+    order = np.random.default_rng(seed).permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, 16)
+    q = workloads.bf16_normal((len(lens), Hq, D), seed + 1, "cuda")
+    kn = workloads.bf16_normal((NB * 16, Hkv, D), seed + 2, "cuda")
+    vn = workloads.bf16_normal((NB * 16, Hkv, D), seed + 3, "cuda")
+    ks = torch.from_numpy(_scales(Hkv, seed + 4, 0.05)).cuda()
+    vs = torch.from_numpy(_scales(Hkv, seed + 5, 0.03)).cuda()
+    k8 = torch.zeros((NB, Hkv, 16, D), dtype=torch.uint8, device="cuda")
+    v8 = torch.zeros((NB, Hkv, D, 16), dtype=torch.uint8, device="cuda")
+    slots = torch.arange(NB * 16, dtype=torch.int64, device="cuda")
+    pk.pa_reshape_and_cache_fp8(kn, vn, k8, v8, slots, ks, vs)
+    for b, L in enumerate(lens):
+        if L % 16:
+            blk = int(tables[b, (L - 1) // 16])
+            k8[blk, :, L % 16:, :] = NAN8
+            v8[blk, :, :, L % 16:] = NAN8
+    torch.cuda.synchronize()
+    return q, k8, v8, ks, vs, tables, lens.astype(np.int32)
+
+
+def _decode_and_check(pk, case, units=None, **kw):
+    import torch
+
+    q, k8, v8, ks, vs, tables, lens = case
+    out = pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=int(lens.max()), k_scale=ks, v_scale=vs, **kw)
+    torch.cuda.synchronize()
+    got = harness.bf16_tensor_to_f64(out)
+    want = oracle.paged_decode_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy(), ks.cpu().numpy(),
+                                   vs.cpu().numpy(), tables, lens, units=units)
+    if units is not None:
+        got = np.stack([got[b, h] for b, h in units])
+    stats = harness.assert_close(got, want)
+    assert pk.pa_device_errors() == 0
+    return stats
+
+
+# ---------------------------------------------------------------- the write
+
+
+def test_fp8_write_bit_exact_with_ties_and_saturation(pk):
+    """Whole caches against the oracle's quantising write. The rows include
+    every exact midpoint between neighbouring E4M3 values (round to nearest
+    even decides them), values past 448 (saturation), zeros and negative
+    slots."""
+    import torch
+
+    Hkv, D, NB = 4, 128, 12
+    rng = np.random.default_rng(5)
+    grid = oracle.e4m3_to_f64(np.arange(0x7F))
+    mids = (grid[1:] + grid[:-1]) / 2  # exact in bf16 (at most 5 significant bits)
+    special = np.concatenate([mids, -mids, [0.0, -0.0, 448.0, 460.0, 470.0, 1000.0, -3e4]])
+    T = 40
+    kn = rng.standard_normal((T, Hkv, D)) * 40
+    vn = rng.standard_normal((T, Hkv, D)) * 40
+    flat = kn.reshape(-1)
+    flat[: len(special)] = special
+    vflat = vn.reshape(-1)
+    vflat[-len(special):] = special[::-1]
+    kn_t = torch.from_numpy(kn).to(torch.bfloat16)
+    vn_t = torch.from_numpy(vn).to(torch.bfloat16)
+    ks = np.array([1.0, 0.5, 2.0, 0.37], dtype=np.float32)  # 1.0: the ties stay exact ties
+    vs = np.array([1.0, 3.0, 0.25, 1.7], dtype=np.float32)
+    slots = rng.permutation(NB * 16)[:T].astype(np.int64)
+    slots[[3, 17]] = -1
+    k0 = rng.integers(0, 256, size=(NB, Hkv, 16, D), dtype=np.uint8)
+    v0 = rng.integers(0, 256, size=(NB, Hkv, D, 16), dtype=np.uint8)
+    kc, vc = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    pk.pa_reshape_and_cache_fp8(kn_t.cuda(), vn_t.cuda(), kc, vc, torch.from_numpy(slots).cuda(),
+                                torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda())
+    torch.cuda.synchronize()
+    ko, vo = oracle.reshape_and_cache_fp8(kn_t, vn_t, k0, v0, slots, ks, vs)
+    assert np.array_equal(kc.cpu().numpy(), ko)
+    assert np.array_equal(vc.cpu().numpy(), vo)
+    assert pk.pa_device_errors() == 0
+
+
+def test_fp8_copy_blocks_bit_exact(pk):
+    import torch
+
+    rng = np.random.default_rng(6)
+    k0 = rng.integers(0, 256, size=(10, 8, 16, 128), dtype=np.uint8)
+    v0 = rng.integers(0, 256, size=(10, 8, 128, 16), dtype=np.uint8)
+    kc, vc = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    pairs = np.array([[1, 7], [3, 2], [9, 0]], dtype=np.int32)
+    pk.pa_copy_blocks_fp8(kc, vc, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    ko, vo = oracle.copy_blocks_fp8(k0, v0, pairs)
+    assert np.array_equal(kc.cpu().numpy(), ko) and np.array_equal(vc.cpu().numpy(), vo)
+
+
+# ---------------------------------------------------------------- the decode
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("Hkv", [1, 4, 8])
+def test_fp8_decode_edge_lengths(pk, G, Hkv):
+    lens = [1, 15, 16, 17, 100, 511, 513, 1025]
+    case = _fp8_case(pk, lens, Hq=G * Hkv, Hkv=Hkv, seed=40 + G + Hkv)
+    _decode_and_check(pk, case)
+
+
+def test_fp8_decode_llama8b_layer_shape(pk):
+    """64 sequences, 32/8 heads, lengths U[128, 2048]: the bench's shape."""
+    r = workloads.llama8b_layer()
+    case = _fp8_case(pk, r.lens0 + 1, Hq=32, Hkv=8, seed=51)
+    units = harness.sample_units(64, 32, 256, seed=2)
+    _decode_and_check(pk, case, units=units)
+
+
+def test_fp8_decode_llama70b_shape(pk):
+    """8 sequences, 64/8 heads, lengths U[8192, 32768]: sequences spread over
+    many CTAs, merged by the split-K merge."""
+    r = workloads.llama70b_long(batch=8)
+    case = _fp8_case(pk, r.lens0 + 1, Hq=64, Hkv=8, seed=52)
+    units = harness.sample_units(8, 64, 96, seed=3)
+    _decode_and_check(pk, case, units=units)
+
+
+def test_fp8_decode_zero_length_rows_are_zero(pk):
+    import torch
+
+    case = _fp8_case(pk, [40, 0, 3, 0], Hq=8, Hkv=2, seed=53)
+    q, k8, v8, ks, vs, tables, lens = case
+    out = torch.full_like(q, 7.0)
+    pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                 max_context_len=40, k_scale=ks, v_scale=vs, out=out)
+    torch.cuda.synchronize()
+    got = harness.bf16_tensor_to_f64(out)
+    assert not got[1].any() and not got[3].any()
+    want = oracle.paged_decode_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy(), ks.cpu().numpy(),
+                                   vs.cpu().numpy(), tables, lens,
+                                   units=[(b, h) for b in (0, 2) for h in range(8)])
+    harness.assert_close(np.concatenate([got[0], got[2]]), want)
+
+
+def test_fp8_decode_placement_invariance_bit_exact(pk):
+    """The same logical cache under two physical placements gives the same bits."""
+    import torch
+
+    lens = [300, 47, 900]
+    a = _fp8_case(pk, lens, Hq=16, Hkv=4, seed=54)
+    q, k8, v8, ks, vs, tables, lens_a = a
+    NB = k8.shape[0]
+    perm = np.random.default_rng(9).permutation(NB)
+    inv = np.argsort(perm)
+    k8b, v8b = torch.empty_like(k8), torch.empty_like(v8)
+    k8b[torch.from_numpy(perm).cuda()] = k8
+    v8b[torch.from_numpy(perm).cuda()] = v8
+    tables_b = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    assert (inv[perm] == np.arange(NB)).all()
+    outs = []
+    for kc, vc, tb in ((k8, v8, tables), (k8b, v8b, tables_b)):
+        outs.append(pk.pa_decode(q, kc, vc, torch.from_numpy(tb).cuda(),
+                                 torch.from_numpy(lens_a).cuda(), max_context_len=900,
+                                 k_scale=ks, v_scale=vs))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_fp8_unsupported_shapes_are_rejected(pk):
+    import torch
+
+    case = _fp8_case(pk, [20], Hq=8, Hkv=2, seed=55)
+    q, k8, v8, ks, vs, tables, lens = case
+    with pytest.raises(pk.PagedKVError):
+        pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                     max_context_len=20, k_scale=ks, v_scale=vs, variant=pk.DECODE_CUDA_CORE)
