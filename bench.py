@@ -371,6 +371,8 @@ def run_ours(args, rank: int, world: int) -> dict:
     if not args.no_workloads:
         res["other_workloads"] = measure_other_workloads(pk, device, variant=args.variant,
                                                          overlap=not args.no_overlap, fused=fused)
+        if args.variant == 0:
+            res["other_workloads"].update(measure_fp8_workloads(pk, device))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(r, W, budget_s=args.cpu_baseline_s)
     return res
@@ -425,6 +427,122 @@ def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True, 
             "step_ms": round(step_ms, 5), "step_gbs": round(step_b / (step_ms * 1e-3) / 1e9, 1),
         }
         del plans, keep, W
+        torch.cuda.empty_cache()
+    return out
+
+
+def decode_bytes_fp8(lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     block_size: int = 16) -> int:
+    """Algorithmic bytes of one decode over the 8-bit cache: one byte per K/V
+    element, bf16 q in and out, table entries, lengths."""
+    lens = np.asarray(lens, dtype=np.int64)
+    B = len(lens)
+    kv = int(lens.sum()) * num_kv_heads * head_dim * 2
+    qo = B * num_q_heads * head_dim * 2 * 2
+    tables = int(((lens + block_size - 1) // block_size).sum()) * 4 + 4 * B
+    return kv + qo + tables
+
+
+class Fp8StepPlan:
+    """One step on the 8-bit cache: copy-on-write copies, the quantising KV
+    write, the decode (query split, decode kernel, merge)."""
+
+    def __init__(self, pk, lib, dec_params, ws, rc_args, cow_args, stream):
+        self.lib, self.dec, self.ws = lib, dec_params, ws
+        self.rc_args, self.cow_args, self.stream = rc_args, cow_args, stream
+
+    def run(self, ev_dec=None):
+        lib = self.lib
+        if self.cow_args is not None:
+            if lib.pa_copy_blocks_fp8(*self.cow_args, self.stream):
+                raise RuntimeError("pa_copy_blocks_fp8 failed")
+        if lib.pa_reshape_and_cache_fp8(*self.rc_args, self.stream):
+            raise RuntimeError("pa_reshape_and_cache_fp8 failed")
+        if ev_dec is not None:
+            ev_dec[0].record()
+        st = lib.pa_decode(ctypes.byref(self.dec), self.ws.data_ptr(), self.ws.numel(), self.stream)
+        if st:
+            raise RuntimeError(f"pa_decode (8-bit cache) failed: {st}: {lib.pa_last_error()}")
+        if ev_dec is not None:
+            ev_dec[1].record()
+
+
+def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10) -> dict:
+    """The same workloads on the 8-bit (E4M3) cache: each bf16 pool copy is
+    quantised into an E4M3 pool (per-KV-head scales 0.05 for K and V) through
+    pa_reshape_and_cache_fp8, then timed like the bf16 runs."""
+    import torch
+
+    lib = pk.load()
+    out = {}
+    recipes = [("llama8b_layer_b64_fp8_e4m3", workloads.llama8b_layer()),
+               ("llama8b_high_concurrency_b256_fp8_e4m3", workloads.llama8b_high_concurrency()),
+               ("llama70b_long_b8_fp8_e4m3", workloads.llama70b_long(batch=8))]
+    peak = measured_peaks()["hbm_gbs"]
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream or None
+    for name, r in recipes:
+        W = setup_workload(r, device, n_copies=2)
+        H, D = r.num_kv_heads, r.head_dim
+        ks = torch.full((H,), 0.05, dtype=torch.float32, device=device)
+        vs = torch.full((H,), 0.05, dtype=torch.float32, device=device)
+        tables_d = torch.from_numpy(W["tables"]).to(device)
+        lens_d = torch.from_numpy(W["lens"]).to(device)
+        slots_d = torch.from_numpy(W["slots"]).to(device)
+        cows_d = torch.from_numpy(W["cows"]).to(device) if len(W["cows"]) else None
+        outb = torch.empty_like(W["q"])
+        keep, plans = [ks, vs, tables_d, lens_d, slots_d, cows_d, outb], []
+        for kc, vc in W["copies"]:
+            NB = kc.shape[0]
+            k8 = torch.empty((NB, H, 16, D), dtype=torch.uint8, device=device)
+            v8 = torch.empty((NB, H, D, 16), dtype=torch.uint8, device=device)
+            rows = torch.arange(NB * 16, dtype=torch.int64, device=device)
+            pk.pa_reshape_and_cache_fp8(kc.permute(0, 2, 1, 3).reshape(NB * 16, H, D).contiguous(),
+                                        vc.permute(0, 2, 1, 3).reshape(NB * 16, H, D).contiguous(),
+                                        k8, v8, rows, ks, vs)
+            p = pk.make_decode_params(W["q"], outb, k8, v8, tables_d, lens_d,
+                                      max_context_len=int(W["lens"].max()), k_scale=ks, v_scale=vs,
+                                      overlap_prologue=True)
+            ws = torch.empty(pk.pa_decode_workspace_size(p), dtype=torch.uint8, device=device)
+            rc_args = (W["kn"].data_ptr(), W["vn"].data_ptr(), k8.data_ptr(), v8.data_ptr(),
+                       slots_d.data_ptr(), ks.data_ptr(), vs.data_ptr(), W["kn"].shape[0], H, D,
+                       16, NB)
+            cow_args = None if cows_d is None else (k8.data_ptr(), v8.data_ptr(),
+                                                     cows_d.data_ptr(), cows_d.shape[0], H, D,
+                                                     16, NB)
+            plans.append(Fp8StepPlan(pk, lib, p, ws, rc_args, cow_args, sh))
+            keep += [k8, v8, ws]
+        del W["copies"]
+        torch.cuda.empty_cache()
+        lens = W["lens"]
+        dec_b = decode_bytes_fp8(lens, r.num_q_heads, H, D)
+        app_b = len(W["slots"]) * H * D * 6 + 8 * len(W["slots"])
+        step_b = dec_b + app_b + len(W["cows"]) * 2 * H * 16 * D * 2
+        for i in range(warmup):
+            plans[i % len(plans)].run()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        for k in range(steps):
+            plans[k % len(plans)].run(evs[k])
+        torch.cuda.synchronize()
+        dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(steps):
+            plans[k % len(plans)].run()
+        b.record(stream)
+        torch.cuda.synchronize()
+        step_ms = a.elapsed_time(b) / steps
+        dec_gbs = dec_b / (dec_ms * 1e-3) / 1e9
+        out[name] = {
+            "num_seqs": r.num_seqs, "num_q_heads": r.num_q_heads,
+            "context_tokens": int(lens.sum()), "decode_bytes": dec_b,
+            "decode_ms": round(dec_ms, 5), "decode_gbs": round(dec_gbs, 1),
+            "decode_frac": round(dec_gbs / peak, 4), "step_ms": round(step_ms, 5),
+            "step_gbs": round(step_b / (step_ms * 1e-3) / 1e9, 1),
+        }
+        del plans, keep
         torch.cuda.empty_cache()
     return out
 

@@ -97,9 +97,14 @@ struct TcCfg {
   static constexpr int Q_BYTES = F8 ? 2 * QH_BYTES : HALVES * QH_BYTES;  // F8: hi, lo
   static constexpr int PH_BYTES = N * 128;         // P^T [N rows][64 keys] or [N rows][128 keys]
   static constexpr int P_BYTES = 2 * PH_BYTES;     // bf16: 128 keys; F8: hi and lo
+  // P buffers. One: a second buffer would let the softmax write P(c) while
+  // the value product of c-1 still reads P, but it costs a ring slot, and on
+  // GB300 neither cache type ran faster with it (the softmax spends ~180
+  // cycles of its ~1400-2400 per chunk waiting for that product).
+  static constexpr int PB = 1;
   static constexpr int MISC_BYTES = 4096;
   static constexpr int ST_FIT =
-      (kMaxDynSmem - 1024 - 2 * Q_BYTES - P_BYTES - MISC_BYTES) / SLOT_BYTES;
+      (kMaxDynSmem - 1024 - 2 * Q_BYTES - PB * P_BYTES - MISC_BYTES) / SLOT_BYTES;
   static constexpr int ST_CAP = F8 ? 6 : 4;
   static constexpr int ST = ST_FIT > ST_CAP ? ST_CAP : ST_FIT;
   static_assert(!F8 || D == 128, "the 8-bit cache is built for head_dim 128");
@@ -107,9 +112,9 @@ struct TcCfg {
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_Q = ST * SLOT_BYTES;
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_MISC = OFF_P + P_BYTES;
-  // full[ST] empty[ST] qempty[2] s[3] o p drain
-  static constexpr int NBARS = 2 * ST + 8;
+  static constexpr int OFF_MISC = OFF_P + PB * P_BYTES;
+  // full[ST] empty[ST] qempty[2] s[3] o[2] p[2] drain
+  static constexpr int NBARS = 2 * ST + 10;
   static constexpr int OFF_BARS = OFF_MISC;
   static constexpr int OFF_META = OFF_BARS + (NBARS * 8 + 15) / 16 * 16;
   static constexpr int OFF_RED = OFF_META + ST * int(sizeof(ChunkMeta));  // [2][8 groups][8]
@@ -123,12 +128,15 @@ struct TcCfg {
   static constexpr int SMEM = OFF_KVSCALE + 64 + 1024;  // + alignment slack
   static_assert(OFF_KVSCALE + 64 <= OFF_MISC + MISC_BYTES, "misc area");
   static_assert(SMEM <= kMaxDynSmem, "shared memory budget");
-  static constexpr int TMEM_COLS = 4 * N;  // S triple buffer [0, 3N), O at [3N, 4N)
+  // MMA width: the query heads, twice over for the 8-bit cache (the hi and lo
+  // terms of Q and of P side by side, one MMA for both)
+  static constexpr int NS = F8 ? 2 * N : N;
+  static constexpr int TMEM_COLS = 4 * NS;  // S triple buffer [0, 3NS), O at [3NS, 4NS)
   static constexpr int kSBufs = 3;
   static constexpr uint32_t IDESC_S =
-      F8 ? dev::idesc_e4m3_f32(ROWS, N) : dev::idesc_bf16_f32(ROWS, N, false, false);
+      F8 ? dev::idesc_e4m3_f32(ROWS, NS) : dev::idesc_bf16_f32(ROWS, N, false, false);
   static constexpr uint32_t IDESC_PV =
-      F8 ? dev::idesc_e4m3_f32(ROWS, N) : dev::idesc_bf16_f32(ROWS, N, true, false);
+      F8 ? dev::idesc_e4m3_f32(ROWS, NS) : dev::idesc_bf16_f32(ROWS, N, true, false);
   static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
   static constexpr uint32_t Q_TX = Q_BYTES + (F8 ? N * 4 : 0);  // F8: + 1/alpha per column
 };
@@ -176,8 +184,7 @@ __device__ __forceinline__ uint32_t p8_offset(int n, int key) {
 }
 
 // S^T = Kchunk . Q^T for one chunk (single thread). bf16: D/16 MMAs of K = 16.
-// E4M3: D/32 MMAs of K = 32 for each of the two query terms (hi, then lo),
-// accumulating into the same scores.
+// E4M3: D/32 MMAs of K = 32, each over both query terms at once.
 template <int D, int N, bool F8>
 __device__ __forceinline__ void issue_scores(uint32_t tmem_col, const unsigned char* kv,
                                              const unsigned char* q) {
@@ -185,15 +192,12 @@ __device__ __forceinline__ void issue_scores(uint32_t tmem_col, const unsigned c
   const uint32_t kb = dev::smem_addr(kv);
   const uint32_t qb = dev::smem_addr(q);
   if constexpr (F8) {
+    // B = the 2N query rows (hi terms, then lo terms): score columns [0, N)
+    // from hi, [N, 2N) from lo, added by the softmax
 #pragma unroll
-    for (int kk = 0; kk < D / 32; ++kk) {
-      const uint64_t a = dev::smem_desc(kb + kk * 32, 16, 1024, dev::kSwizzle128B);
-      dev::mma_e4m3(tmem_col, a, dev::smem_desc(qb + kk * 32, 16, 1024, dev::kSwizzle128B),
-                    C::IDESC_S, kk > 0);
-      dev::mma_e4m3(tmem_col, a,
-                    dev::smem_desc(qb + C::QH_BYTES + kk * 32, 16, 1024, dev::kSwizzle128B),
-                    C::IDESC_S, true);
-    }
+    for (int kk = 0; kk < D / 32; ++kk)
+      dev::mma_e4m3(tmem_col, dev::smem_desc(kb + kk * 32, 16, 1024, dev::kSwizzle128B),
+                    dev::smem_desc(qb + kk * 32, 16, 1024, dev::kSwizzle128B), C::IDESC_S, kk > 0);
   } else {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
@@ -235,7 +239,9 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
   for (;;) {
     bool progress = false;
     // value product first: it frees a ring slot for the producer
-    if (c < s_pos && c != end_pos && dev::mbar_test(bar_p, uint32_t(c) & 1u)) {
+    if (c < s_pos && c != end_pos &&
+        dev::mbar_test(&bar_p[c % C::PB], uint32_t(c / C::PB) & 1u)) {
+      const uint32_t pbc = pbs + uint32_t(c % C::PB) * C::P_BYTES;  // this chunk's P
       const int sl = c % C::ST;
       // O accumulates over a segment's chunks; its first chunk starts afresh
       const bool fresh = (meta[sl].flags & F_FIRST) != 0;
@@ -244,29 +250,26 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       if constexpr (F8) {
         // V^T K-major without swizzle: 8-row x 16-byte core matrices, the
         // next 8 rows of d 128 B on (SBO), the next 16 keys one [D][16]
-        // tile on (LBO); 32 keys per MMA, each against P's hi and lo terms
+        // tile on (LBO); 32 keys per MMA. B = the 2N rows of P (hi terms,
+        // then lo terms): O columns [0, N) from hi, [N, 2N) from lo.
 #pragma unroll
-        for (int kk = 0; kk < ROWS / 32; ++kk) {
-          const uint64_t a =
-              dev::smem_desc(vb + kk * 2 * C::VT_TILE, C::VT_TILE, 128, dev::kSwizzleNone);
-          dev::mma_e4m3(tmem + C::kSBufs * N, a,
-                        dev::smem_desc(pbs + kk * 32, 16, 1024, dev::kSwizzle128B), C::IDESC_PV,
+        for (int kk = 0; kk < ROWS / 32; ++kk)
+          dev::mma_e4m3(tmem + C::kSBufs * C::NS,
+                        dev::smem_desc(vb + kk * 2 * C::VT_TILE, C::VT_TILE, 128,
+                                       dev::kSwizzleNone),
+                        dev::smem_desc(pbc + kk * 32, 16, 1024, dev::kSwizzle128B), C::IDESC_PV,
                         kk > 0 || !fresh);
-          dev::mma_e4m3(tmem + C::kSBufs * N, a,
-                        dev::smem_desc(pbs + C::PH_BYTES + kk * 32, 16, 1024, dev::kSwizzle128B),
-                        C::IDESC_PV, true);
-        }
       } else {
 #pragma unroll
         for (int kk = 0; kk < ROWS / 16; ++kk) {
-          dev::mma_bf16(tmem + C::kSBufs * N,
+          dev::mma_bf16(tmem + C::kSBufs * C::NS,
                         dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
-                        dev::smem_desc(pbs + (kk >> 2) * C::PH_BYTES + (kk & 3) * 32, 16, 1024,
+                        dev::smem_desc(pbc + (kk >> 2) * C::PH_BYTES + (kk & 3) * 32, 16, 1024,
                                        dev::kSwizzle128B),
                         C::IDESC_PV, kk > 0 || !fresh);
         }
       }
-      dev::mma_commit(bar_o);
+      dev::mma_commit(&bar_o[c % C::PB]);
       dev::mma_commit(&empty[sl]);
       ++c;
       progress = true;
@@ -282,7 +285,7 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       } else {
         const int sb = s_pos % C::kSBufs;
         dev::tc_fence_after();
-        issue_scores<D, N, F8>(tmem + sb * N, ring + size_t(sl) * C::SLOT_BYTES,
+        issue_scores<D, N, F8>(tmem + sb * C::NS, ring + size_t(sl) * C::SLOT_BYTES,
                                qbuf + mn.qslot * C::Q_BYTES);
         dev::mma_commit(&bar_s[sb]);
         if (mn.flags & F_LAST) dev::mma_commit(&qempty[mn.qslot]);
@@ -342,7 +345,7 @@ struct Softmax {
     const int col0 = H >= 2 ? h0 * G : 0;
     const bool upper = H >= 2 && lane >= 16;  // this lane's head is the warp's second
     const uint32_t t_lane = uint32_t(cw * 32) << 16;
-    const uint32_t tO = tmem + t_lane + C::kSBufs * N;
+    const uint32_t tO = tmem + t_lane + C::kSBufs * C::NS;  // F8: + N for the lo terms
 
     // Reference maximum per query head (log2 domain) and this row's share of
     // the softmax sum relative to it. O^T accumulates in TMEM relative to the
@@ -356,6 +359,13 @@ struct Softmax {
     }
     int c = 0;  // ring position = chunk index
     bool ok = true;
+    int pv_done = -1;  // highest chunk whose value product is known to be complete
+    // wait for chunk k's value product (k > pv_done)
+    auto wait_pv = [&](int k) {
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[k % C::PB], uint32_t(k / C::PB) & 1u)) &&
+           ok;
+      pv_done = k;
+    };
 
     for (;;) {
       const int slot = c % C::ST;
@@ -374,10 +384,21 @@ struct Softmax {
       ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(c / C::kSBufs) & 1u)) && ok;
       dev::tc_fence_after();
       float s[LDC];
+      const uint32_t tS = tmem + t_lane + buf * C::NS + col0;
       if constexpr (LDC == 8) {
-        dev::tmem_ld8(tmem + t_lane + buf * N + col0, s);
+        dev::tmem_ld8(tS, s);
       } else {
-        dev::tmem_ld16(tmem + t_lane + buf * N + col0, s);
+        dev::tmem_ld16(tS, s);
+      }
+      if constexpr (F8) {  // + the scores of the lo query terms
+        float s2[LDC];
+        if constexpr (LDC == 8) {
+          dev::tmem_ld8(tS + N, s2);
+        } else {
+          dev::tmem_ld16(tS + N, s2);
+        }
+#pragma unroll
+        for (int i = 0; i < LDC; ++i) s[i] += s2[i];
       }
 
       // ---- chunk maximum per query head: row = (block u, head h, key)
@@ -414,7 +435,6 @@ struct Softmax {
       for (int j = 0; j < G; ++j) need |= cm[j] > m_ref[j] + kRescaleLog2;
 
       // ---- raise the reference where needed; rescale l and (in TMEM) O^T
-      bool waited_prev = false;
       if (dev::named_barrier_or(1, kCons, need)) {
 #pragma unroll
         for (int j = 0; j < G; ++j) {
@@ -426,20 +446,22 @@ struct Softmax {
         }
         if (!first) {
           // chunk c-1's value product must be in O^T before it is scaled
-          ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(c - 1) & 1u)) && ok;
-          waited_prev = true;
+          if (pv_done < c - 1) wait_pv(c - 1);
           dev::named_barrier(1, kCons);  // every factor is written
           dev::tc_fence_after();
-          float o[N];
-          dev::tmem_ld_cols<N>(tO, o);
 #pragma unroll
-          for (int n = 0; n < N; ++n) o[n] *= alpha_s[n];
-          dev::tmem_st_cols<N>(tO, o);
+          for (int part = 0; part < (F8 ? 2 : 1); ++part) {  // F8: hi and lo columns
+            float o[N];
+            dev::tmem_ld_cols<N>(tO + part * N, o);
+#pragma unroll
+            for (int n = 0; n < N; ++n) o[n] *= alpha_s[n];
+            dev::tmem_st_cols<N>(tO + part * N, o);
+          }
         }
       }
-      // P of chunk c-1 must have been consumed before P is rewritten
-      if (!first && !waited_prev)
-        ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(c - 1) & 1u)) && ok;
+      // the value product that last read this P buffer (chunk c - PB) must be done
+      if (c - C::PB >= 0 && pv_done < c - C::PB) wait_pv(c - C::PB);
+      unsigned char* pcur = pbuf + (c % C::PB) * C::P_BYTES;
 
 #pragma unroll
       for (int j = 0; j < G; ++j) {
@@ -451,11 +473,11 @@ struct Softmax {
           const uint8_t pl = dev::to_e4m3(p - phf);
           l_part[j] += phf + dev::from_e4m3(pl);
           const uint32_t o = p8_offset(h * G + j, ctid);
-          pbuf[o] = ph;
-          pbuf[C::PH_BYTES + o] = pl;
+          pcur[o] = ph;
+          pcur[C::PH_BYTES + o] = pl;
         } else {
           l_part[j] += p;
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + p_offset<N>(h * G + j, ctid)) =
+          *reinterpret_cast<__nv_bfloat16*>(pcur + p_offset<N>(h * G + j, ctid)) =
               __float2bfloat16_rn(p);
         }
       }
@@ -479,7 +501,7 @@ struct Softmax {
       }
       dev::fence_async_smem();
       dev::tc_fence_before();
-      dev::mbar_arrive(bar_p);  // P(c) written; S(c) read; O^T rescaled
+      dev::mbar_arrive(&bar_p[c % C::PB]);  // P(c) written; S(c) read; O^T rescaled
 
       if (m.flags & F_LAST) {
         // per query head: softmax denominator over all rows of its KV head
@@ -500,13 +522,19 @@ struct Softmax {
             m_s[h * G + j] = m_ref[j];
           }
         }
-        ok = __all_sync(0xffffffffu, dev::mbar_wait(bar_o, uint32_t(c) & 1u)) && ok;
+        wait_pv(c);
         dev::tc_fence_after();
         float o[N];
         dev::tmem_ld_cols<N>(tO, o);
-        if constexpr (F8) {  // the V scale of each query head's KV head
+        if constexpr (F8) {  // hi + lo terms, times the V scale of each head's KV head
 #pragma unroll
-          for (int n = 0; n < N; ++n) o[n] *= kvscale[8 + (n < Hq ? n / G : 0)];
+          for (int cg = 0; cg < N; cg += 16) {
+            float o2[16];
+            dev::tmem_ld_cols<16>(tO + N + cg, o2);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              o[cg + i] = (o[cg + i] + o2[i]) * kvscale[8 + (cg + i < Hq ? (cg + i) / G : 0)];
+          }
         }
         dev::named_barrier(1, kCons);  // l_s, m_s written
         if (ctid < D) {
@@ -560,9 +588,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* empty = bars + C::ST;
   uint64_t* qempty = bars + 2 * C::ST;
   uint64_t* bar_s = bars + 2 * C::ST + 2;  // [3] scores ready
-  uint64_t* bar_o = bar_s + 3;              // value product ready
-  uint64_t* bar_p = bar_o + 1;              // P written by all 128 softmax threads
-  uint64_t* drain = bar_p + 1;
+  uint64_t* bar_o = bar_s + 3;              // [2] value product ready (by P buffer)
+  uint64_t* bar_p = bar_o + 2;              // [2] P written by all 128 softmax threads
+  uint64_t* drain = bar_p + 2;
   ChunkMeta* meta = reinterpret_cast<ChunkMeta*>(smem + C::OFF_META);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* red2 = reinterpret_cast<float*>(smem + C::OFF_RED2);
@@ -589,8 +617,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int i = 0; i < 2; ++i) dev::mbar_init(&qempty[i], 1);
     for (int i = 0; i < 3; ++i) dev::mbar_init(&bar_s[i], 1);
-    dev::mbar_init(bar_o, 1);
-    dev::mbar_init(bar_p, kCons);
+    for (int i = 0; i < 2; ++i) {
+      dev::mbar_init(&bar_o[i], 1);
+      dev::mbar_init(&bar_p[i], kCons);
+    }
     dev::mbar_init(drain, 1);
     *abort_flag = 0;
     *consumed = 0;
@@ -598,7 +628,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     dev::fence_barrier_init();
   }
   // P^T is block-diagonal: the entries off the diagonal stay zero for good.
-  for (int i = tid; i < C::P_BYTES / 16; i += NTHREADS)
+  for (int i = tid; i < C::PB * C::P_BYTES / 16; i += NTHREADS)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
 
   // ---- stream-K plan (uses the still-empty ring as scratch): block counts of
@@ -783,26 +813,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int e = __shfl_sync(0xffffffffu, win, (jb & 31) + (lane % U));
         unsigned char* kdst = ring + size_t(slot) * C::SLOT_BYTES;
         if constexpr (F8) {
-          // lane j < 8 also brings the V^T tile of (block j / H, KV head j % H)
-          const int uv = min(lane / H, U - 1);
-          const int ev = __shfl_sync(0xffffffffu, win, (jb & 31) + uv);
+          // lanes 0..U-1: block `lane`'s K rows, and its H V^T tiles as one
+          // 3-D box (the tiles of a block are adjacent in the cache)
           if (lane < U) {
-            int row = P.oob_row;
+            int row = P.oob_row, tile = P.oob_row_v;
             if (jb + lane < seg_nb) {
               if (e >= 0 && e < P.num_blocks) {
                 row = e * grows;
+                tile = e * H;
               } else {
                 atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
               }
             }
             dev::tma_load_2d(kdst + lane * grows * 128, &tm_k, 0, row, &full[slot], pol);
-          }
-          if (lane < kGroups) {
-            int row = P.oob_row_v;
-            if (jb + uv < seg_nb && ev >= 0 && ev < P.num_blocks)
-              row = (ev * H + (lane - uv * H)) * D;
-            dev::tma_load_2d(kdst + C::K_BYTES + lane * C::VT_TILE, &tm_v, 0, row, &full[slot],
-                             pol);
+            dev::tma_load_3d(kdst + C::K_BYTES + lane * H * C::VT_TILE, &tm_v, 0, 0, tile,
+                             &full[slot], pol);
           } else if (lane == 8 && c == 0) {
             dev::tma_load_2d(qbuf + qs * C::Q_BYTES, &tm_q, 0, b * P.q_rows, &full[slot], pol);
             dev::bulk_load(qalpha + qs * 64, P.q_inv_alpha + size_t(b) * N, N * 4, &full[slot],
@@ -1043,6 +1068,21 @@ int make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, 
   return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
 }
 
+// The 8-bit V^T cache as a 3-D byte tensor: [tiles][D rows][16 bytes], one
+// tile per (block, KV head); box = `heads` whole tiles, no swizzle.
+int make_map_vt(CUtensorMap* m, const void* base, uint64_t tiles, uint64_t d, uint32_t heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (encode_fn(&enc)) return int(cudaErrorNotSupported);
+  cuuint64_t gdim[3] = {uint64_t(BS), d, tiles};
+  cuuint64_t gstride[2] = {uint64_t(BS), d * BS};
+  cuuint32_t box[3] = {uint32_t(BS), uint32_t(d), heads};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
+}
+
 template <int D, int G, int N, bool F8>
 int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   using C = TcCfg<D, N, F8>;
@@ -1063,9 +1103,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
     // head); the split queries, 2N rows of D bytes per sequence
     r = make_map_u8(&tk, p->k_cache, cache_rows, D, D, uint32_t(BS * H),
                     CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!r)
-      r = make_map_u8(&tv, p->v_cache, uint64_t(p->num_blocks) * H * D, BS, BS, uint32_t(D),
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!r) r = make_map_vt(&tv, p->v_cache, uint64_t(p->num_blocks) * H, D, uint32_t(H));
     if (!r)
       r = make_map_u8(&tq, Lc.q8, uint64_t(p->num_seqs) * 2 * N, D, D, uint32_t(2 * N),
                       CU_TENSOR_MAP_SWIZZLE_128B);
@@ -1095,7 +1133,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.k_scale = p->k_scale;
   P.v_scale = p->v_scale;
   P.q_inv_alpha = Lc.q_inv_alpha;
-  P.oob_row_v = int(uint64_t(p->num_blocks) * H * D);
+  P.oob_row_v = int(uint64_t(p->num_blocks) * H);  // first V^T tile past the cache
   P.q_rows = F8 ? 2 * N : p->num_q_heads;
   P.max_blocks_per_seq = p->max_blocks_per_seq;
   P.num_seqs = p->num_seqs;
