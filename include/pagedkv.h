@@ -351,7 +351,9 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int
  *
  * Free list: a stack. free_order[0] (or block 0 when free_order is NULL) is
  * handed out first; a block whose refcount drops to zero is pushed on top
- * and handed out next. Every failing call leaves the pool unchanged.
+ * and handed out next (blocks of the prefix cache, below, excepted). Every
+ * failing call leaves the pool unchanged. free_blocks in the stats counts
+ * every block that can be handed out, evictable cached blocks included.
  * ---------------------------------------------------------------------- */
 typedef struct pa_pool pa_pool;
 
@@ -407,6 +409,44 @@ pa_status pa_seq_table(const pa_pool* pool, int32_t seq, int32_t* out, int32_t c
  * tables[n][max_blocks] (unused entries -1) and lens[n], ready to upload. */
 pa_status pa_pool_export(const pa_pool* pool, const int32_t* seqs, int32_t n, int32_t max_blocks,
                          int32_t* tables, int32_t* lens);
+
+/* ------------------------------------------------------------------------
+ * Prefix cache [P1 FAQ "Where does prefix caching fit?": blocks are
+ * content-hashed and a new request whose prompt hashes to resident blocks
+ * points at them; P3 §The architecture: the prefix cache hashes each full
+ * block's token ids chained with its prefix hash, a match maps the existing
+ * physical block with a bumped refcount and skips its prefill; §End-to-end
+ * flow: on completion the shared blocks' refcounts tick down and the
+ * preamble stays warm in the cache for the next request].
+ *
+ * pa_seq_create_prompt creates a sequence holding a prompt of num_tokens
+ * token ids (host int32). Its full blocks are looked up in order by the chain
+ * key (previous block's key, this block's block_size token ids); the leading
+ * run of matches is mapped (refcount + 1) and the rest of the prompt gets
+ * fresh blocks, whose full ones are entered in the cache. Matching stops at
+ * the first miss. A key match is confirmed on the stored token ids, so a
+ * hash collision never maps the wrong block.
+ *  *cached_tokens = block_size * (matched blocks): their K/V is already in
+ *   the cache; the caller writes only tokens [*cached_tokens, num_tokens).
+ *  slots (nullable, [num_tokens]): every token's slot.
+ * A block whose refcount drops to zero while it is in the cache stays in it
+ * (evictable): pa_pool_alloc and appends hand out never-cached free blocks
+ * first and then the least recently freed cached block, which leaves the
+ * cache at that moment. A cached block is never written in place: an append
+ * into it copies it first (copy-on-write), whatever its refcount. All or
+ * nothing: on PA_ERR_OOM the pool is unchanged. Without this call the pool
+ * behaves exactly as described above.
+ * ---------------------------------------------------------------------- */
+pa_status pa_seq_create_prompt(pa_pool* pool, const int32_t* tokens, int32_t num_tokens,
+                               int32_t* seq, int32_t* cached_tokens, int64_t* slots);
+
+typedef struct {
+  int32_t cached_blocks;     /* blocks in the cache (in use or evictable) */
+  int32_t evictable_blocks;  /* cached blocks with refcount 0 (counted as free) */
+  int64_t lookups;           /* full prompt blocks looked up */
+  int64_t hits;              /* of which mapped from the cache */
+} pa_prefix_stats_t;
+pa_status pa_pool_prefix_stats(const pa_pool* pool, pa_prefix_stats_t* stats);
 
 #ifdef __cplusplus
 }

@@ -364,6 +364,15 @@ class PoolModel:
       refcount + 1 ("How Paged Attention ...", §Paged attention -- sharing).
     * Free: the sequence's blocks are released in logical order.
     * Any failing operation leaves the state unchanged.
+    * Prefix cache ("How Paged Attention ...", FAQ on prefix caching;
+      PagedAttention architecture page, §The architecture and §End-to-end
+      flow): a prompt's full blocks are matched in order against the cache
+      by their whole token prefix (the exact form of a chained block hash);
+      the leading run of matches is shared (refcount + 1), the rest of the
+      prompt gets fresh blocks and its full ones enter the cache. A cached
+      block freed to refcount 0 stays cached and is handed out only when no
+      never-cached block is free, least recently freed first, leaving the
+      cache then. A cached block is immutable: an append into it copies it.
     """
 
     def __init__(self, num_blocks: int, block_size: int, free_order: Optional[Sequence[int]] = None):
@@ -379,12 +388,21 @@ class PoolModel:
         self.tables: Dict[int, List[int]] = {}
         self.lens: Dict[int, int] = {}
         self._next_seq = 0
+        self.prefix_of: Dict[int, tuple] = {}   # cached block -> its whole token prefix
+        self.block_of: Dict[tuple, int] = {}    # token prefix -> cached block
+        self.evictable: List[int] = []          # cached, refcount 0, least recently freed first
+        self.lookups = 0
+        self.hits = 0
 
     # ---- blocks
     def alloc(self) -> int:
-        if not self.free:
+        if self.free:
+            blk = self.free.pop()
+        elif self.evictable:
+            blk = self.evictable.pop(0)
+            del self.block_of[self.prefix_of.pop(blk)]
+        else:
             raise PoolOOM("pool exhausted")
-        blk = self.free.pop()
         self.ref[blk] = 1
         return blk
 
@@ -396,7 +414,10 @@ class PoolModel:
         self._check_live(blk)
         self.ref[blk] -= 1
         if self.ref[blk] == 0:
-            self.free.append(blk)
+            if blk in self.prefix_of:
+                self.evictable.append(blk)
+            else:
+                self.free.append(blk)
 
     def _check_live(self, blk: int) -> None:
         if not (0 <= blk < self.num_blocks):
@@ -406,7 +427,7 @@ class PoolModel:
 
     def stats(self) -> Dict[str, int]:
         used = sum(1 for r in self.ref if r > 0)
-        return {"free": len(self.free), "used": used,
+        return {"free": len(self.free) + len(self.evictable), "used": used,
                 "shared": sum(1 for r in self.ref if r > 1),
                 "max_refcount": max(self.ref) if self.ref else 0}
 
@@ -447,9 +468,9 @@ class PoolModel:
             self.tables[s].append(self.alloc())
         else:
             src = self.tables[s][j]
-            if self.ref[src] > 1:
+            if self.ref[src] > 1 or src in self.prefix_of:  # shared, or cached (immutable)
                 dst = self.alloc()
-                self.ref[src] -= 1  # cannot reach 0: it was > 1
+                self.decref(src)
                 self.tables[s][j] = dst
                 cow = (src, dst)
         self.lens[s] = pos + 1
@@ -463,6 +484,44 @@ class PoolModel:
             if cow:
                 cows.append(cow)
         return slots, cows
+
+    def create_prompt(self, tokens: Sequence[int]):
+        """New sequence holding a prompt. Returns (seq, cached_tokens, slots)."""
+        bs = self.block_size
+        tokens = [int(t) for t in tokens]
+        n = len(tokens)
+        nfull, nblocks = n // bs, -(-n // bs)
+        matched = []
+        for i in range(nfull):
+            blk = self.block_of.get(tuple(tokens[:(i + 1) * bs]))
+            if blk is None:
+                break
+            matched.append(blk)
+        revive = sum(1 for b in matched if self.ref[b] == 0)
+        if nblocks - len(matched) > len(self.free) + len(self.evictable) - revive:
+            raise PoolOOM("pool exhausted")
+        for b in matched:
+            if self.ref[b] == 0:
+                self.evictable.remove(b)
+            self.ref[b] += 1
+        s = self.seq_create()
+        table = list(matched)
+        for i in range(len(matched), nblocks):
+            blk = self.alloc()
+            table.append(blk)
+            prefix = tuple(tokens[:(i + 1) * bs])
+            if i < nfull and prefix not in self.block_of:
+                self.block_of[prefix] = blk
+                self.prefix_of[blk] = prefix
+        self.tables[s] = table
+        self.lens[s] = n
+        self.lookups += nfull
+        self.hits += len(matched)
+        return s, len(matched) * bs, [self.slot_of(s, t) for t in range(n)]
+
+    def prefix_stats(self) -> Dict[str, int]:
+        return {"cached_blocks": len(self.prefix_of), "evictable_blocks": len(self.evictable),
+                "lookups": self.lookups, "hits": self.hits}
 
     def table(self, s: int) -> List[int]:
         return list(self.tables[s])

@@ -43,7 +43,7 @@ EXPORTED_SYMBOLS = [
     "pa_pool_create", "pa_pool_destroy", "pa_pool_alloc", "pa_pool_incref", "pa_pool_decref",
     "pa_pool_refcount", "pa_pool_stats", "pa_seq_create", "pa_seq_free", "pa_seq_fork",
     "pa_seq_append_slot", "pa_seq_append_tokens", "pa_seq_length", "pa_seq_table",
-    "pa_pool_export",
+    "pa_pool_export", "pa_seq_create_prompt", "pa_pool_prefix_stats",
 ]
 
 
@@ -102,6 +102,11 @@ class StepHostParams(ctypes.Structure):
     ]
 
 
+class PrefixStats(ctypes.Structure):
+    _fields_ = [("cached_blocks", ctypes.c_int32), ("evictable_blocks", ctypes.c_int32),
+                ("lookups", ctypes.c_int64), ("hits", ctypes.c_int64)]
+
+
 class PoolStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("num_blocks", "block_size", "free_blocks", "used_blocks", "shared_blocks",
@@ -154,6 +159,8 @@ def load():
         "pa_seq_length": ([vp, i32, P(i32)], ctypes.c_int),
         "pa_seq_table": ([vp, i32, vp, i32, P(i32)], ctypes.c_int),
         "pa_pool_export": ([vp, vp, i32, i32, vp, vp], ctypes.c_int),
+        "pa_seq_create_prompt": ([vp, vp, i32, P(i32), P(i32), vp], ctypes.c_int),
+        "pa_pool_prefix_stats": ([vp, P(PrefixStats)], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -576,3 +583,20 @@ class Pool:
         _check(self._lib.pa_pool_export(self._h, s.ctypes.data, len(s), max_blocks,
                                         tables.ctypes.data, lens.ctypes.data), "pa_pool_export")
         return tables, lens
+
+    def create_prompt(self, tokens: Sequence[int]):
+        """New sequence holding a prompt, its leading full blocks mapped from the
+        prefix cache. Returns (seq, cached_tokens, slots)."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        seq, cached = ctypes.c_int32(), ctypes.c_int32()
+        slots = np.empty(max(len(t), 1), dtype=np.int64)
+        _check(self._lib.pa_seq_create_prompt(self._h, t.ctypes.data if len(t) else None, len(t),
+                                              ctypes.byref(seq), ctypes.byref(cached),
+                                              slots.ctypes.data), "pa_seq_create_prompt")
+        return seq.value, cached.value, slots[:len(t)].tolist()
+
+    def prefix_stats(self) -> dict:
+        st = PrefixStats()
+        _check(self._lib.pa_pool_prefix_stats(self._h, ctypes.byref(st)), "pa_pool_prefix_stats")
+        return {"cached_blocks": st.cached_blocks, "evictable_blocks": st.evictable_blocks,
+                "lookups": st.lookups, "hits": st.hits}

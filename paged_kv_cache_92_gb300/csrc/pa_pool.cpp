@@ -12,13 +12,26 @@
 // [16i, 16i+15]; every 16th token grabs a fresh block; blocks are immutable
 // while shared).
 //
+// Prefix cache: "How Paged Attention and Continuous Batching Actually
+// Work", FAQ (prefix caching is a consequence of paging: blocks are
+// content-hashed, a prompt that hashes to resident blocks points at them);
+// PagedAttention architecture walk-through, §The architecture (each full
+// block's token ids hashed chained with its prefix hash; a match maps the
+// existing block with a bumped refcount) and §End-to-end flow (the shared
+// preamble stays warm for the next request).
+//
 // Policy choices the pages leave open, stated in pagedkv.h: the free list is
 // a stack seeded from a caller-given order; a fresh block is taken when the
 // length is a multiple of the block size before the append; a failing call
-// leaves the pool unchanged.
+// leaves the pool unchanged; cached blocks freed to refcount 0 stay cached
+// and are handed out only after every never-cached free block, least
+// recently freed first.
 #include <cstdint>
 #include <cstring>
+#include <iterator>
+#include <list>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "pa_internal.h"
@@ -36,18 +49,51 @@ struct pa_pool {
   std::vector<Seq> seqs;
   int32_t live_seqs = 0;
 
+  // prefix cache: per-block chain key, the key of the block before it, its
+  // token ids; key -> block; cached blocks with refcount 0, least recently
+  // freed first
+  std::vector<uint8_t> cached;
+  std::vector<uint64_t> key, parent_key;
+  std::vector<std::vector<int32_t>> key_tokens;
+  std::unordered_map<uint64_t, int32_t> by_key;
+  std::list<int32_t> evictable;
+  std::vector<std::list<int32_t>::iterator> ev_pos;
+  int64_t lookups = 0, hits = 0;
+
   bool valid_block(int32_t b) const { return b >= 0 && b < num_blocks; }
   bool valid_seq(int32_t s) const {
     return s >= 0 && s < static_cast<int32_t>(seqs.size()) && seqs[s].live;
   }
+  // blocks that can be handed out
+  size_t available() const { return free_stack.size() + evictable.size(); }
+  void uncache(int32_t b) {
+    auto it = by_key.find(key[b]);
+    if (it != by_key.end() && it->second == b) by_key.erase(it);
+    cached[b] = 0;
+    key_tokens[b].clear();
+  }
   int32_t pop() {
-    int32_t b = free_stack.back();
-    free_stack.pop_back();
+    int32_t b;
+    if (!free_stack.empty()) {
+      b = free_stack.back();
+      free_stack.pop_back();
+    } else {  // evict the least recently freed cached block
+      b = evictable.front();
+      evictable.pop_front();
+      uncache(b);
+    }
     ref[b] = 1;
     return b;
   }
   void release(int32_t b) {
-    if (--ref[b] == 0) free_stack.push_back(b);
+    if (--ref[b] == 0) {
+      if (cached[b]) {
+        evictable.push_back(b);
+        ev_pos[b] = std::prev(evictable.end());
+      } else {
+        free_stack.push_back(b);
+      }
+    }
   }
 };
 
@@ -67,9 +113,9 @@ void append_one(pa_pool* p, pa_pool::Seq& q, int64_t* slot, int32_t* src, int32_
     q.table.push_back(p->pop());
   } else {
     const int32_t old = q.table[j];
-    if (p->ref[old] > 1) {
+    if (p->ref[old] > 1 || p->cached[old]) {  // shared, or cached (immutable)
       const int32_t fresh = p->pop();
-      p->ref[old] -= 1;  // was > 1, stays >= 1
+      p->release(old);
       q.table[j] = fresh;
       *cow = true;
       *src = old;
@@ -80,17 +126,39 @@ void append_one(pa_pool* p, pa_pool::Seq& q, int64_t* slot, int32_t* src, int32_
   *slot = static_cast<int64_t>(q.table[j]) * bs + pos % bs;
 }
 
-// Blocks that appending n tokens to q would take from the free list.
-int64_t blocks_for_append(const pa_pool* p, const pa_pool::Seq& q, int32_t n) {
-  if (n <= 0) return 0;
+// Whether appending n tokens to q finds enough blocks, following the order
+// in which append_one takes and releases them.
+bool append_fits(const pa_pool* p, const pa_pool::Seq& q, int32_t n) {
+  if (n <= 0) return true;
   const int32_t bs = p->block_size;
-  int64_t need = 0;
-  // the partially filled last block, if shared, costs one copy-on-write block
-  if (q.len % bs != 0 && p->ref[q.table[q.len / bs]] > 1) need += 1;
+  int64_t avail = static_cast<int64_t>(p->available());
+  // the partially filled last block, if shared or cached, is first copied
+  // into a fresh block; a cached block only this sequence held then becomes
+  // free (evictable) again
+  if (q.len % bs != 0) {
+    const int32_t b = q.table[q.len / bs];
+    if (p->ref[b] > 1 || p->cached[b]) {
+      if (avail < 1) return false;
+      if (p->ref[b] > 1) avail -= 1;
+    }
+  }
   // fresh blocks for every boundary crossed: positions len..len+n-1 that are multiples of bs
   const int64_t first = q.len, last = static_cast<int64_t>(q.len) + n - 1;
-  need += last / bs - (first + bs - 1) / bs + 1;
-  return need;
+  return avail >= last / bs - (first + bs - 1) / bs + 1;
+}
+
+// Chain key of a full block: its predecessor's key and its token ids
+// (splitmix64-style mixing; collisions are caught by the stored ids).
+uint64_t mix64(uint64_t x) {
+  x += 0x9E3779B97F4A7C15ull;
+  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+  return x ^ (x >> 31);
+}
+uint64_t chain_key(uint64_t parent, const int32_t* tokens, int32_t n) {
+  uint64_t k = mix64(parent ^ 0xC2B2AE3D27D4EB4Full);
+  for (int32_t i = 0; i < n; ++i) k = mix64(k ^ static_cast<uint32_t>(tokens[i]));
+  return k;
 }
 
 }  // namespace
@@ -108,6 +176,11 @@ pa_status pa_pool_create(int32_t num_blocks, int32_t block_size, const int32_t* 
   p->num_blocks = num_blocks;
   p->block_size = block_size;
   p->ref.assign(num_blocks, 0);
+  p->cached.assign(num_blocks, 0);
+  p->key.assign(num_blocks, 0);
+  p->parent_key.assign(num_blocks, 0);
+  p->key_tokens.resize(num_blocks);
+  p->ev_pos.resize(num_blocks);
   p->free_stack.resize(num_blocks);
   if (free_order) {
     std::vector<char> seen(num_blocks, 0);
@@ -131,7 +204,7 @@ void pa_pool_destroy(pa_pool* pool) { delete pool; }
 
 pa_status pa_pool_alloc(pa_pool* p, int32_t* block) {
   if (!p || !block) return fail(PA_ERR_INVALID_ARG, "pa_pool_alloc: NULL argument");
-  if (p->free_stack.empty()) return fail(PA_ERR_OOM, "pa_pool_alloc: pool exhausted");
+  if (p->available() == 0) return fail(PA_ERR_OOM, "pa_pool_alloc: pool exhausted");
   *block = p->pop();
   return PA_OK;
 }
@@ -162,7 +235,7 @@ pa_status pa_pool_stats(const pa_pool* p, pa_pool_stats_t* st) {
   std::memset(st, 0, sizeof(*st));
   st->num_blocks = p->num_blocks;
   st->block_size = p->block_size;
-  st->free_blocks = static_cast<int32_t>(p->free_stack.size());
+  st->free_blocks = static_cast<int32_t>(p->available());
   for (int32_t r : p->ref) {
     if (r >= 1) st->used_blocks += 1;
     if (r >= 2) st->shared_blocks += 1;
@@ -217,7 +290,7 @@ pa_status pa_seq_append_slot(pa_pool* p, int32_t seq, int64_t* slot, int32_t cow
   if (!p->valid_seq(seq)) return fail(PA_ERR_BOUNDS, "pa_seq_append_slot: unknown sequence");
   pa_pool::Seq& q = p->seqs[seq];
   if (q.len == INT32_MAX) return fail(PA_ERR_INVALID_ARG, "pa_seq_append_slot: length overflow");
-  if (blocks_for_append(p, q, 1) > static_cast<int64_t>(p->free_stack.size()))
+  if (!append_fits(p, q, 1))
     return fail(PA_ERR_OOM, "pa_seq_append_slot: pool exhausted");
   int32_t src = -1, dst = -1;
   bool cow = false;
@@ -238,7 +311,7 @@ pa_status pa_seq_append_tokens(pa_pool* p, int32_t seq, int32_t n, int64_t* slot
   pa_pool::Seq& q = p->seqs[seq];
   if (static_cast<int64_t>(q.len) + n > INT32_MAX)
     return fail(PA_ERR_INVALID_ARG, "pa_seq_append_tokens: length overflow");
-  if (blocks_for_append(p, q, n) > static_cast<int64_t>(p->free_stack.size()))
+  if (!append_fits(p, q, n))
     return fail(PA_ERR_OOM, "pa_seq_append_tokens: pool exhausted");
   int32_t ncow = 0;
   for (int32_t i = 0; i < n; ++i) {
@@ -277,6 +350,84 @@ pa_status pa_seq_table(const pa_pool* p, int32_t seq, int32_t* out, int32_t cap,
     if (cap < n) return fail(PA_ERR_INVALID_ARG, "pa_seq_table: cap smaller than the table");
     std::memcpy(out, q.table.data(), sizeof(int32_t) * n);
   }
+  return PA_OK;
+}
+
+pa_status pa_seq_create_prompt(pa_pool* p, const int32_t* tokens, int32_t num_tokens,
+                               int32_t* seq, int32_t* cached_tokens, int64_t* slots) {
+  if (!p || !seq || !cached_tokens || num_tokens < 0 || (num_tokens > 0 && !tokens))
+    return fail(PA_ERR_INVALID_ARG, "pa_seq_create_prompt: bad argument");
+  const int32_t bs = p->block_size;
+  const int32_t nfull = num_tokens / bs;
+  const int32_t nblocks = (num_tokens + bs - 1) / bs;
+  // chain keys of the full blocks; the leading run found in the cache
+  std::vector<uint64_t> keys(nfull);
+  std::vector<int32_t> matched;
+  int64_t revive = 0;  // matched blocks now evictable: they stop being available
+  uint64_t parent = 0;
+  bool matching = true;
+  for (int32_t i = 0; i < nfull; ++i) {
+    const int32_t* tk = tokens + static_cast<size_t>(i) * bs;
+    keys[i] = chain_key(parent, tk, bs);
+    if (matching) {
+      auto it = p->by_key.find(keys[i]);
+      const int32_t b = it == p->by_key.end() ? -1 : it->second;
+      if (b >= 0 && p->parent_key[b] == parent &&
+          std::memcmp(p->key_tokens[b].data(), tk, sizeof(int32_t) * bs) == 0) {
+        matched.push_back(b);
+        if (p->ref[b] == 0) revive += 1;
+      } else {
+        matching = false;
+      }
+    }
+    parent = keys[i];
+  }
+  const int64_t fresh = nblocks - static_cast<int64_t>(matched.size());
+  if (fresh > static_cast<int64_t>(p->available()) - revive)
+    return fail(PA_ERR_OOM, "pa_seq_create_prompt: pool exhausted");
+  // commit: map the matches, then allocate (and enter into the cache) the rest
+  pa_pool::Seq q;
+  q.live = true;
+  q.len = num_tokens;
+  for (int32_t b : matched) {
+    if (p->ref[b] == 0) {
+      p->evictable.erase(p->ev_pos[b]);
+      p->ref[b] = 1;
+    } else {
+      p->ref[b] += 1;
+    }
+    q.table.push_back(b);
+  }
+  for (int32_t i = static_cast<int32_t>(matched.size()); i < nblocks; ++i) {
+    const int32_t b = p->pop();
+    q.table.push_back(b);
+    if (i < nfull && p->by_key.find(keys[i]) == p->by_key.end()) {
+      p->cached[b] = 1;
+      p->key[b] = keys[i];
+      p->parent_key[b] = i > 0 ? keys[i - 1] : 0;
+      p->key_tokens[b].assign(tokens + static_cast<size_t>(i) * bs,
+                              tokens + static_cast<size_t>(i + 1) * bs);
+      p->by_key[keys[i]] = b;
+    }
+  }
+  p->lookups += nfull;
+  p->hits += static_cast<int64_t>(matched.size());
+  if (slots)
+    for (int32_t t = 0; t < num_tokens; ++t)
+      slots[t] = static_cast<int64_t>(q.table[t / bs]) * bs + t % bs;
+  *cached_tokens = static_cast<int32_t>(matched.size()) * bs;
+  p->seqs.push_back(std::move(q));
+  p->live_seqs += 1;
+  *seq = static_cast<int32_t>(p->seqs.size()) - 1;
+  return PA_OK;
+}
+
+pa_status pa_pool_prefix_stats(const pa_pool* p, pa_prefix_stats_t* st) {
+  if (!p || !st) return fail(PA_ERR_INVALID_ARG, "pa_pool_prefix_stats: NULL argument");
+  st->cached_blocks = static_cast<int32_t>(p->by_key.size());
+  st->evictable_blocks = static_cast<int32_t>(p->evictable.size());
+  st->lookups = p->lookups;
+  st->hits = p->hits;
   return PA_OK;
 }
 

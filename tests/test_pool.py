@@ -7,6 +7,7 @@ copy-on-write pairs, refcounts and stats must agree exactly on any sequence
 of operations. Also: the pages' allocator arithmetic and the shared-prefix
 workload's refcounts.
 """
+import copy
 import json
 import os
 
@@ -37,6 +38,7 @@ def _snapshot(pool, model, seqs):
     ms = model.stats()
     assert (st["free_blocks"], st["used_blocks"], st["shared_blocks"], st["max_refcount"]) == \
         (ms["free"], ms["used"], ms["shared"], ms["max_refcount"])
+    assert pool.prefix_stats() == model.prefix_stats()
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -47,10 +49,24 @@ def test_random_operation_sequences_match_model(pk, seed):
     pool = pk.Pool(NB, BS, free_order=order)
     model = oracle.PoolModel(NB, BS, free_order=order)
     live = []
+    # prompts share prefixes with a few base texts, so the prefix cache hits
+    bases = [rng.integers(0, 50, size=40) for _ in range(3)]
     for step in range(400):
-        op = rng.choice(["create", "append", "append_n", "fork", "free"],
-                        p=[0.1, 0.45, 0.15, 0.15, 0.15])
-        if op == "create" or not live:
+        op = rng.choice(["create", "prompt", "append", "append_n", "fork", "free"],
+                        p=[0.06, 0.1, 0.4, 0.14, 0.15, 0.15])
+        if op == "prompt":
+            base = bases[int(rng.integers(0, 3))]
+            toks = np.concatenate([base[:int(rng.integers(0, 41))],
+                                   rng.integers(0, 50, size=int(rng.integers(0, 11)))])
+            try:
+                want = model.create_prompt(toks)
+            except oracle.PoolOOM:
+                with pytest.raises(pk.PoolOOM):
+                    pool.create_prompt(toks)
+            else:
+                assert pool.create_prompt(toks) == want
+                live.append(want[0])
+        elif op == "create" or not live:
             a, b = pool.seq_create(), model.seq_create()
             assert a == b
             live.append(a)
@@ -66,13 +82,12 @@ def test_random_operation_sequences_match_model(pk, seed):
         elif op == "append_n":
             s = int(rng.choice(live))
             n = int(rng.integers(0, 9))
-            before = (list(model.free), list(model.ref), model.table(s), model.length(s))
+            before = copy.deepcopy(model.__dict__)
             try:
                 want = model.append_tokens(s, n)
             except oracle.PoolOOM:
                 # the model stopped part-way; the C pool is all-or-nothing
-                model.free, model.ref = before[0], before[1]
-                model.tables[s], model.lens[s] = before[2], before[3]
+                model.__dict__.update(before)
                 with pytest.raises(pk.PoolOOM):
                     pool.append_tokens(s, n)
             else:
@@ -176,3 +191,55 @@ def test_shared_prefix_workload_refcounts(pk):
     assert all(src == shared[63] for src, _ in cows_pool)
     assert pool.refcount(shared[63]) == 480
     assert all(pool.refcount(x) == 512 for x in shared[:63])
+
+
+def test_prefix_cache_worked_trace(pk, golden_dir):
+    """The pages' end-to-end trace: a 1,200-token prompt whose first 900 tokens
+    are a preamble already seen maps 56 cached blocks (896 tokens, the block
+    granularity) and takes 19 fresh ones, 75 in all; the preamble stays warm
+    after the first request ends."""
+    share = json.load(open(os.path.join(golden_dir, "allocator_arithmetic.json")))["prefix_share"]
+    rng = np.random.default_rng(3)
+    preamble = rng.integers(0, 32000, size=900)
+    first = np.concatenate([preamble, rng.integers(0, 32000, size=300)])
+    second = np.concatenate([preamble, rng.integers(0, 32000, size=300)])
+    for P in (pk.Pool(300, 16), oracle.PoolModel(300, 16)):
+        a, cached_a, _ = P.create_prompt(first)
+        assert cached_a == 0
+        P.seq_free(a)  # the request completes; its blocks stay cached
+        used0 = P.stats()["used"] if isinstance(P, oracle.PoolModel) else P.stats()["used_blocks"]
+        b, cached_b, slots = P.create_prompt(second)
+        assert cached_b == share["shared_blocks"] * 16 == 896
+        assert len(P.table(b)) == share["prompt_tokens"] // 16 == 75
+        used1 = P.stats()["used"] if isinstance(P, oracle.PoolModel) else P.stats()["used_blocks"]
+        assert used1 - used0 == 75 and len(slots) == 1200
+        st = P.prefix_stats()
+        assert st["hits"] == 56 and st["lookups"] == 150
+
+
+def test_prefix_cache_eviction_order_and_immutability(pk):
+    """Never-cached free blocks go first, then the least recently freed cached
+    block (which leaves the cache); an append into a cached block copies it
+    even when no one else holds it."""
+    for P in (pk.Pool(6, 4), oracle.PoolModel(6, 4)):
+        s1, _, _ = P.create_prompt([1, 2, 3, 4, 5, 6, 7, 8])   # 2 cached blocks
+        s2, _, _ = P.create_prompt([9, 9, 9, 9])               # 1 cached block
+        t1, t2 = P.table(s1), P.table(s2)
+        P.seq_free(s1)
+        P.seq_free(s2)  # evictable, oldest first: t1[0], t1[1], t2[0]
+        assert P.prefix_stats()["evictable_blocks"] == 3
+        fresh = [P.alloc() for _ in range(3)]  # the never-cached blocks
+        assert not set(fresh) & set(t1 + t2)
+        assert P.alloc() == t1[0]               # then the oldest cached block
+        assert P.prefix_stats()["cached_blocks"] == 2
+        # a prompt matching the second cached prefix revives it (no allocation)
+        s3, cached, _ = P.create_prompt([9, 9, 9, 9, 1])
+        assert cached == 4 and P.table(s3)[0] == t2[0]
+        # fork a partial view of the cached block, drop the owner, append:
+        # the cached block is copied, not written
+        for b in fresh + [t1[0]]:
+            P.decref(b)
+        c = P.seq_fork(s3, 2)
+        P.seq_free(s3)
+        slot, cow = P.append_slot(c)
+        assert cow is not None and cow[0] == t2[0]
