@@ -72,6 +72,9 @@ def _load():
         lib.oracle_paged_decode_fp8.argtypes = [p, p, p, p, p, p, i32, p, i32, i32, i32, i32,
                                                 i32, i32, ctypes.c_double, p, i64, p, p]
         lib.oracle_paged_decode_fp8.restype = ctypes.c_int
+        lib.oracle_paged_decode_multi.argtypes = [p, p, p, p, i32, p, i32, i32, i32, i32, i32,
+                                                  i32, i32, ctypes.c_double, p]
+        lib.oracle_paged_decode_multi.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -143,6 +146,30 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: Optiona
         raise ValueError(f"oracle_paged_decode failed with code {rc}")
     if return_lse:
         return out, (lse.reshape(B, Hq) if units is None else lse)
+    return out
+
+
+def paged_decode_multi(q, k_cache, v_cache, block_tables, context_lens,
+                       scale: Optional[float] = None) -> np.ndarray:
+    """Decode of several new tokens per sequence, causal among them (C oracle).
+    q [B][query_len][Hq][d] bf16; the last query_len of each sequence's
+    context_lens[b] tokens are the queries. Returns float64 [B][query_len][Hq][d]."""
+    lib = _load()
+    qb = bf16_bits(q)
+    kc, vc = bf16_bits(k_cache), bf16_bits(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, QL, Hq, D = qb.shape
+    NB, Hkv, BS, D2 = kc.shape
+    if D2 != D or vc.shape != kc.shape:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.empty((B, QL, Hq, D), dtype=np.float64)
+    rc = lib.oracle_paged_decode_multi(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                       _ptr(cl), B, QL, Hq, Hkv, D, BS, NB, float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_decode_multi failed with code {rc}")
     return out
 
 

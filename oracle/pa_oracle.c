@@ -139,15 +139,16 @@ static void kv_element(const void* k_cache, const void* v_cache, int fp8, const 
        (double)v_scale[g];
 }
 
-static int decode_one(const uint16_t* q, const void* k_cache, const void* v_cache, int fp8,
-                      const float* k_scale, const float* v_scale,
+/* qrow: this query's head_dim bf16 values; L: the number of cached tokens it
+ * attends to (the first L of sequence b). */
+static int decode_one(const uint16_t* qrow, int32_t L, const void* k_cache, const void* v_cache,
+                      int fp8, const float* k_scale, const float* v_scale,
                       const int32_t* block_tables, int32_t max_blocks_per_seq,
-                      const int32_t* context_lens, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t num_q_heads, int32_t num_kv_heads,
                       int32_t head_dim, int32_t block_size, int32_t num_blocks, double scale,
                       int32_t b, int32_t h, double* out_row, double* lse_out) {
   const int32_t group = num_q_heads / num_kv_heads;
   const int32_t g = h / group;
-  const int32_t L = context_lens[b];
   if (L < 1) return ORACLE_BAD_ARG;
   if ((L + block_size - 1) / block_size > max_blocks_per_seq) return ORACLE_OUT_OF_RANGE;
 
@@ -173,7 +174,6 @@ static int decode_one(const uint16_t* q, const void* k_cache, const void* v_cach
                  block_size, head_dim, &K[(size_t)t * head_dim + c], &V[(size_t)t * head_dim + c]);
   }
   if (rc == ORACLE_OK) {
-    const uint16_t* qrow = q + ((size_t)b * num_q_heads + h) * head_dim;
     /* 2. Scores. */
     for (int32_t t = 0; t < L; ++t) {
       double dot = 0.0;
@@ -239,10 +239,10 @@ static int paged_decode(const uint16_t* q, const void* k_cache, const void* v_ca
     }
     int r = ORACLE_BAD_ARG;
     if (b >= 0 && b < num_seqs && h >= 0 && h < num_q_heads)
-      r = decode_one(q, k_cache, v_cache, fp8, k_scale, v_scale, block_tables,
-                     max_blocks_per_seq, context_lens, num_q_heads, num_kv_heads, head_dim,
-                     block_size, num_blocks, scale, b, h, out + (size_t)u * head_dim,
-                     lse ? lse + u : NULL);
+      r = decode_one(q + ((size_t)b * num_q_heads + h) * head_dim, context_lens[b], k_cache,
+                     v_cache, fp8, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, b, h,
+                     out + (size_t)u * head_dim, lse ? lse + u : NULL);
     if (r != ORACLE_OK) {
 #pragma omp critical
       rc = r;
@@ -260,6 +260,42 @@ int oracle_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16
   return paged_decode(q, k_cache, v_cache, 0, NULL, NULL, block_tables, max_blocks_per_seq,
                       context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, scale, units, n_units, out, lse);
+}
+
+/*
+ * Decode of query_len new tokens per sequence (the last query_len of its
+ * context_lens[b] tokens), causal among themselves: query token i of sequence
+ * b attends to the first context_lens[b] - query_len + i + 1 cached tokens.
+ *   q, out  [num_seqs][query_len][num_q_heads][head_dim] (bf16 bits / double)
+ * Every (b, i, h) is computed; context_lens[b] < query_len is an error.
+ */
+int oracle_paged_decode_multi(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs, int32_t query_len,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int32_t num_blocks, double scale, double* out) {
+  if (num_seqs < 0 || query_len < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 ||
+      block_size < 1 || num_q_heads % num_kv_heads != 0)
+    return ORACLE_BAD_ARG;
+  const int64_t total = (int64_t)num_seqs * query_len * num_q_heads;
+  int rc = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t u = 0; u < total; ++u) {
+    const int32_t h = (int32_t)(u % num_q_heads);
+    const int32_t i = (int32_t)((u / num_q_heads) % query_len);
+    const int32_t b = (int32_t)(u / ((int64_t)num_q_heads * query_len));
+    const int32_t L = context_lens[b] - query_len + i + 1;
+    int r = ORACLE_BAD_ARG;
+    if (context_lens[b] >= query_len)
+      r = decode_one(q + (size_t)u * head_dim, L, k_cache, v_cache, 0, NULL, NULL, block_tables,
+                     max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, b, h, out + (size_t)u * head_dim, NULL);
+    if (r != ORACLE_OK) {
+#pragma omp critical
+      rc = r;
+    }
+  }
+  return rc;
 }
 
 /* The same decode over an E4M3 cache (k/v_cache uint8, layouts above) with

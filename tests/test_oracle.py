@@ -585,3 +585,66 @@ def test_fp8_copy_blocks_is_a_byte_copy():
     k2, v2 = oracle.copy_blocks_fp8(k8, v8, [[1, 4], [2, 0]])
     assert np.array_equal(k2[4], k8[1]) and np.array_equal(v2[0], v8[2])
     assert np.array_equal(k2[3], k8[3])
+
+
+# ---------------------------------------------------------------- several new tokens per sequence
+
+def _multi_case(seed, lens, QL, Hq=4, Hkv=2, D=8, BS=4):
+    q1, kc, vc, tables, lens = _random_case(seed, B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS,
+                                            lens=lens)
+    q = _bf16((len(lens), QL, Hq, D), seed + 7)
+    return q, kc, vc, tables, lens
+
+
+def test_multi_query_equals_library_sdpa_with_explicit_causal_mask():
+    """Identity tables, so the cache is contiguous: query i of a sequence of L
+    tokens attends to keys 0 .. L - QL + i (the new tokens are the last QL),
+    written as a boolean mask handed to torch SDPA in float64."""
+    B, QL, Hq, Hkv, D, BS = 2, 5, 8, 2, 16, 4
+    lens = np.array([13, 5], dtype=np.int32)
+    mb = 4
+    tables = np.arange(B * mb, dtype=np.int32).reshape(B, mb)
+    q = _bf16((B, QL, Hq, D), 31)
+    kc = _bf16((B * mb, Hkv, BS, D), 32)
+    vc = _bf16((B * mb, Hkv, BS, D), 33)
+    got = oracle.paged_decode_multi(q, kc, vc, tables, lens)
+    G = Hq // Hkv
+    for b in range(B):
+        L = int(lens[b])
+        K = kc[b * mb:(b + 1) * mb].double().permute(1, 0, 2, 3).reshape(Hkv, mb * BS, D)[:, :L]
+        V = vc[b * mb:(b + 1) * mb].double().permute(1, 0, 2, 3).reshape(Hkv, mb * BS, D)[:, :L]
+        allowed = torch.arange(L)[None, :] <= (L - QL + torch.arange(QL))[:, None]  # [QL, L]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[b].double().permute(1, 0, 2),  # [Hq, QL, D]
+            K.repeat_interleave(G, dim=0), V.repeat_interleave(G, dim=0), attn_mask=allowed)
+        np.testing.assert_allclose(got[b], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("QL", [1, 2, 7])
+def test_multi_query_rows_equal_single_token_decodes_at_their_lengths(QL):
+    """Row i of a sequence of L tokens is the single-token decode of a sequence
+    of L - QL + i + 1 tokens over the same table; with QL = 1 the two calls
+    coincide."""
+    lens = (7, 9, 16, 30)
+    q, kc, vc, tables, lens = _multi_case(41 + QL, lens, QL)
+    got = oracle.paged_decode_multi(q, kc, vc, tables, lens)
+    for i in range(QL):
+        want = oracle.paged_decode(q[:, i], kc, vc, tables, lens - QL + i + 1)
+        np.testing.assert_array_equal(got[:, i], want)
+
+
+def test_multi_query_brute_force_and_bad_lengths():
+    q, kc, vc, tables, lens = _multi_case(50, (3, 6), QL=3, Hq=2, Hkv=1, D=4, BS=2)
+    got = oracle.paged_decode_multi(q, kc, vc, tables, lens)
+    qd, kd, vd = (oracle.bf16_to_f64(x) for x in (q, kc, vc))
+    for b in range(2):
+        L = int(lens[b])
+        K = [list(kd[tables[b][t // 2], 0, t % 2]) for t in range(L)]
+        V = [list(vd[tables[b][t // 2], 0, t % 2]) for t in range(L)]
+        for i in range(3):
+            n = L - 3 + i + 1
+            ref = oracle.brute_force_decode([list(qd[b, i, h]) for h in range(2)], K[:n], V[:n],
+                                            0.5)
+            np.testing.assert_allclose(got[b, i], np.array(ref), rtol=0, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.paged_decode_multi(q, kc, vc, tables, np.array([2, 6], dtype=np.int32))
