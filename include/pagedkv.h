@@ -85,8 +85,9 @@ typedef enum {
 #define PA_DEVERR_SLOT 0x4u          /* slot_mapping entry >= num_blocks*block_size */
 #define PA_DEVERR_COPY_PAIR 0x8u     /* copy_blocks pair outside [0, num_blocks) */
 #define PA_DEVERR_TIMEOUT 0x10u      /* an mbarrier wait hit its iteration limit */
-#define PA_DEVERR_APPEND_SLOT 0x20u  /* pa_append_decode: slot_mapping[b] is not the slot of
-                                        token context_lens[b]-1 of sequence b (not written) */
+#define PA_DEVERR_APPEND_SLOT 0x20u  /* pa_append_decode: a slot_mapping entry is not the slot
+                                        of its token (context_lens[b]-1 for one new token per
+                                        sequence); that token is not written */
 
 const char* pa_status_string(pa_status s);
 const char* pa_last_error(void);
@@ -141,6 +142,18 @@ typedef struct {
   const float* k_scale;        /* PA_KV_FP8_E4M3 only: device float [num_kv_heads], the
                                   dequantisation scale of each KV head's K (value = code * scale) */
   const float* v_scale;        /* the same for V */
+  int32_t query_len;           /* new tokens per sequence: 0 or 1 = one (the layouts above).
+                                  Q > 1 ("How Paged Attention and Continuous Batching Actually
+                                  Work", §Continuous batching: several scheduled tokens of one
+                                  request, as in a chunked prefill): q and out are
+                                  [num_seqs][Q][num_q_heads][head_dim], the new tokens are the
+                                  last Q of each sequence's context_lens[b] (already in the cache),
+                                  and query token i attends to the first context_lens[b] - Q + i + 1
+                                  of them (causal among the new tokens). Tensor-core kernel only,
+                                  with G * Qp <= 16 (Qp = Q rounded up to a power of two) and
+                                  num_kv_heads * G * Qp <= 128 (<= 64 for the 8-bit cache); other
+                                  shapes return PA_ERR_UNSUPPORTED. A sequence with
+                                  0 < context_lens[b] < Q gets zero rows and PA_DEVERR_CONTEXT_LEN. */
 } pa_decode_params;
 
 /* Decode kernel variants; both compute the same function. The tensor-core
@@ -235,15 +248,20 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cac
  *    nothing (padding); sequences of length 0 write nothing.
  *  - the written block must not be read by another sequence of the batch,
  *    which copy-on-write guarantees (a shared block is copied before a write).
+ *  - with query_len Q > 1 every sequence brings Q new tokens (rows b*Q + i of
+ *    k_new/v_new/slot_mapping, token L-Q+i); each is written by the part of
+ *    the decode that reads its block, with the same slot rule.
  * a->k_cache / a->v_cache must equal p->k_cache / p->v_cache (the caches are
  * written through these). Same workspace as pa_decode. The CUDA-core variant
  * and shapes the tensor-core kernel does not cover run the KV-write kernel
  * and then the decode, with the same result.
  * ---------------------------------------------------------------------- */
 typedef struct {
-  const void* k_new;            /* bf16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned */
+  const void* k_new;            /* bf16 [num_seqs * Q][num_kv_heads][head_dim], 16-byte aligned
+                                   (Q = the decode's query_len, at least 1); row b * Q + i is
+                                   token context_lens[b] - Q + i of sequence b */
   const void* v_new;            /* same */
-  const int64_t* slot_mapping;  /* int64 [num_seqs] */
+  const int64_t* slot_mapping;  /* int64 [num_seqs * Q], the slots of those tokens */
   void* k_cache;                /* == p->k_cache, written */
   void* v_cache;                /* == p->v_cache, written */
 } pa_append_params;

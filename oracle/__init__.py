@@ -75,6 +75,9 @@ def _load():
         lib.oracle_paged_decode_multi.argtypes = [p, p, p, p, i32, p, i32, i32, i32, i32, i32,
                                                   i32, i32, ctypes.c_double, p]
         lib.oracle_paged_decode_multi.restype = ctypes.c_int
+        lib.oracle_paged_decode_multi_fp8.argtypes = [p, p, p, p, p, p, i32, p, i32, i32, i32,
+                                                      i32, i32, i32, i32, ctypes.c_double, p]
+        lib.oracle_paged_decode_multi_fp8.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -347,6 +350,32 @@ def paged_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, contex
                                      None if u is None else _ptr(u), n, _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_paged_decode_fp8 failed with code {rc}")
+    return out
+
+
+def paged_decode_multi_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                           scale: Optional[float] = None) -> np.ndarray:
+    """paged_decode_multi over an E4M3 cache (dequantised exactly, code value x
+    head scale). q [B][query_len][Hq][d] bf16; returns float64 of that shape."""
+    lib = _load()
+    qb = bf16_bits(q)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, QL, Hq, D = qb.shape
+    NB, Hkv, BS, D2 = kc.shape
+    if D2 != D or vc.size != kc.size:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.empty((B, QL, Hq, D), dtype=np.float64)
+    rc = lib.oracle_paged_decode_multi_fp8(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                           _ptr(bt), bt.shape[1], _ptr(cl), B, QL, Hq, Hkv, D, BS,
+                                           NB, float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_decode_multi_fp8 failed with code {rc}")
     return out
 
 

@@ -269,7 +269,8 @@ int oracle_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16
  *   q, out  [num_seqs][query_len][num_q_heads][head_dim] (bf16 bits / double)
  * Every (b, i, h) is computed; context_lens[b] < query_len is an error.
  */
-int oracle_paged_decode_multi(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+static int paged_decode_multi(const uint16_t* q, const void* k_cache, const void* v_cache, int fp8,
+                              const float* k_scale, const float* v_scale,
                               const int32_t* block_tables, int32_t max_blocks_per_seq,
                               const int32_t* context_lens, int32_t num_seqs, int32_t query_len,
                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -287,15 +288,39 @@ int oracle_paged_decode_multi(const uint16_t* q, const uint16_t* k_cache, const 
     const int32_t L = context_lens[b] - query_len + i + 1;
     int r = ORACLE_BAD_ARG;
     if (context_lens[b] >= query_len)
-      r = decode_one(q + (size_t)u * head_dim, L, k_cache, v_cache, 0, NULL, NULL, block_tables,
-                     max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
-                     num_blocks, scale, b, h, out + (size_t)u * head_dim, NULL);
+      r = decode_one(q + (size_t)u * head_dim, L, k_cache, v_cache, fp8, k_scale, v_scale,
+                     block_tables, max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, scale, b, h, out + (size_t)u * head_dim, NULL);
     if (r != ORACLE_OK) {
 #pragma omp critical
       rc = r;
     }
   }
   return rc;
+}
+
+int oracle_paged_decode_multi(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs, int32_t query_len,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int32_t num_blocks, double scale, double* out) {
+  return paged_decode_multi(q, k_cache, v_cache, 0, NULL, NULL, block_tables, max_blocks_per_seq,
+                            context_lens, num_seqs, query_len, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, scale, out);
+}
+
+/* The same over an E4M3 cache (layouts and scales as oracle_paged_decode_fp8 below). */
+int oracle_paged_decode_multi_fp8(const uint16_t* q, const uint8_t* k_cache,
+                                  const uint8_t* v_cache, const float* k_scale,
+                                  const float* v_scale, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t query_len, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t num_blocks, double scale, double* out) {
+  if (!k_scale || !v_scale) return ORACLE_BAD_ARG;
+  return paged_decode_multi(q, k_cache, v_cache, 1, k_scale, v_scale, block_tables,
+                            max_blocks_per_seq, context_lens, num_seqs, query_len, num_q_heads,
+                            num_kv_heads, head_dim, block_size, num_blocks, scale, out);
 }
 
 /* The same decode over an E4M3 cache (k/v_cache uint8, layouts above) with

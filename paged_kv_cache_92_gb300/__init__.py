@@ -69,6 +69,7 @@ class DecodeParams(ctypes.Structure):
         ("scale", ctypes.c_float), ("partition_tokens", ctypes.c_int32),
         ("variant", ctypes.c_int32), ("overlap_prologue", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("query_len", ctypes.c_int32),
     ]
 
 
@@ -210,16 +211,21 @@ def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
                        partition_tokens: int = 0, variant: int = DECODE_TENSOR_CORE,
                        overlap_prologue: bool = False, k_scale=None,
                        v_scale=None) -> DecodeParams:
-    """Marshal a pa_decode call. bf16 caches [NB][Hkv][BS][D]; uint8 caches are
-    the 8-bit E4M3 cache (K [NB][Hkv][BS][D], V^T [NB][Hkv][D][BS]) and need
-    k_scale / v_scale, float32 CUDA tensors [Hkv]."""
+    """Marshal a pa_decode call. q and out are bf16 [B][Hq][D] (one new token
+    per sequence) or [B][Q][Hq][D] (Q new tokens per sequence, causal among
+    them). bf16 caches [NB][Hkv][BS][D]; uint8 caches are the 8-bit E4M3 cache
+    (K [NB][Hkv][BS][D], V^T [NB][Hkv][D][BS]) and need k_scale / v_scale,
+    float32 CUDA tensors [Hkv]."""
     import torch
 
-    B, Hq, D = q.shape
+    if q.dim() == 4:
+        B, QL, Hq, D = q.shape
+    else:
+        (B, Hq, D), QL = q.shape, 0
     fp8 = k_cache.dtype == torch.uint8
     NB, Hkv, BS, D2 = k_cache.shape
     v_want = (NB, Hkv, D2, BS) if fp8 else tuple(k_cache.shape)
-    if D2 != D or tuple(v_cache.shape) != v_want or tuple(out.shape) != (B, Hq, D):
+    if D2 != D or tuple(v_cache.shape) != v_want or tuple(out.shape) != tuple(q.shape):
         raise ValueError("shape mismatch between q / out / k_cache / v_cache")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
@@ -245,6 +251,7 @@ def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
     p.partition_tokens = int(partition_tokens)
     p.variant = int(variant)
     p.overlap_prologue = int(bool(overlap_prologue))
+    p.query_len = int(QL)
     return p
 
 
@@ -256,7 +263,8 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
               scale: Optional[float] = None, partition_tokens: int = 0, out=None,
               workspace=None, stream=None, variant: int = DECODE_TENSOR_CORE,
               overlap_prologue: bool = False, k_scale=None, v_scale=None):
-    """Paged decode attention; returns ``out`` (bf16 [B][Hq][d]).
+    """Paged decode attention; returns ``out`` (bf16, the shape of ``q``:
+    [B][Hq][d], or [B][Q][Hq][d] for Q new tokens per sequence).
 
     ``workspace`` is a uint8 CUDA tensor of at least
     ``pa_decode_workspace_size`` bytes; allocated here when omitted.
@@ -281,11 +289,11 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
 def make_append_params(k_new, v_new, slot_mapping, k_cache, v_cache) -> AppendParams:
     import torch
 
-    B, Hkv, D = k_new.shape
-    if tuple(v_new.shape) != (B, Hkv, D) or tuple(slot_mapping.shape) != (B,) \
+    T, Hkv, D = k_new.shape  # T = num_seqs * (new tokens per sequence)
+    if tuple(v_new.shape) != (T, Hkv, D) or tuple(slot_mapping.shape) != (T,) \
             or tuple(k_cache.shape[1:2]) != (Hkv,) or k_cache.shape[3] != D:
-        raise ValueError("k_new/v_new must be [num_seqs][num_kv_heads][head_dim] matching the "
-                         "cache, slot_mapping [num_seqs]")
+        raise ValueError("k_new/v_new must be [num_seqs * Q][num_kv_heads][head_dim] matching "
+                         "the cache, slot_mapping [num_seqs * Q]")
     a = AppendParams()
     a.k_new = _dev_ptr(k_new, torch.bfloat16, "k_new")
     a.v_new = _dev_ptr(v_new, torch.bfloat16, "v_new")
@@ -303,7 +311,8 @@ def pa_append_decode(q, k_cache, v_cache, block_tables, context_lens, max_contex
     ``v_new[b]``) at ``slot_mapping[b]`` -- which must be the slot of token
     ``context_lens[b] - 1`` of sequence b -- then paged decode attention over
     the updated caches. Same result as ``pa_reshape_and_cache`` followed by
-    ``pa_decode``; returns ``out``."""
+    ``pa_decode``; returns ``out``. With q [B][Q][Hq][d], row b*Q + i of
+    ``k_new``/``v_new``/``slot_mapping`` is token ``context_lens[b] - Q + i``."""
     import torch
 
     lib = load()

@@ -59,6 +59,15 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: scale must be a positive finite number");
   if (p->kv_dtype != PA_KV_BF16 && p->kv_dtype != PA_KV_FP8_E4M3)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: kv_dtype must be PA_KV_BF16 or PA_KV_FP8_E4M3");
+  if (p->query_len < 0 || p->query_len > 1024)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: query_len must be in [0, 1024]");
+  if (int64_t(p->num_seqs) * query_len_of(p) * p->num_q_heads >= (int64_t(1) << 31) - 16)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: query rows exceed 2^31");
+  if (query_len_of(p) > 1 && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
+    return set_error(PA_ERR_UNSUPPORTED,
+                     "pa_decode: query_len > 1 runs on the tensor-core kernel with num_kv_heads "
+                     "1/2/4/8, G * query_len (rounded up to a power of two) <= 16 and "
+                     "num_kv_heads * that <= 128 (64 for the 8-bit cache)");
   if (p->kv_dtype == PA_KV_FP8_E4M3) {
     if (p->head_dim != 128 || p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p))
       return set_error(PA_ERR_UNSUPPORTED,
@@ -116,19 +125,23 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
     w.simt_acc = w.simt_l + round_up(rows * sizeof(float), 256);
     simt_end = w.simt_acc + round_up(rows * p->head_dim * sizeof(float), 256);
   }
-  // tensor-core kernel: stream-K plan, then one partial per (sequence, CTA) segment
+  // tensor-core kernel: stream-K plan, then one partial per (sequence, CTA)
+  // segment and query column (= query head for one token per sequence)
   const size_t segs = size_t(p->num_seqs) + size_t(grid > 0 ? grid : 256);
-  const size_t rows = segs * p->num_q_heads;
+  const size_t rows = segs * size_t(tc_cols(p));
   w.tc_plan = H;
   w.tc_m = w.tc_plan + round_up((size_t(p->num_seqs) + 2) * sizeof(int), 256);
   w.tc_l = w.tc_m + round_up(rows * sizeof(float), 256);
   w.tc_acc = w.tc_l + round_up(rows * sizeof(float), 256);
   size_t tc_end = w.tc_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+  const size_t n_pad = size_t(tc_n_pad(tc_cols(p)));
   if (p->kv_dtype == PA_KV_FP8_E4M3) {  // split queries [B][2N][D] bytes and [B][N] floats
-    const size_t n_pad = size_t(tc_n_pad(p->num_q_heads));
     w.tc_q8 = tc_end;
     w.tc_qa = w.tc_q8 + round_up(size_t(p->num_seqs) * 2 * n_pad * p->head_dim, 256);
     tc_end = w.tc_qa + round_up(size_t(p->num_seqs) * n_pad * sizeof(float), 256);
+  } else if (query_len_of(p) > 1) {  // queries in column order, bf16 [B][N][D]
+    w.tc_qp = tc_end;
+    tc_end = w.tc_qp + round_up(size_t(p->num_seqs) * n_pad * p->head_dim * 2, 256);
   }
   w.total = simt_end > tc_end ? simt_end : tc_end;
   return w;
@@ -151,12 +164,15 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
     L.q8 = p->kv_dtype == PA_KV_FP8_E4M3 ? ws + w.tc_q8 : nullptr;
     L.q_inv_alpha =
         p->kv_dtype == PA_KV_FP8_E4M3 ? reinterpret_cast<float*>(ws + w.tc_qa) : nullptr;
+    L.qp = p->kv_dtype == PA_KV_BF16 && query_len_of(p) > 1 ? ws + w.tc_qp : nullptr;
     L.part_m = reinterpret_cast<float*>(ws + w.tc_m);
     L.part_l = reinterpret_cast<float*>(ws + w.tc_l);
     L.part_acc = reinterpret_cast<float*>(ws + w.tc_acc);
     e = launch_decode_tc(L, stream);
   } else if (p->kv_dtype == PA_KV_FP8_E4M3) {
     return set_error(PA_ERR_UNSUPPORTED, "the 8-bit cache needs the tensor-core kernel");
+  } else if (query_len_of(p) > 1) {
+    return set_error(PA_ERR_UNSUPPORTED, "query_len > 1 needs the tensor-core kernel");
   } else {
     if (append) {  // the same effect in two launches
       AppendCheck chk;

@@ -1,0 +1,1319 @@
+// Paged decode attention on the 5th-generation tensor cores (sm_103a): the
+// kernels and their host-side launch templates. Each including translation
+// unit instantiates a share of the instances (pa_decode_tc.cu: bf16 head_dim
+// 128 and the shared entry points; pa_decode_tc_d64.cu: bf16 head_dim 64;
+// pa_decode_tc_fp8.cu: the 8-bit cache), so they compile in parallel. Each
+// has its own device error word.
+//
+// Same result as the CUDA-core kernel ("Paged Attention as a Memory
+// Manager", §How the Kernel Executes Paged Attention; "PagedAttention and
+// continuous batching", §Attention kernel modification): per (sequence,
+// query head), softmax(scale * q.K^T) V over the cached tokens, K/V gathered
+// block by block through the block table, a running softmax carried across
+// blocks, padding slots of the last block masked.
+//
+// Data movement. A chunk is one paged block with ALL its KV heads: in the
+// [block][kv head][16][d] cache that is 16*Hkv contiguous rows, so K and V
+// each arrive as two 128-byte-swizzled tensor-map TMA boxes of 16*Hkv rows
+// (16 KiB at Hkv = 8). For Hkv < 8 a chunk takes 8/Hkv blocks so that it
+// always has 128 rows: row = (block u, KV head h, key). Large boxes matter:
+// one issuing thread per SM keeps HBM busy with 16 KiB boxes, not with the
+// 2 KiB a (block, head) tile would give.
+//
+// Math. The chunk is the M=128 side of two tcgen05 MMAs whose N side is the
+// sequence's query columns (padded to 16, 32, 64 or 128):
+//   S^T[128 rows][N] = Kchunk . Q^T                 (fp32 in TMEM)
+//   O^T[d][N]       += V^Tchunk . P^T                (V read MN-major)
+// Columns are grouped by KV head: head g owns GE consecutive columns. With
+// one new token per sequence a column is a query head (GE = G, GQA: query
+// head n reads KV head n / G). With Q new tokens ("How Paged Attention and
+// Continuous Batching Actually Work", §Continuous batching: several scheduled
+// tokens of one request) column g*GE + i*G + j is query token i of head
+// g*G + j, GE = G * Q rounded up to a power of two, and it sees the keys up to
+// its own token (causal among the new tokens). Row r only uses the columns of
+// its own KV head, and P^T is block-diagonal (zero unless the column's head
+// is r's), so the second MMA sums each column over its own KV head's keys
+// only. The unused products are free: the tensor pipe runs at a few percent
+// here. Softmax runs on CUDA cores, one thread per row.
+//
+// Scheduling (stream-K). The blocks of all sequences form one stream; CTA c
+// takes the c-th contiguous 1/grid of it. A (sequence, CTA) segment that
+// holds a whole sequence writes the bf16 output directly; otherwise it writes
+// fp32 (max, sum, weighted sum) partials to slot (sequence + CTA), unique
+// along the stream, and the merge kernel combines them by log-sum-exp.
+//
+// Roles: warp 4 produces (TMA into a ring of ST chunk slots; block-table
+// windows and the next sequence's length prefetched into registers); warp 5
+// issues the MMAs; warps 0-3 run the softmax. S is triple-buffered in TMEM, so
+// the scores of chunks c+1 and c+2 and the value product of chunk c run on
+// the tensor core while the CUDA cores do chunk c's softmax. O^T accumulates
+// in TMEM relative to a per-column reference maximum that is raised (and O^T
+// rescaled in place) only when a score exceeds it by more than 2^8. Every
+// mbarrier wait is bounded; a wait that runs out sets PA_DEVERR_TIMEOUT and
+// the CTA winds down through its named barriers, drains, frees TMEM and exits.
+#pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__device__ unsigned int g_tc_errors;
+
+constexpr int BS = kBlockSize;
+constexpr int ROWS = 128;      // rows of a chunk = MMA M
+constexpr int NCONS = 4;       // softmax (consumer) warps 0-3
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int NTHREADS = 6 * 32;
+constexpr int kCons = NCONS * 32;
+constexpr int kGroups = ROWS / BS;  // 16-row groups per chunk: (block, KV head)
+constexpr int kMaxDynSmem = 232448;
+constexpr float kLog2e = 1.4426950408889634f;
+// The softmax reference maximum moves only when a score exceeds it by more
+// than this (log2 units, a factor of 256); values of P stay <= 256.
+constexpr float kRescaleLog2 = 8.0f;
+// Most query columns one KV head owns (G times the new tokens per sequence,
+// rounded up to a power of two).
+constexpr int kMaxGE = 16;
+
+enum : int { F_FIRST = 1, F_LAST = 2, F_WHOLE = 4, F_END = 8 };
+
+struct __align__(16) ChunkMeta {
+  int b;      // sequence
+  int seg;    // partial slot when the sequence spans several CTAs
+  int flags;
+  int tok0;   // first token of the chunk
+  int L;      // context length (clamped)
+  int nblk;   // blocks of the chunk holding cache data (the others read as zeros)
+  int qslot;
+  int pad;
+};
+
+// F8: the 8-bit (E4M3) cache. K rows are D bytes (one 128-byte atom at
+// D = 128); V^T comes as one [D][16 keys] tile per (block, KV head), side by
+// side; Q and P are each split into an E4M3 hi and lo term.
+template <int D, int N, bool F8 = false>
+struct TcCfg {
+  static constexpr int HALVES = F8 ? 1 : D / 64;   // 128-byte swizzle atoms per K row
+  static constexpr int HALF_BYTES = ROWS * 128;    // [128 rows][64 bf16] or [128 rows][128 e4m3]
+  static constexpr int K_BYTES = HALVES * HALF_BYTES;
+  static constexpr int VT_TILE = D * BS;           // F8: one [D][16] V^T tile, bytes
+  static constexpr int V_BYTES = F8 ? kGroups * VT_TILE : K_BYTES;
+  static constexpr int SLOT_BYTES = K_BYTES + V_BYTES;  // K then V
+  static constexpr int QH_BYTES = N * 128;         // [N rows][64 bf16] or [N rows][128 e4m3]
+  static constexpr int Q_BYTES = F8 ? 2 * QH_BYTES : HALVES * QH_BYTES;  // F8: hi, lo
+  static constexpr int PH_BYTES = N * 128;         // P^T [N rows][64 keys] or [N rows][128 keys]
+  static constexpr int P_BYTES = 2 * PH_BYTES;     // bf16: 128 keys; F8: hi and lo
+  // P buffers. One: a second buffer would let the softmax write P(c) while
+  // the value product of c-1 still reads P, but it costs a ring slot, and on
+  // GB300 neither cache type ran faster with it (the softmax spends ~180
+  // cycles of its ~1400-2400 per chunk waiting for that product).
+  static constexpr int PB = 1;
+  static constexpr int MISC_BYTES = 4096;
+  // Q buffers: two let the next segment's queries load while the current
+  // segment runs; at N = 128 only one fits beside a two-slot ring.
+  static constexpr int QB =
+      (kMaxDynSmem - 1024 - 2 * Q_BYTES - PB * P_BYTES - MISC_BYTES) / SLOT_BYTES >= 2 ? 2 : 1;
+  static constexpr int ST_FIT =
+      (kMaxDynSmem - 1024 - QB * Q_BYTES - PB * P_BYTES - MISC_BYTES) / SLOT_BYTES;
+  static constexpr int ST_CAP = F8 ? 6 : 4;
+  static constexpr int ST = ST_FIT > ST_CAP ? ST_CAP : ST_FIT;
+  static_assert(!F8 || D == 128, "the 8-bit cache is built for head_dim 128");
+  static_assert(ST >= 2, "at least a double-buffered ring");
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_Q = ST * SLOT_BYTES;
+  static constexpr int OFF_P = OFF_Q + QB * Q_BYTES;
+  static constexpr int OFF_MISC = OFF_P + PB * P_BYTES;
+  // full[ST] empty[ST] qempty[2] s[3] o[2] p[2] drain
+  static constexpr int NBARS = 2 * ST + 10;
+  static constexpr int OFF_BARS = OFF_MISC;
+  static constexpr int OFF_META = OFF_BARS + (NBARS * 8 + 15) / 16 * 16;
+  static constexpr int OFF_RED = OFF_META + ST * int(sizeof(ChunkMeta));  // [8 groups][kMaxGE]
+  static constexpr int OFF_RED2 = OFF_RED + kGroups * kMaxGE * 4;            // [8 groups][kMaxGE]
+  static constexpr int OFF_ALPHA = OFF_RED2 + kGroups * kMaxGE * 4;          // [128] by column
+  static constexpr int OFF_LS = OFF_ALPHA + 128 * 4;                         // [128]
+  static constexpr int OFF_MS = OFF_LS + 128 * 4;                            // [128]
+  static constexpr int OFF_WORDS = OFF_MS + 128 * 4;
+  static constexpr int OFF_QALPHA = OFF_WORDS + 64;       // F8: [2 q slots][64] 1/alpha
+  static constexpr int OFF_KVSCALE = OFF_QALPHA + 2 * 64 * 4;  // F8: k_scale[8], v_scale[8]
+  static constexpr int OFF_COLROW = OFF_KVSCALE + 64;  // [128] output row of each column
+  static constexpr int SMEM = OFF_COLROW + 128 * 4 + 1024;  // + alignment slack
+  static_assert(OFF_COLROW + 128 * 4 <= OFF_MISC + MISC_BYTES, "misc area");
+  static_assert(N <= 128 && (!F8 || N <= 64), "columns");
+  static_assert(SMEM <= kMaxDynSmem, "shared memory budget");
+  // MMA width: the query heads, twice over for the 8-bit cache (the hi and lo
+  // terms of Q and of P side by side, one MMA for both)
+  static constexpr int NS = F8 ? 2 * N : N;
+  static constexpr int TMEM_COLS = 4 * NS;  // S triple buffer [0, 3NS), O at [3NS, 4NS)
+  static constexpr int kSBufs = 3;
+  static constexpr uint32_t IDESC_S =
+      F8 ? dev::idesc_e4m3_f32(ROWS, NS) : dev::idesc_bf16_f32(ROWS, N, false, false);
+  static constexpr uint32_t IDESC_PV =
+      F8 ? dev::idesc_e4m3_f32(ROWS, NS) : dev::idesc_bf16_f32(ROWS, N, true, false);
+  static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
+  static constexpr uint32_t Q_TX = Q_BYTES + (F8 ? N * 4 : 0);  // F8: + 1/alpha per column
+};
+
+struct TcParams {
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  __nv_bfloat16* out;
+  float* part_m;    // [segments][Hq]
+  float* part_l;    // [segments][Hq]
+  float* part_acc;  // [segments][Hq][D]
+  int* ws_plan;     // [0] = blocks per CTA, [1 .. B+1] = block prefix of the sequences
+  // fused KV append (null k_new: none): token b goes to slot_mapping[b]
+  const uint4* k_new;
+  const uint4* v_new;
+  const int64_t* slot_mapping;
+  uint4* k_cache_w;
+  uint4* v_cache_w;
+  // 8-bit cache: per-KV-head dequantisation scales, and per (sequence, query
+  // head) 1/alpha of the split queries ([B][N] floats)
+  const float* k_scale;
+  const float* v_scale;
+  const float* q_inv_alpha;
+  int max_blocks_per_seq, num_seqs, num_kv_heads, num_q_heads, num_blocks, cap, oob_row;
+  int oob_row_v;   // 8-bit cache: first row past the V^T tensor map
+  int q_rows;      // rows of one sequence's queries in the Q tensor map
+  // Column layout: KV head g owns columns [g*GE, (g+1)*GE); column g*GE + r is
+  // query token r >> g_log2 of query head g*G + (r & (G-1)), unused when that
+  // token index is >= q_len. num_cols = num_kv_heads * GE.
+  int num_cols, q_len, g_log2;
+  float scale_log2;
+};
+
+// Context length of sequence b as the kernel uses it: clamped to the table
+// capacity, and 0 (an empty sequence) when it cannot hold the new tokens.
+__device__ __forceinline__ int seq_len(const TcParams& P, int b) {
+  const int L = min(P.context_lens[b], P.cap);
+  return L >= P.q_len ? L : 0;
+}
+
+// Output row of column n within its sequence's [q_len][Hq] rows, or -1 if the
+// column is unused (with one token per sequence: n itself, for n < Hq).
+__device__ __forceinline__ int column_row(const TcParams& P, int n, int ge) {
+  const int g = n / ge, r = n - g * ge;
+  const int i = r >> P.g_log2;
+  if (n >= P.num_cols || i >= P.q_len) return -1;
+  return i * P.num_q_heads + (g << P.g_log2) + (r & ((1 << P.g_log2) - 1));
+}
+
+// Byte offset of P^T[n][key] in the K-major, 128B-swizzled B-operand layout
+// (two 64-key atoms of [N rows][128 B]).
+template <int N>
+__device__ __forceinline__ uint32_t p_offset(int n, int key) {
+  const int half = key >> 6, kin = key & 63;
+  const int r = n & 7, grp = n >> 3;
+  return uint32_t(half * (N * 128) + grp * 1024 + r * 128 + (((kin >> 3) ^ r) << 4) +
+                  (kin & 7) * 2);
+}
+
+// Byte offset of the E4M3 P^T[n][key] in the K-major, 128B-swizzled B-operand
+// layout [N rows][128 keys] (one atom per row).
+__device__ __forceinline__ uint32_t p8_offset(int n, int key) {
+  const int r = n & 7, grp = n >> 3;
+  return uint32_t(grp * 1024 + r * 128 + (((key >> 4) ^ r) << 4) + (key & 15));
+}
+
+// S^T = Kchunk . Q^T for one chunk (single thread). bf16: D/16 MMAs of K = 16.
+// E4M3: D/32 MMAs of K = 32, each over both query terms at once.
+template <int D, int N, bool F8>
+__device__ __forceinline__ void issue_scores(uint32_t tmem_col, const unsigned char* kv,
+                                             const unsigned char* q) {
+  using C = TcCfg<D, N, F8>;
+  const uint32_t kb = dev::smem_addr(kv);
+  const uint32_t qb = dev::smem_addr(q);
+  if constexpr (F8) {
+    // B = the 2N query rows (hi terms, then lo terms): score columns [0, N)
+    // from hi, [N, 2N) from lo, added by the softmax
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk)
+      dev::mma_e4m3(tmem_col, dev::smem_desc(kb + kk * 32, 16, 1024, dev::kSwizzle128B),
+                    dev::smem_desc(qb + kk * 32, 16, 1024, dev::kSwizzle128B), C::IDESC_S, kk > 0);
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t hf = kk >> 2, off = uint32_t(kk & 3) * 32;
+      dev::mma_bf16(tmem_col,
+                    dev::smem_desc(kb + hf * C::HALF_BYTES + off, 16, 1024, dev::kSwizzle128B),
+                    dev::smem_desc(qb + hf * C::QH_BYTES + off, 16, 1024, dev::kSwizzle128B),
+                    C::IDESC_S, kk > 0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA warp (one thread): per chunk, S^T = K.Q^T into S[chunk & 1] as soon as
+// the chunk has landed, and O^T = V^T.P^T once the softmax warps have written
+// P for it. Scores run one chunk ahead of the value product.
+// ---------------------------------------------------------------------------
+template <int D, int N, bool F8>
+__device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbuf,
+                                         unsigned char* pbuf, uint64_t* full, uint64_t* empty,
+                                         uint64_t* qempty, uint64_t* bar_s, uint64_t* bar_o,
+                                         uint64_t* bar_p, uint64_t* drain, const ChunkMeta* meta,
+                                         uint32_t tmem, volatile int* abort_flag) {
+  using C = TcCfg<D, N, F8>;
+  // D = 64: the second 64-row half of M re-reads the first (LBO 0); those
+  // TMEM lanes are never read back.
+  const uint32_t lbo = C::HALVES == 2 ? uint32_t(C::HALF_BYTES) : 0u;
+  const uint32_t pbs = dev::smem_addr(pbuf);
+  // Event loop: issue whichever is ready first -- the scores of the next
+  // ring position once its data has landed (at most one position ahead of
+  // the value products), or the value product of position c once the softmax
+  // warps have written its P. Every ring position before the end sentinel
+  // is a real chunk, so position = chunk index.
+  int c = 0;           // position whose value product is next
+  int s_pos = 0;       // next position to issue scores for
+  int end_pos = -1;    // position of the end sentinel, once seen
+  bool ok = true;
+  uint64_t t_progress = dev::global_timer_ns();
+  for (;;) {
+    bool progress = false;
+    // value product first: it frees a ring slot for the producer
+    if (c < s_pos && c != end_pos &&
+        dev::mbar_test(&bar_p[c % C::PB], uint32_t(c / C::PB) & 1u)) {
+      const uint32_t pbc = pbs + uint32_t(c % C::PB) * C::P_BYTES;  // this chunk's P
+      const int sl = c % C::ST;
+      // O accumulates over a segment's chunks; its first chunk starts afresh
+      const bool fresh = (meta[sl].flags & F_FIRST) != 0;
+      dev::tc_fence_after();
+      const uint32_t vb = dev::smem_addr(ring + size_t(sl) * C::SLOT_BYTES + C::K_BYTES);
+      if constexpr (F8) {
+        // V^T K-major without swizzle: 8-row x 16-byte core matrices, the
+        // next 8 rows of d 128 B on (SBO), the next 16 keys one [D][16]
+        // tile on (LBO); 32 keys per MMA. B = the 2N rows of P (hi terms,
+        // then lo terms): O columns [0, N) from hi, [N, 2N) from lo.
+#pragma unroll
+        for (int kk = 0; kk < ROWS / 32; ++kk)
+          dev::mma_e4m3(tmem + C::kSBufs * C::NS,
+                        dev::smem_desc(vb + kk * 2 * C::VT_TILE, C::VT_TILE, 128,
+                                       dev::kSwizzleNone),
+                        dev::smem_desc(pbc + kk * 32, 16, 1024, dev::kSwizzle128B), C::IDESC_PV,
+                        kk > 0 || !fresh);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < ROWS / 16; ++kk) {
+          dev::mma_bf16(tmem + C::kSBufs * C::NS,
+                        dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
+                        dev::smem_desc(pbc + (kk >> 2) * C::PH_BYTES + (kk & 3) * 32, 16, 1024,
+                                       dev::kSwizzle128B),
+                        C::IDESC_PV, kk > 0 || !fresh);
+        }
+      }
+      dev::mma_commit(&bar_o[c % C::PB]);
+      dev::mma_commit(&empty[sl]);
+      ++c;
+      progress = true;
+    }
+    // scores of the next positions as soon as their data has landed, up to
+    // two positions ahead of the value products (S is triple-buffered)
+    if (end_pos < 0 && s_pos <= c + 2 &&
+        dev::mbar_test(&full[s_pos % C::ST], uint32_t(s_pos / C::ST) & 1u)) {
+      const int sl = s_pos % C::ST;
+      const ChunkMeta mn = meta[sl];
+      if (mn.flags & F_END) {
+        end_pos = s_pos;
+      } else {
+        const int sb = s_pos % C::kSBufs;
+        dev::tc_fence_after();
+        issue_scores<D, N, F8>(tmem + sb * C::NS, ring + size_t(sl) * C::SLOT_BYTES,
+                               qbuf + mn.qslot * C::Q_BYTES);
+        dev::mma_commit(&bar_s[sb]);
+        if (mn.flags & F_LAST) dev::mma_commit(&qempty[mn.qslot]);
+      }
+      ++s_pos;
+      progress = true;
+    }
+    if (c == end_pos) break;
+    if (progress) {
+      t_progress = dev::global_timer_ns();
+      continue;
+    }
+    if (*abort_flag) break;
+    if (dev::global_timer_ns() - t_progress > dev::kWaitNsLimit) {
+      ok = false;
+      break;
+    }
+    __nanosleep(20);
+  }
+  if (!ok) {
+    atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  }
+  // every MMA this thread issued completes before TMEM can be released
+  dev::mma_commit(drain);
+  (void)dev::mbar_wait(drain, 0);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax warps 0-3: thread = row of the chunk (scores), = head dimension
+// (output). Chunk r: read S, running max (half-warp + shared-memory exchange
+// across the chunk's groups of the same KV head), fold chunk r-1's O^T into
+// the accumulators, write P and signal the MMA warp.
+// ---------------------------------------------------------------------------
+template <int D, int GE, int N, bool F8>
+struct Softmax {
+  using C = TcCfg<D, N, F8>;
+  static constexpr int LDC = 2 * GE <= 8 ? 8 : 2 * GE;  // score columns a warp reads (two heads)
+  // O^T columns per TMEM round trip (the 8-bit epilogue holds a second,
+  // lo-term block beside them)
+  static constexpr int CW = N <= (F8 ? 32 : 64) ? N : 32;
+
+  __device__ __forceinline__ static void run(const TcParams& P, unsigned char* ring,
+                                             unsigned char* pbuf, uint64_t* full,
+                                             uint64_t* bar_s, uint64_t* bar_o, uint64_t* bar_p,
+                                             const ChunkMeta* meta, float* red, float* red2,
+                                             float* alpha_s, float* l_s, float* m_s,
+                                             const float* qalpha, const float* kvscale,
+                                             const int* colrow, uint32_t tmem,
+                                             volatile int* abort_flag, int* consumed_out) {
+    const int ctid = threadIdx.x;
+    const int cw = ctid >> 5, lane = ctid & 31;
+    const int H = P.num_kv_heads;
+    const int NC = P.num_cols;
+    const int U = kGroups / H;
+    const int grp = ctid >> 4;  // (block u, KV head h) group of this row
+    const int u = grp / H, h = grp - (grp / H) * H;
+    const int key = ctid & 15;
+    const int h0 = (2 * cw) % H;  // the warp's first head
+    const int col0 = H >= 2 ? h0 * GE : 0;
+    const bool upper = H >= 2 && lane >= 16;  // this lane's head is the warp's second
+    const uint32_t t_lane = uint32_t(cw * 32) << 16;
+    const uint32_t tO = tmem + t_lane + C::kSBufs * C::NS;  // F8: + N for the lo terms
+
+    // Reference maximum per query column (log2 domain) and this row's share of
+    // the softmax sum relative to it. O^T accumulates in TMEM relative to the
+    // same reference; the reference is raised (and O^T, l rescaled) only when
+    // a score exceeds it by more than kRescaleLog2, and only then is the
+    // chunk's maximum over its keys taken.
+    float m_ref[GE], l_part[GE];
+#pragma unroll
+    for (int j = 0; j < GE; ++j) {
+      m_ref[j] = -INFINITY;
+      l_part[j] = 0.0f;
+    }
+    int c = 0;  // ring position = chunk index
+    bool ok = true;
+    int pv_done = -1;  // highest chunk whose value product is known to be complete
+    // wait for chunk k's value product (k > pv_done)
+    auto wait_pv = [&](int k) {
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[k % C::PB], uint32_t(k / C::PB) & 1u)) &&
+           ok;
+      pv_done = k;
+    };
+
+    for (;;) {
+      const int slot = c % C::ST;
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&full[slot], uint32_t(c / C::ST) & 1u)) && ok;
+      const ChunkMeta m = meta[slot];
+      // every exit below is taken by all 128 threads together (named barriers follow)
+      if (!dev::named_barrier_and(1, kCons, ok && *abort_flag == 0)) {
+        ok = false;
+        break;
+      }
+      if (m.flags & F_END) break;
+      const int buf = c % C::kSBufs;
+      const bool first = (m.flags & F_FIRST) != 0;
+
+      // ---- scores of this chunk -> registers
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(c / C::kSBufs) & 1u)) && ok;
+      dev::tc_fence_after();
+      float s[LDC];
+      const uint32_t tS = tmem + t_lane + buf * C::NS + col0;
+      if constexpr (LDC == 8) {
+        dev::tmem_ld8(tS, s);
+      } else {
+        dev::tmem_ld_cols<LDC>(tS, s);
+      }
+      if constexpr (F8) {  // + the scores of the lo query terms
+        float s2[LDC];
+        if constexpr (LDC == 8) {
+          dev::tmem_ld8(tS + N, s2);
+        } else {
+          dev::tmem_ld_cols<LDC>(tS + N, s2);
+        }
+#pragma unroll
+        for (int i = 0; i < LDC; ++i) s[i] += s2[i];
+      }
+
+      // ---- scaled scores; row = (block u, head h, key)
+      const int t = m.tok0 + u * BS + key;
+      const bool row_in = u < m.nblk;           // the row holds cache data
+      const bool valid = row_in && t < m.L;     // a token of the sequence
+      // Causal limit: column j holds query token i = j >> g_log2, the
+      // (q_len - i)-th last of the sequence, which sees the keys
+      // t < L - q_len + 1 + i; columns with i >= q_len are unused.
+      const int t_rel = t - (m.L - P.q_len + 1);
+      float x[GE];
+      bool need = false;
+#pragma unroll
+      for (int j = 0; j < GE; ++j) {
+        const float sj = upper ? s[GE + j] : s[j];
+        float f = P.scale_log2;
+        if constexpr (F8)  // the head's K scale and the query term's 1/alpha
+          f *= kvscale[h] * qalpha[m.qslot * 64 + h * GE + j];
+        const int i = j >> P.g_log2;
+        x[j] = row_in && t_rel < i && i < P.q_len ? sj * f : -INFINITY;
+        need |= x[j] > m_ref[j] + kRescaleLog2;
+      }
+
+      // ---- raise the reference where a score exceeds it by more than
+      // kRescaleLog2: to the chunk maximum of that column over its KV head's
+      // rows (half-warp, then shared memory across the chunk's groups)
+      if (dev::named_barrier_or(1, kCons, need)) {
+        float cm[GE];
+#pragma unroll
+        for (int j = 0; j < GE; ++j) {
+          float v = x[j];
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          cm[j] = v;
+        }
+        if (U > 1) {  // the head's rows span several 16-row groups of the chunk
+          if (key == 0) {
+#pragma unroll
+            for (int j = 0; j < GE; ++j) red[grp * kMaxGE + j] = cm[j];
+          }
+          dev::named_barrier(1, kCons);
+#pragma unroll
+          for (int j = 0; j < GE; ++j) {
+            float v = -INFINITY;
+            for (int uu = 0; uu < U; ++uu) v = fmaxf(v, red[(uu * H + h) * kMaxGE + j]);
+            cm[j] = v;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < GE; ++j) {
+          const float nr = cm[j] > m_ref[j] + kRescaleLog2 ? cm[j] : m_ref[j];
+          // 1 where unchanged (also for a column that has seen no key yet)
+          const float f = nr == m_ref[j] ? 1.0f : dev::fast_exp2(m_ref[j] - nr);
+          l_part[j] *= f;
+          m_ref[j] = nr;
+          if (u == 0 && key == 0) alpha_s[h * GE + j] = f;
+        }
+        if (!first) {
+          // chunk c-1's value product must be in O^T before it is scaled
+          if (pv_done < c - 1) wait_pv(c - 1);
+          dev::named_barrier(1, kCons);  // every factor is written
+          dev::tc_fence_after();
+#pragma unroll
+          for (int part = 0; part < (F8 ? 2 : 1); ++part) {  // F8: hi and lo columns
+#pragma unroll
+            for (int cg = 0; cg < N; cg += CW) {
+              float o[CW];
+              dev::tmem_ld_cols<CW>(tO + part * N + cg, o);
+#pragma unroll
+              for (int n = 0; n < CW; ++n) o[n] *= alpha_s[cg + n];
+              dev::tmem_st_cols<CW>(tO + part * N + cg, o);
+            }
+          }
+        }
+      }
+      // the value product that last read this P buffer (chunk c - PB) must be done
+      if (c - C::PB >= 0 && pv_done < c - C::PB) wait_pv(c - C::PB);
+      unsigned char* pcur = pbuf + (c % C::PB) * C::P_BYTES;
+
+#pragma unroll
+      for (int j = 0; j < GE; ++j) {
+        // a masked score gives 0 (m_ref may still be -inf for its column)
+        const float p = x[j] == -INFINITY ? 0.0f : dev::fast_exp2(x[j] - m_ref[j]);
+        if constexpr (F8) {
+          // P as two E4M3 terms; the sum uses exactly what the MMA multiplies
+          const uint8_t ph = dev::to_e4m3(p);
+          const float phf = dev::from_e4m3(ph);
+          const uint8_t pl = dev::to_e4m3(p - phf);
+          l_part[j] += phf + dev::from_e4m3(pl);
+          const uint32_t o = p8_offset(h * GE + j, ctid);
+          pcur[o] = ph;
+          pcur[C::PH_BYTES + o] = pl;
+        } else {
+          l_part[j] += p;
+          *reinterpret_cast<__nv_bfloat16*>(pcur + p_offset<N>(h * GE + j, ctid)) =
+              __float2bfloat16_rn(p);
+        }
+      }
+      // A row past the sequence inside a loaded block (the sequence's last,
+      // partial block) may hold anything, NaN included: clear its V row so
+      // 0 * V = 0.
+      if (!valid && row_in) {
+        unsigned char* kv = ring + size_t(slot) * C::SLOT_BYTES;
+        if constexpr (F8) {  // the key is column `key` of its [D][16] V^T tile
+          unsigned char* tile = kv + C::K_BYTES + grp * C::VT_TILE + key;
+#pragma unroll 16
+          for (int d = 0; d < D; ++d) tile[d * BS] = 0;
+        } else {
+#pragma unroll
+          for (int hf = 0; hf < C::HALVES; ++hf) {
+            uint4* row =
+                reinterpret_cast<uint4*>(kv + C::K_BYTES + hf * C::HALF_BYTES + ctid * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      dev::fence_async_smem();
+      dev::tc_fence_before();
+      dev::mbar_arrive(&bar_p[c % C::PB]);  // P(c) written; S(c) read; O^T rescaled
+
+      if (m.flags & F_LAST) {
+        // per query column: softmax denominator over all rows of its KV head
+#pragma unroll
+        for (int j = 0; j < GE; ++j) {
+          float v = l_part[j];
+#pragma unroll
+          for (int o2 = 8; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+          if (key == 0) red2[grp * kMaxGE + j] = v;
+        }
+        dev::named_barrier(1, kCons);
+        if (u == 0 && key == 0) {
+#pragma unroll
+          for (int j = 0; j < GE; ++j) {
+            float l = 0.0f;
+            for (int uu = 0; uu < U; ++uu) l += red2[(uu * H + h) * kMaxGE + j];
+            l_s[h * GE + j] = l;
+            m_s[h * GE + j] = m_ref[j];
+          }
+        }
+        wait_pv(c);
+        dev::tc_fence_after();
+        // O^T columns [cg, cg + CW) of this thread's lane (row d = ctid)
+        auto load_o = [&](int cg, float (&o)[CW]) {
+          dev::tmem_ld_cols<CW>(tO + cg, o);
+          if constexpr (F8) {  // hi + lo terms, times the V scale of each column's KV head
+#pragma unroll
+            for (int c16 = 0; c16 < CW; c16 += 16) {
+              float o2[16];
+              dev::tmem_ld_cols<16>(tO + N + cg + c16, o2);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int n = cg + c16 + i;
+                o[c16 + i] = (o[c16 + i] + o2[i]) * kvscale[8 + (n < NC ? n / GE : 0)];
+              }
+            }
+          }
+        };
+        float o[CW];
+        load_o(0, o);
+        dev::named_barrier(1, kCons);  // l_s, m_s written
+        __nv_bfloat16* o_row =
+            P.out + size_t(m.b) * P.q_len * P.num_q_heads * D + (ctid < D ? ctid : 0);
+        float* a_row = P.part_acc + size_t(m.seg) * NC * D + (ctid < D ? ctid : 0);
+#pragma unroll
+        for (int cg = 0; cg < N; cg += CW) {
+          if (cg > 0) load_o(cg, o);
+          if (ctid < D) {
+            if (m.flags & F_WHOLE) {
+#pragma unroll
+              for (int i = 0; i < CW; ++i) {
+                const int r = colrow[cg + i];
+                if (r >= 0) o_row[size_t(r) * D] = __float2bfloat16_rn(o[i] * __frcp_rn(l_s[cg + i]));
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < CW; ++i)
+                if (cg + i < NC) a_row[size_t(cg + i) * D] = o[i];
+            }
+          }
+        }
+        if (!(m.flags & F_WHOLE) && ctid < NC) {
+          P.part_m[size_t(m.seg) * NC + ctid] = m_s[ctid];
+          P.part_l[size_t(m.seg) * NC + ctid] = l_s[ctid];
+        }
+        dev::tc_fence_before();
+#pragma unroll
+        for (int j = 0; j < GE; ++j) {
+          m_ref[j] = -INFINITY;
+          l_part[j] = 0.0f;
+        }
+      }
+      ++c;
+    }
+    if (!ok && ctid == 0) {
+      atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    if (ctid == 0) *consumed_out = c;
+  }
+};
+
+template <int D, int GE, int N, bool F8>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_q, const TcParams P) {
+  using C = TcCfg<D, N, F8>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* ring = smem + C::OFF_RING;
+  unsigned char* qbuf = smem + C::OFF_Q;
+  unsigned char* pbuf = smem + C::OFF_P;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::ST;
+  uint64_t* qempty = bars + 2 * C::ST;
+  uint64_t* bar_s = bars + 2 * C::ST + 2;  // [3] scores ready
+  uint64_t* bar_o = bar_s + 3;              // [2] value product ready (by P buffer)
+  uint64_t* bar_p = bar_o + 2;              // [2] P written by all 128 softmax threads
+  uint64_t* drain = bar_p + 2;
+  ChunkMeta* meta = reinterpret_cast<ChunkMeta*>(smem + C::OFF_META);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  float* red2 = reinterpret_cast<float*>(smem + C::OFF_RED2);
+  float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
+  float* l_s = reinterpret_cast<float*>(smem + C::OFF_LS);
+  float* m_s = reinterpret_cast<float*>(smem + C::OFF_MS);
+  int* words = reinterpret_cast<int*>(smem + C::OFF_WORDS);
+  float* qalpha = reinterpret_cast<float*>(smem + C::OFF_QALPHA);    // F8
+  float* kvscale = reinterpret_cast<float*>(smem + C::OFF_KVSCALE);  // F8
+  int* colrow = reinterpret_cast<int*>(smem + C::OFF_COLROW);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&words[0]);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&words[1]);
+  int* consumed = &words[2];
+  int* issued = &words[3];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int B = P.num_seqs;
+  const int H = P.num_kv_heads;
+
+  if (tid == 0) {
+    for (int i = 0; i < C::ST; ++i) {
+      dev::mbar_init(&full[i], 1);
+      dev::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) dev::mbar_init(&qempty[i], 1);
+    for (int i = 0; i < 3; ++i) dev::mbar_init(&bar_s[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      dev::mbar_init(&bar_o[i], 1);
+      dev::mbar_init(&bar_p[i], kCons);
+    }
+    dev::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    *issued = 0;
+    dev::fence_barrier_init();
+  }
+  // P^T is block-diagonal: the entries off the diagonal stay zero for good.
+  for (int i = tid; i < C::PB * C::P_BYTES / 16; i += NTHREADS)
+    reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+
+  // ---- stream-K plan (uses the still-empty ring as scratch): block counts of
+  // the sequences, their exclusive prefix, this CTA's range of the stream.
+  int* pre = reinterpret_cast<int*>(ring);
+  {
+    const int seg = (B + NTHREADS - 1) / NTHREADS;
+    const int b0 = min(B, tid * seg), b1 = min(B, b0 + seg);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int L0 = P.context_lens[b];
+      if (blockIdx.x == 0 && (L0 > P.cap || (L0 > 0 && L0 < P.q_len)))
+        atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
+      const int L = seq_len(P, b);
+      local += (L + BS - 1) / BS;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) reinterpret_cast<int*>(red)[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += reinterpret_cast<int*>(red)[w];
+    for (int b = b0; b < b1; ++b) {
+      pre[b] = run;
+      run += (seq_len(P, b) + BS - 1) / BS;
+    }
+    if (tid == NTHREADS - 1) pre[B] = run;
+  }
+  __syncthreads();
+  const int total = pre[B];
+  const int R = total > 0 ? (total + int(gridDim.x) - 1) / int(gridDim.x) : 1;
+  const int u0 = min(total, int(blockIdx.x) * R);
+  const int u1 = min(total, u0 + R);
+  int b_start = 0;
+  if (u0 < u1) {
+    int lo = 0, hi = B;  // largest b with pre[b] <= u0: the sequence holding block u0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] <= u0) lo = mid; else hi = mid;
+    }
+    b_start = lo;
+  }
+  const int off_start = u0 < u1 ? u0 - pre[b_start] : 0;
+  for (int i = tid; i < 128; i += NTHREADS) {
+    alpha_s[i] = 1.0f;  // padded columns stay 1
+    colrow[i] = column_row(P, i, GE);
+  }
+
+  if (warp == 0) dev::tmem_alloc(tmem_slot, C::TMEM_COLS);
+  // Everything above read only context_lens (and shared memory). When this
+  // kernel overlaps the previous one, that is all it may touch before
+  // waiting; the producer also fetches its first block-table window first.
+  int win0 = -1, len0 = 0;
+  if (warp == kProducerWarp && u0 < u1) {
+    const int j = off_start + lane;
+    win0 = j < P.max_blocks_per_seq
+               ? P.block_tables[size_t(b_start) * P.max_blocks_per_seq + j] : -1;
+    len0 = seq_len(P, b_start);
+  }
+  dev::griddep_wait();
+  if constexpr (F8) {  // per-KV-head scales: k_scale in [0, 8), v_scale in [8, 16)
+    if (tid < 16) kvscale[tid] = (tid & 7) < H ? (tid < 8 ? P.k_scale : P.v_scale)[tid & 7] : 1.0f;
+  }
+  if (blockIdx.x == 0) {  // the stream-K plan, for the merge kernel
+    for (int i = tid; i <= B; i += NTHREADS) P.ws_plan[1 + i] = pre[i];
+    if (tid == 0) P.ws_plan[0] = R;
+  }
+  dev::fence_async_smem();
+  dev::tc_fence_before();
+  __syncthreads();  // the ring is free for TMA from here on
+  dev::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      dev::prefetch_tmap(&tm_k);
+      dev::prefetch_tmap(&tm_v);
+      dev::prefetch_tmap(&tm_q);
+    }
+    const uint64_t pol = dev::l2_evict_first_policy();
+    const int U = kGroups / H;   // blocks per chunk
+    const int grows = BS * H;    // rows of one block (all KV heads)
+    int chunk_seq = 0, seg_seq = 0;
+    bool ok = true;
+    // block-table window: lane j holds the entry of block first_block + j
+    auto load_window = [&](int b, int first_block) {
+      const int j = first_block + lane;
+      return (b < B && j < P.max_blocks_per_seq)
+                 ? P.block_tables[size_t(b) * P.max_blocks_per_seq + j] : -1;
+    };
+    // Fused KV append: sequence b's new tokens (its last q_len, tokens
+    // L-q_len .. L-1; row b*q_len + i of k_new/v_new/slot_mapping) are
+    // written by the pieces that read their blocks, before those blocks'
+    // copies are issued: the piece of blocks [blk0, blk1) writes the new
+    // tokens that fall in them. Generic-proxy stores, then a proxy fence so
+    // the TMA (async proxy) that follows reads the new rows.
+    auto append_tokens = [&](int b, int L, int blk0, int blk1) {
+      for (int i = 0; i < P.q_len; ++i) {
+        const int pos = L - P.q_len + i;
+        if (pos < blk0 * BS || pos >= blk1 * BS) continue;
+        const size_t tok = size_t(b) * P.q_len + i;
+        const int64_t slot = P.slot_mapping[tok];
+        if (slot < 0) continue;  // padding token
+        if (slot >= int64_t(P.num_blocks) * BS) {
+          if (lane == 0) atomicOr(&g_tc_errors, PA_DEVERR_SLOT);
+          continue;
+        }
+        const int e = P.block_tables[size_t(b) * P.max_blocks_per_seq + pos / BS];
+        if (e < 0 || e >= P.num_blocks || slot != int64_t(e) * BS + pos % BS) {
+          if (lane == 0) atomicOr(&g_tc_errors, PA_DEVERR_APPEND_SLOT);
+          continue;
+        }
+        constexpr int CPR = D / 8;  // 16-byte chunks of one row
+        const int n = H * CPR;
+        for (int k = lane; k < n; k += 32) {
+          const int hh = k / CPR, ch = k - (k / CPR) * CPR;
+          const size_t src = tok * n + k;
+          const size_t dst = ((size_t(e) * H + hh) * BS + pos % BS) * CPR + ch;
+          const uint4 kv = P.k_new[src];
+          const uint4 vv = P.v_new[src];
+          P.k_cache_w[dst] = kv;
+          P.v_cache_w[dst] = vv;
+        }
+      }
+      dev::fence_async_global();
+    };
+    int b = b_start, off = off_start, unit = u0;
+    int win = win0;
+    int L_cur = len0;
+    while (ok && unit < u1) {
+      if (*abort_flag) break;
+      const int nb = L_cur > 0 ? (L_cur + BS - 1) / BS : 0;
+      if (nb == 0) {  // empty sequence: nothing of it in the stream
+        ++b;
+        win = load_window(b, 0);
+        L_cur = b < B ? seq_len(P, b) : 0;
+        continue;
+      }
+      const int seg_nb = min(nb - off, u1 - unit);
+      const bool whole = off == 0 && seg_nb == nb;
+      if constexpr (!F8) {
+        // this piece holds a block of the new tokens
+        if (P.k_new != nullptr && off + seg_nb > (L_cur - P.q_len) / BS) {
+          append_tokens(b, L_cur, off, off + seg_nb);
+          __syncwarp();
+          dev::fence_async_global();
+        }
+      }
+      // prefetched for later: the next sequence's length and first window,
+      // this segment's second window
+      const int L_nxt = b + 1 < B ? seq_len(P, b + 1) : 0;
+      const int win_nxt_seq = load_window(b + 1, 0);
+      int win_nxt = seg_nb > 32 ? load_window(b, off + 32) : -1;
+      const int qs = seg_seq % C::QB;
+      const int nch = (seg_nb + U - 1) / U;
+      for (int c = 0; c < nch; ++c) {
+        const int jb = c * U;  // first block of the chunk within the segment
+        if (jb > 0 && (jb & 31) == 0) {
+          win = win_nxt;
+          win_nxt = jb + 32 < seg_nb ? load_window(b, off + jb + 32) : -1;
+        }
+        const int slot = chunk_seq % C::ST;
+        const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
+        if (lane == 0) {
+          ok = dev::mbar_wait_sleep(&empty[slot], ph ^ 1u, 64);
+          if (ok && c == 0)
+            ok = dev::mbar_wait_sleep(&qempty[qs], (uint32_t(seg_seq / C::QB) & 1u) ^ 1u, 64);
+          if (ok) {
+            ChunkMeta m;
+            m.b = b;
+            m.seg = b + int(blockIdx.x);
+            m.flags = (c == 0 ? F_FIRST : 0) | (c == nch - 1 ? F_LAST : 0) | (whole ? F_WHOLE : 0);
+            m.tok0 = (off + jb) * BS;
+            m.L = L_cur;
+            m.nblk = min(U, seg_nb - jb);
+            m.qslot = qs;
+            m.pad = 0;
+            meta[slot] = m;
+            dev::mbar_arrive_expect_tx(&full[slot], C::CHUNK_TX + (c == 0 ? C::Q_TX : 0u));
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+        if (!ok) break;
+        // lanes 0..U-1: one block (all KV heads) each
+        const int e = __shfl_sync(0xffffffffu, win, (jb & 31) + (lane % U));
+        unsigned char* kdst = ring + size_t(slot) * C::SLOT_BYTES;
+        if constexpr (F8) {
+          // lanes 0..U-1: block `lane`'s K rows, and its H V^T tiles as one
+          // 3-D box (the tiles of a block are adjacent in the cache)
+          if (lane < U) {
+            int row = P.oob_row, tile = P.oob_row_v;
+            if (jb + lane < seg_nb) {
+              if (e >= 0 && e < P.num_blocks) {
+                row = e * grows;
+                tile = e * H;
+              } else {
+                atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+              }
+            }
+            dev::tma_load_2d(kdst + lane * grows * 128, &tm_k, 0, row, &full[slot], pol);
+            dev::tma_load_3d(kdst + C::K_BYTES + lane * H * C::VT_TILE, &tm_v, 0, 0, tile,
+                             &full[slot], pol);
+          } else if (lane == 8 && c == 0) {
+            dev::tma_load_2d(qbuf + qs * C::Q_BYTES, &tm_q, 0, b * P.q_rows, &full[slot], pol);
+            dev::bulk_load(qalpha + qs * 64, P.q_inv_alpha + size_t(b) * N, N * 4, &full[slot],
+                           pol);
+          }
+        } else {
+          if (lane < U) {
+            int row = P.oob_row;
+            if (jb + lane < seg_nb) {
+              if (e >= 0 && e < P.num_blocks) {
+                row = e * grows;
+              } else {
+                atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+              }
+            }
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf) {
+              unsigned char* d = kdst + hf * C::HALF_BYTES + lane * grows * 128;
+              dev::tma_load_2d(d, &tm_k, hf * 64, row, &full[slot], pol);
+              dev::tma_load_2d(d + C::K_BYTES, &tm_v, hf * 64, row, &full[slot], pol);
+            }
+          } else if (lane == 8 && c == 0) {
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf)
+              dev::tma_load_2d(qbuf + qs * C::Q_BYTES + hf * C::QH_BYTES, &tm_q, hf * 64,
+                               b * P.q_rows, &full[slot], pol);
+          }
+        }
+        ++chunk_seq;
+        if (lane == 0) *issued = chunk_seq;
+      }
+      ++seg_seq;
+      unit += seg_nb;
+      ++b;
+      off = 0;
+      win = win_nxt_seq;
+      L_cur = L_nxt;
+    }
+    // end of work: a sentinel chunk tells the consumers to stop
+    if (lane == 0) {
+      const int slot = chunk_seq % C::ST;
+      const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
+      const bool ok2 = dev::mbar_wait(&empty[slot], ph ^ 1u);
+      ChunkMeta m{};
+      m.flags = F_END;
+      meta[slot] = m;
+      dev::mbar_arrive(&full[slot]);
+      if (!ok || !ok2) {
+        atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0)
+      mma_loop<D, N, F8>(ring, qbuf, pbuf, full, empty, qempty, bar_s, bar_o, bar_p, drain,
+                         meta, tmem, abort_flag);
+  } else {
+    // ------------------------------------------------------------ softmax
+    Softmax<D, GE, N, F8>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2,
+                              alpha_s, l_s, m_s, qalpha, kvscale, colrow, tmem, abort_flag,
+                              consumed);
+  }
+
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // Wind down after a stalled wait: every bulk copy issued but not consumed
+    // lands (each wait bounded) before shared memory is released. (The MMA
+    // warp has already waited for its own MMAs.)
+    for (int c = *consumed; c < *issued; ++c)
+      (void)dev::mbar_wait(&full[c % C::ST], uint32_t(c / C::ST) & 1u);
+  }
+  dev::tc_fence_before();
+  __syncthreads();
+  // The merge kernel (a programmatic dependent) can do nothing before this
+  // grid ends: let it launch as the CTAs finish, not earlier, so its waiting
+  // CTAs never share an SM with a running decode CTA.
+  if (tid == 0) dev::griddep_launch_dependents();
+  if (warp == 0) {
+    dev::tc_fence_after();
+    dev::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Log-sum-exp merge of the partials of sequences that span several CTAs, and
+// zero rows for empty sequences. One warp per (sequence, column). The
+// lanes read the pieces' (max, sum) pairs side by side while the rows of the
+// first kPrefetch pieces are already in flight, so a typical merge costs one
+// memory round trip.
+template <int VPL>
+struct Row {
+  float v[VPL];
+  __device__ void load(const float* src) {
+    if constexpr (VPL == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(src);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      v[0] = t.x; v[1] = t.y;
+    }
+  }
+  __device__ void madd_into(float* acc, float w) const {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) acc[j] = fmaf(w, v[j], acc[j]);
+  }
+};
+
+struct MergeCols {
+  int num_q_heads, num_cols, group_cols, g_log2, q_len;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128)
+    merge_segments_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ part_m,
+                          const float* __restrict__ part_l, const float* __restrict__ part_acc,
+                          const int* __restrict__ ws_plan, const MergeCols mc) {
+  constexpr int VPL = D / 32;
+  constexpr int kPrefetch = 16;
+  // The next kernel on the stream may start its own set-up now (it waits
+  // for this grid before it touches memory this grid writes).
+  dev::griddep_launch_dependents();
+  dev::griddep_wait();  // launched as a programmatic dependent of the decode
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 4 + warp;  // column (the decode kernel's layout)
+  const int b = blockIdx.y;
+  if (n >= mc.num_cols) return;
+  const int g = n / mc.group_cols, r = n - g * mc.group_cols;
+  const int qi = r >> mc.g_log2;  // query token of the column
+  if (qi >= mc.q_len) return;     // unused column
+  const int R = ws_plan[0];
+  const int pre0 = ws_plan[1 + b], pre1 = ws_plan[2 + b];
+  const size_t orow = (size_t(b) * mc.q_len + qi) * mc.num_q_heads + (g << mc.g_log2) +
+                      (r & ((1 << mc.g_log2) - 1));
+  __nv_bfloat16* o = out + orow * D + lane * VPL;
+  if (pre1 <= pre0) {  // empty sequence
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(0.0f);
+    return;
+  }
+  const int c0 = pre0 / R, c1 = (pre1 - 1) / R;
+  if (c0 == c1) return;  // written whole by the decode kernel
+  const int nseg = c1 - c0 + 1;
+  // piece k of the sequence sits in partial slot (b + c0 + k)
+  const size_t slot0 = size_t(b + c0) * mc.num_cols + n;
+  const size_t stride = size_t(mc.num_cols);
+  const float* src0 = part_acc + slot0 * D + lane * VPL;
+  Row<VPL> pf[kPrefetch];
+#pragma unroll
+  for (int k = 0; k < kPrefetch; ++k)
+    if (k < nseg) pf[k].load(src0 + size_t(k) * stride * D);
+  float m_first = -INFINITY, l_first = 0.0f;  // this lane's piece among the first 32
+  if (lane < nseg) {
+    m_first = part_m[slot0 + lane * stride];
+    l_first = part_l[slot0 + lane * stride];
+  }
+  float M = m_first;
+  for (int k = 32 + lane; k < nseg; k += 32) M = fmaxf(M, part_m[slot0 + k * stride]);
+#pragma unroll
+  for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+  float acc[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) acc[j] = 0.0f;
+  float den = 0.0f;
+  for (int base = 0; base < nseg; base += 32) {
+    float w = 0.0f;
+    if (base + lane < nseg) {
+      const float mk = base == 0 ? m_first : part_m[slot0 + (base + lane) * stride];
+      const float lk = base == 0 ? l_first : part_l[slot0 + (base + lane) * stride];
+      w = dev::fast_exp2(mk - M);
+      den = fmaf(w, lk, den);
+    }
+    const int cnt = min(32, nseg - base);
+    int k0 = 0;
+    if (base == 0) {
+#pragma unroll
+      for (int k = 0; k < kPrefetch; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        if (k < cnt) pf[k].madd_into(acc, wk);
+      }
+      k0 = kPrefetch;
+    }
+    for (int k = k0; k < cnt; k += 8) {
+      Row<VPL> r[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (k + j < cnt) r[j].load(src0 + size_t(base + k + j) * stride * D);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, (k + j) & 31);
+        if (k + j < cnt) r[j].madd_into(acc, wj);
+      }
+    }
+  }
+#pragma unroll
+  for (int o2 = 16; o2 >= 1; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
+  const float inv = __frcp_rn(den);
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(acc[j] * inv);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+int g_sm_count[64] = {};
+
+int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  *fn = g_encode;
+  return g_encode ? 0 : int(cudaErrorNotSupported);
+}
+
+// 2-D bf16 tensor [rows][cols] (row pitch cols*2 bytes), box box_rows x 64 cols,
+// 128B swizzle, out-of-range elements read as zero.
+int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (encode_fn(&enc)) return int(cudaErrorNotSupported);
+  cuuint64_t gdim[2] = {cols, rows};
+  cuuint64_t gstride[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
+}
+
+// 2-D byte tensor [rows][cols] (row pitch cols bytes), box box_rows x
+// box_cols, the given swizzle, out-of-range elements read as zero.
+int make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (encode_fn(&enc)) return int(cudaErrorNotSupported);
+  cuuint64_t gdim[2] = {cols, rows};
+  cuuint64_t gstride[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
+}
+
+// The 8-bit V^T cache as a 3-D byte tensor: [tiles][D rows][16 bytes], one
+// tile per (block, KV head); box = `heads` whole tiles, no swizzle.
+int make_map_vt(CUtensorMap* m, const void* base, uint64_t tiles, uint64_t d, uint32_t heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (encode_fn(&enc)) return int(cudaErrorNotSupported);
+  cuuint64_t gdim[3] = {uint64_t(BS), d, tiles};
+  cuuint64_t gstride[2] = {uint64_t(BS), d * BS};
+  cuuint32_t box[3] = {uint32_t(BS), uint32_t(d), heads};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
+}
+
+template <int D, int GE, int N, bool F8>
+int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
+  using C = TcCfg<D, N, F8>;
+  const pa_decode_params* p = Lc.p;
+  const QueryMap qm = query_map(p);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GE, N, F8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return int(e);
+    configured = true;
+  }
+  const int H = p->num_kv_heads;
+  CUtensorMap tk, tv, tq;
+  const uint64_t cache_rows = uint64_t(p->num_blocks) * H * BS;
+  int r = 0;
+  if constexpr (F8) {
+    // K rows of D bytes; V^T rows of 16 bytes, one [D][16] tile per (block,
+    // head); the split queries, 2N rows of D bytes per sequence
+    r = make_map_u8(&tk, p->k_cache, cache_rows, D, D, uint32_t(BS * H),
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r) r = make_map_vt(&tv, p->v_cache, uint64_t(p->num_blocks) * H, D, uint32_t(H));
+    if (!r)
+      r = make_map_u8(&tq, Lc.q8, uint64_t(p->num_seqs) * 2 * N, D, D, uint32_t(2 * N),
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r) r = launch_quantize_q(p->q, Lc.q8, Lc.q_inv_alpha, qm, stream);
+  } else {
+    r = make_map(&tk, p->k_cache, cache_rows, D, uint32_t(BS * H));
+    if (!r) r = make_map(&tv, p->v_cache, cache_rows, D, uint32_t(BS * H));
+    if (qm.query_len == 1) {
+      // the rows of q are already in column order (column = query head); a
+      // box of N rows may run into the next sequence's rows, never used
+      if (!r) r = make_map(&tq, p->q, uint64_t(p->num_seqs) * p->num_q_heads, D, uint32_t(N));
+    } else {
+      if (!r) r = make_map(&tq, Lc.qp, uint64_t(p->num_seqs) * N, D, uint32_t(N));
+      if (!r) r = launch_permute_q(p->q, Lc.qp, qm, stream);
+    }
+  }
+  if (r) return r;
+  TcParams P;
+  P.block_tables = p->block_tables;
+  P.context_lens = p->context_lens;
+  P.out = static_cast<__nv_bfloat16*>(p->out);
+  P.part_m = Lc.part_m;
+  P.part_l = Lc.part_l;
+  P.part_acc = Lc.part_acc;
+  P.ws_plan = Lc.plan;
+  const pa_append_params* a = Lc.append;
+  P.k_new = a ? static_cast<const uint4*>(a->k_new) : nullptr;
+  P.v_new = a ? static_cast<const uint4*>(a->v_new) : nullptr;
+  P.slot_mapping = a ? a->slot_mapping : nullptr;
+  P.k_cache_w = a ? static_cast<uint4*>(a->k_cache) : nullptr;
+  P.v_cache_w = a ? static_cast<uint4*>(a->v_cache) : nullptr;
+  P.k_scale = p->k_scale;
+  P.v_scale = p->v_scale;
+  P.q_inv_alpha = Lc.q_inv_alpha;
+  P.oob_row_v = int(uint64_t(p->num_blocks) * H);  // first V^T tile past the cache
+  P.q_rows = F8 ? 2 * N : (qm.query_len == 1 ? p->num_q_heads : N);
+  P.num_cols = qm.num_cols;
+  P.q_len = qm.query_len;
+  P.g_log2 = qm.g_log2;
+  P.max_blocks_per_seq = p->max_blocks_per_seq;
+  P.num_seqs = p->num_seqs;
+  P.num_kv_heads = H;
+  P.num_q_heads = p->num_q_heads;
+  P.num_blocks = p->num_blocks;
+  P.cap = min(p->max_blocks_per_seq * BS, p->max_context_len);
+  P.oob_row = int(cache_rows);
+  P.scale_log2 = p->scale * kLog2e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Lc.grid);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // overlap the set-up with the previous kernel only when the caller says
+  // context_lens and block_tables were final before that kernel began
+  attr[0].val.programmaticStreamSerializationAllowed = p->overlap_prologue ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<D, GE, N, F8>, tk, tv, tq, P);
+  if (e != cudaSuccess) return int(e);
+  // the merge launches while the decode drains and waits for it on the device
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3((qm.num_cols + 3) / 4, p->num_seqs);
+  mcfg.blockDim = dim3(128);
+  mcfg.stream = stream;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  MergeCols mc;
+  mc.num_q_heads = p->num_q_heads;
+  mc.num_cols = qm.num_cols;
+  mc.group_cols = qm.group_cols;
+  mc.g_log2 = qm.g_log2;
+  mc.q_len = qm.query_len;
+  e = cudaLaunchKernelEx(&mcfg, merge_segments_kernel<D>, P.out,
+                         static_cast<const float*>(P.part_m), static_cast<const float*>(P.part_l),
+                         static_cast<const float*>(P.part_acc),
+                         static_cast<const int*>(P.ws_plan), mc);
+  return int(e);
+}
+
+// Instances by (columns per KV head GE, padded columns N).
+template <int D, bool F8>
+int dispatch_tc(const DecodeLaunch& Lc, cudaStream_t s) {
+  const int GE = tc_group_cols(Lc.p);
+  const int N = tc_n_pad(tc_cols(Lc.p));
+  switch (GE * 1000 + N) {
+    case 1016: return launch_tc_t<D, 1, 16, F8>(Lc, s);
+    case 2016: return launch_tc_t<D, 2, 16, F8>(Lc, s);
+    case 4016: return launch_tc_t<D, 4, 16, F8>(Lc, s);
+    case 4032: return launch_tc_t<D, 4, 32, F8>(Lc, s);
+    case 8016: return launch_tc_t<D, 8, 16, F8>(Lc, s);
+    case 8032: return launch_tc_t<D, 8, 32, F8>(Lc, s);
+    case 8064: return launch_tc_t<D, 8, 64, F8>(Lc, s);
+    case 16016: return launch_tc_t<D, 16, 16, F8>(Lc, s);
+    case 16032: return launch_tc_t<D, 16, 32, F8>(Lc, s);
+    case 16064: return launch_tc_t<D, 16, 64, F8>(Lc, s);
+    case 16128:
+      if constexpr (!F8) return launch_tc_t<D, 16, 128, F8>(Lc, s);
+      return int(cudaErrorInvalidValue);
+    default: return int(cudaErrorInvalidValue);
+  }
+}
+
+// Device error word of the including translation unit, read and cleared.
+inline int read_and_clear_tc_error_word(uint32_t* flags) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc_errors, sizeof(v));
+  if (e != cudaSuccess) return int(e);
+  e = cudaMemcpyToSymbol(g_tc_errors, &zero, sizeof(zero));
+  *flags = v;
+  return int(e);
+}
+
+}  // namespace
+}  // namespace pa

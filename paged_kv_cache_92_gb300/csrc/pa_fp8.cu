@@ -1,5 +1,5 @@
-// 8-bit (FP8 E4M3) KV cache support for sm_103a: the quantising KV write and
-// the split of the bf16 queries into two E4M3 terms for the tensor cores.
+// 8-bit (FP8 E4M3) KV cache support for sm_103a: the quantising KV write.
+// (The split of the queries into two E4M3 terms is in pa_query.cu.)
 //
 // The pages say only that paging combines with 8-bit KV quantisation, which
 // halves the bytes per block ("PagedAttention" glossary page, §What paging
@@ -26,7 +26,6 @@ __device__ unsigned int g_fp8_errors;
 
 constexpr int BS = kBlockSize;
 
-using dev::from_e4m3;
 using dev::to_e4m3;
 
 // One thread per 8 elements (one 16-byte chunk of the bf16 input) of one
@@ -73,55 +72,6 @@ __global__ void __launch_bounds__(256)
     v_cache[tile + int64_t(c * 8 + i) * BS + off] = to_e4m3(__fdiv_rn(__bfloat162float(vb[i]), vs));
 }
 
-// Queries for the E4M3 tensor-core decode. For every (sequence b, query head
-// n) the row is scaled by a power of two alpha (its largest magnitude lands
-// in [64, 128)), split into hi = E4M3(q * alpha) and lo = E4M3(q * alpha - hi),
-// which together carry about 8 significant bits (the scores use hi + lo), and
-// 1/alpha is kept for the softmax. Output rows: q8[b][n] = hi, q8[b][N + n] =
-// lo, zero for n >= Hq; inv_alpha[b][n] (1 for n >= Hq). One warp per (b, n).
-__global__ void __launch_bounds__(128)
-    quantize_q_kernel(const __nv_bfloat16* __restrict__ q, uint8_t* __restrict__ q8,
-                      float* __restrict__ inv_alpha, int num_seqs, int num_q_heads, int N,
-                      int head_dim) {
-  dev::griddep_launch_dependents();
-  dev::griddep_wait();  // q may come from the previous kernel
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t gw = int64_t(blockIdx.x) * 4 + warp;
-  if (gw >= int64_t(num_seqs) * N) return;
-  const int b = int(gw / N), n = int(gw % N);
-  const int per = head_dim / 32;  // elements per lane (4 at head_dim 128)
-  uint8_t* hi_row = q8 + (int64_t(b) * 2 * N + n) * head_dim;
-  uint8_t* lo_row = q8 + (int64_t(b) * 2 * N + N + n) * head_dim;
-  if (n >= num_q_heads) {
-    for (int i = 0; i < per; ++i) {
-      hi_row[lane * per + i] = 0;
-      lo_row[lane * per + i] = 0;
-    }
-    if (lane == 0) inv_alpha[int64_t(b) * N + n] = 1.0f;
-    return;
-  }
-  const __nv_bfloat16* src = q + (int64_t(b) * num_q_heads + n) * head_dim + lane * per;
-  float v[4];
-  float amax = 0.0f;
-  for (int i = 0; i < per; ++i) {
-    v[i] = __bfloat162float(src[i]);
-    amax = fmaxf(amax, fabsf(v[i]));
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  int e = 0;
-  if (amax > 0.0f) (void)frexpf(amax, &e);  // amax < 2^e
-  e = max(e, -100);
-  const float alpha = ldexpf(1.0f, 7 - e);  // a power of two: exact
-  for (int i = 0; i < per; ++i) {
-    const float y = v[i] * alpha;
-    const uint8_t h = to_e4m3(y);
-    hi_row[lane * per + i] = h;
-    lo_row[lane * per + i] = to_e4m3(y - from_e4m3(h));
-  }
-  if (lane == 0) inv_alpha[int64_t(b) * N + n] = ldexpf(1.0f, e - 7);
-}
-
 }  // namespace
 
 int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_cache,
@@ -138,24 +88,6 @@ int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_c
       static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), slot_mapping, k_scale,
       v_scale, num_chunks, num_kv_heads, head_dim, int64_t(num_blocks) * BS);
   return int(cudaGetLastError());
-}
-
-int launch_quantize_q(const void* q, void* q8, float* inv_alpha, int32_t num_seqs,
-                      int32_t num_q_heads, int32_t n_pad, int32_t head_dim, void* stream) {
-  const int64_t warps = int64_t(num_seqs) * n_pad;
-  if (warps == 0) return int(cudaSuccess);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned((warps + 3) / 4));
-  cfg.blockDim = dim3(128);
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return int(cudaLaunchKernelEx(&cfg, quantize_q_kernel, static_cast<const __nv_bfloat16*>(q),
-                                static_cast<uint8_t*>(q8), inv_alpha, int(num_seqs),
-                                int(num_q_heads), int(n_pad), int(head_dim)));
 }
 
 int read_and_clear_fp8_errors(uint32_t* flags) {

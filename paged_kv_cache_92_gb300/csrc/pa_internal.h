@@ -33,11 +33,53 @@ struct DecodeLaunch {
   const pa_append_params* append;  // non-null: write each sequence's new token first
   unsigned char* q8;     // 8-bit cache: split queries [B][2N][D] (workspace)
   float* q_inv_alpha;    // 8-bit cache: [B][N] (workspace)
+  void* qp;              // bf16, query_len > 1: queries in column order [B][N][D] (workspace)
 };
 
-// Query heads padded to the tensor-core N (16, 32 or 64).
-inline int tc_n_pad(int num_q_heads) {
-  return num_q_heads <= 16 ? 16 : (num_q_heads <= 32 ? 32 : 64);
+// New tokens per sequence (query_len 0 means 1).
+inline int query_len_of(const pa_decode_params* p) {
+  return p->query_len > 1 ? p->query_len : 1;
+}
+
+// Tensor-core column layout. The kernel's query rows ("columns": the N side
+// of its MMAs) are grouped by KV head: head g owns columns [g*GE, (g+1)*GE),
+// column g*GE + i*G + j being query token i of query head g*G + j. GE is G
+// times query_len rounded up to a power of two; columns whose token index is
+// >= query_len are unused. With one token per sequence GE = G and the column
+// of query head h is h itself.
+inline int tc_group_cols(const pa_decode_params* p) {
+  int q = 1;
+  while (q < query_len_of(p)) q <<= 1;
+  return (p->num_q_heads / p->num_kv_heads) * q;
+}
+inline int tc_cols(const pa_decode_params* p) { return p->num_kv_heads * tc_group_cols(p); }
+
+// Columns padded to the tensor-core N (16, 32, 64 or 128).
+inline int tc_n_pad(int cols) {
+  return cols <= 16 ? 16 : (cols <= 32 ? 32 : (cols <= 64 ? 64 : 128));
+}
+
+inline int log2_of(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+
+// Where the query rows of one sequence sit in the column layout above.
+struct QueryMap {
+  int num_seqs, num_q_heads, query_len, g_log2, group_cols, num_cols, n_pad, head_dim;
+};
+inline QueryMap query_map(const pa_decode_params* p) {
+  QueryMap m;
+  m.num_seqs = p->num_seqs;
+  m.num_q_heads = p->num_q_heads;
+  m.query_len = query_len_of(p);
+  m.g_log2 = log2_of(p->num_q_heads / p->num_kv_heads);
+  m.group_cols = tc_group_cols(p);
+  m.num_cols = tc_cols(p);
+  m.n_pad = tc_n_pad(m.num_cols);
+  m.head_dim = p->head_dim;
+  return m;
 }
 
 // Bytes at the start of every decode workspace (reserved).
@@ -49,6 +91,7 @@ struct WorkspaceLayout {
   size_t simt_m, simt_l, simt_acc;    // [seqs][q heads][partitions](+[dim])
   size_t tc_plan, tc_m, tc_l, tc_acc; // plan, then [seqs + grid][q heads](+[dim])
   size_t tc_q8, tc_qa;                // 8-bit cache: split queries, their 1/alpha
+  size_t tc_qp;                       // bf16, query_len > 1: queries in column order
 };
 WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_partitions,
                                         int tc_grid);
@@ -61,6 +104,8 @@ int tc_grid();
 // Kernel launchers (pa_decode.cu / pa_cache.cu). Return a cudaError_t as int.
 int launch_decode(const DecodeLaunch& L, void* stream);      // CUDA-core decode kernel
 int launch_decode_tc(const DecodeLaunch& L, void* stream);   // tensor-core decode kernel
+int launch_decode_tc_d64(const DecodeLaunch& L, void* stream);  // its bf16 head_dim 64 share
+int launch_decode_tc_fp8(const DecodeLaunch& L, void* stream);  // its 8-bit cache share
 int launch_merge(const DecodeLaunch& L, void* stream);       // split-K merge (if needed)
 // Decode-step check (block_tables non-null): token t is sequence t's newest
 // token; it is written only if slot_mapping[t] is the slot of token
@@ -81,15 +126,21 @@ int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_c
                                  void* v_cache, const int64_t* slot_mapping, const float* k_scale,
                                  const float* v_scale, int32_t num_tokens, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t num_blocks, void* stream);
-int launch_quantize_q(const void* q, void* q8, float* inv_alpha, int32_t num_seqs,
-                      int32_t num_q_heads, int32_t n_pad, int32_t head_dim, void* stream);
 int read_and_clear_fp8_errors(uint32_t* flags);
+// Query preparation for the tensor-core decode (pa_query.cu): the rows of q
+// ([B][query_len][Hq][D] bf16) in the column layout, padded to n_pad rows with
+// zeros -- as bf16 ([B][n_pad][D]), or split into two E4M3 terms ([B][2*n_pad][D]
+// bytes, hi rows then lo rows, and [B][n_pad] floats 1/alpha).
+int launch_permute_q(const void* q, void* qp, const QueryMap& m, void* stream);
+int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap& m, void* stream);
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
                        int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, void* stream);
 
 // Device error words, one per kernel translation unit: read and clear.
 int read_and_clear_decode_errors(uint32_t* flags);
-int read_and_clear_decode_tc_errors(uint32_t* flags);
+int read_and_clear_decode_tc_errors(uint32_t* flags);  // all three shares below
+int read_and_clear_decode_tc_d64_errors(uint32_t* flags);
+int read_and_clear_decode_tc_fp8_errors(uint32_t* flags);
 
 // Size of the library-owned device scratch used by pa_decode_noalloc.
 constexpr size_t kNoAllocScratchBytes = PA_NOALLOC_SCRATCH_BYTES;

@@ -71,6 +71,12 @@ def _params(pk, **kw):
     (dict(num_seqs=70000), 1),
     (dict(variant=2), 1),
     (dict(num_blocks=1 << 24, num_kv_heads=8), 1),  # cache rows past 2^31
+    (dict(query_len=-1), 1),
+    (dict(query_len=2000), 1),
+    (dict(query_len=3, num_q_heads=16, num_kv_heads=2), 2),  # G * 4 = 32 columns per KV head
+    (dict(query_len=2, variant=1), 2),  # several new tokens: tensor-core kernel only
+    (dict(query_len=4, num_q_heads=64, num_kv_heads=8, kv_dtype=1), 2),  # > 64 fp8 columns
+    (dict(query_len=4), 1),  # valid shapes (G 4, 16 columns per KV head), NULL pointers
     (dict(), 1),  # valid shapes, NULL pointers
 ])
 def test_decode_rejects_bad_arguments_on_the_host(pk, kw, status):
@@ -84,13 +90,23 @@ def _ru(x):
     return (x + 255) // 256 * 256
 
 
-def _expected_ws(B, Hq, D, parts, grid):
+def _expected_ws(B, Hq, D, parts, grid, Hkv=None, QL=1):
+    """Tensor-core partials are per query column: Hkv * G * (QL rounded up to
+    a power of two); with QL > 1 the bf16 queries are also staged in column
+    order, [B][N][D] with N the columns padded to 16/32/64/128."""
     simt = 0
     if parts > 1:
         rows = B * Hq * parts
         simt = 2 * _ru(rows * 4) + _ru(rows * D * 4)
-    rows = (B + grid) * Hq
+    qlp = 1
+    while qlp < QL:
+        qlp *= 2
+    cols = Hq * qlp
+    rows = (B + grid) * cols
     tc = _ru((B + 2) * 4) + 2 * _ru(rows * 4) + _ru(rows * D * 4)
+    if QL > 1:
+        n_pad = next(n for n in (16, 32, 64, 128) if cols <= n)
+        tc += _ru(B * n_pad * D * 2)
     return 256 + max(simt, tc)
 
 
@@ -107,6 +123,16 @@ def test_decode_workspace_size(pk):
                 max_blocks_per_seq=2048)
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 64, 256)
     assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk, head_dim=96))) == 0
+    # several new tokens per sequence
+    for ql in (2, 3, 4):
+        p = _params(pk, query_len=ql)
+        assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(2, 8, 128, 1, 256,
+                                                                             QL=ql)
+    p = _params(pk, num_seqs=64, num_q_heads=32, num_kv_heads=8, max_context_len=2048,
+                max_blocks_per_seq=128, query_len=4)
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
+                                                                         QL=4)
+    assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk, query_len=8))) == 0
 
 
 def test_cache_ops_reject_bad_arguments_on_the_host(pk):

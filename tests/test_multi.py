@@ -1,0 +1,303 @@
+"""GPU parity of the decode of several new tokens per sequence (query_len Q > 1).
+
+The new tokens are the last Q of each sequence's context_lens[b] and already
+in the cache; query token i attends to the first L - Q + i + 1 tokens (causal
+among the new tokens). The float64 oracle computes every (sequence, token,
+head) row; the bar is the decode's: max-abs <= 2e-2, mean-abs <= 2e-3, and
+bit-exact caches for the fused KV write. Padding slots hold NaN, so a masked
+slot that leaks into a result fails the finiteness check.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+DEVERR_CONTEXT_LEN = 0x2
+DEVERR_APPEND_SLOT = 0x20
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import torch
+
+    from paged_kv_cache_92_gb300 import build
+
+    build.build()
+    import paged_kv_cache_92_gb300 as pk
+
+    pk.load()
+    assert torch.cuda.is_available()
+    return pk
+
+
+def _sm_count():
+    import torch
+
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _case(lens, QL, Hq, Hkv, D, seed, extra_blocks=3):
+    """Random tables over a shuffled pool, N(0,1) bf16 cache with NaN in the
+    padding slots, q [B][QL][Hq][D]."""
+    import torch
+
+    lens = np.asarray(lens, dtype=np.int64)
+    need = int(((lens + 15) // 16).sum())
+    NB = need + extra_blocks
+    order = np.random.default_rng(seed).permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, 16)
+    q = workloads.bf16_normal((len(lens), QL, Hq, D), seed + 1, "cuda")
+    kc = workloads.bf16_normal((NB, Hkv, 16, D), seed + 2, "cuda")
+    vc = workloads.bf16_normal((NB, Hkv, 16, D), seed + 3, "cuda")
+    workloads.fill_padding_nan(kc, tables, lens, 16)
+    workloads.fill_padding_nan(vc, tables, lens, 16)
+    return q, kc, vc, tables, lens.astype(np.int32), torch
+
+
+def _decode(pk, q, kc, vc, tables, lens, torch, **kw):
+    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=int(lens.max()), **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def _check(pk, q, kc, vc, tables, lens, torch, **kw):
+    out = _decode(pk, q, kc, vc, tables, lens, torch, **kw)
+    want = oracle.paged_decode_multi(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    stats = harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+    return stats
+
+
+# (G, Hkv, Q): every columns-per-KV-head width (G x Q rounded up to a power
+# of two: 2 .. 16), padded widths N = 16 .. 128, Q not a power of two
+SHAPES = [(1, 8, 2), (1, 1, 16), (1, 8, 16), (2, 4, 4), (2, 2, 8), (4, 8, 2), (4, 8, 3),
+          (4, 8, 4), (4, 1, 4), (8, 8, 2), (8, 1, 2), (8, 4, 2)]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G,Hkv,QL", SHAPES)
+def test_multi_edge_lengths(pk, D, G, Hkv, QL):
+    """Lengths from exactly Q (every key is a new token) through block
+    boundaries inside the new tokens to several thousand (split over CTAs)."""
+    lens = sorted({QL, QL + 1, 15, 16, 17, 18, 31, 33, 100, 511, 513, 1025, 4098})
+    lens = [L for L in lens if L >= QL]
+    _check(pk, *_case(lens, QL, G * Hkv, Hkv, D, seed=G * 100 + Hkv * 10 + QL + D))
+
+
+@pytest.mark.parametrize("QL", [2, 3, 4, 16])
+def test_multi_piece_with_masked_columns_merges(pk, QL):
+    """One sequence of SM count + 1 (or + 2, odd) blocks: the split gives two
+    blocks to each CTA, so its last block is a piece of its own. With the
+    sequence ending 2 tokens into that block, the first Q - 2 query tokens see
+    nothing of it: their partials there are (max -inf, sum 0) and the merge
+    must drop them."""
+    nb = _sm_count() + 1
+    if nb % 2 == 0:
+        nb += 1
+    L = (nb - 1) * 16 + 2
+    G, Hkv = (1, 8) if QL == 16 else (4, 8)
+    _check(pk, *_case([L, 40], QL, G * Hkv, Hkv, 128, seed=70 + QL))
+
+
+def test_multi_llama8b_layer(pk):
+    """64 sequences, 32/8 heads, lengths U[128, 2048], 4 new tokens each (N = 128)."""
+    r = workloads.llama8b_layer()
+    _check(pk, *_case(r.lens0 + 4, 4, 32, 8, 128, seed=81))
+
+
+def test_multi_llama70b_long(pk):
+    """8 sequences, 64/8 heads, lengths U[8192, 32768], 2 new tokens each."""
+    r = workloads.llama70b_long(batch=8)
+    _check(pk, *_case(r.lens0 + 2, 2, 64, 8, 128, seed=82))
+
+
+def test_one_token_as_4d_is_bit_identical(pk):
+    """q [B][1][Hq][D] is the single-token decode."""
+    q, kc, vc, tables, lens, torch = _case([1, 17, 300, 2049], 1, 32, 8, 128, seed=83)
+    a = _decode(pk, q, kc, vc, tables, lens, torch)
+    b = _decode(pk, q[:, 0].contiguous(), kc, vc, tables, lens, torch)
+    assert torch.equal(a[:, 0].view(torch.int16), b.view(torch.int16))
+
+
+def test_multi_rows_equal_single_token_decodes(pk):
+    """Token i of Q equals the single-token decode of a sequence that ends at
+    it: the causal limit is the only difference between the rows."""
+    QL = 4
+    q, kc, vc, tables, lens, torch = _case([37, 64, 700], QL, 32, 8, 128, seed=84)
+    multi = harness.bf16_tensor_to_f64(_decode(pk, q, kc, vc, tables, lens, torch))
+    for i in range(QL):
+        li = (lens - QL + i + 1).astype(np.int32)
+        one = _decode(pk, q[:, i].contiguous(), kc, vc, tables, li, torch)
+        d = np.abs(multi[:, i] - harness.bf16_tensor_to_f64(one))
+        assert d.max() <= 2e-2 and d.mean() <= 2e-3
+
+
+def test_multi_short_sequences_are_flagged_and_zero(pk):
+    """0 < L < Q cannot hold the new tokens: zero rows and PA_DEVERR_CONTEXT_LEN;
+    L = 0 gives zero rows; the other sequences are unaffected."""
+    QL = 4
+    q, kc, vc, tables, lens, torch = _case([40, 2, 0, 50], QL, 16, 4, 128, seed=85)
+    out = torch.full_like(q, 7.0)
+    pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                 max_context_len=50, out=out)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() & DEVERR_CONTEXT_LEN
+    got = harness.bf16_tensor_to_f64(out)
+    assert not got[1].any() and not got[2].any()
+    keep = [0, 3]
+    want = oracle.paged_decode_multi(q.cpu()[keep], kc.cpu(), vc.cpu(), tables[keep], lens[keep])
+    harness.assert_close(got[keep], want)
+
+
+def test_multi_placement_invariance_bit_exact(pk):
+    import torch
+
+    q, kc, vc, tables, lens, _ = _case([300, 47, 900], 3, 16, 4, 128, seed=86)
+    NB = kc.shape[0]
+    perm = np.random.default_rng(9).permutation(NB)
+    kcb, vcb = torch.empty_like(kc), torch.empty_like(vc)
+    kcb[torch.from_numpy(perm).cuda()] = kc
+    vcb[torch.from_numpy(perm).cuda()] = vc
+    tables_b = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    a = _decode(pk, q, kc, vc, tables, lens, torch)
+    b = _decode(pk, q, kcb, vcb, tables_b, lens, torch)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_multi_unsupported_shapes_are_rejected(pk):
+    q, kc, vc, tables, lens, torch = _case([20], 3, 16, 2, 128, seed=87)  # G 8 x 4 > 16
+    with pytest.raises(pk.PagedKVError):
+        _decode(pk, q, kc, vc, tables, lens, torch)
+    q, kc, vc, tables, lens, torch = _case([20], 2, 8, 2, 128, seed=88)
+    with pytest.raises(pk.PagedKVError):
+        _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+
+
+# ---------------------------------------------------------------- fused KV write
+
+
+def _append_case(lens, QL, Hq, Hkv, seed):
+    """The new tokens' slots hold NaN before the step; k_new/v_new rows
+    b*QL + i are written at token L - QL + i."""
+    q, kc, vc, tables, lens, torch = _case(lens, QL, Hq, Hkv, 128, seed)
+    slots = []
+    for b, L in enumerate(lens):
+        for i in range(QL):
+            pos = int(L) - QL + i
+            slots.append(int(tables[b, pos // 16]) * 16 + pos % 16)
+    slots = np.array(slots, dtype=np.int64)
+    for s in slots.tolist():
+        kc[s // 16, :, s % 16] = float("nan")
+        vc[s // 16, :, s % 16] = float("nan")
+    T = len(slots)
+    kn = workloads.bf16_normal((T, Hkv, 128), seed + 11, "cuda")
+    vn = workloads.bf16_normal((T, Hkv, 128), seed + 12, "cuda")
+    return q, kc, vc, tables, lens, slots, kn, vn, torch
+
+
+@pytest.mark.parametrize("QL", [2, 4])
+def test_multi_fused_append_matches_oracle(pk, QL):
+    """The new tokens straddle block boundaries, and in the long sequence the
+    two blocks holding them go to different CTAs."""
+    nb = _sm_count() + 1
+    if nb % 2 == 0:
+        nb += 1
+    long_len = (nb - 1) * 16 + 2
+    lens = [long_len, 17, 33, 16 + QL, 500]
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case(lens, QL, 32, 8, seed=90 + QL)
+    kc2, vc2 = kc.clone(), vc.clone()
+    out = pk.pa_append_decode(q, kc2, vc2, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
+                              torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() == 0
+    ko, vo = oracle.reshape_and_cache(kn.cpu(), vn.cpu(), oracle.bf16_bits(kc.cpu()),
+                                      oracle.bf16_bits(vc.cpu()), slots)
+    assert np.array_equal(oracle.bf16_bits(kc2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
+    want = oracle.paged_decode_multi(q.cpu(), ko, vo, tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+
+
+def test_multi_fused_append_slot_rules(pk):
+    """A slot that is not its token's is not written (PA_DEVERR_APPEND_SLOT); a
+    negative slot writes nothing; the other tokens are written."""
+    QL = 3
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case([40, 70], QL, 16, 4, seed=95)
+    bad = slots.copy()
+    bad[1] = slots[1] + 1 if slots[1] % 16 != 15 else slots[1] - 1  # wrong offset
+    bad[4] = -1
+    kc2, vc2 = kc.clone(), vc.clone()
+    pk.pa_append_decode(q, kc2, vc2, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                        int(lens.max()), kn, vn, torch.from_numpy(bad).cuda())
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() & DEVERR_APPEND_SLOT
+    written = [t for t in range(len(slots)) if t not in (1, 4)]
+    ko, vo = oracle.reshape_and_cache(kn.cpu()[written], vn.cpu()[written],
+                                      oracle.bf16_bits(kc.cpu()), oracle.bf16_bits(vc.cpu()),
+                                      slots[written])
+    assert np.array_equal(oracle.bf16_bits(kc2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
+
+
+# ---------------------------------------------------------------- 8-bit cache
+
+
+def _fp8_multi_case(pk, lens, QL, Hq, Hkv, seed):
+    import torch
+
+    D = 128
+    lens = np.asarray(lens, dtype=np.int64)
+    need = int(((lens + 15) // 16).sum())
+    NB = need + 3
+    order = np.random.default_rng(seed).permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, 16)
+    q = workloads.bf16_normal((len(lens), QL, Hq, D), seed + 1, "cuda")
+    kn = workloads.bf16_normal((NB * 16, Hkv, D), seed + 2, "cuda")
+    vn = workloads.bf16_normal((NB * 16, Hkv, D), seed + 3, "cuda")
+    rng = np.random.default_rng(seed + 4)
+    ks = torch.from_numpy((0.05 * np.exp(rng.uniform(-0.5, 0.5, Hkv))).astype(np.float32)).cuda()
+    vs = torch.from_numpy((0.03 * np.exp(rng.uniform(-0.5, 0.5, Hkv))).astype(np.float32)).cuda()
+    k8 = torch.zeros((NB, Hkv, 16, D), dtype=torch.uint8, device="cuda")
+    v8 = torch.zeros((NB, Hkv, D, 16), dtype=torch.uint8, device="cuda")
+    pk.pa_reshape_and_cache_fp8(kn, vn, k8, v8, torch.arange(NB * 16, device="cuda"), ks, vs)
+    for b, L in enumerate(lens):
+        if L % 16:
+            blk = int(tables[b, (L - 1) // 16])
+            k8[blk, :, L % 16:, :] = 0x7F  # E4M3 NaN
+            v8[blk, :, :, L % 16:] = 0x7F
+    torch.cuda.synchronize()
+    return q, k8, v8, ks, vs, tables, lens.astype(np.int32), torch
+
+
+@pytest.mark.parametrize("G,Hkv,QL", [(4, 8, 2), (1, 8, 4), (2, 4, 4), (4, 4, 4), (8, 2, 2),
+                                      (4, 1, 3)])
+def test_multi_fp8_edge_lengths(pk, G, Hkv, QL):
+    lens = [L for L in (QL, 15, 16, 17, 18, 100, 513, 1025, 4098) if L >= QL]
+    q, k8, v8, ks, vs, tables, lens, torch = _fp8_multi_case(pk, lens, QL, G * Hkv, Hkv,
+                                                             seed=G * 10 + Hkv + QL)
+    out = pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=int(lens.max()), k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    want = oracle.paged_decode_multi_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy(),
+                                         ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+
+
+def test_multi_fp8_llama8b_layer(pk):
+    """64 sequences, 32/8 heads, U[128, 2048], 2 new tokens (64 columns)."""
+    r = workloads.llama8b_layer()
+    q, k8, v8, ks, vs, tables, lens, torch = _fp8_multi_case(pk, r.lens0 + 2, 2, 32, 8, seed=96)
+    out = pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=int(lens.max()), k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    want = oracle.paged_decode_multi_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy(),
+                                         ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0

@@ -648,3 +648,25 @@ def test_multi_query_brute_force_and_bad_lengths():
             np.testing.assert_allclose(got[b, i], np.array(ref), rtol=0, atol=1e-12)
     with pytest.raises(ValueError):
         oracle.paged_decode_multi(q, kc, vc, tables, np.array([2, 6], dtype=np.int32))
+
+
+def test_multi_query_fp8_equals_bf16_multi_on_the_dequantised_cache():
+    """As for one token: with power-of-two scales the dequantised cache is
+    exactly bf16, so the 8-bit multi-token decode equals the (pinned) bf16
+    multi-token decode over it."""
+    _, k8, v8, _, _, tables, lens, _, _ = _fp8_case(23, lens=(4, 6, 11), scales=(0.25, 4.0))
+    ks = np.array([0.25, 0.5], dtype=np.float32)
+    vs = np.array([4.0, 2.0], dtype=np.float32)
+    NB, Hkv, BS, D = k8.shape
+    kd = oracle.e4m3_to_f64(k8) * ks[None, :, None, None]
+    vd = (oracle.e4m3_to_f64(v8).reshape(NB, Hkv, D, BS) * vs[None, :, None, None]).transpose(0, 1, 3, 2)
+    kb = torch.from_numpy(np.ascontiguousarray(kd)).to(torch.bfloat16)
+    vb = torch.from_numpy(np.ascontiguousarray(vd)).to(torch.bfloat16)
+    q = _bf16((3, 4, 8, D), 24)
+    want = oracle.paged_decode_multi(q, kb, vb, tables, lens)
+    got = oracle.paged_decode_multi_fp8(q, k8, v8, ks, vs, tables, lens)
+    assert np.abs(got - want).max() < 1e-12
+    # one new token: the single-token 8-bit decode
+    one = oracle.paged_decode_multi_fp8(q[:, :1], k8, v8, ks, vs, tables, lens)
+    np.testing.assert_array_equal(one[:, 0], oracle.paged_decode_fp8(q[:, 0], k8, v8, ks, vs,
+                                                                      tables, lens))
