@@ -373,13 +373,14 @@ def run_ours(args, rank: int, world: int) -> dict:
                                                          overlap=not args.no_overlap, fused=fused)
         if args.variant == 0:
             res["other_workloads"].update(measure_fp8_workloads(pk, device))
+            res["other_workloads"].update(measure_multi_workloads(pk, device))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(r, W, budget_s=args.cpu_baseline_s)
     return res
 
 
 def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True, fused: bool = True,
-                            steps: int = 200, warmup: int = 10) -> dict:
+                            steps: int = 200, warmup: int = 10, only=None) -> dict:
     """The decode on the other workload shapes, measured after the main timed
     region: decode-only GB/s from CUDA events around each decode, and the
     whole step's GB/s (copy-on-write + KV write + decode) from the loop time.
@@ -396,6 +397,8 @@ def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True, 
     peak = measured_peaks()["hbm_gbs"]
     stream = torch.cuda.current_stream()
     for name, r in recipes:
+        if only is not None and name != only:
+            continue
         W = setup_workload(r, device, n_copies=2)
         plans, _, keep = make_plans(pk, W, device, variant=variant, overlap=overlap, fused=fused)
         lens = W["lens"]
@@ -467,7 +470,7 @@ class Fp8StepPlan:
             ev_dec[1].record()
 
 
-def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10) -> dict:
+def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10, only=None) -> dict:
     """The same workloads on the 8-bit (E4M3) cache: each bf16 pool copy is
     quantised into an E4M3 pool (per-KV-head scales 0.05 for K and V) through
     pa_reshape_and_cache_fp8, then timed like the bf16 runs."""
@@ -482,6 +485,8 @@ def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10) -> dic
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream or None
     for name, r in recipes:
+        if only is not None and name != only:
+            continue
         W = setup_workload(r, device, n_copies=2)
         H, D = r.num_kv_heads, r.head_dim
         ks = torch.full((H,), 0.05, dtype=torch.float32, device=device)
@@ -543,6 +548,96 @@ def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10) -> dic
             "step_gbs": round(step_b / (step_ms * 1e-3) / 1e9, 1),
         }
         del plans, keep
+        torch.cuda.empty_cache()
+    return out
+
+
+class DecodeCallPlan:
+    """One pre-marshalled pa_append_decode call (KV write fused into the decode)."""
+
+    def __init__(self, lib, dec_params, app_params, ws, stream):
+        self.lib, self.dec, self.app, self.ws, self.stream = lib, dec_params, app_params, ws, stream
+
+    def run(self, ev_dec=None):
+        if ev_dec is not None:
+            ev_dec[0].record()
+        st = self.lib.pa_append_decode(ctypes.byref(self.dec), ctypes.byref(self.app),
+                                       self.ws.data_ptr(), self.ws.numel(), self.stream)
+        if st:
+            raise RuntimeError(f"pa_append_decode failed: {st}: {self.lib.pa_last_error()}")
+        if ev_dec is not None:
+            ev_dec[1].record()
+
+
+def measure_multi_workloads(pk, device, steps: int = 200, warmup: int = 10, only=None) -> dict:
+    """Q new tokens per sequence (query_len Q, causal among them), the KV write
+    of all of them fused into the decode: the bf16 caches of the workloads
+    above, each sequence's last Q tokens being the new ones. Algorithmic
+    bytes: the decode's (K/V once per KV head, tables) with Q rows of q and
+    out per sequence, plus the new tokens' K/V written."""
+    import torch
+
+    lib = pk.load()
+    out = {}
+    cases = [("llama8b_layer_b64_q2", workloads.llama8b_layer(), 2),
+             ("llama8b_layer_b64_q4", workloads.llama8b_layer(), 4),
+             ("llama8b_high_concurrency_b256_q4", workloads.llama8b_high_concurrency(), 4),
+             ("llama70b_long_b8_q2", workloads.llama70b_long(batch=8), 2)]
+    peak = measured_peaks()["hbm_gbs"]
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream or None
+    for name, r, Q in cases:
+        if only is not None and name != only:
+            continue
+        W = setup_workload(r, device, n_copies=2)
+        H, D, Hq = r.num_kv_heads, r.head_dim, r.num_q_heads
+        lens, tables = W["lens"], W["tables"]
+        B = len(lens)
+        pos = (lens[:, None] - Q + np.arange(Q)[None, :]).reshape(-1)
+        seq = np.repeat(np.arange(B), Q)
+        slots = (tables[seq, pos // 16].astype(np.int64) * 16 + pos % 16).astype(np.int64)
+        g = torch.Generator(device="cpu").manual_seed(7)
+        q = torch.randn(B, Q, Hq, D, generator=g).to(torch.bfloat16).to(device)
+        kn = torch.randn(B * Q, H, D, generator=g).to(torch.bfloat16).to(device)
+        vn = torch.randn(B * Q, H, D, generator=g).to(torch.bfloat16).to(device)
+        tables_d = torch.from_numpy(tables).to(device)
+        lens_d = torch.from_numpy(lens).to(device)
+        slots_d = torch.from_numpy(slots).to(device)
+        o = torch.empty_like(q)
+        keep, plans = [q, kn, vn, tables_d, lens_d, slots_d, o], []
+        for kc, vc in W["copies"]:
+            p = pk.make_decode_params(q, o, kc, vc, tables_d, lens_d,
+                                      max_context_len=int(lens.max()), overlap_prologue=True)
+            a = pk.make_append_params(kn, vn, slots_d, kc, vc)
+            ws = torch.empty(pk.pa_decode_workspace_size(p), dtype=torch.uint8, device=device)
+            plans.append(DecodeCallPlan(lib, p, a, ws, sh))
+            keep.append(ws)
+        dec_b = decode_bytes(lens, Hq, H, D) + B * (Q - 1) * Hq * D * 2 * 2
+        step_b = dec_b + append_bytes(B * Q, H, D)
+        for i in range(warmup):
+            plans[i % len(plans)].run()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        for k in range(steps):
+            plans[k % len(plans)].run(evs[k])
+        torch.cuda.synchronize()
+        dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(steps):
+            plans[k % len(plans)].run()
+        b.record(stream)
+        torch.cuda.synchronize()
+        step_ms = a.elapsed_time(b) / steps
+        out[name] = {
+            "num_seqs": B, "num_q_heads": Hq, "query_len": Q,
+            "context_tokens": int(np.asarray(lens, dtype=np.int64).sum()), "bytes": step_b,
+            "decode_ms": round(dec_ms, 5), "decode_gbs": round(step_b / (dec_ms * 1e-3) / 1e9, 1),
+            "decode_frac": round(step_b / (dec_ms * 1e-3) / 1e9 / peak, 4),
+            "step_ms": round(step_ms, 5), "step_gbs": round(step_b / (step_ms * 1e-3) / 1e9, 1),
+        }
+        del plans, keep, W
         torch.cuda.empty_cache()
     return out
 
@@ -671,6 +766,27 @@ def run_reference(args) -> dict:
 
 # ----------------------------------------------------------------------------- main
 
+def run_case(args) -> int:
+    """One secondary workload alone, on cuda:0."""
+    import torch
+
+    import paged_kv_cache_92_gb300 as pk
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    pk.load()
+    kw = dict(steps=args.steps, warmup=args.warmup, only=args.case)
+    res = measure_other_workloads(pk, device, variant=args.variant, **kw)
+    if args.variant == 0:
+        res.update(measure_fp8_workloads(pk, device, **kw))
+        res.update(measure_multi_workloads(pk, device, **kw))
+    if not res:
+        print(json.dumps({"case": args.case, "error": "no such workload"}))
+        return 2
+    print(json.dumps({"case": args.case, **res[args.case]}))
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -691,6 +807,10 @@ def main(argv=None) -> int:
                          "set-up with the KV write")
     ap.add_argument("--variant", type=int, default=0, choices=[0, 1],
                     help="decode kernel: 0 tensor-core (default), 1 CUDA-core")
+    ap.add_argument("--case", default=None,
+                    help="run only this entry of other_workloads (e.g. "
+                         "llama8b_layer_b64_fp8_e4m3) for --steps steps after --warmup, and "
+                         "print its figures (for profiling one kernel; not the bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -703,6 +823,8 @@ def main(argv=None) -> int:
         print(json.dumps(run_reference(args)))
         return 0
 
+    if args.case is not None:
+        return run_case(args)
     if world > 1:
         import torch
 
