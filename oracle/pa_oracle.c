@@ -45,7 +45,9 @@
  *    infinities) to +-448, NaN to 0x7F;
  *  - read: value = decode(code) * scale[h], in double;
  *  - layout: K as the bf16 cache, [block][head][offset][d]; V transposed
- *    inside each (block, head) tile, [block][head][d][offset].
+ *    inside each (block, head) tile in sub-tiles of W = min(16, BS) keys,
+ *    [block][head][offset / W][d][offset % W] (one [d][BS] sub-tile for
+ *    BS <= 16, two [d][16] sub-tiles at BS = 32).
  */
 #include <math.h>
 #include <stdint.h>
@@ -120,6 +122,13 @@ static size_t cache_row(int64_t blk, int32_t kv_head, int32_t off, int32_t num_k
  * out_row: head_dim doubles. lse_out (nullable): log sum_i exp(score_i).
  * Returns ORACLE_OK or an error code.
  */
+/* Byte offset of V element (off, c) inside its (block, head) tile of the
+ * E4M3 cache: sub-tile off / W, row c, column off % W, W = min(16, BS). */
+static size_t vt_offset(int32_t off, int32_t c, int32_t block_size, int32_t head_dim) {
+  const int32_t w = block_size < 16 ? block_size : 16;
+  return (size_t)(off / w) * (size_t)w * head_dim + (size_t)c * w + (size_t)(off % w);
+}
+
 /* Element c of row (blk, head, off) of K and of V, as double, for a bf16
  * cache (fp8 == 0) or an E4M3 cache with per-head scales (fp8 == 1). */
 static void kv_element(const void* k_cache, const void* v_cache, int fp8, const float* k_scale,
@@ -132,10 +141,10 @@ static void kv_element(const void* k_cache, const void* v_cache, int fp8, const 
     *v = bf16_bits_to_double(((const uint16_t*)v_cache)[row + c]);
     return;
   }
-  /* V is transposed inside its (block, head) tile: [d][offset] */
+  /* V is transposed inside its (block, head) tile (sub-tiles of 16 keys) */
   const size_t tile = ((size_t)blk * num_kv_heads + g) * (size_t)block_size * head_dim;
   *k = e4m3_to_double(((const uint8_t*)k_cache)[row + c]) * (double)k_scale[g];
-  *v = e4m3_to_double(((const uint8_t*)v_cache)[tile + (size_t)c * block_size + off]) *
+  *v = e4m3_to_double(((const uint8_t*)v_cache)[tile + vt_offset(off, c, block_size, head_dim)]) *
        (double)v_scale[g];
 }
 
@@ -388,7 +397,7 @@ int oracle_reshape_and_cache_fp8(const uint16_t* k_new, const uint16_t* v_new, u
         const float kx = (float)bf16_bits_to_double(k_new[src + c]) / k_scale[h];
         const float vx = (float)bf16_bits_to_double(v_new[src + c]) / v_scale[h];
         k_cache[row + c] = e4m3_from_float(kx);
-        v_cache[tile + (size_t)c * block_size + off] = e4m3_from_float(vx);
+        v_cache[tile + vt_offset(off, c, block_size, head_dim)] = e4m3_from_float(vx);
       }
     }
   }

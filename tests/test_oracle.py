@@ -670,3 +670,38 @@ def test_multi_query_fp8_equals_bf16_multi_on_the_dequantised_cache():
     one = oracle.paged_decode_multi_fp8(q[:, :1], k8, v8, ks, vs, tables, lens)
     np.testing.assert_array_equal(one[:, 0], oracle.paged_decode_fp8(q[:, 0], k8, v8, ks, vs,
                                                                       tables, lens))
+
+
+@needs_torch_fp8
+def test_fp8_write_at_block_size_32_uses_16_key_subtiles():
+    """Block size 32: V of slot offset `off` sits in sub-tile off // 16 of its
+    (block, head) tile, row d, column off % 16 -- checked by plain numpy
+    reshapes against torch's cast -- and the decode over that cache equals the
+    bf16 oracle on the exactly dequantised cache (power-of-two scales)."""
+    BS, Hkv, D, NB = 32, 2, 16, 4
+    ks = np.array([0.25, 0.5], dtype=np.float32)
+    vs = np.array([4.0, 2.0], dtype=np.float32)
+    slots = np.arange(NB * BS, dtype=np.int64)
+    kn = _bf16((NB * BS, Hkv, D), 61)
+    vn = _bf16((NB * BS, Hkv, D), 62)
+    k8, v8 = oracle.reshape_and_cache_fp8(kn, vn, np.zeros((NB, Hkv, BS, D), np.uint8),
+                                          np.zeros((NB, Hkv, BS, D), np.uint8), slots, ks, vs)
+    vx = torch.from_numpy(oracle.bf16_to_f64(vn).astype(np.float32)) / torch.from_numpy(vs)[:, None]
+    vcode = vx.to(E4M3).view(torch.uint8).numpy()  # [slot][h][d]
+    tiles = v8.reshape(NB, Hkv, BS // 16, D, 16)
+    for slot in (0, 15, 16, 31, 77, NB * BS - 1):
+        blk, off = divmod(slot, BS)
+        for h in range(Hkv):
+            assert np.array_equal(tiles[blk, h, off // 16, :, off % 16], vcode[slot, h])
+    kd = oracle.e4m3_to_f64(k8) * ks[None, :, None, None]
+    vd = np.ascontiguousarray((oracle.e4m3_to_f64(v8).reshape(NB, Hkv, BS // 16, D, 16)
+                               * vs[None, :, None, None, None]).transpose(0, 1, 2, 4, 3)
+                              .reshape(NB, Hkv, BS, D))
+    kb = torch.from_numpy(np.ascontiguousarray(kd)).to(torch.bfloat16)
+    vb = torch.from_numpy(vd).to(torch.bfloat16)
+    tables = np.array([[2, 0], [3, 1]], dtype=np.int32)
+    lens = np.array([40, 64], dtype=np.int32)
+    q = _bf16((2, 4, D), 63)
+    want = oracle.paged_decode(q, kb, vb, tables, lens)
+    got = oracle.paged_decode_fp8(q, k8, v8, ks, vs, tables, lens)
+    assert np.abs(got - want).max() < 1e-12
