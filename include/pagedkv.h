@@ -54,8 +54,11 @@
  *  - pa_last_error() returns a thread-local message for the last failing
  *    call on that thread.
  *
- * Supported shapes: block_size 16; head_dim 64 or 128; num_q_heads /
- * num_kv_heads in {1, 2, 4, 8}. Anything else returns PA_ERR_UNSUPPORTED.
+ * Supported shapes: block_size 8, 16 or 32 ("Paged Attention as a Memory
+ * Manager", §PagedAttention: a compile-time constant, typically 8, 16 or 32);
+ * head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}. Block sizes
+ * 8 and 32 decode on the tensor-core kernel at head_dim 128 (the 8-bit cache:
+ * 16 and 32). Anything else returns PA_ERR_UNSUPPORTED.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -165,7 +168,9 @@ typedef struct {
  * block; the format is this library's reading): OCP E4M3 codes (uint8) with one
  * dequantisation scale per KV head for K and for V.
  *   k_cache  uint8 [num_blocks][num_kv_heads][block_size][head_dim]
- *   v_cache  uint8 [num_blocks][num_kv_heads][head_dim][block_size]  (V^T per tile)
+ *   v_cache  uint8 [num_blocks][num_kv_heads][block_size/16][head_dim][16]
+ *            (V^T of each (block, head) tile in sub-tiles of 16 keys; block size
+ *            16 or 32)
  * Written by pa_reshape_and_cache_fp8, copied by pa_copy_blocks_fp8. The decode
  * computes on the tensor cores (variant PA_DECODE_TENSOR_CORE, head_dim 128; the
  * rest of the tensor-core shape rules apply, other shapes return
@@ -331,11 +336,12 @@ pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t wor
  * cache: for token t and KV head h,
  *   code = E4M3(float32(x) / scale[h])   (round to nearest even; finite values
  *                                         beyond +-448 saturate)
- * K codes go to row (slot / block_size, h, slot % block_size); V codes to
- * column slot % block_size of the tile [h][d][offset] of block slot /
- * block_size. k_scale, v_scale: device float [num_kv_heads]. Otherwise as
- * pa_reshape_and_cache (negative slots skipped, out-of-range slots set
- * PA_DEVERR_SLOT). head_dim a multiple of 8.
+ * K codes go to row (slot / block_size, h, slot % block_size); the V code of
+ * offset o = slot % block_size, element d, to byte d*16 + o%16 of sub-tile
+ * o/16 of the (block, h) tile. k_scale, v_scale: device float
+ * [num_kv_heads]. Otherwise as pa_reshape_and_cache (negative slots skipped,
+ * out-of-range slots set PA_DEVERR_SLOT). head_dim a multiple of 8; block_size
+ * 16 or 32.
  * ---------------------------------------------------------------------- */
 pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_cache,
                                    void* v_cache, const int64_t* slot_mapping,
@@ -344,7 +350,7 @@ pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k
                                    int32_t block_size, int32_t num_blocks, pa_stream_t stream);
 
 /* pa_copy_blocks for an 8-bit cache: the same whole-block copy of both caches
- * (block_size * head_dim bytes per KV head). */
+ * (block_size * head_dim bytes per KV head); block_size 16 or 32. */
 pa_status pa_copy_blocks_fp8(void* k_cache, void* v_cache, const int32_t* pairs,
                              int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
                              int32_t block_size, int32_t num_blocks, pa_stream_t stream);

@@ -214,8 +214,8 @@ def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
     """Marshal a pa_decode call. q and out are bf16 [B][Hq][D] (one new token
     per sequence) or [B][Q][Hq][D] (Q new tokens per sequence, causal among
     them). bf16 caches [NB][Hkv][BS][D]; uint8 caches are the 8-bit E4M3 cache
-    (K [NB][Hkv][BS][D], V^T [NB][Hkv][D][BS]) and need k_scale / v_scale,
-    float32 CUDA tensors [Hkv]."""
+    (K [NB][Hkv][BS][D], V^T in 16-key sub-tiles [NB][Hkv][BS/16][D][16]) and
+    need k_scale / v_scale, float32 CUDA tensors [Hkv]."""
     import torch
 
     if q.dim() == 4:
@@ -224,8 +224,9 @@ def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
         (B, Hq, D), QL = q.shape, 0
     fp8 = k_cache.dtype == torch.uint8
     NB, Hkv, BS, D2 = k_cache.shape
-    v_want = (NB, Hkv, D2, BS) if fp8 else tuple(k_cache.shape)
-    if D2 != D or tuple(v_cache.shape) != v_want or tuple(out.shape) != tuple(q.shape):
+    v_ok = tuple(v_cache.shape) in fp8_v_shapes(NB, Hkv, BS, D2) if fp8 else \
+        tuple(v_cache.shape) == tuple(k_cache.shape)
+    if D2 != D or not v_ok or tuple(out.shape) != tuple(q.shape):
         raise ValueError("shape mismatch between q / out / k_cache / v_cache")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
@@ -452,15 +453,26 @@ def pa_copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
         _stream_handle(stream)), "pa_copy_blocks")
 
 
+def fp8_v_shapes(NB: int, Hkv: int, BS: int, D: int):
+    """Shapes accepted for the 8-bit V^T cache: [NB][Hkv][BS/16][D][16] (16-key
+    sub-tiles), and for block size 16 also [NB][Hkv][D][16]."""
+    shapes = [(NB, Hkv, BS // 16, D, 16)]
+    if BS == 16:
+        shapes.append((NB, Hkv, D, 16))
+    return shapes
+
+
 def pa_reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale, v_scale,
                              stream=None) -> None:
-    """KV write into the 8-bit cache (uint8 K [NB][Hkv][BS][D], V^T [NB][Hkv][D][BS])."""
+    """KV write into the 8-bit cache (uint8 K [NB][Hkv][BS][D], V^T in 16-key
+    sub-tiles [NB][Hkv][BS/16][D][16])."""
     import torch
 
     T, Hkv, D = k_new.shape
     NB, Hkv2, BS, D2 = k_cache.shape
     if (Hkv2, D2) != (Hkv, D) or tuple(v_new.shape) != tuple(k_new.shape) \
-            or tuple(v_cache.shape) != (NB, Hkv, D, BS) or tuple(slot_mapping.shape) != (T,):
+            or tuple(v_cache.shape) not in fp8_v_shapes(NB, Hkv, BS, D) \
+            or tuple(slot_mapping.shape) != (T,):
         raise ValueError("shape mismatch in pa_reshape_and_cache_fp8")
     lib = load()
     _check(lib.pa_reshape_and_cache_fp8(

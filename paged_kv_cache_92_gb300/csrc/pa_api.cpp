@@ -32,8 +32,8 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
                      "pa_decode: num_q_heads must be a positive multiple of num_kv_heads");
   if (p->num_kv_heads > 65535)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: num_kv_heads must be <= 65535");
-  if (p->block_size != kBlockSize)
-    return set_error(PA_ERR_UNSUPPORTED, "pa_decode: only block_size 16 is built");
+  if (!block_size_ok(p->block_size))
+    return set_error(PA_ERR_UNSUPPORTED, "pa_decode: block_size must be 8, 16 or 32");
   if (p->head_dim != 64 && p->head_dim != 128)
     return set_error(PA_ERR_UNSUPPORTED, "pa_decode: head_dim must be 64 or 128");
   const int g = p->num_q_heads / p->num_kv_heads;
@@ -44,7 +44,7 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq < 1");
   if (p->max_context_len < 1)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_context_len < 1");
-  if (int64_t(p->max_blocks_per_seq) * kBlockSize > INT32_MAX)
+  if (int64_t(p->max_blocks_per_seq) * p->block_size > INT32_MAX)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq too large");
   const int pt = resolve_partition_tokens(p);
   if (pt < kBlockSize || pt > kMaxPartitionTokens || pt % kBlockSize != 0)
@@ -52,7 +52,7 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
                      "pa_decode: partition_tokens must be 0 or a multiple of 16 in [16, 4096]");
   if (p->variant != PA_DECODE_TENSOR_CORE && p->variant != PA_DECODE_CUDA_CORE)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: variant must be 0 (tensor core) or 1 (CUDA core)");
-  if (int64_t(p->num_blocks) * p->num_kv_heads * kBlockSize >= (int64_t(1) << 31) - 16 ||
+  if (int64_t(p->num_blocks) * p->num_kv_heads * p->block_size >= (int64_t(1) << 31) - 16 ||
       int64_t(p->num_seqs) * p->num_q_heads >= (int64_t(1) << 31) - 16)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: cache or query rows exceed 2^31");
   if (!(p->scale > 0.0f) || p->scale != p->scale)
@@ -63,6 +63,11 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: query_len must be in [0, 1024]");
   if (int64_t(p->num_seqs) * query_len_of(p) * p->num_q_heads >= (int64_t(1) << 31) - 16)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: query rows exceed 2^31");
+  if (p->block_size != kBlockSize && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
+    return set_error(PA_ERR_UNSUPPORTED,
+                     "pa_decode: block_size 8 and 32 run on the tensor-core kernel (head_dim 128, "
+                     "num_kv_heads 1/2/4/8; block_size 8: at most 8 query columns per KV head and "
+                     "the bf16 cache only)");
   if (query_len_of(p) > 1 && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
     return set_error(PA_ERR_UNSUPPORTED,
                      "pa_decode: query_len > 1 runs on the tensor-core kernel with num_kv_heads "
@@ -95,7 +100,7 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
 
 int num_partitions_for(const pa_decode_params* p) {
   const int pt = resolve_partition_tokens(p);
-  int64_t cap = int64_t(p->max_blocks_per_seq) * kBlockSize;
+  int64_t cap = int64_t(p->max_blocks_per_seq) * p->block_size;
   int64_t mx = p->max_context_len < cap ? p->max_context_len : cap;
   return int((mx + pt - 1) / pt);
 }
@@ -171,19 +176,21 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
     e = launch_decode_tc(L, stream);
   } else if (p->kv_dtype == PA_KV_FP8_E4M3) {
     return set_error(PA_ERR_UNSUPPORTED, "the 8-bit cache needs the tensor-core kernel");
-  } else if (query_len_of(p) > 1) {
-    return set_error(PA_ERR_UNSUPPORTED, "query_len > 1 needs the tensor-core kernel");
+  } else if (query_len_of(p) > 1 || p->block_size != kBlockSize) {
+    return set_error(PA_ERR_UNSUPPORTED,
+                     "query_len > 1 and block sizes other than 16 need the tensor-core kernel");
   } else {
     if (append) {  // the same effect in two launches
       AppendCheck chk;
       chk.block_tables = p->block_tables;
       chk.context_lens = p->context_lens;
       chk.max_blocks_per_seq = p->max_blocks_per_seq;
-      chk.cap = p->max_blocks_per_seq * kBlockSize < p->max_context_len
-                    ? p->max_blocks_per_seq * kBlockSize : p->max_context_len;
+      chk.cap = p->max_blocks_per_seq * p->block_size < p->max_context_len
+                    ? p->max_blocks_per_seq * p->block_size : p->max_context_len;
       e = launch_reshape_and_cache(append->k_new, append->v_new, append->k_cache,
                                    append->v_cache, append->slot_mapping, p->num_seqs,
-                                   p->num_kv_heads, p->head_dim, p->num_blocks, stream, chk);
+                                   p->num_kv_heads, p->head_dim, p->block_size, p->num_blocks,
+                                   stream, chk);
     }
     if (e) {
       std::snprintf(where, sizeof(where), "%s: launch", who);
@@ -426,7 +433,7 @@ pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t wor
     const int r = pa::launch_copy_blocks(p->k_cache, p->v_cache,
                                          reinterpret_cast<const int32_t*>(ws + sp.in.cow_pairs),
                                          p->num_cow_pairs, p->num_kv_heads, p->head_dim,
-                                         p->num_blocks, stream);
+                                         p->block_size, p->num_blocks, stream);
     if (r != 0) return pa::set_cuda_error("pa_step_host: copy_blocks launch", r);
   }
   if (p->num_seqs > 0) {
@@ -456,8 +463,8 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cac
   if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1)
     return pa::set_error(PA_ERR_INVALID_ARG,
                          "pa_reshape_and_cache: num_tokens >= 0, num_kv_heads >= 1, num_blocks >= 1");
-  if (block_size != pa::kBlockSize)
-    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache: only block_size 16 is built");
+  if (!pa::block_size_ok(block_size))
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache: block_size must be 8, 16 or 32");
   if (head_dim < 8 || head_dim % 8 != 0 || head_dim > 1024)
     return pa::set_error(PA_ERR_UNSUPPORTED,
                          "pa_reshape_and_cache: head_dim must be a multiple of 8 in [8, 1024]");
@@ -471,7 +478,8 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cac
   if (int64_t(num_tokens) * num_kv_heads * (head_dim / 8) > (int64_t(1) << 38))
     return pa::set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: too many tokens");
   const int e = pa::launch_reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping,
-                                             num_tokens, num_kv_heads, head_dim, num_blocks, stream);
+                                             num_tokens, num_kv_heads, head_dim, block_size,
+                                             num_blocks, stream);
   if (e != 0) return pa::set_cuda_error("pa_reshape_and_cache: launch", e);
   return PA_OK;
 }
@@ -485,8 +493,8 @@ pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k
     return pa::set_error(PA_ERR_INVALID_ARG,
                          "pa_reshape_and_cache_fp8: num_tokens >= 0, num_kv_heads >= 1, "
                          "num_blocks >= 1");
-  if (block_size != pa::kBlockSize)
-    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache_fp8: only block_size 16");
+  if (block_size != 16 && block_size != 32)
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache_fp8: block_size 16 or 32");
   if (head_dim < 8 || head_dim % 8 != 0 || head_dim > 1024)
     return pa::set_error(PA_ERR_UNSUPPORTED,
                          "pa_reshape_and_cache_fp8: head_dim must be a multiple of 8 in [8, 1024]");
@@ -501,7 +509,7 @@ pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k
     return pa::set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache_fp8: too many tokens");
   const int e = pa::launch_reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping,
                                                  k_scale, v_scale, num_tokens, num_kv_heads,
-                                                 head_dim, num_blocks, stream);
+                                                 head_dim, block_size, num_blocks, stream);
   if (e != 0) return pa::set_cuda_error("pa_reshape_and_cache_fp8: launch", e);
   return PA_OK;
 }
@@ -511,6 +519,8 @@ pa_status pa_copy_blocks_fp8(void* k_cache, void* v_cache, const int32_t* pairs,
                              int32_t block_size, int32_t num_blocks, pa_stream_t stream) {
   if (head_dim % 16 != 0)
     return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: head_dim must be a multiple of 16");
+  if (block_size != 16 && block_size != 32)
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: block_size 16 or 32");
   // one byte per element: the same bytes as a bf16 block of head_dim / 2
   return pa_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_kv_heads, head_dim / 2, block_size,
                         num_blocks, stream);
@@ -522,8 +532,8 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int
   if (num_pairs < 0 || num_pairs > 65535 || num_kv_heads < 1 || num_blocks < 1)
     return pa::set_error(PA_ERR_INVALID_ARG,
                          "pa_copy_blocks: num_pairs in [0, 65535], num_kv_heads >= 1, num_blocks >= 1");
-  if (block_size != pa::kBlockSize)
-    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks: only block_size 16 is built");
+  if (!pa::block_size_ok(block_size))
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks: block_size must be 8, 16 or 32");
   if (head_dim < 8 || head_dim % 8 != 0 || head_dim > 1024)
     return pa::set_error(PA_ERR_UNSUPPORTED,
                          "pa_copy_blocks: head_dim must be a multiple of 8 in [8, 1024]");
@@ -534,7 +544,7 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int
       (reinterpret_cast<uintptr_t>(pairs) & 3u))
     return pa::set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: misaligned pointer");
   const int e = pa::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_kv_heads, head_dim,
-                                       num_blocks, stream);
+                                       block_size, num_blocks, stream);
   if (e != 0) return pa::set_cuda_error("pa_copy_blocks: launch", e);
   return PA_OK;
 }

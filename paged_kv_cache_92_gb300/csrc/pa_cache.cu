@@ -6,7 +6,9 @@
 // Sources: "How Paged Attention and Continuous Batching Actually Work",
 // §One step, end to end (write KV through the slot-mapping formula);
 // "Paged Attention as a Memory Manager", §Prefix Caching and Copy-on-Write
-// (allocate a fresh block, copy the existing content).
+// (allocate a fresh block, copy the existing content). The block size is a
+// power of two ("Paged Attention as a Memory Manager", §PagedAttention: 8, 16
+// or 32 tokens); slots split into (block, offset) by shift and mask.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -19,15 +21,14 @@ namespace {
 
 __device__ unsigned int g_cache_errors;
 
-constexpr int BS = kBlockSize;
-
 // One thread per 16-byte chunk of one (token, KV head) row, for K and V.
 __global__ void __launch_bounds__(256)
     reshape_and_cache_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                              uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                              const int64_t* __restrict__ slot_mapping, int64_t num_chunks,
-                             int num_kv_heads, int chunks_per_row, int64_t num_slots,
+                             int num_kv_heads, int chunks_per_row, int64_t num_slots, int bs_log2,
                              AppendCheck check) {
+  const int BS = 1 << bs_log2;
   // a decode launched as a programmatic dependent may start its set-up now;
   // it waits for this kernel before it reads the cache
   dev::griddep_launch_dependents();
@@ -52,8 +53,8 @@ __global__ void __launch_bounds__(256)
       return;
     }
   }
-  const int64_t blk = slot / BS;
-  const int64_t off = slot % BS;
+  const int64_t blk = slot >> bs_log2;
+  const int64_t off = slot & (BS - 1);
   const int64_t dst = ((blk * num_kv_heads + h) * BS + off) * chunks_per_row + c;
   k_cache[dst] = k_new[idx];
   v_cache[dst] = v_new[idx];
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(256)
 
 int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
-                             int32_t head_dim, int32_t num_blocks, void* stream,
+                             int32_t head_dim, int32_t block_size, int32_t num_blocks, void* stream,
                              const AppendCheck& check) {
   const int chunks_per_row = head_dim * 2 / 16;
   const int64_t num_chunks = int64_t(num_tokens) * num_kv_heads * chunks_per_row;
@@ -92,14 +93,15 @@ int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache
   reshape_and_cache_kernel<<<unsigned(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_chunks,
-      num_kv_heads, chunks_per_row, int64_t(num_blocks) * BS, check);
+      num_kv_heads, chunks_per_row, int64_t(num_blocks) * block_size, log2_of(block_size), check);
   return int(cudaGetLastError());
 }
 
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
-                       int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, void* stream) {
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int32_t num_blocks, void* stream) {
   if (num_pairs == 0) return int(cudaSuccess);
-  const int64_t block_chunks = int64_t(num_kv_heads) * BS * head_dim * 2 / 16;
+  const int64_t block_chunks = int64_t(num_kv_heads) * block_size * head_dim * 2 / 16;
   const int threads = 256;
   int64_t gx = (block_chunks + threads - 1) / threads;
   if (gx > 64) gx = 64;

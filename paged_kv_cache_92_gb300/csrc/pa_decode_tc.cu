@@ -1,6 +1,7 @@
-// Tensor-core paged decode: the bf16 head_dim 128 instances and the entry
-// points shared by all instances (shape rules, grid, dispatch, error words).
-// The kernels themselves are in pa_decode_tc.cuh.
+// Tensor-core paged decode: the bf16 head_dim 128 block-size-16 instances and
+// the entry points shared by all instances (shape rules, grid, dispatch by
+// block size and cache type, error words). The kernels themselves are in
+// pa_decode_tc.cuh.
 #include "pa_decode_tc.cuh"
 
 namespace pa {
@@ -11,8 +12,12 @@ bool tc_supports(const pa_decode_params* p) {
   if (!(H == 1 || H == 2 || H == 4 || H == 8) || !(G == 1 || G == 2 || G == 4 || G == 8) ||
       p->num_seqs > kTcMaxSeqs || query_len_of(p) > kMaxGE)
     return false;
-  return tc_group_cols(p) <= kMaxGE &&
-         tc_cols(p) <= (p->kv_dtype == PA_KV_FP8_E4M3 ? 64 : 128);
+  const bool fp8 = p->kv_dtype == PA_KV_FP8_E4M3;
+  if (p->block_size != 16) {  // block sizes 8 and 32: head_dim 128
+    if (p->head_dim != 128 || (p->block_size == 8 && (fp8 || tc_group_cols(p) > 8)))
+      return false;
+  }
+  return tc_group_cols(p) <= kMaxGE && tc_cols(p) <= (fp8 ? 64 : 128);
 }
 
 int tc_grid() {
@@ -28,21 +33,35 @@ int tc_grid() {
 
 int launch_decode_tc(const DecodeLaunch& Lc, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (Lc.p->kv_dtype == PA_KV_FP8_E4M3)
-    return Lc.p->head_dim == 128 ? launch_decode_tc_fp8(Lc, s) : int(cudaErrorInvalidValue);
-  switch (Lc.p->head_dim) {
-    case 64: return launch_decode_tc_d64(Lc, s);
-    case 128: return dispatch_tc<128, false>(Lc, s);
+  const pa_decode_params* p = Lc.p;
+  const bool fp8 = p->kv_dtype == PA_KV_FP8_E4M3;
+  switch (p->block_size) {
+    case 8:
+      return !fp8 && p->head_dim == 128 ? launch_decode_tc_bs8(Lc, s) : int(cudaErrorInvalidValue);
+    case 32:
+      if (p->head_dim != 128) return int(cudaErrorInvalidValue);
+      return fp8 ? launch_decode_tc_bs32_fp8(Lc, s) : launch_decode_tc_bs32(Lc, s);
+    case 16:
+      if (fp8)
+        return p->head_dim == 128 ? launch_decode_tc_fp8(Lc, s) : int(cudaErrorInvalidValue);
+      switch (p->head_dim) {
+        case 64: return launch_decode_tc_d64(Lc, s);
+        case 128: return dispatch_tc<128, false, 16>(Lc, s);
+        default: return int(cudaErrorInvalidValue);
+      }
     default: return int(cudaErrorInvalidValue);
   }
 }
 
 int read_and_clear_decode_tc_errors(uint32_t* flags) {
-  uint32_t a = 0, b = 0, c = 0;
-  int r = read_and_clear_tc_error_word(&a);
-  if (r == 0) r = read_and_clear_decode_tc_d64_errors(&b);
-  if (r == 0) r = read_and_clear_decode_tc_fp8_errors(&c);
-  *flags = a | b | c;
+  uint32_t f[6] = {};
+  int r = read_and_clear_tc_error_word(&f[0]);
+  if (r == 0) r = read_and_clear_decode_tc_d64_errors(&f[1]);
+  if (r == 0) r = read_and_clear_decode_tc_fp8_errors(&f[2]);
+  if (r == 0) r = read_and_clear_decode_tc_bs8_errors(&f[3]);
+  if (r == 0) r = read_and_clear_decode_tc_bs32_errors(&f[4]);
+  if (r == 0) r = read_and_clear_decode_tc_bs32_fp8_errors(&f[5]);
+  *flags = f[0] | f[1] | f[2] | f[3] | f[4] | f[5];
   return r;
 }
 

@@ -68,14 +68,22 @@ namespace {
 
 __device__ unsigned int g_tc_errors;
 
-constexpr int BS = kBlockSize;
 constexpr int ROWS = 128;      // rows of a chunk = MMA M
 constexpr int NCONS = 4;       // softmax (consumer) warps 0-3
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int NTHREADS = 6 * 32;
 constexpr int kCons = NCONS * 32;
-constexpr int kGroups = ROWS / BS;  // 16-row groups per chunk: (block, KV head)
+// A chunk's rows come in groups of GB = min(block size, 16) keys of one KV
+// head. Its "units" (the stream-K grain) are blocks, or for block size 32 the
+// 16-token halves of a block, each with all its KV heads.
+template <int BS>
+struct Units {
+  static constexpr int GB = BS < 16 ? BS : 16;  // rows of one (unit, KV head) group, tokens per unit
+  static constexpr int VS = BS / GB;            // units per block (1, or 2 at block size 32)
+  static constexpr int GROUPS = ROWS / GB;      // groups per chunk
+};
+constexpr int kF8Tile = 16;  // keys of one 8-bit V^T sub-tile
 constexpr int kMaxDynSmem = 232448;
 constexpr float kLog2e = 1.4426950408889634f;
 // The softmax reference maximum moves only when a score exceeds it by more
@@ -106,8 +114,8 @@ struct TcCfg {
   static constexpr int HALVES = F8 ? 1 : D / 64;   // 128-byte swizzle atoms per K row
   static constexpr int HALF_BYTES = ROWS * 128;    // [128 rows][64 bf16] or [128 rows][128 e4m3]
   static constexpr int K_BYTES = HALVES * HALF_BYTES;
-  static constexpr int VT_TILE = D * BS;           // F8: one [D][16] V^T tile, bytes
-  static constexpr int V_BYTES = F8 ? kGroups * VT_TILE : K_BYTES;
+  static constexpr int VT_TILE = D * kF8Tile;     // F8: one [D][16] V^T sub-tile, bytes
+  static constexpr int V_BYTES = F8 ? (ROWS / kF8Tile) * VT_TILE : K_BYTES;
   static constexpr int SLOT_BYTES = K_BYTES + V_BYTES;  // K then V
   static constexpr int QH_BYTES = N * 128;         // [N rows][64 bf16] or [N rows][128 e4m3]
   static constexpr int Q_BYTES = F8 ? 2 * QH_BYTES : HALVES * QH_BYTES;  // F8: hi, lo
@@ -137,9 +145,10 @@ struct TcCfg {
   static constexpr int NBARS = 2 * ST + 10;
   static constexpr int OFF_BARS = OFF_MISC;
   static constexpr int OFF_META = OFF_BARS + (NBARS * 8 + 15) / 16 * 16;
-  static constexpr int OFF_RED = OFF_META + ST * int(sizeof(ChunkMeta));  // [8 groups][kMaxGE]
-  static constexpr int OFF_RED2 = OFF_RED + kGroups * kMaxGE * 4;            // [8 groups][kMaxGE]
-  static constexpr int OFF_ALPHA = OFF_RED2 + kGroups * kMaxGE * 4;          // [128] by column
+  // red, red2: [groups][128 / groups] (8 groups of 16 columns, or 16 of 8)
+  static constexpr int OFF_RED = OFF_META + ST * int(sizeof(ChunkMeta));
+  static constexpr int OFF_RED2 = OFF_RED + 128 * 4;
+  static constexpr int OFF_ALPHA = OFF_RED2 + 128 * 4;                       // [128] by column
   static constexpr int OFF_LS = OFF_ALPHA + 128 * 4;                         // [128]
   static constexpr int OFF_MS = OFF_LS + 128 * 4;                            // [128]
   static constexpr int OFF_WORDS = OFF_MS + 128 * 4;
@@ -183,7 +192,9 @@ struct TcParams {
   const float* v_scale;
   const float* q_inv_alpha;
   int max_blocks_per_seq, num_seqs, num_kv_heads, num_q_heads, num_blocks, cap, oob_row;
-  int oob_row_v;   // 8-bit cache: first row past the V^T tensor map
+  int oob_row_v;   // 8-bit cache: first V^T tile past the tensor map
+  // (oob_row: the first K/V row past the tensor map -- or, for block size 32,
+  // the first (block, head) tile past it)
   int q_rows;      // rows of one sequence's queries in the Q tensor map
   // Column layout: KV head g owns columns [g*GE, (g+1)*GE); column g*GE + r is
   // query token r >> g_log2 of query head g*G + (r & (G-1)), unused when that
@@ -362,10 +373,16 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
 // across the chunk's groups of the same KV head), fold chunk r-1's O^T into
 // the accumulators, write P and signal the MMA warp.
 // ---------------------------------------------------------------------------
-template <int D, int GE, int N, bool F8>
+template <int D, int GE, int N, bool F8, int BS>
 struct Softmax {
   using C = TcCfg<D, N, F8>;
-  static constexpr int LDC = 2 * GE <= 8 ? 8 : 2 * GE;  // score columns a warp reads (two heads)
+  static constexpr int GB = Units<BS>::GB;          // rows of one (unit, KV head) group
+  static constexpr int GROUPS = Units<BS>::GROUPS;  // groups per chunk
+  static constexpr int WG = 32 / GB;                // groups per warp (2, or 4 at GB 8)
+  static constexpr int KRED = 128 / GROUPS;         // columns per group in red, red2
+  static_assert(GE <= KRED, "columns per KV head");
+  // score columns a warp reads: the GE columns of each of its groups' heads
+  static constexpr int LDC = WG * GE <= 8 ? 8 : WG * GE;
   // O^T columns per TMEM round trip (the 8-bit epilogue holds a second,
   // lo-term block beside them)
   static constexpr int CW = N <= (F8 ? 32 : 64) ? N : 32;
@@ -382,13 +399,16 @@ struct Softmax {
     const int cw = ctid >> 5, lane = ctid & 31;
     const int H = P.num_kv_heads;
     const int NC = P.num_cols;
-    const int U = kGroups / H;
-    const int grp = ctid >> 4;  // (block u, KV head h) group of this row
+    const int U = GROUPS / H;  // units per chunk
+    const int grp = ctid / GB;  // (unit u, KV head h) group of this row
     const int u = grp / H, h = grp - (grp / H) * H;
-    const int key = ctid & 15;
-    const int h0 = (2 * cw) % H;  // the warp's first head
-    const int col0 = H >= 2 ? h0 * GE : 0;
-    const bool upper = H >= 2 && lane >= 16;  // this lane's head is the warp's second
+    const int key = ctid % GB;
+    // The warp's groups hold min(H, WG) consecutive heads from h0 (all H of
+    // them, repeated, when H < WG); this lane's head is the slice-th of them.
+    const int HW = H < WG ? H : WG;
+    const int h0 = (WG * cw) % H;
+    const int col0 = h0 * GE;
+    const int slice = (lane / GB) % HW;
     const uint32_t t_lane = uint32_t(cw * 32) << 16;
     const uint32_t tO = tmem + t_lane + C::kSBufs * C::NS;  // F8: + N for the lo terms
 
@@ -448,7 +468,7 @@ struct Softmax {
       }
 
       // ---- scaled scores; row = (block u, head h, key)
-      const int t = m.tok0 + u * BS + key;
+      const int t = m.tok0 + u * GB + key;
       const bool row_in = u < m.nblk;           // the row holds cache data
       const bool valid = row_in && t < m.L;     // a token of the sequence
       // Causal limit: column j holds query token i = j >> g_log2, the
@@ -459,7 +479,12 @@ struct Softmax {
       bool need = false;
 #pragma unroll
       for (int j = 0; j < GE; ++j) {
-        const float sj = upper ? s[GE + j] : s[j];
+        float sj;
+        if constexpr (WG == 2) {
+          sj = slice ? s[GE + j] : s[j];
+        } else {
+          sj = slice == 0 ? s[j] : slice == 1 ? s[GE + j] : slice == 2 ? s[2 * GE + j] : s[3 * GE + j];
+        }
         float f = P.scale_log2;
         if constexpr (F8)  // the head's K scale and the query term's 1/alpha
           f *= kvscale[h] * qalpha[m.qslot * 64 + h * GE + j];
@@ -477,19 +502,19 @@ struct Softmax {
         for (int j = 0; j < GE; ++j) {
           float v = x[j];
 #pragma unroll
-          for (int o = 8; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          for (int o = GB / 2; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
           cm[j] = v;
         }
-        if (U > 1) {  // the head's rows span several 16-row groups of the chunk
+        if (U > 1) {  // the head's rows span several groups of the chunk
           if (key == 0) {
 #pragma unroll
-            for (int j = 0; j < GE; ++j) red[grp * kMaxGE + j] = cm[j];
+            for (int j = 0; j < GE; ++j) red[grp * KRED + j] = cm[j];
           }
           dev::named_barrier(1, kCons);
 #pragma unroll
           for (int j = 0; j < GE; ++j) {
             float v = -INFINITY;
-            for (int uu = 0; uu < U; ++uu) v = fmaxf(v, red[(uu * H + h) * kMaxGE + j]);
+            for (int uu = 0; uu < U; ++uu) v = fmaxf(v, red[(uu * H + h) * KRED + j]);
             cm[j] = v;
           }
         }
@@ -548,10 +573,10 @@ struct Softmax {
       // 0 * V = 0.
       if (!valid && row_in) {
         unsigned char* kv = ring + size_t(slot) * C::SLOT_BYTES;
-        if constexpr (F8) {  // the key is column `key` of its [D][16] V^T tile
-          unsigned char* tile = kv + C::K_BYTES + grp * C::VT_TILE + key;
+        if constexpr (F8) {  // row r is column r % 16 of [D][16] V^T sub-tile r / 16
+          unsigned char* tile = kv + C::K_BYTES + (ctid / kF8Tile) * C::VT_TILE + ctid % kF8Tile;
 #pragma unroll 16
-          for (int d = 0; d < D; ++d) tile[d * BS] = 0;
+          for (int d = 0; d < D; ++d) tile[d * kF8Tile] = 0;
         } else {
 #pragma unroll
           for (int hf = 0; hf < C::HALVES; ++hf) {
@@ -572,15 +597,15 @@ struct Softmax {
         for (int j = 0; j < GE; ++j) {
           float v = l_part[j];
 #pragma unroll
-          for (int o2 = 8; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
-          if (key == 0) red2[grp * kMaxGE + j] = v;
+          for (int o2 = GB / 2; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+          if (key == 0) red2[grp * KRED + j] = v;
         }
         dev::named_barrier(1, kCons);
         if (u == 0 && key == 0) {
 #pragma unroll
           for (int j = 0; j < GE; ++j) {
             float l = 0.0f;
-            for (int uu = 0; uu < U; ++uu) l += red2[(uu * H + h) * kMaxGE + j];
+            for (int uu = 0; uu < U; ++uu) l += red2[(uu * H + h) * KRED + j];
             l_s[h * GE + j] = l;
             m_s[h * GE + j] = m_ref[j];
           }
@@ -647,12 +672,13 @@ struct Softmax {
   }
 };
 
-template <int D, int GE, int N, bool F8>
+template <int D, int GE, int N, bool F8, int BS>
 __global__ void __launch_bounds__(NTHREADS, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, const TcParams P) {
   using C = TcCfg<D, N, F8>;
+  static_assert(!F8 || BS >= 16, "the 8-bit V^T sub-tiles hold 16 keys");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -686,6 +712,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int B = P.num_seqs;
   const int H = P.num_kv_heads;
+  constexpr int UT = Units<BS>::GB;  // tokens per unit (the stream-K grain)
+  constexpr int VS = Units<BS>::VS;  // units per block
 
   if (tid == 0) {
     for (int i = 0; i < C::ST; ++i) {
@@ -708,7 +736,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   for (int i = tid; i < C::PB * C::P_BYTES / 16; i += NTHREADS)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
 
-  // ---- stream-K plan (uses the still-empty ring as scratch): block counts of
+  // ---- stream-K plan (uses the still-empty ring as scratch): unit counts of
   // the sequences, their exclusive prefix, this CTA's range of the stream.
   int* pre = reinterpret_cast<int*>(ring);
   {
@@ -720,7 +748,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (blockIdx.x == 0 && (L0 > P.cap || (L0 > 0 && L0 < P.q_len)))
         atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
       const int L = seq_len(P, b);
-      local += (L + BS - 1) / BS;
+      local += (L + UT - 1) / UT;
     }
     int incl = local;
 #pragma unroll
@@ -734,7 +762,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int w = 0; w < warp; ++w) run += reinterpret_cast<int*>(red)[w];
     for (int b = b0; b < b1; ++b) {
       pre[b] = run;
-      run += (seq_len(P, b) + BS - 1) / BS;
+      run += (seq_len(P, b) + UT - 1) / UT;
     }
     if (tid == NTHREADS - 1) pre[B] = run;
   }
@@ -745,7 +773,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int u1 = min(total, u0 + R);
   int b_start = 0;
   if (u0 < u1) {
-    int lo = 0, hi = B;  // largest b with pre[b] <= u0: the sequence holding block u0
+    int lo = 0, hi = B;  // largest b with pre[b] <= u0: the sequence holding unit u0
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (pre[mid] <= u0) lo = mid; else hi = mid;
@@ -764,7 +792,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // waiting; the producer also fetches its first block-table window first.
   int win0 = -1, len0 = 0;
   if (warp == kProducerWarp && u0 < u1) {
-    const int j = off_start + lane;
+    const int j = (off_start + lane) / VS;  // the block of unit off_start + lane
     win0 = j < P.max_blocks_per_seq
                ? P.block_tables[size_t(b_start) * P.max_blocks_per_seq + j] : -1;
     len0 = seq_len(P, b_start);
@@ -791,26 +819,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       dev::prefetch_tmap(&tm_q);
     }
     const uint64_t pol = dev::l2_evict_first_policy();
-    const int U = kGroups / H;   // blocks per chunk
-    const int grows = BS * H;    // rows of one block (all KV heads)
+    const int U = Units<BS>::GROUPS / H;  // units per chunk
+    const int grows = UT * H;              // rows of one unit (all KV heads)
     int chunk_seq = 0, seg_seq = 0;
     bool ok = true;
-    // block-table window: lane j holds the entry of block first_block + j
-    auto load_window = [&](int b, int first_block) {
-      const int j = first_block + lane;
+    // block-table window: lane j holds the entry of the block of unit first_unit + j
+    auto load_window = [&](int b, int first_unit) {
+      const int j = (first_unit + lane) / VS;
       return (b < B && j < P.max_blocks_per_seq)
                  ? P.block_tables[size_t(b) * P.max_blocks_per_seq + j] : -1;
     };
     // Fused KV append: sequence b's new tokens (its last q_len, tokens
     // L-q_len .. L-1; row b*q_len + i of k_new/v_new/slot_mapping) are
     // written by the pieces that read their blocks, before those blocks'
-    // copies are issued: the piece of blocks [blk0, blk1) writes the new
+    // copies are issued: the piece of units [unit0, unit1) writes the new
     // tokens that fall in them. Generic-proxy stores, then a proxy fence so
     // the TMA (async proxy) that follows reads the new rows.
-    auto append_tokens = [&](int b, int L, int blk0, int blk1) {
+    auto append_tokens = [&](int b, int L, int unit0, int unit1) {
       for (int i = 0; i < P.q_len; ++i) {
         const int pos = L - P.q_len + i;
-        if (pos < blk0 * BS || pos >= blk1 * BS) continue;
+        if (pos < unit0 * UT || pos >= unit1 * UT) continue;
         const size_t tok = size_t(b) * P.q_len + i;
         const int64_t slot = P.slot_mapping[tok];
         if (slot < 0) continue;  // padding token
@@ -842,7 +870,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int L_cur = len0;
     while (ok && unit < u1) {
       if (*abort_flag) break;
-      const int nb = L_cur > 0 ? (L_cur + BS - 1) / BS : 0;
+      const int nb = L_cur > 0 ? (L_cur + UT - 1) / UT : 0;  // units
       if (nb == 0) {  // empty sequence: nothing of it in the stream
         ++b;
         win = load_window(b, 0);
@@ -853,7 +881,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool whole = off == 0 && seg_nb == nb;
       if constexpr (!F8) {
         // this piece holds a block of the new tokens
-        if (P.k_new != nullptr && off + seg_nb > (L_cur - P.q_len) / BS) {
+        if (P.k_new != nullptr && off + seg_nb > (L_cur - P.q_len) / UT) {
           append_tokens(b, L_cur, off, off + seg_nb);
           __syncwarp();
           dev::fence_async_global();
@@ -867,7 +895,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int qs = seg_seq % C::QB;
       const int nch = (seg_nb + U - 1) / U;
       for (int c = 0; c < nch; ++c) {
-        const int jb = c * U;  // first block of the chunk within the segment
+        const int jb = c * U;  // first unit of the chunk within the segment
         if (jb > 0 && (jb & 31) == 0) {
           win = win_nxt;
           win_nxt = jb + 32 < seg_nb ? load_window(b, off + jb + 32) : -1;
@@ -883,7 +911,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             m.b = b;
             m.seg = b + int(blockIdx.x);
             m.flags = (c == 0 ? F_FIRST : 0) | (c == nch - 1 ? F_LAST : 0) | (whole ? F_WHOLE : 0);
-            m.tok0 = (off + jb) * BS;
+            m.tok0 = (off + jb) * UT;
             m.L = L_cur;
             m.nblk = min(U, seg_nb - jb);
             m.qslot = qs;
@@ -894,47 +922,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
         if (!ok) break;
-        // lanes 0..U-1: one block (all KV heads) each
+        // lanes 0..U-1: one unit (all KV heads) each; lane 31 the queries
         const int e = __shfl_sync(0xffffffffu, win, (jb & 31) + (lane % U));
         unsigned char* kdst = ring + size_t(slot) * C::SLOT_BYTES;
+        // A unit's coordinates: its block's rows (block size <= 16), or for
+        // block size 32 its half (keys 16*half ..) of the block's H tiles.
+        // Units past the segment, and bad table entries, read the zero fill
+        // past the end of the tensor.
+        int crd = P.oob_row, crd_v = P.oob_row_v, half = 0;
+        if (lane < U && jb + lane < seg_nb) {
+          if (e >= 0 && e < P.num_blocks) {
+            crd = VS == 1 ? e * grows : e * H;
+            crd_v = e * H;  // 8-bit V^T: the block's first tile
+            half = (off + jb + lane) & (VS - 1);
+          } else {
+            atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+          }
+        }
         if constexpr (F8) {
-          // lanes 0..U-1: block `lane`'s K rows, and its H V^T tiles as one
-          // 3-D box (the tiles of a block are adjacent in the cache)
+          // K rows, and the unit's H V^T sub-tiles as one box
           if (lane < U) {
-            int row = P.oob_row, tile = P.oob_row_v;
-            if (jb + lane < seg_nb) {
-              if (e >= 0 && e < P.num_blocks) {
-                row = e * grows;
-                tile = e * H;
-              } else {
-                atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
-              }
+            if constexpr (VS == 1) {
+              dev::tma_load_2d(kdst + lane * grows * 128, &tm_k, 0, crd, &full[slot], pol);
+              dev::tma_load_3d(kdst + C::K_BYTES + lane * H * C::VT_TILE, &tm_v, 0, 0, crd_v,
+                               &full[slot], pol);
+            } else {
+              dev::tma_load_3d(kdst + lane * grows * 128, &tm_k, 0, half * UT, crd, &full[slot],
+                               pol);
+              dev::tma_load_4d(kdst + C::K_BYTES + lane * H * C::VT_TILE, &tm_v, 0, 0, half,
+                               crd_v, &full[slot], pol);
             }
-            dev::tma_load_2d(kdst + lane * grows * 128, &tm_k, 0, row, &full[slot], pol);
-            dev::tma_load_3d(kdst + C::K_BYTES + lane * H * C::VT_TILE, &tm_v, 0, 0, tile,
-                             &full[slot], pol);
-          } else if (lane == 8 && c == 0) {
+          } else if (lane == 31 && c == 0) {
             dev::tma_load_2d(qbuf + qs * C::Q_BYTES, &tm_q, 0, b * P.q_rows, &full[slot], pol);
             dev::bulk_load(qalpha + qs * 64, P.q_inv_alpha + size_t(b) * N, N * 4, &full[slot],
                            pol);
           }
         } else {
           if (lane < U) {
-            int row = P.oob_row;
-            if (jb + lane < seg_nb) {
-              if (e >= 0 && e < P.num_blocks) {
-                row = e * grows;
-              } else {
-                atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
-              }
-            }
 #pragma unroll
             for (int hf = 0; hf < C::HALVES; ++hf) {
               unsigned char* d = kdst + hf * C::HALF_BYTES + lane * grows * 128;
-              dev::tma_load_2d(d, &tm_k, hf * 64, row, &full[slot], pol);
-              dev::tma_load_2d(d + C::K_BYTES, &tm_v, hf * 64, row, &full[slot], pol);
+              if constexpr (VS == 1) {
+                dev::tma_load_2d(d, &tm_k, hf * 64, crd, &full[slot], pol);
+                dev::tma_load_2d(d + C::K_BYTES, &tm_v, hf * 64, crd, &full[slot], pol);
+              } else {
+                dev::tma_load_3d(d, &tm_k, hf * 64, half * UT, crd, &full[slot], pol);
+                dev::tma_load_3d(d + C::K_BYTES, &tm_v, hf * 64, half * UT, crd, &full[slot], pol);
+              }
             }
-          } else if (lane == 8 && c == 0) {
+          } else if (lane == 31 && c == 0) {
 #pragma unroll
             for (int hf = 0; hf < C::HALVES; ++hf)
               dev::tma_load_2d(qbuf + qs * C::Q_BYTES + hf * C::QH_BYTES, &tm_q, hf * 64,
@@ -972,7 +1008,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                          meta, tmem, abort_flag);
   } else {
     // ------------------------------------------------------------ softmax
-    Softmax<D, GE, N, F8>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2,
+    Softmax<D, GE, N, F8, BS>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2,
                               alpha_s, l_s, m_s, qalpha, kvscale, colrow, tmem, abort_flag,
                               consumed);
   }
@@ -1132,60 +1168,80 @@ int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return g_encode ? 0 : int(cudaErrorNotSupported);
 }
 
-// 2-D bf16 tensor [rows][cols] (row pitch cols*2 bytes), box box_rows x 64 cols,
-// 128B swizzle, out-of-range elements read as zero.
-int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// A tiled tensor map of `rank` dimensions (innermost first): dims, byte
+// strides of dimensions 1.., box; out-of-range elements read as zero.
+int make_map_nd(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base,
+                const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                CUtensorMapSwizzle swizzle) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   if (encode_fn(&enc)) return int(cudaErrorNotSupported);
-  cuuint64_t gdim[2] = {cols, rows};
-  cuuint64_t gstride[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
-                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(m, type, cuuint32_t(rank), const_cast<void*>(base), dims, strides, box,
+                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
 }
 
-// 2-D byte tensor [rows][cols] (row pitch cols bytes), box box_rows x
-// box_cols, the given swizzle, out-of-range elements read as zero.
+// 2-D bf16 tensor [rows][cols], box box_rows x 64 cols, 128B swizzle.
+int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// 2-D byte tensor [rows][cols], box box_rows x box_cols, the given swizzle.
 int make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
                 uint32_t box_rows, CUtensorMapSwizzle swizzle) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc;
-  if (encode_fn(&enc)) return int(cudaErrorNotSupported);
-  cuuint64_t gdim[2] = {cols, rows};
-  cuuint64_t gstride[1] = {cols};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride,
-                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, swizzle);
 }
 
-// The 8-bit V^T cache as a 3-D byte tensor: [tiles][D rows][16 bytes], one
-// tile per (block, KV head); box = `heads` whole tiles, no swizzle.
-int make_map_vt(CUtensorMap* m, const void* base, uint64_t tiles, uint64_t d, uint32_t heads) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc;
-  if (encode_fn(&enc)) return int(cudaErrorNotSupported);
-  cuuint64_t gdim[3] = {uint64_t(BS), d, tiles};
-  cuuint64_t gstride[2] = {uint64_t(BS), d * BS};
-  cuuint32_t box[3] = {uint32_t(BS), uint32_t(d), heads};
-  cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride,
-                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? 0 : int(cudaErrorInvalidValue);
+// Block size 32: the K or V cache ([tiles][32 keys][D], one tile per (block,
+// KV head)) as a 3-D tensor; box = 16 keys of `heads` consecutive tiles
+// (box_cols of the row), 128B swizzle. elem: 2 (bf16) or 1 (E4M3) bytes.
+int make_map_halves(CUtensorMap* m, const void* base, uint64_t tiles, uint64_t d, int elem,
+                    uint32_t box_cols, uint32_t heads) {
+  const cuuint64_t dims[3] = {d, 32, tiles};
+  const cuuint64_t strides[2] = {d * elem, 32 * d * elem};
+  const cuuint32_t box[3] = {box_cols, uint32_t(kF8Tile), heads};
+  return make_map_nd(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                     3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, int GE, int N, bool F8>
+// The 8-bit V^T cache: per (block, KV head) tile, BS/16 sub-tiles of
+// [D rows][16 bytes]. Block size 16: a 3-D tensor [tiles][D][16], box =
+// `heads` whole tiles. Block size 32: a 4-D tensor [tiles][2][D][16], box =
+// one sub-tile of `heads` tiles. No swizzle.
+int make_map_vt(CUtensorMap* m, const void* base, uint64_t tiles, uint64_t d, uint32_t heads,
+                int block_size) {
+  const uint64_t sub = d * kF8Tile;  // bytes of one sub-tile
+  if (block_size == 16) {
+    const cuuint64_t dims[3] = {uint64_t(kF8Tile), d, tiles};
+    const cuuint64_t strides[2] = {uint64_t(kF8Tile), sub};
+    const cuuint32_t box[3] = {uint32_t(kF8Tile), uint32_t(d), heads};
+    return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  const cuuint64_t dims[4] = {uint64_t(kF8Tile), d, 2, tiles};
+  const cuuint64_t strides[3] = {uint64_t(kF8Tile), sub, 2 * sub};
+  const cuuint32_t box[4] = {uint32_t(kF8Tile), uint32_t(d), 1, heads};
+  return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+template <int D, int GE, int N, bool F8, int BS>
 int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   using C = TcCfg<D, N, F8>;
+  constexpr int VS = Units<BS>::VS;
   const pa_decode_params* p = Lc.p;
   const QueryMap qm = query_map(p);
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GE, N, F8>,
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GE, N, F8, BS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return int(e);
     configured = true;
@@ -1193,20 +1249,30 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   const int H = p->num_kv_heads;
   CUtensorMap tk, tv, tq;
   const uint64_t cache_rows = uint64_t(p->num_blocks) * H * BS;
+  const uint64_t tiles = uint64_t(p->num_blocks) * H;
   int r = 0;
   if constexpr (F8) {
-    // K rows of D bytes; V^T rows of 16 bytes, one [D][16] tile per (block,
+    // K rows of D bytes; V^T rows of 16 bytes, [D][16] sub-tiles per (block,
     // head); the split queries, 2N rows of D bytes per sequence
-    r = make_map_u8(&tk, p->k_cache, cache_rows, D, D, uint32_t(BS * H),
-                    CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!r) r = make_map_vt(&tv, p->v_cache, uint64_t(p->num_blocks) * H, D, uint32_t(H));
+    if constexpr (VS == 1) {
+      r = make_map_u8(&tk, p->k_cache, cache_rows, D, D, uint32_t(BS * H),
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+      r = make_map_halves(&tk, p->k_cache, tiles, D, 1, D, uint32_t(H));
+    }
+    if (!r) r = make_map_vt(&tv, p->v_cache, tiles, D, uint32_t(H), BS);
     if (!r)
       r = make_map_u8(&tq, Lc.q8, uint64_t(p->num_seqs) * 2 * N, D, D, uint32_t(2 * N),
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (!r) r = launch_quantize_q(p->q, Lc.q8, Lc.q_inv_alpha, qm, stream);
   } else {
-    r = make_map(&tk, p->k_cache, cache_rows, D, uint32_t(BS * H));
-    if (!r) r = make_map(&tv, p->v_cache, cache_rows, D, uint32_t(BS * H));
+    if constexpr (VS == 1) {
+      r = make_map(&tk, p->k_cache, cache_rows, D, uint32_t(BS * H));
+      if (!r) r = make_map(&tv, p->v_cache, cache_rows, D, uint32_t(BS * H));
+    } else {
+      r = make_map_halves(&tk, p->k_cache, tiles, D, 2, 64, uint32_t(H));
+      if (!r) r = make_map_halves(&tv, p->v_cache, tiles, D, 2, 64, uint32_t(H));
+    }
     if (qm.query_len == 1) {
       // the rows of q are already in column order (column = query head); a
       // box of N rows may run into the next sequence's rows, never used
@@ -1234,7 +1300,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.k_scale = p->k_scale;
   P.v_scale = p->v_scale;
   P.q_inv_alpha = Lc.q_inv_alpha;
-  P.oob_row_v = int(uint64_t(p->num_blocks) * H);  // first V^T tile past the cache
+  P.oob_row_v = int(tiles);  // first V^T tile past the cache
   P.q_rows = F8 ? 2 * N : (qm.query_len == 1 ? p->num_q_heads : N);
   P.num_cols = qm.num_cols;
   P.q_len = qm.query_len;
@@ -1245,7 +1311,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.num_q_heads = p->num_q_heads;
   P.num_blocks = p->num_blocks;
   P.cap = min(p->max_blocks_per_seq * BS, p->max_context_len);
-  P.oob_row = int(cache_rows);
+  P.oob_row = VS == 1 ? int(cache_rows) : int(tiles);
   P.scale_log2 = p->scale * kLog2e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1259,7 +1325,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   // overlap the set-up with the previous kernel only when the caller says
   // context_lens and block_tables were final before that kernel began
   attr[0].val.programmaticStreamSerializationAllowed = p->overlap_prologue ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<D, GE, N, F8>, tk, tv, tq, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<D, GE, N, F8, BS>, tk, tv, tq, P);
   if (e != cudaSuccess) return int(e);
   // the merge launches while the decode drains and waits for it on the device
   cudaLaunchConfig_t mcfg = {};
@@ -1282,27 +1348,34 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   return int(e);
 }
 
-// Instances by (columns per KV head GE, padded columns N).
-template <int D, bool F8>
+// Instances by (columns per KV head GE, padded columns N). Block size 8 takes
+// GE <= 8 (its groups of 8 rows leave 8 reduction columns per group).
+template <int D, bool F8, int BS>
 int dispatch_tc(const DecodeLaunch& Lc, cudaStream_t s) {
   const int GE = tc_group_cols(Lc.p);
   const int N = tc_n_pad(tc_cols(Lc.p));
   switch (GE * 1000 + N) {
-    case 1016: return launch_tc_t<D, 1, 16, F8>(Lc, s);
-    case 2016: return launch_tc_t<D, 2, 16, F8>(Lc, s);
-    case 4016: return launch_tc_t<D, 4, 16, F8>(Lc, s);
-    case 4032: return launch_tc_t<D, 4, 32, F8>(Lc, s);
-    case 8016: return launch_tc_t<D, 8, 16, F8>(Lc, s);
-    case 8032: return launch_tc_t<D, 8, 32, F8>(Lc, s);
-    case 8064: return launch_tc_t<D, 8, 64, F8>(Lc, s);
-    case 16016: return launch_tc_t<D, 16, 16, F8>(Lc, s);
-    case 16032: return launch_tc_t<D, 16, 32, F8>(Lc, s);
-    case 16064: return launch_tc_t<D, 16, 64, F8>(Lc, s);
-    case 16128:
-      if constexpr (!F8) return launch_tc_t<D, 16, 128, F8>(Lc, s);
-      return int(cudaErrorInvalidValue);
-    default: return int(cudaErrorInvalidValue);
+    case 1016: return launch_tc_t<D, 1, 16, F8, BS>(Lc, s);
+    case 2016: return launch_tc_t<D, 2, 16, F8, BS>(Lc, s);
+    case 4016: return launch_tc_t<D, 4, 16, F8, BS>(Lc, s);
+    case 4032: return launch_tc_t<D, 4, 32, F8, BS>(Lc, s);
+    case 8016: return launch_tc_t<D, 8, 16, F8, BS>(Lc, s);
+    case 8032: return launch_tc_t<D, 8, 32, F8, BS>(Lc, s);
+    case 8064: return launch_tc_t<D, 8, 64, F8, BS>(Lc, s);
+    default: break;
   }
+  if constexpr (BS >= 16) {
+    switch (GE * 1000 + N) {
+      case 16016: return launch_tc_t<D, 16, 16, F8, BS>(Lc, s);
+      case 16032: return launch_tc_t<D, 16, 32, F8, BS>(Lc, s);
+      case 16064: return launch_tc_t<D, 16, 64, F8, BS>(Lc, s);
+      case 16128:
+        if constexpr (!F8) return launch_tc_t<D, 16, 128, F8, BS>(Lc, s);
+        return int(cudaErrorInvalidValue);
+      default: break;
+    }
+  }
+  return int(cudaErrorInvalidValue);
 }
 
 // Device error word of the including translation unit, read and cleared.

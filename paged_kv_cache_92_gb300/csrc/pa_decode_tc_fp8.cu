@@ -5,7 +5,7 @@
 namespace pa {
 
 int launch_decode_tc_fp8(const DecodeLaunch& Lc, void* stream) {
-  return dispatch_tc<128, true>(Lc, static_cast<cudaStream_t>(stream));
+  return dispatch_tc<128, true, 16>(Lc, static_cast<cudaStream_t>(stream));
 }
 
 int read_and_clear_decode_tc_fp8_errors(uint32_t* flags) {

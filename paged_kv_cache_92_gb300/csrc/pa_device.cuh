@@ -187,6 +187,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, in
       : "memory");
 }
 
+// 4-D tiled TMA load (coordinates innermost first), completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tmap, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Pull `bytes` (multiple of 16, 16-byte aligned) from global memory into L2
 // without touching shared memory.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {

@@ -8,8 +8,10 @@
 //  - write: code = E4M3(float32(x) / scale[h]), round to nearest even,
 //    saturating to +-448 (the CUDA conversion intrinsic with satfinite);
 //  - layout: K [block][head][offset][d] like the bf16 cache; V transposed
-//    inside each (block, head) tile, [block][head][d][offset], so that the
-//    value product reads V^T K-major (keys contiguous) on the tensor cores.
+//    inside each (block, head) tile in sub-tiles of 16 keys,
+//    [block][head][offset / 16][d][offset % 16] (one [d][16] sub-tile at block
+//    size 16, two at 32), so that the value product reads V^T K-major (16
+//    contiguous keys per row) on the tensor cores.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -24,8 +26,6 @@ namespace {
 
 __device__ unsigned int g_fp8_errors;
 
-constexpr int BS = kBlockSize;
-
 using dev::to_e4m3;
 
 // One thread per 8 elements (one 16-byte chunk of the bf16 input) of one
@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(256)
                                  const int64_t* __restrict__ slot_mapping,
                                  const float* __restrict__ k_scale,
                                  const float* __restrict__ v_scale, int64_t num_chunks,
-                                 int num_kv_heads, int head_dim, int64_t num_slots) {
+                                 int num_kv_heads, int head_dim, int64_t num_slots, int bs_log2) {
+  const int BS = 1 << bs_log2;
   dev::griddep_launch_dependents();
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= num_chunks) return;
@@ -51,8 +52,8 @@ __global__ void __launch_bounds__(256)
     if (h == 0 && c == 0) atomicOr(&g_fp8_errors, PA_DEVERR_SLOT);
     return;
   }
-  const int64_t blk = slot / BS;
-  const int off = int(slot % BS);
+  const int64_t blk = slot >> bs_log2;
+  const int off = int(slot & (BS - 1));
   const float ks = k_scale[h], vs = v_scale[h];
   const uint4 kr = k_new[idx], vr = v_new[idx];
   const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kr);
@@ -66,10 +67,12 @@ __global__ void __launch_bounds__(256)
   kw.x = uint32_t(kq[0]) | uint32_t(kq[1]) << 8 | uint32_t(kq[2]) << 16 | uint32_t(kq[3]) << 24;
   kw.y = uint32_t(kq[4]) | uint32_t(kq[5]) << 8 | uint32_t(kq[6]) << 16 | uint32_t(kq[7]) << 24;
   *reinterpret_cast<uint2*>(k_cache + tile + int64_t(off) * head_dim + c * 8) = kw;
-  // V column: element d of the row goes to byte d * BS + off of the tile
+  // V column: element d of the row goes to byte d * 16 + off % 16 of the
+  // tile's sub-tile off / 16
+  const int64_t sub = tile + int64_t(off >> 4) * 16 * head_dim + (off & 15);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    v_cache[tile + int64_t(c * 8 + i) * BS + off] = to_e4m3(__fdiv_rn(__bfloat162float(vb[i]), vs));
+    v_cache[sub + int64_t(c * 8 + i) * 16] = to_e4m3(__fdiv_rn(__bfloat162float(vb[i]), vs));
 }
 
 }  // namespace
@@ -77,7 +80,8 @@ __global__ void __launch_bounds__(256)
 int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_cache,
                                  void* v_cache, const int64_t* slot_mapping, const float* k_scale,
                                  const float* v_scale, int32_t num_tokens, int32_t num_kv_heads,
-                                 int32_t head_dim, int32_t num_blocks, void* stream) {
+                                 int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                 void* stream) {
   const int64_t num_chunks = int64_t(num_tokens) * num_kv_heads * (head_dim / 8);
   if (num_chunks == 0) return int(cudaSuccess);
   const int threads = 256;
@@ -86,7 +90,8 @@ int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_c
                                  static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
       static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), slot_mapping, k_scale,
-      v_scale, num_chunks, num_kv_heads, head_dim, int64_t(num_blocks) * BS);
+      v_scale, num_chunks, num_kv_heads, head_dim, int64_t(num_blocks) * block_size,
+      log2_of(block_size));
   return int(cudaGetLastError());
 }
 

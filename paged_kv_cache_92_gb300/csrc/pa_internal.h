@@ -13,7 +13,9 @@ namespace pa {
 pa_status set_error(pa_status s, const char* msg);
 pa_status set_cuda_error(const char* where, int cuda_err);
 
-constexpr int kBlockSize = 16;
+constexpr int kBlockSize = 16;  // the CUDA-core decode's block size
+// Block sizes the cache kernels and the tensor-core decode take.
+inline bool block_size_ok(int bs) { return bs == 8 || bs == 16 || bs == 32; }
 constexpr int kDefaultPartitionTokens = 512;
 constexpr int kMaxPartitionTokens = 4096;
 // The tensor-core decode kernel plans its stream-K split in shared memory
@@ -104,8 +106,13 @@ int tc_grid();
 // Kernel launchers (pa_decode.cu / pa_cache.cu). Return a cudaError_t as int.
 int launch_decode(const DecodeLaunch& L, void* stream);      // CUDA-core decode kernel
 int launch_decode_tc(const DecodeLaunch& L, void* stream);   // tensor-core decode kernel
-int launch_decode_tc_d64(const DecodeLaunch& L, void* stream);  // its bf16 head_dim 64 share
-int launch_decode_tc_fp8(const DecodeLaunch& L, void* stream);  // its 8-bit cache share
+// its shares by translation unit: bf16 head_dim 64; the 8-bit cache; block
+// size 8; block size 32 (bf16, 8-bit)
+int launch_decode_tc_d64(const DecodeLaunch& L, void* stream);
+int launch_decode_tc_fp8(const DecodeLaunch& L, void* stream);
+int launch_decode_tc_bs8(const DecodeLaunch& L, void* stream);
+int launch_decode_tc_bs32(const DecodeLaunch& L, void* stream);
+int launch_decode_tc_bs32_fp8(const DecodeLaunch& L, void* stream);
 int launch_merge(const DecodeLaunch& L, void* stream);       // split-K merge (if needed)
 // Decode-step check (block_tables non-null): token t is sequence t's newest
 // token; it is written only if slot_mapping[t] is the slot of token
@@ -119,13 +126,14 @@ struct AppendCheck {
 };
 int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
-                             int32_t head_dim, int32_t num_blocks, void* stream,
+                             int32_t head_dim, int32_t block_size, int32_t num_blocks, void* stream,
                              const AppendCheck& check = AppendCheck());
 // 8-bit cache (pa_fp8.cu)
 int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_cache,
                                  void* v_cache, const int64_t* slot_mapping, const float* k_scale,
                                  const float* v_scale, int32_t num_tokens, int32_t num_kv_heads,
-                                 int32_t head_dim, int32_t num_blocks, void* stream);
+                                 int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                 void* stream);
 int read_and_clear_fp8_errors(uint32_t* flags);
 // Query preparation for the tensor-core decode (pa_query.cu): the rows of q
 // ([B][query_len][Hq][D] bf16) in the column layout, padded to n_pad rows with
@@ -134,13 +142,17 @@ int read_and_clear_fp8_errors(uint32_t* flags);
 int launch_permute_q(const void* q, void* qp, const QueryMap& m, void* stream);
 int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap& m, void* stream);
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
-                       int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, void* stream);
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int32_t num_blocks, void* stream);
 
 // Device error words, one per kernel translation unit: read and clear.
 int read_and_clear_decode_errors(uint32_t* flags);
 int read_and_clear_decode_tc_errors(uint32_t* flags);  // all three shares below
 int read_and_clear_decode_tc_d64_errors(uint32_t* flags);
 int read_and_clear_decode_tc_fp8_errors(uint32_t* flags);
+int read_and_clear_decode_tc_bs8_errors(uint32_t* flags);
+int read_and_clear_decode_tc_bs32_errors(uint32_t* flags);
+int read_and_clear_decode_tc_bs32_fp8_errors(uint32_t* flags);
 
 // Size of the library-owned device scratch used by pa_decode_noalloc.
 constexpr size_t kNoAllocScratchBytes = PA_NOALLOC_SCRATCH_BYTES;

@@ -61,7 +61,13 @@ def _params(pk, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=96), 2),
-    (dict(block_size=32), 2),
+    (dict(block_size=64), 2),
+    (dict(block_size=32), 1),  # block size 32: tensor-core kernel, valid shapes, NULL pointers
+    (dict(block_size=8), 1),
+    (dict(block_size=32, head_dim=64), 2),  # block sizes 8 and 32: head_dim 128 only
+    (dict(block_size=8, variant=1), 2),  # ... and the tensor-core kernel only
+    (dict(block_size=8, query_len=4), 2),  # block size 8: at most 8 columns per KV head
+    (dict(block_size=8, kv_dtype=1), 2),  # the 8-bit cache: block size 16 or 32
     (dict(num_q_heads=12, num_kv_heads=1), 2),
     (dict(num_q_heads=6, num_kv_heads=4), 1),
     (dict(max_context_len=0), 1),
@@ -137,8 +143,17 @@ def test_decode_workspace_size(pk):
 
 def test_cache_ops_reject_bad_arguments_on_the_host(pk):
     lib = pk.load()
-    assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, 32, 10, None) == 2
-    assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, 16, 10, None) == 1
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, 64, 10, None) == 2
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, 12, 10, None) == 2
+    for bs in (8, 16, 32):
+        assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, bs, 10, None) == 1
+        assert lib.pa_copy_blocks(None, None, None, 2, 8, 128, bs, 10, None) == 1
+    assert lib.pa_copy_blocks(None, None, None, 2, 8, 128, 4, 10, None) == 2
+    assert lib.pa_reshape_and_cache_fp8(None, None, None, None, None, None, None, 4, 8, 128, 8,
+                                        10, None) == 2
+    assert lib.pa_reshape_and_cache_fp8(None, None, None, None, None, None, None, 4, 8, 128, 32,
+                                        10, None) == 1
+    assert lib.pa_copy_blocks_fp8(None, None, None, 2, 8, 128, 8, 10, None) == 2
     assert lib.pa_reshape_and_cache(None, None, None, None, None, 0, 8, 128, 16, 10, None) == 0
     assert lib.pa_copy_blocks(None, None, None, 2, 8, 128, 16, 10, None) == 1
     assert lib.pa_copy_blocks(None, None, None, 0, 8, 128, 16, 10, None) == 0

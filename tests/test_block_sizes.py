@@ -1,0 +1,255 @@
+"""GPU parity at block sizes 8 and 32 ("Paged Attention as a Memory Manager",
+§PagedAttention: the block size is a compile-time constant, typically 8, 16
+or 32).
+
+The same bars as at block size 16: bit-exact caches after the KV write and
+the copy-on-write copy; decode within max-abs 2e-2 / mean-abs 2e-3 of the
+float64 oracle; NaN in every padding slot.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+BLOCK_SIZES = pytest.mark.parametrize("bs", [8, 32])
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import torch
+
+    from paged_kv_cache_92_gb300 import build
+
+    build.build()
+    import paged_kv_cache_92_gb300 as pk
+
+    pk.load()
+    assert torch.cuda.is_available()
+    return pk
+
+
+def _case(lens, Hq, Hkv, bs, seed, QL=0, D=128, extra_blocks=3):
+    import torch
+
+    lens = np.asarray(lens, dtype=np.int64)
+    need = int(((lens + bs - 1) // bs).sum())
+    NB = need + extra_blocks
+    order = np.random.default_rng(seed).permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, bs)
+    qshape = (len(lens), QL, Hq, D) if QL else (len(lens), Hq, D)
+    q = workloads.bf16_normal(qshape, seed + 1, "cuda")
+    kc = workloads.bf16_normal((NB, Hkv, bs, D), seed + 2, "cuda")
+    vc = workloads.bf16_normal((NB, Hkv, bs, D), seed + 3, "cuda")
+    workloads.fill_padding_nan(kc, tables, lens, bs)
+    workloads.fill_padding_nan(vc, tables, lens, bs)
+    return q, kc, vc, tables, lens.astype(np.int32), torch
+
+
+def _decode(pk, q, kc, vc, tables, lens, torch, **kw):
+    out = pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=int(lens.max()), **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+# ---------------------------------------------------------------- whole steps through the pool
+
+
+@BLOCK_SIZES
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_llama8b_layer_step(pk, bs, fused):
+    """The pool lays out the 64-sequence layer at this block size; one step
+    (KV write + decode) against the oracle's own pool model and decode."""
+    case = harness.build_case(workloads.llama8b_layer(block_size=bs))
+    out, kg, vg = harness.run_step_gpu(case, fused_append=fused)
+    ref, ko, vo = harness.run_step_oracle(case)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert pk.pa_device_errors() == 0
+
+
+@BLOCK_SIZES
+def test_llama70b_long_step(pk, bs):
+    case = harness.build_case(workloads.llama70b_long(batch=8, block_size=bs))
+    out, kg, vg = harness.run_step_gpu(case, fused_append=True)
+    units = harness.sample_units(8, 64, 96, seed=5)
+    ref, ko, vo = harness.run_step_oracle(case, units=units)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    got = harness.bf16_tensor_to_f64(out)
+    harness.assert_close(np.stack([got[b, h] for b, h in units]), ref)
+    assert pk.pa_device_errors() == 0
+
+
+# ---------------------------------------------------------------- decode edge cases
+
+
+@BLOCK_SIZES
+@pytest.mark.parametrize("G,Hkv", [(1, 8), (2, 4), (4, 8), (8, 8), (4, 1), (8, 2), (1, 1)])
+def test_edge_lengths(pk, bs, G, Hkv):
+    """Lengths at and around every block boundary of both sizes, and long
+    enough to split over CTAs."""
+    lens = [1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 100, 511, 513, 1025, 4097]
+    q, kc, vc, tables, lens, torch = _case(lens, G * Hkv, Hkv, bs, seed=bs * 10 + G * 3 + Hkv)
+    out = _decode(pk, q, kc, vc, tables, lens, torch)
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert pk.pa_device_errors() == 0
+
+
+@BLOCK_SIZES
+def test_split_and_placement(pk, bs):
+    """One long sequence beside short ones (stream-K pieces across CTAs), and
+    the same logical cache under another physical placement gives the same
+    bits."""
+    import torch
+
+    q, kc, vc, tables, lens, _ = _case([9000, 3, 47, 700], 32, 8, bs, seed=90 + bs)
+    a = _decode(pk, q, kc, vc, tables, lens, torch)
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(a), ref)
+    NB = kc.shape[0]
+    perm = np.random.default_rng(3).permutation(NB)
+    kcb, vcb = torch.empty_like(kc), torch.empty_like(vc)
+    kcb[torch.from_numpy(perm).cuda()] = kc
+    vcb[torch.from_numpy(perm).cuda()] = vc
+    tables_b = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    b = _decode(pk, q, kcb, vcb, tables_b, lens, torch)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("bs,G,Hkv,QL", [(8, 4, 8, 2), (8, 1, 8, 8), (8, 2, 2, 4), (32, 4, 8, 4),
+                                         (32, 8, 8, 2), (32, 1, 1, 16), (32, 4, 1, 3)])
+def test_multi_token(pk, bs, G, Hkv, QL):
+    lens = [L for L in (QL, 9, 16, 17, 31, 33, 34, 100, 513, 2049) if L >= QL]
+    q, kc, vc, tables, lens, torch = _case(lens, G * Hkv, Hkv, bs, seed=bs + G * 7 + QL, QL=QL)
+    out = _decode(pk, q, kc, vc, tables, lens, torch)
+    ref = oracle.paged_decode_multi(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert pk.pa_device_errors() == 0
+
+
+@BLOCK_SIZES
+def test_copy_blocks_bit_exact(pk, bs):
+    import torch
+
+    rng = np.random.default_rng(bs)
+    k0 = workloads.bf16_normal((12, 8, bs, 128), 5, "cuda")
+    v0 = workloads.bf16_normal((12, 8, bs, 128), 6, "cuda")
+    kc, vc = k0.clone(), v0.clone()
+    pairs = np.array([[1, 7], [3, 2], [11, 0]], dtype=np.int32)
+    pk.pa_copy_blocks(kc, vc, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    ko, vo = oracle.copy_blocks(oracle.bf16_bits(k0.cpu()), oracle.bf16_bits(v0.cpu()), pairs)
+    assert np.array_equal(oracle.bf16_bits(kc.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc.cpu()), vo)
+    _ = rng
+
+
+def test_unsupported_block_size_shapes_are_rejected(pk):
+    import torch
+
+    q, kc, vc, tables, lens, _ = _case([40], 8, 2, 32, seed=7, D=64)  # head_dim 64
+    with pytest.raises(pk.PagedKVError):
+        _decode(pk, q, kc, vc, tables, lens, torch)
+    q, kc, vc, tables, lens, _ = _case([40], 8, 2, 8, seed=8)
+    with pytest.raises(pk.PagedKVError):
+        _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+
+
+# ---------------------------------------------------------------- the 8-bit cache at block size 32
+
+
+def _fp8_case(pk, lens, Hq, Hkv, seed, QL=0):
+    import torch
+
+    BS, D = 32, 128
+    lens = np.asarray(lens, dtype=np.int64)
+    need = int(((lens + BS - 1) // BS).sum())
+    NB = need + 3
+    order = np.random.default_rng(seed).permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, BS)
+    qshape = (len(lens), QL, Hq, D) if QL else (len(lens), Hq, D)
+    q = workloads.bf16_normal(qshape, seed + 1, "cuda")
+    kn = workloads.bf16_normal((NB * BS, Hkv, D), seed + 2, "cuda")
+    vn = workloads.bf16_normal((NB * BS, Hkv, D), seed + 3, "cuda")
+    rng = np.random.default_rng(seed + 4)
+    ks = torch.from_numpy((0.05 * np.exp(rng.uniform(-0.5, 0.5, Hkv))).astype(np.float32)).cuda()
+    vs = torch.from_numpy((0.03 * np.exp(rng.uniform(-0.5, 0.5, Hkv))).astype(np.float32)).cuda()
+    k8 = torch.zeros((NB, Hkv, BS, D), dtype=torch.uint8, device="cuda")
+    v8 = torch.zeros((NB, Hkv, BS // 16, D, 16), dtype=torch.uint8, device="cuda")
+    pk.pa_reshape_and_cache_fp8(kn, vn, k8, v8, torch.arange(NB * BS, device="cuda"), ks, vs)
+    for b, L in enumerate(lens):
+        if L % BS:
+            blk, off = int(tables[b, (L - 1) // BS]), int(L % BS)
+            k8[blk, :, off:, :] = 0x7F  # E4M3 NaN in the padding slots
+            for o in range(off, BS):
+                v8[blk, :, o // 16, :, o % 16] = 0x7F
+    torch.cuda.synchronize()
+    return q, k8, v8, ks, vs, tables, lens.astype(np.int32), kn, vn, torch
+
+
+def test_fp8_write_bit_exact_at_block_size_32(pk):
+    import torch
+
+    Hkv, D, NB, BS = 4, 128, 6, 32
+    rng = np.random.default_rng(11)
+    T = 70
+    kn = torch.from_numpy(rng.standard_normal((T, Hkv, D)) * 30).to(torch.bfloat16)
+    vn = torch.from_numpy(rng.standard_normal((T, Hkv, D)) * 30).to(torch.bfloat16)
+    ks = np.array([1.0, 0.5, 2.0, 0.37], dtype=np.float32)
+    vs = np.array([1.0, 3.0, 0.25, 1.7], dtype=np.float32)
+    slots = rng.permutation(NB * BS)[:T].astype(np.int64)
+    slots[[4, 40]] = -1
+    k0 = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
+    v0 = rng.integers(0, 256, size=(NB, Hkv, BS // 16, D, 16), dtype=np.uint8)
+    kc, vc = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    pk.pa_reshape_and_cache_fp8(kn.cuda(), vn.cuda(), kc, vc, torch.from_numpy(slots).cuda(),
+                                torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda())
+    torch.cuda.synchronize()
+    ko, vo = oracle.reshape_and_cache_fp8(kn, vn, k0, v0.reshape(NB, Hkv, BS, D), slots, ks, vs)
+    assert np.array_equal(kc.cpu().numpy(), ko)
+    assert np.array_equal(vc.cpu().numpy().reshape(NB, Hkv, BS, D), vo)
+    assert pk.pa_device_errors() == 0
+
+
+@pytest.mark.parametrize("G,Hkv", [(4, 8), (8, 8), (1, 4), (4, 2), (8, 1)])
+def test_fp8_decode_at_block_size_32(pk, G, Hkv):
+    lens = [1, 15, 16, 17, 31, 32, 33, 100, 513, 1025, 4097]
+    q, k8, v8, ks, vs, tables, lens, _, _, torch = _fp8_case(pk, lens, G * Hkv, Hkv,
+                                                              seed=40 + G + Hkv)
+    out = _decode(pk, q, k8, v8, tables, lens, torch, k_scale=ks, v_scale=vs)
+    NB = k8.shape[0]
+    want = oracle.paged_decode_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy().reshape(NB, Hkv, 32, 128),
+                                   ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+
+
+def test_fp8_multi_token_at_block_size_32(pk):
+    QL = 2
+    lens = [2, 17, 31, 32, 33, 600, 2049]
+    q, k8, v8, ks, vs, tables, lens, _, _, torch = _fp8_case(pk, lens, 32, 8, seed=77, QL=QL)
+    out = _decode(pk, q, k8, v8, tables, lens, torch, k_scale=ks, v_scale=vs)
+    NB = k8.shape[0]
+    want = oracle.paged_decode_multi_fp8(q.cpu(), k8.cpu().numpy(),
+                                         v8.cpu().numpy().reshape(NB, 8, 32, 128),
+                                         ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+
+
+def test_fp8_block_size_8_is_rejected(pk):
+    import torch
+
+    k8 = torch.zeros((4, 2, 8, 128), dtype=torch.uint8, device="cuda")
+    v8 = torch.zeros((4, 2, 8, 128), dtype=torch.uint8, device="cuda")
+    kn = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda")
+    ks = torch.ones(2, dtype=torch.float32, device="cuda")
+    with pytest.raises((pk.PagedKVError, ValueError)):
+        pk.pa_reshape_and_cache_fp8(kn, kn, k8, v8, torch.zeros(1, dtype=torch.int64,
+                                                                device="cuda"), ks, ks)

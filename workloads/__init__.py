@@ -12,7 +12,9 @@ Shapes follow the model geometry the pages quote: a Llama-3.1-8B-class layer
 Continuous Batching Actually Work", §The problem) and a Llama-3-70B-class
 layer (64/8 heads, head dim 128; "PagedAttention" glossary, §The
 fragmentation problem). Block size is 16 ("How Paged Attention ...",
-§Paged attention: virtual memory for the KV cache).
+§Paged attention: virtual memory for the KV cache) unless a recipe is asked
+for 8 or 32, the other typical sizes ("Paged Attention as a Memory Manager",
+§PagedAttention).
 
 Every random draw is seeded: numpy ``default_rng(seed)`` for lengths,
 permutations and structure; a torch generator for tensor contents
@@ -74,14 +76,18 @@ def tiny(seed: int = 1) -> Recipe:
                   rng.permutation(16).astype(np.int32), seed=seed)
 
 
-def llama8b_layer(seed: int = 2, batch: int = 64) -> Recipe:
+def _bs_suffix(block_size: int) -> str:
+    return "" if block_size == BLOCK_SIZE else f"_bs{block_size}"
+
+
+def llama8b_layer(seed: int = 2, batch: int = 64, block_size: int = BLOCK_SIZE) -> Recipe:
     """Llama-3.1-8B-class layer: B=64, 32/8 heads, d=128, L~U[128,2048]."""
     rng = np.random.default_rng(seed)
     lens = rng.integers(128, 2048, size=batch, endpoint=True).astype(np.int64)
-    need = int(_blocks_for(lens + 1, BLOCK_SIZE).sum())
+    need = int(_blocks_for(lens + 1, block_size).sum())
     nb = _pool_size(need)
-    return Recipe("llama8b_b64", batch, 32, 8, 128, BLOCK_SIZE, lens, 1, nb,
-                  rng.permutation(nb).astype(np.int32), seed=seed)
+    return Recipe("llama8b_b64" + _bs_suffix(block_size), batch, 32, 8, 128, block_size, lens, 1,
+                  nb, rng.permutation(nb).astype(np.int32), seed=seed)
 
 
 def llama8b_high_concurrency(seed: int = 3, batch: int = 256) -> Recipe:
@@ -95,14 +101,14 @@ def llama8b_high_concurrency(seed: int = 3, batch: int = 256) -> Recipe:
                   rng.permutation(nb).astype(np.int32), seed=seed)
 
 
-def llama70b_long(seed: int = 4, batch: int = 8) -> Recipe:
+def llama70b_long(seed: int = 4, batch: int = 8, block_size: int = BLOCK_SIZE) -> Recipe:
     """Llama-3-70B-class long context: 64/8 heads, d=128, L ~ U[8192, 32768]."""
     rng = np.random.default_rng(seed * 100 + batch)
     lens = rng.integers(8192, 32768, size=batch, endpoint=True).astype(np.int64)
-    need = int(_blocks_for(lens + 1, BLOCK_SIZE).sum())
+    need = int(_blocks_for(lens + 1, block_size).sum())
     nb = _pool_size(need)
-    return Recipe(f"llama70b_long_b{batch}", batch, 64, 8, 128, BLOCK_SIZE, lens, 1, nb,
-                  rng.permutation(nb).astype(np.int32), seed=seed)
+    return Recipe(f"llama70b_long_b{batch}" + _bs_suffix(block_size), batch, 64, 8, 128,
+                  block_size, lens, 1, nb, rng.permutation(nb).astype(np.int32), seed=seed)
 
 
 def shared_prefix(seed: int = 5, batch: int = 512, prefix_tokens: int = 1024,
