@@ -393,7 +393,10 @@ def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True, 
     recipes = [("llama8b_high_concurrency_b256", workloads.llama8b_high_concurrency()),
                ("llama70b_long_b8", workloads.llama70b_long(batch=8)),
                ("llama70b_long_b32", workloads.llama70b_long(batch=32)),
-               ("shared_prefix_cow_b512", workloads.shared_prefix())]
+               ("shared_prefix_cow_b512", workloads.shared_prefix()),
+               ("llama8b_layer_b64_bs8", workloads.llama8b_layer(block_size=8)),
+               ("llama8b_layer_b64_bs32", workloads.llama8b_layer(block_size=32)),
+               ("llama70b_long_b8_bs32", workloads.llama70b_long(batch=8, block_size=32))]
     peak = measured_peaks()["hbm_gbs"]
     stream = torch.cuda.current_stream()
     for name, r in recipes:
@@ -402,9 +405,9 @@ def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True, 
         W = setup_workload(r, device, n_copies=2)
         plans, _, keep = make_plans(pk, W, device, variant=variant, overlap=overlap, fused=fused)
         lens = W["lens"]
-        dec_b = decode_bytes(lens, r.num_q_heads, r.num_kv_heads, r.head_dim)
+        dec_b = decode_bytes(lens, r.num_q_heads, r.num_kv_heads, r.head_dim, r.block_size)
         step_b = dec_b + append_bytes(len(W["slots"]), r.num_kv_heads, r.head_dim) + \
-            cow_bytes(len(W["cows"]), r.num_kv_heads, r.head_dim)
+            cow_bytes(len(W["cows"]), r.num_kv_heads, r.head_dim, r.block_size)
         for i in range(warmup):
             plans[i % len(plans)].run()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -423,7 +426,7 @@ def measure_other_workloads(pk, device, variant: int = 0, overlap: bool = True, 
         step_ms = a.elapsed_time(b) / steps
         dec_gbs = dec_b / (dec_ms * 1e-3) / 1e9
         out[name] = {
-            "num_seqs": r.num_seqs, "num_q_heads": r.num_q_heads,
+            "num_seqs": r.num_seqs, "num_q_heads": r.num_q_heads, "block_size": r.block_size,
             "context_tokens": int(lens.sum()), "cow_pairs": int(len(W["cows"])),
             "decode_bytes": dec_b, "decode_ms": round(dec_ms, 5),
             "decode_gbs": round(dec_gbs, 1), "decode_frac": round(dec_gbs / peak, 4),
@@ -480,7 +483,8 @@ def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10, only=N
     out = {}
     recipes = [("llama8b_layer_b64_fp8_e4m3", workloads.llama8b_layer()),
                ("llama8b_high_concurrency_b256_fp8_e4m3", workloads.llama8b_high_concurrency()),
-               ("llama70b_long_b8_fp8_e4m3", workloads.llama70b_long(batch=8))]
+               ("llama70b_long_b8_fp8_e4m3", workloads.llama70b_long(batch=8)),
+               ("llama8b_layer_b64_bs32_fp8_e4m3", workloads.llama8b_layer(block_size=32))]
     peak = measured_peaks()["hbm_gbs"]
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream or None
@@ -498,12 +502,12 @@ def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10, only=N
         outb = torch.empty_like(W["q"])
         keep, plans = [ks, vs, tables_d, lens_d, slots_d, cows_d, outb], []
         for kc, vc in W["copies"]:
-            NB = kc.shape[0]
-            k8 = torch.empty((NB, H, 16, D), dtype=torch.uint8, device=device)
-            v8 = torch.empty((NB, H, D, 16), dtype=torch.uint8, device=device)
-            rows = torch.arange(NB * 16, dtype=torch.int64, device=device)
-            pk.pa_reshape_and_cache_fp8(kc.permute(0, 2, 1, 3).reshape(NB * 16, H, D).contiguous(),
-                                        vc.permute(0, 2, 1, 3).reshape(NB * 16, H, D).contiguous(),
+            NB, BS = kc.shape[0], kc.shape[2]
+            k8 = torch.empty((NB, H, BS, D), dtype=torch.uint8, device=device)
+            v8 = torch.empty((NB, H, BS // 16, D, 16), dtype=torch.uint8, device=device)
+            rows = torch.arange(NB * BS, dtype=torch.int64, device=device)
+            pk.pa_reshape_and_cache_fp8(kc.permute(0, 2, 1, 3).reshape(NB * BS, H, D).contiguous(),
+                                        vc.permute(0, 2, 1, 3).reshape(NB * BS, H, D).contiguous(),
                                         k8, v8, rows, ks, vs)
             p = pk.make_decode_params(W["q"], outb, k8, v8, tables_d, lens_d,
                                       max_context_len=int(W["lens"].max()), k_scale=ks, v_scale=vs,
@@ -511,18 +515,18 @@ def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10, only=N
             ws = torch.empty(pk.pa_decode_workspace_size(p), dtype=torch.uint8, device=device)
             rc_args = (W["kn"].data_ptr(), W["vn"].data_ptr(), k8.data_ptr(), v8.data_ptr(),
                        slots_d.data_ptr(), ks.data_ptr(), vs.data_ptr(), W["kn"].shape[0], H, D,
-                       16, NB)
+                       BS, NB)
             cow_args = None if cows_d is None else (k8.data_ptr(), v8.data_ptr(),
                                                      cows_d.data_ptr(), cows_d.shape[0], H, D,
-                                                     16, NB)
+                                                     BS, NB)
             plans.append(Fp8StepPlan(pk, lib, p, ws, rc_args, cow_args, sh))
             keep += [k8, v8, ws]
         del W["copies"]
         torch.cuda.empty_cache()
         lens = W["lens"]
-        dec_b = decode_bytes_fp8(lens, r.num_q_heads, H, D)
+        dec_b = decode_bytes_fp8(lens, r.num_q_heads, H, D, r.block_size)
         app_b = len(W["slots"]) * H * D * 6 + 8 * len(W["slots"])
-        step_b = dec_b + app_b + len(W["cows"]) * 2 * H * 16 * D * 2
+        step_b = dec_b + app_b + len(W["cows"]) * 2 * H * r.block_size * D * 2
         for i in range(warmup):
             plans[i % len(plans)].run()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -541,7 +545,7 @@ def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10, only=N
         step_ms = a.elapsed_time(b) / steps
         dec_gbs = dec_b / (dec_ms * 1e-3) / 1e9
         out[name] = {
-            "num_seqs": r.num_seqs, "num_q_heads": r.num_q_heads,
+            "num_seqs": r.num_seqs, "num_q_heads": r.num_q_heads, "block_size": r.block_size,
             "context_tokens": int(lens.sum()), "decode_bytes": dec_b,
             "decode_ms": round(dec_ms, 5), "decode_gbs": round(dec_gbs, 1),
             "decode_frac": round(dec_gbs / peak, 4), "step_ms": round(step_ms, 5),

@@ -831,38 +831,73 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // Fused KV append: sequence b's new tokens (its last q_len, tokens
     // L-q_len .. L-1; row b*q_len + i of k_new/v_new/slot_mapping) are
-    // written by the pieces that read their blocks, before those blocks'
-    // copies are issued: the piece of units [unit0, unit1) writes the new
-    // tokens that fall in them. Generic-proxy stores, then a proxy fence so
-    // the TMA (async proxy) that follows reads the new rows.
+    // written just before the copy of the chunk that reads their unit is
+    // issued (so the chunks before it stream meanwhile). A token's slot, table
+    // entry and K/V rows are loaded together (one memory round trip) -- for
+    // one new token per sequence already at the start of the piece -- then
+    // checked and stored; a proxy fence makes the generic-proxy stores
+    // visible to the TMA (async proxy) that follows.
+    constexpr int CPR = D / 8;   // 16-byte chunks of one K or V row of one head
+    constexpr int kRowMax = 4;   // chunks per lane of one token's rows (H <= 8, D <= 128)
+    static_assert(8 * CPR <= 32 * kRowMax, "append row per lane");
+    struct NewRow {
+      int64_t slot;
+      int e, pos;
+      uint4 k[kRowMax], v[kRowMax];
+    };
+    const int n_row = H * CPR;
+    auto load_row = [&](int b, int pos, int i, NewRow& r) {
+      const size_t tok = size_t(b) * P.q_len + i;
+      r.pos = pos;
+      r.slot = P.slot_mapping[tok];
+      r.e = P.block_tables[size_t(b) * P.max_blocks_per_seq + pos / BS];
+#pragma unroll
+      for (int j = 0; j < kRowMax; ++j) {
+        const int k = lane + 32 * j;
+        if (k < n_row) {
+          r.k[j] = P.k_new[tok * n_row + k];
+          r.v[j] = P.v_new[tok * n_row + k];
+        }
+      }
+    };
+    auto store_row = [&](const NewRow& r) {
+      if (r.slot < 0) return;  // padding token
+      if (r.slot >= int64_t(P.num_blocks) * BS) {
+        if (lane == 0) atomicOr(&g_tc_errors, PA_DEVERR_SLOT);
+        return;
+      }
+      if (r.e < 0 || r.e >= P.num_blocks || r.slot != int64_t(r.e) * BS + r.pos % BS) {
+        if (lane == 0) atomicOr(&g_tc_errors, PA_DEVERR_APPEND_SLOT);
+        return;
+      }
+#pragma unroll
+      for (int j = 0; j < kRowMax; ++j) {
+        const int k = lane + 32 * j;
+        if (k < n_row) {
+          const int hh = k / CPR, ch = k - (k / CPR) * CPR;
+          const size_t dst = ((size_t(r.e) * H + hh) * BS + r.pos % BS) * CPR + ch;
+          P.k_cache_w[dst] = r.k[j];
+          P.v_cache_w[dst] = r.v[j];
+        }
+      }
+    };
+    NewRow pre_row;          // one new token per sequence: loaded at the piece start
+    bool have_pre = false;
+    // the new tokens that fall in units [unit0, unit1) of sequence b
     auto append_tokens = [&](int b, int L, int unit0, int unit1) {
       for (int i = 0; i < P.q_len; ++i) {
         const int pos = L - P.q_len + i;
         if (pos < unit0 * UT || pos >= unit1 * UT) continue;
-        const size_t tok = size_t(b) * P.q_len + i;
-        const int64_t slot = P.slot_mapping[tok];
-        if (slot < 0) continue;  // padding token
-        if (slot >= int64_t(P.num_blocks) * BS) {
-          if (lane == 0) atomicOr(&g_tc_errors, PA_DEVERR_SLOT);
-          continue;
-        }
-        const int e = P.block_tables[size_t(b) * P.max_blocks_per_seq + pos / BS];
-        if (e < 0 || e >= P.num_blocks || slot != int64_t(e) * BS + pos % BS) {
-          if (lane == 0) atomicOr(&g_tc_errors, PA_DEVERR_APPEND_SLOT);
-          continue;
-        }
-        constexpr int CPR = D / 8;  // 16-byte chunks of one row
-        const int n = H * CPR;
-        for (int k = lane; k < n; k += 32) {
-          const int hh = k / CPR, ch = k - (k / CPR) * CPR;
-          const size_t src = tok * n + k;
-          const size_t dst = ((size_t(e) * H + hh) * BS + pos % BS) * CPR + ch;
-          const uint4 kv = P.k_new[src];
-          const uint4 vv = P.v_new[src];
-          P.k_cache_w[dst] = kv;
-          P.v_cache_w[dst] = vv;
+        if (have_pre && pre_row.pos == pos) {
+          store_row(pre_row);
+          have_pre = false;
+        } else {
+          NewRow r;
+          load_row(b, pos, i, r);
+          store_row(r);
         }
       }
+      __syncwarp();
       dev::fence_async_global();
     };
     int b = b_start, off = off_start, unit = u0;
@@ -879,12 +914,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const int seg_nb = min(nb - off, u1 - unit);
       const bool whole = off == 0 && seg_nb == nb;
+      const int new_unit0 = (L_cur - P.q_len) / UT;  // first unit holding a new token
       if constexpr (!F8) {
-        // this piece holds a block of the new tokens
-        if (P.k_new != nullptr && off + seg_nb > (L_cur - P.q_len) / UT) {
-          append_tokens(b, L_cur, off, off + seg_nb);
-          __syncwarp();
-          dev::fence_async_global();
+        if (P.k_new != nullptr && P.q_len == 1 && off + seg_nb > new_unit0) {
+          load_row(b, L_cur - 1, 0, pre_row);  // consumed at the chunk of its unit
+          have_pre = true;
         }
       }
       // prefetched for later: the next sequence's length and first window,
@@ -899,6 +933,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (jb > 0 && (jb & 31) == 0) {
           win = win_nxt;
           win_nxt = jb + 32 < seg_nb ? load_window(b, off + jb + 32) : -1;
+        }
+        if constexpr (!F8) {
+          // this chunk holds a unit of the new tokens
+          const int nu = min(U, seg_nb - jb);
+          if (P.k_new != nullptr && off + jb + nu > new_unit0)
+            append_tokens(b, L_cur, off + jb, off + jb + nu);
         }
         const int slot = chunk_seq % C::ST;
         const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
