@@ -736,8 +736,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   for (int i = tid; i < C::PB * C::P_BYTES / 16; i += NTHREADS)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
 
-  // ---- stream-K plan (uses the still-empty ring as scratch): unit counts of
-  // the sequences, their exclusive prefix, this CTA's range of the stream.
+  // ---- stream-K plan (uses the still-empty ring as scratch). The stream is
+  // measured in cost: a sequence costs its units plus SC for its start (the
+  // epilogue, the new queries and the pipeline turn-over of an extra segment
+  // take about one chunk's time), so CTAs that hold several sequence starts
+  // get fewer units. pre = exclusive prefix of the costs; CTA c takes the
+  // cost range [c R, (c+1) R).
+  const int SC = Units<BS>::GROUPS / H;  // one chunk's units
   int* pre = reinterpret_cast<int*>(ring);
   {
     const int seg = (B + NTHREADS - 1) / NTHREADS;
@@ -747,8 +752,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int L0 = P.context_lens[b];
       if (blockIdx.x == 0 && (L0 > P.cap || (L0 > 0 && L0 < P.q_len)))
         atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
-      const int L = seq_len(P, b);
-      local += (L + UT - 1) / UT;
+      const int n = (seq_len(P, b) + UT - 1) / UT;
+      local += n > 0 ? n + SC : 0;
     }
     int incl = local;
 #pragma unroll
@@ -762,25 +767,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int w = 0; w < warp; ++w) run += reinterpret_cast<int*>(red)[w];
     for (int b = b0; b < b1; ++b) {
       pre[b] = run;
-      run += (seq_len(P, b) + UT - 1) / UT;
+      const int n = (seq_len(P, b) + UT - 1) / UT;
+      run += n > 0 ? n + SC : 0;
     }
     if (tid == NTHREADS - 1) pre[B] = run;
   }
   __syncthreads();
   const int total = pre[B];
   const int R = total > 0 ? (total + int(gridDim.x) - 1) / int(gridDim.x) : 1;
-  const int u0 = min(total, int(blockIdx.x) * R);
+  const int u0 = min(total, int(blockIdx.x) * R);  // this CTA's cost range [u0, u1)
   const int u1 = min(total, u0 + R);
   int b_start = 0;
   if (u0 < u1) {
-    int lo = 0, hi = B;  // largest b with pre[b] <= u0: the sequence holding unit u0
+    int lo = 0, hi = B;  // largest b with pre[b] <= u0: the sequence holding position u0
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (pre[mid] <= u0) lo = mid; else hi = mid;
     }
     b_start = lo;
   }
-  const int off_start = u0 < u1 ? u0 - pre[b_start] : 0;
+  const int cpos_start = u0 < u1 ? pre[b_start] : 0;  // cost position of b_start's start
+  const int off_start = max(0, u0 - cpos_start - SC);  // its first unit in the range
   for (int i = tid; i < 128; i += NTHREADS) {
     alpha_s[i] = 1.0f;  // padded columns stay 1
     colrow[i] = column_row(P, i, GE);
@@ -803,7 +810,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   if (blockIdx.x == 0) {  // the stream-K plan, for the merge kernel
     for (int i = tid; i <= B; i += NTHREADS) P.ws_plan[1 + i] = pre[i];
-    if (tid == 0) P.ws_plan[0] = R;
+    if (tid == 0) P.ws_plan[0] = R;  // (the merge also takes SC)
   }
   dev::fence_async_smem();
   dev::tc_fence_before();
@@ -900,19 +907,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       dev::fence_async_global();
     };
-    int b = b_start, off = off_start, unit = u0;
+    int b = b_start, off = off_start;
+    int cpos = cpos_start;  // cost position of sequence b's start
     int win = win0;
     int L_cur = len0;
-    while (ok && unit < u1) {
+    while (ok && u0 < u1 && b < B) {
       if (*abort_flag) break;
       const int nb = L_cur > 0 ? (L_cur + UT - 1) / UT : 0;  // units
       if (nb == 0) {  // empty sequence: nothing of it in the stream
         ++b;
+        off = 0;
         win = load_window(b, 0);
         L_cur = b < B ? seq_len(P, b) : 0;
         continue;
       }
-      const int seg_nb = min(nb - off, u1 - unit);
+      const int uend = min(nb, u1 - cpos - SC);  // b's units before the range's end
+      if (uend <= off) break;                    // nothing of b (or after it) in range
+      const int seg_nb = uend - off;
       const bool whole = off == 0 && seg_nb == nb;
       const int new_unit0 = (L_cur - P.q_len) / UT;  // first unit holding a new token
       if constexpr (!F8) {
@@ -1021,7 +1032,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) *issued = chunk_seq;
       }
       ++seg_seq;
-      unit += seg_nb;
+      if (uend < nb) break;  // the range ends inside b
+      cpos += nb + SC;
       ++b;
       off = 0;
       win = win_nxt_seq;
@@ -1098,6 +1110,7 @@ struct Row {
 
 struct MergeCols {
   int num_q_heads, num_cols, group_cols, g_log2, q_len;
+  int seg_cost;  // the decode plan's cost of a sequence start (units)
 };
 
 template <int D>
@@ -1128,7 +1141,8 @@ __global__ void __launch_bounds__(128)
     for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(0.0f);
     return;
   }
-  const int c0 = pre0 / R, c1 = (pre1 - 1) / R;
+  // the sequence's units occupy cost positions [pre0 + seg_cost, pre1)
+  const int c0 = (pre0 + mc.seg_cost) / R, c1 = (pre1 - 1) / R;
   if (c0 == c1) return;  // written whole by the decode kernel
   const int nseg = c1 - c0 + 1;
   // piece k of the sequence sits in partial slot (b + c0 + k)
@@ -1381,6 +1395,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   mc.group_cols = qm.group_cols;
   mc.g_log2 = qm.g_log2;
   mc.q_len = qm.query_len;
+  mc.seg_cost = Units<BS>::GROUPS / H;
   e = cudaLaunchKernelEx(&mcfg, merge_segments_kernel<D>, P.out,
                          static_cast<const float*>(P.part_m), static_cast<const float*>(P.part_l),
                          static_cast<const float*>(P.part_acc),
