@@ -93,6 +93,23 @@ def profiled_traffic(summary: str = "pa_decode_tc_llama8b_b64.md"):
     return int(m.group(1))
 
 
+def max_over_ranks(x: float, device, world: int) -> float:
+    """The largest of every rank's x (all ranks call this; one rank returns x)."""
+    if world <= 1:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes: int, steps: int, elapsed_ms: float, world: int) -> float:
+    """Whole-job throughput of N replicas: every rank processes step_bytes per
+    step, and the job takes the slowest rank's time."""
+    return world * step_bytes * steps / (elapsed_ms * 1e-3) / 1e9
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -317,12 +334,9 @@ def run_ours(args, rank: int, world: int) -> dict:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(stop)
     dec_ms = [a.elapsed_time(b) for a, b in evs]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, device, world)
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_b * args.steps / (elapsed_ms * 1e-3) / 1e9
+    value = whole_job_gbs(step_b, args.steps, elapsed_ms, world)
 
     peaks = measured_peaks()
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
