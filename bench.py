@@ -464,25 +464,26 @@ def decode_bytes_fp8(lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
 
 
 class Fp8StepPlan:
-    """One step on the 8-bit cache: copy-on-write copies, the quantising KV
-    write, the decode (query split, decode kernel, merge)."""
+    """One step on the 8-bit cache: copy-on-write copies, then the quantising
+    KV write fused into the decode (pa_append_decode: decode kernel with the
+    write and the query split in its producer, then the merge)."""
 
-    def __init__(self, pk, lib, dec_params, ws, rc_args, cow_args, stream):
-        self.lib, self.dec, self.ws = lib, dec_params, ws
-        self.rc_args, self.cow_args, self.stream = rc_args, cow_args, stream
+    def __init__(self, pk, lib, dec_params, app_params, ws, cow_args, stream):
+        self.lib, self.dec, self.app, self.ws = lib, dec_params, app_params, ws
+        self.cow_args, self.stream = cow_args, stream
 
     def run(self, ev_dec=None):
         lib = self.lib
         if self.cow_args is not None:
             if lib.pa_copy_blocks_fp8(*self.cow_args, self.stream):
                 raise RuntimeError("pa_copy_blocks_fp8 failed")
-        if lib.pa_reshape_and_cache_fp8(*self.rc_args, self.stream):
-            raise RuntimeError("pa_reshape_and_cache_fp8 failed")
         if ev_dec is not None:
             ev_dec[0].record()
-        st = lib.pa_decode(ctypes.byref(self.dec), self.ws.data_ptr(), self.ws.numel(), self.stream)
+        st = lib.pa_append_decode(ctypes.byref(self.dec), ctypes.byref(self.app),
+                                  self.ws.data_ptr(), self.ws.numel(), self.stream)
         if st:
-            raise RuntimeError(f"pa_decode (8-bit cache) failed: {st}: {lib.pa_last_error()}")
+            raise RuntimeError(f"pa_append_decode (8-bit cache) failed: {st}: "
+                               f"{lib.pa_last_error()}")
         if ev_dec is not None:
             ev_dec[1].record()
 
@@ -490,7 +491,8 @@ class Fp8StepPlan:
 def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10, only=None) -> dict:
     """The same workloads on the 8-bit (E4M3) cache: each bf16 pool copy is
     quantised into an E4M3 pool (per-KV-head scales 0.05 for K and V) through
-    pa_reshape_and_cache_fp8, then timed like the bf16 runs."""
+    pa_reshape_and_cache_fp8, then the step (quantising KV write fused into the
+    decode) is timed like the bf16 runs; "decode" is the pa_append_decode call."""
     import torch
 
     lib = pk.load()
@@ -527,13 +529,11 @@ def measure_fp8_workloads(pk, device, steps: int = 200, warmup: int = 10, only=N
                                       max_context_len=int(W["lens"].max()), k_scale=ks, v_scale=vs,
                                       overlap_prologue=True)
             ws = torch.empty(pk.pa_decode_workspace_size(p), dtype=torch.uint8, device=device)
-            rc_args = (W["kn"].data_ptr(), W["vn"].data_ptr(), k8.data_ptr(), v8.data_ptr(),
-                       slots_d.data_ptr(), ks.data_ptr(), vs.data_ptr(), W["kn"].shape[0], H, D,
-                       BS, NB)
+            app = pk.make_append_params(W["kn"], W["vn"], slots_d, k8, v8)
             cow_args = None if cows_d is None else (k8.data_ptr(), v8.data_ptr(),
                                                      cows_d.data_ptr(), cows_d.shape[0], H, D,
                                                      BS, NB)
-            plans.append(Fp8StepPlan(pk, lib, p, ws, rc_args, cow_args, sh))
+            plans.append(Fp8StepPlan(pk, lib, p, app, ws, cow_args, sh))
             keep += [k8, v8, ws]
         del W["copies"]
         torch.cuda.empty_cache()

@@ -257,7 +257,9 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_cac
  *    k_new/v_new/slot_mapping, token L-Q+i); each is written by the part of
  *    the decode that reads its block, with the same slot rule.
  * a->k_cache / a->v_cache must equal p->k_cache / p->v_cache (the caches are
- * written through these). Same workspace as pa_decode. The CUDA-core variant
+ * written through these). With the 8-bit cache (p->kv_dtype PA_KV_FP8_E4M3)
+ * the write is that of pa_reshape_and_cache_fp8 with p->k_scale / p->v_scale
+ * (bit-identical codes). Same workspace as pa_decode. The CUDA-core variant
  * and shapes the tensor-core kernel does not cover run the KV-write kernel
  * and then the decode, with the same result.
  * ---------------------------------------------------------------------- */

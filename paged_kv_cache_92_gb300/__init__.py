@@ -299,28 +299,33 @@ def make_append_params(k_new, v_new, slot_mapping, k_cache, v_cache) -> AppendPa
     a.k_new = _dev_ptr(k_new, torch.bfloat16, "k_new")
     a.v_new = _dev_ptr(v_new, torch.bfloat16, "v_new")
     a.slot_mapping = _dev_ptr(slot_mapping, torch.int64, "slot_mapping")
-    a.k_cache = _dev_ptr(k_cache, torch.bfloat16, "k_cache")
-    a.v_cache = _dev_ptr(v_cache, torch.bfloat16, "v_cache")
+    cache_dtype = torch.uint8 if k_cache.dtype == torch.uint8 else torch.bfloat16
+    a.k_cache = _dev_ptr(k_cache, cache_dtype, "k_cache")
+    a.v_cache = _dev_ptr(v_cache, cache_dtype, "v_cache")
     return a
 
 
 def pa_append_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
                      k_new, v_new, slot_mapping, scale: Optional[float] = None,
                      partition_tokens: int = 0, out=None, workspace=None, stream=None,
-                     variant: int = DECODE_TENSOR_CORE, overlap_prologue: bool = False):
+                     variant: int = DECODE_TENSOR_CORE, overlap_prologue: bool = False,
+                     k_scale=None, v_scale=None):
     """One decode step in one launch: write token b's K/V (``k_new[b]``,
     ``v_new[b]``) at ``slot_mapping[b]`` -- which must be the slot of token
     ``context_lens[b] - 1`` of sequence b -- then paged decode attention over
     the updated caches. Same result as ``pa_reshape_and_cache`` followed by
     ``pa_decode``; returns ``out``. With q [B][Q][Hq][d], row b*Q + i of
-    ``k_new``/``v_new``/``slot_mapping`` is token ``context_lens[b] - Q + i``."""
+    ``k_new``/``v_new``/``slot_mapping`` is token ``context_lens[b] - Q + i``.
+    For the 8-bit cache (uint8 caches, with ``k_scale``/``v_scale``) the write
+    is the quantising one of ``pa_reshape_and_cache_fp8``."""
     import torch
 
     lib = load()
     if out is None:
         out = torch.empty_like(q)
     p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
-                           max_context_len, scale, partition_tokens, variant, overlap_prologue)
+                           max_context_len, scale, partition_tokens, variant, overlap_prologue,
+                           k_scale, v_scale)
     a = make_append_params(k_new, v_new, slot_mapping, k_cache, v_cache)
     need = int(lib.pa_decode_workspace_size(ctypes.byref(p)))
     if workspace is None and need > 0:

@@ -362,10 +362,6 @@ pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
   pa_status st = pa::check_decode(p, true);
   if (st != PA_OK) return st;
   if (!a) return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: append params are NULL");
-  if (p->kv_dtype != PA_KV_BF16)
-    return pa::set_error(PA_ERR_UNSUPPORTED,
-                         "pa_append_decode: bf16 caches only (use pa_reshape_and_cache_fp8 and "
-                         "pa_decode for the 8-bit cache)");
   if (p->num_seqs == 0) return PA_OK;
   if (!a->k_new || !a->v_new || !a->slot_mapping || !a->k_cache || !a->v_cache)
     return pa::set_error(PA_ERR_INVALID_ARG, "pa_append_decode: a required pointer is NULL");

@@ -126,7 +126,7 @@ struct TcCfg {
   // GB300 neither cache type ran faster with it (the softmax spends ~180
   // cycles of its ~1400-2400 per chunk waiting for that product).
   static constexpr int PB = 1;
-  static constexpr int MISC_BYTES = 4096;
+  static constexpr int MISC_BYTES = 4224;
   // Q buffers: two let the next segment's queries load while the current
   // segment runs; at N = 128 only one fits beside a two-slot ring.
   static constexpr int QB =
@@ -153,8 +153,9 @@ struct TcCfg {
   static constexpr int OFF_MS = OFF_LS + 128 * 4;                            // [128]
   static constexpr int OFF_WORDS = OFF_MS + 128 * 4;
   static constexpr int OFF_QALPHA = OFF_WORDS + 64;       // F8: [2 q slots][64] 1/alpha
-  static constexpr int OFF_KVSCALE = OFF_QALPHA + 2 * 64 * 4;  // F8: k_scale[8], v_scale[8]
-  static constexpr int OFF_COLROW = OFF_KVSCALE + 64;  // [128] output row of each column
+  // F8: k_scale[8], v_scale[8], then their reciprocals (the fused KV write)
+  static constexpr int OFF_KVSCALE = OFF_QALPHA + 2 * 64 * 4;
+  static constexpr int OFF_COLROW = OFF_KVSCALE + 128;  // [128] output row of each column
   static constexpr int SMEM = OFF_COLROW + 128 * 4 + 1024;  // + alignment slack
   static_assert(OFF_COLROW + 128 * 4 <= OFF_MISC + MISC_BYTES, "misc area");
   static_assert(N <= 128 && (!F8 || N <= 64), "columns");
@@ -171,6 +172,25 @@ struct TcCfg {
   static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
   static constexpr uint32_t Q_TX = Q_BYTES + (F8 ? N * 4 : 0);  // F8: + 1/alpha per column
 };
+
+// x / s rounded to nearest even, for a positive normal s with r = RN(1/s):
+// Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990; also Muller et al., Handbook of Floating-Point Arithmetic, on
+// division with a fused multiply-add). q0 = RN(x r) lies within one ulp of
+// x / s, the remainder x - q0 s is exact in one FMA, and RN(q0 + rem r) is
+// the correctly rounded quotient while nothing underflows. A non-finite q0
+// (x infinite or NaN, or x / s past the float range) is returned as it is,
+// which is the division's own result there, and so is a zero q0, whose sign
+// the correction would lose (+0 + -0 = +0). Quotients below the float
+// normal range may differ in the last place; the 8-bit write maps every
+// quotient below 2^-10 to a signed zero, so its codes do not depend on it.
+__device__ __forceinline__ float div_rn_by(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  if (!isfinite(q0) || q0 == 0.0f) return q0;  // a zero keeps the sign of x
+  const float rem = __fmaf_rn(-q0, s, x);
+  return __fmaf_rn(rem, r, q0);
+}
 
 struct TcParams {
   const int32_t* block_tables;
@@ -297,7 +317,8 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       const uint32_t pbc = pbs + uint32_t(c % C::PB) * C::P_BYTES;  // this chunk's P
       const int sl = c % C::ST;
       // O accumulates over a segment's chunks; its first chunk starts afresh
-      const bool fresh = (meta[sl].flags & F_FIRST) != 0;
+      const int fl = meta[sl].flags, qsl = meta[sl].qslot;  // read before the slot is freed
+      const bool fresh = (fl & F_FIRST) != 0;
       dev::tc_fence_after();
       const uint32_t vb = dev::smem_addr(ring + size_t(sl) * C::SLOT_BYTES + C::K_BYTES);
       if constexpr (F8) {
@@ -324,6 +345,11 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       }
       dev::mma_commit(&bar_o[c % C::PB]);
       dev::mma_commit(&empty[sl]);
+      // 8-bit cache: the softmax reads the segment's 1/alpha until it has
+      // written this chunk's P, so the query slot is released only here
+      if constexpr (F8) {
+        if (fl & F_LAST) dev::mma_commit(&qempty[qsl]);
+      }
       ++c;
       progress = true;
     }
@@ -341,7 +367,9 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
         issue_scores<D, N, F8>(tmem + sb * C::NS, ring + size_t(sl) * C::SLOT_BYTES,
                                qbuf + mn.qslot * C::Q_BYTES);
         dev::mma_commit(&bar_s[sb]);
-        if (mn.flags & F_LAST) dev::mma_commit(&qempty[mn.qslot]);
+        if constexpr (!F8) {
+          if (mn.flags & F_LAST) dev::mma_commit(&qempty[mn.qslot]);
+        }
       }
       ++s_pos;
       progress = true;
@@ -806,7 +834,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   dev::griddep_wait();
   if constexpr (F8) {  // per-KV-head scales: k_scale in [0, 8), v_scale in [8, 16)
-    if (tid < 16) kvscale[tid] = (tid & 7) < H ? (tid < 8 ? P.k_scale : P.v_scale)[tid & 7] : 1.0f;
+    if (tid < 16) {
+      const float sc = (tid & 7) < H ? (tid < 8 ? P.k_scale : P.v_scale)[tid & 7] : 1.0f;
+      kvscale[tid] = sc;
+      kvscale[16 + tid] = __frcp_rn(sc);
+    }
   }
   if (blockIdx.x == 0) {  // the stream-K plan, for the merge kernel
     for (int i = tid; i <= B; i += NTHREADS) P.ws_plan[1 + i] = pre[i];
@@ -882,9 +914,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int k = lane + 32 * j;
         if (k < n_row) {
           const int hh = k / CPR, ch = k - (k / CPR) * CPR;
-          const size_t dst = ((size_t(r.e) * H + hh) * BS + r.pos % BS) * CPR + ch;
-          P.k_cache_w[dst] = r.k[j];
-          P.v_cache_w[dst] = r.v[j];
+          const int off = r.pos % BS;
+          if constexpr (F8) {
+            // the quantising write of the 8-bit cache: code = E4M3(x / scale),
+            // K as 8 bytes of its row, V as 8 bytes of its column of the
+            // tile's 16-key V^T sub-tile
+            const size_t tile = (size_t(r.e) * H + hh) * BS * D;
+            uint8_t* kc = reinterpret_cast<uint8_t*>(P.k_cache_w);
+            uint8_t* vc = reinterpret_cast<uint8_t*>(P.v_cache_w);
+            float kf[8], vf[8];
+            dev::unpack8(r.k[j], kf);
+            dev::unpack8(r.v[j], vf);
+            uint32_t kw0 = 0, kw1 = 0;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const uint32_t code = dev::to_e4m3(div_rn_by(kf[t], kvscale[hh], kvscale[16 + hh]));
+              if (t < 4) kw0 |= code << (8 * t); else kw1 |= code << (8 * (t - 4));
+            }
+            *reinterpret_cast<uint2*>(kc + tile + size_t(off) * D + ch * 8) = make_uint2(kw0, kw1);
+            uint8_t* vsub = vc + tile + size_t(off >> 4) * kF8Tile * D + (off & 15);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              vsub[size_t(ch * 8 + t) * kF8Tile] =
+                  dev::to_e4m3(div_rn_by(vf[t], kvscale[8 + hh], kvscale[24 + hh]));
+          } else {
+            const size_t dst = ((size_t(r.e) * H + hh) * BS + off) * CPR + ch;
+            P.k_cache_w[dst] = r.k[j];
+            P.v_cache_w[dst] = r.v[j];
+          }
         }
       }
     };
@@ -904,8 +961,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           store_row(r);
         }
       }
-      __syncwarp();
+      // each lane fences its own stores, then the warp syncs, so the copies
+      // the issuing lanes start next see every lane's stores
       dev::fence_async_global();
+      __syncwarp();
     };
     int b = b_start, off = off_start;
     int cpos = cpos_start;  // cost position of sequence b's start
@@ -926,11 +985,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int seg_nb = uend - off;
       const bool whole = off == 0 && seg_nb == nb;
       const int new_unit0 = (L_cur - P.q_len) / UT;  // first unit holding a new token
-      if constexpr (!F8) {
-        if (P.k_new != nullptr && P.q_len == 1 && off + seg_nb > new_unit0) {
-          load_row(b, L_cur - 1, 0, pre_row);  // consumed at the chunk of its unit
-          have_pre = true;
-        }
+      if (P.k_new != nullptr && P.q_len == 1 && off + seg_nb > new_unit0) {
+        load_row(b, L_cur - 1, 0, pre_row);  // consumed at the chunk of its unit
+        have_pre = true;
       }
       // prefetched for later: the next sequence's length and first window,
       // this segment's second window
@@ -945,8 +1002,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           win = win_nxt;
           win_nxt = jb + 32 < seg_nb ? load_window(b, off + jb + 32) : -1;
         }
-        if constexpr (!F8) {
-          // this chunk holds a unit of the new tokens
+        {  // this chunk holds a unit of the new tokens
           const int nu = min(U, seg_nb - jb);
           if (P.k_new != nullptr && off + jb + nu > new_unit0)
             append_tokens(b, L_cur, off + jb, off + jb + nu);

@@ -216,3 +216,137 @@ def test_fp8_unsupported_shapes_are_rejected(pk):
     with pytest.raises(pk.PagedKVError):
         pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
                      max_context_len=20, k_scale=ks, v_scale=vs, variant=pk.DECODE_CUDA_CORE)
+
+
+# ---------------------------------------------------------------- the write fused into the decode
+
+
+def _fused_fp8(pk, lens, Hq, Hkv, seed, QL=1, bad=None, bs=16):
+    """pa_append_decode on the 8-bit cache: the new tokens' (the last QL of each
+    sequence) slots are overwritten with the quantised rows of k_new/v_new, as
+    pa_reshape_and_cache_fp8 would, before the decode reads them."""
+    import torch
+
+    D = 128
+    lens = np.asarray(lens, dtype=np.int64)
+    NB = int(((lens + bs - 1) // bs).sum()) + 3
+    order = np.random.default_rng(seed).permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, bs)
+    q = workloads.bf16_normal((len(lens), QL, Hq, D) if QL > 1 else (len(lens), Hq, D), seed + 1,
+                              "cuda")
+    ks = torch.from_numpy(_scales(Hkv, seed + 4, 0.05)).cuda()
+    vs = torch.from_numpy(_scales(Hkv, seed + 5, 0.03)).cuda()
+    # the pool before the step: every slot holds the oracle's codes of bf16
+    # N(0,1) rows; the padding slots of each last block hold the NaN code
+    k0, v0 = oracle.reshape_and_cache_fp8(
+        workloads.bf16_normal((NB * bs, Hkv, D), seed + 6, "cpu"),
+        workloads.bf16_normal((NB * bs, Hkv, D), seed + 7, "cpu"),
+        np.zeros((NB, Hkv, bs, D), np.uint8), np.zeros((NB, Hkv, bs, D), np.uint8),
+        np.arange(NB * bs, dtype=np.int64), ks.cpu().numpy(), vs.cpu().numpy())
+    v0 = v0.reshape(NB, Hkv, bs // 16, D, 16)
+    for b, L in enumerate(lens):
+        if L % bs:
+            blk = int(tables[b, (L - 1) // bs])
+            k0[blk, :, L % bs:, :] = NAN8
+            for o in range(int(L % bs), bs):
+                v0[blk, :, o // 16, :, o % 16] = NAN8
+    slots = []
+    for b, L in enumerate(lens):
+        for i in range(QL):
+            pos = int(L) - QL + i
+            slots.append(int(tables[b, pos // bs]) * bs + pos % bs)
+    slots = np.array(slots, dtype=np.int64)
+    if bad is not None:
+        slots = bad(slots)
+    T = len(slots)
+    kn = workloads.bf16_normal((T, Hkv, D), seed + 2, "cuda")
+    vn = workloads.bf16_normal((T, Hkv, D), seed + 3, "cuda")
+    k8, v8 = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    out = pk.pa_append_decode(q, k8, v8, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens.astype(np.int32)).cuda(), int(lens.max()),
+                              kn, vn, torch.from_numpy(slots).cuda(), k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    return dict(q=q, k0=k0, v0=v0, k8=k8, v8=v8, kn=kn, vn=vn, ks=ks, vs=vs, slots=slots,
+                tables=tables, lens=lens.astype(np.int32), out=out, NB=NB, Hkv=Hkv, bs=bs)
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("QL", [1, 2])
+def test_fp8_fused_append_matches_the_quantising_write_and_oracle(pk, bs, QL):
+    lens = [QL, 15, 16, 17, 33, 100, 513, 2049]
+    c = _fused_fp8(pk, lens, 32, 8, seed=60 + bs + QL, QL=QL, bs=bs)
+    assert pk.pa_device_errors() == 0
+    NB, Hkv, D = c["NB"], c["Hkv"], 128
+    ks, vs = c["ks"].cpu().numpy(), c["vs"].cpu().numpy()
+    ko, vo = oracle.reshape_and_cache_fp8(c["kn"].cpu(), c["vn"].cpu(), c["k0"],
+                                          c["v0"].reshape(NB, Hkv, bs, D), c["slots"], ks, vs)
+    assert np.array_equal(c["k8"].cpu().numpy(), ko)
+    assert np.array_equal(c["v8"].cpu().numpy().reshape(NB, Hkv, bs, D), vo)
+    if QL > 1:
+        want = oracle.paged_decode_multi_fp8(c["q"].cpu(), ko, vo, ks, vs, c["tables"], c["lens"])
+    else:
+        want = oracle.paged_decode_fp8(c["q"].cpu(), ko, vo, ks, vs, c["tables"], c["lens"])
+    harness.assert_close(harness.bf16_tensor_to_f64(c["out"]), want)
+
+
+def test_fp8_fused_append_slot_rules(pk):
+    """A slot that is not its token's is not written (PA_DEVERR_APPEND_SLOT); a
+    negative slot writes nothing."""
+    def bad(s):
+        s = s.copy()
+        s[1] = s[1] + 1 if s[1] % 16 != 15 else s[1] - 1
+        s[2] = -1
+        return s
+
+    c = _fused_fp8(pk, [40, 70, 33], 16, 4, seed=71, bad=bad)
+    assert pk.pa_device_errors() & 0x20
+    NB, Hkv, D = c["NB"], c["Hkv"], 128
+    keep = [0]
+    ko, vo = oracle.reshape_and_cache_fp8(c["kn"].cpu()[keep], c["vn"].cpu()[keep], c["k0"],
+                                          c["v0"].reshape(NB, Hkv, 16, D), c["slots"][keep],
+                                          c["ks"].cpu().numpy(), c["vs"].cpu().numpy())
+    assert np.array_equal(c["k8"].cpu().numpy(), ko)
+    assert np.array_equal(c["v8"].cpu().numpy().reshape(NB, Hkv, 16, D), vo)
+
+
+@pytest.mark.parametrize("scale_set", [0, 1, 2])
+def test_fp8_fused_write_every_bf16_value(pk, scale_set):
+    """The fused write divides by the head's scale with a reciprocal and one
+    correction step; its codes must equal the oracle's for every bf16 bit
+    pattern (zeros, subnormals, infinities and NaNs included), for power-of-two
+    and other scales. 64 sequences append one token each with 8 KV heads of
+    128 values: 65,536 K and 65,536 V values per call."""
+    import torch
+
+    B, Hkv, D, bs = 64, 8, 128, 16
+    rng = np.random.default_rng(90 + scale_set)
+    lens = rng.integers(1, 100, size=B).astype(np.int64)
+    NB = int(((lens + bs - 1) // bs).sum()) + 2
+    order = rng.permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, bs)
+    slots = np.array([int(tables[b, (L - 1) // bs]) * bs + (L - 1) % bs
+                      for b, L in enumerate(lens)], dtype=np.int64)
+    bits = np.arange(65536, dtype=np.uint16)
+    kn = torch.from_numpy(bits.view(np.int16).reshape(B, Hkv, D).copy()).view(torch.bfloat16)
+    vn = torch.from_numpy(rng.permutation(bits).view(np.int16).reshape(B, Hkv, D).copy()
+                          ).view(torch.bfloat16)
+    if scale_set == 0:
+        ks = np.array([1.0, 0.5, 0.25, 2.0, 0.0625, 4.0, 0.125, 1.0], np.float32)
+        vs = np.array([0.75, 3.0, 0.1, 0.3, 7.0, 0.01, 1.5, 0.2], np.float32)
+    else:
+        ks = (np.exp(rng.uniform(-6, 4, size=Hkv))).astype(np.float32)
+        vs = (np.exp(rng.uniform(-6, 4, size=Hkv))).astype(np.float32)
+    k0 = rng.integers(0, 0x7F, size=(NB, Hkv, bs, D), dtype=np.uint8)
+    v0 = rng.integers(0, 0x7F, size=(NB, Hkv, bs, D), dtype=np.uint8)
+    k8 = torch.from_numpy(k0).cuda()
+    v8 = torch.from_numpy(v0.reshape(NB, Hkv, bs // 16, D, 16)).cuda()  # V^T sub-tiles
+    q = workloads.bf16_normal((B, 32, D), 93, "cuda")
+    pk.pa_append_decode(q, k8, v8, torch.from_numpy(tables).cuda(),
+                        torch.from_numpy(lens.astype(np.int32)).cuda(), int(lens.max()),
+                        kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda(),
+                        k_scale=torch.from_numpy(ks).cuda(), v_scale=torch.from_numpy(vs).cuda())
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() == 0
+    ko, vo = oracle.reshape_and_cache_fp8(kn, vn, k0, v0, slots, ks, vs)
+    assert np.array_equal(k8.cpu().numpy(), ko)
+    assert np.array_equal(v8.cpu().numpy().reshape(NB, Hkv, bs, D), vo)
