@@ -665,7 +665,9 @@ def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int
     """The same step end to end through ``pa_step_host``: each step is one C
     call that copies the packed inputs (q, new K/V, slots, tables, lengths,
     copy-on-write pairs) from pinned host memory to the device, runs the
-    step, copies the output back to pinned host memory and synchronises."""
+    step, returns the output to pinned host memory and synchronises. Both
+    buffers are pinned, so a kernel reads the inputs over the host link and
+    the decode writes the output rows into host memory (no DMA copies)."""
     import torch
 
     lib = pk.load()
@@ -702,8 +704,9 @@ def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int
     return {"value": round(step_b * steps / dt / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(host_in.numel()), "d2h_bytes_per_step": int(host_out.numel() * 2),
             "ms_per_step": round(dt / steps * 1e3, 4),
-            "api": "pa_step_host (one C call per step: H2D of the packed inputs, copy-on-write, "
-                   "fused KV write + decode + merge, D2H of the output, stream sync)"}
+            "api": "pa_step_host (one C call per step: a kernel stages the packed inputs from "
+                   "pinned host memory over the host link, copy-on-write, fused KV write + decode "
+                   "+ merge writing the output rows into pinned host memory, stream sync)"}
 
 def _oracle_sample_inputs(r: workloads.Recipe):
     """Host layout and contents for the oracle (its own pool model)."""

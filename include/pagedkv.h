@@ -283,11 +283,17 @@ pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
  * taken from one packed host buffer and the output returned to host memory.
  *
  * The call enqueues on `stream`
- *   1. one host->device copy of the packed inputs into the workspace,
+ *   1. the staging of the packed inputs into the workspace,
  *   2. pa_copy_blocks (if num_cow_pairs > 0), then pa_append_decode on the
  *      staged inputs and the device-resident caches,
- *   3. one device->host copy of the output,
+ *   3. the return of the output to host_out,
  * and synchronises the stream before it returns (the output is in host_out).
+ * Pinned host memory (page-locked through CUDA, hence mapped under unified
+ * addressing) that is 16-byte aligned is read and written by the kernels
+ * themselves over the host link (NVLink-C2C on a Grace-Blackwell part): a
+ * staging kernel copies host_in into the workspace, and the decode writes its
+ * output rows straight into host_out. Any other host memory goes through one
+ * DMA copy each way (cudaMemcpyAsync). The bytes moved are the same.
  *
  * Packed input (host memory; pinned memory lets the copy run at full speed):
  * sections at the byte offsets pa_step_host_layout reports, each 256-byte

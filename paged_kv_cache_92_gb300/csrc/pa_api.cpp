@@ -212,6 +212,21 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
 
 // ---- host-driven step: packed input layout and the decode params over it
 
+// The device address of host memory `p` when kernels can reach it (memory
+// pinned through CUDA, mapped under unified addressing) and it is `align`-byte
+// aligned there; nullptr otherwise (pageable memory, or an address CUDA does
+// not know). Clears the error that the query leaves for unknown addresses.
+static const void* device_view(const void* p, size_t align) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+  if (reinterpret_cast<uintptr_t>(at.devicePointer) % align != 0) return nullptr;
+  return at.devicePointer;
+}
+
 static pa_status check_step(const pa_step_host_params* p) {
   if (!p) return set_error(PA_ERR_INVALID_ARG, "pa_step_host: params is NULL");
   if (p->num_seqs < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->head_dim < 1 ||
@@ -423,8 +438,20 @@ pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t wor
   st = pa::check_decode(&d, true);
   if (st != PA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(ws, p->host_in, sp.in.total, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: input copy", int(e));
+  // Pinned host buffers are addressable from kernels (over NVLink-C2C on a
+  // Grace-Blackwell part): a kernel then stages the inputs, and the decode
+  // writes the output rows straight into host_out. Other host memory goes
+  // through DMA copies.
+  const void* in_dev = pa::device_view(p->host_in, 16);
+  void* out_dev = const_cast<void*>(pa::device_view(p->host_out, 16));
+  cudaError_t e = cudaSuccess;
+  if (in_dev) {
+    const int r = pa::launch_stage_in(in_dev, ws, sp.in.total, stream);
+    if (r != 0) return pa::set_cuda_error("pa_step_host: input staging launch", r);
+  } else {
+    e = cudaMemcpyAsync(ws, p->host_in, sp.in.total, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: input copy", int(e));
+  }
   if (p->num_cow_pairs > 0) {
     const int r = pa::launch_copy_blocks(p->k_cache, p->v_cache,
                                          reinterpret_cast<const int32_t*>(ws + sp.in.cow_pairs),
@@ -440,12 +467,15 @@ pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t wor
     a.k_cache = p->k_cache;
     a.v_cache = p->v_cache;
     const pa::WorkspaceLayout w = pa::decode_workspace_layout(&d, np, grid);
+    if (out_dev) d.out = out_dev;
     st = pa::run_decode(&d, ws + sp.dec_off, w, np, grid, stream, "pa_step_host", &a);
     if (st != PA_OK) return st;
-    e = cudaMemcpyAsync(p->host_out, ws + sp.out_off,
-                        size_t(p->num_seqs) * p->num_q_heads * p->head_dim * 2,
-                        cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: output copy", int(e));
+    if (!out_dev) {
+      e = cudaMemcpyAsync(p->host_out, ws + sp.out_off,
+                          size_t(p->num_seqs) * p->num_q_heads * p->head_dim * 2,
+                          cudaMemcpyDeviceToHost, s);
+      if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: output copy", int(e));
+    }
   }
   e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: synchronize", int(e));

@@ -79,7 +79,37 @@ __global__ void __launch_bounds__(256)
     d[i] = s[i];
 }
 
+// A plain copy of n16 16-byte chunks (then `tail` bytes) from memory the GPU
+// reads over the host link -- pinned host memory -- into device memory: the
+// staging of a host-driven step's packed inputs. Each thread issues its two
+// loads before its stores, so a warp has two link round trips in flight.
+__global__ void __launch_bounds__(256)
+    stage_in_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n16,
+                    int tail) {
+  const int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 2;
+  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+  if (i < n16) a = src[i];
+  if (i + 1 < n16) b = src[i + 1];
+  if (i < n16) dst[i] = a;
+  if (i + 1 < n16) dst[i + 1] = b;
+  if (i == 0)
+    for (int t = 0; t < tail; ++t)
+      reinterpret_cast<uint8_t*>(dst + n16)[t] = reinterpret_cast<const uint8_t*>(src + n16)[t];
+}
+
 }  // namespace
+
+int launch_stage_in(const void* src, void* dst, size_t bytes, void* stream) {
+  if (bytes == 0) return int(cudaSuccess);
+  const int64_t n16 = int64_t(bytes / 16);
+  const int tail = int(bytes % 16);
+  const int threads = 256;
+  const int64_t blocks = (n16 + 2 * threads - 1) / (2 * threads);
+  stage_in_kernel<<<unsigned(blocks > 0 ? blocks : 1), threads, 0,
+                    static_cast<cudaStream_t>(stream)>>>(static_cast<const uint4*>(src),
+                                                         static_cast<uint4*>(dst), n16, tail);
+  return int(cudaGetLastError());
+}
 
 int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,

@@ -141,6 +141,10 @@ int read_and_clear_fp8_errors(uint32_t* flags);
 // bytes, hi rows then lo rows, and [B][n_pad] floats 1/alpha).
 int launch_permute_q(const void* q, void* qp, const QueryMap& m, void* stream);
 int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap& m, void* stream);
+// Copy `bytes` from src -- host memory the GPU can address (pinned, mapped
+// under unified addressing), 16-byte aligned -- to device memory dst (16-byte
+// aligned), with a kernel rather than a DMA copy (pa_cache.cu).
+int launch_stage_in(const void* src, void* dst, size_t bytes, void* stream);
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                        int32_t num_blocks, void* stream);

@@ -488,3 +488,35 @@ def test_step_host_matches_device_step(pk, name, variant):
     assert np.array_equal(oracle.bf16_bits(kc.cpu()), ko)
     assert np.array_equal(oracle.bf16_bits(vc.cpu()), vo)
     _check_errors(pk)
+
+
+@pytest.mark.parametrize("pinned_in,pinned_out", [(False, False), (True, False), (False, True)])
+def test_step_host_pageable_buffers(pk, pinned_in, pinned_out):
+    """Pinned buffers are read and written by the kernels themselves; pageable
+    ones take the DMA copies. Every mix gives the device-side step's output
+    and caches bit for bit."""
+    import torch
+
+    case = harness.build_case(FUSED_CASES["shared_prefix"]())
+    want, kw, vw = harness.run_step_gpu(case, variant=0, fused_append=True)
+    kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    B, Hq, D = case.q.shape
+    p = pk.make_step_host_params(kc, vc, B, Hq, case.tables.shape[1], int(case.lens.max()),
+                                 num_cow_pairs=len(case.cows))
+    host_in = pk.pack_step_inputs(p, case.q.cpu(), case.k_new.cpu(), case.v_new.cpu(), case.slots,
+                                  case.tables, case.lens, case.cows if len(case.cows) else None,
+                                  pin=pinned_in)
+    host_out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16)
+    if pinned_out:
+        host_out = host_out.pin_memory()
+    assert host_in.is_pinned() == pinned_in and host_out.is_pinned() == pinned_out
+    ws = torch.empty(pk.pa_step_host_workspace_size(p), dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace
+        pk.pa_step_host(p, host_in, host_out, ws)
+        assert torch.equal(host_out.view(torch.int16), want.cpu().view(torch.int16))
+        kc.copy_(case.k_cache)
+        vc.copy_(case.v_cache)
+    pk.pa_step_host(p, host_in, host_out, ws)
+    assert torch.equal(kc.view(torch.int16), kw.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vw.view(torch.int16))
+    _check_errors(pk)
