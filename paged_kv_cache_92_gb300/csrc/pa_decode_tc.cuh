@@ -83,6 +83,15 @@ struct Units {
   static constexpr int VS = BS / GB;            // units per block (1, or 2 at block size 32)
   static constexpr int GROUPS = ROWS / GB;      // groups per chunk
 };
+// P^T per 16-key step (bf16, head_dim 128, 64 query columns, a KV head owning
+// >= 8 of them, 16 tokens per unit): a 16-key step of the chunk is one (unit,
+// KV head), and P is block-diagonal, so the value product runs per step over
+// the 16 columns that hold the step's head, from a [16 columns][16 keys] tile
+// whose other columns are zero. P takes 4 KiB instead of 16 KiB, which makes
+// room for a third 64 KiB ring slot. (At 128 columns it frees no slot, and
+// its narrower P stores made the step slower.)
+template <int D, int GE, int N, bool F8, int BS>
+constexpr bool kDiagP = !F8 && D == 128 && GE >= 8 && N == 64 && Units<BS>::GB == 16;
 constexpr int kF8Tile = 16;  // keys of one 8-bit V^T sub-tile
 constexpr int kMaxDynSmem = 232448;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -109,8 +118,9 @@ struct __align__(16) ChunkMeta {
 // F8: the 8-bit (E4M3) cache. K rows are D bytes (one 128-byte atom at
 // D = 128); V^T comes as one [D][16 keys] tile per (block, KV head), side by
 // side; Q and P are each split into an E4M3 hi and lo term.
-template <int D, int N, bool F8 = false>
+template <int D, int N, bool F8 = false, bool DIAG = false>
 struct TcCfg {
+  static_assert(!DIAG || (!F8 && D == 128 && N == 64), "per-head P tiles");
   static constexpr int HALVES = F8 ? 1 : D / 64;   // 128-byte swizzle atoms per K row
   static constexpr int HALF_BYTES = ROWS * 128;    // [128 rows][64 bf16] or [128 rows][128 e4m3]
   static constexpr int K_BYTES = HALVES * HALF_BYTES;
@@ -120,7 +130,8 @@ struct TcCfg {
   static constexpr int QH_BYTES = N * 128;         // [N rows][64 bf16] or [N rows][128 e4m3]
   static constexpr int Q_BYTES = F8 ? 2 * QH_BYTES : HALVES * QH_BYTES;  // F8: hi, lo
   static constexpr int PH_BYTES = N * 128;         // P^T [N rows][64 keys] or [N rows][128 keys]
-  static constexpr int P_BYTES = 2 * PH_BYTES;     // bf16: 128 keys; F8: hi and lo
+  // bf16: 128 keys; F8: hi and lo; DIAG: 8 steps of [16 columns][16 keys]
+  static constexpr int P_BYTES = DIAG ? (ROWS / 16) * 512 : 2 * PH_BYTES;
   // P buffers. One: a second buffer would let the softmax write P(c) while
   // the value product of c-1 still reads P, but it costs a ring slot, and on
   // GB300 neither cache type ran faster with it (the softmax spends ~180
@@ -128,12 +139,17 @@ struct TcCfg {
   static constexpr int PB = 1;
   static constexpr int MISC_BYTES = 4224;
   // Q buffers: two let the next segment's queries load while the current
-  // segment runs; at N = 128 only one fits beside a two-slot ring.
+  // segment runs. One is kept when a second would cost a ring slot (at
+  // N = 128, and at N = 64 with per-head P tiles: three slots instead of two).
+  static constexpr int ST_CAP = F8 ? 6 : 4;
+  static constexpr int FIT_Q2 =
+      (kMaxDynSmem - 1024 - 2 * Q_BYTES - PB * P_BYTES - MISC_BYTES) / SLOT_BYTES;
+  static constexpr int FIT_Q1 =
+      (kMaxDynSmem - 1024 - Q_BYTES - PB * P_BYTES - MISC_BYTES) / SLOT_BYTES;
   static constexpr int QB =
-      (kMaxDynSmem - 1024 - 2 * Q_BYTES - PB * P_BYTES - MISC_BYTES) / SLOT_BYTES >= 2 ? 2 : 1;
+      FIT_Q2 >= 2 && (FIT_Q2 >= ST_CAP || FIT_Q2 >= FIT_Q1) ? 2 : 1;
   static constexpr int ST_FIT =
       (kMaxDynSmem - 1024 - QB * Q_BYTES - PB * P_BYTES - MISC_BYTES) / SLOT_BYTES;
-  static constexpr int ST_CAP = F8 ? 6 : 4;
   static constexpr int ST = ST_FIT > ST_CAP ? ST_CAP : ST_FIT;
   static_assert(!F8 || D == 128, "the 8-bit cache is built for head_dim 128");
   static_assert(ST >= 2, "at least a double-buffered ring");
@@ -169,6 +185,7 @@ struct TcCfg {
       F8 ? dev::idesc_e4m3_f32(ROWS, NS) : dev::idesc_bf16_f32(ROWS, N, false, false);
   static constexpr uint32_t IDESC_PV =
       F8 ? dev::idesc_e4m3_f32(ROWS, NS) : dev::idesc_bf16_f32(ROWS, N, true, false);
+  static constexpr uint32_t IDESC_PV16 = dev::idesc_bf16_f32(ROWS, 16, true, true);  // DIAG
   static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
   static constexpr uint32_t Q_TX = Q_BYTES + (F8 ? N * 4 : 0);  // F8: + 1/alpha per column
 };
@@ -256,6 +273,15 @@ __device__ __forceinline__ uint32_t p8_offset(int n, int key) {
   return uint32_t(grp * 1024 + r * 128 + (((key >> 4) ^ r) << 4) + (key & 15));
 }
 
+// Byte offset of the 8 columns [8 cg, 8 cg + 8) of key t in the per-head P^T
+// tile of 16-key step kk (columns within the step's 16-column window): the
+// B operand MN-major without swizzle, core matrices of 8 keys x 16 bytes (8
+// columns), the next 8 keys 128 bytes on, the next 8 columns 256 bytes on.
+// A thread (one key) writes its 8 columns as one 16-byte store.
+__device__ __forceinline__ uint32_t pdiag_offset(int kk, int cg, int t) {
+  return uint32_t(kk * 512 + cg * 256 + (t >> 3) * 128 + (t & 7) * 16);
+}
+
 // S^T = Kchunk . Q^T for one chunk (single thread). bf16: D/16 MMAs of K = 16.
 // E4M3: D/32 MMAs of K = 32, each over both query terms at once.
 template <int D, int N, bool F8>
@@ -288,13 +314,13 @@ __device__ __forceinline__ void issue_scores(uint32_t tmem_col, const unsigned c
 // the chunk has landed, and O^T = V^T.P^T once the softmax warps have written
 // P for it. Scores run one chunk ahead of the value product.
 // ---------------------------------------------------------------------------
-template <int D, int N, bool F8>
+template <int D, int GE, int N, bool F8, bool DIAG>
 __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbuf,
                                          unsigned char* pbuf, uint64_t* full, uint64_t* empty,
                                          uint64_t* qempty, uint64_t* bar_s, uint64_t* bar_o,
                                          uint64_t* bar_p, uint64_t* drain, const ChunkMeta* meta,
-                                         uint32_t tmem, volatile int* abort_flag) {
-  using C = TcCfg<D, N, F8>;
+                                         uint32_t tmem, volatile int* abort_flag, int H) {
+  using C = TcCfg<D, N, F8, DIAG>;
   // D = 64: the second 64-row half of M re-reads the first (LBO 0); those
   // TMEM lanes are never read back.
   const uint32_t lbo = C::HALVES == 2 ? uint32_t(C::HALF_BYTES) : 0u;
@@ -333,6 +359,23 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
                                        dev::kSwizzleNone),
                         dev::smem_desc(pbc + kk * 32, 16, 1024, dev::kSwizzle128B), C::IDESC_PV,
                         kk > 0 || !fresh);
+      } else if constexpr (DIAG) {
+        // step kk = (unit kk / H, KV head kk % H): O^T columns of the 16-wide
+        // window holding that head's columns. With 8 columns per head a
+        // window holds two heads; the first step of the pair in a chunk
+        // starts it afresh in a segment's first chunk, the second (zero
+        // P^T for the first head's columns) adds on.
+#pragma unroll
+        for (int kk = 0; kk < ROWS / 16; ++kk) {
+          const int h = kk % H;
+          const bool first = kk < H && (GE >= 16 || (h & 1) == 0);
+          dev::mma_bf16(tmem + C::kSBufs * C::NS + uint32_t((h * GE) & ~15),
+                        dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
+                        // MN-major, no swizzle: next 8 keys (K) 128 B on, next 8
+                        // columns (N) 256 B on
+                        dev::smem_desc(pbc + kk * 512, 128, 256, dev::kSwizzleNone),
+                        C::IDESC_PV16, !(fresh && first));
+        }
       } else {
 #pragma unroll
         for (int kk = 0; kk < ROWS / 16; ++kk) {
@@ -403,7 +446,7 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
 // ---------------------------------------------------------------------------
 template <int D, int GE, int N, bool F8, int BS>
 struct Softmax {
-  using C = TcCfg<D, N, F8>;
+  using C = TcCfg<D, N, F8, kDiagP<D, GE, N, F8, BS>>;
   static constexpr int GB = Units<BS>::GB;          // rows of one (unit, KV head) group
   static constexpr int GROUPS = Units<BS>::GROUPS;  // groups per chunk
   static constexpr int WG = 32 / GB;                // groups per warp (2, or 4 at GB 8)
@@ -577,6 +620,7 @@ struct Softmax {
       if (c - C::PB >= 0 && pv_done < c - C::PB) wait_pv(c - C::PB);
       unsigned char* pcur = pbuf + (c % C::PB) * C::P_BYTES;
 
+      float pd[GE];  // per-head P tiles: this row's P, stored after the loop
 #pragma unroll
       for (int j = 0; j < GE; ++j) {
         // a masked score gives 0 (m_ref may still be -inf for its column)
@@ -590,10 +634,29 @@ struct Softmax {
           const uint32_t o = p8_offset(h * GE + j, ctid);
           pcur[o] = ph;
           pcur[C::PH_BYTES + o] = pl;
+        } else if constexpr (kDiagP<D, GE, N, F8, BS>) {
+          l_part[j] += p;
+          pd[j] = p;  // stored below, 8 columns per 16-byte store
         } else {
           l_part[j] += p;
           *reinterpret_cast<__nv_bfloat16*>(pcur + p_offset<N>(h * GE + j, ctid)) =
               __float2bfloat16_rn(p);
+        }
+      }
+      if constexpr (kDiagP<D, GE, N, F8, BS>) {
+        // columns [h GE, h GE + GE) are 8-column groups ((h GE) & 15) / 8 + g
+        // of the step's window
+#pragma unroll
+        for (int g = 0; g < GE / 8; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(pd[8 * g + 2 * i], pd[8 * g + 2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          *reinterpret_cast<uint4*>(pcur + pdiag_offset(ctid >> 4, ((h * GE) & 15) / 8 + g,
+                                                        ctid & 15)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       // A row past the sequence inside a loaded block (the sequence's last,
@@ -705,7 +768,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, const TcParams P) {
-  using C = TcCfg<D, N, F8>;
+  using C = TcCfg<D, N, F8, kDiagP<D, GE, N, F8, BS>>;
   static_assert(!F8 || BS >= 16, "the 8-bit V^T sub-tiles hold 16 keys");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -1112,8 +1175,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0)
-      mma_loop<D, N, F8>(ring, qbuf, pbuf, full, empty, qempty, bar_s, bar_o, bar_p, drain,
-                         meta, tmem, abort_flag);
+      mma_loop<D, GE, N, F8, kDiagP<D, GE, N, F8, BS>>(ring, qbuf, pbuf, full, empty, qempty,
+                                                        bar_s, bar_o, bar_p, drain, meta, tmem,
+                                                        abort_flag, H);
   } else {
     // ------------------------------------------------------------ softmax
     Softmax<D, GE, N, F8, BS>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2,
@@ -1345,7 +1409,7 @@ int make_map_vt(CUtensorMap* m, const void* base, uint64_t tiles, uint64_t d, ui
 
 template <int D, int GE, int N, bool F8, int BS>
 int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
-  using C = TcCfg<D, N, F8>;
+  using C = TcCfg<D, N, F8, kDiagP<D, GE, N, F8, BS>>;
   constexpr int VS = Units<BS>::VS;
   const pa_decode_params* p = Lc.p;
   const QueryMap qm = query_map(p);
