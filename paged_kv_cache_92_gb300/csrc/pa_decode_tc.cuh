@@ -137,7 +137,7 @@ struct TcCfg {
   // GB300 neither cache type ran faster with it (the softmax spends ~180
   // cycles of its ~1400-2400 per chunk waiting for that product).
   static constexpr int PB = 1;
-  static constexpr int MISC_BYTES = 4224;
+  static constexpr int MISC_BYTES = 4096;
   // Q buffers: two let the next segment's queries load while the current
   // segment runs. One is kept when a second would cost a ring slot (at
   // N = 128, and at N = 64 with per-head P tiles: three slots instead of two).
@@ -169,9 +169,8 @@ struct TcCfg {
   static constexpr int OFF_MS = OFF_LS + 128 * 4;                            // [128]
   static constexpr int OFF_WORDS = OFF_MS + 128 * 4;
   static constexpr int OFF_QALPHA = OFF_WORDS + 64;       // F8: [2 q slots][64] 1/alpha
-  // F8: k_scale[8], v_scale[8], then their reciprocals (the fused KV write)
-  static constexpr int OFF_KVSCALE = OFF_QALPHA + 2 * 64 * 4;
-  static constexpr int OFF_COLROW = OFF_KVSCALE + 128;  // [128] output row of each column
+  static constexpr int OFF_KVSCALE = OFF_QALPHA + 2 * 64 * 4;  // F8: k_scale[8], v_scale[8]
+  static constexpr int OFF_COLROW = OFF_KVSCALE + 64;  // [128] output row of each column
   static constexpr int SMEM = OFF_COLROW + 128 * 4 + 1024;  // + alignment slack
   static_assert(OFF_COLROW + 128 * 4 <= OFF_MISC + MISC_BYTES, "misc area");
   static_assert(N <= 128 && (!F8 || N <= 64), "columns");
@@ -189,25 +188,6 @@ struct TcCfg {
   static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
   static constexpr uint32_t Q_TX = Q_BYTES + (F8 ? N * 4 : 0);  // F8: + 1/alpha per column
 };
-
-// x / s rounded to nearest even, for a positive normal s with r = RN(1/s):
-// Markstein's correction step (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
-// 1990; also Muller et al., Handbook of Floating-Point Arithmetic, on
-// division with a fused multiply-add). q0 = RN(x r) lies within one ulp of
-// x / s, the remainder x - q0 s is exact in one FMA, and RN(q0 + rem r) is
-// the correctly rounded quotient while nothing underflows. A non-finite q0
-// (x infinite or NaN, or x / s past the float range) is returned as it is,
-// which is the division's own result there, and so is a zero q0, whose sign
-// the correction would lose (+0 + -0 = +0). Quotients below the float
-// normal range may differ in the last place; the 8-bit write maps every
-// quotient below 2^-10 to a signed zero, so its codes do not depend on it.
-__device__ __forceinline__ float div_rn_by(float x, float s, float r) {
-  const float q0 = __fmul_rn(x, r);
-  if (!isfinite(q0) || q0 == 0.0f) return q0;  // a zero keeps the sign of x
-  const float rem = __fmaf_rn(-q0, s, x);
-  return __fmaf_rn(rem, r, q0);
-}
 
 struct TcParams {
   const int32_t* block_tables;
@@ -897,11 +877,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   dev::griddep_wait();
   if constexpr (F8) {  // per-KV-head scales: k_scale in [0, 8), v_scale in [8, 16)
-    if (tid < 16) {
-      const float sc = (tid & 7) < H ? (tid < 8 ? P.k_scale : P.v_scale)[tid & 7] : 1.0f;
-      kvscale[tid] = sc;
-      kvscale[16 + tid] = __frcp_rn(sc);
-    }
+    if (tid < 16) kvscale[tid] = (tid & 7) < H ? (tid < 8 ? P.k_scale : P.v_scale)[tid & 7] : 1.0f;
   }
   if (blockIdx.x == 0) {  // the stream-K plan, for the merge kernel
     for (int i = tid; i <= B; i += NTHREADS) P.ws_plan[1 + i] = pre[i];
@@ -978,33 +954,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (k < n_row) {
           const int hh = k / CPR, ch = k - (k / CPR) * CPR;
           const int off = r.pos % BS;
-          if constexpr (F8) {
-            // the quantising write of the 8-bit cache: code = E4M3(x / scale),
-            // K as 8 bytes of its row, V as 8 bytes of its column of the
-            // tile's 16-key V^T sub-tile
-            const size_t tile = (size_t(r.e) * H + hh) * BS * D;
-            uint8_t* kc = reinterpret_cast<uint8_t*>(P.k_cache_w);
-            uint8_t* vc = reinterpret_cast<uint8_t*>(P.v_cache_w);
-            float kf[8], vf[8];
-            dev::unpack8(r.k[j], kf);
-            dev::unpack8(r.v[j], vf);
-            uint32_t kw0 = 0, kw1 = 0;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const uint32_t code = dev::to_e4m3(div_rn_by(kf[t], kvscale[hh], kvscale[16 + hh]));
-              if (t < 4) kw0 |= code << (8 * t); else kw1 |= code << (8 * (t - 4));
-            }
-            *reinterpret_cast<uint2*>(kc + tile + size_t(off) * D + ch * 8) = make_uint2(kw0, kw1);
-            uint8_t* vsub = vc + tile + size_t(off >> 4) * kF8Tile * D + (off & 15);
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-              vsub[size_t(ch * 8 + t) * kF8Tile] =
-                  dev::to_e4m3(div_rn_by(vf[t], kvscale[8 + hh], kvscale[24 + hh]));
-          } else {
-            const size_t dst = ((size_t(r.e) * H + hh) * BS + off) * CPR + ch;
-            P.k_cache_w[dst] = r.k[j];
-            P.v_cache_w[dst] = r.v[j];
-          }
+          const size_t dst = ((size_t(r.e) * H + hh) * BS + off) * CPR + ch;
+          P.k_cache_w[dst] = r.k[j];
+          P.v_cache_w[dst] = r.v[j];
         }
       }
     };
@@ -1048,9 +1000,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int seg_nb = uend - off;
       const bool whole = off == 0 && seg_nb == nb;
       const int new_unit0 = (L_cur - P.q_len) / UT;  // first unit holding a new token
-      if (P.k_new != nullptr && P.q_len == 1 && off + seg_nb > new_unit0) {
-        load_row(b, L_cur - 1, 0, pre_row);  // consumed at the chunk of its unit
-        have_pre = true;
+      if constexpr (!F8) {  // (the 8-bit cache is written by the query-split launch)
+        if (P.k_new != nullptr && P.q_len == 1 && off + seg_nb > new_unit0) {
+          load_row(b, L_cur - 1, 0, pre_row);  // consumed at the chunk of its unit
+          have_pre = true;
+        }
       }
       // prefetched for later: the next sequence's length and first window,
       // this segment's second window
@@ -1065,7 +1019,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           win = win_nxt;
           win_nxt = jb + 32 < seg_nb ? load_window(b, off + jb + 32) : -1;
         }
-        {  // this chunk holds a unit of the new tokens
+        if constexpr (!F8) {  // this chunk holds a unit of the new tokens
           const int nu = min(U, seg_nb - jb);
           if (P.k_new != nullptr && off + jb + nu > new_unit0)
             append_tokens(b, L_cur, off + jb, off + jb + nu);
@@ -1438,7 +1392,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
     if (!r)
       r = make_map_u8(&tq, Lc.q8, uint64_t(p->num_seqs) * 2 * N, D, D, uint32_t(2 * N),
                       CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!r) r = launch_quantize_q(p->q, Lc.q8, Lc.q_inv_alpha, qm, stream);
+    if (!r) r = launch_quantize_q(p->q, Lc.q8, Lc.q_inv_alpha, qm, p, Lc.append, stream);
   } else {
     if constexpr (VS == 1) {
       r = make_map(&tk, p->k_cache, cache_rows, D, uint32_t(BS * H));
@@ -1465,7 +1419,8 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.part_l = Lc.part_l;
   P.part_acc = Lc.part_acc;
   P.ws_plan = Lc.plan;
-  const pa_append_params* a = Lc.append;
+  // the 8-bit cache's new tokens were written by the query-split launch
+  const pa_append_params* a = F8 ? nullptr : Lc.append;
   P.k_new = a ? static_cast<const uint4*>(a->k_new) : nullptr;
   P.v_new = a ? static_cast<const uint4*>(a->v_new) : nullptr;
   P.slot_mapping = a ? a->slot_mapping : nullptr;

@@ -20,6 +20,25 @@ __device__ __forceinline__ float from_e4m3(uint8_t c) {
   return __half2float(__half(h));
 }
 
+// x / s rounded to nearest even, for a positive normal s with r = RN(1/s):
+// Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990; also Muller et al., Handbook of Floating-Point Arithmetic, on
+// division with a fused multiply-add). q0 = RN(x r) lies within one ulp of
+// x / s, the remainder x - q0 s is exact in one FMA, and RN(q0 + rem r) is
+// the correctly rounded quotient while nothing underflows. A non-finite q0
+// (x infinite or NaN, or x / s past the float range) is returned as it is,
+// which is the division's own result there, and so is a zero q0, whose sign
+// the correction would lose (+0 + -0 = +0). Quotients below the float
+// normal range may differ in the last place; the 8-bit write maps every
+// quotient below 2^-10 to a signed zero, so its codes do not depend on it.
+__device__ __forceinline__ float div_rn_by(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  if (!isfinite(q0) || q0 == 0.0f) return q0;  // a zero keeps the sign of x
+  const float rem = __fmaf_rn(-q0, s, x);
+  return __fmaf_rn(rem, r, q0);
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

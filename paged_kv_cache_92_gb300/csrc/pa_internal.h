@@ -83,6 +83,16 @@ inline QueryMap query_map(const pa_decode_params* p) {
   m.head_dim = p->head_dim;
   return m;
 }
+#ifdef __CUDACC__
+// Row of q ([B][query_len][Hq][D]) that column n of sequence b holds, or -1.
+__device__ __forceinline__ int64_t query_source_row(const QueryMap& m, int b, int n) {
+  if (n >= m.num_cols) return -1;
+  const int g = n / m.group_cols, r = n - g * m.group_cols;
+  const int i = r >> m.g_log2, j = r & ((1 << m.g_log2) - 1);
+  if (i >= m.query_len) return -1;
+  return (int64_t(b) * m.query_len + i) * m.num_q_heads + (g << m.g_log2) + j;
+}
+#endif
 
 // Bytes at the start of every decode workspace (reserved).
 constexpr size_t kWorkspaceHeaderBytes = 256;
@@ -135,12 +145,17 @@ int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_c
                                  int32_t head_dim, int32_t block_size, int32_t num_blocks,
                                  void* stream);
 int read_and_clear_fp8_errors(uint32_t* flags);
-// Query preparation for the tensor-core decode (pa_query.cu): the rows of q
-// ([B][query_len][Hq][D] bf16) in the column layout, padded to n_pad rows with
-// zeros -- as bf16 ([B][n_pad][D]), or split into two E4M3 terms ([B][2*n_pad][D]
-// bytes, hi rows then lo rows, and [B][n_pad] floats 1/alpha).
+// Query preparation for the bf16 tensor-core decode with several new tokens
+// per sequence (pa_query.cu): the rows of q ([B][query_len][Hq][D] bf16) in
+// the column layout, padded to n_pad rows with zeros ([B][n_pad][D]).
 int launch_permute_q(const void* q, void* qp, const QueryMap& m, void* stream);
-int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap& m, void* stream);
+// The 8-bit decode's preparation launch (pa_fp8.cu): the rows of q split into
+// two E4M3 terms in the column layout ([B][2*n_pad][D] bytes, hi rows then lo
+// rows, and [B][n_pad] floats 1/alpha), and -- with `append` (pa_append_decode)
+// -- the quantising KV write of the step's new tokens, checked against their
+// positions like the fused bf16 write.
+int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap& m,
+                      const pa_decode_params* p, const pa_append_params* append, void* stream);
 // Copy `bytes` from src -- host memory the GPU can address (pinned, mapped
 // under unified addressing), 16-byte aligned -- to device memory dst (16-byte
 // aligned), with a kernel rather than a DMA copy (pa_cache.cu).
