@@ -93,6 +93,18 @@ struct Units {
 template <int D, int GE, int N, bool F8, int BS>
 constexpr bool kDiagP = !F8 && D == 128 && GE >= 8 && N == 64 && Units<BS>::GB == 16;
 constexpr int kF8Tile = 16;  // keys of one 8-bit V^T sub-tile
+// The stream-K plan's cost of a sequence start, in chunks: what an extra
+// segment in a CTA costs (its epilogue, its queries, the pipeline
+// turn-over), in units of chunk time. Chosen by measurement on GB300 (steps
+// in us for costs 1 / 2 / 3):
+//   bf16, one new token, 64-sequence 8B layer: 56.6 / 55.9 / 56.2
+//   bf16, two new tokens, same layer: 65.7 / 62.1 / 62.2
+//   bf16, four new tokens, same layer: 94.5 / 88.2 / 87.1
+//   8-bit (chunks take half as long), same layer: 42.1 / 41.0 / 41.0, and
+//   256 sequences: 134.7 / 133.7 / 132.2 (4 chunks: 132.0, but slower at 64)
+__host__ __device__ constexpr int start_chunks(bool f8, int q_len) {
+  return f8 || q_len >= 4 ? 3 : 2;
+}
 constexpr int kMaxDynSmem = 232448;
 constexpr float kLog2e = 1.4426950408889634f;
 // The softmax reference maximum moves only when a score exceeds it by more
@@ -813,7 +825,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // take about one chunk's time), so CTAs that hold several sequence starts
   // get fewer units. pre = exclusive prefix of the costs; CTA c takes the
   // cost range [c R, (c+1) R).
-  const int SC = Units<BS>::GROUPS / H;  // one chunk's units
+  const int SC = start_chunks(F8, P.q_len) * (Units<BS>::GROUPS / H);  // a sequence start's cost
   int* pre = reinterpret_cast<int*>(ring);
   {
     const int seg = (B + NTHREADS - 1) / NTHREADS;
@@ -1470,7 +1482,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   mc.group_cols = qm.group_cols;
   mc.g_log2 = qm.g_log2;
   mc.q_len = qm.query_len;
-  mc.seg_cost = Units<BS>::GROUPS / H;
+  mc.seg_cost = start_chunks(F8, qm.query_len) * (Units<BS>::GROUPS / H);
   e = cudaLaunchKernelEx(&mcfg, merge_segments_kernel<D>, P.out,
                          static_cast<const float*>(P.part_m), static_cast<const float*>(P.part_l),
                          static_cast<const float*>(P.part_acc),
