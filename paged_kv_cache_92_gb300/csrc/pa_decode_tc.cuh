@@ -889,18 +889,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     win0 = j < P.max_blocks_per_seq
                ? P.block_tables[size_t(b_start) * P.max_blocks_per_seq + j] : -1;
     len0 = seq_len(P, b_start);
-    // 8-bit cache: pull the blocks of the first ring's worth of units into
-    // L2 now, so that their copies after the wait find them there. The
-    // kernel runs as a dependent of the query-split launch, and their DRAM
-    // latency overlaps it (a prefetch cannot go stale: every later write to
-    // these lines goes through L2). One lane per block; a block's K, and
-    // its V^T, for all KV heads is one contiguous range. Measured on the
-    // 64-sequence 8B layer: 41.5 -> 38.9 us per step. On bf16, whose decode
-    // follows the short merge of the previous step, the same prefetch made
-    // the step slower (54.9 -> 55.7 us): the copies after the wait queued
-    // behind prefetches still in progress.
-    const int n_pf = F8 ? min(C::ST * (Units<BS>::GROUPS / H), (len0 + UT - 1) / UT - off_start)
-                        : 0;
+    // Pull the first blocks into L2 now, so that their copies after the
+    // wait find them there: the kernel runs as a dependent of the previous
+    // launch, and their DRAM latency overlaps its end (a prefetch cannot go
+    // stale: every later write to these lines goes through L2). One lane per
+    // block; a block's K, and its V (V^T), for all KV heads is one
+    // contiguous range. The 8-bit decode follows the query-split launch and
+    // takes the first ring's worth (64-sequence 8B layer: 41.5 -> 38.8 us
+    // per step); bf16 follows the short merge of the previous step, and
+    // takes one chunk's worth (55.6 -> 54.7 us; a whole ring made it slower,
+    // 54.9 -> 55.7 us, as the copies after the wait queued behind it).
+    const int n_pf = min((F8 ? C::ST : 1) * (Units<BS>::GROUPS / H),
+                         (len0 + UT - 1) / UT - off_start);
     if (lane < n_pf && win0 >= 0 && win0 < P.num_blocks &&
         (lane == 0 || ((off_start + lane) % VS) == 0)) {
       const uint32_t blk_bytes = uint32_t(H * BS * D * (F8 ? 1 : 2));
