@@ -96,14 +96,19 @@ constexpr int kF8Tile = 16;  // keys of one 8-bit V^T sub-tile
 // The stream-K plan's cost of a sequence start, in chunks: what an extra
 // segment in a CTA costs (its epilogue, its queries, the pipeline
 // turn-over), in units of chunk time. Chosen by measurement on GB300 (steps
-// in us for costs 1 / 2 / 3):
-//   bf16, one new token, 64-sequence 8B layer: 56.6 / 55.9 / 56.2
-//   bf16, two new tokens, same layer: 65.7 / 62.1 / 62.2
-//   bf16, four new tokens, same layer: 94.5 / 88.2 / 87.1
-//   8-bit (chunks take half as long), same layer: 42.1 / 41.0 / 41.0, and
-//   256 sequences: 134.7 / 133.7 / 132.2 (4 chunks: 132.0, but slower at 64)
+// in us for the costs given):
+//   bf16, one new token, 64-sequence 8B layer: 56.6 / 55.9 / 56.2 (1 / 2 / 3)
+//   bf16, two new tokens, same layer: 65.7 / 62.1 / 62.2 (1 / 2 / 3); 60.9 at 4,
+//     but the 70B-class batch of 8 is 124.4 at 2 and 124.8 at 3 or 4
+//   bf16, four new tokens (128 columns: 32 KiB of queries, one query buffer,
+//     64 KiB of partials per split segment), same layer: 94.5 / 88.2 / 87.1
+//     (1 / 2 / 3), 85.1 / 81.1 / 82.6 (4 / 6 / 8); 256 sequences:
+//     309.8 / 316.7 / 301.5 / 296.6 (3 / 4 / 6 / 8)
+//   8-bit (chunks take half as long), same layer: 42.1 / 41.0 / 41.0
+//     (1 / 2 / 3), and 256 sequences: 134.7 / 133.7 / 132.2 (4: 132.0, but
+//     slower at 64 sequences)
 __host__ __device__ constexpr int start_chunks(bool f8, int q_len) {
-  return f8 || q_len >= 4 ? 3 : 2;
+  return q_len >= 4 ? 6 : f8 ? 3 : 2;
 }
 constexpr int kMaxDynSmem = 232448;
 constexpr float kLog2e = 1.4426950408889634f;
