@@ -291,9 +291,12 @@ pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
  * Pinned host memory (page-locked through CUDA, hence mapped under unified
  * addressing) that is 16-byte aligned is read and written by the kernels
  * themselves over the host link (NVLink-C2C on a Grace-Blackwell part): a
- * staging kernel copies host_in into the workspace, and the decode writes its
- * output rows straight into host_out. Any other host memory goes through one
- * DMA copy each way (cudaMemcpyAsync). The bytes moved are the same.
+ * staging kernel copies host_in into the workspace, the tensor-core decode
+ * reads the lengths and tables in host_in to plan its work while that kernel
+ * runs, and the decode writes its output rows straight into host_out. Any
+ * other host memory goes through one DMA copy each way (cudaMemcpyAsync).
+ * The bytes moved are the same. host_in must not change until the call
+ * returns.
  *
  * Packed input (host memory; pinned memory lets the copy run at full speed):
  * sections at the byte offsets pa_step_host_layout reports, each 256-byte

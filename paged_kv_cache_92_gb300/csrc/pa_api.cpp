@@ -468,6 +468,16 @@ pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t wor
     a.v_cache = p->v_cache;
     const pa::WorkspaceLayout w = pa::decode_workspace_layout(&d, np, grid);
     if (out_dev) d.out = out_dev;
+    if (in_dev && d.variant == PA_DECODE_TENSOR_CORE && pa::tc_supports(&d)) {
+      // The lengths and tables in host_in are final before this call, so the
+      // tensor-core decode reads them there and plans its work while the
+      // staging kernel still runs (programmatic dependent launch); it reads
+      // everything else from the staged copy after that kernel completes.
+      const unsigned char* hin = static_cast<const unsigned char*>(in_dev);
+      d.block_tables = reinterpret_cast<const int32_t*>(hin + sp.in.block_tables);
+      d.context_lens = reinterpret_cast<const int32_t*>(hin + sp.in.context_lens);
+      d.overlap_prologue = 1;
+    }
     st = pa::run_decode(&d, ws + sp.dec_off, w, np, grid, stream, "pa_step_host", &a);
     if (st != PA_OK) return st;
     if (!out_dev) {

@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     stage_in_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n16,
                     int tail) {
+  // a decode launched as a programmatic dependent may start its set-up now;
+  // it waits for this kernel before it reads what this kernel writes
+  dev::griddep_launch_dependents();
   const int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 2;
   uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
   if (i < n16) a = src[i];
