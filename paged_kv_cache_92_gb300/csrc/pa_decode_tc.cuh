@@ -1066,8 +1066,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
         if (lane == 0) {
           ok = dev::mbar_wait_sleep(&empty[slot], ph ^ 1u, 64);
-          if (ok && c == 0)
-            ok = dev::mbar_wait_sleep(&qempty[qs], (uint32_t(seg_seq / C::QB) & 1u) ^ 1u, 64);
           if (ok) {
             ChunkMeta m;
             m.b = b;
@@ -1114,10 +1112,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               dev::tma_load_4d(kdst + C::K_BYTES + lane * H * C::VT_TILE, &tm_v, 0, 0, half,
                                crd_v, &full[slot], pol);
             }
-          } else if (lane == 31 && c == 0) {
-            dev::tma_load_2d(qbuf + qs * C::Q_BYTES, &tm_q, 0, b * P.q_rows, &full[slot], pol);
-            dev::bulk_load(qalpha + qs * 64, P.q_inv_alpha + size_t(b) * N, N * 4, &full[slot],
-                           pol);
           }
         } else {
           if (lane < U) {
@@ -1132,11 +1126,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 dev::tma_load_3d(d + C::K_BYTES, &tm_v, hf * 64, half * UT, crd, &full[slot], pol);
               }
             }
-          } else if (lane == 31 && c == 0) {
+          }
+        }
+        if (c == 0) {
+          // The segment's queries, into query buffer qs once its previous
+          // segment has read it. Only this copy waits for that: the chunk's
+          // K/V copies above are already on their way, so with one query
+          // buffer a segment's first data no longer waits behind the previous
+          // segment's last score product.
+          bool qok = true;
+          if (lane == 31) {
+            qok = dev::mbar_wait_sleep(&qempty[qs], (uint32_t(seg_seq / C::QB) & 1u) ^ 1u, 64);
+            if (qok) {
+              if constexpr (F8) {
+                dev::tma_load_2d(qbuf + qs * C::Q_BYTES, &tm_q, 0, b * P.q_rows, &full[slot],
+                                 pol);
+                dev::bulk_load(qalpha + qs * 64, P.q_inv_alpha + size_t(b) * N, N * 4,
+                               &full[slot], pol);
+              } else {
 #pragma unroll
-            for (int hf = 0; hf < C::HALVES; ++hf)
-              dev::tma_load_2d(qbuf + qs * C::Q_BYTES + hf * C::QH_BYTES, &tm_q, hf * 64,
-                               b * P.q_rows, &full[slot], pol);
+                for (int hf = 0; hf < C::HALVES; ++hf)
+                  dev::tma_load_2d(qbuf + qs * C::Q_BYTES + hf * C::QH_BYTES, &tm_q, hf * 64,
+                                   b * P.q_rows, &full[slot], pol);
+              }
+            }
+          }
+          if (__shfl_sync(0xffffffffu, int(qok), 31) == 0) {
+            ok = false;
+            break;
           }
         }
         ++chunk_seq;
