@@ -92,6 +92,13 @@ struct Units {
 // its narrower P stores made the step slower.)
 template <int D, int GE, int N, bool F8, int BS>
 constexpr bool kDiagP = !F8 && D == 128 && GE >= 8 && N == 64 && Units<BS>::GB == 16;
+// P^T MN-major at 128 columns (bf16, head_dim 128, 16 columns per KV head,
+// 16 tokens per unit): stored like V -- two 64-column halves of [128 keys]
+// [128 bytes], 128B-swizzled -- so that each softmax thread (one key) writes
+// its head's 16 columns as two 16-byte stores instead of 16 scattered 2-byte
+// ones, and the value product reads P^T as an MN-major B operand.
+template <int D, int GE, int N, bool F8, int BS>
+constexpr bool kMnP = !F8 && D == 128 && GE == 16 && N == 128 && Units<BS>::GB == 16;
 constexpr int kF8Tile = 16;  // keys of one 8-bit V^T sub-tile
 // The stream-K plan's cost of a sequence start, in chunks: what an extra
 // segment in a CTA costs (its epilogue, its queries, the pipeline
@@ -202,6 +209,7 @@ struct TcCfg {
   static constexpr uint32_t IDESC_PV =
       F8 ? dev::idesc_e4m3_f32(ROWS, NS) : dev::idesc_bf16_f32(ROWS, N, true, false);
   static constexpr uint32_t IDESC_PV16 = dev::idesc_bf16_f32(ROWS, 16, true, true);  // DIAG
+  static constexpr uint32_t IDESC_PV_MN = dev::idesc_bf16_f32(ROWS, N, true, true);  // MN-major P^T
   static constexpr uint32_t CHUNK_TX = SLOT_BYTES;
   static constexpr uint32_t Q_TX = Q_BYTES + (F8 ? N * 4 : 0);  // F8: + 1/alpha per column
 };
@@ -314,7 +322,7 @@ __device__ __forceinline__ void issue_scores(uint32_t tmem_col, const unsigned c
 // the chunk has landed, and O^T = V^T.P^T once the softmax warps have written
 // P for it. Scores run one chunk ahead of the value product.
 // ---------------------------------------------------------------------------
-template <int D, int GE, int N, bool F8, bool DIAG>
+template <int D, int GE, int N, bool F8, bool DIAG, bool MNP>
 __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbuf,
                                          unsigned char* pbuf, uint64_t* full, uint64_t* empty,
                                          uint64_t* qempty, uint64_t* bar_s, uint64_t* bar_o,
@@ -375,6 +383,16 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
                         // columns (N) 256 B on
                         dev::smem_desc(pbc + kk * 512, 128, 256, dev::kSwizzleNone),
                         C::IDESC_PV16, !(fresh && first));
+        }
+      } else if constexpr (MNP) {
+        // P^T MN-major, laid out like V: the next 8 keys 1024 B on (SBO), the
+        // second 64-column half 16 KiB on (LBO)
+#pragma unroll
+        for (int kk = 0; kk < ROWS / 16; ++kk) {
+          dev::mma_bf16(tmem + C::kSBufs * C::NS,
+                        dev::smem_desc(vb + kk * 2048, lbo, 1024, dev::kSwizzle128B),
+                        dev::smem_desc(pbc + kk * 2048, 16384, 1024, dev::kSwizzle128B),
+                        C::IDESC_PV_MN, kk > 0 || !fresh);
         }
       } else {
 #pragma unroll
@@ -634,13 +652,30 @@ struct Softmax {
           const uint32_t o = p8_offset(h * GE + j, ctid);
           pcur[o] = ph;
           pcur[C::PH_BYTES + o] = pl;
-        } else if constexpr (kDiagP<D, GE, N, F8, BS>) {
+        } else if constexpr (kDiagP<D, GE, N, F8, BS> || kMnP<D, GE, N, F8, BS>) {
           l_part[j] += p;
           pd[j] = p;  // stored below, 8 columns per 16-byte store
         } else {
           l_part[j] += p;
           *reinterpret_cast<__nv_bfloat16*>(pcur + p_offset<N>(h * GE + j, ctid)) =
               __float2bfloat16_rn(p);
+        }
+      }
+      if constexpr (kMnP<D, GE, N, F8, BS>) {
+        // columns [16 h, 16 h + 16): 16-byte chunks 2 (h % 4) and 2 (h % 4) + 1
+        // of key ctid's 128-byte row in half h / 4, each at its chunk index
+        // XOR (ctid % 8) (the 128B swizzle)
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(pd[8 * g + 2 * i], pd[8 * g + 2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          const int chunk = 2 * (h & 3) + g;
+          *reinterpret_cast<uint4*>(pcur + (h >> 2) * 16384 + ctid * 128 +
+                                    ((chunk ^ (ctid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       if constexpr (kDiagP<D, GE, N, F8, BS>) {
@@ -1184,9 +1219,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0)
-      mma_loop<D, GE, N, F8, kDiagP<D, GE, N, F8, BS>>(ring, qbuf, pbuf, full, empty, qempty,
-                                                        bar_s, bar_o, bar_p, drain, meta, tmem,
-                                                        abort_flag, H);
+      mma_loop<D, GE, N, F8, kDiagP<D, GE, N, F8, BS>, kMnP<D, GE, N, F8, BS>>(
+          ring, qbuf, pbuf, full, empty, qempty, bar_s, bar_o, bar_p, drain, meta, tmem,
+          abort_flag, H);
   } else {
     // ------------------------------------------------------------ softmax
     Softmax<D, GE, N, F8, BS>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2,
