@@ -139,8 +139,11 @@ typedef struct {
                                   previous kernel on `stream` began (e.g. uploaded once per step),
                                   so the tensor-core kernel may read them -- and plan its work --
                                   while that kernel still runs (programmatic dependent launch).
-                                  q, the caches and every output are touched only after the
-                                  previous kernel has completed. 0 = plain stream order. */
+                                  q, the caches and every output are read or written only after
+                                  the previous kernel has completed; before that the kernel only
+                                  prefetches its first cache blocks into L2, which cannot change
+                                  any result even if that kernel writes them. 0 = plain stream
+                                  order. */
   int32_t kv_dtype;            /* PA_KV_BF16 (0, default) or PA_KV_FP8_E4M3 (1) */
   const float* k_scale;        /* PA_KV_FP8_E4M3 only: device float [num_kv_heads], the
                                   dequantisation scale of each KV head's K (value = code * scale) */
