@@ -287,8 +287,9 @@ pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
  *
  * The call enqueues on `stream`
  *   1. the staging of the packed inputs into the workspace,
- *   2. pa_copy_blocks (if num_cow_pairs > 0), then pa_append_decode on the
- *      staged inputs and the device-resident caches,
+ *   2. pa_copy_blocks (pa_copy_blocks_fp8 for the 8-bit cache; if
+ *      num_cow_pairs > 0), then pa_append_decode on the staged inputs and the
+ *      device-resident caches (bf16, or 8-bit with kv_dtype and the scales),
  *   3. the return of the output to host_out,
  * and synchronises the stream before it returns (the output is in host_out).
  * Pinned host memory (page-locked through CUDA, hence mapped under unified
@@ -338,6 +339,12 @@ typedef struct {
   int32_t num_cow_pairs;
   float scale;
   int32_t variant;            /* PA_DECODE_TENSOR_CORE or PA_DECODE_CUDA_CORE */
+  int32_t kv_dtype;           /* PA_KV_BF16 (0) or PA_KV_FP8_E4M3: the caches as in pa_decode;
+                                 the 8-bit cache takes the tensor-core variant, the quantising
+                                 KV write and pa_copy_blocks_fp8 */
+  const float* k_scale;       /* PA_KV_FP8_E4M3 only: device float [num_kv_heads], as in
+                                 pa_decode_params */
+  const float* v_scale;
 } pa_step_host_params;
 
 pa_status pa_step_host_layout(const pa_step_host_params* p, pa_step_layout* out);

@@ -100,6 +100,7 @@ class StepHostParams(ctypes.Structure):
         ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
         ("max_blocks_per_seq", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
         ("num_cow_pairs", ctypes.c_int32), ("scale", ctypes.c_float), ("variant", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -340,15 +341,25 @@ def pa_append_decode(q, k_cache, v_cache, block_tables, context_lens, max_contex
 def make_step_host_params(k_cache, v_cache, num_seqs: int, num_q_heads: int,
                           max_blocks_per_seq: int, max_context_len: int, num_cow_pairs: int = 0,
                           scale: Optional[float] = None,
-                          variant: int = DECODE_TENSOR_CORE) -> StepHostParams:
+                          variant: int = DECODE_TENSOR_CORE, k_scale=None,
+                          v_scale=None) -> StepHostParams:
     """Shape half of a host-driven step; host_in / host_out are set by the caller
-    (or by ``pa_step_host``)."""
+    (or by ``pa_step_host``). uint8 caches are the 8-bit (E4M3) cache and need
+    ``k_scale`` / ``v_scale`` (float32 CUDA tensors [num_kv_heads])."""
     import torch
 
     NB, Hkv, BS, D = k_cache.shape
     p = StepHostParams()
-    p.k_cache = _dev_ptr(k_cache, torch.bfloat16, "k_cache")
-    p.v_cache = _dev_ptr(v_cache, torch.bfloat16, "v_cache")
+    fp8 = k_cache.dtype == torch.uint8
+    cache_dtype = torch.uint8 if fp8 else torch.bfloat16
+    p.k_cache = _dev_ptr(k_cache, cache_dtype, "k_cache")
+    p.v_cache = _dev_ptr(v_cache, cache_dtype, "v_cache")
+    if fp8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("the 8-bit cache needs k_scale and v_scale")
+        p.kv_dtype = KV_FP8_E4M3
+        p.k_scale = _dev_ptr(k_scale, torch.float32, "k_scale")
+        p.v_scale = _dev_ptr(v_scale, torch.float32, "v_scale")
     p.num_seqs, p.num_q_heads, p.num_kv_heads, p.head_dim = num_seqs, num_q_heads, Hkv, D
     p.block_size, p.num_blocks = BS, NB
     p.max_blocks_per_seq, p.max_context_len = max_blocks_per_seq, int(max_context_len)

@@ -234,6 +234,8 @@ static pa_status check_step(const pa_step_host_params* p) {
     return set_error(PA_ERR_INVALID_ARG, "pa_step_host: counts must be positive");
   if (p->num_cow_pairs < 0 || p->num_cow_pairs > 65535)
     return set_error(PA_ERR_INVALID_ARG, "pa_step_host: num_cow_pairs must be in [0, 65535]");
+  if (p->kv_dtype != PA_KV_BF16 && p->kv_dtype != PA_KV_FP8_E4M3)
+    return set_error(PA_ERR_INVALID_ARG, "pa_step_host: kv_dtype must be PA_KV_BF16 or PA_KV_FP8_E4M3");
   return PA_OK;
 }
 
@@ -281,6 +283,9 @@ static void step_decode_params(const pa_step_host_params* p, unsigned char* ws,
   d->partition_tokens = 0;
   d->variant = p->variant;
   d->overlap_prologue = 0;
+  d->kv_dtype = p->kv_dtype;
+  d->k_scale = p->k_scale;
+  d->v_scale = p->v_scale;
 }
 
 static StepSpace step_space(const pa_step_host_params* p, const pa_decode_params& d, int np,
@@ -453,9 +458,12 @@ pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t wor
     if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: input copy", int(e));
   }
   if (p->num_cow_pairs > 0) {
+    // the 8-bit cache's blocks are the bytes of a bf16 block of half the head_dim
     const int r = pa::launch_copy_blocks(p->k_cache, p->v_cache,
                                          reinterpret_cast<const int32_t*>(ws + sp.in.cow_pairs),
-                                         p->num_cow_pairs, p->num_kv_heads, p->head_dim,
+                                         p->num_cow_pairs, p->num_kv_heads,
+                                         p->kv_dtype == PA_KV_FP8_E4M3 ? p->head_dim / 2
+                                                                       : p->head_dim,
                                          p->block_size, p->num_blocks, stream);
     if (r != 0) return pa::set_cuda_error("pa_step_host: copy_blocks launch", r);
   }

@@ -350,3 +350,65 @@ def test_fp8_fused_write_every_bf16_value(pk, scale_set):
     ko, vo = oracle.reshape_and_cache_fp8(kn, vn, k0, v0, slots, ks, vs)
     assert np.array_equal(k8.cpu().numpy(), ko)
     assert np.array_equal(v8.cpu().numpy().reshape(NB, Hkv, bs, D), vo)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_fp8_step_host_matches_device_step(pk, pinned):
+    """pa_step_host on the 8-bit cache (one copy-on-write pair, then the
+    quantising KV write and the decode) gives the device-side step's output
+    and caches bit for bit: pa_copy_blocks_fp8, then pa_append_decode."""
+    import torch
+
+    Hq, Hkv, D, bs = 32, 8, 128, 16
+    lens = np.array([1, 17, 64, 300, 1025], dtype=np.int64)
+    NB = int(((lens + bs - 1) // bs).sum()) + 4
+    order = np.random.default_rng(95).permutation(NB).astype(np.int32)
+    tables = workloads.sequential_tables(lens, order, bs)
+    slots = np.array([int(tables[b, (L - 1) // bs]) * bs + (L - 1) % bs
+                      for b, L in enumerate(lens)], dtype=np.int64)
+    used = set(int(x) for x in tables.ravel() if x >= 0)
+    spare = [b for b in range(NB) if b not in used]
+    cows = np.array([[int(tables[3, 2]), spare[0]]], dtype=np.int32)  # a full block of seq 3
+    B = len(lens)
+    ks = torch.from_numpy(_scales(Hkv, 96, 0.05)).cuda()
+    vs = torch.from_numpy(_scales(Hkv, 97, 0.03)).cuda()
+    k0, v0 = oracle.reshape_and_cache_fp8(
+        workloads.bf16_normal((NB * bs, Hkv, D), 98, "cpu"),
+        workloads.bf16_normal((NB * bs, Hkv, D), 99, "cpu"),
+        np.zeros((NB, Hkv, bs, D), np.uint8), np.zeros((NB, Hkv, bs, D), np.uint8),
+        np.arange(NB * bs, dtype=np.int64), ks.cpu().numpy(), vs.cpu().numpy())
+    q = workloads.bf16_normal((B, Hq, D), 100, "cuda")
+    kn = workloads.bf16_normal((B, Hkv, D), 101, "cuda")
+    vn = workloads.bf16_normal((B, Hkv, D), 102, "cuda")
+    t_d = torch.from_numpy(tables).cuda()
+    l_d = torch.from_numpy(lens.astype(np.int32)).cuda()
+
+    def fresh():
+        return (torch.from_numpy(k0).cuda(),
+                torch.from_numpy(v0.reshape(NB, Hkv, bs // 16, D, 16)).cuda())
+
+    kd, vd = fresh()
+    pk.pa_copy_blocks_fp8(kd, vd, torch.from_numpy(cows).cuda())
+    want = pk.pa_append_decode(q, kd, vd, t_d, l_d, int(lens.max()), kn, vn,
+                               torch.from_numpy(slots).cuda(), k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+
+    kh, vh = fresh()
+    p = pk.make_step_host_params(kh, vh, B, Hq, tables.shape[1], int(lens.max()),
+                                 num_cow_pairs=len(cows), k_scale=ks, v_scale=vs)
+    host_in = pk.pack_step_inputs(p, q.cpu(), kn.cpu(), vn.cpu(), slots, tables,
+                                  lens.astype(np.int32), cows, pin=pinned)
+    host_out = torch.empty((B, Hq, D), dtype=torch.bfloat16)
+    if pinned:
+        host_out = host_out.pin_memory()
+    ws = torch.empty(pk.pa_step_host_workspace_size(p), dtype=torch.uint8, device="cuda")
+    pk.pa_step_host(p, host_in, host_out, ws)
+    assert pk.pa_device_errors() == 0
+    assert torch.equal(host_out.view(torch.int16), want.cpu().view(torch.int16))
+    assert torch.equal(kh, kd) and torch.equal(vh, vd)
+    # and the caches are the oracle's copy + quantising write
+    ko, vo = oracle.copy_blocks_fp8(k0, v0, cows.tolist())
+    ko, vo = oracle.reshape_and_cache_fp8(kn.cpu(), vn.cpu(), ko, vo, slots, ks.cpu().numpy(),
+                                          vs.cpu().numpy())
+    assert np.array_equal(kh.cpu().numpy(), ko)
+    assert np.array_equal(vh.cpu().numpy().reshape(NB, Hkv, bs, D), vo)
