@@ -305,9 +305,9 @@ pa_status pa_append_decode(const pa_decode_params* p, const pa_append_params* a,
  * Packed input (host memory; pinned memory lets the copy run at full speed):
  * sections at the byte offsets pa_step_host_layout reports, each 256-byte
  * aligned, in this order:
- *   q             bf16  [num_seqs][num_q_heads][head_dim]
- *   k_new, v_new  bf16  [num_seqs][num_kv_heads][head_dim]
- *   slot_mapping  int64 [num_seqs]          (rules of pa_append_decode)
+ *   q             bf16  [num_seqs][num_q_heads][head_dim]     (x Q: see query_len)
+ *   k_new, v_new  bf16  [num_seqs][num_kv_heads][head_dim]    (x Q)
+ *   slot_mapping  int64 [num_seqs]          (x Q; rules of pa_append_decode)
  *   block_tables  int32 [num_seqs][max_blocks_per_seq]
  *   context_lens  int32 [num_seqs]          (counting the new token)
  *   cow_pairs     int32 [num_cow_pairs][2]  (rules of pa_copy_blocks)
@@ -345,6 +345,11 @@ typedef struct {
   const float* k_scale;       /* PA_KV_FP8_E4M3 only: device float [num_kv_heads], as in
                                  pa_decode_params */
   const float* v_scale;
+  int32_t query_len;          /* new tokens per sequence, Q (0 or 1 = one): q and host_out hold
+                                 [num_seqs][Q][num_q_heads][head_dim], k_new / v_new
+                                 [num_seqs * Q][num_kv_heads][head_dim], slot_mapping
+                                 [num_seqs * Q]; row b * Q + i is token context_lens[b] - Q + i
+                                 (as in pa_append_decode) */
 } pa_step_host_params;
 
 pa_status pa_step_host_layout(const pa_step_host_params* p, pa_step_layout* out);

@@ -101,6 +101,7 @@ class StepHostParams(ctypes.Structure):
         ("max_blocks_per_seq", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
         ("num_cow_pairs", ctypes.c_int32), ("scale", ctypes.c_float), ("variant", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("query_len", ctypes.c_int32),
     ]
 
 
@@ -342,10 +343,12 @@ def make_step_host_params(k_cache, v_cache, num_seqs: int, num_q_heads: int,
                           max_blocks_per_seq: int, max_context_len: int, num_cow_pairs: int = 0,
                           scale: Optional[float] = None,
                           variant: int = DECODE_TENSOR_CORE, k_scale=None,
-                          v_scale=None) -> StepHostParams:
+                          v_scale=None, query_len: int = 0) -> StepHostParams:
     """Shape half of a host-driven step; host_in / host_out are set by the caller
     (or by ``pa_step_host``). uint8 caches are the 8-bit (E4M3) cache and need
-    ``k_scale`` / ``v_scale`` (float32 CUDA tensors [num_kv_heads])."""
+    ``k_scale`` / ``v_scale`` (float32 CUDA tensors [num_kv_heads]). With
+    ``query_len`` Q > 1 every sequence brings Q new tokens (the layouts of
+    ``pa_append_decode``)."""
     import torch
 
     NB, Hkv, BS, D = k_cache.shape
@@ -366,6 +369,7 @@ def make_step_host_params(k_cache, v_cache, num_seqs: int, num_q_heads: int,
     p.num_cow_pairs = num_cow_pairs
     p.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
     p.variant = int(variant)
+    p.query_len = int(query_len)
     return p
 
 
@@ -402,7 +406,8 @@ def pack_step_inputs(params: StepHostParams, q, k_new, v_new, slot_mapping, bloc
 def pa_step_host(params: StepHostParams, host_in, host_out, workspace, stream=None) -> None:
     """One whole step from host memory (see the C header): ``host_in`` is a
     uint8 CPU tensor packed by ``pa_step_host_layout`` (pinned for speed),
-    ``host_out`` a bf16 CPU tensor [num_seqs][num_q_heads][head_dim],
+    ``host_out`` a bf16 CPU tensor [num_seqs][num_q_heads][head_dim] (with Q new
+    tokens per sequence [num_seqs][Q][num_q_heads][head_dim]),
     ``workspace`` a uint8 CUDA tensor. Returns when host_out holds the result."""
     import torch
 

@@ -236,20 +236,23 @@ static pa_status check_step(const pa_step_host_params* p) {
     return set_error(PA_ERR_INVALID_ARG, "pa_step_host: num_cow_pairs must be in [0, 65535]");
   if (p->kv_dtype != PA_KV_BF16 && p->kv_dtype != PA_KV_FP8_E4M3)
     return set_error(PA_ERR_INVALID_ARG, "pa_step_host: kv_dtype must be PA_KV_BF16 or PA_KV_FP8_E4M3");
+  if (p->query_len < 0 || p->query_len > 1024)
+    return set_error(PA_ERR_INVALID_ARG, "pa_step_host: query_len must be in [0, 1024]");
   return PA_OK;
 }
 
 static void step_layout(const pa_step_host_params* p, pa_step_layout* L) {
   const size_t B = size_t(p->num_seqs), D = size_t(p->head_dim);
+  const size_t Q = p->query_len > 1 ? size_t(p->query_len) : 1;  // new tokens per sequence
   size_t off = 0;
   auto put = [&](uint64_t& field, size_t bytes) {
     field = off;
     off = round_up(off + bytes, 256);
   };
-  put(L->q, B * p->num_q_heads * D * 2);
-  put(L->k_new, B * p->num_kv_heads * D * 2);
-  put(L->v_new, B * p->num_kv_heads * D * 2);
-  put(L->slot_mapping, B * sizeof(int64_t));
+  put(L->q, B * Q * p->num_q_heads * D * 2);
+  put(L->k_new, B * Q * p->num_kv_heads * D * 2);
+  put(L->v_new, B * Q * p->num_kv_heads * D * 2);
+  put(L->slot_mapping, B * Q * sizeof(int64_t));
   put(L->block_tables, B * size_t(p->max_blocks_per_seq) * sizeof(int32_t));
   put(L->context_lens, B * sizeof(int32_t));
   put(L->cow_pairs, size_t(p->num_cow_pairs) * 2 * sizeof(int32_t));
@@ -286,6 +289,7 @@ static void step_decode_params(const pa_step_host_params* p, unsigned char* ws,
   d->kv_dtype = p->kv_dtype;
   d->k_scale = p->k_scale;
   d->v_scale = p->v_scale;
+  d->query_len = p->query_len;
 }
 
 static StepSpace step_space(const pa_step_host_params* p, const pa_decode_params& d, int np,
@@ -293,7 +297,8 @@ static StepSpace step_space(const pa_step_host_params* p, const pa_decode_params
   StepSpace sp;
   step_layout(p, &sp.in);
   sp.out_off = sp.in.total;
-  const size_t out_bytes = size_t(p->num_seqs) * p->num_q_heads * p->head_dim * 2;
+  const size_t out_bytes = size_t(p->num_seqs) * (p->query_len > 1 ? p->query_len : 1) *
+                           p->num_q_heads * p->head_dim * 2;
   sp.dec_off = round_up(sp.out_off + out_bytes, 256);
   sp.total = sp.dec_off + decode_workspace_layout(&d, np, grid).total;
   return sp;
@@ -490,7 +495,8 @@ pa_status pa_step_host(const pa_step_host_params* p, void* workspace, size_t wor
     if (st != PA_OK) return st;
     if (!out_dev) {
       e = cudaMemcpyAsync(p->host_out, ws + sp.out_off,
-                          size_t(p->num_seqs) * p->num_q_heads * p->head_dim * 2,
+                          size_t(p->num_seqs) * (p->query_len > 1 ? p->query_len : 1) *
+                              p->num_q_heads * p->head_dim * 2,
                           cudaMemcpyDeviceToHost, s);
       if (e != cudaSuccess) return pa::set_cuda_error("pa_step_host: output copy", int(e));
     }

@@ -245,6 +245,37 @@ def test_multi_fused_append_slot_rules(pk):
     assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
 
 
+@pytest.mark.parametrize("QL,pinned", [(2, True), (4, True), (3, False)])
+def test_multi_step_host_matches_device_step(pk, QL, pinned):
+    """pa_step_host with query_len Q (q, k_new, v_new, slots and the output
+    carrying Q rows per sequence) gives pa_append_decode's output and caches
+    bit for bit, with pinned and pageable buffers."""
+    lens = [QL, 17, 33, 16 + QL, 500, 2049]
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case(lens, QL, 32, 8, seed=120 + QL)
+    kd, vd = kc.clone(), vc.clone()
+    want = pk.pa_append_decode(q, kd, vd, torch.from_numpy(tables).cuda(),
+                               torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
+                               torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    kh, vh = kc.clone(), vc.clone()
+    B, _, Hq, D = q.shape
+    p = pk.make_step_host_params(kh, vh, B, Hq, tables.shape[1], int(lens.max()), query_len=QL)
+    host_in = pk.pack_step_inputs(p, q.cpu(), kn.cpu(), vn.cpu(), slots, tables, lens, pin=pinned)
+    host_out = torch.empty((B, QL, Hq, D), dtype=torch.bfloat16)
+    if pinned:
+        host_out = host_out.pin_memory()
+    ws = torch.empty(pk.pa_step_host_workspace_size(p), dtype=torch.uint8, device="cuda")
+    pk.pa_step_host(p, host_in, host_out, ws)
+    assert pk.pa_device_errors() == 0
+    assert torch.equal(host_out.view(torch.int16), want.cpu().view(torch.int16))
+    assert torch.equal(kh.view(torch.int16), kd.view(torch.int16))
+    assert torch.equal(vh.view(torch.int16), vd.view(torch.int16))
+    ko, vo = oracle.reshape_and_cache(kn.cpu(), vn.cpu(), oracle.bf16_bits(kc.cpu()),
+                                      oracle.bf16_bits(vc.cpu()), slots)
+    harness.assert_close(harness.bf16_tensor_to_f64(host_out),
+                         oracle.paged_decode_multi(q.cpu(), ko, vo, tables, lens))
+
+
 # ---------------------------------------------------------------- 8-bit cache
 
 
