@@ -211,3 +211,33 @@ def test_step_host_layout_and_workspace(pk):
     p.num_cow_pairs = 70000
     assert lib.pa_step_host_layout(ctypes.byref(p), ctypes.byref(L)) == 1
     assert lib.pa_step_host_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_step_host_layout_with_new_tokens_and_cache_type(pk):
+    """With query_len Q the q, k_new, v_new and slot sections hold Q rows per
+    sequence and the staged output Q times the rows; kv_dtype and query_len
+    outside their ranges are rejected."""
+    lib = pk.load()
+    p = pk.StepHostParams()
+    p.num_seqs, p.num_q_heads, p.num_kv_heads, p.head_dim = 3, 8, 2, 128
+    p.block_size, p.num_blocks, p.max_blocks_per_seq, p.max_context_len = 16, 10, 5, 80
+    p.scale, p.query_len = 0.088, 4
+    L = pk.StepLayout()
+    assert lib.pa_step_host_layout(ctypes.byref(p), ctypes.byref(L)) == 0
+    sizes = [3 * 4 * 8 * 128 * 2, 3 * 4 * 2 * 128 * 2, 3 * 4 * 2 * 128 * 2, 3 * 4 * 8, 3 * 5 * 4,
+             3 * 4, 0]
+    offs = [L.q, L.k_new, L.v_new, L.slot_mapping, L.block_tables, L.context_lens, L.cow_pairs]
+    for i in range(len(offs)):
+        assert offs[i] % 256 == 0
+        end = offs[i + 1] if i + 1 < len(offs) else L.total
+        assert end == _ru(offs[i] + sizes[i])
+    dec = _params(pk, num_seqs=3, num_q_heads=8, num_kv_heads=2, max_blocks_per_seq=5,
+                  max_context_len=80, num_blocks=10)
+    dec.query_len = 4
+    want = _ru(L.total + 3 * 4 * 8 * 128 * 2) + lib.pa_decode_workspace_size(ctypes.byref(dec))
+    assert lib.pa_step_host_workspace_size(ctypes.byref(p)) == want
+    for field, bad in (("query_len", -1), ("query_len", 1025), ("kv_dtype", 7)):
+        q = pk.StepHostParams.from_buffer_copy(p)
+        setattr(q, field, bad)
+        assert lib.pa_step_host_layout(ctypes.byref(q), ctypes.byref(L)) == 1  # PA_ERR_INVALID_ARG
+        assert lib.pa_step_host_workspace_size(ctypes.byref(q)) == 0
