@@ -2,8 +2,9 @@
 // kernels and their host-side launch templates. Each including translation
 // unit instantiates a share of the instances (pa_decode_tc.cu: bf16 head_dim
 // 128 and the shared entry points; pa_decode_tc_d64.cu: bf16 head_dim 64;
-// pa_decode_tc_fp8.cu: the 8-bit cache), so they compile in parallel. Each
-// has its own device error word.
+// pa_decode_tc_fp8.cu: the 8-bit cache; pa_decode_tc_bs8.cu,
+// pa_decode_tc_bs32.cu, pa_decode_tc_bs32_fp8.cu: block sizes 8 and 32), so
+// they compile in parallel. Each has its own device error word.
 //
 // Same result as the CUDA-core kernel ("Paged Attention as a Memory
 // Manager", §How the Kernel Executes Paged Attention; "PagedAttention and
@@ -34,10 +35,18 @@
 // its own KV head, and P^T is block-diagonal (zero unless the column's head
 // is r's), so the second MMA sums each column over its own KV head's keys
 // only. The unused products are free: the tensor pipe runs at a few percent
-// here. Softmax runs on CUDA cores, one thread per row.
+// here. Softmax runs on CUDA cores, one thread per row. P^T's layout depends
+// on the columns: K-major up to 32 (and at 64 with block size 8), per-head
+// [16 keys][16 columns] tiles at 64 (the value product then runs per head and
+// P^T takes 4 KiB, which leaves room for a third ring slot), MN-major like V
+// at 128. The 8-bit cache splits queries and P into two E4M3 terms each
+// (kind::f8f6f4), its queries split by a preparation launch.
 //
-// Scheduling (stream-K). The blocks of all sequences form one stream; CTA c
-// takes the c-th contiguous 1/grid of it. A (sequence, CTA) segment that
+// Scheduling (stream-K). The blocks of all sequences form one stream,
+// measured in cost: a sequence costs its units plus a start charge of a few
+// chunks (start_chunks); CTA c takes the c-th contiguous share of the cost.
+// Before its dependency wait each CTA prefetches its first blocks into L2,
+// so their DRAM latency overlaps the previous launch. A (sequence, CTA) segment that
 // holds a whole sequence writes the bf16 output directly; otherwise it writes
 // fp32 (max, sum, weighted sum) partials to slot (sequence + CTA), unique
 // along the stream, and the merge kernel combines them by log-sum-exp.
