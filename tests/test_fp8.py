@@ -412,3 +412,26 @@ def test_fp8_step_host_matches_device_step(pk, pinned):
                                           vs.cpu().numpy())
     assert np.array_equal(kh.cpu().numpy(), ko)
     assert np.array_equal(vh.cpu().numpy().reshape(NB, Hkv, bs, D), vo)
+
+
+def test_fp8_step_host_with_several_new_tokens(pk):
+    """pa_step_host on the 8-bit cache with query_len 2: output and caches bit
+    for bit against pa_append_decode on the same inputs."""
+    import torch
+
+    QL = 2
+    c = _fused_fp8(pk, [QL, 17, 40, 300, 1025], 32, 8, seed=130, QL=QL)
+    NB, Hkv, D, bs = c["NB"], c["Hkv"], 128, c["bs"]
+    B = len(c["lens"])
+    kh = torch.from_numpy(c["k0"]).cuda()
+    vh = torch.from_numpy(c["v0"]).cuda()
+    p = pk.make_step_host_params(kh, vh, B, 32, c["tables"].shape[1], int(c["lens"].max()),
+                                 k_scale=c["ks"], v_scale=c["vs"], query_len=QL)
+    host_in = pk.pack_step_inputs(p, c["q"].cpu(), c["kn"].cpu(), c["vn"].cpu(), c["slots"],
+                                  c["tables"], c["lens"])
+    host_out = torch.empty((B, QL, 32, D), dtype=torch.bfloat16).pin_memory()
+    ws = torch.empty(pk.pa_step_host_workspace_size(p), dtype=torch.uint8, device="cuda")
+    pk.pa_step_host(p, host_in, host_out, ws)
+    assert pk.pa_device_errors() == 0
+    assert torch.equal(host_out.view(torch.int16), c["out"].cpu().view(torch.int16))
+    assert torch.equal(kh, c["k8"]) and torch.equal(vh, c["v8"])
