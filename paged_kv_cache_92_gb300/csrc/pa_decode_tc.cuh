@@ -1440,22 +1440,31 @@ int make_map_halves(CUtensorMap* m, const void* base, uint64_t tiles, uint64_t d
 }
 
 // The 8-bit V^T cache: per (block, KV head) tile, BS/16 sub-tiles of
-// [D rows][16 bytes]. Block size 16: a 3-D tensor [tiles][D][16], box =
-// `heads` whole tiles. Block size 32: a 4-D tensor [tiles][2][D][16], box =
-// one sub-tile of `heads` tiles. No swizzle.
+// [D rows][16 bytes], each sub-tile D * 16 contiguous bytes. The map reads a
+// sub-tile as rows of 256 bytes rather than D rows of 16 bytes: the same
+// bytes land at the same shared-memory offsets (both boxes are contiguous
+// row-major copies), with a sixteenth of the rows for the copy engine to walk
+// and whole 32-byte sectors per row. Block size 16: a 3-D tensor
+// [tiles][D/16][256], box = `heads` whole tiles. Block size 32: a 4-D tensor
+// [tiles][2][D/16][256], box = one sub-tile of `heads` tiles. The kernel's
+// coordinates are (0, 0, tile) and (0, 0, sub-tile, tile) either way. No
+// swizzle.
 int make_map_vt(CUtensorMap* m, const void* base, uint64_t tiles, uint64_t d, uint32_t heads,
                 int block_size) {
-  const uint64_t sub = d * kF8Tile;  // bytes of one sub-tile
+  constexpr uint64_t kRow = 256;                  // bytes of one box row
+  const uint64_t sub = d * kF8Tile;               // bytes of one sub-tile
+  const uint64_t rows = sub / kRow;               // box rows of one sub-tile
+  if (sub % kRow != 0) return int(cudaErrorInvalidValue);
   if (block_size == 16) {
-    const cuuint64_t dims[3] = {uint64_t(kF8Tile), d, tiles};
-    const cuuint64_t strides[2] = {uint64_t(kF8Tile), sub};
-    const cuuint32_t box[3] = {uint32_t(kF8Tile), uint32_t(d), heads};
+    const cuuint64_t dims[3] = {kRow, rows, tiles};
+    const cuuint64_t strides[2] = {kRow, sub};
+    const cuuint32_t box[3] = {uint32_t(kRow), uint32_t(rows), heads};
     return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box,
                        CU_TENSOR_MAP_SWIZZLE_NONE);
   }
-  const cuuint64_t dims[4] = {uint64_t(kF8Tile), d, 2, tiles};
-  const cuuint64_t strides[3] = {uint64_t(kF8Tile), sub, 2 * sub};
-  const cuuint32_t box[4] = {uint32_t(kF8Tile), uint32_t(d), 1, heads};
+  const cuuint64_t dims[4] = {kRow, rows, 2, tiles};
+  const cuuint64_t strides[3] = {kRow, sub, 2 * sub};
+  const cuuint32_t box[4] = {uint32_t(kRow), uint32_t(rows), 1, heads};
   return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
 }
