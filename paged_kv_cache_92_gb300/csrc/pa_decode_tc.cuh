@@ -1488,8 +1488,8 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   const uint64_t tiles = uint64_t(p->num_blocks) * H;
   int r = 0;
   if constexpr (F8) {
-    // K rows of D bytes; V^T rows of 16 bytes, [D][16] sub-tiles per (block,
-    // head); the split queries, 2N rows of D bytes per sequence
+    // K rows of D bytes; V^T [D][16] sub-tiles per (block, head), copied as
+    // 256-byte rows; the split queries, 2N rows of D bytes per sequence
     if constexpr (VS == 1) {
       r = make_map_u8(&tk, p->k_cache, cache_rows, D, D, uint32_t(BS * H),
                       CU_TENSOR_MAP_SWIZZLE_128B);
