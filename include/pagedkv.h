@@ -160,6 +160,14 @@ typedef struct {
                                   num_kv_heads * G * Qp <= 128 (<= 64 for the 8-bit cache); other
                                   shapes return PA_ERR_UNSUPPORTED. A sequence with
                                   0 < context_lens[b] < Q gets zero rows and PA_DEVERR_CONTEXT_LEN. */
+  int32_t wait_timeout_us;     /* tensor-core kernel: the longest one of its barrier waits may
+                                  take, in microseconds; 0 = 2 s. A wait that runs out sets
+                                  PA_DEVERR_TIMEOUT, and every CTA that saw it stops, lets the
+                                  copies it has in flight land, frees its tensor memory and
+                                  exits: the outputs are then unspecified, the context stays
+                                  usable. A budget far below a launch's normal waits makes a
+                                  well-formed launch run out (what the tests do to exercise that
+                                  exit). Must be >= 0. */
 } pa_decode_params;
 
 /* Decode kernel variants; both compute the same function. The tensor-core
@@ -187,10 +195,11 @@ typedef struct {
 #define PA_DECODE_CUDA_CORE 1   /* fp32 FMAs on CUDA cores, 1-D bulk-copy rings */
 
 /* Bytes of device workspace pa_decode needs for these parameters on the
- * current device: a 256-byte header, then the larger of the two kernels'
- * needs -- the CUDA-core kernel's per-partition partials, or the tensor-core
- * kernel's work plan and per-(sequence, SM) partials. Returns 0 for invalid
- * params. */
+ * current device: a 256-byte header, then what the kernel these parameters
+ * select needs -- the tensor-core kernel's work plan and per-(sequence + SM)
+ * partials of every query column (variant PA_DECODE_TENSOR_CORE on a shape it
+ * handles), else the CUDA-core kernel's per-partition partials (none when no
+ * sequence can split). Returns 0 for invalid params. */
 size_t pa_decode_workspace_size(const pa_decode_params* p);
 
 /* Enqueue the decode. `workspace` is caller-owned device memory of at least
@@ -210,10 +219,14 @@ pa_status pa_decode(const pa_decode_params* p, void* workspace, size_t workspace
  * The split-K partials go to a fixed device array inside the library
  * (PA_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library until
  * the process exits). Nothing is allocated or freed by the call.
- *  - Shapes whose workspace (pa_decode_workspace_size) exceeds that are
- *    rejected with PA_ERR_INVALID_ARG.
- *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture.
+ *  - Shapes whose workspace (pa_decode_workspace_size, which sizes the
+ *    kernel the parameters select) exceeds that are rejected with
+ *    PA_ERR_INVALID_ARG.
+ *  - The first call in each CUDA context looks up the array's device address
+ *    with that context's device current; make that first call before any
+ *    stream capture. A device reset (cudaDeviceReset) or another context on
+ *    the same device is a new context, and its first call looks the address
+ *    up again.
  *  - Every call on a device shares the one array and leaves its partials in
  *    it. Calls whose kernels overlap on the GPU (different streams, no
  *    ordering between them) race on it and give unspecified results.

@@ -62,6 +62,8 @@ def _load():
         lib.oracle_copy_blocks.argtypes = [p, p, p, i32, i32, i32, i32, i32]
         lib.oracle_copy_blocks.restype = ctypes.c_int
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         u8 = ctypes.c_uint8
         lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
         lib.oracle_e4m3_from_float.restype = u8
@@ -84,6 +86,12 @@ def _load():
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Host threads the C oracle's loops use from now on (timing only; every
+    unit is computed by one thread, so results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _ptr(a: np.ndarray):

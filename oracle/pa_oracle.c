@@ -432,3 +432,15 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads the OpenMP loops use from now on (n >= 1); for timing the oracle
+ * on a given number of host cores. The results do not depend on it: every
+ * unit is computed independently by one thread. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  extern void omp_set_num_threads(int);
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

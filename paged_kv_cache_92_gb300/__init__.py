@@ -69,7 +69,7 @@ class DecodeParams(ctypes.Structure):
         ("scale", ctypes.c_float), ("partition_tokens", ctypes.c_int32),
         ("variant", ctypes.c_int32), ("overlap_prologue", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
-        ("query_len", ctypes.c_int32),
+        ("query_len", ctypes.c_int32), ("wait_timeout_us", ctypes.c_int32),
     ]
 
 
@@ -212,7 +212,7 @@ def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
                        max_context_len: int, scale: Optional[float] = None,
                        partition_tokens: int = 0, variant: int = DECODE_TENSOR_CORE,
                        overlap_prologue: bool = False, k_scale=None,
-                       v_scale=None) -> DecodeParams:
+                       v_scale=None, wait_timeout_us: int = 0) -> DecodeParams:
     """Marshal a pa_decode call. q and out are bf16 [B][Hq][D] (one new token
     per sequence) or [B][Q][Hq][D] (Q new tokens per sequence, causal among
     them). bf16 caches [NB][Hkv][BS][D]; uint8 caches are the 8-bit E4M3 cache
@@ -255,6 +255,7 @@ def make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
     p.variant = int(variant)
     p.overlap_prologue = int(bool(overlap_prologue))
     p.query_len = int(QL)
+    p.wait_timeout_us = int(wait_timeout_us)
     return p
 
 
@@ -265,7 +266,8 @@ def pa_decode_workspace_size(params: DecodeParams) -> int:
 def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
               scale: Optional[float] = None, partition_tokens: int = 0, out=None,
               workspace=None, stream=None, variant: int = DECODE_TENSOR_CORE,
-              overlap_prologue: bool = False, k_scale=None, v_scale=None):
+              overlap_prologue: bool = False, k_scale=None, v_scale=None,
+              wait_timeout_us: int = 0):
     """Paged decode attention; returns ``out`` (bf16, the shape of ``q``:
     [B][Hq][d], or [B][Q][Hq][d] for Q new tokens per sequence).
 
@@ -279,7 +281,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
         out = torch.empty_like(q)
     p = make_decode_params(q, out, k_cache, v_cache, block_tables, context_lens,
                            max_context_len, scale, partition_tokens, variant, overlap_prologue,
-                           k_scale, v_scale)
+                           k_scale, v_scale, wait_timeout_us)
     need = int(lib.pa_decode_workspace_size(ctypes.byref(p)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

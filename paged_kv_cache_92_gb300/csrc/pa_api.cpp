@@ -61,6 +61,8 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: kv_dtype must be PA_KV_BF16 or PA_KV_FP8_E4M3");
   if (p->query_len < 0 || p->query_len > 1024)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: query_len must be in [0, 1024]");
+  if (p->wait_timeout_us < 0)
+    return set_error(PA_ERR_INVALID_ARG, "pa_decode: wait_timeout_us must be >= 0");
   if (int64_t(p->num_seqs) * query_len_of(p) * p->num_q_heads >= (int64_t(1) << 31) - 16)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: query rows exceed 2^31");
   if (p->block_size != kBlockSize && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
@@ -117,21 +119,29 @@ pa_status set_cuda_error(const char* where, int err) {
   return PA_ERR_CUDA;
 }
 
+bool decode_uses_tc(const pa_decode_params* p) {
+  return p->variant == PA_DECODE_TENSOR_CORE && tc_supports(p);
+}
+
 WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_partitions,
                                         int grid) {
   WorkspaceLayout w{};
   const size_t H = kWorkspaceHeaderBytes;
-  // CUDA-core kernel: per-partition partials (only when a sequence can split)
-  size_t simt_end = H;
-  if (num_partitions > 1) {
-    const size_t rows = size_t(p->num_seqs) * p->num_q_heads * num_partitions;
-    w.simt_m = H;
-    w.simt_l = w.simt_m + round_up(rows * sizeof(float), 256);
-    w.simt_acc = w.simt_l + round_up(rows * sizeof(float), 256);
-    simt_end = w.simt_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+  if (!decode_uses_tc(p)) {
+    // CUDA-core kernel: per-partition partials (only when a sequence can split)
+    w.total = H;
+    if (num_partitions > 1) {
+      const size_t rows = size_t(p->num_seqs) * p->num_q_heads * num_partitions;
+      w.simt_m = H;
+      w.simt_l = w.simt_m + round_up(rows * sizeof(float), 256);
+      w.simt_acc = w.simt_l + round_up(rows * sizeof(float), 256);
+      w.total = w.simt_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+    }
+    return w;
   }
   // tensor-core kernel: stream-K plan, then one partial per (sequence, CTA)
-  // segment and query column (= query head for one token per sequence)
+  // segment and query column (= query head for one token per sequence). With
+  // no device to query, the grid is taken as 256 CTAs (an upper bound).
   const size_t segs = size_t(p->num_seqs) + size_t(grid > 0 ? grid : 256);
   const size_t rows = segs * size_t(tc_cols(p));
   w.tc_plan = H;
@@ -148,7 +158,7 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
     w.tc_qp = tc_end;
     tc_end = w.tc_qp + round_up(size_t(p->num_seqs) * n_pad * p->head_dim * 2, 256);
   }
-  w.total = simt_end > tc_end ? simt_end : tc_end;
+  w.total = tc_end;
   return w;
 }
 
@@ -164,7 +174,9 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
   L.grid = grid;
   char where[96];
   int e = 0;
-  if (p->variant == PA_DECODE_TENSOR_CORE && tc_supports(p) && grid > 0) {
+  if (decode_uses_tc(p)) {
+    if (grid <= 0)
+      return set_cuda_error("the SM count of the current device", int(cudaErrorNoDevice));
     L.plan = reinterpret_cast<int*>(ws + w.tc_plan);
     L.q8 = p->kv_dtype == PA_KV_FP8_E4M3 ? ws + w.tc_q8 : nullptr;
     L.q_inv_alpha =
@@ -370,9 +382,14 @@ pa_status pa_decode_noalloc(const pa_decode_params* p, pa_stream_t stream) {
   const pa::WorkspaceLayout w = pa::decode_workspace_layout(p, np, grid);
   if (w.total > pa::kNoAllocScratchBytes)
     return pa::set_error(PA_ERR_INVALID_ARG,
-                         "pa_decode_noalloc: these shapes need more split-K scratch than the "
-                         "library's fixed PA_NOALLOC_SCRATCH_BYTES; use pa_decode with a workspace "
-                         "or a larger partition_tokens");
+                         pa::decode_uses_tc(p)
+                             ? "pa_decode_noalloc: these shapes need more split-K scratch than the "
+                               "library's fixed PA_NOALLOC_SCRATCH_BYTES (the tensor-core kernel's "
+                               "partials grow with num_seqs + SM count times the query columns); "
+                               "use pa_decode with a workspace"
+                             : "pa_decode_noalloc: these shapes need more split-K scratch than the "
+                               "library's fixed PA_NOALLOC_SCRATCH_BYTES; use pa_decode with a "
+                               "workspace or a larger partition_tokens");
   void* scratch = nullptr;
   const int e = pa::decode_scratch_address(&scratch);
   if (e != 0) return pa::set_cuda_error("pa_decode_noalloc: scratch lookup", e);

@@ -30,6 +30,7 @@
 //    workspace, combined by the merge kernel (log-sum-exp).
 //  * The reduction order depends only on logical token positions, so results
 //    are bit-identical under any physical block placement.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -472,15 +473,51 @@ int launch_decode(const DecodeLaunch& Lc, void* stream) {
 //
 // Host code cannot pass the array's name to a kernel (on the host it is only
 // a stand-in, not a device address), so its device address is looked up with
-// cudaGetSymbolAddress once per device, with that device current, on the
-// first call made on that device, and cached.
+// cudaGetSymbolAddress, with the device current, on the first call made in
+// each CUDA context, and cached under the context's process-unique ID
+// (cuCtxGetId). A device reset, or a driver-API context other than the
+// primary one, is a new context: the address is looked up again there
+// instead of reusing one that may no longer be valid.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+  unsigned long long ctx_id;  // 0: not looked up yet
+  void* addr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+std::once_flag g_ctx_fn_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// The process-unique ID of the calling thread's current context, 0 if there is none.
+unsigned long long current_context_id() {
+  std::call_once(g_ctx_fn_once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 }  // namespace
 
 int decode_scratch_address(void** addr) {
@@ -489,13 +526,16 @@ int decode_scratch_address(void** addr) {
   if (e != cudaSuccess) return int(e);
   if (dev < 0 || dev >= kMaxDevices) return int(cudaErrorInvalidDevice);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  const unsigned long long id = current_context_id();
+  if (id == 0 || g_scratch[dev].ctx_id != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);  // makes the device's context current
     if (e != cudaSuccess) return int(e);
-    g_scratch_addr[dev] = p;
+    // the context the lookup ran in (it may have just been created)
+    g_scratch[dev].ctx_id = current_context_id();
+    g_scratch[dev].addr = p;
   }
-  *addr = g_scratch_addr[dev];
+  *addr = g_scratch[dev].addr;
   return int(cudaSuccess);
 }
 

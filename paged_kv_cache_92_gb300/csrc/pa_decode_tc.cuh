@@ -186,6 +186,9 @@ struct TcCfg {
   static constexpr int ST = ST_FIT > ST_CAP ? ST_CAP : ST_FIT;
   static_assert(!F8 || D == 128, "the 8-bit cache is built for head_dim 128");
   static_assert(ST >= 2, "at least a double-buffered ring");
+  // the stream-K plan's prefix pre[0 .. B] is built in the still-empty ring
+  static_assert(size_t(ST) * SLOT_BYTES >= (size_t(kTcMaxSeqs) + 1) * sizeof(int),
+                "the ring holds the plan of the largest batch");
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_Q = ST * SLOT_BYTES;
   static constexpr int OFF_P = OFF_Q + QB * Q_BYTES;
@@ -255,6 +258,7 @@ struct TcParams {
   // token index is >= q_len. num_cols = num_kv_heads * GE.
   int num_cols, q_len, g_log2;
   float scale_log2;
+  uint64_t wait_ns;  // budget of one barrier wait (2 s unless the caller set another)
 };
 
 // Context length of sequence b as the kernel uses it: clamped to the table
@@ -336,7 +340,8 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
                                          unsigned char* pbuf, uint64_t* full, uint64_t* empty,
                                          uint64_t* qempty, uint64_t* bar_s, uint64_t* bar_o,
                                          uint64_t* bar_p, uint64_t* drain, const ChunkMeta* meta,
-                                         uint32_t tmem, volatile int* abort_flag, int H) {
+                                         uint32_t tmem, volatile int* abort_flag, int H,
+                                         uint64_t wait_ns) {
   using C = TcCfg<D, N, F8, DIAG>;
   // D = 64: the second 64-row half of M re-reads the first (LBO 0); those
   // TMEM lanes are never read back.
@@ -450,7 +455,7 @@ __device__ __forceinline__ void mma_loop(unsigned char* ring, unsigned char* qbu
       continue;
     }
     if (*abort_flag) break;
-    if (dev::global_timer_ns() - t_progress > dev::kWaitNsLimit) {
+    if (dev::global_timer_ns() - t_progress > wait_ns) {
       ok = false;
       break;
     }
@@ -526,14 +531,17 @@ struct Softmax {
     int pv_done = -1;  // highest chunk whose value product is known to be complete
     // wait for chunk k's value product (k > pv_done)
     auto wait_pv = [&](int k) {
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[k % C::PB], uint32_t(k / C::PB) & 1u)) &&
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[k % C::PB], uint32_t(k / C::PB) & 1u,
+                                                   P.wait_ns, abort_flag)) &&
            ok;
       pv_done = k;
     };
 
     for (;;) {
       const int slot = c % C::ST;
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&full[slot], uint32_t(c / C::ST) & 1u)) && ok;
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&full[slot], uint32_t(c / C::ST) & 1u, P.wait_ns,
+                                                 abort_flag)) &&
+           ok;
       const ChunkMeta m = meta[slot];
       // every exit below is taken by all 128 threads together (named barriers follow)
       if (!dev::named_barrier_and(1, kCons, ok && *abort_flag == 0)) {
@@ -545,7 +553,9 @@ struct Softmax {
       const bool first = (m.flags & F_FIRST) != 0;
 
       // ---- scores of this chunk -> registers
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(c / C::kSBufs) & 1u)) && ok;
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[buf], uint32_t(c / C::kSBufs) & 1u,
+                                                 P.wait_ns, abort_flag)) &&
+           ok;
       dev::tc_fence_after();
       float s[LDC];
       const uint32_t tS = tmem + t_lane + buf * C::NS + col0;
@@ -1109,7 +1119,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int slot = chunk_seq % C::ST;
         const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
         if (lane == 0) {
-          ok = dev::mbar_wait_sleep(&empty[slot], ph ^ 1u, 64);
+          ok = dev::mbar_wait_sleep(&empty[slot], ph ^ 1u, 64, P.wait_ns, abort_flag);
           if (ok) {
             ChunkMeta m;
             m.b = b;
@@ -1180,8 +1190,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // segment's last score product.
           bool qok = true;
           if (lane == 31) {
-            qok = dev::mbar_wait_sleep(&qempty[qs], (uint32_t(seg_seq / C::QB) & 1u) ^ 1u, 64);
-            if (qok) {
+            qok = dev::mbar_wait_sleep(&qempty[qs], (uint32_t(seg_seq / C::QB) & 1u) ^ 1u, 64,
+                                       P.wait_ns, abort_flag);
+            if (!qok) {
+              // the chunk's barrier was told to expect the queries too: take
+              // their bytes off it, so that its phase completes when the K/V
+              // copies already issued have landed
+              *abort_flag = 1;
+              dev::mbar_complete_tx(&full[slot], C::Q_TX);
+            } else {
               if constexpr (F8) {
                 dev::tma_load_2d(qbuf + qs * C::Q_BYTES, &tm_q, 0, b * P.q_rows, &full[slot],
                                  pol);
@@ -1195,13 +1212,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
             }
           }
-          if (__shfl_sync(0xffffffffu, int(qok), 31) == 0) {
-            ok = false;
-            break;
-          }
+          if (__shfl_sync(0xffffffffu, int(qok), 31) == 0) ok = false;
         }
+        // counted as issued even when its queries were not: its K/V copies
+        // are in flight, and the wind-down waits for them
         ++chunk_seq;
         if (lane == 0) *issued = chunk_seq;
+        if (!ok) break;
       }
       ++seg_seq;
       if (uend < nb) break;  // the range ends inside b
@@ -1211,18 +1228,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       win = win_nxt_seq;
       L_cur = L_nxt;
     }
-    // end of work: a sentinel chunk tells the consumers to stop
+    // end of work: a sentinel chunk tells the consumers to stop. After an
+    // abort there is none: every other role gives up its waits on the flag,
+    // and an extra arrival on a barrier whose copies are still in flight
+    // would be undefined.
     if (lane == 0) {
-      const int slot = chunk_seq % C::ST;
-      const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
-      const bool ok2 = dev::mbar_wait(&empty[slot], ph ^ 1u);
-      ChunkMeta m{};
-      m.flags = F_END;
-      meta[slot] = m;
-      dev::mbar_arrive(&full[slot]);
-      if (!ok || !ok2) {
+      if (!ok) {
         atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
+      }
+      if (!*abort_flag) {
+        const int slot = chunk_seq % C::ST;
+        const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
+        if (dev::mbar_wait(&empty[slot], ph ^ 1u, P.wait_ns, abort_flag)) {
+          ChunkMeta m{};
+          m.flags = F_END;
+          meta[slot] = m;
+          dev::mbar_arrive(&full[slot]);
+        } else if (!*abort_flag) {
+          atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
       }
     }
   } else if (warp == kMmaWarp) {
@@ -1230,7 +1256,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0)
       mma_loop<D, GE, N, F8, kDiagP<D, GE, N, F8, BS>, kMnP<D, GE, N, F8, BS>>(
           ring, qbuf, pbuf, full, empty, qempty, bar_s, bar_o, bar_p, drain, meta, tmem,
-          abort_flag, H);
+          abort_flag, H, P.wait_ns);
   } else {
     // ------------------------------------------------------------ softmax
     Softmax<D, GE, N, F8, BS>::run(P, ring, pbuf, full, bar_s, bar_o, bar_p, meta, red, red2,
@@ -1241,8 +1267,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (*abort_flag && tid == 0) {
     // Wind down after a stalled wait: every bulk copy issued but not consumed
-    // lands (each wait bounded) before shared memory is released. (The MMA
-    // warp has already waited for its own MMAs.)
+    // lands (each wait bounded by the full 2 s budget, whatever the caller's,
+    // and deaf to the flag) before shared memory is released. (The MMA warp
+    // has already waited for its own MMAs.)
     for (int c = *consumed; c < *issued; ++c)
       (void)dev::mbar_wait(&full[c % C::ST], uint32_t(c / C::ST) & 1u);
   }
@@ -1552,6 +1579,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.cap = min(p->max_blocks_per_seq * BS, p->max_context_len);
   P.oob_row = VS == 1 ? int(cache_rows) : int(tiles);
   P.scale_log2 = p->scale * kLog2e;
+  P.wait_ns = p->wait_timeout_us > 0 ? uint64_t(p->wait_timeout_us) * 1000u : dev::kWaitNsLimit;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   cudaLaunchConfig_t cfg = {};

@@ -92,17 +92,27 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Upper bounds of a barrier wait: an iteration count and a wall-clock
-// budget. A wait that runs out returns false; the caller records
-// PA_DEVERR_TIMEOUT and winds down instead of spinning forever.
+// budget (kWaitNsLimit unless the caller passes another). A wait that runs
+// out returns false; the caller records PA_DEVERR_TIMEOUT and winds down
+// instead of spinning forever. With `abort` a wait also gives up (false)
+// once another role of the CTA has set that flag. Budgets below
+// kShortWaitNs are checked on every poll, so they run out promptly.
 constexpr uint32_t kWaitIterLimit = 1u << 24;
 constexpr uint64_t kWaitNsLimit = 2000000000ull;  // 2 s
+constexpr uint64_t kShortWaitNs = 1000000ull;     // 1 ms
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitNsLimit,
+                                          const volatile int* abort = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const uint32_t mask = limit_ns < kShortWaitNs ? 0u : 255u;
   for (uint32_t it = 0; it < kWaitIterLimit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u && global_timer_ns() - t0 > kWaitNsLimit) break;
+    if ((it & mask) == mask) {
+      if (global_timer_ns() - t0 > limit_ns) break;
+      if (abort != nullptr && *abort) break;
+    }
   }
   return false;
 }
@@ -110,15 +120,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // Same bounds, but the waiting thread sleeps between polls so that a warp
 // that is only waiting (producer, MMA issue) leaves the issue slots of its
 // SM sub-partition to the warps doing arithmetic.
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns,
+                                                uint64_t limit_ns = kWaitNsLimit,
+                                                const volatile int* abort = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const uint32_t mask = limit_ns < kShortWaitNs ? 0u : 63u;
   for (uint32_t it = 0; it < kWaitIterLimit; ++it) {
     __nanosleep(ns);
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitNsLimit) break;
+    if ((it & mask) == mask) {
+      if (global_timer_ns() - t0 > limit_ns) break;
+      if (abort != nullptr && *abort) break;
+    }
   }
   return false;
+}
+
+// Take `bytes` off the transaction count of the barrier's current phase, as
+// if a copy of that many bytes had landed: for a copy that was announced
+// with expect_tx but is not issued after all.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
 }
 
 // Programmatic dependent launch. launch_dependents: the next kernel on the

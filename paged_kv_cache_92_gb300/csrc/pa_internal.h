@@ -97,7 +97,9 @@ __device__ __forceinline__ int64_t query_source_row(const QueryMap& m, int b, in
 // Bytes at the start of every decode workspace (reserved).
 constexpr size_t kWorkspaceHeaderBytes = 256;
 
-// Workspace carve-up. Both kernels start after the header; a call uses one.
+// Workspace carve-up of the kernel a call will run (decode_uses_tc: the
+// tensor-core kernel; otherwise the CUDA-core one), after the header. The
+// other kernel's fields are zero.
 struct WorkspaceLayout {
   size_t total;
   size_t simt_m, simt_l, simt_acc;    // [seqs][q heads][partitions](+[dim])
@@ -112,6 +114,9 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
 // device, or 0 if that cannot be queried).
 bool tc_supports(const pa_decode_params* p);
 int tc_grid();
+// The decode runs on the tensor-core kernel: variant PA_DECODE_TENSOR_CORE and
+// a shape it handles (else the CUDA-core kernel runs).
+bool decode_uses_tc(const pa_decode_params* p);
 
 // Kernel launchers (pa_decode.cu / pa_cache.cu). Return a cudaError_t as int.
 int launch_decode(const DecodeLaunch& L, void* stream);      // CUDA-core decode kernel

@@ -96,14 +96,19 @@ def _ru(x):
     return (x + 255) // 256 * 256
 
 
-def _expected_ws(B, Hq, D, parts, grid, Hkv=None, QL=1):
-    """Tensor-core partials are per query column: Hkv * G * (QL rounded up to
-    a power of two); with QL > 1 the bf16 queries are also staged in column
-    order, [B][N][D] with N the columns padded to 16/32/64/128."""
-    simt = 0
-    if parts > 1:
-        rows = B * Hq * parts
-        simt = 2 * _ru(rows * 4) + _ru(rows * D * 4)
+def _expected_ws(B, Hq, D, parts, grid, Hkv=None, QL=1, variant=0):
+    """The workspace of the kernel that will run. Tensor-core kernel (variant
+    0): the stream-K plan and the partials per (sequence + CTA) and query
+    column, Hkv * G * (QL rounded up to a power of two) columns; with QL > 1
+    the bf16 queries are also staged in column order, [B][N][D] with N the
+    columns padded to 16/32/64/128. CUDA-core kernel (variant 1): the
+    per-partition partials, when a sequence can split."""
+    if variant == 1:
+        simt = 0
+        if parts > 1:
+            rows = B * Hq * parts
+            simt = 2 * _ru(rows * 4) + _ru(rows * D * 4)
+        return 256 + simt
     qlp = 1
     while qlp < QL:
         qlp *= 2
@@ -113,13 +118,14 @@ def _expected_ws(B, Hq, D, parts, grid, Hkv=None, QL=1):
     if QL > 1:
         n_pad = next(n for n in (16, 32, 64, 128) if cols <= n)
         tc += _ru(B * n_pad * D * 2)
-    return 256 + max(simt, tc)
+    return 256 + tc
 
 
 def test_decode_workspace_size(pk):
-    """Header + the larger of the CUDA-core per-partition partials and the
-    tensor-core plan + per-(sequence, SM) partials. Without a GPU the SM count
-    used for sizing is 256."""
+    """Header + the workspace of the kernel the parameters select: the
+    tensor-core plan + per-(sequence, SM) partials, or the CUDA-core
+    per-partition partials. Without a GPU the SM count used for sizing is
+    256."""
     lib = pk.load()
     got = lib.pa_decode_workspace_size(ctypes.byref(_params(pk)))
     assert got == _expected_ws(2, 8, 128, 1, 256)
@@ -129,6 +135,29 @@ def test_decode_workspace_size(pk):
                 max_blocks_per_seq=2048)
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 64, 256)
     assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk, head_dim=96))) == 0
+    # the CUDA-core variant sizes its own partials only
+    for mx, parts in ((64, 1), (2048, 4), (32768, 64)):
+        p = _params(pk, num_seqs=64, num_q_heads=32, num_kv_heads=8, max_context_len=mx,
+                    max_blocks_per_seq=2048, variant=1)
+        assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, parts,
+                                                                             256, variant=1)
+    # the 70B-class batch of 32 (64/8 heads, contexts up to 32768): only the
+    # tensor-core kernel's partials, far below the CUDA-core kernel's
+    # 32 x 64 x 64 partitions x 130 floats
+    p = _params(pk, num_seqs=32, num_q_heads=64, num_kv_heads=8, max_context_len=32769,
+                max_blocks_per_seq=2049)
+    tc = lib.pa_decode_workspace_size(ctypes.byref(p))
+    assert tc == _expected_ws(32, 64, 128, 65, 256)
+    assert tc < 12 * 1024 * 1024
+    p.variant = 1
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(32, 64, 128, 65, 256,
+                                                                         variant=1)
+    # a shape the tensor-core kernel does not take runs on the CUDA-core one,
+    # whatever the variant says, and is sized for it
+    p = _params(pk, num_q_heads=16, num_kv_heads=16, max_context_len=2048,
+                max_blocks_per_seq=128)
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(2, 16, 128, 4, 256,
+                                                                         variant=1)
     # several new tokens per sequence
     for ql in (2, 3, 4):
         p = _params(pk, query_len=ql)

@@ -435,3 +435,21 @@ def test_fp8_step_host_with_several_new_tokens(pk):
     assert pk.pa_device_errors() == 0
     assert torch.equal(host_out.view(torch.int16), c["out"].cpu().view(torch.int16))
     assert torch.equal(kh, c["k8"]) and torch.equal(vh, c["v8"])
+
+
+def test_fp8_wait_budget_exit_reports_timeout_and_leaves_the_context_usable(pk):
+    """The 8-bit decode with a 1 us budget per barrier wait: the launch gives
+    up, reports PA_DEVERR_TIMEOUT and winds down; the next launch with the
+    default budget matches the oracle."""
+    import torch
+
+    rng = np.random.default_rng(41)
+    case = _fp8_case(pk, rng.integers(128, 2048, size=64), 32, 8, seed=43)
+    q, k8, v8, ks, vs, tables, lens = case
+    assert pk.pa_device_errors() == 0
+    for _ in range(2):
+        pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                     max_context_len=int(lens.max()), k_scale=ks, v_scale=vs, wait_timeout_us=1)
+        assert pk.pa_device_errors() & pk.DEVERR_TIMEOUT
+    _decode_and_check(pk, case)
+    assert pk.pa_device_errors() == 0

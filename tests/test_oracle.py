@@ -291,14 +291,71 @@ def _twin_mutant(kind):
     return run
 
 
+def _brute_force_pin(q, kc, vc, tables, lens):
+    """The brute-force pin: each sequence's K/V assembled by walking its table
+    with plain loops, then the pure-Python triple loop."""
+    qd, kd, vd = (oracle.bf16_to_f64(x) for x in (q, kc, vc))
+    B, Hq, D = qd.shape
+    Hkv, BS = kd.shape[1], kd.shape[2]
+    G = Hq // Hkv
+    out = np.empty((B, Hq, D))
+    for b in range(B):
+        for g in range(Hkv):
+            K, V = [], []
+            for t in range(int(lens[b])):
+                blk = int(tables[b][t // BS])
+                K.append(list(kd[blk, g, t % BS]))
+                V.append(list(vd[blk, g, t % BS]))
+            out[b, g * G:(g + 1) * G] = np.array(oracle.brute_force_decode(
+                [list(qd[b, h]) for h in range(g * G, g * G + G)], K, V, 1.0 / math.sqrt(D)))
+    return out
+
+
+def _identity_case(seed):
+    """An identity-table case for the library pin (torch SDPA in float64)."""
+    B, Hq, Hkv, D, BS, mb = 2, 4, 2, 8, 4, 4
+    lens = np.array([13, 7], dtype=np.int32)
+    tables = np.arange(B * mb, dtype=np.int32).reshape(B, mb)
+    q = _bf16((B, Hq, D), seed + 1)
+    kc = _bf16((B * mb, Hkv, BS, D), seed + 2)
+    vc = _bf16((B * mb, Hkv, BS, D), seed + 3)
+    return q, kc, vc, tables, lens
+
+
+def _sdpa_pin(q, kc, vc, tables, lens):
+    B, Hq, D = q.shape
+    Hkv, BS = kc.shape[1], kc.shape[2]
+    mb = tables.shape[1]
+    out = np.empty((B, Hq, D))
+    for b in range(B):
+        L = int(lens[b])
+        K = kc[b * mb:(b + 1) * mb].double().permute(1, 0, 2, 3).reshape(Hkv, mb * BS, D)[:, :L]
+        V = vc[b * mb:(b + 1) * mb].double().permute(1, 0, 2, 3).reshape(Hkv, mb * BS, D)[:, :L]
+        out[b] = _sdpa_unpaged(q[b].double(), K, V).numpy()
+    return out
+
+
+def _rejected_by_a_pin(impl):
+    """True when ``impl`` disagrees with the brute-force pin on a shuffled
+    table or with the library pin on an identity table."""
+    q, kc, vc, tables, lens = _random_case(16, Hq=4, Hkv=2, lens=(5, 9, 13))
+    bf = np.abs(impl(q, kc, vc, tables, lens) - _brute_force_pin(q, kc, vc, tables, lens)).max()
+    q, kc, vc, tables, lens = _identity_case(17)
+    lib = np.abs(impl(q, kc, vc, tables, lens) - _sdpa_pin(q, kc, vc, tables, lens)).max()
+    return bf > 1e-3 or lib > 1e-3
+
+
+def test_pins_accept_the_unmutated_twin():
+    """Control for the mutation test: the unmutated twin passes both pins."""
+    assert not _rejected_by_a_pin(oracle.paged_decode_numpy)
+    assert not _rejected_by_a_pin(_twin_mutant("none"))
+
+
 @pytest.mark.parametrize("kind", ["no_scale", "gqa_modulo", "offset", "mask_off_by_one"])
 def test_pins_reject_planted_mistakes(kind):
-    """Each planted mistake must be caught by a library or brute-force pin."""
-    q, kc, vc, tables, lens = _random_case(16, Hq=4, Hkv=2, lens=(5, 9, 13))
-    mutant = _twin_mutant(kind)(q, kc, vc, tables, lens)
-    ok = oracle.paged_decode(q, kc, vc, tables, lens)
-    # the brute-force pin distinguishes the mutant from the definition
-    assert np.abs(mutant - ok).max() > 1e-3
+    """Each planted mistake is caught by the brute-force or the library pin
+    themselves (not by a comparison with the oracle)."""
+    assert _rejected_by_a_pin(_twin_mutant(kind))
 
 
 # ---------------------------------------------------------------- cache writes

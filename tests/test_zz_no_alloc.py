@@ -69,6 +69,61 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row(pk):
     assert pk.pa_device_errors() == 0
 
 
+def _noalloc_call(pk, q, kc, vc, bt, cl, mx, variant=0):
+    """pa_decode_noalloc through the C ABI; returns the output tensor."""
+    import torch
+
+    out = torch.empty_like(q)
+    p = pk.make_decode_params(q, out, kc, vc, bt, cl, max_context_len=mx, variant=variant)
+    stream = torch.cuda.current_stream().cuda_stream or None
+    status = pk.load().pa_decode_noalloc(ctypes.byref(p), stream)
+    assert status == 0, pk.load().pa_last_error()
+    torch.cuda.synchronize()
+    return out
+
+
+def test_noalloc_cuda_core_variant_on_two_calls_in_a_row(pk):
+    """The CUDA-core kernel keeps its per-partition partials in the same
+    array when a sequence spans several 512-token partitions."""
+    cases = [_inputs(5, [1900, 37, 2049, 700, 1, 1536]),
+             _inputs(6, [513, 1200, 16, 2000, 1100])]
+    for q, kc, vc, bt, cl, mx, tables, lens in cases:
+        assert mx > 512  # several partitions
+        ref_out = pk.pa_decode(q, kc, vc, bt, cl, max_context_len=mx, variant=1)
+        out = _noalloc_call(pk, q, kc, vc, bt, cl, mx, variant=1)
+        harness.assert_close(harness.bf16_tensor_to_f64(out), harness.bf16_tensor_to_f64(ref_out))
+        want = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens.astype(np.int32))
+        harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+
+
+@pytest.mark.parametrize("recipe", ["llama70b_long_b8", "shared_prefix_cow_b512"])
+def test_noalloc_full_workloads_against_the_oracle(pk, recipe):
+    """Whole steps of the 70B-class batch of 8 (long contexts, split over
+    CTAs) and of the shared-prefix batch with its copy-on-write appends: the
+    block copies and the KV write, then the decode through pa_decode_noalloc,
+    whose tensor-core partials fit the fixed array."""
+    import torch
+
+    r = (workloads.llama70b_long(batch=8) if recipe == "llama70b_long_b8"
+         else workloads.shared_prefix())
+    case = harness.build_case(r)
+    kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    if len(case.cows):
+        pk.pa_copy_blocks(kc, vc, torch.from_numpy(case.cows).cuda())
+    pk.pa_reshape_and_cache(case.k_new, case.v_new, kc, vc, torch.from_numpy(case.slots).cuda())
+    bt = torch.from_numpy(case.tables).cuda()
+    cl = torch.from_numpy(case.lens).cuda()
+    mx = int(case.lens.max())
+    p = pk.make_decode_params(case.q, torch.empty_like(case.q), kc, vc, bt, cl, max_context_len=mx)
+    assert pk.pa_decode_workspace_size(p) <= 16 << 20
+    ref, _, _ = harness.run_step_oracle(case)
+    for _ in range(2):
+        out = _noalloc_call(pk, case.q, kc, vc, bt, cl, mx)
+        harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert pk.pa_device_errors() == 0
+
+
 def test_noalloc_rejects_shapes_beyond_its_fixed_scratch(pk):
     import torch
 

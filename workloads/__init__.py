@@ -139,6 +139,22 @@ def shared_prefix(seed: int = 5, batch: int = 512, prefix_tokens: int = 1024,
                   diverge_seqs=div, diverge_cut=cut, seed=seed)
 
 
+def subset(r: Recipe, seqs, seed: int = 99) -> Recipe:
+    """The sequences ``seqs`` of a recipe without sharing, laid on a pool of
+    their own (1.25x their need, a seeded permutation): the same lengths and
+    geometry as in the full workload at a fraction of its memory. Used for
+    bounded host-side samples."""
+    if r.diverge_seqs is not None:
+        raise ValueError("subset() takes recipes without a shared prefix")
+    lens = np.asarray(r.lens0, dtype=np.int64)[np.asarray(seqs, dtype=np.int64)]
+    need = int(_blocks_for(lens + r.append, r.block_size).sum())
+    nb = _pool_size(need)
+    rng = np.random.default_rng(seed)
+    return Recipe(r.name + f"_sample{len(lens)}", len(lens), r.num_q_heads, r.num_kv_heads,
+                  r.head_dim, r.block_size, lens, r.append, nb,
+                  rng.permutation(nb).astype(np.int32), seed=r.seed)
+
+
 def all_recipes() -> List[Recipe]:
     return [tiny(), llama8b_layer(), llama8b_high_concurrency(), llama70b_long(batch=8),
             llama70b_long(batch=32), shared_prefix()]
