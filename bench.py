@@ -400,20 +400,23 @@ def time_launches(plans, n: int) -> float:
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
+# columns of one other_workloads row (a compact table: the bench line must fit
+# the few thousand characters a log tail keeps)
+ROW_COLS = ["config", "seqs", "step_bytes", "step_us", "step_gbs", "step_frac", "launch_bytes",
+            "launch_us", "launch_frac"]
+
+
 def entry(step_bytes: int, step_ms: float, launch_bytes: int, launch_ms: float, peak: float,
-          **extra) -> dict:
-    """One secondary workload's figures: the plain step loop (``step_*``) and
-    the bracketed decode call (``launch_*``), as GB/s of algorithmic bytes and
-    fractions of the measured and the nominal HBM peak."""
+          config=None, seqs=None, hbm_fraction: bool = True) -> list:
+    """One secondary workload's row (ROW_COLS): the plain step loop
+    (``step_*``) and the bracketed decode call (``launch_*``), GB/s of
+    algorithmic bytes and fractions of the measured HBM peak (None where the
+    bytes are logical, not HBM: the shared prefix is read from L2)."""
     sg = step_bytes / (step_ms * 1e-3) / 1e9
     lg = launch_bytes / (launch_ms * 1e-3) / 1e9
-    d = dict(extra)
-    d.update({"step_bytes": int(step_bytes), "step_us": round(step_ms * 1e3, 2),
-              "step_gbs": round(sg, 1), "step_frac": round(sg / peak, 4),
-              "step_frac_nominal": round(sg / NOMINAL_HBM_GBS, 4),
-              "launch_bytes": int(launch_bytes), "launch_us": round(launch_ms * 1e3, 2),
-              "launch_gbs": round(lg, 1), "launch_frac": round(lg / peak, 4)})
-    return d
+    return [config, seqs, int(step_bytes), round(step_ms * 1e3, 2), round(sg, 1),
+            round(sg / peak, 4) if hbm_fraction else None, int(launch_bytes),
+            round(launch_ms * 1e3, 2), round(lg / peak, 4) if hbm_fraction else None]
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -527,16 +530,19 @@ def run_ours(args, rank: int, world: int) -> dict:
     }
     del plans, keep, W
     torch.cuda.empty_cache()
+    other = None
     if not args.no_workloads:
-        other = measure_bf16_workloads(pk, device, variant=args.variant,
-                                       overlap=not args.no_overlap, fused=fused,
-                                       skip=(name,))
+        other = {"cols": ROW_COLS}
+        other.update(measure_bf16_workloads(pk, device, variant=args.variant,
+                                            overlap=not args.no_overlap, fused=fused,
+                                            skip=(name,)))
         if args.variant == 0:
             other.update(measure_fp8_workloads(pk, device))
             other.update(measure_multi_workloads(pk, device))
-        res["other_workloads"] = other
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(name, budget_s=args.cpu_baseline_s)
+    if other is not None:
+        res["other_workloads"] = other  # last: the end of the line survives a log's tail
     return res
 
 
@@ -572,19 +578,15 @@ def measure_bf16_workloads(pk, device, variant: int = 0, overlap: bool = True, f
             plans[i % len(plans)].run()
         step_ms = time_loop(plans, steps, stream)
         launch_ms = time_launches(plans, launches)
-        e = entry(step_b, step_ms, dec_b + (app_b if fused else 0), launch_ms, peak,
-                  config=CONFIG_OF.get(name), B=r.num_seqs, cow_pairs=int(len(W["cows"])))
-        if name == "shared_prefix_cow_b512":
-            for k in ("step_frac", "step_frac_nominal", "launch_frac"):
-                e[k] = None
-            e["bytes_note"] = "logical K/V bytes; the 64 shared blocks hit L2"
+        shared = name == "shared_prefix_cow_b512"
+        out[name] = entry(step_b, step_ms, dec_b + (app_b if fused else 0), launch_ms, peak,
+                          config=CONFIG_OF.get(name), seqs=r.num_seqs, hbm_fraction=not shared)
+        if shared:
+            # logical K/V bytes (the 64 shared blocks hit L2); the true DRAM
+            # fraction from the launch's ncu DRAM bytes, while that summary is current
             dram = profiled_traffic(f"pa_decode_tc_{PROFILE_OF[name]}.md") if fused else None
-            e["dram_bytes_ncu"] = dram
-            e["dram_frac"] = (round(dram / (launch_ms * 1e-3) / 1e9 / peak, 4)
-                              if dram else None)
-        if name == "tiny_b4":
-            e["note"] = "launch-latency bound (18 KiB): parity only, no bandwidth bar"
-        out[name] = e
+            out["shared_prefix_dram_frac"] = (round(dram / (launch_ms * 1e-3) / 1e9 / peak, 4)
+                                              if dram else None)
         del plans, keep, W
         torch.cuda.empty_cache()
     return out
@@ -653,8 +655,7 @@ def measure_fp8_workloads(pk, device, steps: int = 200, launches: int = 100, war
             plans[i % len(plans)].run()
         step_ms = time_loop(plans, steps, stream)
         launch_ms = time_launches(plans, launches)
-        out[name] = entry(step_b, step_ms, dec_b + app_b, launch_ms, peak, B=r.num_seqs,
-                          kv="e4m3", block_size=r.block_size)
+        out[name] = entry(step_b, step_ms, dec_b + app_b, launch_ms, peak, seqs=r.num_seqs)
         del plans, keep, W
         torch.cuda.empty_cache()
     return out
@@ -710,7 +711,7 @@ def measure_multi_workloads(pk, device, steps: int = 200, launches: int = 100, w
             plans[i % len(plans)].run()
         step_ms = time_loop(plans, steps, stream)
         launch_ms = time_launches(plans, launches)
-        out[name] = entry(step_b, step_ms, step_b, launch_ms, peak, B=B, query_len=Q)
+        out[name] = entry(step_b, step_ms, step_b, launch_ms, peak, seqs=B)
         del plans, keep, W
         torch.cuda.empty_cache()
     return out
@@ -831,11 +832,10 @@ def cpu_baseline(headline: str, budget_s: float = 2.5) -> dict:
         sub = workloads.subset(r, list(range(k)))
         tables, lens, q, kc, vc = _oracle_sample_inputs(sub)
         inputs = (tables, lens, oracle.bf16_bits(q), oracle.bf16_bits(kc), oracle.bf16_bits(vc))
-        res = {"config": CONFIG_OF.get(name), "sample_seqs": k}
+        res = [CONFIG_OF.get(name), k]
         for threads in (nproc, 1):
             gbs, n_units, dt = time_oracle(sub, inputs, threads, budget_s)
-            res[f"gbs_{threads}t"] = round(gbs, 4)
-            res[f"units_{threads}t"] = n_units
+            res.append(round(gbs, 4))
             if name == headline and threads == nproc:
                 head = (gbs, n_units, dt, k)
         per[name] = res
@@ -847,6 +847,7 @@ def cpu_baseline(headline: str, budget_s: float = 2.5) -> dict:
             "sample": f"float64 C oracle (OpenMP over (sequence, query head) units) on the first "
                       f"{k} sequences of {headline} (same lengths and geometry, own pool): "
                       f"{n_units} units in {dt:.1f} s on {nproc} threads",
+            "per_config_cols": ["config", "sample_seqs", f"gbs_{nproc}_threads", "gbs_1_thread"],
             "per_config": per}
 
 
@@ -913,7 +914,7 @@ def run_case(args) -> int:
     if not res:
         print(json.dumps({"case": args.case, "error": "no such workload"}))
         return 2
-    print(json.dumps({"case": args.case, **res[args.case]}))
+    print(json.dumps({"case": args.case, **dict(zip(ROW_COLS, res[args.case]))}))
     return 0
 
 
