@@ -674,6 +674,11 @@ def measure_multi_workloads(pk, device, steps: int = 200, launches: int = 100, w
     out = {}
     cases = [("llama8b_layer_b64_q2", workloads.llama8b_layer(), 2),
              ("llama8b_layer_b64_q4", workloads.llama8b_layer(), 4),
+             # more tokens than one column group holds: groups of 4 (G 4) or 2 (G 8)
+             ("llama8b_layer_b64_q8", workloads.llama8b_layer(), 8),
+             ("llama8b_layer_b64_q16", workloads.llama8b_layer(), 16),
+             ("llama8b_layer_b64_q64", workloads.llama8b_layer(), 64),
+             ("llama70b_long_b8_q8", workloads.llama70b_long(batch=8), 8),
              ("llama8b_high_concurrency_b256_q4", workloads.llama8b_high_concurrency(), 4),
              ("llama70b_long_b8_q2", workloads.llama70b_long(batch=8), 2)]
     peak = measured_peaks()["hbm_gbs"]

@@ -73,8 +73,7 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
   if (query_len_of(p) > 1 && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
     return set_error(PA_ERR_UNSUPPORTED,
                      "pa_decode: query_len > 1 runs on the tensor-core kernel with num_kv_heads "
-                     "1/2/4/8, G * query_len (rounded up to a power of two) <= 16 and "
-                     "num_kv_heads * that <= 128 (64 for the 8-bit cache)");
+                     "1/2/4/8 and num_seqs * (query_len split into column groups) <= 16384");
   if (p->kv_dtype == PA_KV_FP8_E4M3) {
     if (p->head_dim != 128 || p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p))
       return set_error(PA_ERR_UNSUPPORTED,
@@ -142,21 +141,23 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
   // tensor-core kernel: stream-K plan, then one partial per (sequence, CTA)
   // segment and query column (= query head for one token per sequence). With
   // no device to query, the grid is taken as 256 CTAs (an upper bound).
-  const size_t segs = size_t(p->num_seqs) + size_t(grid > 0 ? grid : 256);
+  // (one virtual sequence per sequence and column group of its new tokens)
+  const size_t V = size_t(tc_virtual_seqs(p));
+  const size_t segs = V + size_t(grid > 0 ? grid : 256);
   const size_t rows = segs * size_t(tc_cols(p));
   w.tc_plan = H;
-  w.tc_m = w.tc_plan + round_up((size_t(p->num_seqs) + 2) * sizeof(int), 256);
+  w.tc_m = w.tc_plan + round_up((V + 2) * sizeof(int), 256);
   w.tc_l = w.tc_m + round_up(rows * sizeof(float), 256);
   w.tc_acc = w.tc_l + round_up(rows * sizeof(float), 256);
   size_t tc_end = w.tc_acc + round_up(rows * p->head_dim * sizeof(float), 256);
   const size_t n_pad = size_t(tc_n_pad(tc_cols(p)));
   if (p->kv_dtype == PA_KV_FP8_E4M3) {  // split queries [B][2N][D] bytes and [B][N] floats
     w.tc_q8 = tc_end;
-    w.tc_qa = w.tc_q8 + round_up(size_t(p->num_seqs) * 2 * n_pad * p->head_dim, 256);
-    tc_end = w.tc_qa + round_up(size_t(p->num_seqs) * n_pad * sizeof(float), 256);
-  } else if (query_len_of(p) > 1) {  // queries in column order, bf16 [B][N][D]
+    w.tc_qa = w.tc_q8 + round_up(V * 2 * n_pad * p->head_dim, 256);
+    tc_end = w.tc_qa + round_up(V * n_pad * sizeof(float), 256);
+  } else if (query_len_of(p) > 1) {  // queries in column order, bf16 [V][N][D]
     w.tc_qp = tc_end;
-    tc_end = w.tc_qp + round_up(size_t(p->num_seqs) * n_pad * p->head_dim * 2, 256);
+    tc_end = w.tc_qp + round_up(V * n_pad * p->head_dim * 2, 256);
   }
   w.total = tc_end;
   return w;

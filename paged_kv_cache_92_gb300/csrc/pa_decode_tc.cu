@@ -9,15 +9,16 @@ namespace pa {
 bool tc_supports(const pa_decode_params* p) {
   const int H = p->num_kv_heads;
   const int G = p->num_q_heads / H;
-  if (!(H == 1 || H == 2 || H == 4 || H == 8) || !(G == 1 || G == 2 || G == 4 || G == 8) ||
-      p->num_seqs > kTcMaxSeqs || query_len_of(p) > kMaxGE)
+  if (!(H == 1 || H == 2 || H == 4 || H == 8) || !(G == 1 || G == 2 || G == 4 || G == 8))
     return false;
   const bool fp8 = p->kv_dtype == PA_KV_FP8_E4M3;
-  if (p->block_size != 16) {  // block sizes 8 and 32: head_dim 128
-    if (p->head_dim != 128 || (p->block_size == 8 && (fp8 || tc_group_cols(p) > 8)))
-      return false;
+  if (p->block_size != 16) {  // block sizes 8 and 32: head_dim 128; no 8-bit cache at 8
+    if (p->head_dim != 128 || (p->block_size == 8 && fp8)) return false;
   }
-  return tc_group_cols(p) <= kMaxGE && tc_cols(p) <= (fp8 ? 64 : 128);
+  // column groups within the column budget (always, for these shapes), and
+  // every virtual sequence (sequence x column group) in the kernel's plan
+  return tc_max_group_tokens(p) >= 1 && tc_group_cols(p) <= kMaxGE &&
+         tc_cols(p) <= (fp8 ? 64 : 128) && tc_virtual_seqs(p) <= kTcMaxSeqs;
 }
 
 int tc_grid() {

@@ -138,14 +138,15 @@ constexpr int kMaxGE = 16;
 enum : int { F_FIRST = 1, F_LAST = 2, F_WHOLE = 4, F_END = 8 };
 
 struct __align__(16) ChunkMeta {
-  int b;      // sequence
-  int seg;    // partial slot when the sequence spans several CTAs
+  int b;      // virtual sequence (its partial slot is b + blockIdx.x when it spans several CTAs)
+  int orow0;  // its first output row: (sequence * query_len + first token of its group) * Hq
   int flags;
   int tok0;   // first token of the chunk
-  int L;      // context length (clamped)
+  int L;      // keys the virtual sequence streams (context length, clamped, less the
+              // new tokens after its group's last)
   int nblk;   // blocks of the chunk holding cache data (the others read as zeros)
   int qslot;
-  int pad;
+  int qlen;   // query tokens of its group
 };
 
 // F8: the 8-bit (E4M3) cache. K rows are D bytes (one 128-byte atom at
@@ -248,14 +249,18 @@ struct TcParams {
   // the caches as plain pointers: L2 prefetch of the first blocks
   const unsigned char* k_base;
   const unsigned char* v_base;
-  int max_blocks_per_seq, num_seqs, num_kv_heads, num_q_heads, num_blocks, cap, oob_row;
+  int max_blocks_per_seq, num_kv_heads, num_q_heads, num_blocks, cap, oob_row;
+  // virtual sequences: num_seqs = sequences x n_groups; virtual sequence v is
+  // column group v % n_groups (q_len tokens of the q_total new ones) of
+  // sequence v / n_groups
+  int num_seqs, n_groups, q_total;
   int oob_row_v;   // 8-bit cache: first V^T tile past the tensor map
   // (oob_row: the first K/V row past the tensor map -- or, for block size 32,
   // the first (block, head) tile past it)
   int q_rows;      // rows of one sequence's queries in the Q tensor map
   // Column layout: KV head g owns columns [g*GE, (g+1)*GE); column g*GE + r is
-  // query token r >> g_log2 of query head g*G + (r & (G-1)), unused when that
-  // token index is >= q_len. num_cols = num_kv_heads * GE.
+  // query token r >> g_log2 (of the column group) of query head g*G + (r & (G-1)),
+  // unused when that token index is >= q_len. num_cols = num_kv_heads * GE.
   int num_cols, q_len, g_log2;
   float scale_log2;
   uint64_t wait_ns;  // budget of one barrier wait (2 s unless the caller set another)
@@ -263,12 +268,24 @@ struct TcParams {
 
 // Context length of sequence b as the kernel uses it: clamped to the table
 // capacity, and 0 (an empty sequence) when it cannot hold the new tokens.
-__device__ __forceinline__ int seq_len(const TcParams& P, int b) {
+__device__ __forceinline__ int real_len(const TcParams& P, int b) {
   const int L = min(P.context_lens[b], P.cap);
-  return L >= P.q_len ? L : 0;
+  return L >= P.q_total ? L : 0;
+}
+// Query tokens of virtual sequence v's column group.
+__device__ __forceinline__ int group_tokens(const TcParams& P, int v) {
+  const int g = v % P.n_groups;
+  return min(P.q_len, P.q_total - g * P.q_len);
+}
+// Keys virtual sequence v streams: those its group's last token sees.
+__device__ __forceinline__ int seq_len(const TcParams& P, int v) {
+  const int L = real_len(P, v / P.n_groups);
+  if (L == 0) return 0;
+  const int g = v % P.n_groups;
+  return L - P.q_total + g * P.q_len + group_tokens(P, v);
 }
 
-// Output row of column n within its sequence's [q_len][Hq] rows, or -1 if the
+// Output row of column n within its group's [q_len][Hq] rows, or -1 if the
 // column is unused (with one token per sequence: n itself, for n < Hq).
 __device__ __forceinline__ int column_row(const TcParams& P, int n, int ge) {
   const int g = n / ge, r = n - g * ge;
@@ -579,10 +596,10 @@ struct Softmax {
       const int t = m.tok0 + u * GB + key;
       const bool row_in = u < m.nblk;           // the row holds cache data
       const bool valid = row_in && t < m.L;     // a token of the sequence
-      // Causal limit: column j holds query token i = j >> g_log2, the
-      // (q_len - i)-th last of the sequence, which sees the keys
-      // t < L - q_len + 1 + i; columns with i >= q_len are unused.
-      const int t_rel = t - (m.L - P.q_len + 1);
+      // Causal limit: column j holds query token i = j >> g_log2 of the
+      // group, whose last token (qlen - 1) sees the keys t < L; token i sees
+      // t < L - qlen + 1 + i; columns with i >= qlen are unused.
+      const int t_rel = t - (m.L - m.qlen + 1);
       float x[GE];
       bool need = false;
 #pragma unroll
@@ -597,7 +614,7 @@ struct Softmax {
         if constexpr (F8)  // the head's K scale and the query term's 1/alpha
           f *= kvscale[h] * qalpha[m.qslot * 64 + h * GE + j];
         const int i = j >> P.g_log2;
-        x[j] = row_in && t_rel < i && i < P.q_len ? sj * f : -INFINITY;
+        x[j] = row_in && t_rel < i && i < m.qlen ? sj * f : -INFINITY;
         need |= x[j] > m_ref[j] + kRescaleLog2;
       }
 
@@ -776,9 +793,10 @@ struct Softmax {
         float o[CW];
         load_o(0, o);
         dev::named_barrier(1, kCons);  // l_s, m_s written
-        __nv_bfloat16* o_row =
-            P.out + size_t(m.b) * P.q_len * P.num_q_heads * D + (ctid < D ? ctid : 0);
-        float* a_row = P.part_acc + size_t(m.seg) * NC * D + (ctid < D ? ctid : 0);
+        __nv_bfloat16* o_row = P.out + size_t(m.orow0) * D + (ctid < D ? ctid : 0);
+        const int seg = m.b + int(blockIdx.x);  // partial slot
+        const int row_end = m.qlen * P.num_q_heads;  // rows of the group's tokens
+        float* a_row = P.part_acc + size_t(seg) * NC * D + (ctid < D ? ctid : 0);
 #pragma unroll
         for (int cg = 0; cg < N; cg += CW) {
           if (cg > 0) load_o(cg, o);
@@ -787,7 +805,8 @@ struct Softmax {
 #pragma unroll
               for (int i = 0; i < CW; ++i) {
                 const int r = colrow[cg + i];
-                if (r >= 0) o_row[size_t(r) * D] = __float2bfloat16_rn(o[i] * __frcp_rn(l_s[cg + i]));
+                if (r >= 0 && r < row_end)
+                  o_row[size_t(r) * D] = __float2bfloat16_rn(o[i] * __frcp_rn(l_s[cg + i]));
               }
             } else {
 #pragma unroll
@@ -797,8 +816,8 @@ struct Softmax {
           }
         }
         if (!(m.flags & F_WHOLE) && ctid < NC) {
-          P.part_m[size_t(m.seg) * NC + ctid] = m_s[ctid];
-          P.part_l[size_t(m.seg) * NC + ctid] = l_s[ctid];
+          P.part_m[size_t(seg) * NC + ctid] = m_s[ctid];
+          P.part_l[size_t(seg) * NC + ctid] = l_s[ctid];
         }
         dev::tc_fence_before();
 #pragma unroll
@@ -888,15 +907,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // get fewer units. pre = exclusive prefix of the costs; CTA c takes the
   // cost range [c R, (c+1) R).
   const int SC = start_chunks(F8, P.q_len) * (Units<BS>::GROUPS / H);  // a sequence start's cost
+  // (P.q_len: the tokens of a column group)
   int* pre = reinterpret_cast<int*>(ring);
   {
     const int seg = (B + NTHREADS - 1) / NTHREADS;
     const int b0 = min(B, tid * seg), b1 = min(B, b0 + seg);
     int local = 0;
     for (int b = b0; b < b1; ++b) {
-      const int L0 = P.context_lens[b];
-      if (blockIdx.x == 0 && (L0 > P.cap || (L0 > 0 && L0 < P.q_len)))
-        atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
+      if (blockIdx.x == 0 && b % P.n_groups == 0) {
+        const int L0 = P.context_lens[b / P.n_groups];
+        if (L0 > P.cap || (L0 > 0 && L0 < P.q_total)) atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
+      }
       const int n = (seq_len(P, b) + UT - 1) / UT;
       local += n > 0 ? n + SC : 0;
     }
@@ -946,7 +967,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == kProducerWarp && u0 < u1) {
     const int j = (off_start + lane) / VS;  // the block of unit off_start + lane
     win0 = j < P.max_blocks_per_seq
-               ? P.block_tables[size_t(b_start) * P.max_blocks_per_seq + j] : -1;
+               ? P.block_tables[size_t(b_start / P.n_groups) * P.max_blocks_per_seq + j] : -1;
     len0 = seq_len(P, b_start);
     // Pull the first blocks into L2 now, so that their copies after the
     // wait find them there: the kernel runs as a dependent of the previous
@@ -994,15 +1015,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int chunk_seq = 0, seg_seq = 0;
     bool ok = true;
     // block-table window: lane j holds the entry of the block of unit first_unit + j
-    auto load_window = [&](int b, int first_unit) {
+    auto load_window = [&](int v, int first_unit) {  // (v: virtual sequence)
       const int j = (first_unit + lane) / VS;
-      return (b < B && j < P.max_blocks_per_seq)
-                 ? P.block_tables[size_t(b) * P.max_blocks_per_seq + j] : -1;
+      return (v < B && j < P.max_blocks_per_seq)
+                 ? P.block_tables[size_t(v / P.n_groups) * P.max_blocks_per_seq + j] : -1;
     };
-    // Fused KV append: sequence b's new tokens (its last q_len, tokens
-    // L-q_len .. L-1; row b*q_len + i of k_new/v_new/slot_mapping) are
+    // Fused KV append: sequence b's new tokens (its last q_total, tokens
+    // L-q_total .. L-1; row b*q_total + i of k_new/v_new/slot_mapping) are
     // written just before the copy of the chunk that reads their unit is
-    // issued (so the chunks before it stream meanwhile). A token's slot, table
+    // issued (so the chunks before it stream meanwhile). With several column
+    // groups every group writes the new tokens its own stream reads (the same
+    // bytes; each write precedes that group's own copy). A token's slot, table
     // entry and K/V rows are loaded together (one memory round trip) -- for
     // one new token per sequence already at the start of the piece -- then
     // checked and stored; a proxy fence makes the generic-proxy stores
@@ -1016,8 +1039,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint4 k[kRowMax], v[kRowMax];
     };
     const int n_row = H * CPR;
-    auto load_row = [&](int b, int pos, int i, NewRow& r) {
-      const size_t tok = size_t(b) * P.q_len + i;
+    auto load_row = [&](int b, int pos, int i, NewRow& r) {  // (b: a sequence)
+      const size_t tok = size_t(b) * P.q_total + i;
       r.pos = pos;
       r.slot = P.slot_mapping[tok];
       r.e = P.block_tables[size_t(b) * P.max_blocks_per_seq + pos / BS];
@@ -1054,10 +1077,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     NewRow pre_row;          // one new token per sequence: loaded at the piece start
     bool have_pre = false;
-    // the new tokens that fall in units [unit0, unit1) of sequence b
-    auto append_tokens = [&](int b, int L, int unit0, int unit1) {
-      for (int i = 0; i < P.q_len; ++i) {
-        const int pos = L - P.q_len + i;
+    // the new tokens of sequence b (context length L) that fall in units
+    // [unit0, unit1) of a stream of its first L_stream tokens
+    auto append_tokens = [&](int b, int L, int L_stream, int unit0, int unit1) {
+      for (int i = 0; i < P.q_total; ++i) {
+        const int pos = L - P.q_total + i;
+        if (pos >= L_stream) break;
         if (pos < unit0 * UT || pos >= unit1 * UT) continue;
         if (have_pre && pre_row.pos == pos) {
           store_row(pre_row);
@@ -1091,10 +1116,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (uend <= off) break;                    // nothing of b (or after it) in range
       const int seg_nb = uend - off;
       const bool whole = off == 0 && seg_nb == nb;
-      const int new_unit0 = (L_cur - P.q_len) / UT;  // first unit holding a new token
+      const int b_real = b / P.n_groups;
+      const int L_real = real_len(P, b_real);
+      const int new_unit0 = (L_real - P.q_total) / UT;  // first unit holding a new token
       if constexpr (!F8) {  // (the 8-bit cache is written by the query-split launch)
-        if (P.k_new != nullptr && P.q_len == 1 && off + seg_nb > new_unit0) {
-          load_row(b, L_cur - 1, 0, pre_row);  // consumed at the chunk of its unit
+        if (P.k_new != nullptr && P.q_total == 1 && off + seg_nb > new_unit0) {
+          load_row(b_real, L_cur - 1, 0, pre_row);  // consumed at the chunk of its unit
           have_pre = true;
         }
       }
@@ -1114,7 +1141,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if constexpr (!F8) {  // this chunk holds a unit of the new tokens
           const int nu = min(U, seg_nb - jb);
           if (P.k_new != nullptr && off + jb + nu > new_unit0)
-            append_tokens(b, L_cur, off + jb, off + jb + nu);
+            append_tokens(b_real, L_real, L_cur, off + jb, off + jb + nu);
         }
         const int slot = chunk_seq % C::ST;
         const uint32_t ph = uint32_t(chunk_seq / C::ST) & 1u;
@@ -1123,13 +1150,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (ok) {
             ChunkMeta m;
             m.b = b;
-            m.seg = b + int(blockIdx.x);
+            m.orow0 = (b_real * P.q_total + (b - b_real * P.n_groups) * P.q_len) * P.num_q_heads;
+            m.qlen = group_tokens(P, b);
             m.flags = (c == 0 ? F_FIRST : 0) | (c == nch - 1 ? F_LAST : 0) | (whole ? F_WHOLE : 0);
             m.tok0 = (off + jb) * UT;
             m.L = L_cur;
             m.nblk = min(U, seg_nb - jb);
             m.qslot = qs;
-            m.pad = 0;
             meta[slot] = m;
             dev::mbar_arrive_expect_tx(&full[slot], C::CHUNK_TX + (c == 0 ? C::Q_TX : 0u));
           }
@@ -1309,7 +1336,8 @@ struct Row {
 };
 
 struct MergeCols {
-  int num_q_heads, num_cols, group_cols, g_log2, q_len;
+  int num_q_heads, num_cols, group_cols, g_log2;
+  int q_group, q_total, n_groups;  // tokens per column group, new tokens, groups
   int seg_cost;  // the decode plan's cost of a sequence start (units)
 };
 
@@ -1326,14 +1354,15 @@ __global__ void __launch_bounds__(128)
   dev::griddep_wait();  // launched as a programmatic dependent of the decode
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 4 + warp;  // column (the decode kernel's layout)
-  const int b = blockIdx.y;
+  const int b = blockIdx.y;             // virtual sequence
   if (n >= mc.num_cols) return;
   const int g = n / mc.group_cols, r = n - g * mc.group_cols;
-  const int qi = r >> mc.g_log2;  // query token of the column
-  if (qi >= mc.q_len) return;     // unused column
+  const int qi = r >> mc.g_log2;  // query token of the column within its group
+  const int seq = b / mc.n_groups, tok = (b - seq * mc.n_groups) * mc.q_group + qi;
+  if (qi >= mc.q_group || tok >= mc.q_total) return;  // unused column
   const int R = ws_plan[0];
   const int pre0 = ws_plan[1 + b], pre1 = ws_plan[2 + b];
-  const size_t orow = (size_t(b) * mc.q_len + qi) * mc.num_q_heads + (g << mc.g_log2) +
+  const size_t orow = (size_t(seq) * mc.q_total + tok) * mc.num_q_heads + (g << mc.g_log2) +
                       (r & ((1 << mc.g_log2) - 1));
   __nv_bfloat16* o = out + orow * D + lane * VPL;
   if (pre1 <= pre0) {  // empty sequence
@@ -1525,7 +1554,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
     }
     if (!r) r = make_map_vt(&tv, p->v_cache, tiles, D, uint32_t(H), BS);
     if (!r)
-      r = make_map_u8(&tq, Lc.q8, uint64_t(p->num_seqs) * 2 * N, D, D, uint32_t(2 * N),
+      r = make_map_u8(&tq, Lc.q8, uint64_t(qm.num_seqs) * 2 * N, D, D, uint32_t(2 * N),
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (!r) r = launch_quantize_q(p->q, Lc.q8, Lc.q_inv_alpha, qm, p, Lc.append, stream);
   } else {
@@ -1541,7 +1570,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
       // box of N rows may run into the next sequence's rows, never used
       if (!r) r = make_map(&tq, p->q, uint64_t(p->num_seqs) * p->num_q_heads, D, uint32_t(N));
     } else {
-      if (!r) r = make_map(&tq, Lc.qp, uint64_t(p->num_seqs) * N, D, uint32_t(N));
+      if (!r) r = make_map(&tq, Lc.qp, uint64_t(qm.num_seqs) * N, D, uint32_t(N));
       if (!r) r = launch_permute_q(p->q, Lc.qp, qm, stream);
     }
   }
@@ -1569,10 +1598,12 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   P.oob_row_v = int(tiles);  // first V^T tile past the cache
   P.q_rows = F8 ? 2 * N : (qm.query_len == 1 ? p->num_q_heads : N);
   P.num_cols = qm.num_cols;
-  P.q_len = qm.query_len;
+  P.q_len = qm.q_group;
+  P.q_total = qm.query_len;
+  P.n_groups = qm.n_groups;
   P.g_log2 = qm.g_log2;
   P.max_blocks_per_seq = p->max_blocks_per_seq;
-  P.num_seqs = p->num_seqs;
+  P.num_seqs = qm.num_seqs;  // virtual sequences
   P.num_kv_heads = H;
   P.num_q_heads = p->num_q_heads;
   P.num_blocks = p->num_blocks;
@@ -1596,7 +1627,7 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   if (e != cudaSuccess) return int(e);
   // the merge launches while the decode drains and waits for it on the device
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3((qm.num_cols + 3) / 4, p->num_seqs);
+  mcfg.gridDim = dim3((qm.num_cols + 3) / 4, qm.num_seqs);
   mcfg.blockDim = dim3(128);
   mcfg.stream = stream;
   mcfg.attrs = attr;
@@ -1607,8 +1638,10 @@ int launch_tc_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   mc.num_cols = qm.num_cols;
   mc.group_cols = qm.group_cols;
   mc.g_log2 = qm.g_log2;
-  mc.q_len = qm.query_len;
-  mc.seg_cost = start_chunks(F8, qm.query_len) * (Units<BS>::GROUPS / H);
+  mc.q_group = qm.q_group;
+  mc.q_total = qm.query_len;
+  mc.n_groups = qm.n_groups;
+  mc.seg_cost = start_chunks(F8, qm.q_group) * (Units<BS>::GROUPS / H);
   e = cudaLaunchKernelEx(&mcfg, merge_segments_kernel<D>, P.out,
                          static_cast<const float*>(P.part_m), static_cast<const float*>(P.part_l),
                          static_cast<const float*>(P.part_acc),

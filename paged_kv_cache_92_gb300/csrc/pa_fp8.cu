@@ -252,7 +252,7 @@ int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap&
     a.q_len = m.query_len;
     a.bs_log2 = log2_of(p->block_size);
     a.num_slots = int64_t(p->num_blocks) * p->block_size;
-    a.num_chunks = int64_t(m.num_seqs) * m.query_len * p->num_kv_heads * (p->head_dim / 8);
+    a.num_chunks = int64_t(m.num_real_seqs) * m.query_len * p->num_kv_heads * (p->head_dim / 8);
   }
   const int64_t q_blocks = (int64_t(m.num_seqs) * m.n_pad + 3) / 4;
   const int64_t w_blocks = (a.num_chunks + 127) / 128;

@@ -46,15 +46,43 @@ inline int query_len_of(const pa_decode_params* p) {
 // Tensor-core column layout. The kernel's query rows ("columns": the N side
 // of its MMAs) are grouped by KV head: head g owns columns [g*GE, (g+1)*GE),
 // column g*GE + i*G + j being query token i of query head g*G + j. GE is G
-// times query_len rounded up to a power of two; columns whose token index is
-// >= query_len are unused. With one token per sequence GE = G and the column
-// of query head h is h itself.
-inline int tc_group_cols(const pa_decode_params* p) {
+// times the tokens of a column group rounded up to a power of two; columns
+// whose token index is past the group's tokens are unused. With one token per
+// sequence GE = G and the column of query head h is h itself.
+//
+// A column group holds at most tc_max_group_tokens() query tokens: GE <= 16
+// (8 at block size 8) and num_kv_heads * GE <= 128 (64 for the 8-bit cache).
+// A sequence with more new tokens is split into n_groups groups of that many
+// (the last one possibly shorter), each decoded as a virtual sequence of its
+// own that streams the keys its last token can see.
+inline int pow2_ceil(int x) {
   int q = 1;
-  while (q < query_len_of(p)) q <<= 1;
-  return (p->num_q_heads / p->num_kv_heads) * q;
+  while (q < x) q <<= 1;
+  return q;
+}
+inline int tc_max_group_tokens(const pa_decode_params* p) {
+  const int g = p->num_q_heads / p->num_kv_heads;
+  int cols = p->block_size == 8 ? 8 : 16;  // columns per KV head
+  const int total = p->kv_dtype == PA_KV_FP8_E4M3 ? 64 : 128;
+  if (cols * p->num_kv_heads > total) cols = total / p->num_kv_heads;
+  return cols >= g ? cols / g : 0;
+}
+inline int tc_q_group(const pa_decode_params* p) {
+  const int q = query_len_of(p), cap = tc_max_group_tokens(p);
+  return q <= cap ? q : cap;
+}
+inline int tc_n_groups(const pa_decode_params* p) {
+  const int qg = tc_q_group(p);
+  return qg > 0 ? (query_len_of(p) + qg - 1) / qg : 0;
+}
+inline int tc_group_cols(const pa_decode_params* p) {
+  return (p->num_q_heads / p->num_kv_heads) * pow2_ceil(tc_q_group(p));
 }
 inline int tc_cols(const pa_decode_params* p) { return p->num_kv_heads * tc_group_cols(p); }
+// Virtual sequences of the tensor-core decode: num_seqs * n_groups.
+inline int64_t tc_virtual_seqs(const pa_decode_params* p) {
+  return int64_t(p->num_seqs) * tc_n_groups(p);
+}
 
 // Columns padded to the tensor-core N (16, 32, 64 or 128).
 inline int tc_n_pad(int cols) {
@@ -67,15 +95,22 @@ inline int log2_of(int x) {
   return r;
 }
 
-// Where the query rows of one sequence sit in the column layout above.
+// Where the query rows of one virtual sequence sit in the column layout
+// above. Virtual sequence v is column group v % n_groups (tokens
+// [g * q_group, g * q_group + q_group) of query_len) of sequence v / n_groups.
 struct QueryMap {
-  int num_seqs, num_q_heads, query_len, g_log2, group_cols, num_cols, n_pad, head_dim;
+  int num_seqs;       // virtual sequences (sequences x n_groups)
+  int num_real_seqs;  // sequences
+  int num_q_heads, query_len, q_group, n_groups, g_log2, group_cols, num_cols, n_pad, head_dim;
 };
 inline QueryMap query_map(const pa_decode_params* p) {
   QueryMap m;
-  m.num_seqs = p->num_seqs;
+  m.num_real_seqs = p->num_seqs;
+  m.n_groups = tc_n_groups(p);
+  m.num_seqs = int(tc_virtual_seqs(p));
   m.num_q_heads = p->num_q_heads;
   m.query_len = query_len_of(p);
+  m.q_group = tc_q_group(p);
   m.g_log2 = log2_of(p->num_q_heads / p->num_kv_heads);
   m.group_cols = tc_group_cols(p);
   m.num_cols = tc_cols(p);
@@ -84,12 +119,14 @@ inline QueryMap query_map(const pa_decode_params* p) {
   return m;
 }
 #ifdef __CUDACC__
-// Row of q ([B][query_len][Hq][D]) that column n of sequence b holds, or -1.
-__device__ __forceinline__ int64_t query_source_row(const QueryMap& m, int b, int n) {
+// Row of q ([B][query_len][Hq][D]) that column n of virtual sequence v holds, or -1.
+__device__ __forceinline__ int64_t query_source_row(const QueryMap& m, int v, int n) {
   if (n >= m.num_cols) return -1;
+  const int b = v / m.n_groups, grp = v - b * m.n_groups;
   const int g = n / m.group_cols, r = n - g * m.group_cols;
-  const int i = r >> m.g_log2, j = r & ((1 << m.g_log2) - 1);
-  if (i >= m.query_len) return -1;
+  const int il = r >> m.g_log2, j = r & ((1 << m.g_log2) - 1);
+  const int i = grp * m.q_group + il;
+  if (il >= m.q_group || i >= m.query_len) return -1;
   return (int64_t(b) * m.query_len + i) * m.num_q_heads + (g << m.g_log2) + j;
 }
 #endif

@@ -66,7 +66,7 @@ def _params(pk, **kw):
     (dict(block_size=8), 1),
     (dict(block_size=32, head_dim=64), 2),  # block sizes 8 and 32: head_dim 128 only
     (dict(block_size=8, variant=1), 2),  # ... and the tensor-core kernel only
-    (dict(block_size=8, query_len=4), 2),  # block size 8: at most 8 columns per KV head
+    (dict(block_size=8, query_len=4), 1),  # block size 8: column groups of 8 per KV head
     (dict(block_size=8, kv_dtype=1), 2),  # the 8-bit cache: block size 16 or 32
     (dict(num_q_heads=12, num_kv_heads=1), 2),
     (dict(num_q_heads=6, num_kv_heads=4), 1),
@@ -79,9 +79,11 @@ def _params(pk, **kw):
     (dict(num_blocks=1 << 24, num_kv_heads=8), 1),  # cache rows past 2^31
     (dict(query_len=-1), 1),
     (dict(query_len=2000), 1),
-    (dict(query_len=3, num_q_heads=16, num_kv_heads=2), 2),  # G * 4 = 32 columns per KV head
+    (dict(query_len=3, num_q_heads=16, num_kv_heads=2), 1),  # two column groups (G 8)
     (dict(query_len=2, variant=1), 2),  # several new tokens: tensor-core kernel only
-    (dict(query_len=4, num_q_heads=64, num_kv_heads=8, kv_dtype=1), 2),  # > 64 fp8 columns
+    (dict(query_len=4, num_q_heads=64, num_kv_heads=8, kv_dtype=1), 1),  # groups of one token
+    # more virtual sequences (sequences x column groups) than the plan holds
+    (dict(query_len=1024, num_seqs=40, num_q_heads=64, num_kv_heads=8), 2),
     (dict(query_len=4), 1),  # valid shapes (G 4, 16 columns per KV head), NULL pointers
     (dict(), 1),  # valid shapes, NULL pointers
 ])
@@ -94,6 +96,18 @@ def test_decode_rejects_bad_arguments_on_the_host(pk, kw, status):
 
 def _ru(x):
     return (x + 255) // 256 * 256
+
+
+def _groups(Hq, Hkv, QL, cols_total=128, cols_head=16):
+    """Tokens per column group and groups: G x (tokens rounded up to a power
+    of two) <= cols_head columns per KV head and Hkv x that <= cols_total."""
+    if QL <= 1:
+        return 1, 1
+    G = Hq // Hkv
+    cols = min(cols_head, cols_total // Hkv)
+    cap = cols // G
+    qg = QL if QL <= cap else cap
+    return qg, -(-QL // qg)
 
 
 def _expected_ws(B, Hq, D, parts, grid, Hkv=None, QL=1, variant=0):
@@ -109,15 +123,17 @@ def _expected_ws(B, Hq, D, parts, grid, Hkv=None, QL=1, variant=0):
             rows = B * Hq * parts
             simt = 2 * _ru(rows * 4) + _ru(rows * D * 4)
         return 256 + simt
+    qg, ng = _groups(Hq, Hkv or 2, QL)
+    V = B * ng  # virtual sequences
     qlp = 1
-    while qlp < QL:
+    while qlp < qg:
         qlp *= 2
     cols = Hq * qlp
-    rows = (B + grid) * cols
-    tc = _ru((B + 2) * 4) + 2 * _ru(rows * 4) + _ru(rows * D * 4)
+    rows = (V + grid) * cols
+    tc = _ru((V + 2) * 4) + 2 * _ru(rows * 4) + _ru(rows * D * 4)
     if QL > 1:
         n_pad = next(n for n in (16, 32, 64, 128) if cols <= n)
-        tc += _ru(B * n_pad * D * 2)
+        tc += _ru(V * n_pad * D * 2)
     return 256 + tc
 
 
@@ -166,8 +182,16 @@ def test_decode_workspace_size(pk):
     p = _params(pk, num_seqs=64, num_q_heads=32, num_kv_heads=8, max_context_len=2048,
                 max_blocks_per_seq=128, query_len=4)
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
-                                                                         QL=4)
-    assert lib.pa_decode_workspace_size(ctypes.byref(_params(pk, query_len=8))) == 0
+                                                                         Hkv=8, QL=4)
+    # more new tokens than one column group holds: groups as virtual sequences
+    for ql in (8, 9, 64):
+        p = _params(pk, query_len=ql)
+        assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(2, 8, 128, 1, 256,
+                                                                             QL=ql)
+    p = _params(pk, num_seqs=64, num_q_heads=32, num_kv_heads=8, max_context_len=2048,
+                max_blocks_per_seq=128, query_len=16)
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
+                                                                         Hkv=8, QL=16)
 
 
 def test_cache_ops_reject_bad_arguments_on_the_host(pk):

@@ -123,7 +123,11 @@ def test_split_and_placement(pk, bs):
 
 
 @pytest.mark.parametrize("bs,G,Hkv,QL", [(8, 4, 8, 2), (8, 1, 8, 8), (8, 2, 2, 4), (32, 4, 8, 4),
-                                         (32, 8, 8, 2), (32, 1, 1, 16), (32, 4, 1, 3)])
+                                         (32, 8, 8, 2), (32, 1, 1, 16), (32, 4, 1, 3),
+                                         # column groups: 8 columns per KV head at block
+                                         # size 8, 16 at 32
+                                         (8, 4, 8, 8), (8, 8, 2, 3), (32, 4, 8, 16),
+                                         (32, 8, 8, 5)])
 def test_multi_token(pk, bs, G, Hkv, QL):
     lens = [L for L in (QL, 9, 16, 17, 31, 33, 34, 100, 513, 2049) if L >= QL]
     q, kc, vc, tables, lens, torch = _case(lens, G * Hkv, Hkv, bs, seed=bs + G * 7 + QL, QL=QL)

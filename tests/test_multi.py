@@ -170,12 +170,102 @@ def test_multi_placement_invariance_bit_exact(pk):
 
 
 def test_multi_unsupported_shapes_are_rejected(pk):
-    q, kc, vc, tables, lens, torch = _case([20], 3, 16, 2, 128, seed=87)  # G 8 x 4 > 16
-    with pytest.raises(pk.PagedKVError):
-        _decode(pk, q, kc, vc, tables, lens, torch)
+    """Several new tokens need the tensor-core kernel (the number of virtual
+    sequences is checked on the host, in the ABI tests)."""
     q, kc, vc, tables, lens, torch = _case([20], 2, 8, 2, 128, seed=88)
     with pytest.raises(pk.PagedKVError):
         _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+
+
+# ---------------------------------------------------------------- column groups
+#
+# A column group holds G x (its tokens, rounded up to a power of two) <= 16
+# columns per KV head and at most 128 in all (64 for the 8-bit cache). More
+# new tokens are split into groups of that many, each decoded as a virtual
+# sequence that streams the keys its last token sees: (G, Hkv, Q) below have
+# 2 to 16 groups, a last group shorter than the others, and Q = 64.
+
+GROUP_SHAPES = [(4, 8, 8), (4, 8, 16), (4, 8, 5), (8, 8, 3), (8, 8, 8), (8, 2, 3), (2, 8, 64),
+                (4, 1, 64), (1, 8, 33)]
+
+
+@pytest.mark.parametrize("G,Hkv,QL", GROUP_SHAPES)
+def test_multi_column_groups(pk, G, Hkv, QL):
+    lens = sorted({QL, QL + 1, 15, 16, 17, 33, 100, 513, 1025, 3000})
+    lens = [L for L in lens if L >= QL]
+    _check(pk, *_case(lens, QL, G * Hkv, Hkv, 128, seed=300 + G * 100 + Hkv * 10 + QL))
+
+
+def test_multi_column_groups_head_dim_64(pk):
+    lens = [8, 9, 16, 17, 100, 700, 2049]
+    _check(pk, *_case(lens, 8, 32, 8, 64, seed=331))
+
+
+def test_multi_column_groups_llama8b_layer(pk):
+    """The 64-sequence 8B layer with 16 new tokens per sequence (chunked-prefill
+    slices): 4 column groups of 4 tokens, 256 virtual sequences."""
+    r = workloads.llama8b_layer()
+    _check(pk, *_case(r.lens0 + 16, 16, 32, 8, 128, seed=332))
+
+
+def test_multi_column_groups_llama70b_long(pk):
+    """Three 70B-class sequences (64/8 heads, 8k-33k tokens) with 8 new tokens:
+    4 column groups of 2, each streaming up to 33k tokens over many CTAs."""
+    r = workloads.llama70b_long(batch=8)
+    _check(pk, *_case(r.lens0[:3] + 8, 8, 64, 8, 128, seed=333))
+
+
+def test_multi_column_groups_placement_invariance_bit_exact(pk):
+    import torch
+
+    q, kc, vc, tables, lens, _ = _case([300, 47, 900, 8], 8, 32, 8, 128, seed=334)
+    NB = kc.shape[0]
+    perm = np.random.default_rng(19).permutation(NB)
+    kcb, vcb = torch.empty_like(kc), torch.empty_like(vc)
+    kcb[torch.from_numpy(perm).cuda()] = kc
+    vcb[torch.from_numpy(perm).cuda()] = vc
+    tables_b = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    a = _decode(pk, q, kc, vc, tables, lens, torch)
+    b = _decode(pk, q, kcb, vcb, tables_b, lens, torch)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("QL", [8, 13])
+def test_multi_column_groups_fused_append(pk, QL):
+    """Every group writes the new tokens its own stream reads before it reads
+    their blocks (the same bytes where groups overlap): caches bit-exact, and
+    the rows against the oracle."""
+    nb = _sm_count() + 1
+    long_len = nb * 16 + 5
+    lens = [long_len, 17, 33, 16 + QL, 500, QL]
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case(lens, QL, 32, 8, seed=340 + QL)
+    kc2, vc2 = kc.clone(), vc.clone()
+    out = pk.pa_append_decode(q, kc2, vc2, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
+                              torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() == 0
+    ko, vo = oracle.reshape_and_cache(kn.cpu(), vn.cpu(), oracle.bf16_bits(kc.cpu()),
+                                      oracle.bf16_bits(vc.cpu()), slots)
+    assert np.array_equal(oracle.bf16_bits(kc2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
+    want = oracle.paged_decode_multi(q.cpu(), ko, vo, tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+
+
+def test_multi_column_groups_short_sequences_are_flagged_and_zero(pk):
+    QL = 8
+    q, kc, vc, tables, lens, torch = _case([40, 5, 0, 50], QL, 32, 8, 128, seed=345)
+    out = torch.full_like(q, 7.0)
+    pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                 max_context_len=50, out=out)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() & DEVERR_CONTEXT_LEN
+    got = harness.bf16_tensor_to_f64(out)
+    assert not got[1].any() and not got[2].any()
+    keep = [0, 3]
+    want = oracle.paged_decode_multi(q.cpu()[keep], kc.cpu(), vc.cpu(), tables[keep], lens[keep])
+    harness.assert_close(got[keep], want)
 
 
 # ---------------------------------------------------------------- fused KV write
@@ -312,6 +402,22 @@ def test_multi_fp8_edge_lengths(pk, G, Hkv, QL):
     lens = [L for L in (QL, 15, 16, 17, 18, 100, 513, 1025, 4098) if L >= QL]
     q, k8, v8, ks, vs, tables, lens, torch = _fp8_multi_case(pk, lens, QL, G * Hkv, Hkv,
                                                              seed=G * 10 + Hkv + QL)
+    out = pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=int(lens.max()), k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    want = oracle.paged_decode_multi_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy(),
+                                         ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+
+
+@pytest.mark.parametrize("G,Hkv,QL", [(8, 8, 4), (4, 8, 8), (4, 8, 5), (2, 2, 16)])
+def test_multi_fp8_column_groups(pk, G, Hkv, QL):
+    """The 8-bit cache allows 64 columns: 8 query heads per KV head take one
+    token per group, four take two."""
+    lens = [L for L in (QL, 15, 16, 17, 100, 513, 2049) if L >= QL]
+    q, k8, v8, ks, vs, tables, lens, torch = _fp8_multi_case(pk, lens, QL, G * Hkv, Hkv,
+                                                             seed=350 + G * 10 + QL)
     out = pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
                        max_context_len=int(lens.max()), k_scale=ks, v_scale=vs)
     torch.cuda.synchronize()
