@@ -57,8 +57,8 @@
  * Supported shapes: block_size 8, 16 or 32 ("Paged Attention as a Memory
  * Manager", §PagedAttention: a compile-time constant, typically 8, 16 or 32);
  * head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}. Block sizes
- * 8 and 32 decode on the tensor-core kernel at head_dim 128 (the 8-bit cache:
- * 16 and 32). Anything else returns PA_ERR_UNSUPPORTED.
+ * 8 and 32 decode on the tensor-core kernel (the 8-bit cache: head_dim 128 and
+ * block size 16 or 32). Anything else returns PA_ERR_UNSUPPORTED.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -155,11 +155,15 @@ typedef struct {
                                   [num_seqs][Q][num_q_heads][head_dim], the new tokens are the
                                   last Q of each sequence's context_lens[b] (already in the cache),
                                   and query token i attends to the first context_lens[b] - Q + i + 1
-                                  of them (causal among the new tokens). Tensor-core kernel only,
-                                  with G * Qp <= 16 (Qp = Q rounded up to a power of two) and
-                                  num_kv_heads * G * Qp <= 128 (<= 64 for the 8-bit cache); other
-                                  shapes return PA_ERR_UNSUPPORTED. A sequence with
-                                  0 < context_lens[b] < Q gets zero rows and PA_DEVERR_CONTEXT_LEN. */
+                                  of them (causal among the new tokens). Tensor-core kernel only.
+                                  Its MMAs take the query tokens in column groups: G * Qp <= 16
+                                  columns per KV head (8 at block size 8, Qp = the group's tokens
+                                  rounded up to a power of two) and num_kv_heads * G * Qp <= 128
+                                  (64 for the 8-bit cache); a sequence with more new tokens is
+                                  decoded as several groups, each streaming the keys its last
+                                  token sees, with num_seqs * groups <= 16384 (else
+                                  PA_ERR_UNSUPPORTED). A sequence with 0 < context_lens[b] < Q
+                                  gets zero rows and PA_DEVERR_CONTEXT_LEN. */
   int32_t wait_timeout_us;     /* tensor-core kernel: the longest one of its barrier waits may
                                   take, in microseconds; 0 = 2 s. A wait that runs out sets
                                   PA_DEVERR_TIMEOUT, and every CTA that saw it stops, lets the

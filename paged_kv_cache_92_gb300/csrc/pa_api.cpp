@@ -67,9 +67,8 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: query rows exceed 2^31");
   if (p->block_size != kBlockSize && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
     return set_error(PA_ERR_UNSUPPORTED,
-                     "pa_decode: block_size 8 and 32 run on the tensor-core kernel (head_dim 128, "
-                     "num_kv_heads 1/2/4/8; block_size 8: at most 8 query columns per KV head and "
-                     "the bf16 cache only)");
+                     "pa_decode: block_size 8 and 32 run on the tensor-core kernel (head_dim 64 "
+                     "or 128, num_kv_heads 1/2/4/8; block_size 8: the bf16 cache only)");
   if (query_len_of(p) > 1 && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
     return set_error(PA_ERR_UNSUPPORTED,
                      "pa_decode: query_len > 1 runs on the tensor-core kernel with num_kv_heads "

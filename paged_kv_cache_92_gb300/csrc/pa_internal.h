@@ -159,12 +159,14 @@ bool decode_uses_tc(const pa_decode_params* p);
 int launch_decode(const DecodeLaunch& L, void* stream);      // CUDA-core decode kernel
 int launch_decode_tc(const DecodeLaunch& L, void* stream);   // tensor-core decode kernel
 // its shares by translation unit: bf16 head_dim 64; the 8-bit cache; block
-// size 8; block size 32 (bf16, 8-bit)
+// size 8; block size 32 (bf16, 8-bit); block sizes 8 and 32 at head_dim 64
 int launch_decode_tc_d64(const DecodeLaunch& L, void* stream);
 int launch_decode_tc_fp8(const DecodeLaunch& L, void* stream);
 int launch_decode_tc_bs8(const DecodeLaunch& L, void* stream);
 int launch_decode_tc_bs32(const DecodeLaunch& L, void* stream);
 int launch_decode_tc_bs32_fp8(const DecodeLaunch& L, void* stream);
+int launch_decode_tc_bs8_d64(const DecodeLaunch& L, void* stream);   // bf16 head_dim 64
+int launch_decode_tc_bs32_d64(const DecodeLaunch& L, void* stream);
 int launch_merge(const DecodeLaunch& L, void* stream);       // split-K merge (if needed)
 // Decode-step check (block_tables non-null): token t is sequence t's newest
 // token; it is written only if slot_mapping[t] is the slot of token
@@ -214,6 +216,8 @@ int read_and_clear_decode_tc_fp8_errors(uint32_t* flags);
 int read_and_clear_decode_tc_bs8_errors(uint32_t* flags);
 int read_and_clear_decode_tc_bs32_errors(uint32_t* flags);
 int read_and_clear_decode_tc_bs32_fp8_errors(uint32_t* flags);
+int read_and_clear_decode_tc_bs8_d64_errors(uint32_t* flags);
+int read_and_clear_decode_tc_bs32_d64_errors(uint32_t* flags);
 
 // Size of the library-owned device scratch used by pa_decode_noalloc.
 constexpr size_t kNoAllocScratchBytes = PA_NOALLOC_SCRATCH_BYTES;

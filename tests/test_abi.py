@@ -64,7 +64,8 @@ def _params(pk, **kw):
     (dict(block_size=64), 2),
     (dict(block_size=32), 1),  # block size 32: tensor-core kernel, valid shapes, NULL pointers
     (dict(block_size=8), 1),
-    (dict(block_size=32, head_dim=64), 2),  # block sizes 8 and 32: head_dim 128 only
+    (dict(block_size=32, head_dim=64), 1),  # block sizes 8 and 32 at head_dim 64: bf16
+    (dict(block_size=8, head_dim=64, kv_dtype=1), 2),  # the 8-bit cache: head_dim 128
     (dict(block_size=8, variant=1), 2),  # ... and the tensor-core kernel only
     (dict(block_size=8, query_len=4), 1),  # block size 8: column groups of 8 per KV head
     (dict(block_size=8, kv_dtype=1), 2),  # the 8-bit cache: block size 16 or 32

@@ -154,12 +154,27 @@ def test_copy_blocks_bit_exact(pk, bs):
     _ = rng
 
 
+@BLOCK_SIZES
+@pytest.mark.parametrize("G,Hkv,QL", [(4, 8, 1), (8, 1, 1), (1, 4, 1), (4, 2, 3), (4, 8, 8)])
+def test_head_dim_64(pk, bs, G, Hkv, QL):
+    """head_dim 64 at block sizes 8 and 32: lengths around both block sizes,
+    one sequence split over CTAs, several new tokens (column groups at 8)."""
+    nb = 2 * int(__import__("torch").cuda.get_device_properties(0).multi_processor_count) + 3
+    lens = [L for L in (QL, 7, 8, 9, 31, 32, 33, 100, 513, nb * bs + 1) if L >= QL]
+    q, kc, vc, tables, lens, torch = _case(lens, G * Hkv, Hkv, bs, seed=bs * 7 + G + QL, D=64,
+                                           QL=QL if QL > 1 else 0)
+    out = _decode(pk, q, kc, vc, tables, lens, torch)
+    if QL > 1:
+        ref = oracle.paged_decode_multi(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    else:
+        ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert pk.pa_device_errors() == 0
+
+
 def test_unsupported_block_size_shapes_are_rejected(pk):
     import torch
 
-    q, kc, vc, tables, lens, _ = _case([40], 8, 2, 32, seed=7, D=64)  # head_dim 64
-    with pytest.raises(pk.PagedKVError):
-        _decode(pk, q, kc, vc, tables, lens, torch)
     q, kc, vc, tables, lens, _ = _case([40], 8, 2, 8, seed=8)
     with pytest.raises(pk.PagedKVError):
         _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
