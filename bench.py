@@ -402,20 +402,21 @@ def time_launches(plans, n: int) -> float:
 
 # columns of one other_workloads row (a compact table: the bench line must fit
 # the few thousand characters a log tail keeps)
-ROW_COLS = ["config", "seqs", "step_bytes", "step_us", "step_gbs", "step_frac", "launch_bytes",
-            "launch_us", "launch_frac"]
+ROW_COLS = ["config", "seqs", "step_bytes", "step_us", "step_gbs", "step_frac", "launch_us",
+            "launch_frac"]
 
 
 def entry(step_bytes: int, step_ms: float, launch_bytes: int, launch_ms: float, peak: float,
           config=None, seqs=None, hbm_fraction: bool = True) -> list:
     """One secondary workload's row (ROW_COLS): the plain step loop
-    (``step_*``) and the bracketed decode call (``launch_*``), GB/s of
-    algorithmic bytes and fractions of the measured HBM peak (None where the
-    bytes are logical, not HBM: the shared prefix is read from L2)."""
+    (``step_*``) and the bracketed decode call (``launch_*``; its bytes are the
+    step's less any copy-on-write copies), GB/s of algorithmic bytes and
+    fractions of the measured HBM peak (None where the bytes are logical, not
+    HBM: the shared prefix is read from L2)."""
     sg = step_bytes / (step_ms * 1e-3) / 1e9
     lg = launch_bytes / (launch_ms * 1e-3) / 1e9
     return [config, seqs, int(step_bytes), round(step_ms * 1e3, 2), round(sg, 1),
-            round(sg / peak, 4) if hbm_fraction else None, int(launch_bytes),
+            round(sg / peak, 4) if hbm_fraction else None,
             round(launch_ms * 1e3, 2), round(lg / peak, 4) if hbm_fraction else None]
 
 
