@@ -486,7 +486,8 @@ def run_ours(args, rank: int, world: int) -> dict:
 
     # end to end through the public API: pinned host inputs -> device, step,
     # result -> pinned host, every step
-    e2e = run_e2e(pk, W, r, device, args.steps, args.warmup, step_b, args.variant)
+    e2e = run_e2e(pk, W, r, device, max(args.steps, args.e2e_steps), args.warmup, step_b,
+                  args.variant)
 
     traffic = profiled_traffic(f"pa_decode_tc_{PROFILE_OF.get(name, name)}.md") \
         if args.variant == 0 and fused else None
@@ -759,13 +760,18 @@ def run_e2e(pk, W, r, device, steps: int, warmup: int, step_b: int, variant: int
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
+    marks = [0.0] * (steps + 1)
+    marks[0] = time.perf_counter()
     for i in range(steps):
         step(i)  # returns once the output is in host memory
-    dt = time.perf_counter() - t0
+        marks[i + 1] = time.perf_counter()
+    dt = marks[-1] - marks[0]
+    per_step = sorted(marks[i + 1] - marks[i] for i in range(steps))
     return {"value": round(step_b * steps / dt / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(host_in.numel()), "d2h_bytes_per_step": int(host_out.numel() * 2),
-            "ms_per_step": round(dt / steps * 1e3, 4),
+            "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4),
+            "ms_per_step_median": round(per_step[steps // 2] * 1e3, 4),
+            "ms_per_step_max": round(per_step[-1] * 1e3, 4),
             "api": "pa_step_host (one C call per step: a kernel stages the packed inputs from "
                    "pinned host memory over the host link, copy-on-write, fused KV write + decode "
                    "+ merge writing the output rows into pinned host memory, stream sync)"}
@@ -933,6 +939,9 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE,
                     help="the workload of the headline line (default: the largest "
                          "single-GPU configuration)")
+    ap.add_argument("--e2e-steps", type=int, default=200,
+                    help="end-to-end steps (at least --steps): one host hiccup in a short loop "
+                         "would otherwise move the mean")
     ap.add_argument("--sustain-s", type=float, default=1.0,
                     help="untimed loaded seconds before the timed region (clock sampling)")
     ap.add_argument("--launch-samples", type=int, default=50,
