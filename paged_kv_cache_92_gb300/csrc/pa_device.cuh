@@ -19,6 +19,14 @@ __device__ __forceinline__ float from_e4m3(uint8_t c) {
   const __half_raw h = __nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t(c), __NV_E4M3);
   return __half2float(__half(h));
 }
+// The same for a pair (a in the low byte): one conversion instruction each way.
+__device__ __forceinline__ uint32_t to_e4m3x2(float a, float b) {
+  return uint32_t(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float2 from_e4m3x2(uint32_t c) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(c), __NV_E4M3);
+  return __half22float2(__half2(h));
+}
 
 // x / s rounded to nearest even, for a positive normal s with r = RN(1/s):
 // Markstein's correction step (P. Markstein, "Computation of elementary

@@ -143,6 +143,7 @@ struct Fp8Append {
   int64_t num_chunks;  // rows x (head_dim / 8); 0 = nothing to write
   int64_t num_slots;
   int num_kv_heads, head_dim, max_blocks_per_seq, cap, q_len, bs_log2;
+  int early;  // lengths and tables final before the previous kernel began (overlap_prologue)
 };
 
 // One launch ahead of the 8-bit decode. The first blocks write the new
@@ -158,9 +159,9 @@ __global__ void __launch_bounds__(128)
                     float* __restrict__ inv_alpha, const QueryMap m, int q_blocks,
                     const Fp8Append a) {
   dev::griddep_launch_dependents();
-  dev::griddep_wait();  // q and the new rows may come from the previous kernel
   const int w_blocks = int(gridDim.x) - q_blocks;
   if (int(blockIdx.x) >= w_blocks) {
+    dev::griddep_wait();  // q may come from the previous kernel
     split_query_row(q, q8, inv_alpha, m,
                     int64_t(blockIdx.x - w_blocks) * 4 + (threadIdx.x >> 5), threadIdx.x & 31);
     return;
@@ -174,10 +175,21 @@ __global__ void __launch_bounds__(128)
   const int h = int(row % a.num_kv_heads);
   const int64_t t = row / a.num_kv_heads;
   const int b = int(t / a.q_len), i = int(t % a.q_len);
-  // every load that does not depend on another first (one round trip), then
-  // the table entry of the token's position
+  // The token's position (from its sequence's length) and that position's
+  // table entry: two dependent loads. When the lengths and tables were final
+  // before the previous kernel began they are taken before waiting for it,
+  // and only the loads of this step's inputs remain after the wait (one
+  // round trip on the decode's critical path instead of two).
+  int L = 0, e = -1;
+  auto locate = [&]() {
+    L = min(a.context_lens[b], a.cap);
+    if (L >= a.q_len)
+      e = a.block_tables[int64_t(b) * a.max_blocks_per_seq + ((L - a.q_len + i) >> a.bs_log2)];
+  };
+  if (a.early) locate();
+  dev::griddep_wait();  // the slots and the new rows may come from the previous kernel
+  if (!a.early) locate();
   const int64_t slot = a.slot_mapping[t];
-  const int L = min(a.context_lens[b], a.cap);
   const uint4 kr = a.k_new[idx], vr = a.v_new[idx];
   const float ks = a.k_scale[h], vs = a.v_scale[h];
   if (slot < 0) return;  // padding token: no write
@@ -187,7 +199,6 @@ __global__ void __launch_bounds__(128)
   }
   if (L < a.q_len) return;  // no room for the new tokens: the decode flags the length
   const int pos = L - a.q_len + i;
-  const int e = a.block_tables[int64_t(b) * a.max_blocks_per_seq + (pos >> a.bs_log2)];
   if (e < 0 || slot != int64_t(e) * BS + (pos & (BS - 1))) {
     if (h == 0 && c == 0) atomicOr(&g_fp8_errors, PA_DEVERR_APPEND_SLOT);
     return;
@@ -253,6 +264,7 @@ int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap&
     a.bs_log2 = log2_of(p->block_size);
     a.num_slots = int64_t(p->num_blocks) * p->block_size;
     a.num_chunks = int64_t(m.num_real_seqs) * m.query_len * p->num_kv_heads * (p->head_dim / 8);
+    a.early = p->overlap_prologue ? 1 : 0;
   }
   const int64_t q_blocks = (int64_t(m.num_seqs) * m.n_pad + 3) / 4;
   const int64_t w_blocks = (a.num_chunks + 127) / 128;
