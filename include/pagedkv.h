@@ -155,15 +155,18 @@ typedef struct {
                                   [num_seqs][Q][num_q_heads][head_dim], the new tokens are the
                                   last Q of each sequence's context_lens[b] (already in the cache),
                                   and query token i attends to the first context_lens[b] - Q + i + 1
-                                  of them (causal among the new tokens). Tensor-core kernel only.
-                                  Its MMAs take the query tokens in column groups: G * Qp <= 16
+                                  of them (causal among the new tokens). The tensor-core
+                                  kernel's MMAs take the query tokens in column groups: G * Qp <= 16
                                   columns per KV head (8 at block size 8, Qp = the group's tokens
                                   rounded up to a power of two) and num_kv_heads * G * Qp <= 128
                                   (64 for the 8-bit cache); a sequence with more new tokens is
                                   decoded as several groups, each streaming the keys its last
-                                  token sees, with num_seqs * groups <= 16384 (else
-                                  PA_ERR_UNSUPPORTED). A sequence with 0 < context_lens[b] < Q
-                                  gets zero rows and PA_DEVERR_CONTEXT_LEN. */
+                                  token sees, with num_seqs * groups <= 16384. Shapes beyond
+                                  that, and the CUDA-core variant, decode each (sequence, token)
+                                  on its own with num_seqs * Q <= 65535 (else
+                                  PA_ERR_UNSUPPORTED; bf16 cache, block size 16). A sequence with
+                                  0 < context_lens[b] < Q gets zero rows and
+                                  PA_DEVERR_CONTEXT_LEN. */
   int32_t wait_timeout_us;     /* tensor-core kernel: the longest one of its barrier waits may
                                   take, in microseconds; 0 = 2 s. A wait that runs out sets
                                   PA_DEVERR_TIMEOUT, and every CTA that saw it stops, lets the

@@ -69,10 +69,12 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
     return set_error(PA_ERR_UNSUPPORTED,
                      "pa_decode: block_size 8 and 32 run on the tensor-core kernel (head_dim 64 "
                      "or 128, num_kv_heads 1/2/4/8; block_size 8: the bf16 cache only)");
-  if (query_len_of(p) > 1 && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
+  // the CUDA-core kernel runs one CTA row per (sequence, new token) in grid z
+  if (!decode_uses_tc(p) && int64_t(p->num_seqs) * query_len_of(p) > 65535)
     return set_error(PA_ERR_UNSUPPORTED,
-                     "pa_decode: query_len > 1 runs on the tensor-core kernel with num_kv_heads "
-                     "1/2/4/8 and num_seqs * (query_len split into column groups) <= 16384");
+                     "pa_decode: on the CUDA-core kernel num_seqs * query_len must be <= 65535 "
+                     "(the tensor-core kernel takes num_kv_heads 1/2/4/8 and num_seqs * "
+                     "(query_len split into column groups) <= 16384)");
   if (p->kv_dtype == PA_KV_FP8_E4M3) {
     if (p->head_dim != 128 || p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p))
       return set_error(PA_ERR_UNSUPPORTED,
@@ -129,7 +131,8 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
     // CUDA-core kernel: per-partition partials (only when a sequence can split)
     w.total = H;
     if (num_partitions > 1) {
-      const size_t rows = size_t(p->num_seqs) * p->num_q_heads * num_partitions;
+      const size_t rows =
+          size_t(p->num_seqs) * query_len_of(p) * p->num_q_heads * num_partitions;
       w.simt_m = H;
       w.simt_l = w.simt_m + round_up(rows * sizeof(float), 256);
       w.simt_acc = w.simt_l + round_up(rows * sizeof(float), 256);
@@ -188,9 +191,8 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
     e = launch_decode_tc(L, stream);
   } else if (p->kv_dtype == PA_KV_FP8_E4M3) {
     return set_error(PA_ERR_UNSUPPORTED, "the 8-bit cache needs the tensor-core kernel");
-  } else if (query_len_of(p) > 1 || p->block_size != kBlockSize) {
-    return set_error(PA_ERR_UNSUPPORTED,
-                     "query_len > 1 and block sizes other than 16 need the tensor-core kernel");
+  } else if (p->block_size != kBlockSize) {
+    return set_error(PA_ERR_UNSUPPORTED, "block sizes other than 16 need the tensor-core kernel");
   } else {
     if (append) {  // the same effect in two launches
       AppendCheck chk;
@@ -199,10 +201,11 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
       chk.max_blocks_per_seq = p->max_blocks_per_seq;
       chk.cap = p->max_blocks_per_seq * p->block_size < p->max_context_len
                     ? p->max_blocks_per_seq * p->block_size : p->max_context_len;
+      chk.q_len = query_len_of(p);
       e = launch_reshape_and_cache(append->k_new, append->v_new, append->k_cache,
-                                   append->v_cache, append->slot_mapping, p->num_seqs,
-                                   p->num_kv_heads, p->head_dim, p->block_size, p->num_blocks,
-                                   stream, chk);
+                                   append->v_cache, append->slot_mapping,
+                                   p->num_seqs * query_len_of(p), p->num_kv_heads, p->head_dim,
+                                   p->block_size, p->num_blocks, stream, chk);
     }
     if (e) {
       std::snprintf(where, sizeof(where), "%s: launch", who);

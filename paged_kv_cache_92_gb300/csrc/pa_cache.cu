@@ -44,11 +44,16 @@ __global__ void __launch_bounds__(256)
     atomicOr(&g_cache_errors, PA_DEVERR_SLOT);
     return;
   }
-  if (check.block_tables) {  // decode step: only the slot of the sequence's last token
-    const int L = min(check.context_lens[t], check.cap);
-    if (L <= 0) return;
-    const int e = check.block_tables[t * check.max_blocks_per_seq + (L - 1) / BS];
-    if (slot != int64_t(e) * BS + (L - 1) % BS) {
+  if (check.block_tables) {
+    // decode step: token t is new token i of sequence b, written only at its
+    // position's slot (the last q_len tokens of the sequence)
+    const int64_t b = t / check.q_len;
+    const int i = int(t - b * check.q_len);
+    const int L = min(check.context_lens[b], check.cap);
+    if (L < check.q_len) return;  // no room for the new tokens: the decode flags the length
+    const int pos = L - check.q_len + i;
+    const int e = check.block_tables[b * check.max_blocks_per_seq + pos / BS];
+    if (slot != int64_t(e) * BS + pos % BS) {
       if (h == 0 && c == 0) atomicOr(&g_cache_errors, PA_DEVERR_APPEND_SLOT);
       return;
     }

@@ -6,7 +6,10 @@
 // softmax(scale * q.K^T) V over the sequence's cached tokens, with K/V read
 // block by block through the block table and a running softmax carried
 // across blocks. Tokens past the context length inside the last block are
-// masked.
+// masked. With Q new tokens per sequence ("How Paged Attention and
+// Continuous Batching Actually Work", §Continuous batching) row (b, i) of q
+// is token L - Q + i of its sequence and sees its first L - Q + i + 1 tokens;
+// each (sequence, token) is decoded as a sequence of its own (grid z).
 //
 // GB300 design (the pages' thread-group layout targets older GPUs and is not
 // followed):
@@ -109,12 +112,13 @@ __global__ void __launch_bounds__(NTHREADS)
                         const int32_t* __restrict__ context_lens, int max_blocks_per_seq,
                         int num_kv_heads, int num_blocks, int max_context_len, float scale_log2,
                         int partition_tokens, int num_partitions, float* __restrict__ part_m,
-                        float* __restrict__ part_l, float* __restrict__ part_acc) {
+                        float* __restrict__ part_l, float* __restrict__ part_acc, int q_len) {
   using C = Cfg<D, G>;
   constexpr int ST = C::ST;
   const int part = blockIdx.x;
   const int g = blockIdx.y;
-  const int b = blockIdx.z;
+  const int z = blockIdx.z;  // row of q / out: sequence b, its new token qi
+  const int b = z / q_len, qi = z - (z / q_len) * q_len;
   const int num_q_heads = num_kv_heads * G;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -122,14 +126,20 @@ __global__ void __launch_bounds__(NTHREADS)
 
   int L = context_lens[b];
   const int cap = min(max_blocks_per_seq * BS, max_context_len);
+  const bool report = tid == 0 && part == 0 && g == 0 && qi == 0;
   if (L > cap) {
-    if (tid == 0 && part == 0 && g == 0) atomicOr(&g_decode_errors, PA_DEVERR_CONTEXT_LEN);
+    if (report) atomicOr(&g_decode_errors, PA_DEVERR_CONTEXT_LEN);
     L = cap;
   }
+  if (L > 0 && L < q_len) {  // no room for the new tokens: an empty sequence
+    if (report) atomicOr(&g_decode_errors, PA_DEVERR_CONTEXT_LEN);
+    L = 0;
+  }
+  if (L > 0) L = L - q_len + qi + 1;  // the keys token qi sees
   if (L <= 0) {
     if (part == 0) {
       for (int i = tid; i < G * D; i += NTHREADS)
-        out[(size_t(b) * num_q_heads + g * G) * D + i] = __float2bfloat16_rn(0.0f);
+        out[(size_t(z) * num_q_heads + g * G) * D + i] = __float2bfloat16_rn(0.0f);
     }
     return;
   }
@@ -192,7 +202,7 @@ __global__ void __launch_bounds__(NTHREADS)
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     const uint4* qrow =
-        reinterpret_cast<const uint4*>(q + (size_t(b) * num_q_heads + g * G + h) * D);
+        reinterpret_cast<const uint4*>(q + (size_t(z) * num_q_heads + g * G + h) * D);
 #pragma unroll
     for (int k = 0; k < C::CHUNKS; ++k) {
       float f[8];
@@ -344,7 +354,7 @@ __global__ void __launch_bounds__(NTHREADS)
       num = fmaf(wt, sm_acc[(w * G + h) * D + d], num);
       den = fmaf(wt, sm_l[w * G + h], den);
     }
-    const size_t row = size_t(b) * num_q_heads + g * G + h;
+    const size_t row = size_t(z) * num_q_heads + g * G + h;
     if (!split) {
       out[row * D + d] = __float2bfloat16_rn(num * __frcp_rn(den));
     } else {
@@ -358,25 +368,29 @@ __global__ void __launch_bounds__(NTHREADS)
   }
 }
 
-// Log-sum-exp merge of split-K partials: one warp per (sequence, query head).
+// Log-sum-exp merge of split-K partials: one warp per (row of q, query head),
+// a row being a sequence's new token.
 template <int D>
 __global__ void __launch_bounds__(128)
     merge_partitions_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ part_m,
                             const float* __restrict__ part_l, const float* __restrict__ part_acc,
                             const int32_t* __restrict__ context_lens, int num_q_heads,
                             int max_blocks_per_seq, int max_context_len, int partition_tokens,
-                            int num_partitions) {
+                            int num_partitions, int q_len) {
   constexpr int VPL = D / 32;  // values per lane
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.x * 4 + warp;
-  const int b = blockIdx.y;
+  const int z = blockIdx.y;
+  const int b = z / q_len, qi = z - (z / q_len) * q_len;
   if (h >= num_q_heads) return;
   int L = context_lens[b];
   L = min(L, min(max_blocks_per_seq * BS, max_context_len));
+  if (L < q_len) return;  // empty: zero rows written by the decode kernel
+  L = L - q_len + qi + 1;
   if (L <= partition_tokens) return;  // written directly by the decode kernel
   const int np = (L + partition_tokens - 1) / partition_tokens;
-  const size_t row = (size_t(b) * num_q_heads + h) * num_partitions;
+  const size_t row = (size_t(z) * num_q_heads + h) * num_partitions;
   float M = -INFINITY;
   for (int p = lane; p < np; p += 32) M = fmaxf(M, part_m[row + p]);
 #pragma unroll
@@ -401,7 +415,7 @@ __global__ void __launch_bounds__(128)
     }
   }
   const float inv = __frcp_rn(den);
-  __nv_bfloat16* o = out + (size_t(b) * num_q_heads + h) * D + lane * VPL;
+  __nv_bfloat16* o = out + (size_t(z) * num_q_heads + h) * D + lane * VPL;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(acc[j] * inv);
 }
@@ -417,25 +431,27 @@ int launch_decode_t(const DecodeLaunch& Lc, cudaStream_t stream) {
     if (e != cudaSuccess) return int(e);
     configured = smem;
   }
-  dim3 grid(Lc.num_partitions, p->num_kv_heads, p->num_seqs);
+  const int q_len = query_len_of(p);
+  dim3 grid(Lc.num_partitions, p->num_kv_heads, p->num_seqs * q_len);
   const float scale_log2 = p->scale * kLog2e;
   paged_decode_kernel<D, G><<<grid, NTHREADS, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(p->q), static_cast<__nv_bfloat16*>(p->out),
       static_cast<const __nv_bfloat16*>(p->k_cache), static_cast<const __nv_bfloat16*>(p->v_cache),
       p->block_tables, p->context_lens, p->max_blocks_per_seq, p->num_kv_heads, p->num_blocks,
       p->max_context_len, scale_log2, Lc.partition_tokens, Lc.num_partitions, Lc.part_m, Lc.part_l,
-      Lc.part_acc);
+      Lc.part_acc, q_len);
   return int(cudaGetLastError());
 }
 
 template <int D>
 int launch_merge_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   const pa_decode_params* p = Lc.p;
-  dim3 mgrid((p->num_q_heads + 3) / 4, p->num_seqs);
+  const int q_len = query_len_of(p);
+  dim3 mgrid((p->num_q_heads + 3) / 4, p->num_seqs * q_len);
   merge_partitions_kernel<D><<<mgrid, 128, 0, stream>>>(
       static_cast<__nv_bfloat16*>(p->out), Lc.part_m, Lc.part_l, Lc.part_acc, p->context_lens,
       p->num_q_heads, p->max_blocks_per_seq, p->max_context_len, Lc.partition_tokens,
-      Lc.num_partitions);
+      Lc.num_partitions, q_len);
   return int(cudaGetLastError());
 }
 

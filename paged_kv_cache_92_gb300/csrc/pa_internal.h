@@ -177,6 +177,7 @@ struct AppendCheck {
   const int32_t* context_lens = nullptr;
   int max_blocks_per_seq = 0;
   int cap = 0;
+  int q_len = 1;  // new tokens per sequence: token row t is token t % q_len of sequence t / q_len
 };
 int launch_reshape_and_cache(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,

@@ -81,10 +81,14 @@ def _params(pk, **kw):
     (dict(query_len=-1), 1),
     (dict(query_len=2000), 1),
     (dict(query_len=3, num_q_heads=16, num_kv_heads=2), 1),  # two column groups (G 8)
-    (dict(query_len=2, variant=1), 2),  # several new tokens: tensor-core kernel only
+    (dict(query_len=2, variant=1), 1),  # several new tokens on the CUDA-core kernel too
+    (dict(query_len=1024, num_seqs=70, variant=1), 2),  # ... up to 65535 (sequence, token) rows
     (dict(query_len=4, num_q_heads=64, num_kv_heads=8, kv_dtype=1), 1),  # groups of one token
-    # more virtual sequences (sequences x column groups) than the plan holds
-    (dict(query_len=1024, num_seqs=40, num_q_heads=64, num_kv_heads=8), 2),
+    # more virtual sequences (sequences x column groups) than the tensor-core
+    # plan holds: the CUDA-core kernel takes them (40 x 1024 rows) ...
+    (dict(query_len=1024, num_seqs=40, num_q_heads=64, num_kv_heads=8), 1),
+    # ... and no more than 65535 rows
+    (dict(query_len=1024, num_seqs=70, num_q_heads=64, num_kv_heads=8), 2),
     (dict(query_len=4), 1),  # valid shapes (G 4, 16 columns per KV head), NULL pointers
     (dict(), 1),  # valid shapes, NULL pointers
 ])
@@ -117,11 +121,12 @@ def _expected_ws(B, Hq, D, parts, grid, Hkv=None, QL=1, variant=0):
     column, Hkv * G * (QL rounded up to a power of two) columns; with QL > 1
     the bf16 queries are also staged in column order, [B][N][D] with N the
     columns padded to 16/32/64/128. CUDA-core kernel (variant 1): the
-    per-partition partials, when a sequence can split."""
+    per-partition partials of every (sequence, new token) row, when a
+    sequence can split."""
     if variant == 1:
         simt = 0
         if parts > 1:
-            rows = B * Hq * parts
+            rows = B * QL * Hq * parts
             simt = 2 * _ru(rows * 4) + _ru(rows * D * 4)
         return 256 + simt
     qg, ng = _groups(Hq, Hkv or 2, QL)
@@ -193,6 +198,11 @@ def test_decode_workspace_size(pk):
                 max_blocks_per_seq=128, query_len=16)
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
                                                                          Hkv=8, QL=16)
+    # several new tokens on the CUDA-core kernel: partials per (sequence, token)
+    for ql in (2, 7):
+        p = _params(pk, query_len=ql, max_context_len=2048, max_blocks_per_seq=128, variant=1)
+        assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(2, 8, 128, 4, 256,
+                                                                             QL=ql, variant=1)
 
 
 def test_cache_ops_reject_bad_arguments_on_the_host(pk):

@@ -169,12 +169,69 @@ def test_multi_placement_invariance_bit_exact(pk):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_multi_unsupported_shapes_are_rejected(pk):
-    """Several new tokens need the tensor-core kernel (the number of virtual
-    sequences is checked on the host, in the ABI tests)."""
-    q, kc, vc, tables, lens, torch = _case([20], 2, 8, 2, 128, seed=88)
-    with pytest.raises(pk.PagedKVError):
-        _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+# ---------------------------------------------------------------- CUDA-core kernel
+#
+# The CUDA-core variant decodes each (sequence, new token) row on its own:
+# row (b, i) streams the first L - Q + i + 1 keys, split into 512-token
+# partitions and merged like a one-token decode.
+
+CUDA_CORE_SHAPES = [(1, 8, 2), (4, 8, 3), (8, 8, 2), (4, 2, 8), (2, 4, 17)]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G,Hkv,QL", CUDA_CORE_SHAPES)
+def test_multi_cuda_core_edge_lengths(pk, D, G, Hkv, QL):
+    """Lengths from exactly Q through block and partition boundaries (511 ..
+    514 put the rows of one sequence on both sides of 512) to five partitions."""
+    lens = sorted({QL, QL + 1, 15, 16, 17, 33, 511, 512, 513, 514, 1025, 2100})
+    lens = [L for L in lens if L >= QL]
+    _check(pk, *_case(lens, QL, G * Hkv, Hkv, D, seed=500 + G * 100 + Hkv * 10 + QL + D),
+           variant=pk.DECODE_CUDA_CORE)
+
+
+def test_multi_cuda_core_rows_are_single_token_decodes_bit_exact(pk):
+    """Row (b, i) is bit for bit the one-token CUDA-core decode of query row
+    (b, i) over a sequence that ends at its token."""
+    QL = 5
+    q, kc, vc, tables, lens, torch = _case([37, 64, 515, 1030], QL, 32, 8, 128, seed=510)
+    multi = _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+    for i in range(QL):
+        li = (lens - QL + i + 1).astype(np.int32)
+        one = _decode(pk, q[:, i].contiguous(), kc, vc, tables, li, torch,
+                      variant=pk.DECODE_CUDA_CORE)
+        assert torch.equal(multi[:, i].contiguous().view(torch.int16), one.view(torch.int16))
+
+
+def test_multi_cuda_core_short_sequences_are_flagged_and_zero(pk):
+    QL = 4
+    q, kc, vc, tables, lens, torch = _case([40, 2, 0, 600], QL, 16, 4, 128, seed=511)
+    out = torch.full_like(q, 7.0)
+    pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                 max_context_len=600, out=out, variant=pk.DECODE_CUDA_CORE)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() & DEVERR_CONTEXT_LEN
+    got = harness.bf16_tensor_to_f64(out)
+    assert not got[1].any() and not got[2].any()
+    keep = [0, 3]
+    want = oracle.paged_decode_multi(q.cpu()[keep], kc.cpu(), vc.cpu(), tables[keep], lens[keep])
+    harness.assert_close(got[keep], want)
+
+
+def test_multi_cuda_core_llama70b_rows(pk):
+    """64/8 heads, two new tokens, contexts of several partitions."""
+    q, kc, vc, tables, lens, torch = _case([3000, 4097, 130], 2, 64, 8, 128, seed=512)
+    _check(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+
+
+def test_multi_cuda_core_matches_tensor_core(pk):
+    """Both kernels compute the same function: within the bf16 tolerance of
+    each other on the same inputs."""
+    q, kc, vc, tables, lens, torch = _case([100, 513, 2000], 3, 32, 8, 128, seed=513)
+    a = harness.bf16_tensor_to_f64(_decode(pk, q, kc, vc, tables, lens, torch))
+    b = harness.bf16_tensor_to_f64(_decode(pk, q, kc, vc, tables, lens, torch,
+                                           variant=pk.DECODE_CUDA_CORE))
+    d = np.abs(a - b)
+    assert d.max() <= 2e-2 and d.mean() <= 2e-3
 
 
 # ---------------------------------------------------------------- column groups
@@ -314,6 +371,46 @@ def test_multi_fused_append_matches_oracle(pk, QL):
     harness.assert_close(harness.bf16_tensor_to_f64(out), want)
 
 
+@pytest.mark.parametrize("QL", [2, 5])
+def test_multi_cuda_core_fused_append_matches_oracle(pk, QL):
+    """On the CUDA-core kernel the step's write runs first (same slot rule,
+    token L - Q + i), then the decode."""
+    lens = [600, 17, 33, 16 + QL, 1500]
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case(lens, QL, 32, 8, seed=520 + QL)
+    kc2, vc2 = kc.clone(), vc.clone()
+    out = pk.pa_append_decode(q, kc2, vc2, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
+                              torch.from_numpy(slots).cuda(), variant=pk.DECODE_CUDA_CORE)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() == 0
+    ko, vo = oracle.reshape_and_cache(kn.cpu(), vn.cpu(), oracle.bf16_bits(kc.cpu()),
+                                      oracle.bf16_bits(vc.cpu()), slots)
+    assert np.array_equal(oracle.bf16_bits(kc2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
+    want = oracle.paged_decode_multi(q.cpu(), ko, vo, tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+
+
+def test_multi_cuda_core_fused_append_slot_rules(pk):
+    QL = 3
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case([40, 70], QL, 16, 4, seed=530)
+    bad = slots.copy()
+    bad[1] = slots[1] + 1 if slots[1] % 16 != 15 else slots[1] - 1  # wrong offset
+    bad[4] = -1
+    kc2, vc2 = kc.clone(), vc.clone()
+    pk.pa_append_decode(q, kc2, vc2, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                        int(lens.max()), kn, vn, torch.from_numpy(bad).cuda(),
+                        variant=pk.DECODE_CUDA_CORE)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() & DEVERR_APPEND_SLOT
+    written = [t for t in range(len(slots)) if t not in (1, 4)]
+    ko, vo = oracle.reshape_and_cache(kn.cpu()[written], vn.cpu()[written],
+                                      oracle.bf16_bits(kc.cpu()), oracle.bf16_bits(vc.cpu()),
+                                      slots[written])
+    assert np.array_equal(oracle.bf16_bits(kc2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
+
+
 def test_multi_fused_append_slot_rules(pk):
     """A slot that is not its token's is not written (PA_DEVERR_APPEND_SLOT); a
     negative slot writes nothing; the other tokens are written."""
@@ -364,6 +461,30 @@ def test_multi_step_host_matches_device_step(pk, QL, pinned):
                                       oracle.bf16_bits(vc.cpu()), slots)
     harness.assert_close(harness.bf16_tensor_to_f64(host_out),
                          oracle.paged_decode_multi(q.cpu(), ko, vo, tables, lens))
+
+
+def test_multi_cuda_core_step_host_matches_device_step(pk):
+    """The same on the CUDA-core kernel (its write kernel, then the decode)."""
+    QL = 3
+    lens = [QL, 17, 33, 16 + QL, 600]
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case(lens, QL, 32, 8, seed=540)
+    kd, vd = kc.clone(), vc.clone()
+    want = pk.pa_append_decode(q, kd, vd, torch.from_numpy(tables).cuda(),
+                               torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
+                               torch.from_numpy(slots).cuda(), variant=pk.DECODE_CUDA_CORE)
+    torch.cuda.synchronize()
+    kh, vh = kc.clone(), vc.clone()
+    B, _, Hq, D = q.shape
+    p = pk.make_step_host_params(kh, vh, B, Hq, tables.shape[1], int(lens.max()), query_len=QL,
+                                 variant=pk.DECODE_CUDA_CORE)
+    host_in = pk.pack_step_inputs(p, q.cpu(), kn.cpu(), vn.cpu(), slots, tables, lens, pin=True)
+    host_out = torch.empty((B, QL, Hq, D), dtype=torch.bfloat16).pin_memory()
+    ws = torch.empty(pk.pa_step_host_workspace_size(p), dtype=torch.uint8, device="cuda")
+    pk.pa_step_host(p, host_in, host_out, ws)
+    assert pk.pa_device_errors() == 0
+    assert torch.equal(host_out.view(torch.int16), want.cpu().view(torch.int16))
+    assert torch.equal(kh.view(torch.int16), kd.view(torch.int16))
+    assert torch.equal(vh.view(torch.int16), vd.view(torch.int16))
 
 
 # ---------------------------------------------------------------- 8-bit cache
