@@ -190,11 +190,13 @@ typedef struct {
  *            (V^T of each (block, head) tile in sub-tiles of 16 keys; block size
  *            16 or 32)
  * Written by pa_reshape_and_cache_fp8, copied by pa_copy_blocks_fp8. The decode
- * computes on the tensor cores (variant PA_DECODE_TENSOR_CORE, head_dim 128; the
- * rest of the tensor-core shape rules apply, other shapes return
- * PA_ERR_UNSUPPORTED) with the queries and the softmax weights each split into
- * two E4M3 terms, so the result is within the bf16 tolerance of the exact decode
- * over the dequantised cache. */
+ * computes on the tensor cores (variant PA_DECODE_TENSOR_CORE, head_dim 128 and
+ * the rest of the tensor-core shape rules) with the queries and the softmax
+ * weights each split into two E4M3 terms, or on CUDA cores (variant
+ * PA_DECODE_CUDA_CORE and shapes the tensor-core kernel does not take; head_dim
+ * 64 or 128, block size 16) with the codes dequantised in fp32; either result is
+ * within the bf16 tolerance of the exact decode over the dequantised cache.
+ * Other shapes return PA_ERR_UNSUPPORTED. */
 #define PA_KV_BF16 0
 #define PA_KV_FP8_E4M3 1
 

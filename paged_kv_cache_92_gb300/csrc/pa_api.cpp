@@ -76,10 +76,11 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
                      "(the tensor-core kernel takes num_kv_heads 1/2/4/8 and num_seqs * "
                      "(query_len split into column groups) <= 16384)");
   if (p->kv_dtype == PA_KV_FP8_E4M3) {
-    if (p->head_dim != 128 || p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p))
+    if (!decode_uses_tc(p) && p->block_size != kBlockSize)
       return set_error(PA_ERR_UNSUPPORTED,
-                       "pa_decode: the 8-bit cache runs on the tensor-core kernel with head_dim "
-                       "128, num_kv_heads 1/2/4/8, num_q_heads <= 64");
+                       "pa_decode: the 8-bit cache runs on the tensor-core kernel (head_dim 128, "
+                       "num_kv_heads 1/2/4/8, block size 16 or 32) or on the CUDA-core kernel "
+                       "(head_dim 64 or 128, block size 16)");
     if (need_pointers && p->num_seqs > 0 &&
         (!p->k_scale || !p->v_scale || (reinterpret_cast<uintptr_t>(p->k_scale) & 3u) ||
          (reinterpret_cast<uintptr_t>(p->v_scale) & 3u)))
@@ -189,12 +190,13 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
     L.part_l = reinterpret_cast<float*>(ws + w.tc_l);
     L.part_acc = reinterpret_cast<float*>(ws + w.tc_acc);
     e = launch_decode_tc(L, stream);
-  } else if (p->kv_dtype == PA_KV_FP8_E4M3) {
-    return set_error(PA_ERR_UNSUPPORTED, "the 8-bit cache needs the tensor-core kernel");
   } else if (p->block_size != kBlockSize) {
     return set_error(PA_ERR_UNSUPPORTED, "block sizes other than 16 need the tensor-core kernel");
   } else {
-    if (append) {  // the same effect in two launches
+    if (append && p->kv_dtype == PA_KV_FP8_E4M3) {
+      // the quantising write with the fused path's slot rule, then the decode
+      e = launch_quantize_q(nullptr, nullptr, nullptr, query_map(p), p, append, stream);
+    } else if (append) {  // the same effect in two launches
       AppendCheck chk;
       chk.block_tables = p->block_tables;
       chk.context_lens = p->context_lens;

@@ -33,6 +33,12 @@
 //    workspace, combined by the merge kernel (log-sum-exp).
 //  * The reduction order depends only on logical token positions, so results
 //    are bit-identical under any physical block placement.
+//  * The 8-bit (E4M3) cache ("PagedAttention" glossary page, §What paging
+//    costs): K rows are read as 8-byte chunks of codes, dequantised on the
+//    fly with the head's K scale folded into the query; each (block, head)
+//    V^T tile ([D][16] codes) is transposed in shared memory into V rows,
+//    which the value loop reads like K, and the head's V scale multiplies the
+//    weighted sum before the normalisation.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -53,29 +59,49 @@ constexpr int NWARPS = 4;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, int G>
+template <int D, int G, bool F8>
 struct Cfg {
   // dims per lane: keep the per-lane query registers (DPL * G) at 64.
   static constexpr int DPL = (D >= 128 && G <= 4) ? 16 : 8;
   static constexpr int LPT = D / DPL;    // lanes per token
   static constexpr int TPI = 32 / LPT;   // tokens per warp step
   static constexpr int NIT = BS / TPI;   // warp steps per block
-  static constexpr int CHUNKS = DPL / 8; // 16-byte chunks per lane per row
+  static constexpr int CHUNKS = DPL / 8; // 8-element chunks per lane per row
+  static constexpr int EB = F8 ? 1 : 2;  // bytes per cache element
   static constexpr int HSTRIDE = LPT / G;  // lanes between heads after the reduce-scatter
-  static constexpr int TILE = BS * D * 2;  // bytes of one (block, KV head) tile
+  static constexpr int TILE = BS * D * EB;  // bytes of one (block, KV head) tile
   static constexpr int ST = (D >= 128) ? 3 : 4;  // ring stages per warp
+  // 8-bit: each warp's V rows, transposed from the V^T tile of its block
+  static constexpr int VROWS = F8 ? BS * D : 0;
   static_assert(G <= LPT, "each head needs a lane after the reduce-scatter");
   static_assert(BS % TPI == 0, "tokens per step must divide the block");
 };
 
-template <int D, int G>
+template <int D, int G, bool F8>
 constexpr size_t decode_smem_bytes(int partition_tokens) {
-  using C = Cfg<D, G>;
-  size_t tiles = size_t(NWARPS) * C::ST * 2 * C::TILE;
+  using C = Cfg<D, G, F8>;
+  size_t tiles = size_t(NWARPS) * (C::ST * 2 * C::TILE + C::VROWS);
   size_t merge = size_t(NWARPS) * G * (D + 2) * sizeof(float);
   if (merge > tiles) tiles = merge;
   return tiles + size_t(NWARPS) * C::ST * sizeof(uint64_t) +
          size_t(partition_tokens / BS) * sizeof(int32_t);
+}
+
+// 8 consecutive elements of a row in shared memory as floats: bf16 (16 bytes)
+// or E4M3 codes (8 bytes).
+template <bool F8>
+__device__ __forceinline__ void load_row8(const unsigned char* p, float (&f)[8]) {
+  if constexpr (F8) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = dev::from_e4m3x2(((i < 2 ? raw.x : raw.y) >> (16 * (i & 1))) & 0xffffu);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  } else {
+    dev::unpack8(*reinterpret_cast<const uint4*>(p), f);
+  }
 }
 
 // Sum G values over the LPT lanes of a token group, scattering heads: on
@@ -103,17 +129,18 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int lane) {
   return v[0];
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(NTHREADS)
     paged_decode_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out,
-                        const __nv_bfloat16* __restrict__ k_cache,
-                        const __nv_bfloat16* __restrict__ v_cache,
+                        const unsigned char* __restrict__ k_cache,
+                        const unsigned char* __restrict__ v_cache,
+                        const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                         const int32_t* __restrict__ block_tables,
                         const int32_t* __restrict__ context_lens, int max_blocks_per_seq,
                         int num_kv_heads, int num_blocks, int max_context_len, float scale_log2,
                         int partition_tokens, int num_partitions, float* __restrict__ part_m,
                         float* __restrict__ part_l, float* __restrict__ part_acc, int q_len) {
-  using C = Cfg<D, G>;
+  using C = Cfg<D, G, F8>;
   constexpr int ST = C::ST;
   const int part = blockIdx.x;
   const int g = blockIdx.y;
@@ -151,7 +178,7 @@ __global__ void __launch_bounds__(NTHREADS)
   const bool split = L > partition_tokens;
 
   extern __shared__ __align__(128) unsigned char smem[];
-  size_t tiles_bytes = size_t(NWARPS) * ST * 2 * C::TILE;
+  size_t tiles_bytes = size_t(NWARPS) * (ST * 2 * C::TILE + C::VROWS);
   {
     const size_t merge = size_t(NWARPS) * G * (D + 2) * sizeof(float);
     if (merge > tiles_bytes) tiles_bytes = merge;
@@ -178,14 +205,15 @@ __global__ void __launch_bounds__(NTHREADS)
   __syncthreads();
 
   const int n_my = nblk > warp ? (nblk - warp + NWARPS - 1) / NWARPS : 0;
-  unsigned char* my_tiles = tiles + size_t(warp) * ST * 2 * C::TILE;
-  const size_t head_tile_elems = size_t(BS) * D;
+  unsigned char* my_tiles = tiles + size_t(warp) * (ST * 2 * C::TILE + C::VROWS);
+  unsigned char* my_vrows = my_tiles + ST * 2 * C::TILE;  // 8-bit: [BS][D] codes
+  const size_t head_tile_bytes = size_t(C::TILE);
   const uint64_t policy = dev::l2_evict_first_policy();
 
   auto issue = [&](int i) {
     const int s = i % ST;
     const int32_t blk = table[warp + NWARPS * i];
-    const size_t off = (size_t(blk) * num_kv_heads + g) * head_tile_elems;
+    const size_t off = (size_t(blk) * num_kv_heads + g) * head_tile_bytes;
     dev::mbar_arrive_expect_tx(&my_bars[s], 2 * C::TILE);
     dev::bulk_load(my_tiles + size_t(s) * 2 * C::TILE, k_cache + off, C::TILE, &my_bars[s], policy);
     dev::bulk_load(my_tiles + size_t(s) * 2 * C::TILE + C::TILE, v_cache + off, C::TILE,
@@ -195,9 +223,11 @@ __global__ void __launch_bounds__(NTHREADS)
     for (int i = 0; i < ST && i < n_my; ++i) issue(i);
   }
 
-  // Query slice of this lane, prescaled by scale*log2(e): qf[h][k*8+e].
+  // Query slice of this lane, prescaled by scale*log2(e) (and, 8-bit, the
+  // head's K scale): qf[h][k*8+e].
   const int dl = lane % C::LPT;
   const int tg = lane / C::LPT;
+  const float qscale = F8 ? scale_log2 * k_scale[g] : scale_log2;
   float qf[G][C::DPL];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -208,7 +238,7 @@ __global__ void __launch_bounds__(NTHREADS)
       float f[8];
       dev::unpack8(qrow[dl + C::LPT * k], f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qf[h][k * 8 + e] = f[e] * scale_log2;
+      for (int e = 0; e < 8; ++e) qf[h][k * 8 + e] = f[e] * qscale;
     }
   }
 
@@ -230,6 +260,31 @@ __global__ void __launch_bounds__(NTHREADS)
     }
     const unsigned char* kt = my_tiles + size_t(s) * 2 * C::TILE;
     const unsigned char* vt = kt + C::TILE;
+    if constexpr (F8) {
+      // V^T [D][16 keys] -> V rows [16 keys][D]: lane l takes V^T rows
+      // RPL*l .. RPL*l + RPL-1 and stores, per key, their RPL codes together.
+      constexpr int RPL = D / 32;
+      uint4 r[RPL];
+#pragma unroll
+      for (int j = 0; j < RPL; ++j)
+        r[j] = *reinterpret_cast<const uint4*>(vt + (RPL * lane + j) * 16);
+#pragma unroll
+      for (int t = 0; t < BS; ++t) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int j = 0; j < RPL; ++j) {
+          const uint32_t word = reinterpret_cast<const uint32_t*>(&r[j])[t >> 2];
+          w |= ((word >> ((t & 3) * 8)) & 0xffu) << (8 * j);
+        }
+        if constexpr (RPL == 4) {
+          *reinterpret_cast<uint32_t*>(my_vrows + t * D + RPL * lane) = w;
+        } else {
+          *reinterpret_cast<uint16_t*>(my_vrows + t * D + RPL * lane) = uint16_t(w);
+        }
+      }
+      __syncwarp();
+    }
+    const unsigned char* vrows = F8 ? my_vrows : vt;
     const int t_base = (lblk0 + warp + NWARPS * i) * BS;
     const bool partial = t_base + BS > L;
 
@@ -242,10 +297,8 @@ __global__ void __launch_bounds__(NTHREADS)
       for (int h = 0; h < G; ++h) part_dot[h] = 0.0f;
 #pragma unroll
       for (int k = 0; k < C::CHUNKS; ++k) {
-        const uint4 raw =
-            *reinterpret_cast<const uint4*>(kt + size_t(t) * D * 2 + (dl + C::LPT * k) * 16);
         float f[8];
-        dev::unpack8(raw, f);
+        load_row8<F8>(kt + (size_t(t) * D + (dl + C::LPT * k) * 8) * C::EB, f);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
 #pragma unroll
@@ -282,11 +335,12 @@ __global__ void __launch_bounds__(NTHREADS)
       const bool masked = partial && t_base + t >= L;
 #pragma unroll
       for (int k = 0; k < C::CHUNKS; ++k) {
-        uint4 raw =
-            *reinterpret_cast<const uint4*>(vt + size_t(t) * D * 2 + (dl + C::LPT * k) * 16);
-        if (masked) raw = make_uint4(0u, 0u, 0u, 0u);
         float f[8];
-        dev::unpack8(raw, f);
+        load_row8<F8>(vrows + (size_t(t) * D + (dl + C::LPT * k) * 8) * C::EB, f);
+        if (masked) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = 0.0f;
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e)
 #pragma unroll
@@ -354,6 +408,7 @@ __global__ void __launch_bounds__(NTHREADS)
       num = fmaf(wt, sm_acc[(w * G + h) * D + d], num);
       den = fmaf(wt, sm_l[w * G + h], den);
     }
+    if constexpr (F8) num *= v_scale[g];  // the head's V dequantisation scale
     const size_t row = size_t(z) * num_q_heads + g * G + h;
     if (!split) {
       out[row * D + d] = __float2bfloat16_rn(num * __frcp_rn(den));
@@ -420,13 +475,13 @@ __global__ void __launch_bounds__(128)
   for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(acc[j] * inv);
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 int launch_decode_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   const pa_decode_params* p = Lc.p;
-  const size_t smem = decode_smem_bytes<D, G>(Lc.partition_tokens);
+  const size_t smem = decode_smem_bytes<D, G, F8>(Lc.partition_tokens);
   static size_t configured = 0;
   if (configured < smem) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, G, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return int(e);
     configured = smem;
@@ -434,10 +489,10 @@ int launch_decode_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   const int q_len = query_len_of(p);
   dim3 grid(Lc.num_partitions, p->num_kv_heads, p->num_seqs * q_len);
   const float scale_log2 = p->scale * kLog2e;
-  paged_decode_kernel<D, G><<<grid, NTHREADS, smem, stream>>>(
+  paged_decode_kernel<D, G, F8><<<grid, NTHREADS, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(p->q), static_cast<__nv_bfloat16*>(p->out),
-      static_cast<const __nv_bfloat16*>(p->k_cache), static_cast<const __nv_bfloat16*>(p->v_cache),
-      p->block_tables, p->context_lens, p->max_blocks_per_seq, p->num_kv_heads, p->num_blocks,
+      static_cast<const unsigned char*>(p->k_cache), static_cast<const unsigned char*>(p->v_cache),
+      p->k_scale, p->v_scale, p->block_tables, p->context_lens, p->max_blocks_per_seq, p->num_kv_heads, p->num_blocks,
       p->max_context_len, scale_log2, Lc.partition_tokens, Lc.num_partitions, Lc.part_m, Lc.part_l,
       Lc.part_acc, q_len);
   return int(cudaGetLastError());
@@ -455,13 +510,13 @@ int launch_merge_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   return int(cudaGetLastError());
 }
 
-template <int D>
+template <int D, bool F8>
 int dispatch_group(const DecodeLaunch& Lc, cudaStream_t s) {
   switch (Lc.p->num_q_heads / Lc.p->num_kv_heads) {
-    case 1: return launch_decode_t<D, 1>(Lc, s);
-    case 2: return launch_decode_t<D, 2>(Lc, s);
-    case 4: return launch_decode_t<D, 4>(Lc, s);
-    case 8: return launch_decode_t<D, 8>(Lc, s);
+    case 1: return launch_decode_t<D, 1, F8>(Lc, s);
+    case 2: return launch_decode_t<D, 2, F8>(Lc, s);
+    case 4: return launch_decode_t<D, 4, F8>(Lc, s);
+    case 8: return launch_decode_t<D, 8, F8>(Lc, s);
     default: return int(cudaErrorInvalidValue);
   }
 }
@@ -470,9 +525,10 @@ int dispatch_group(const DecodeLaunch& Lc, cudaStream_t s) {
 
 int launch_decode(const DecodeLaunch& Lc, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool f8 = Lc.p->kv_dtype == PA_KV_FP8_E4M3;
   switch (Lc.p->head_dim) {
-    case 64: return dispatch_group<64>(Lc, s);
-    case 128: return dispatch_group<128>(Lc, s);
+    case 64: return f8 ? dispatch_group<64, true>(Lc, s) : dispatch_group<64, false>(Lc, s);
+    case 128: return f8 ? dispatch_group<128, true>(Lc, s) : dispatch_group<128, false>(Lc, s);
     default: return int(cudaErrorInvalidValue);
   }
 }

@@ -12,6 +12,7 @@ bool tc_supports(const pa_decode_params* p) {
   if (!(H == 1 || H == 2 || H == 4 || H == 8) || !(G == 1 || G == 2 || G == 4 || G == 8))
     return false;
   const bool fp8 = p->kv_dtype == PA_KV_FP8_E4M3;
+  if (fp8 && p->head_dim != 128) return false;  // (the CUDA-core kernel takes head_dim 64)
   if (p->block_size != 16) {  // block sizes 8 and 32: bf16 head_dim 64 or 128, the
                               // 8-bit cache at 32 only (head_dim 128)
     if ((p->head_dim != 128 && p->head_dim != 64) || (p->block_size == 8 && fp8)) return false;

@@ -244,7 +244,7 @@ int launch_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_c
 
 int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap& m,
                       const pa_decode_params* p, const pa_append_params* ap, void* stream) {
-  if (m.head_dim != 128) return int(cudaErrorInvalidValue);
+  if (q != nullptr && m.head_dim != 128) return int(cudaErrorInvalidValue);
   Fp8Append a = {};
   if (ap) {
     a.k_new = static_cast<const uint4*>(ap->k_new);
@@ -266,7 +266,7 @@ int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap&
     a.num_chunks = int64_t(m.num_real_seqs) * m.query_len * p->num_kv_heads * (p->head_dim / 8);
     a.early = p->overlap_prologue ? 1 : 0;
   }
-  const int64_t q_blocks = (int64_t(m.num_seqs) * m.n_pad + 3) / 4;
+  const int64_t q_blocks = q != nullptr ? (int64_t(m.num_seqs) * m.n_pad + 3) / 4 : 0;
   const int64_t w_blocks = (a.num_chunks + 127) / 128;
   if (q_blocks + w_blocks == 0) return int(cudaSuccess);
   // a programmatic dependent of the previous kernel on the stream (it waits

@@ -198,7 +198,8 @@ int launch_permute_q(const void* q, void* qp, const QueryMap& m, void* stream);
 // two E4M3 terms in the column layout ([B][2*n_pad][D] bytes, hi rows then lo
 // rows, and [B][n_pad] floats 1/alpha), and -- with `append` (pa_append_decode)
 // -- the quantising KV write of the step's new tokens, checked against their
-// positions like the fused bf16 write.
+// positions like the fused bf16 write. With q == nullptr only the write runs
+// (the CUDA-core decode of the 8-bit cache).
 int launch_quantize_q(const void* q, void* q8, float* inv_alpha, const QueryMap& m,
                       const pa_decode_params* p, const pa_append_params* append, void* stream);
 // Copy `bytes` from src -- host memory the GPU can address (pinned, mapped

@@ -65,7 +65,10 @@ def _params(pk, **kw):
     (dict(block_size=32), 1),  # block size 32: tensor-core kernel, valid shapes, NULL pointers
     (dict(block_size=8), 1),
     (dict(block_size=32, head_dim=64), 1),  # block sizes 8 and 32 at head_dim 64: bf16
-    (dict(block_size=8, head_dim=64, kv_dtype=1), 2),  # the 8-bit cache: head_dim 128
+    (dict(block_size=8, head_dim=64, kv_dtype=1), 2),  # the 8-bit cache: not at block size 8
+    (dict(kv_dtype=1, variant=1), 1),  # ... on the CUDA-core kernel (NULL pointers)
+    (dict(kv_dtype=1, head_dim=64), 1),  # ... head_dim 64 there
+    (dict(kv_dtype=1, variant=1, block_size=32), 2),  # ... block size 16 there
     (dict(block_size=8, variant=1), 2),  # ... and the tensor-core kernel only
     (dict(block_size=8, query_len=4), 1),  # block size 8: column groups of 8 per KV head
     (dict(block_size=8, kv_dtype=1), 2),  # the 8-bit cache: block size 16 or 32

@@ -38,19 +38,19 @@ def _scales(Hkv, seed, base):
     return (base * np.exp(rng.uniform(-0.5, 0.5, size=Hkv))).astype(np.float32)
 
 
-def _fp8_case(pk, lens, Hq, Hkv, seed, extra_blocks=3):
+def _fp8_case(pk, lens, Hq, Hkv, seed, extra_blocks=3, D=128, QL=1):
     """Random tables; every slot of the pool written through
     pa_reshape_and_cache_fp8 (bf16 N(0,1) rows, per-head scales); padding
     slots of each sequence's last block then set to the NaN code."""
     import torch
 
-    D = 128
     lens = np.asarray(lens, dtype=np.int64)
     need = int(((lens + 15) // 16).sum())
     NB = need + extra_blocks
     order = np.random.default_rng(seed).permutation(NB).astype(np.int32)
     tables = workloads.sequential_tables(lens, order, 16)
-    q = workloads.bf16_normal((len(lens), Hq, D), seed + 1, "cuda")
+    q = workloads.bf16_normal((len(lens), QL, Hq, D) if QL > 1 else (len(lens), Hq, D), seed + 1,
+                              "cuda")
     kn = workloads.bf16_normal((NB * 16, Hkv, D), seed + 2, "cuda")
     vn = workloads.bf16_normal((NB * 16, Hkv, D), seed + 3, "cuda")
     ks = torch.from_numpy(_scales(Hkv, seed + 4, 0.05)).cuda()
@@ -208,20 +208,103 @@ def test_fp8_decode_placement_invariance_bit_exact(pk):
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
 
-def test_fp8_unsupported_shapes_are_rejected(pk):
+# ---------------------------------------------------------------- the CUDA-core kernel
+#
+# The CUDA-core variant dequantises the codes in fp32: K rows with the head's
+# scale folded into the query, V from each V^T tile transposed in shared
+# memory, the V scale on the weighted sum. Same oracle, same bar.
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G,Hkv", [(1, 8), (4, 8), (8, 8), (2, 1), (4, 4), (8, 2)])
+def test_fp8_cuda_core_edge_lengths(pk, D, G, Hkv):
+    lens = [1, 15, 16, 17, 100, 511, 512, 513, 1025, 1600]
+    case = _fp8_case(pk, lens, Hq=G * Hkv, Hkv=Hkv, seed=600 + G * 10 + Hkv + D, D=D)
+    _decode_and_check(pk, case, variant=pk.DECODE_CUDA_CORE)
+
+
+def test_fp8_cuda_core_matches_tensor_core(pk):
     import torch
 
-    case = _fp8_case(pk, [20], Hq=8, Hkv=2, seed=55)
+    case = _fp8_case(pk, [40, 700, 2049], Hq=32, Hkv=8, seed=610)
     q, k8, v8, ks, vs, tables, lens = case
-    with pytest.raises(pk.PagedKVError):
+    outs = [harness.bf16_tensor_to_f64(
         pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
-                     max_context_len=20, k_scale=ks, v_scale=vs, variant=pk.DECODE_CUDA_CORE)
+                     max_context_len=2049, k_scale=ks, v_scale=vs, variant=v))
+        for v in (pk.DECODE_TENSOR_CORE, pk.DECODE_CUDA_CORE)]
+    d = np.abs(outs[0] - outs[1])
+    assert d.max() <= 2e-2 and d.mean() <= 2e-3
+
+
+def test_fp8_cuda_core_zero_length_rows_are_zero(pk):
+    import torch
+
+    case = _fp8_case(pk, [40, 0, 3, 0, 600], Hq=8, Hkv=2, seed=611)
+    q, k8, v8, ks, vs, tables, lens = case
+    out = torch.full_like(q, 7.0)
+    pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                 max_context_len=600, k_scale=ks, v_scale=vs, out=out,
+                 variant=pk.DECODE_CUDA_CORE)
+    torch.cuda.synchronize()
+    got = harness.bf16_tensor_to_f64(out)
+    assert not got[1].any() and not got[3].any()
+    keep = [0, 2, 4]
+    want = oracle.paged_decode_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy(), ks.cpu().numpy(),
+                                   vs.cpu().numpy(), tables, lens,
+                                   units=[(b, h) for b in keep for h in range(8)])
+    harness.assert_close(np.concatenate([got[b] for b in keep]), want)
+
+
+def test_fp8_cuda_core_placement_invariance_bit_exact(pk):
+    import torch
+
+    q, k8, v8, ks, vs, tables, lens = _fp8_case(pk, [300, 47, 900], Hq=16, Hkv=4, seed=612)
+    NB = k8.shape[0]
+    perm = np.random.default_rng(19).permutation(NB)
+    k8b, v8b = torch.empty_like(k8), torch.empty_like(v8)
+    k8b[torch.from_numpy(perm).cuda()] = k8
+    v8b[torch.from_numpy(perm).cuda()] = v8
+    tables_b = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    outs = [pk.pa_decode(q, kc, vc, torch.from_numpy(tb).cuda(), torch.from_numpy(lens).cuda(),
+                         max_context_len=900, k_scale=ks, v_scale=vs, variant=pk.DECODE_CUDA_CORE)
+            for kc, vc, tb in ((k8, v8, tables), (k8b, v8b, tables_b))]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_fp8_cuda_core_several_new_tokens(pk):
+    import torch
+
+    QL = 3
+    q, k8, v8, ks, vs, tables, lens = _fp8_case(pk, [QL, 17, 513, 1100], Hq=32, Hkv=8, seed=613,
+                                                QL=QL)
+    out = pk.pa_decode(q, k8, v8, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                       max_context_len=1100, k_scale=ks, v_scale=vs, variant=pk.DECODE_CUDA_CORE)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() == 0
+    want = oracle.paged_decode_multi_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy(),
+                                         ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+
+
+def test_fp8_cuda_core_block_size_32_is_rejected(pk):
+    import torch
+
+    D, NB, Hkv = 128, 4, 2
+    q = torch.zeros((1, 8, D), dtype=torch.bfloat16, device="cuda")
+    k8 = torch.zeros((NB, Hkv, 32, D), dtype=torch.uint8, device="cuda")
+    v8 = torch.zeros((NB, Hkv, 2, D, 16), dtype=torch.uint8, device="cuda")
+    ks = torch.ones((Hkv,), dtype=torch.float32, device="cuda")
+    with pytest.raises(pk.PagedKVError):
+        pk.pa_decode(q, k8, v8, torch.zeros((1, 2), dtype=torch.int32, device="cuda"),
+                     torch.full((1,), 20, dtype=torch.int32, device="cuda"), max_context_len=20,
+                     k_scale=ks, v_scale=ks, variant=pk.DECODE_CUDA_CORE)
 
 
 # ---------------------------------------------------------------- the write fused into the decode
 
 
-def _fused_fp8(pk, lens, Hq, Hkv, seed, QL=1, bad=None, bs=16):
+def _fused_fp8(pk, lens, Hq, Hkv, seed, QL=1, bad=None, bs=16, variant=0):
     """pa_append_decode on the 8-bit cache: the new tokens' (the last QL of each
     sequence) slots are overwritten with the quantised rows of k_new/v_new, as
     pa_reshape_and_cache_fp8 would, before the decode reads them."""
@@ -264,17 +347,20 @@ def _fused_fp8(pk, lens, Hq, Hkv, seed, QL=1, bad=None, bs=16):
     k8, v8 = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
     out = pk.pa_append_decode(q, k8, v8, torch.from_numpy(tables).cuda(),
                               torch.from_numpy(lens.astype(np.int32)).cuda(), int(lens.max()),
-                              kn, vn, torch.from_numpy(slots).cuda(), k_scale=ks, v_scale=vs)
+                              kn, vn, torch.from_numpy(slots).cuda(), k_scale=ks, v_scale=vs,
+                              variant=variant)
     torch.cuda.synchronize()
     return dict(q=q, k0=k0, v0=v0, k8=k8, v8=v8, kn=kn, vn=vn, ks=ks, vs=vs, slots=slots,
                 tables=tables, lens=lens.astype(np.int32), out=out, NB=NB, Hkv=Hkv, bs=bs)
 
 
-@pytest.mark.parametrize("bs", [16, 32])
-@pytest.mark.parametrize("QL", [1, 2])
-def test_fp8_fused_append_matches_the_quantising_write_and_oracle(pk, bs, QL):
+@pytest.mark.parametrize("bs,QL,variant", [(16, 1, 0), (16, 2, 0), (32, 1, 0), (32, 2, 0),
+                                           (16, 1, 1), (16, 3, 1)])
+def test_fp8_fused_append_matches_the_quantising_write_and_oracle(pk, bs, QL, variant):
+    """variant 1: the CUDA-core kernel (the preparation launch's write, then the decode)."""
     lens = [QL, 15, 16, 17, 33, 100, 513, 2049]
-    c = _fused_fp8(pk, lens, 32, 8, seed=60 + bs + QL, QL=QL, bs=bs)
+    c = _fused_fp8(pk, lens, 32, 8, seed=60 + bs + QL + 7 * variant, QL=QL, bs=bs,
+                   variant=variant)
     assert pk.pa_device_errors() == 0
     NB, Hkv, D = c["NB"], c["Hkv"], 128
     ks, vs = c["ks"].cpu().numpy(), c["vs"].cpu().numpy()
@@ -289,7 +375,8 @@ def test_fp8_fused_append_matches_the_quantising_write_and_oracle(pk, bs, QL):
     harness.assert_close(harness.bf16_tensor_to_f64(c["out"]), want)
 
 
-def test_fp8_fused_append_slot_rules(pk):
+@pytest.mark.parametrize("variant", [0, 1])
+def test_fp8_fused_append_slot_rules(pk, variant):
     """A slot that is not its token's is not written (PA_DEVERR_APPEND_SLOT); a
     negative slot writes nothing."""
     def bad(s):
@@ -298,7 +385,7 @@ def test_fp8_fused_append_slot_rules(pk):
         s[2] = -1
         return s
 
-    c = _fused_fp8(pk, [40, 70, 33], 16, 4, seed=71, bad=bad)
+    c = _fused_fp8(pk, [40, 70, 33], 16, 4, seed=71, bad=bad, variant=variant)
     assert pk.pa_device_errors() & 0x20
     NB, Hkv, D = c["NB"], c["Hkv"], 128
     keep = [0]
