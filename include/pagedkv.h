@@ -56,9 +56,10 @@
  *
  * Supported shapes: block_size 8, 16 or 32 ("Paged Attention as a Memory
  * Manager", §PagedAttention: a compile-time constant, typically 8, 16 or 32);
- * head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}. Block sizes
- * 8 and 32 decode on the tensor-core kernel (the 8-bit cache: head_dim 128 and
- * block size 16 or 32). Anything else returns PA_ERR_UNSUPPORTED.
+ * head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}. Both decode
+ * kernels take every block size (the tensor-core kernel's 8-bit cache: head_dim
+ * 128 and block size 16 or 32; the 8-bit cache at block size 8 decodes on the
+ * CUDA-core kernel). Anything else returns PA_ERR_UNSUPPORTED.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -132,8 +133,8 @@ typedef struct {
   int32_t num_blocks;
   int32_t max_context_len;     /* host-known upper bound of every context_lens[b] (>= 1) */
   float scale;                 /* softmax scale, normally 1/sqrt(head_dim) */
-  int32_t partition_tokens;    /* split-K partition length; 0 = 512; else a multiple of
-                                  block_size in [block_size, 4096] */
+  int32_t partition_tokens;    /* split-K partition length; 0 = 512; else a multiple of 16 in
+                                  [16, 4096], and on the CUDA-core kernel of block_size too */
   int32_t variant;             /* PA_DECODE_TENSOR_CORE (default) or PA_DECODE_CUDA_CORE */
   int32_t overlap_prologue;    /* nonzero: context_lens and block_tables were final before the
                                   previous kernel on `stream` began (e.g. uploaded once per step),
@@ -186,15 +187,15 @@ typedef struct {
  * block; the format is this library's reading): OCP E4M3 codes (uint8) with one
  * dequantisation scale per KV head for K and for V.
  *   k_cache  uint8 [num_blocks][num_kv_heads][block_size][head_dim]
- *   v_cache  uint8 [num_blocks][num_kv_heads][block_size/16][head_dim][16]
- *            (V^T of each (block, head) tile in sub-tiles of 16 keys; block size
- *            16 or 32)
+ *   v_cache  uint8 [num_blocks][num_kv_heads][block_size/W][head_dim][W],
+ *            W = min(block_size, 16) (V^T of each (block, head) tile in
+ *            sub-tiles of W keys)
  * Written by pa_reshape_and_cache_fp8, copied by pa_copy_blocks_fp8. The decode
  * computes on the tensor cores (variant PA_DECODE_TENSOR_CORE, head_dim 128 and
  * the rest of the tensor-core shape rules) with the queries and the softmax
  * weights each split into two E4M3 terms, or on CUDA cores (variant
- * PA_DECODE_CUDA_CORE and shapes the tensor-core kernel does not take; head_dim
- * 64 or 128, block size 16) with the codes dequantised in fp32; either result is
+ * PA_DECODE_CUDA_CORE and shapes the tensor-core kernel does not take: head_dim
+ * 64, block size 8) with the codes dequantised in fp32; either result is
  * within the bf16 tolerance of the exact decode over the dequantised cache.
  * Other shapes return PA_ERR_UNSUPPORTED. */
 #define PA_KV_BF16 0

@@ -477,18 +477,19 @@ def pa_copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
 
 
 def fp8_v_shapes(NB: int, Hkv: int, BS: int, D: int):
-    """Shapes accepted for the 8-bit V^T cache: [NB][Hkv][BS/16][D][16] (16-key
-    sub-tiles), and for block size 16 also [NB][Hkv][D][16]."""
-    shapes = [(NB, Hkv, BS // 16, D, 16)]
-    if BS == 16:
-        shapes.append((NB, Hkv, D, 16))
+    """Shapes accepted for the 8-bit V^T cache: [NB][Hkv][BS/W][D][W] (sub-tiles
+    of W = min(BS, 16) keys), and up to block size 16 also [NB][Hkv][D][W]."""
+    W = min(BS, 16)
+    shapes = [(NB, Hkv, BS // W, D, W)]
+    if BS <= 16:
+        shapes.append((NB, Hkv, D, W))
     return shapes
 
 
 def pa_reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale, v_scale,
                              stream=None) -> None:
-    """KV write into the 8-bit cache (uint8 K [NB][Hkv][BS][D], V^T in 16-key
-    sub-tiles [NB][Hkv][BS/16][D][16])."""
+    """KV write into the 8-bit cache (uint8 K [NB][Hkv][BS][D], V^T in sub-tiles
+    of W = min(BS, 16) keys, [NB][Hkv][BS/W][D][W])."""
     import torch
 
     T, Hkv, D = k_new.shape

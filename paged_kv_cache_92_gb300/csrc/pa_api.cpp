@@ -65,10 +65,11 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: wait_timeout_us must be >= 0");
   if (int64_t(p->num_seqs) * query_len_of(p) * p->num_q_heads >= (int64_t(1) << 31) - 16)
     return set_error(PA_ERR_INVALID_ARG, "pa_decode: query rows exceed 2^31");
-  if (p->block_size != kBlockSize && (p->variant != PA_DECODE_TENSOR_CORE || !tc_supports(p)))
-    return set_error(PA_ERR_UNSUPPORTED,
-                     "pa_decode: block_size 8 and 32 run on the tensor-core kernel (head_dim 64 "
-                     "or 128, num_kv_heads 1/2/4/8; block_size 8: the bf16 cache only)");
+  // the CUDA-core kernel's partitions are whole blocks
+  if (!decode_uses_tc(p) && pt % p->block_size != 0)
+    return set_error(PA_ERR_INVALID_ARG,
+                     "pa_decode: on the CUDA-core kernel partition_tokens must be a multiple of "
+                     "block_size");
   // the CUDA-core kernel runs one CTA row per (sequence, new token) in grid z
   if (!decode_uses_tc(p) && int64_t(p->num_seqs) * query_len_of(p) > 65535)
     return set_error(PA_ERR_UNSUPPORTED,
@@ -76,11 +77,6 @@ pa_status check_decode(const pa_decode_params* p, bool need_pointers) {
                      "(the tensor-core kernel takes num_kv_heads 1/2/4/8 and num_seqs * "
                      "(query_len split into column groups) <= 16384)");
   if (p->kv_dtype == PA_KV_FP8_E4M3) {
-    if (!decode_uses_tc(p) && p->block_size != kBlockSize)
-      return set_error(PA_ERR_UNSUPPORTED,
-                       "pa_decode: the 8-bit cache runs on the tensor-core kernel (head_dim 128, "
-                       "num_kv_heads 1/2/4/8, block size 16 or 32) or on the CUDA-core kernel "
-                       "(head_dim 64 or 128, block size 16)");
     if (need_pointers && p->num_seqs > 0 &&
         (!p->k_scale || !p->v_scale || (reinterpret_cast<uintptr_t>(p->k_scale) & 3u) ||
          (reinterpret_cast<uintptr_t>(p->v_scale) & 3u)))
@@ -190,8 +186,6 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
     L.part_l = reinterpret_cast<float*>(ws + w.tc_l);
     L.part_acc = reinterpret_cast<float*>(ws + w.tc_acc);
     e = launch_decode_tc(L, stream);
-  } else if (p->block_size != kBlockSize) {
-    return set_error(PA_ERR_UNSUPPORTED, "block sizes other than 16 need the tensor-core kernel");
   } else {
     if (append && p->kv_dtype == PA_KV_FP8_E4M3) {
       // the quantising write with the fused path's slot rule, then the decode
@@ -565,8 +559,8 @@ pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k
     return pa::set_error(PA_ERR_INVALID_ARG,
                          "pa_reshape_and_cache_fp8: num_tokens >= 0, num_kv_heads >= 1, "
                          "num_blocks >= 1");
-  if (block_size != 16 && block_size != 32)
-    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache_fp8: block_size 16 or 32");
+  if (!pa::block_size_ok(block_size))
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache_fp8: block_size 8, 16 or 32");
   if (head_dim < 8 || head_dim % 8 != 0 || head_dim > 1024)
     return pa::set_error(PA_ERR_UNSUPPORTED,
                          "pa_reshape_and_cache_fp8: head_dim must be a multiple of 8 in [8, 1024]");
@@ -591,8 +585,8 @@ pa_status pa_copy_blocks_fp8(void* k_cache, void* v_cache, const int32_t* pairs,
                              int32_t block_size, int32_t num_blocks, pa_stream_t stream) {
   if (head_dim % 16 != 0)
     return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: head_dim must be a multiple of 16");
-  if (block_size != 16 && block_size != 32)
-    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: block_size 16 or 32");
+  if (!pa::block_size_ok(block_size))
+    return pa::set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks_fp8: block_size 8, 16 or 32");
   // one byte per element: the same bytes as a bf16 block of head_dim / 2
   return pa_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_kv_heads, head_dim / 2, block_size,
                         num_blocks, stream);

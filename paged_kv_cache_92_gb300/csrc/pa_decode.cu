@@ -54,12 +54,11 @@ namespace {
 
 __device__ unsigned int g_decode_errors;
 
-constexpr int BS = kBlockSize;
 constexpr int NWARPS = 4;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, int BS>
 struct Cfg {
   // dims per lane: keep the per-lane query registers (DPL * G) at 64.
   static constexpr int DPL = (D >= 128 && G <= 4) ? 16 : 8;
@@ -72,14 +71,16 @@ struct Cfg {
   static constexpr int TILE = BS * D * EB;  // bytes of one (block, KV head) tile
   static constexpr int ST = (D >= 128) ? 3 : 4;  // ring stages per warp
   // 8-bit: each warp's V rows, transposed from the V^T tile of its block
+  // (sub-tiles of W keys)
   static constexpr int VROWS = F8 ? BS * D : 0;
+  static constexpr int W = BS < 16 ? BS : 16;
   static_assert(G <= LPT, "each head needs a lane after the reduce-scatter");
   static_assert(BS % TPI == 0, "tokens per step must divide the block");
 };
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, int BS>
 constexpr size_t decode_smem_bytes(int partition_tokens) {
-  using C = Cfg<D, G, F8>;
+  using C = Cfg<D, G, F8, BS>;
   size_t tiles = size_t(NWARPS) * (C::ST * 2 * C::TILE + C::VROWS);
   size_t merge = size_t(NWARPS) * G * (D + 2) * sizeof(float);
   if (merge > tiles) tiles = merge;
@@ -129,7 +130,7 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int lane) {
   return v[0];
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, int BS>
 __global__ void __launch_bounds__(NTHREADS)
     paged_decode_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out,
                         const unsigned char* __restrict__ k_cache,
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(NTHREADS)
                         int num_kv_heads, int num_blocks, int max_context_len, float scale_log2,
                         int partition_tokens, int num_partitions, float* __restrict__ part_m,
                         float* __restrict__ part_l, float* __restrict__ part_acc, int q_len) {
-  using C = Cfg<D, G, F8>;
+  using C = Cfg<D, G, F8, BS>;
   constexpr int ST = C::ST;
   const int part = blockIdx.x;
   const int g = blockIdx.y;
@@ -261,25 +262,36 @@ __global__ void __launch_bounds__(NTHREADS)
     const unsigned char* kt = my_tiles + size_t(s) * 2 * C::TILE;
     const unsigned char* vt = kt + C::TILE;
     if constexpr (F8) {
-      // V^T [D][16 keys] -> V rows [16 keys][D]: lane l takes V^T rows
-      // RPL*l .. RPL*l + RPL-1 and stores, per key, their RPL codes together.
+      // V^T sub-tiles [D][W keys] -> V rows [BS keys][D]: lane l takes V^T
+      // rows RPL*l .. RPL*l + RPL-1 of each sub-tile and stores, per key,
+      // their RPL codes together.
       constexpr int RPL = D / 32;
-      uint4 r[RPL];
+      constexpr int W = C::W;
 #pragma unroll
-      for (int j = 0; j < RPL; ++j)
-        r[j] = *reinterpret_cast<const uint4*>(vt + (RPL * lane + j) * 16);
-#pragma unroll
-      for (int t = 0; t < BS; ++t) {
-        uint32_t w = 0;
+      for (int sub = 0; sub < BS / W; ++sub) {
+        uint32_t r[RPL][W / 4];
 #pragma unroll
         for (int j = 0; j < RPL; ++j) {
-          const uint32_t word = reinterpret_cast<const uint32_t*>(&r[j])[t >> 2];
-          w |= ((word >> ((t & 3) * 8)) & 0xffu) << (8 * j);
+          const unsigned char* src = vt + (sub * D + RPL * lane + j) * W;
+          if constexpr (W == 16) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src);
+            r[j][0] = x.x; r[j][1] = x.y; r[j][2] = x.z; r[j][3] = x.w;
+          } else {
+            const uint2 x = *reinterpret_cast<const uint2*>(src);
+            r[j][0] = x.x; r[j][1] = x.y;
+          }
         }
-        if constexpr (RPL == 4) {
-          *reinterpret_cast<uint32_t*>(my_vrows + t * D + RPL * lane) = w;
-        } else {
-          *reinterpret_cast<uint16_t*>(my_vrows + t * D + RPL * lane) = uint16_t(w);
+#pragma unroll
+        for (int t = 0; t < W; ++t) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int j = 0; j < RPL; ++j) w |= ((r[j][t >> 2] >> ((t & 3) * 8)) & 0xffu) << (8 * j);
+          unsigned char* dst = my_vrows + (sub * W + t) * D + RPL * lane;
+          if constexpr (RPL == 4) {
+            *reinterpret_cast<uint32_t*>(dst) = w;
+          } else {
+            *reinterpret_cast<uint16_t*>(dst) = uint16_t(w);
+          }
         }
       }
       __syncwarp();
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(128)
                             const float* __restrict__ part_l, const float* __restrict__ part_acc,
                             const int32_t* __restrict__ context_lens, int num_q_heads,
                             int max_blocks_per_seq, int max_context_len, int partition_tokens,
-                            int num_partitions, int q_len) {
+                            int num_partitions, int q_len, int block_size) {
   constexpr int VPL = D / 32;  // values per lane
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -440,7 +452,7 @@ __global__ void __launch_bounds__(128)
   const int b = z / q_len, qi = z - (z / q_len) * q_len;
   if (h >= num_q_heads) return;
   int L = context_lens[b];
-  L = min(L, min(max_blocks_per_seq * BS, max_context_len));
+  L = min(L, min(max_blocks_per_seq * block_size, max_context_len));
   if (L < q_len) return;  // empty: zero rows written by the decode kernel
   L = L - q_len + qi + 1;
   if (L <= partition_tokens) return;  // written directly by the decode kernel
@@ -475,13 +487,13 @@ __global__ void __launch_bounds__(128)
   for (int j = 0; j < VPL; ++j) o[j] = __float2bfloat16_rn(acc[j] * inv);
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, int BS>
 int launch_decode_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   const pa_decode_params* p = Lc.p;
-  const size_t smem = decode_smem_bytes<D, G, F8>(Lc.partition_tokens);
+  const size_t smem = decode_smem_bytes<D, G, F8, BS>(Lc.partition_tokens);
   static size_t configured = 0;
   if (configured < smem) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, G, F8>,
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, G, F8, BS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return int(e);
     configured = smem;
@@ -489,7 +501,7 @@ int launch_decode_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   const int q_len = query_len_of(p);
   dim3 grid(Lc.num_partitions, p->num_kv_heads, p->num_seqs * q_len);
   const float scale_log2 = p->scale * kLog2e;
-  paged_decode_kernel<D, G, F8><<<grid, NTHREADS, smem, stream>>>(
+  paged_decode_kernel<D, G, F8, BS><<<grid, NTHREADS, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(p->q), static_cast<__nv_bfloat16*>(p->out),
       static_cast<const unsigned char*>(p->k_cache), static_cast<const unsigned char*>(p->v_cache),
       p->k_scale, p->v_scale, p->block_tables, p->context_lens, p->max_blocks_per_seq, p->num_kv_heads, p->num_blocks,
@@ -506,17 +518,27 @@ int launch_merge_t(const DecodeLaunch& Lc, cudaStream_t stream) {
   merge_partitions_kernel<D><<<mgrid, 128, 0, stream>>>(
       static_cast<__nv_bfloat16*>(p->out), Lc.part_m, Lc.part_l, Lc.part_acc, p->context_lens,
       p->num_q_heads, p->max_blocks_per_seq, p->max_context_len, Lc.partition_tokens,
-      Lc.num_partitions, q_len);
+      Lc.num_partitions, q_len, p->block_size);
   return int(cudaGetLastError());
 }
 
-template <int D, bool F8>
+template <int D, bool F8, int BS>
 int dispatch_group(const DecodeLaunch& Lc, cudaStream_t s) {
   switch (Lc.p->num_q_heads / Lc.p->num_kv_heads) {
-    case 1: return launch_decode_t<D, 1, F8>(Lc, s);
-    case 2: return launch_decode_t<D, 2, F8>(Lc, s);
-    case 4: return launch_decode_t<D, 4, F8>(Lc, s);
-    case 8: return launch_decode_t<D, 8, F8>(Lc, s);
+    case 1: return launch_decode_t<D, 1, F8, BS>(Lc, s);
+    case 2: return launch_decode_t<D, 2, F8, BS>(Lc, s);
+    case 4: return launch_decode_t<D, 4, F8, BS>(Lc, s);
+    case 8: return launch_decode_t<D, 8, F8, BS>(Lc, s);
+    default: return int(cudaErrorInvalidValue);
+  }
+}
+
+template <int D, bool F8>
+int dispatch_block(const DecodeLaunch& Lc, cudaStream_t s) {
+  switch (Lc.p->block_size) {
+    case 8: return dispatch_group<D, F8, 8>(Lc, s);
+    case 16: return dispatch_group<D, F8, 16>(Lc, s);
+    case 32: return dispatch_group<D, F8, 32>(Lc, s);
     default: return int(cudaErrorInvalidValue);
   }
 }
@@ -527,8 +549,8 @@ int launch_decode(const DecodeLaunch& Lc, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool f8 = Lc.p->kv_dtype == PA_KV_FP8_E4M3;
   switch (Lc.p->head_dim) {
-    case 64: return f8 ? dispatch_group<64, true>(Lc, s) : dispatch_group<64, false>(Lc, s);
-    case 128: return f8 ? dispatch_group<128, true>(Lc, s) : dispatch_group<128, false>(Lc, s);
+    case 64: return f8 ? dispatch_block<64, true>(Lc, s) : dispatch_block<64, false>(Lc, s);
+    case 128: return f8 ? dispatch_block<128, true>(Lc, s) : dispatch_block<128, false>(Lc, s);
     default: return int(cudaErrorInvalidValue);
   }
 }

@@ -71,10 +71,11 @@ __global__ void __launch_bounds__(256)
   *reinterpret_cast<uint2*>(k_cache + tile + int64_t(off) * head_dim + c * 8) = kw;
   // V column: element d of the row goes to byte d * 16 + off % 16 of the
   // tile's sub-tile off / 16
-  const int64_t sub = tile + int64_t(off >> 4) * 16 * head_dim + (off & 15);
+  const int W = BS < 16 ? BS : 16;  // keys of one V^T sub-tile
+  const int64_t sub = tile + int64_t(off / W) * W * head_dim + (off % W);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    v_cache[sub + int64_t(c * 8 + i) * 16] = to_e4m3(__fdiv_rn(__bfloat162float(vb[i]), vs));
+    v_cache[sub + int64_t(c * 8 + i) * W] = to_e4m3(__fdiv_rn(__bfloat162float(vb[i]), vs));
 }
 
 // Queries for the E4M3 tensor-core decode. For every (sequence b, column n)
@@ -215,10 +216,11 @@ __global__ void __launch_bounds__(128)
   const int64_t tile = (int64_t(e) * a.num_kv_heads + h) * int64_t(BS) * a.head_dim;
   *reinterpret_cast<uint2*>(a.k_cache + tile + int64_t(off) * a.head_dim + c * 8) =
       make_uint2(kw[0], kw[1]);
-  const int64_t sub = tile + int64_t(off >> 4) * 16 * a.head_dim + (off & 15);
+  const int W = BS < 16 ? BS : 16;  // keys of one V^T sub-tile
+  const int64_t sub = tile + int64_t(off / W) * W * a.head_dim + (off % W);
 #pragma unroll
   for (int j = 0; j < 8; ++j)
-    a.v_cache[sub + int64_t(c * 8 + j) * 16] =
+    a.v_cache[sub + int64_t(c * 8 + j) * W] =
         to_e4m3(dev::div_rn_by(__bfloat162float(vb[j]), vs, rv));
 }
 

@@ -65,13 +65,14 @@ def _params(pk, **kw):
     (dict(block_size=32), 1),  # block size 32: tensor-core kernel, valid shapes, NULL pointers
     (dict(block_size=8), 1),
     (dict(block_size=32, head_dim=64), 1),  # block sizes 8 and 32 at head_dim 64: bf16
-    (dict(block_size=8, head_dim=64, kv_dtype=1), 2),  # the 8-bit cache: not at block size 8
-    (dict(kv_dtype=1, variant=1), 1),  # ... on the CUDA-core kernel (NULL pointers)
-    (dict(kv_dtype=1, head_dim=64), 1),  # ... head_dim 64 there
-    (dict(kv_dtype=1, variant=1, block_size=32), 2),  # ... block size 16 there
-    (dict(block_size=8, variant=1), 2),  # ... and the tensor-core kernel only
+    # the 8-bit cache at block size 8 and head_dim 64: the CUDA-core kernel (NULL pointers)
+    (dict(block_size=8, head_dim=64, kv_dtype=1), 1),
+    (dict(kv_dtype=1, variant=1), 1),
+    (dict(kv_dtype=1, head_dim=64), 1),
+    (dict(kv_dtype=1, variant=1, block_size=32), 1),
+    (dict(block_size=8, variant=1), 1),  # block sizes 8 and 32 on the CUDA-core kernel too
     (dict(block_size=8, query_len=4), 1),  # block size 8: column groups of 8 per KV head
-    (dict(block_size=8, kv_dtype=1), 2),  # the 8-bit cache: block size 16 or 32
+    (dict(block_size=8, kv_dtype=1), 1),
     (dict(num_q_heads=12, num_kv_heads=1), 2),
     (dict(num_q_heads=6, num_kv_heads=4), 1),
     (dict(max_context_len=0), 1),
@@ -216,11 +217,13 @@ def test_cache_ops_reject_bad_arguments_on_the_host(pk):
         assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, bs, 10, None) == 1
         assert lib.pa_copy_blocks(None, None, None, 2, 8, 128, bs, 10, None) == 1
     assert lib.pa_copy_blocks(None, None, None, 2, 8, 128, 4, 10, None) == 2
-    assert lib.pa_reshape_and_cache_fp8(None, None, None, None, None, None, None, 4, 8, 128, 8,
+    for bs in (8, 16, 32):  # the 8-bit cache at every block size (NULL pointers)
+        assert lib.pa_reshape_and_cache_fp8(None, None, None, None, None, None, None, 4, 8, 128,
+                                            bs, 10, None) == 1
+        assert lib.pa_copy_blocks_fp8(None, None, None, 2, 8, 128, bs, 10, None) == 1
+    assert lib.pa_reshape_and_cache_fp8(None, None, None, None, None, None, None, 4, 8, 128, 12,
                                         10, None) == 2
-    assert lib.pa_reshape_and_cache_fp8(None, None, None, None, None, None, None, 4, 8, 128, 32,
-                                        10, None) == 1
-    assert lib.pa_copy_blocks_fp8(None, None, None, 2, 8, 128, 8, 10, None) == 2
+    assert lib.pa_copy_blocks_fp8(None, None, None, 2, 8, 128, 4, 10, None) == 2
     assert lib.pa_reshape_and_cache(None, None, None, None, None, 0, 8, 128, 16, 10, None) == 0
     assert lib.pa_copy_blocks(None, None, None, 2, 8, 128, 16, 10, None) == 1
     assert lib.pa_copy_blocks(None, None, None, 0, 8, 128, 16, 10, None) == 0

@@ -172,21 +172,63 @@ def test_head_dim_64(pk, bs, G, Hkv, QL):
     assert pk.pa_device_errors() == 0
 
 
-def test_unsupported_block_size_shapes_are_rejected(pk):
+# ---------------------------------------------------------------- the CUDA-core kernel
+
+
+@BLOCK_SIZES
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G,Hkv", [(1, 8), (4, 8), (8, 8), (4, 3)])
+def test_cuda_core_edge_lengths(pk, bs, D, G, Hkv):
+    """Block and partition boundaries on the CUDA-core kernel (4 KV heads
+    with G 4 is a shape only it takes)."""
+    lens = [1, bs - 1, bs, bs + 1, 100, 511, 512, 513, 1025, 1600]
+    q, kc, vc, tables, lens, torch = _case(lens, G * Hkv, Hkv, bs, seed=900 + bs + G + Hkv + D, D=D)
+    out = _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+    harness.assert_close(harness.bf16_tensor_to_f64(out),
+                         oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens))
+    assert pk.pa_device_errors() == 0
+
+
+@BLOCK_SIZES
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_cuda_core_llama8b_layer_step(pk, bs, fused):
+    case = harness.build_case(workloads.llama8b_layer(block_size=bs))
+    out, kg, vg = harness.run_step_gpu(case, variant=1, fused_append=fused)
+    ref, ko, vo = harness.run_step_oracle(case)
+    assert np.array_equal(oracle.bf16_bits(kg.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vg.cpu()), vo)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert pk.pa_device_errors() == 0
+
+
+@BLOCK_SIZES
+def test_cuda_core_multi_token(pk, bs):
+    QL = 3
+    lens = [QL, bs + 1, 2 * bs + 2, 600]
+    q, kc, vc, tables, lens, torch = _case(lens, 32, 8, bs, seed=910 + bs, QL=QL)
+    out = _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+    harness.assert_close(harness.bf16_tensor_to_f64(out),
+                         oracle.paged_decode_multi(q.cpu(), kc.cpu(), vc.cpu(), tables, lens))
+
+
+def test_cuda_core_partitions_must_be_whole_blocks(pk):
     import torch
 
-    q, kc, vc, tables, lens, _ = _case([40], 8, 2, 8, seed=8)
+    q, kc, vc, tables, lens, _ = _case([40], 8, 2, 32, seed=8)
     with pytest.raises(pk.PagedKVError):
-        _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE)
+        _decode(pk, q, kc, vc, tables, lens, torch, variant=pk.DECODE_CUDA_CORE,
+                partition_tokens=48)
 
 
 # ---------------------------------------------------------------- the 8-bit cache at block size 32
 
 
-def _fp8_case(pk, lens, Hq, Hkv, seed, QL=0):
+def _fp8_case(pk, lens, Hq, Hkv, seed, QL=0, BS=32, D=128):
+    """The 8-bit cache at block size BS (V^T in sub-tiles of W = min(BS, 16)
+    keys), every slot written through pa_reshape_and_cache_fp8, E4M3 NaN in
+    every padding slot."""
     import torch
 
-    BS, D = 32, 128
     lens = np.asarray(lens, dtype=np.int64)
     need = int(((lens + BS - 1) // BS).sum())
     NB = need + 3
@@ -199,15 +241,16 @@ def _fp8_case(pk, lens, Hq, Hkv, seed, QL=0):
     rng = np.random.default_rng(seed + 4)
     ks = torch.from_numpy((0.05 * np.exp(rng.uniform(-0.5, 0.5, Hkv))).astype(np.float32)).cuda()
     vs = torch.from_numpy((0.03 * np.exp(rng.uniform(-0.5, 0.5, Hkv))).astype(np.float32)).cuda()
+    W = min(BS, 16)
     k8 = torch.zeros((NB, Hkv, BS, D), dtype=torch.uint8, device="cuda")
-    v8 = torch.zeros((NB, Hkv, BS // 16, D, 16), dtype=torch.uint8, device="cuda")
+    v8 = torch.zeros((NB, Hkv, BS // W, D, W), dtype=torch.uint8, device="cuda")
     pk.pa_reshape_and_cache_fp8(kn, vn, k8, v8, torch.arange(NB * BS, device="cuda"), ks, vs)
     for b, L in enumerate(lens):
         if L % BS:
             blk, off = int(tables[b, (L - 1) // BS]), int(L % BS)
             k8[blk, :, off:, :] = 0x7F  # E4M3 NaN in the padding slots
             for o in range(off, BS):
-                v8[blk, :, o // 16, :, o % 16] = 0x7F
+                v8[blk, :, o // W, :, o % W] = 0x7F
     torch.cuda.synchronize()
     return q, k8, v8, ks, vs, tables, lens.astype(np.int32), kn, vn, torch
 
@@ -262,13 +305,101 @@ def test_fp8_multi_token_at_block_size_32(pk):
     assert pk.pa_device_errors() == 0
 
 
-def test_fp8_block_size_8_is_rejected(pk):
+@pytest.mark.parametrize("G,Hkv", [(4, 8), (1, 4), (8, 2)])
+def test_fp8_decode_at_block_size_32_cuda_core(pk, G, Hkv):
+    lens = [1, 31, 32, 33, 513, 1025]
+    q, k8, v8, ks, vs, tables, lens, _, _, torch = _fp8_case(pk, lens, G * Hkv, Hkv,
+                                                              seed=140 + G + Hkv)
+    out = _decode(pk, q, k8, v8, tables, lens, torch, k_scale=ks, v_scale=vs,
+                  variant=pk.DECODE_CUDA_CORE)
+    NB = k8.shape[0]
+    want = oracle.paged_decode_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy().reshape(NB, Hkv, 32, 128),
+                                   ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+
+
+# ---------------------------------------------------------------- the 8-bit cache at block size 8
+#
+# V^T is stored in sub-tiles of 8 keys, [NB][Hkv][D][8] per (block, head); the
+# tensor-core kernel's operand layout needs 16-key rows, so this cache decodes
+# on the CUDA-core kernel whatever the variant says.
+
+
+def test_fp8_write_bit_exact_at_block_size_8(pk):
     import torch
 
-    k8 = torch.zeros((4, 2, 8, 128), dtype=torch.uint8, device="cuda")
-    v8 = torch.zeros((4, 2, 8, 128), dtype=torch.uint8, device="cuda")
-    kn = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda")
-    ks = torch.ones(2, dtype=torch.float32, device="cuda")
-    with pytest.raises((pk.PagedKVError, ValueError)):
-        pk.pa_reshape_and_cache_fp8(kn, kn, k8, v8, torch.zeros(1, dtype=torch.int64,
-                                                                device="cuda"), ks, ks)
+    Hkv, D, NB, BS = 4, 128, 10, 8
+    rng = np.random.default_rng(12)
+    T = 60
+    kn = torch.from_numpy(rng.standard_normal((T, Hkv, D)) * 30).to(torch.bfloat16)
+    vn = torch.from_numpy(rng.standard_normal((T, Hkv, D)) * 30).to(torch.bfloat16)
+    ks = np.array([1.0, 0.5, 2.0, 0.37], dtype=np.float32)
+    vs = np.array([1.0, 3.0, 0.25, 1.7], dtype=np.float32)
+    slots = rng.permutation(NB * BS)[:T].astype(np.int64)
+    slots[[3, 30]] = -1
+    k0 = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
+    v0 = rng.integers(0, 256, size=(NB, Hkv, D, BS), dtype=np.uint8)
+    kc, vc = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    pk.pa_reshape_and_cache_fp8(kn.cuda(), vn.cuda(), kc, vc, torch.from_numpy(slots).cuda(),
+                                torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda())
+    torch.cuda.synchronize()
+    ko, vo = oracle.reshape_and_cache_fp8(kn, vn, k0, v0.reshape(NB, Hkv, BS, D), slots, ks, vs)
+    assert np.array_equal(kc.cpu().numpy(), ko)
+    assert np.array_equal(vc.cpu().numpy().reshape(NB, Hkv, BS, D), vo)
+    assert pk.pa_device_errors() == 0
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("D,G,Hkv", [(128, 4, 8), (128, 8, 8), (64, 1, 4), (128, 2, 1)])
+def test_fp8_decode_at_block_size_8(pk, variant, D, G, Hkv):
+    lens = [1, 7, 8, 9, 100, 511, 512, 513, 1025]
+    q, k8, v8, ks, vs, tables, lens, _, _, torch = _fp8_case(pk, lens, G * Hkv, Hkv,
+                                                              seed=150 + G + Hkv + D, BS=8, D=D)
+    out = _decode(pk, q, k8, v8, tables, lens, torch, k_scale=ks, v_scale=vs, variant=variant)
+    NB = k8.shape[0]
+    want = oracle.paged_decode_fp8(q.cpu(), k8.cpu().numpy(), v8.cpu().numpy().reshape(NB, Hkv, 8, D),
+                                   ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+
+
+def test_fp8_multi_token_at_block_size_8(pk):
+    QL = 3
+    lens = [3, 9, 17, 600]
+    q, k8, v8, ks, vs, tables, lens, _, _, torch = _fp8_case(pk, lens, 32, 8, seed=160, QL=QL, BS=8)
+    out = _decode(pk, q, k8, v8, tables, lens, torch, k_scale=ks, v_scale=vs)
+    NB = k8.shape[0]
+    want = oracle.paged_decode_multi_fp8(q.cpu(), k8.cpu().numpy(),
+                                         v8.cpu().numpy().reshape(NB, 8, 8, 128),
+                                         ks.cpu().numpy(), vs.cpu().numpy(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+    assert pk.pa_device_errors() == 0
+
+
+def test_fp8_fused_append_at_block_size_8(pk):
+    """The step's write (the preparation launch's write, same slot rule), then
+    the decode: caches bit-exact against the oracle's write, rows against its
+    decode."""
+    import torch
+
+    lens = [1, 8, 9, 300, 1025]
+    q, k8, v8, ks, vs, tables, lens, _, _, _ = _fp8_case(pk, lens, 32, 8, seed=170, BS=8)
+    NB, BS, Hkv, D = k8.shape[0], 8, 8, 128
+    slots = np.array([int(tables[b, (L - 1) // BS]) * BS + (L - 1) % BS for b, L in enumerate(lens)],
+                     dtype=np.int64)
+    kn = workloads.bf16_normal((len(lens), Hkv, D), 171, "cuda")
+    vn = workloads.bf16_normal((len(lens), Hkv, D), 172, "cuda")
+    k0, v0 = k8.cpu().numpy(), v8.cpu().numpy().reshape(NB, Hkv, BS, D)
+    out = pk.pa_append_decode(q, k8, v8, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
+                              torch.from_numpy(slots).cuda(), k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() == 0
+    ko, vo = oracle.reshape_and_cache_fp8(kn.cpu(), vn.cpu(), k0, v0, slots, ks.cpu().numpy(),
+                                          vs.cpu().numpy())
+    assert np.array_equal(k8.cpu().numpy(), ko)
+    assert np.array_equal(v8.cpu().numpy().reshape(NB, Hkv, BS, D), vo)
+    want = oracle.paged_decode_fp8(q.cpu(), ko, vo, ks.cpu().numpy(), vs.cpu().numpy(), tables,
+                                   lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)

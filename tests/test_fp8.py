@@ -287,20 +287,6 @@ def test_fp8_cuda_core_several_new_tokens(pk):
     harness.assert_close(harness.bf16_tensor_to_f64(out), want)
 
 
-def test_fp8_cuda_core_block_size_32_is_rejected(pk):
-    import torch
-
-    D, NB, Hkv = 128, 4, 2
-    q = torch.zeros((1, 8, D), dtype=torch.bfloat16, device="cuda")
-    k8 = torch.zeros((NB, Hkv, 32, D), dtype=torch.uint8, device="cuda")
-    v8 = torch.zeros((NB, Hkv, 2, D, 16), dtype=torch.uint8, device="cuda")
-    ks = torch.ones((Hkv,), dtype=torch.float32, device="cuda")
-    with pytest.raises(pk.PagedKVError):
-        pk.pa_decode(q, k8, v8, torch.zeros((1, 2), dtype=torch.int32, device="cuda"),
-                     torch.full((1,), 20, dtype=torch.int32, device="cuda"), max_context_len=20,
-                     k_scale=ks, v_scale=ks, variant=pk.DECODE_CUDA_CORE)
-
-
 # ---------------------------------------------------------------- the write fused into the decode
 
 
