@@ -21,7 +21,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["pa_decode_tc.cu", "pa_decode_tc_d64.cu", "pa_decode_tc_fp8.cu", "pa_decode_tc_bs8.cu",
            "pa_decode_tc_bs32.cu", "pa_decode_tc_bs32_fp8.cu", "pa_decode_tc_bs8_d64.cu",
-           "pa_decode_tc_bs32_d64.cu", "pa_decode.cu", "pa_cache.cu", "pa_fp8.cu", "pa_query.cu",
+           "pa_decode_tc_bs32_d64.cu", "pa_prefill_tc.cu", "pa_decode.cu", "pa_cache.cu", "pa_fp8.cu",
+           "pa_query.cu",
            "pa_api.cpp", "pa_pool.cpp"]
 HEADERS = ["pa_device.cuh", "pa_decode_tc.cuh", "pa_internal.h"]
 

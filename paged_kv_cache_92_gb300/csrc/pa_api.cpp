@@ -124,6 +124,10 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
                                         int grid) {
   WorkspaceLayout w{};
   const size_t H = kWorkspaceHeaderBytes;
+  if (use_query_major(p)) {  // no split of the keys: nothing but the header
+    w.total = H;
+    return w;
+  }
   if (!decode_uses_tc(p)) {
     // CUDA-core kernel: per-partition partials (only when a sequence can split)
     w.total = H;
@@ -174,7 +178,22 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
   L.grid = grid;
   char where[96];
   int e = 0;
-  if (decode_uses_tc(p)) {
+  if (use_query_major(p)) {
+    if (append) {  // the step's write first, with the fused path's slot rule
+      AppendCheck chk;
+      chk.block_tables = p->block_tables;
+      chk.context_lens = p->context_lens;
+      chk.max_blocks_per_seq = p->max_blocks_per_seq;
+      chk.cap = p->max_blocks_per_seq * p->block_size < p->max_context_len
+                    ? p->max_blocks_per_seq * p->block_size : p->max_context_len;
+      chk.q_len = query_len_of(p);
+      e = launch_reshape_and_cache(append->k_new, append->v_new, append->k_cache,
+                                   append->v_cache, append->slot_mapping,
+                                   p->num_seqs * query_len_of(p), p->num_kv_heads, p->head_dim,
+                                   p->block_size, p->num_blocks, stream, chk);
+    }
+    if (!e) e = launch_query_major_tc(p, stream);
+  } else if (decode_uses_tc(p)) {
     if (grid <= 0)
       return set_cuda_error("the SM count of the current device", int(cudaErrorNoDevice));
     L.plan = reinterpret_cast<int*>(ws + w.tc_plan);
@@ -340,13 +359,14 @@ pa_status pa_device_errors(pa_stream_t stream, uint32_t* flags) {
   if (!flags) return pa::set_error(PA_ERR_INVALID_ARG, "pa_device_errors: flags is NULL");
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return pa::set_cuda_error("pa_device_errors: stream sync", int(e));
-  uint32_t a = 0, b = 0, c = 0, d = 0;
+  uint32_t a = 0, b = 0, c = 0, d = 0, qm = 0;
   int r = pa::read_and_clear_decode_errors(&a);
   if (r == 0) r = pa::read_and_clear_decode_tc_errors(&c);
   if (r == 0) r = pa::read_and_clear_cache_errors(&b);
   if (r == 0) r = pa::read_and_clear_fp8_errors(&d);
+  if (r == 0) r = pa::read_and_clear_query_major_errors(&qm);
   if (r != 0) return pa::set_cuda_error("pa_device_errors: read", r);
-  *flags = a | b | c | d;
+  *flags = a | b | c | d | qm;
   return PA_OK;
 }
 

@@ -1,0 +1,484 @@
+// Several new tokens per sequence on the tensor cores, query-major: one CTA per
+// (sequence, KV head, tile of 128 query rows) streams that KV head's blocks
+// once for all its rows ("How Paged Attention and Continuous Batching
+// Actually Work", §Continuous batching: the scheduled tokens of one request,
+// as in a chunked prefill). Row r of a tile is new token i = tile*QT + r/G of
+// query head g*G + r%G, and sees the sequence's first L - Q + i + 1 keys.
+//
+// The column-group decode (pa_decode_tc.cuh) puts the keys on the MMAs' M side
+// and streams them once per group of new tokens; with many new tokens each
+// group re-reads the keys. Here the queries are on the M side:
+//   S[128 rows][64 keys]  = Q . K^T        (A = Q, B = K chunk, both K-major)
+//   O[128 rows][128 d]   += P . V          (A = P, K-major; B = V, MN-major)
+// with S and P double-buffered and O in TMEM (256 columns). A thread owns a row: its
+// softmax (running maximum, sum, the conditional rescale of its O row) needs
+// no other thread. A chunk is 64 keys, four blocks of one KV head, each block
+// [16 keys][128 d] one 2-D tensor-map box per 64-d half.
+#include "pa_decode_tc.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int QM_D = 128;
+constexpr int QM_KC = 64;         // keys per chunk
+constexpr int QM_ROWS = 128;      // query rows per tile (MMA M)
+constexpr int QM_ST = 4;          // ring slots
+constexpr int QM_THREADS = 192;   // softmax warps 0-3, producer 4, MMA 5
+constexpr int QM_HALF_Q = QM_ROWS * 128;     // one 64-d half of Q: [128 rows][128 B]
+constexpr int QM_Q_BYTES = 2 * QM_HALF_Q;
+constexpr int QM_HALF_KV = QM_KC * 128;      // one 64-d half of a K or V chunk: [64 keys][128 B]
+constexpr int QM_SLOT = 4 * QM_HALF_KV;      // K halves, then V halves
+constexpr int QM_P_BYTES = QM_ROWS * 128;    // one P buffer: [128 rows][64 keys] bf16
+constexpr int QM_OFF_Q = 0;
+constexpr int QM_OFF_RING = QM_OFF_Q + QM_Q_BYTES;
+constexpr int QM_OFF_P = QM_OFF_RING + QM_ST * QM_SLOT;
+constexpr int QM_OFF_BARS = QM_OFF_P + 2 * QM_P_BYTES;
+constexpr int QM_NBARS = 2 * QM_ST + 8;  // full, empty, qfull, s[2], p[2], o[2], drain
+constexpr int QM_OFF_WORDS = QM_OFF_BARS + QM_NBARS * 8;
+constexpr int QM_SMEM = QM_OFF_WORDS + 64 + 1024;  // + alignment slack
+static_assert(QM_SMEM <= kMaxDynSmem, "shared memory budget");
+constexpr uint32_t QM_TMEM_COLS = 256;  // S[2] at [0, 128), O at [128, 256)
+constexpr uint32_t QM_IDESC_S = dev::idesc_bf16_f32(QM_ROWS, QM_KC, false, false);
+constexpr uint32_t QM_IDESC_PV = dev::idesc_bf16_f32(QM_ROWS, QM_D, false, true);
+
+struct QmParams {
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  __nv_bfloat16* out;
+  int num_seqs, num_kv_heads, num_q_heads, q_len, tiles, max_blocks_per_seq, num_blocks, cap,
+      oob_row;
+  float scale_log2;
+  uint64_t wait_ns;
+};
+
+template <int G>
+__global__ void __launch_bounds__(QM_THREADS, 1)
+    query_major_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_q, const QmParams P) {
+  constexpr int QT = QM_ROWS / G;  // new tokens per tile
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* qbuf = smem + QM_OFF_Q;
+  unsigned char* ring = smem + QM_OFF_RING;
+  unsigned char* pbuf = smem + QM_OFF_P;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QM_OFF_BARS);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + QM_ST;
+  uint64_t* qfull = bars + 2 * QM_ST;
+  uint64_t* bar_s = qfull + 1;  // [2] scores of chunk c in S[c % 2]
+  uint64_t* bar_p = bar_s + 2;  // [2] P[c % 2] of chunk c written, S[c % 2] read
+  uint64_t* bar_o = bar_p + 2;  // [2] value product of chunk c (which read P[c % 2]) done
+  uint64_t* drain = bar_o + 2;
+  int* words = reinterpret_cast<int*>(smem + QM_OFF_WORDS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&words[0]);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&words[1]);
+  int* issued = &words[2];
+  int* consumed = &words[3];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = int(blockIdx.x) % P.tiles;
+  const int hg = (int(blockIdx.x) / P.tiles) % P.num_kv_heads;
+  const int rank = int(blockIdx.x) / (P.tiles * P.num_kv_heads);
+  const int Q = P.q_len;
+  // Longest sequences first (the CTAs start in index order, so the last wave
+  // holds the shortest work): up to 256 sequences every CTA ranks the lengths
+  // and takes the sequence of its rank (ties by index).
+  int b = rank;
+  if (P.num_seqs <= 256) {
+    int* found = reinterpret_cast<int*>(smem + QM_OFF_WORDS) + 4;
+    if (tid == 0) *found = rank;
+    __syncthreads();
+    for (int v = tid; v < P.num_seqs; v += QM_THREADS) {
+      const int Lv = P.context_lens[v];
+      int above = 0;
+      for (int u = 0; u < P.num_seqs; ++u) {
+        const int Lu = P.context_lens[u];
+        above += Lu > Lv || (Lu == Lv && u < v);
+      }
+      if (above == rank) *found = v;
+    }
+    __syncthreads();
+    b = *found;
+  }
+
+  int L = P.context_lens[b];
+  const bool report = tid == 0 && tile == 0 && hg == 0;
+  if (L > P.cap) {
+    if (report) atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
+    L = P.cap;
+  }
+  if (L > 0 && L < Q) {  // no room for the new tokens: an empty sequence
+    if (report) atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
+    L = 0;
+  }
+  const int i_last = min(Q, (tile + 1) * QT) - 1;  // the tile's last new token
+  if (L <= 0) {  // zero rows
+    for (int e = tid; e < QM_ROWS * (QM_D / 8); e += QM_THREADS) {
+      const int r = e / (QM_D / 8), ch = e % (QM_D / 8);
+      const int i = tile * QT + r / G;
+      if (i < Q) {
+        const size_t row = (size_t(b) * Q + i) * P.num_q_heads + hg * G + r % G;
+        reinterpret_cast<uint4*>(P.out + row * QM_D)[ch] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
+  const int keys = L - Q + i_last + 1;  // what the tile's last row sees
+  const int n = (keys + QM_KC - 1) / QM_KC;
+
+  if (tid == 0) {
+    for (int s = 0; s < QM_ST; ++s) {
+      dev::mbar_init(&full[s], 1);
+      dev::mbar_init(&empty[s], 1);
+    }
+    dev::mbar_init(qfull, 1);
+    for (int k = 0; k < 2; ++k) {
+      dev::mbar_init(&bar_s[k], 1);
+      dev::mbar_init(&bar_p[k], 128);
+      dev::mbar_init(&bar_o[k], 1);
+    }
+    dev::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *issued = 0;
+    *consumed = 0;
+    dev::fence_barrier_init();
+  }
+  if (warp == 0) dev::tmem_alloc(tmem_slot, QM_TMEM_COLS);
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    const uint64_t pol = dev::l2_evict_first_policy();
+    if (lane == 0) {
+      dev::prefetch_tmap(&tm_k);
+      dev::prefetch_tmap(&tm_v);
+      dev::mbar_arrive_expect_tx(qfull, QM_Q_BYTES);
+      for (int hf = 0; hf < 2; ++hf)
+        dev::tma_load_4d(qbuf + hf * QM_HALF_Q, &tm_q, hf * 64, hg * G, tile * QT, b, qfull, pol);
+    }
+    const int32_t* trow = P.block_tables + size_t(b) * P.max_blocks_per_seq;
+    // lane l holds the table entry of block w0 + l (8 chunks per window)
+    auto window = [&](int w0) {
+      const int j = w0 + lane;
+      return (j < P.max_blocks_per_seq && j * 16 < L) ? trow[j] : -1;
+    };
+    int w0 = 0;
+    int win = window(0);
+    bool ok = true;
+    for (int c = 0; c < n && ok; ++c) {
+      if (c * 4 >= w0 + 32) {
+        w0 += 32;
+        win = window(w0);
+      }
+      const int slot = c % QM_ST;
+      if (lane == 0) {
+        ok = dev::mbar_wait_sleep(&empty[slot], (uint32_t(c / QM_ST) & 1u) ^ 1u, 64, P.wait_ns,
+                                  abort_flag);
+        if (ok) dev::mbar_arrive_expect_tx(&full[slot], QM_SLOT);
+      }
+      ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+      if (!ok) break;
+      unsigned char* kdst = ring + size_t(slot) * QM_SLOT;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = c * 4 + u;
+        const int e = __shfl_sync(0xffffffffu, win, j - w0);
+        int row = P.oob_row;  // past the sequence (or a bad entry): zero fill
+        if (j * 16 < L) {
+          if (e >= 0 && e < P.num_blocks) {
+            row = (e * P.num_kv_heads + hg) * 16;
+          } else if (lane == 0) {
+            atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+          }
+        }
+        if (lane == 0) {
+          for (int hf = 0; hf < 2; ++hf) {
+            dev::tma_load_2d(kdst + hf * QM_HALF_KV + u * 2048, &tm_k, hf * 64, row, &full[slot],
+                             pol);
+            dev::tma_load_2d(kdst + 2 * QM_HALF_KV + hf * QM_HALF_KV + u * 2048, &tm_v, hf * 64,
+                             row, &full[slot], pol);
+          }
+        }
+      }
+      if (lane == 0) *issued = c + 1;
+    }
+    if (!ok && lane == 0) {
+      atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t qb = dev::smem_addr(qbuf), pb = dev::smem_addr(pbuf);
+      bool ok = dev::mbar_wait(qfull, 0, P.wait_ns, abort_flag);
+      auto issue_s = [&](int c) {
+        const uint32_t kb = dev::smem_addr(ring + size_t(c % QM_ST) * QM_SLOT);
+        dev::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < QM_D / 16; ++kk) {
+          const uint32_t hf = kk >> 2, off = uint32_t(kk & 3) * 32;
+          dev::mma_bf16(tmem + uint32_t(c & 1) * QM_KC,
+                        dev::smem_desc(qb + hf * QM_HALF_Q + off, 16, 1024, dev::kSwizzle128B),
+                        dev::smem_desc(kb + hf * QM_HALF_KV + off, 16, 1024, dev::kSwizzle128B),
+                        QM_IDESC_S, kk > 0);
+        }
+        dev::mma_commit(&bar_s[c & 1]);
+      };
+      // Event loop: the scores of chunk s once it has landed (its S buffer was
+      // read by the softmax of chunk s - 2, whose value product is issued), and
+      // the value product of chunk v once the softmax has written its P --
+      // whichever is ready first, so that neither waits behind the other.
+      int s_next = 0, v_next = 0;
+      uint64_t t_idle = 0;
+      uint32_t idle = 0;
+      while (ok && v_next < n) {
+        bool progress = false;
+        if (s_next < n && s_next <= v_next + 1 &&
+            dev::mbar_test(&full[s_next % QM_ST], uint32_t(s_next / QM_ST) & 1u)) {
+          issue_s(s_next);
+          ++s_next;
+          progress = true;
+        }
+        if (v_next < s_next &&
+            dev::mbar_test(&bar_p[v_next & 1], uint32_t(v_next >> 1) & 1u)) {
+          const int c = v_next;
+          dev::tc_fence_after();
+          const uint32_t vb = dev::smem_addr(ring + size_t(c % QM_ST) * QM_SLOT + 2 * QM_HALF_KV);
+#pragma unroll
+          for (int kk = 0; kk < QM_KC / 16; ++kk)
+            dev::mma_bf16(tmem + 2 * QM_KC,
+                          dev::smem_desc(pb + uint32_t(c & 1) * QM_P_BYTES + kk * 32, 16, 1024,
+                                         dev::kSwizzle128B),
+                          // V MN-major: next 8 keys 1024 B on (SBO), second 64-d
+                          // half one half on (LBO)
+                          dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
+                          QM_IDESC_PV, c > 0 || kk > 0);
+          dev::mma_commit(&bar_o[c & 1]);
+          dev::mma_commit(&empty[c % QM_ST]);
+          *consumed = c + 1;
+          ++v_next;
+          progress = true;
+        }
+        if (progress) {
+          idle = 0;
+          continue;
+        }
+        // bounded idle: sleep between polls (the softmax warp sharing this
+        // warp's sub-partition has much to issue); the wall clock is read
+        // every 256 polls
+        __nanosleep(32);
+        if ((++idle & 255u) != 0u) continue;
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint64_t now = dev::global_timer_ns();
+        if (idle == 256u) {
+          t_idle = now;
+        } else if (now - t_idle > P.wait_ns) {
+          ok = false;
+        }
+      }
+      if (!ok) {
+        atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      dev::mma_commit(drain);
+      (void)dev::mbar_wait(drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------- softmax
+    const int r = tid;  // query row of the tile (= TMEM lane)
+    const int i = tile * QT + r / G;
+    const bool valid = i < Q;
+    const int L_row = valid ? L - Q + i + 1 : 0;
+    const uint32_t t_lane = uint32_t(warp * 32) << 16;
+    float m_ref = -INFINITY, l = 0.0f;
+    int pv_done = -1;
+    bool ok = true;
+    // value product of chunk k done (it completes bar_o[k % 2], phase k / 2)
+    auto wait_pv = [&](int k) {
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[k & 1], uint32_t(k >> 1) & 1u,
+                                                  P.wait_ns, abort_flag)) &&
+           ok;
+      pv_done = k;
+    };
+    for (int c = 0; c < n && ok; ++c) {
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[c & 1], uint32_t(c >> 1) & 1u,
+                                                  P.wait_ns, abort_flag));
+      if (!ok) break;
+      dev::tc_fence_after();
+      float s[QM_KC];
+      dev::tmem_ld_cols<QM_KC>(tmem + t_lane + uint32_t(c & 1) * QM_KC, s);
+      float cm = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < QM_KC; ++k) {
+        s[k] = c * QM_KC + k < L_row ? s[k] * P.scale_log2 : -INFINITY;
+        cm = fmaxf(cm, s[k]);
+      }
+      // the reference moves only when a score exceeds it by more than 2^8
+      const bool need = cm > m_ref + kRescaleLog2;
+      if (__any_sync(0xffffffffu, need)) {
+        const float nr = need ? cm : m_ref;
+        const float f = nr == m_ref || m_ref == -INFINITY ? 1.0f : dev::fast_exp2(m_ref - nr);
+        if (c > 0) {
+          if (pv_done < c - 1) wait_pv(c - 1);
+          if (!ok) break;
+          dev::tc_fence_after();
+#pragma unroll
+          for (int cg = 0; cg < QM_D; cg += 32) {
+            float o[32];
+            dev::tmem_ld_cols<32>(tmem + t_lane + 2 * QM_KC + cg, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= f;
+            dev::tmem_st_cols<32>(tmem + t_lane + 2 * QM_KC + cg, o);
+          }
+        }
+        l *= f;
+        m_ref = nr;
+      }
+      uint32_t pw[QM_KC / 2];
+#pragma unroll
+      for (int k = 0; k < QM_KC; k += 2) {
+        const float p0 = s[k] == -INFINITY ? 0.0f : dev::fast_exp2(s[k] - m_ref);
+        const float p1 = s[k + 1] == -INFINITY ? 0.0f : dev::fast_exp2(s[k + 1] - m_ref);
+        l += p0 + p1;
+        const __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+        pw[k / 2] = *reinterpret_cast<const uint32_t*>(&v2);
+      }
+      // the value product of chunk c - 2 read this P buffer
+      if (c > 1 && pv_done < c - 2) wait_pv(c - 2);
+      if (!ok) break;
+      unsigned char* slotp = ring + size_t(c % QM_ST) * QM_SLOT;
+      if ((c + 1) * QM_KC > L) {
+        // keys past the sequence in its last block may hold anything (NaN
+        // included): clear their V rows so that 0 * V = 0
+        const int key = r % QM_KC, hf = r / QM_KC;
+        if (c * QM_KC + key >= L) {
+          uint4* vrow = reinterpret_cast<uint4*>(slotp + 2 * QM_HALF_KV + hf * QM_HALF_KV + key * 128);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // P row r: 128 bytes, its 16-byte chunks at chunk XOR (r % 8) (128B swizzle)
+      unsigned char* pcur = pbuf + (c & 1) * QM_P_BYTES;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(pcur + r * 128 + ((ch ^ (r & 7)) << 4)) =
+            make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]);
+      dev::fence_async_smem();
+      dev::tc_fence_before();
+      dev::mbar_arrive(&bar_p[c & 1]);
+    }
+    if (ok && n > 0) wait_pv(n - 1);
+    if (ok) {
+      dev::tc_fence_after();
+      const float inv = l > 0.0f ? __frcp_rn(l) : 0.0f;
+      __nv_bfloat16* orow =
+          P.out + ((size_t(b) * Q + (valid ? i : 0)) * P.num_q_heads + hg * G + r % G) * QM_D;
+#pragma unroll
+      for (int cg = 0; cg < QM_D; cg += 32) {
+        float o[32];
+        dev::tmem_ld_cols<32>(tmem + t_lane + 2 * QM_KC + cg, o);
+        if (valid) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+              const __nv_bfloat162 v2 =
+                  __floats2bfloat162_rn(o[k + 2 * q2] * inv, o[k + 2 * q2 + 1] * inv);
+              w[q2] = *reinterpret_cast<const uint32_t*>(&v2);
+            }
+            *reinterpret_cast<uint4*>(orow + cg + k) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    } else if (tid == 0) {
+      atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // every copy issued but not consumed lands before shared memory is released
+    for (int c = *consumed; c < *issued; ++c)
+      (void)dev::mbar_wait(&full[c % QM_ST], uint32_t(c / QM_ST) & 1u);
+  }
+  dev::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    dev::tc_fence_after();
+    dev::tmem_dealloc(tmem, QM_TMEM_COLS);
+  }
+}
+
+template <int G>
+int launch_qm_t(const pa_decode_params* p, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, QM_SMEM);
+    if (e != cudaSuccess) return int(e);
+    configured = true;
+  }
+  const int H = p->num_kv_heads, Q = query_len_of(p);
+  const uint64_t cache_rows = uint64_t(p->num_blocks) * H * 16;
+  CUtensorMap tk, tv, tq;
+  int r = make_map(&tk, p->k_cache, cache_rows, QM_D, 16);
+  if (!r) r = make_map(&tv, p->v_cache, cache_rows, QM_D, 16);
+  if (!r) {
+    // q [B][Q][Hq][128]: box (64 d, G heads, QT tokens, 1 sequence)
+    const cuuint64_t dims[4] = {uint64_t(QM_D), uint64_t(p->num_q_heads), uint64_t(Q),
+                                uint64_t(p->num_seqs)};
+    const cuuint64_t strides[3] = {uint64_t(QM_D) * 2, uint64_t(p->num_q_heads) * QM_D * 2,
+                                   uint64_t(Q) * p->num_q_heads * QM_D * 2};
+    const cuuint32_t box[4] = {64, uint32_t(G), uint32_t(QM_ROWS / G), 1};
+    r = make_map_nd(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p->q, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (r) return r;
+  QmParams P;
+  P.block_tables = p->block_tables;
+  P.context_lens = p->context_lens;
+  P.out = static_cast<__nv_bfloat16*>(p->out);
+  P.num_seqs = p->num_seqs;
+  P.num_kv_heads = H;
+  P.num_q_heads = p->num_q_heads;
+  P.q_len = Q;
+  P.tiles = query_major_tiles(p);
+  P.max_blocks_per_seq = p->max_blocks_per_seq;
+  P.num_blocks = p->num_blocks;
+  P.cap = std::min(p->max_blocks_per_seq * 16, p->max_context_len);
+  P.oob_row = int(cache_rows);
+  P.scale_log2 = p->scale * kLog2e;
+  P.wait_ns = p->wait_timeout_us > 0 ? uint64_t(p->wait_timeout_us) * 1000u : dev::kWaitNsLimit;
+  const dim3 grid(unsigned(p->num_seqs) * unsigned(H) * unsigned(P.tiles));
+  query_major_kernel<G><<<grid, QM_THREADS, QM_SMEM, stream>>>(tk, tv, tq, P);
+  return int(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_query_major_tc(const pa_decode_params* p, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (p->num_q_heads / p->num_kv_heads) {
+    case 1: return launch_qm_t<1>(p, s);
+    case 2: return launch_qm_t<2>(p, s);
+    case 4: return launch_qm_t<4>(p, s);
+    case 8: return launch_qm_t<8>(p, s);
+    default: return int(cudaErrorInvalidValue);
+  }
+}
+
+int read_and_clear_query_major_errors(uint32_t* flags) {
+  return read_and_clear_tc_error_word(flags);
+}
+
+}  // namespace pa

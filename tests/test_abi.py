@@ -198,10 +198,17 @@ def test_decode_workspace_size(pk):
         p = _params(pk, query_len=ql)
         assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(2, 8, 128, 1, 256,
                                                                              QL=ql)
-    p = _params(pk, num_seqs=64, num_q_heads=32, num_kv_heads=8, max_context_len=2048,
+    p = _params(pk, num_seqs=8, num_q_heads=32, num_kv_heads=8, max_context_len=2048,
                 max_blocks_per_seq=128, query_len=16)
-    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(8, 32, 128, 4, 256,
                                                                          Hkv=8, QL=16)
+    # ... unless the batch gives the query-major kernel 128 (sequence, KV head,
+    # 128-row tile) CTAs: it splits no keys and needs the header only
+    p.num_seqs = 64
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == 256
+    p.query_len = 4  # one column group: the column-layout decode
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
+                                                                         Hkv=8, QL=4)
     # several new tokens on the CUDA-core kernel: partials per (sequence, token)
     for ql in (2, 7):
         p = _params(pk, query_len=ql, max_context_len=2048, max_blocks_per_seq=128, variant=1)

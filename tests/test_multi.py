@@ -169,6 +169,92 @@ def test_multi_placement_invariance_bit_exact(pk):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+# ---------------------------------------------------------------- query-major kernel
+#
+# When the column-group decode would need several groups and the batch gives
+# at least 128 (sequence, KV head, 128-row tile) CTAs, the new tokens run on
+# the query-major tensor-core kernel: each CTA streams one KV head's blocks
+# once for up to 128 query rows (tokens x G heads).
+
+QM_LENS = [64, 65, 63, 129, 200, 511, 513, 1025, 2049, 100, 300, 700, 90, 1500, 127, 128]
+
+
+def _qm_lens(QL, B=16):
+    lens = [max(L, QL) for L in QM_LENS]
+    lens[0], lens[1] = QL, QL + 1  # every key a new token; one older key
+    return (lens * ((B + len(lens) - 1) // len(lens)))[:B]
+
+
+@pytest.mark.parametrize("G,Hkv,QL,B", [(4, 8, 8, 16), (4, 8, 16, 16), (8, 8, 4, 16),
+                                        (1, 8, 33, 16), (2, 8, 64, 16), (4, 8, 64, 16),
+                                        (8, 4, 16, 32), (8, 8, 40, 16)])
+def test_query_major_against_the_oracle(pk, G, Hkv, QL, B):
+    """Lengths from Q (every key a new token) across chunk (64 keys) and block
+    boundaries to 2049; one and two 128-row tiles (Q x G = 256)."""
+    q, kc, vc, tables, lens, torch = _case(_qm_lens(QL, B), QL, G * Hkv, Hkv, 128,
+                                           seed=700 + G * 10 + QL)
+    _check(pk, q, kc, vc, tables, lens, torch)
+
+
+def test_query_major_short_and_empty_sequences(pk):
+    QL = 8
+    lens = _qm_lens(QL)
+    lens[3], lens[5], lens[7] = 0, 5, 0  # empty, and too short for the new tokens
+    q, kc, vc, tables, lens, torch = _case(lens, QL, 32, 8, 128, seed=720)
+    out = torch.full_like(q, 7.0)
+    pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                 max_context_len=int(lens.max()), out=out)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() & DEVERR_CONTEXT_LEN
+    got = harness.bf16_tensor_to_f64(out)
+    for b in (3, 5, 7):
+        assert not got[b].any()
+    keep = [b for b in range(len(lens)) if b not in (3, 5, 7)]
+    want = oracle.paged_decode_multi(q.cpu()[keep], kc.cpu(), vc.cpu(), tables[keep], lens[keep])
+    harness.assert_close(got[keep], want)
+
+
+def test_query_major_placement_invariance_bit_exact(pk):
+    import torch
+
+    q, kc, vc, tables, lens, _ = _case(_qm_lens(16), 16, 32, 8, 128, seed=721)
+    NB = kc.shape[0]
+    perm = np.random.default_rng(29).permutation(NB)
+    kcb, vcb = torch.empty_like(kc), torch.empty_like(vc)
+    kcb[torch.from_numpy(perm).cuda()] = kc
+    vcb[torch.from_numpy(perm).cuda()] = vc
+    tables_b = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    a = _decode(pk, q, kc, vc, tables, lens, torch)
+    b = _decode(pk, q, kcb, vcb, tables_b, lens, torch)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_query_major_fused_append(pk):
+    """pa_append_decode on this path: the KV write with the slot rule, then the
+    query-major decode; caches bit-exact, rows against the oracle."""
+    QL = 16
+    lens = _qm_lens(QL)
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case(lens, QL, 32, 8, seed=722)
+    kc2, vc2 = kc.clone(), vc.clone()
+    out = pk.pa_append_decode(q, kc2, vc2, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
+                              torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() == 0
+    ko, vo = oracle.reshape_and_cache(kn.cpu(), vn.cpu(), oracle.bf16_bits(kc.cpu()),
+                                      oracle.bf16_bits(vc.cpu()), slots)
+    assert np.array_equal(oracle.bf16_bits(kc2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
+    want = oracle.paged_decode_multi(q.cpu(), ko, vo, tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+
+
+def test_query_major_llama8b_layer(pk):
+    """The bench's 8B layer with 16 new tokens per sequence (the query-major path)."""
+    r = workloads.llama8b_layer()
+    _check(pk, *_case(r.lens0 + 16, 16, 32, 8, 128, seed=723))
+
+
 # ---------------------------------------------------------------- CUDA-core kernel
 #
 # The CUDA-core variant decodes each (sequence, new token) row on its own:
