@@ -90,6 +90,19 @@ inline int query_major_tiles(const pa_decode_params* p) {
   const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
   return (rows + 127) / 128;
 }
+// KV heads per CTA: two (adjacent in a block, one 4 KiB box per half) when a
+// head has at most 64 rows and the head count is even, else one.
+inline int query_major_heads(const pa_decode_params* p) {
+  const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
+  return rows <= 64 && p->num_kv_heads % 2 == 0 ? 2 : 1;
+}
+// Copies of the rows in a tile: the 128 rows hold (heads x rows per head,
+// rounded up to 32 or 64) this many times.
+inline int query_major_copies(const pa_decode_params* p) {
+  const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
+  const int per_head = rows <= 32 ? 32 : (rows <= 64 ? 64 : 128);
+  return 128 / (per_head * query_major_heads(p));
+}
 // It takes the bf16 cache at head_dim 128 and block size 16 when the
 // column-group decode would split the new tokens into several groups (each
 // re-reading the keys) and the batch gives it at least 128 CTAs.

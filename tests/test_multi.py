@@ -185,12 +185,19 @@ def _qm_lens(QL, B=16):
     return (lens * ((B + len(lens) - 1) // len(lens)))[:B]
 
 
-@pytest.mark.parametrize("G,Hkv,QL,B", [(4, 8, 8, 16), (4, 8, 16, 16), (8, 8, 4, 16),
-                                        (1, 8, 33, 16), (2, 8, 64, 16), (4, 8, 64, 16),
-                                        (8, 4, 16, 32), (8, 8, 40, 16)])
+@pytest.mark.parametrize("G,Hkv,QL,B", [
+    # at most 32 rows (tokens x G): four copies of each row, 16 keys of a chunk each
+    (4, 8, 8, 16), (8, 8, 4, 16), (1, 8, 20, 16), (2, 8, 12, 16), (4, 8, 5, 16), (8, 8, 3, 16),
+    # at most 64 rows: two copies, 32 keys each
+    (4, 8, 16, 16), (1, 8, 33, 16), (2, 8, 24, 16), (4, 8, 12, 16), (8, 8, 6, 16),
+    # one copy; one, two and three 128-row tiles
+    (2, 8, 64, 16), (4, 8, 64, 16), (8, 4, 16, 32), (8, 8, 40, 16),
+    # an odd number of KV heads: one head per CTA (four copies; two)
+    (2, 3, 16, 48), (8, 1, 6, 128)])
 def test_query_major_against_the_oracle(pk, G, Hkv, QL, B):
-    """Lengths from Q (every key a new token) across chunk (64 keys) and block
-    boundaries to 2049; one and two 128-row tiles (Q x G = 256)."""
+    """Lengths from Q (every key a new token) across chunk and block boundaries
+    to 2049; two KV heads per CTA (rows held twice or once) or one (four
+    times, twice, once), partly filled tiles and several tiles per head."""
     q, kc, vc, tables, lens, torch = _case(_qm_lens(QL, B), QL, G * Hkv, Hkv, 128,
                                            seed=700 + G * 10 + QL)
     _check(pk, q, kc, vc, tables, lens, torch)
