@@ -24,7 +24,7 @@ SOURCES = ["pa_decode_tc.cu", "pa_decode_tc_d64.cu", "pa_decode_tc_fp8.cu", "pa_
            "pa_decode_tc_bs32_d64.cu", "pa_prefill_tc.cu", "pa_decode.cu", "pa_cache.cu", "pa_fp8.cu",
            "pa_query.cu",
            "pa_api.cpp", "pa_pool.cpp"]
-HEADERS = ["pa_device.cuh", "pa_decode_tc.cuh", "pa_internal.h"]
+HEADERS = ["pa_device.cuh", "pa_decode_tc.cuh", "pa_internal.h", "pa_query_major.h"]
 
 
 def _nvcc() -> str:

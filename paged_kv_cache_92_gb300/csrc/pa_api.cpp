@@ -8,6 +8,7 @@
 #include <cstring>
 
 #include "pa_internal.h"
+#include "pa_query_major.h"
 
 namespace pa {
 

@@ -84,36 +84,6 @@ inline int64_t tc_virtual_seqs(const pa_decode_params* p) {
   return int64_t(p->num_seqs) * tc_n_groups(p);
 }
 
-// Query-major tensor-core kernel (pa_prefill_tc.cu) for many new tokens:
-// one CTA per (sequence, KV head, tile of 128 query rows = tokens x G heads).
-inline int query_major_tiles(const pa_decode_params* p) {
-  const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
-  return (rows + 127) / 128;
-}
-// KV heads per CTA: two (adjacent in a block, one 4 KiB box per half) when a
-// head has at most 64 rows and the head count is even, else one.
-inline int query_major_heads(const pa_decode_params* p) {
-  const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
-  return rows <= 64 && p->num_kv_heads % 2 == 0 ? 2 : 1;
-}
-// Copies of the rows in a tile: the 128 rows hold (heads x rows per head,
-// rounded up to 32 or 64) this many times.
-inline int query_major_copies(const pa_decode_params* p) {
-  const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
-  const int per_head = rows <= 32 ? 32 : (rows <= 64 ? 64 : 128);
-  return 128 / (per_head * query_major_heads(p));
-}
-// It takes the bf16 cache at head_dim 128 and block size 16 when the
-// column-group decode would split the new tokens into several groups (each
-// re-reading the keys) and the batch gives it at least 128 CTAs.
-inline bool use_query_major(const pa_decode_params* p) {
-  const int g = p->num_q_heads / p->num_kv_heads;
-  return p->variant == PA_DECODE_TENSOR_CORE && p->kv_dtype == PA_KV_BF16 && p->head_dim == 128 &&
-         p->block_size == 16 && query_len_of(p) > 1 && (g == 1 || g == 2 || g == 4 || g == 8) &&
-         tc_n_groups(p) > 1 &&
-         int64_t(p->num_seqs) * p->num_kv_heads * query_major_tiles(p) >= 128;
-}
-
 // Columns padded to the tensor-core N (16, 32, 64 or 128).
 inline int tc_n_pad(int cols) {
   return cols <= 16 ? 16 : (cols <= 32 ? 32 : (cols <= 64 ? 64 : 128));
@@ -242,9 +212,7 @@ int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32
 
 // Device error words, one per kernel translation unit: read and clear.
 int read_and_clear_decode_errors(uint32_t* flags);
-int read_and_clear_decode_tc_errors(uint32_t* flags);
-int launch_query_major_tc(const pa_decode_params* p, void* stream);
-int read_and_clear_query_major_errors(uint32_t* flags);  // all three shares below
+int read_and_clear_decode_tc_errors(uint32_t* flags);  // all three shares below
 int read_and_clear_decode_tc_d64_errors(uint32_t* flags);
 int read_and_clear_decode_tc_fp8_errors(uint32_t* flags);
 int read_and_clear_decode_tc_bs8_errors(uint32_t* flags);

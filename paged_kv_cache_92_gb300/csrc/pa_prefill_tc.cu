@@ -28,6 +28,7 @@
 //    scores a chunk and the softmax spreads over the four SM sub-partitions.
 //    The copies of a row are merged once, at the end, as split-K partials are.
 #include "pa_decode_tc.cuh"
+#include "pa_query_major.h"
 
 namespace pa {
 namespace {
@@ -107,24 +108,28 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   // Longest sequences first (the CTAs start in index order, so the last wave
   // holds the shortest work): up to 256 sequences every CTA ranks the lengths
   // and takes the sequence of its rank (ties by index).
-  int b = rank;
+  int b = rank, L;
   if (P.num_seqs <= 256) {
+    // the lengths staged in the (not yet used) P buffer, one load each
+    int* lens_s = reinterpret_cast<int*>(pbuf);
+    for (int v = tid; v < P.num_seqs; v += QM_THREADS) lens_s[v] = P.context_lens[v];
     if (tid == 0) *found = rank;
     __syncthreads();
     for (int v = tid; v < P.num_seqs; v += QM_THREADS) {
-      const int Lv = P.context_lens[v];
+      const int Lv = lens_s[v];
       int above = 0;
       for (int u = 0; u < P.num_seqs; ++u) {
-        const int Lu = P.context_lens[u];
+        const int Lu = lens_s[u];
         above += Lu > Lv || (Lu == Lv && u < v);
       }
       if (above == rank) *found = v;
     }
     __syncthreads();
     b = *found;
+    L = lens_s[b];
+  } else {
+    L = P.context_lens[b];
   }
-
-  int L = P.context_lens[b];
   const bool report = tid == 0 && tile == 0 && hg0 == 0;
   if (L > P.cap) {
     if (report) atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
