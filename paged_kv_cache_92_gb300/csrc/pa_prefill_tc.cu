@@ -9,10 +9,12 @@
 // and streams them once per group of new tokens; with many new tokens each
 // group re-reads the keys. Here the queries are on the M side:
 //   S[128 rows][64 columns]  = Q . K^T     (A = Q, B = K chunk, both K-major)
-//   O[128 rows][128 d]      += P . V       (A = P, K-major; B = V, MN-major)
-// with S and P double-buffered and O in TMEM (256 columns). A thread owns a
-// row: its softmax (running maximum, sum, the conditional rescale of its O
-// row) needs no other thread.
+//   O[128 rows][128 d]      += P . V       (A = P from TMEM; B = V, MN-major)
+// with S double-buffered and O in TMEM (256 columns). P (bf16, two to a
+// 32-bit column) overwrites the first 32 columns of its chunk's S buffer and
+// feeds the value product from there, so shared memory holds Q and the K/V
+// ring only. A thread owns a row: its softmax (running maximum, sum, the
+// conditional rescale of its O row) needs no other thread.
 //
 // Layout of a tile's 128 rows (TMEM lanes): R copies x HB heads x RPH rows,
 // row r0 of a head being token tile*QT + r0/G, query head g = r0 % G.
@@ -27,6 +29,7 @@
 //    its own running maximum and sum, so each thread exponentiates 16 or 32
 //    scores a chunk and the softmax spreads over the four SM sub-partitions.
 //    The copies of a row are merged once, at the end, as split-K partials are.
+//    A row's P is zero outside its own keys.
 #include "pa_decode_tc.cuh"
 #include "pa_query_major.h"
 
@@ -36,25 +39,36 @@ namespace {
 constexpr int QM_D = 128;
 constexpr int QM_KC = 64;         // columns per chunk
 constexpr int QM_ROWS = 128;      // query rows per tile (MMA M)
-constexpr int QM_ST = 5;          // ring slots
+constexpr int QM_ST = 6;          // ring slots
 constexpr int QM_THREADS = 192;   // softmax warps 0-3, producer 4, MMA 5
 constexpr int QM_HALF_Q = QM_ROWS * 128;     // one 64-d half of Q: [128 rows][128 B]
 constexpr int QM_Q_BYTES = 2 * QM_HALF_Q;
 constexpr int QM_HALF_KV = QM_KC * 128;      // one 64-d half of a K or V chunk: [64 rows][128 B]
 constexpr int QM_KV_BYTES = 2 * QM_HALF_KV;  // K (or V) of a chunk
 constexpr int QM_SLOT = 2 * QM_KV_BYTES;     // K halves, then V halves
-constexpr int QM_P_BYTES = QM_ROWS * 128;    // one P buffer: [128 rows][64 columns] bf16
 constexpr int QM_OFF_Q = 0;
 constexpr int QM_OFF_RING = QM_OFF_Q + QM_Q_BYTES;
-constexpr int QM_OFF_P = QM_OFF_RING + QM_ST * QM_SLOT;
-constexpr int QM_OFF_BARS = QM_OFF_P + 2 * QM_P_BYTES;
+constexpr int QM_OFF_BARS = QM_OFF_RING + QM_ST * QM_SLOT;
 constexpr int QM_NBARS = 2 * QM_ST + 8;  // full, empty, qfull, s[2], p[2], o[2], drain
 constexpr int QM_OFF_WORDS = QM_OFF_BARS + QM_NBARS * 8;
-constexpr int QM_SMEM = QM_OFF_WORDS + 64 + 1024;  // + alignment slack
+constexpr int QM_OFF_LENS = QM_OFF_WORDS + 64;      // up to 256 sequence lengths
+constexpr int QM_SMEM = QM_OFF_LENS + 1024 + 1024;  // + alignment slack
 static_assert(QM_SMEM <= kMaxDynSmem, "shared memory budget");
-constexpr uint32_t QM_TMEM_COLS = 256;  // S[2] at [0, 128), O at [128, 256)
+constexpr uint32_t QM_TMEM_COLS = 256;  // S[2] (P in each's first 32) at [0, 128), O at [128, 256)
 constexpr uint32_t QM_IDESC_S = dev::idesc_bf16_f32(QM_ROWS, QM_KC, false, false);
 constexpr uint32_t QM_IDESC_PV = dev::idesc_bf16_f32(QM_ROWS, QM_D, false, true);
+
+// tcgen05.mma with A in TMEM (M rows in lanes; a K = 16 step is 8 columns,
+// two bf16 of a row per 32-bit column, the lower-indexed in the low half).
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
+      : "memory");
+}
 
 struct QmParams {
   const int32_t* block_tables;
@@ -84,14 +98,13 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* qbuf = smem + QM_OFF_Q;
   unsigned char* ring = smem + QM_OFF_RING;
-  unsigned char* pbuf = smem + QM_OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QM_OFF_BARS);
   uint64_t* full = bars;
   uint64_t* empty = bars + QM_ST;
   uint64_t* qfull = bars + 2 * QM_ST;
   uint64_t* bar_s = qfull + 1;  // [2] scores of chunk c in S[c % 2]
-  uint64_t* bar_p = bar_s + 2;  // [2] P[c % 2] of chunk c written, S[c % 2] read
-  uint64_t* bar_o = bar_p + 2;  // [2] value product of chunk c (which read P[c % 2]) done
+  uint64_t* bar_p = bar_s + 2;  // [2] P of chunk c written over S[c % 2]
+  uint64_t* bar_o = bar_p + 2;  // [2] value product of chunk c (which read S[c % 2]'s P) done
   uint64_t* drain = bar_o + 2;
   int* words = reinterpret_cast<int*>(smem + QM_OFF_WORDS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&words[0]);
@@ -110,8 +123,8 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   // and takes the sequence of its rank (ties by index).
   int b = rank, L;
   if (P.num_seqs <= 256) {
-    // the lengths staged in the (not yet used) P buffer, one load each
-    int* lens_s = reinterpret_cast<int*>(pbuf);
+    // the lengths staged in shared memory, one load each
+    int* lens_s = reinterpret_cast<int*>(smem + QM_OFF_LENS);
     for (int v = tid; v < P.num_seqs; v += QM_THREADS) lens_s[v] = P.context_lens[v];
     if (tid == 0) *found = rank;
     __syncthreads();
@@ -241,7 +254,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   } else if (warp == 5) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
-      const uint32_t qb = dev::smem_addr(qbuf), pb = dev::smem_addr(pbuf);
+      const uint32_t qb = dev::smem_addr(qbuf);
       bool ok = dev::mbar_wait(qfull, 0, P.wait_ns, abort_flag);
       auto issue_s = [&](int c) {
         const uint32_t kb = dev::smem_addr(ring + size_t(c % QM_ST) * QM_SLOT);
@@ -256,16 +269,18 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
         }
         dev::mma_commit(&bar_s[c & 1]);
       };
-      // Event loop: the scores of chunk s once it has landed (its S buffer was
-      // read by the softmax of chunk s - 2, whose value product is issued), and
-      // the value product of chunk v once the softmax has written its P --
-      // whichever is ready first, so that neither waits behind the other.
+      // Event loop: the scores of chunk s once it has landed and the value
+      // product of chunk s - 2 (which read P from the same S buffer) has
+      // completed, and the value product of chunk v once the softmax has
+      // written its P -- whichever is ready first, so that neither waits
+      // behind the other.
       int s_next = 0, v_next = 0;
       uint64_t t_idle = 0;
       uint32_t idle = 0;
       while (ok && v_next < n) {
         bool progress = false;
         if (s_next < n && s_next <= v_next + 1 &&
+            (s_next < 2 || dev::mbar_test(&bar_o[s_next & 1], uint32_t((s_next - 2) >> 1) & 1u)) &&
             dev::mbar_test(&full[s_next % QM_ST], uint32_t(s_next / QM_ST) & 1u)) {
           issue_s(s_next);
           ++s_next;
@@ -278,13 +293,11 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           const uint32_t vb = dev::smem_addr(ring + size_t(c % QM_ST) * QM_SLOT + QM_KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < QM_KC / 16; ++kk)
-            dev::mma_bf16(tmem + 2 * QM_KC,
-                          dev::smem_desc(pb + uint32_t(c & 1) * QM_P_BYTES + kk * 32, 16, 1024,
-                                         dev::kSwizzle128B),
-                          // V MN-major: next 8 rows 1024 B on (SBO), second 64-d
-                          // half one half on (LBO)
-                          dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
-                          QM_IDESC_PV, c > 0 || kk > 0);
+            mma_bf16_tmem_a(tmem + 2 * QM_KC, tmem + uint32_t(c & 1) * QM_KC + uint32_t(kk * 8),
+                            // V MN-major: next 8 rows 1024 B on (SBO), second 64-d
+                            // half one half on (LBO)
+                            dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
+                            QM_IDESC_PV, c > 0 || kk > 0);
           dev::mma_commit(&bar_o[c & 1]);
           dev::mma_commit(&empty[c % QM_ST]);
           *consumed = c + 1;
@@ -327,14 +340,6 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     float m_ref = -INFINITY, l = 0.0f;
     int pv_done = -1;
     bool ok = true;
-    if (R > 1 || HB > 1) {
-      // this row's P is zero outside its own keys, written once here
-      for (int k = 0; k < 2; ++k)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(pbuf + k * QM_P_BYTES + r * 128 + ch * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-    }
     // value product of chunk k done (it completes bar_o[k % 2], phase k / 2)
     auto wait_pv = [&](int k) {
       ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[k & 1], uint32_t(k >> 1) & 1u,
@@ -415,9 +420,6 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
         pw[k / 2] = *reinterpret_cast<const uint32_t*>(&v2);
       }
       l += la + lb;
-      // the value product of chunk c - 2 read this P buffer
-      if (c > 1 && pv_done < c - 2) wait_pv(c - 2);
-      if (!ok) break;
       if ((c + 1) * NB * 16 > L) {
         // keys past the sequence in its last block may hold anything (NaN
         // included): clear their V rows so that 0 * V = 0. Thread r clears
@@ -429,20 +431,22 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0u, 0u, 0u, 0u);
         }
+        dev::fence_async_smem();  // before the value product reads the ring
       }
-      // P row r: 128 bytes, its 16-byte chunks at chunk XOR (r % 8) (128B
-      // swizzle); block u's 16 columns of this head are chunks (u*BR + h*16)/8 + {0, 1}
-      unsigned char* pcur = pbuf + (c & 1) * QM_P_BYTES + r * 128;
+      // P over the first 32 columns of this chunk's S buffer (its scores are
+      // in registers): column j holds columns 2j, 2j+1 of the chunk; block u's
+      // 16 columns of this head are P columns (u*BR + h*16)/2 + [0, 8), the
+      // rest zero. The value product of chunk c - 2, which read this buffer's
+      // last P, completed before S(c) was issued.
+      {
+        float pp[QM_KC / 2];
 #pragma unroll
-      for (int t = 0; t < TB; ++t)
-#pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-          const int ch = ((q * TB + t) * BR + h * 16) / 8 + hc;
-          const int w = 8 * t + 4 * hc;
-          *reinterpret_cast<uint4*>(pcur + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(pw[w], pw[w + 1], pw[w + 2], pw[w + 3]);
+        for (int k = 0; k < QM_KC / 2; ++k) {
+          const int u = 2 * k / BR, hh = 2 * k % BR / 16;  // block and head of P column k
+          pp[k] = u / TB == q && hh == h ? __uint_as_float(pw[8 * (u % TB) + k % 8]) : 0.0f;
         }
-      dev::fence_async_smem();
+        dev::tmem_st_cols<QM_KC / 2>(tmem + t_lane + uint32_t(c & 1) * QM_KC, pp);
+      }
       dev::tc_fence_before();
       dev::mbar_arrive(&bar_p[c & 1]);
     }
