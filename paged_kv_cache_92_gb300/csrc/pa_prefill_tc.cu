@@ -1,35 +1,36 @@
-// Several new tokens per sequence on the tensor cores, query-major: one CTA per
-// (sequence, group of HB KV heads, tile of query rows) streams those heads'
-// blocks once for all their rows ("How Paged Attention and Continuous Batching
-// Actually Work", §Continuous batching: the scheduled tokens of one request,
-// as in a chunked prefill). A row is new token i of query head (kv head)*G + g
-// and sees the sequence's first L - Q + i + 1 keys.
+// Several new tokens per sequence on the tensor cores, query-major ("How Paged
+// Attention and Continuous Batching Actually Work", §Continuous batching: the
+// scheduled tokens of one request, as in a chunked prefill). A unit of work (an
+// item) is (sequence, group of HB KV heads, tile of query rows); it streams
+// those heads' blocks once for all its rows. A row is new token i of query head
+// (kv head)*G + g and sees the sequence's first L - Q + i + 1 keys.
 //
 // The column-group decode (pa_decode_tc.cuh) puts the keys on the MMAs' M side
 // and streams them once per group of new tokens; with many new tokens each
 // group re-reads the keys. Here the queries are on the M side:
 //   S[128 rows][64 columns]  = Q . K^T     (A = Q, B = K chunk, both K-major)
 //   O[128 rows][128 d]      += P . V       (A = P from TMEM; B = V, MN-major)
-// with S double-buffered and O in TMEM (256 columns). P (bf16, two to a
-// 32-bit column) overwrites the first 32 columns of its chunk's S buffer and
-// feeds the value product from there, so shared memory holds Q and the K/V
-// ring only. A thread owns a row: its softmax (running maximum, sum, the
-// conditional rescale of its O row) needs no other thread.
+// S and P are double-buffered in TMEM; P (bf16, two to a 32-bit column) feeds
+// the value product from there, in columns of its own so that the scores of
+// the next chunks need not wait for the value product that reads it. A thread
+// owns a row: its softmax (running maximum, sum, the conditional rescale of
+// its O row) needs no other thread.
 //
-// Layout of a tile's 128 rows (TMEM lanes): R copies x HB heads x RPH rows,
-// row r0 of a head being token tile*QT + r0/G, query head g = r0 % G.
-//  * A chunk's 64 columns are NB = 4/HB blocks x HB heads x 16 keys: one
-//    2-D tensor-map box [HB*16 rows][64 d] per block and 64-d half (the HB
-//    heads of a block are adjacent in the cache), so with HB = 2 every TMA
-//    request moves 4 KiB (the TMA unit's fixed cost per request caps 2 KiB
-//    requests well below the HBM rate). A row's scores against the other
-//    heads' keys are computed and ignored: its P row is zero there.
-//  * With at most 32 (or 64) rows per head-group the rows are held R = 2 (or
-//    4) times over; copy q takes blocks [q*NB/R, (q+1)*NB/R) of each chunk with
-//    its own running maximum and sum, so each thread exponentiates 16 or 32
-//    scores a chunk and the softmax spreads over the four SM sub-partitions.
-//    The copies of a row are merged once, at the end, as split-K partials are.
-//    A row's P is zero outside its own keys.
+// Persistent: one CTA per SM takes the items of its rank in a snake over the
+// items sorted by sequence length (longest first, every second pass reversed).
+// The producer, MMA and softmax warps each walk that list and keep their own
+// counters, so the loads of the next item overlap the end of the current one:
+// two Q buffers in shared memory, two O accumulators in TMEM, and one K/V
+// ring whose chunk and barrier phases run on across items.
+//
+// Layout of an item's 128 rows (TMEM lanes): HB heads x RPH rows, row r0 of a
+// head being token tile*QT + r0/G, query head g = r0 % G. A chunk's 64 columns
+// are NB = 4/HB blocks x HB heads x 16 keys: one 2-D tensor-map box
+// [HB*16 rows][64 d] per block and 64-d half (the HB heads of a block are
+// adjacent in the cache), so with HB = 2 every TMA request moves 4 KiB (the
+// TMA unit spends a fixed time per request: streaming 2 KiB requests tops out
+// well below 4 KiB ones). A row's scores against the other heads' keys are
+// computed and ignored: its P is zero there.
 #include "pa_decode_tc.cuh"
 #include "pa_query_major.h"
 
@@ -38,23 +39,27 @@ namespace {
 
 constexpr int QM_D = 128;
 constexpr int QM_KC = 64;         // columns per chunk
-constexpr int QM_ROWS = 128;      // query rows per tile (MMA M)
-constexpr int QM_ST = 6;          // ring slots
+constexpr int QM_ROWS = 128;      // query rows per item (MMA M)
+constexpr int QM_ST = 5;          // ring slots
 constexpr int QM_THREADS = 192;   // softmax warps 0-3, producer 4, MMA 5
 constexpr int QM_HALF_Q = QM_ROWS * 128;     // one 64-d half of Q: [128 rows][128 B]
 constexpr int QM_Q_BYTES = 2 * QM_HALF_Q;
 constexpr int QM_HALF_KV = QM_KC * 128;      // one 64-d half of a K or V chunk: [64 rows][128 B]
 constexpr int QM_KV_BYTES = 2 * QM_HALF_KV;  // K (or V) of a chunk
 constexpr int QM_SLOT = 2 * QM_KV_BYTES;     // K halves, then V halves
-constexpr int QM_OFF_Q = 0;
-constexpr int QM_OFF_RING = QM_OFF_Q + QM_Q_BYTES;
+constexpr int QM_OFF_Q = 0;                  // two Q buffers
+constexpr int QM_OFF_RING = QM_OFF_Q + 2 * QM_Q_BYTES;
 constexpr int QM_OFF_BARS = QM_OFF_RING + QM_ST * QM_SLOT;
-constexpr int QM_NBARS = 2 * QM_ST + 8;  // full, empty, qfull, s[2], p[2], o[2], drain
+// full[ST], empty[ST], qfull[2], qempty[2], s[2], p[2], o[2], oempty[2], drain
+constexpr int QM_NBARS = 2 * QM_ST + 13;
 constexpr int QM_OFF_WORDS = QM_OFF_BARS + QM_NBARS * 8;
-constexpr int QM_OFF_LENS = QM_OFF_WORDS + 64;      // up to 256 sequence lengths
-constexpr int QM_SMEM = QM_OFF_LENS + 1024 + 1024;  // + alignment slack
+constexpr int QM_OFF_ORDER = QM_OFF_WORDS + 64;      // sequence of each length rank (<= 256)
+constexpr int QM_SMEM = QM_OFF_ORDER + 1024 + 1024;  // + alignment slack
 static_assert(QM_SMEM <= kMaxDynSmem, "shared memory budget");
-constexpr uint32_t QM_TMEM_COLS = 256;  // S[2] (P in each's first 32) at [0, 128), O at [128, 256)
+constexpr int QM_MAX_RANKED = 256;
+// TMEM: S[2] at [0, 128), O[2] at [128, 384), P[2] at [384, 448)
+constexpr uint32_t QM_TMEM_COLS = 512;
+constexpr uint32_t QM_TMEM_P = 384;
 constexpr uint32_t QM_IDESC_S = dev::idesc_bf16_f32(QM_ROWS, QM_KC, false, false);
 constexpr uint32_t QM_IDESC_PV = dev::idesc_bf16_f32(QM_ROWS, QM_D, false, true);
 
@@ -74,25 +79,31 @@ struct QmParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   __nv_bfloat16* out;
-  int num_seqs, num_kv_heads, num_q_heads, q_len, tiles, head_groups, max_blocks_per_seq,
-      num_blocks, cap, oob_row;
+  int num_seqs, num_kv_heads, num_q_heads, q_len, tiles, head_groups, num_items,
+      max_blocks_per_seq, num_blocks, cap, oob_row;
   float scale_log2;
   uint64_t wait_ns;
 };
 
-template <int G, int R, int HB>
+// One item as every role sees it.
+struct QmItem {
+  int b, hg0, tile;  // sequence, first KV head, tile of new tokens
+  int L;             // length after the rules (0: an empty sequence)
+  int nblk, n;       // blocks the item's last row sees, chunks
+  bool bad_len;      // the length broke a rule (reported once per sequence)
+};
+
+template <int G, int HB>
 __global__ void __launch_bounds__(QM_THREADS, 1)
     query_major_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_q, const QmParams P) {
-  constexpr int RW = QM_ROWS / R;   // rows per copy
-  constexpr int RPH = RW / HB;      // rows per head
-  constexpr int QT = RPH / G;       // new tokens per tile
-  constexpr int NB = 4 / HB;        // blocks per chunk
-  constexpr int BR = 16 * HB;       // rows of one block's box (HB heads x 16 keys)
-  constexpr int TB = NB / R;        // blocks of a chunk per copy
-  constexpr int NC = 16 * TB;       // scores of a chunk per thread
-  static_assert(QT >= 1 && RPH >= 32 && TB >= 1, "tile shape");
+  constexpr int RPH = QM_ROWS / HB;  // rows per head
+  constexpr int QT = RPH / G;        // new tokens per item
+  constexpr int NB = 4 / HB;         // blocks per chunk
+  constexpr int BR = 16 * HB;        // rows of one block's box (HB heads x 16 keys)
+  constexpr int NC = 16 * NB;        // scores of a chunk per thread (its head's keys)
+  static_assert(QT >= 1, "tile shape");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -101,32 +112,32 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QM_OFF_BARS);
   uint64_t* full = bars;
   uint64_t* empty = bars + QM_ST;
-  uint64_t* qfull = bars + 2 * QM_ST;
-  uint64_t* bar_s = qfull + 1;  // [2] scores of chunk c in S[c % 2]
-  uint64_t* bar_p = bar_s + 2;  // [2] P of chunk c written over S[c % 2]
-  uint64_t* bar_o = bar_p + 2;  // [2] value product of chunk c (which read S[c % 2]'s P) done
-  uint64_t* drain = bar_o + 2;
+  uint64_t* qfull = bars + 2 * QM_ST;  // [2] Q of the item landed in buffer k
+  uint64_t* qempty = qfull + 2;        // [2] the last scores reading Q buffer k completed
+  uint64_t* bar_s = qempty + 2;        // [2] scores of chunk c (global count) in S[c % 2]
+  uint64_t* bar_p = bar_s + 2;         // [2] P of chunk c written (P[c % 2]), S[c % 2] read
+  uint64_t* bar_o = bar_p + 2;         // [2] value product of chunk c done
+  uint64_t* oempty = bar_o + 2;        // [2] O accumulator k read out by the softmax warps
+  uint64_t* drain = oempty + 2;
   int* words = reinterpret_cast<int*>(smem + QM_OFF_WORDS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&words[0]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&words[1]);
-  int* issued = &words[2];
-  int* consumed = &words[3];
-  int* found = &words[4];  // the sequence of this CTA's rank (below)
+  int* issued = &words[2];     // K/V chunks requested
+  int* consumed = &words[3];   // K/V chunks whose value product was issued
+  int* q_issued = &words[4];   // Q loads requested
+  int* q_waited = &words[5];   // Q loads seen landed
+  int* order = reinterpret_cast<int*>(smem + QM_OFF_ORDER);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = int(blockIdx.x) % P.tiles;
-  const int hg0 = (int(blockIdx.x) / P.tiles) % P.head_groups * HB;  // first KV head
-  const int rank = int(blockIdx.x) / (P.tiles * P.head_groups);
   const int Q = P.q_len;
-  // Longest sequences first (the CTAs start in index order, so the last wave
-  // holds the shortest work): up to 256 sequences every CTA ranks the lengths
-  // and takes the sequence of its rank (ties by index).
-  int b = rank, L;
-  if (P.num_seqs <= 256) {
-    // the lengths staged in shared memory, one load each
-    int* lens_s = reinterpret_cast<int*>(smem + QM_OFF_LENS);
+  const bool ranked = P.num_seqs <= QM_MAX_RANKED;
+
+  // ------------------------------------------------------------ set-up
+  if (ranked) {
+    // Sequences by decreasing length (ties by index): the lengths are staged
+    // in the ring (before any copy lands there), then order[rank] = sequence.
+    int* lens_s = reinterpret_cast<int*>(ring);
     for (int v = tid; v < P.num_seqs; v += QM_THREADS) lens_s[v] = P.context_lens[v];
-    if (tid == 0) *found = rank;
     __syncthreads();
     for (int v = tid; v < P.num_seqs; v += QM_THREADS) {
       const int Lv = lens_s[v];
@@ -135,54 +146,29 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
         const int Lu = lens_s[u];
         above += Lu > Lv || (Lu == Lv && u < v);
       }
-      if (above == rank) *found = v;
+      order[above] = v;
     }
-    __syncthreads();
-    b = *found;
-    L = lens_s[b];
-  } else {
-    L = P.context_lens[b];
+    dev::fence_async_smem();  // the staged lengths before the ring's first copy
   }
-  const bool report = tid == 0 && tile == 0 && hg0 == 0;
-  if (L > P.cap) {
-    if (report) atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
-    L = P.cap;
-  }
-  if (L > 0 && L < Q) {  // no room for the new tokens: an empty sequence
-    if (report) atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
-    L = 0;
-  }
-  const int i_last = min(Q, (tile + 1) * QT) - 1;  // the tile's last new token
-  if (L <= 0) {  // zero rows
-    for (int e = tid; e < HB * RPH * (QM_D / 8); e += QM_THREADS) {
-      const int x = e / (QM_D / 8), ch = e % (QM_D / 8);
-      const int h = x / RPH, r0 = x % RPH, i = tile * QT + r0 / G;
-      if (i < Q && hg0 + h < P.num_kv_heads) {
-        const size_t row = (size_t(b) * Q + i) * P.num_q_heads + (hg0 + h) * G + r0 % G;
-        reinterpret_cast<uint4*>(P.out + row * QM_D)[ch] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    return;
-  }
-  const int keys = L - Q + i_last + 1;  // what the tile's last row sees
-  const int nblk = (keys + 15) / 16;
-  const int n = (nblk + NB - 1) / NB;
-
   if (tid == 0) {
     for (int s = 0; s < QM_ST; ++s) {
       dev::mbar_init(&full[s], 1);
       dev::mbar_init(&empty[s], 1);
     }
-    dev::mbar_init(qfull, 1);
     for (int k = 0; k < 2; ++k) {
+      dev::mbar_init(&qfull[k], 1);
+      dev::mbar_init(&qempty[k], 1);
       dev::mbar_init(&bar_s[k], 1);
       dev::mbar_init(&bar_p[k], 128);
       dev::mbar_init(&bar_o[k], 1);
+      dev::mbar_init(&oempty[k], 128);
     }
     dev::mbar_init(drain, 1);
     *abort_flag = 0;
     *issued = 0;
     *consumed = 0;
+    *q_issued = 0;
+    *q_waited = 0;
     dev::fence_barrier_init();
   }
   if (warp == 0) dev::tmem_alloc(tmem_slot, QM_TMEM_COLS);
@@ -191,61 +177,107 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // The items of this CTA: pass j takes item j*grid + k (j even) or
+  // j*grid + grid - 1 - k (j odd).
+  const int grid = int(gridDim.x), k = int(blockIdx.x);
+  auto item_index = [&](int j) { return j * grid + ((j & 1) ? grid - 1 - k : k); };
+  auto item_of = [&](int j) {
+    QmItem it;
+    const int x = item_index(j);
+    const int per_seq = P.head_groups * P.tiles;
+    const int rank = x / per_seq, rem = x % per_seq;
+    it.b = ranked ? order[rank] : rank;
+    it.hg0 = rem / P.tiles * HB;
+    it.tile = rem % P.tiles;
+    int L = P.context_lens[it.b];
+    it.bad_len = L > P.cap;
+    if (L > P.cap) L = P.cap;
+    if (L > 0 && L < Q) {  // no room for the new tokens: an empty sequence
+      it.bad_len = true;
+      L = 0;
+    }
+    it.L = L;
+    const int i_last = min(Q, (it.tile + 1) * QT) - 1;  // the item's last new token
+    const int keys = L > 0 ? L - Q + i_last + 1 : 0;     // what its last row sees
+    it.nblk = (keys + 15) / 16;
+    it.n = (it.nblk + NB - 1) / NB;
+    return it;
+  };
+  auto has_item = [&](int j) { return item_index(j) < P.num_items; };
+
   if (warp == 4) {
     // ---------------------------------------------------------- producer
     const uint64_t pol = dev::l2_evict_first_policy();
     if (lane == 0) {
       dev::prefetch_tmap(&tm_k);
       dev::prefetch_tmap(&tm_v);
-      dev::mbar_arrive_expect_tx(qfull, QM_Q_BYTES);
-      // rows [q*RW + h*RPH, +RPH) of each half: head hg0 + h, QT tokens
-      for (int hf = 0; hf < 2; ++hf)
-        for (int q = 0; q < R; ++q)
-          for (int h = 0; h < HB; ++h)
-            dev::tma_load_4d(qbuf + hf * QM_HALF_Q + (q * RW + h * RPH) * 128, &tm_q, hf * 64,
-                             (hg0 + h) * G, tile * QT, b, qfull, pol);
+      dev::prefetch_tmap(&tm_q);
     }
-    const int32_t* trow = P.block_tables + size_t(b) * P.max_blocks_per_seq;
-    // lane l holds the table entry of block w0 + l
-    auto window = [&](int w0) {
-      const int j = w0 + lane;
-      return (j < P.max_blocks_per_seq && j < nblk) ? trow[j] : -1;
-    };
-    int w0 = 0;
-    int win = window(0);
-    bool ok = true;
-    // lane l < 4*NB issues one request of the chunk: block u = l/4, K or V,
+    // lane l < 4*NB issues one request of a chunk: block u = l/4, K or V,
     // one 64-d half (the TMA unit takes requests from several lanes at once)
     const int u = (lane >> 2) % NB, hf = (lane >> 1) & 1, kv = lane & 1;
-    for (int c = 0; c < n && ok; ++c) {
-      if (c * NB >= w0 + 32) {
-        w0 += 32;
-        win = window(w0);
-      }
-      const int slot = c % QM_ST;
+    int gc = 0, qi = 0;
+    bool ok = true;
+    for (int j = 0; ok && has_item(j); ++j) {
+      const QmItem it = item_of(j);
+      if (it.n == 0) continue;
+      const int nblk = it.nblk;
       if (lane == 0) {
-        ok = dev::mbar_wait_sleep(&empty[slot], (uint32_t(c / QM_ST) & 1u) ^ 1u, 64, P.wait_ns,
+        // Q of this item into buffer qi % 2 once the scores of the item that
+        // used it last have completed
+        const int qb = qi & 1;
+        ok = dev::mbar_wait_sleep(&qempty[qb], (uint32_t(qi >> 1) & 1u) ^ 1u, 64, P.wait_ns,
                                   abort_flag);
-        if (ok) dev::mbar_arrive_expect_tx(&full[slot], QM_SLOT);
+        if (ok) {
+          dev::mbar_arrive_expect_tx(&qfull[qb], QM_Q_BYTES);
+          for (int h2 = 0; h2 < 2; ++h2)
+            for (int h = 0; h < HB; ++h)
+              dev::tma_load_4d(qbuf + qb * QM_Q_BYTES + h2 * QM_HALF_Q + h * RPH * 128, &tm_q,
+                               h2 * 64, (it.hg0 + h) * G, it.tile * QT, it.b, &qfull[qb], pol);
+          *q_issued = qi + 1;
+        }
       }
       ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
       if (!ok) break;
-      const int j = c * NB + u;
-      const int e = __shfl_sync(0xffffffffu, win, j - w0);
-      if (lane < 4 * NB) {
-        int row = P.oob_row;  // past the sequence (or a bad entry): zero fill
-        if (j < nblk) {
-          if (e >= 0 && e < P.num_blocks) {
-            row = (e * P.num_kv_heads + hg0) * 16;
-          } else if (kv == 0 && hf == 0) {
-            atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
-          }
+      const int32_t* trow = P.block_tables + size_t(it.b) * P.max_blocks_per_seq;
+      // lane l holds the table entry of block w0 + l
+      auto window = [&](int w0) {
+        const int jj = w0 + lane;
+        return (jj < P.max_blocks_per_seq && jj < nblk) ? trow[jj] : -1;
+      };
+      int w0 = 0;
+      int win = window(0);
+      for (int c = 0; c < it.n; ++c, ++gc) {
+        if (c * NB >= w0 + 32) {
+          w0 += 32;
+          win = window(w0);
         }
-        unsigned char* dst =
-            ring + size_t(slot) * QM_SLOT + kv * QM_KV_BYTES + hf * QM_HALF_KV + u * BR * 128;
-        dev::tma_load_2d(dst, kv ? &tm_v : &tm_k, hf * 64, row, &full[slot], pol);
+        const int slot = gc % QM_ST;
+        if (lane == 0) {
+          ok = dev::mbar_wait_sleep(&empty[slot], (uint32_t(gc / QM_ST) & 1u) ^ 1u, 64, P.wait_ns,
+                                    abort_flag);
+          if (ok) dev::mbar_arrive_expect_tx(&full[slot], QM_SLOT);
+        }
+        ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+        if (!ok) break;
+        const int jb = c * NB + u;
+        const int e = __shfl_sync(0xffffffffu, win, jb - w0);
+        if (lane < 4 * NB) {
+          int row = P.oob_row;  // past the sequence (or a bad entry): zero fill
+          if (jb < nblk) {
+            if (e >= 0 && e < P.num_blocks) {
+              row = (e * P.num_kv_heads + it.hg0) * 16;
+            } else if (kv == 0 && hf == 0) {
+              atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+            }
+          }
+          unsigned char* dst =
+              ring + size_t(slot) * QM_SLOT + kv * QM_KV_BYTES + hf * QM_HALF_KV + u * BR * 128;
+          dev::tma_load_2d(dst, kv ? &tm_v : &tm_k, hf * 64, row, &full[slot], pol);
+        }
+        if (lane == 0) *issued = gc + 1;
       }
-      if (lane == 0) *issued = c + 1;
+      ++qi;
     }
     if (!ok && lane == 0) {
       atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
@@ -254,54 +286,78 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   } else if (warp == 5) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
-      const uint32_t qb = dev::smem_addr(qbuf);
-      bool ok = dev::mbar_wait(qfull, 0, P.wait_ns, abort_flag);
-      auto issue_s = [&](int c) {
-        const uint32_t kb = dev::smem_addr(ring + size_t(c % QM_ST) * QM_SLOT);
-        dev::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < QM_D / 16; ++kk) {
-          const uint32_t hf = kk >> 2, off = uint32_t(kk & 3) * 32;
-          dev::mma_bf16(tmem + uint32_t(c & 1) * QM_KC,
-                        dev::smem_desc(qb + hf * QM_HALF_Q + off, 16, 1024, dev::kSwizzle128B),
-                        dev::smem_desc(kb + hf * QM_HALF_KV + off, 16, 1024, dev::kSwizzle128B),
-                        QM_IDESC_S, kk > 0);
+      // Two cursors over the items: the scores (S) run up to two chunks ahead
+      // of the value products (PV), across item boundaries.
+      int js = 0, cs = 0, gs = 0, qs = 0;  // S: item, chunk in item, global chunk, Q uses
+      int jv = 0, cv = 0, gv = 0, qv = 0;  // PV: the same, qv = O uses
+      QmItem its{}, itv{};
+      auto seek = [&](int& j, int& c, QmItem& it) {  // the next item with chunks
+        while (has_item(j)) {
+          it = item_of(j);
+          if (c < it.n) return true;
+          ++j;
+          c = 0;
         }
-        dev::mma_commit(&bar_s[c & 1]);
+        return false;
       };
-      // Event loop: the scores of chunk s once it has landed and the value
-      // product of chunk s - 2 (which read P from the same S buffer) has
-      // completed, and the value product of chunk v once the softmax has
-      // written its P -- whichever is ready first, so that neither waits
-      // behind the other.
-      int s_next = 0, v_next = 0;
+      bool s_more = seek(js, cs, its), v_more = seek(jv, cv, itv);
+      bool ok = true;
       uint64_t t_idle = 0;
       uint32_t idle = 0;
-      while (ok && v_next < n) {
+      while (ok && v_more) {
         bool progress = false;
-        if (s_next < n && s_next <= v_next + 1 &&
-            (s_next < 2 || dev::mbar_test(&bar_o[s_next & 1], uint32_t((s_next - 2) >> 1) & 1u)) &&
-            dev::mbar_test(&full[s_next % QM_ST], uint32_t(s_next / QM_ST) & 1u)) {
-          issue_s(s_next);
-          ++s_next;
+        // the scores of chunk gs: it has landed, its Q is in, and the softmax
+        // of chunk gs - 2 has read S[gs % 2] (its value product is issued)
+        if (s_more && gs <= gv + 1 &&
+            (cs > 0 || dev::mbar_test(&qfull[qs & 1], uint32_t(qs >> 1) & 1u)) &&
+            dev::mbar_test(&full[gs % QM_ST], uint32_t(gs / QM_ST) & 1u)) {
+          if (cs == 0) *q_waited = qs + 1;
+          const uint32_t qb = dev::smem_addr(qbuf + (qs & 1) * QM_Q_BYTES);
+          const uint32_t kb = dev::smem_addr(ring + size_t(gs % QM_ST) * QM_SLOT);
+          dev::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < QM_D / 16; ++kk) {
+            const uint32_t h2 = kk >> 2, off = uint32_t(kk & 3) * 32;
+            dev::mma_bf16(tmem + uint32_t(gs & 1) * QM_KC,
+                          dev::smem_desc(qb + h2 * QM_HALF_Q + off, 16, 1024, dev::kSwizzle128B),
+                          dev::smem_desc(kb + h2 * QM_HALF_KV + off, 16, 1024, dev::kSwizzle128B),
+                          QM_IDESC_S, kk > 0);
+          }
+          dev::mma_commit(&bar_s[gs & 1]);
+          ++gs;
+          if (++cs == its.n) {  // the item's last scores: its Q buffer frees when they complete
+            dev::mma_commit(&qempty[qs & 1]);
+            ++qs;
+            ++js;
+            cs = 0;
+            s_more = seek(js, cs, its);
+          }
           progress = true;
         }
-        if (v_next < s_next &&
-            dev::mbar_test(&bar_p[v_next & 1], uint32_t(v_next >> 1) & 1u)) {
-          const int c = v_next;
+        // the value product of chunk gv once its P is written (and, on an
+        // item's first chunk, once its O accumulator has been read out)
+        if (gv < gs && dev::mbar_test(&bar_p[gv & 1], uint32_t(gv >> 1) & 1u) &&
+            (cv > 0 || dev::mbar_test(&oempty[qv & 1], (uint32_t(qv >> 1) & 1u) ^ 1u))) {
           dev::tc_fence_after();
-          const uint32_t vb = dev::smem_addr(ring + size_t(c % QM_ST) * QM_SLOT + QM_KV_BYTES);
+          const uint32_t vb = dev::smem_addr(ring + size_t(gv % QM_ST) * QM_SLOT + QM_KV_BYTES);
+          const uint32_t od = tmem + 2 * QM_KC + uint32_t(qv & 1) * QM_D;
 #pragma unroll
           for (int kk = 0; kk < QM_KC / 16; ++kk)
-            mma_bf16_tmem_a(tmem + 2 * QM_KC, tmem + uint32_t(c & 1) * QM_KC + uint32_t(kk * 8),
+            mma_bf16_tmem_a(od, tmem + QM_TMEM_P + uint32_t(gv & 1) * 32 + uint32_t(kk * 8),
                             // V MN-major: next 8 rows 1024 B on (SBO), second 64-d
                             // half one half on (LBO)
                             dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
-                            QM_IDESC_PV, c > 0 || kk > 0);
-          dev::mma_commit(&bar_o[c & 1]);
-          dev::mma_commit(&empty[c % QM_ST]);
-          *consumed = c + 1;
-          ++v_next;
+                            QM_IDESC_PV, cv > 0 || kk > 0);
+          dev::mma_commit(&bar_o[gv & 1]);
+          dev::mma_commit(&empty[gv % QM_ST]);
+          *consumed = gv + 1;
+          ++gv;
+          if (++cv == itv.n) {
+            ++qv;
+            ++jv;
+            cv = 0;
+            v_more = seek(jv, cv, itv);
+          }
           progress = true;
         }
         if (progress) {
@@ -331,228 +387,173 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   } else {
     // ---------------------------------------------------------- softmax
     const int r = tid;  // TMEM lane
-    const int q = r / RW, h = (r % RW) / RPH, r0 = r % RPH;  // copy, head, row of the head
-    const int i = tile * QT + r0 / G;
-    const bool valid = i < Q && hg0 + h < P.num_kv_heads;
-    const int L_row = valid ? L - Q + i + 1 : 0;
+    const int h = r / RPH, r0 = r % RPH;  // head of the group, row of the head
     const uint32_t t_lane = uint32_t(warp * 32) << 16;
     const float sl2 = P.scale_log2;
-    float m_ref = -INFINITY, l = 0.0f;
-    int pv_done = -1;
+    int pv_done = -1, gc = 0, qi = 0;
     bool ok = true;
-    // value product of chunk k done (it completes bar_o[k % 2], phase k / 2)
-    auto wait_pv = [&](int k) {
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[k & 1], uint32_t(k >> 1) & 1u,
+    // value product of chunk kc done (it completes bar_o[kc % 2], phase kc / 2)
+    auto wait_pv = [&](int kc) {
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[kc & 1], uint32_t(kc >> 1) & 1u,
                                                   P.wait_ns, abort_flag)) &&
            ok;
-      pv_done = k;
+      pv_done = kc;
     };
-    for (int c = 0; c < n && ok; ++c) {
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[c & 1], uint32_t(c >> 1) & 1u,
-                                                  P.wait_ns, abort_flag));
+    for (int j = 0; ok && has_item(j); ++j) {
+      const QmItem it = item_of(j);
+      const int i = it.tile * QT + r0 / G;
+      const bool valid = i < Q && it.hg0 + h < P.num_kv_heads;
+      __nv_bfloat16* orow =
+          P.out +
+          ((size_t(it.b) * Q + (valid ? i : 0)) * P.num_q_heads + (it.hg0 + h) * G + r0 % G) *
+              QM_D;
+      if (r == 0 && it.bad_len && it.tile == 0 && it.hg0 == 0)
+        atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
+      if (it.n == 0) {  // an empty sequence: zero rows
+        if (valid)
+#pragma unroll
+          for (int cg = 0; cg < QM_D; cg += 8)
+            *reinterpret_cast<uint4*>(orow + cg) = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      const int L = it.L;
+      const int L_row = valid ? L - Q + i + 1 : 0;
+      const uint32_t o_col = 2 * QM_KC + uint32_t(qi & 1) * QM_D;
+      float m_ref = -INFINITY, l = 0.0f;
+      for (int c = 0; c < it.n; ++c) {
+        const int g = gc + c;
+        ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[g & 1], uint32_t(g >> 1) & 1u,
+                                                    P.wait_ns, abort_flag));
+        if (!ok) break;
+        dev::tc_fence_after();
+        // this thread's scores: block u of the chunk, 16 columns at u*BR + h*16
+        float s[NC];
+        {
+          uint32_t raw[NC];
+#pragma unroll
+          for (int t = 0; t < NB; ++t)
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+                "%10, %11, %12, %13, %14, %15}, [%16];"
+                : "=r"(raw[16 * t + 0]), "=r"(raw[16 * t + 1]), "=r"(raw[16 * t + 2]),
+                  "=r"(raw[16 * t + 3]), "=r"(raw[16 * t + 4]), "=r"(raw[16 * t + 5]),
+                  "=r"(raw[16 * t + 6]), "=r"(raw[16 * t + 7]), "=r"(raw[16 * t + 8]),
+                  "=r"(raw[16 * t + 9]), "=r"(raw[16 * t + 10]), "=r"(raw[16 * t + 11]),
+                  "=r"(raw[16 * t + 12]), "=r"(raw[16 * t + 13]), "=r"(raw[16 * t + 14]),
+                  "=r"(raw[16 * t + 15])
+                : "r"(tmem + t_lane + uint32_t(g & 1) * QM_KC + uint32_t(t * BR + h * 16)));
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int kx = 0; kx < NC; ++kx) s[kx] = __uint_as_float(raw[kx]);
+        }
+        const int key0 = c * NB * 16;  // key of s[0]; s[kx] is key key0 + kx
+        if (!__all_sync(0xffffffffu, key0 + NC <= L_row)) {
+#pragma unroll
+          for (int kx = 0; kx < NC; ++kx) s[kx] = key0 + kx < L_row ? s[kx] : -INFINITY;
+        }
+        // maximum of the raw scores (the scale is positive), four chains
+        float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int kx = 4; kx < NC; ++kx) mx[kx & 3] = fmaxf(mx[kx & 3], s[kx]);
+        const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        // the reference moves only when a score exceeds it by more than 2^8
+        const bool need = cm > m_ref + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float nr = need ? cm : m_ref;
+          const float f = nr == m_ref || m_ref == -INFINITY ? 1.0f : dev::fast_exp2(m_ref - nr);
+          if (c > 0) {
+            if (pv_done < g - 1) wait_pv(g - 1);
+            if (!ok) break;
+            dev::tc_fence_after();
+#pragma unroll
+            for (int cg = 0; cg < QM_D; cg += 32) {
+              float o[32];
+              dev::tmem_ld_cols<32>(tmem + t_lane + o_col + cg, o);
+#pragma unroll
+              for (int kx = 0; kx < 32; ++kx) o[kx] *= f;
+              dev::tmem_st_cols<32>(tmem + t_lane + o_col + cg, o);
+            }
+          }
+          l *= f;
+          m_ref = nr;
+        }
+        // p = 2^(s * scale - m): masked scores give 2^-inf = 0; with no
+        // reference yet every score is masked and the offset is moot
+        const float nm = m_ref == -INFINITY ? 0.0f : -m_ref;
+        uint32_t pw[NC / 2];
+        float la = 0.0f, lb = 0.0f;
+#pragma unroll
+        for (int kx = 0; kx < NC; kx += 2) {
+          const float p0 = dev::fast_exp2(fmaf(s[kx], sl2, nm));
+          const float p1 = dev::fast_exp2(fmaf(s[kx + 1], sl2, nm));
+          la += p0;
+          lb += p1;
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+          pw[kx / 2] = *reinterpret_cast<const uint32_t*>(&v2);
+        }
+        l += la + lb;
+        if ((c + 1) * NB * 16 > L) {
+          // keys past the sequence in its last block may hold anything (NaN
+          // included): clear their V rows so that 0 * V = 0. Thread r clears
+          // row x = r % 64 of half r / 64: block x / BR, key x % 16.
+          const int x = r % QM_KC, h2 = r / QM_KC;
+          if ((c * NB + x / BR) * 16 + x % 16 >= L) {
+            uint4* vrow = reinterpret_cast<uint4*>(ring + size_t(g % QM_ST) * QM_SLOT +
+                                                   QM_KV_BYTES + h2 * QM_HALF_KV + x * 128);
+#pragma unroll
+            for (int kx = 0; kx < 8; ++kx) vrow[kx] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          dev::fence_async_smem();  // before the value product reads the ring
+        }
+        // P[g % 2]: column m holds chunk columns 2m, 2m+1; block u's 16
+        // columns of this head are P columns (u*BR + h*16)/2 + [0, 8), the
+        // rest zero. The value product of chunk g - 2 read this buffer last.
+        if (g >= 2 && pv_done < g - 2) wait_pv(g - 2);
+        if (!ok) break;
+        {
+          float pp[QM_KC / 2];
+#pragma unroll
+          for (int m = 0; m < QM_KC / 2; ++m) {
+            const int u = 2 * m / BR, hh = 2 * m % BR / 16;  // block and head of P column m
+            pp[m] = hh == h ? __uint_as_float(pw[8 * u + m % 8]) : 0.0f;
+          }
+          dev::tmem_st_cols<QM_KC / 2>(tmem + t_lane + QM_TMEM_P + uint32_t(g & 1) * 32, pp);
+        }
+        dev::tc_fence_before();
+        dev::mbar_arrive(&bar_p[g & 1]);
+      }
+      if (!ok) break;
+      gc += it.n;
+      wait_pv(gc - 1);
       if (!ok) break;
       dev::tc_fence_after();
-      // this thread's scores: blocks u = q*TB + t of the chunk, 16 columns each
-      // at u*BR + h*16 (contiguous when HB = 1)
-      float s[NC];
-      {
-        uint32_t raw[NC];
+      const float inv = l > 0.0f ? __frcp_rn(l) : 0.0f;
 #pragma unroll
-        for (int t = 0; t < TB; ++t)
-          asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
-              "%10, %11, %12, %13, %14, %15}, [%16];"
-              : "=r"(raw[16 * t + 0]), "=r"(raw[16 * t + 1]), "=r"(raw[16 * t + 2]),
-                "=r"(raw[16 * t + 3]), "=r"(raw[16 * t + 4]), "=r"(raw[16 * t + 5]),
-                "=r"(raw[16 * t + 6]), "=r"(raw[16 * t + 7]), "=r"(raw[16 * t + 8]),
-                "=r"(raw[16 * t + 9]), "=r"(raw[16 * t + 10]), "=r"(raw[16 * t + 11]),
-                "=r"(raw[16 * t + 12]), "=r"(raw[16 * t + 13]), "=r"(raw[16 * t + 14]),
-                "=r"(raw[16 * t + 15])
-              : "r"(tmem + t_lane + uint32_t(c & 1) * QM_KC +
-                    uint32_t((q * TB + t) * BR + h * 16)));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-        for (int k = 0; k < NC; ++k) s[k] = __uint_as_float(raw[k]);
-      }
-      const int key0 = (c * NB + q * TB) * 16;  // key of s[0]; s[k] is key key0 + k
-      if (!__all_sync(0xffffffffu, key0 + NC <= L_row)) {
-#pragma unroll
-        for (int k = 0; k < NC; ++k) s[k] = key0 + k < L_row ? s[k] : -INFINITY;
-      }
-      // maximum of the raw scores (the scale is positive), four chains
-      float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-      for (int k = 4; k < NC; ++k) mx[k & 3] = fmaxf(mx[k & 3], s[k]);
-      const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
-      // the reference moves only when a score exceeds it by more than 2^8
-      const bool need = cm > m_ref + kRescaleLog2;
-      if (__any_sync(0xffffffffu, need)) {
-        const float nr = need ? cm : m_ref;
-        const float f = nr == m_ref || m_ref == -INFINITY ? 1.0f : dev::fast_exp2(m_ref - nr);
-        if (c > 0) {
-          if (pv_done < c - 1) wait_pv(c - 1);
-          if (!ok) break;
-          dev::tc_fence_after();
-#pragma unroll
-          for (int cg = 0; cg < QM_D; cg += 32) {
-            float o[32];
-            dev::tmem_ld_cols<32>(tmem + t_lane + 2 * QM_KC + cg, o);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] *= f;
-            dev::tmem_st_cols<32>(tmem + t_lane + 2 * QM_KC + cg, o);
-          }
-        }
-        l *= f;
-        m_ref = nr;
-      }
-      // p = 2^(s * scale - m): masked scores give 2^-inf = 0; with no
-      // reference yet every score is masked and the offset is moot
-      const float nm = m_ref == -INFINITY ? 0.0f : -m_ref;
-      uint32_t pw[NC / 2];
-      float la = 0.0f, lb = 0.0f;
-#pragma unroll
-      for (int k = 0; k < NC; k += 2) {
-        const float p0 = dev::fast_exp2(fmaf(s[k], sl2, nm));
-        const float p1 = dev::fast_exp2(fmaf(s[k + 1], sl2, nm));
-        la += p0;
-        lb += p1;
-        const __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
-        pw[k / 2] = *reinterpret_cast<const uint32_t*>(&v2);
-      }
-      l += la + lb;
-      if ((c + 1) * NB * 16 > L) {
-        // keys past the sequence in its last block may hold anything (NaN
-        // included): clear their V rows so that 0 * V = 0. Thread r clears
-        // row x = r % 64 of half r / 64: block x / BR, key x % 16.
-        const int x = r % QM_KC, hf = r / QM_KC;
-        if ((c * NB + x / BR) * 16 + x % 16 >= L) {
-          uint4* vrow = reinterpret_cast<uint4*>(ring + size_t(c % QM_ST) * QM_SLOT +
-                                                 QM_KV_BYTES + hf * QM_HALF_KV + x * 128);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        dev::fence_async_smem();  // before the value product reads the ring
-      }
-      // P over the first 32 columns of this chunk's S buffer (its scores are
-      // in registers): column j holds columns 2j, 2j+1 of the chunk; block u's
-      // 16 columns of this head are P columns (u*BR + h*16)/2 + [0, 8), the
-      // rest zero. The value product of chunk c - 2, which read this buffer's
-      // last P, completed before S(c) was issued.
-      {
-        float pp[QM_KC / 2];
-#pragma unroll
-        for (int k = 0; k < QM_KC / 2; ++k) {
-          const int u = 2 * k / BR, hh = 2 * k % BR / 16;  // block and head of P column k
-          pp[k] = u / TB == q && hh == h ? __uint_as_float(pw[8 * (u % TB) + k % 8]) : 0.0f;
-        }
-        dev::tmem_st_cols<QM_KC / 2>(tmem + t_lane + uint32_t(c & 1) * QM_KC, pp);
-      }
-      dev::tc_fence_before();
-      dev::mbar_arrive(&bar_p[c & 1]);
-    }
-    if (ok && n > 0) wait_pv(n - 1);
-    __nv_bfloat16* orow =
-        P.out + ((size_t(b) * Q + (valid ? i : 0)) * P.num_q_heads + (hg0 + h) * G + r0 % G) * QM_D;
-    if (R == 1) {
-      if (ok) {
-        dev::tc_fence_after();
-        const float inv = l > 0.0f ? __frcp_rn(l) : 0.0f;
-#pragma unroll
-        for (int cg = 0; cg < QM_D; cg += 32) {
-          float o[32];
-          dev::tmem_ld_cols<32>(tmem + t_lane + 2 * QM_KC + cg, o);
-          if (valid) {
-#pragma unroll
-            for (int k = 0; k < 32; k += 8) {
-              uint32_t w[4];
-#pragma unroll
-              for (int q2 = 0; q2 < 4; ++q2) {
-                const __nv_bfloat162 v2 =
-                    __floats2bfloat162_rn(o[k + 2 * q2] * inv, o[k + 2 * q2 + 1] * inv);
-                w[q2] = *reinterpret_cast<const uint32_t*>(&v2);
-              }
-              *reinterpret_cast<uint4*>(orow + cg + k) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-        }
-      } else if (lane == 0) {
-        atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-    } else {
-      // Merge the R copies of each row (every value product has completed,
-      // so the ring is free): each thread leaves its raw O row, reference and
-      // sum in shared memory; then copy q of a row writes output columns
-      // [q*128/R, (q+1)*128/R), each the sum over copies of 2^(m_c - M) O_c,
-      // divided by the sum of 2^(m_c - M) l_c (M the largest reference).
-      // 16-byte chunk j of TMEM lane x sits at chunk (j + x) % 32 of its 512 bytes.
-      if (!ok && lane == 0) {
-        atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-      // a uniform decision: the softmax warps all finished, or none merges
-      if (dev::named_barrier_and(1, 128, ok)) {
-        float* mbuf = reinterpret_cast<float*>(ring + QM_ROWS * 512);
-        float* lbuf = mbuf + QM_ROWS;
-        dev::tc_fence_after();
-        unsigned char* orow_s = ring + r * 512;
-#pragma unroll
-        for (int cg = 0; cg < QM_D; cg += 32) {
-          float o[32];
-          dev::tmem_ld_cols<32>(tmem + t_lane + 2 * QM_KC + cg, o);
-#pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(orow_s + ((((cg + k) / 4 + r) & 31) << 4)) =
-                make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-        }
-        mbuf[r] = m_ref;
-        lbuf[r] = l;
-        dev::named_barrier(1, 128);
-        const int rr = r % RW;  // the row within a copy
-        float M = -INFINITY;
-#pragma unroll
-        for (int qq = 0; qq < R; ++qq) M = fmaxf(M, mbuf[qq * RW + rr]);
-        float fq[R], lt = 0.0f;
-#pragma unroll
-        for (int qq = 0; qq < R; ++qq) {
-          const float mq = mbuf[qq * RW + rr];
-          fq[qq] = mq == -INFINITY ? 0.0f : dev::fast_exp2(mq - M);
-          lt += fq[qq] * lbuf[qq * RW + rr];
-        }
-        const float inv = lt > 0.0f ? __frcp_rn(lt) : 0.0f;
+      for (int cg = 0; cg < QM_D; cg += 32) {
+        float o[32];
+        dev::tmem_ld_cols<32>(tmem + t_lane + o_col + cg, o);
         if (valid) {
-          constexpr int OC = QM_D / R;  // output columns of this thread
 #pragma unroll
-          for (int k = 0; k < OC; k += 8) {
-            const int col = q * OC + k;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int qq = 0; qq < R; ++qq) {
-              const int x = qq * RW + rr;
-              const unsigned char* src = ring + x * 512;
-              const float4 a0 = *reinterpret_cast<const float4*>(src + (((col / 4 + x) & 31) << 4));
-              const float4 a1 =
-                  *reinterpret_cast<const float4*>(src + (((col / 4 + 1 + x) & 31) << 4));
-              acc[0] += fq[qq] * a0.x;
-              acc[1] += fq[qq] * a0.y;
-              acc[2] += fq[qq] * a0.z;
-              acc[3] += fq[qq] * a0.w;
-              acc[4] += fq[qq] * a1.x;
-              acc[5] += fq[qq] * a1.y;
-              acc[6] += fq[qq] * a1.z;
-              acc[7] += fq[qq] * a1.w;
-            }
+          for (int kx = 0; kx < 32; kx += 8) {
             uint32_t w[4];
 #pragma unroll
             for (int q2 = 0; q2 < 4; ++q2) {
               const __nv_bfloat162 v2 =
-                  __floats2bfloat162_rn(acc[2 * q2] * inv, acc[2 * q2 + 1] * inv);
+                  __floats2bfloat162_rn(o[kx + 2 * q2] * inv, o[kx + 2 * q2 + 1] * inv);
               w[q2] = *reinterpret_cast<const uint32_t*>(&v2);
             }
-            *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(orow + cg + kx) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
+      // this O accumulator may take the item after next
+      dev::tc_fence_before();
+      dev::mbar_arrive(&oempty[qi & 1]);
+      ++qi;
+    }
+    if (!ok && lane == 0) {
+      atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
     }
   }
 
@@ -561,6 +562,8 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     // every copy issued but not consumed lands before shared memory is released
     for (int c = *consumed; c < *issued; ++c)
       (void)dev::mbar_wait(&full[c % QM_ST], uint32_t(c / QM_ST) & 1u);
+    for (int c = *q_waited; c < *q_issued; ++c)
+      (void)dev::mbar_wait(&qfull[c & 1], uint32_t(c >> 1) & 1u);
   }
   dev::tc_fence_before();
   __syncthreads();
@@ -570,11 +573,11 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   }
 }
 
-template <int G, int R, int HB>
+template <int G, int HB>
 int launch_qm_t(const pa_decode_params* p, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G, R, HB>,
+    cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G, HB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, QM_SMEM);
     if (e != cudaSuccess) return int(e);
     configured = true;
@@ -591,7 +594,7 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream) {
                                 uint64_t(p->num_seqs)};
     const cuuint64_t strides[3] = {uint64_t(QM_D) * 2, uint64_t(p->num_q_heads) * QM_D * 2,
                                    uint64_t(Q) * p->num_q_heads * QM_D * 2};
-    const cuuint32_t box[4] = {64, uint32_t(G), uint32_t(QM_ROWS / (R * HB * G)), 1};
+    const cuuint32_t box[4] = {64, uint32_t(G), uint32_t(QM_ROWS / (HB * G)), 1};
     r = make_map_nd(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p->q, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   }
@@ -606,23 +609,23 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream) {
   P.q_len = Q;
   P.tiles = query_major_tiles(p);
   P.head_groups = H / HB;
+  P.num_items = p->num_seqs * P.head_groups * P.tiles;
   P.max_blocks_per_seq = p->max_blocks_per_seq;
   P.num_blocks = p->num_blocks;
   P.cap = std::min(p->max_blocks_per_seq * 16, p->max_context_len);
   P.oob_row = int(cache_rows);
   P.scale_log2 = p->scale * kLog2e;
   P.wait_ns = p->wait_timeout_us > 0 ? uint64_t(p->wait_timeout_us) * 1000u : dev::kWaitNsLimit;
-  const dim3 grid(unsigned(p->num_seqs) * unsigned(P.head_groups) * unsigned(P.tiles));
-  query_major_kernel<G, R, HB><<<grid, QM_THREADS, QM_SMEM, stream>>>(tk, tv, tq, P);
+  const int sms = tc_grid();
+  if (sms <= 0) return int(cudaErrorInvalidDevice);
+  const dim3 grid(unsigned(std::min(P.num_items, sms)));
+  query_major_kernel<G, HB><<<grid, QM_THREADS, QM_SMEM, stream>>>(tk, tv, tq, P);
   return int(cudaGetLastError());
 }
 
 template <int G>
 int launch_qm_g(const pa_decode_params* p, cudaStream_t stream) {
-  const int R = query_major_copies(p), HB = query_major_heads(p);
-  if (HB == 2) return R == 2 ? launch_qm_t<G, 2, 2>(p, stream) : launch_qm_t<G, 1, 2>(p, stream);
-  return R == 4 ? launch_qm_t<G, 4, 1>(p, stream)
-                : (R == 2 ? launch_qm_t<G, 2, 1>(p, stream) : launch_qm_t<G, 1, 1>(p, stream));
+  return query_major_heads(p) == 2 ? launch_qm_t<G, 2>(p, stream) : launch_qm_t<G, 1>(p, stream);
 }
 
 }  // namespace

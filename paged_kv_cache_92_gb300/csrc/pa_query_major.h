@@ -6,8 +6,9 @@
 
 namespace pa {
 
-// One CTA per (sequence, group of KV heads, tile of 128 query rows = tokens x G
-// heads of each head in the group).
+// A unit of work is (sequence, group of KV heads, tile of 128 query rows =
+// tokens x G heads of each head in the group); one persistent CTA per SM takes
+// its share of them.
 inline int query_major_tiles(const pa_decode_params* p) {
   const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
   return (rows + 127) / 128;
@@ -17,13 +18,6 @@ inline int query_major_tiles(const pa_decode_params* p) {
 inline int query_major_heads(const pa_decode_params* p) {
   const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
   return rows <= 64 && p->num_kv_heads % 2 == 0 ? 2 : 1;
-}
-// Copies of the rows in a tile: the 128 rows hold (heads x rows per head,
-// rounded up to 32 or 64) this many times.
-inline int query_major_copies(const pa_decode_params* p) {
-  const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
-  const int per_head = rows <= 32 ? 32 : (rows <= 64 ? 64 : 128);
-  return 128 / (per_head * query_major_heads(p));
 }
 // It takes the bf16 cache at head_dim 128 and block size 16 when the
 // column-group decode would split the new tokens into several groups (each

@@ -186,20 +186,32 @@ def _qm_lens(QL, B=16):
 
 
 @pytest.mark.parametrize("G,Hkv,QL,B", [
-    # at most 32 rows (tokens x G): four copies of each row, 16 keys of a chunk each
+    # at most 32 rows (tokens x G) per KV head: two heads per work item, half filled
     (4, 8, 8, 16), (8, 8, 4, 16), (1, 8, 20, 16), (2, 8, 12, 16), (4, 8, 5, 16), (8, 8, 3, 16),
-    # at most 64 rows: two copies, 32 keys each
+    # at most 64 rows: two heads per item
     (4, 8, 16, 16), (1, 8, 33, 16), (2, 8, 24, 16), (4, 8, 12, 16), (8, 8, 6, 16),
-    # one copy; one, two and three 128-row tiles
+    # one head per item; one, two and three 128-row tiles
     (2, 8, 64, 16), (4, 8, 64, 16), (8, 4, 16, 32), (8, 8, 40, 16),
-    # an odd number of KV heads: one head per CTA (four copies; two)
+    # an odd number of KV heads: one head per item, few rows
     (2, 3, 16, 48), (8, 1, 6, 128)])
 def test_query_major_against_the_oracle(pk, G, Hkv, QL, B):
     """Lengths from Q (every key a new token) across chunk and block boundaries
-    to 2049; two KV heads per CTA (rows held twice or once) or one (four
-    times, twice, once), partly filled tiles and several tiles per head."""
+    to 2049; two KV heads per work item or one, partly filled tiles and
+    several tiles per head."""
     q, kc, vc, tables, lens, torch = _case(_qm_lens(QL, B), QL, G * Hkv, Hkv, 128,
                                            seed=700 + G * 10 + QL)
+    _check(pk, q, kc, vc, tables, lens, torch)
+
+
+@pytest.mark.parametrize("G,Hkv,QL,B", [(4, 8, 8, 400), (4, 8, 64, 24), (2, 8, 24, 200)])
+def test_query_major_many_items_per_cta(pk, G, Hkv, QL, B):
+    """More work items than SMs: each persistent CTA takes several in turn
+    (a snake over the items by length; unranked beyond 256 sequences), the
+    next item's loads overlapping the current one's end. Short lengths keep
+    the oracle quick."""
+    lens = np.random.default_rng(730 + QL).integers(QL, QL + 300, size=B)
+    lens[:3] = [QL, QL + 1, QL + 15]
+    q, kc, vc, tables, lens, torch = _case(lens, QL, G * Hkv, Hkv, 128, seed=731 + QL)
     _check(pk, q, kc, vc, tables, lens, torch)
 
 
