@@ -19,15 +19,15 @@ inline int query_major_heads(const pa_decode_params* p) {
   const int rows = query_len_of(p) * (p->num_q_heads / p->num_kv_heads);
   return rows <= 64 && p->num_kv_heads % 2 == 0 ? 2 : 1;
 }
-// It takes the bf16 cache at head_dim 128 and block size 16 when the
-// column-group decode would split the new tokens into several groups (each
-// re-reading the keys) and the batch gives it at least 128 (sequence, KV head,
-// tile) units of work.
+// It takes the bf16 cache at head_dim 128 and block size 16 when a KV head has
+// at least 16 query rows (new tokens x G) or the column-group decode would
+// split the new tokens into several groups (each re-reading the keys), and
+// the batch gives it at least 128 (sequence, KV head, tile) units of work.
 inline bool use_query_major(const pa_decode_params* p) {
   const int g = p->num_q_heads / p->num_kv_heads;
   return p->variant == PA_DECODE_TENSOR_CORE && p->kv_dtype == PA_KV_BF16 && p->head_dim == 128 &&
          p->block_size == 16 && query_len_of(p) > 1 && (g == 1 || g == 2 || g == 4 || g == 8) &&
-         tc_n_groups(p) > 1 &&
+         (tc_n_groups(p) > 1 || query_len_of(p) * g >= 16) &&
          int64_t(p->num_seqs) * p->num_kv_heads * query_major_tiles(p) >= 128;
 }
 

@@ -190,9 +190,9 @@ def test_decode_workspace_size(pk):
         assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(2, 8, 128, 1, 256,
                                                                              QL=ql)
     p = _params(pk, num_seqs=64, num_q_heads=32, num_kv_heads=8, max_context_len=2048,
-                max_blocks_per_seq=128, query_len=4)
+                max_blocks_per_seq=128, query_len=2)
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
-                                                                         Hkv=8, QL=4)
+                                                                         Hkv=8, QL=2)
     # more new tokens than one column group holds: groups as virtual sequences
     for ql in (8, 9, 64):
         p = _params(pk, query_len=ql)
@@ -203,12 +203,14 @@ def test_decode_workspace_size(pk):
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(8, 32, 128, 4, 256,
                                                                          Hkv=8, QL=16)
     # ... unless the batch gives the query-major kernel 128 (sequence, KV head,
-    # 128-row tile) CTAs: it splits no keys and needs the header only
+    # 128-row tile) units: it splits no keys and needs the header only
     p.num_seqs = 64
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == 256
-    p.query_len = 4  # one column group: the column-layout decode
+    p.query_len = 4  # one column group but 16 rows per KV head: query-major as well
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == 256
+    p.query_len = 3  # 12 rows per KV head in one column group: the column-layout decode
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
-                                                                         Hkv=8, QL=4)
+                                                                         Hkv=8, QL=3)
     # several new tokens on the CUDA-core kernel: partials per (sequence, token)
     for ql in (2, 7):
         p = _params(pk, query_len=ql, max_context_len=2048, max_blocks_per_seq=128, variant=1)

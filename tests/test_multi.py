@@ -188,6 +188,8 @@ def _qm_lens(QL, B=16):
 @pytest.mark.parametrize("G,Hkv,QL,B", [
     # at most 32 rows (tokens x G) per KV head: two heads per work item, half filled
     (4, 8, 8, 16), (8, 8, 4, 16), (1, 8, 20, 16), (2, 8, 12, 16), (4, 8, 5, 16), (8, 8, 3, 16),
+    # 16 rows, within one column group: query-major from 16 rows per head
+    (4, 8, 4, 16), (2, 8, 8, 16), (8, 8, 2, 16),
     # at most 64 rows: two heads per item
     (4, 8, 16, 16), (1, 8, 33, 16), (2, 8, 24, 16), (4, 8, 12, 16), (8, 8, 6, 16),
     # one head per item; one, two and three 128-row tiles
