@@ -125,8 +125,16 @@ WorkspaceLayout decode_workspace_layout(const pa_decode_params* p, int num_parti
                                         int grid) {
   WorkspaceLayout w{};
   const size_t H = kWorkspaceHeaderBytes;
-  if (use_query_major(p)) {  // no split of the keys: nothing but the header
+  if (use_query_major(p)) {
+    // the header, and with split keys the partials (m, l pairs, then O rows)
     w.total = H;
+    const int ns = query_major_splits(p);
+    if (ns > 1) {
+      const size_t rows = size_t(p->num_seqs) * query_len_of(p) * p->num_q_heads * ns;
+      w.tc_m = H;
+      w.tc_acc = w.tc_m + round_up(rows * 2 * sizeof(float), 256);
+      w.total = w.tc_acc + round_up(rows * p->head_dim * sizeof(float), 256);
+    }
     return w;
   }
   if (!decode_uses_tc(p)) {
@@ -193,7 +201,11 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
                                    p->num_seqs * query_len_of(p), p->num_kv_heads, p->head_dim,
                                    p->block_size, p->num_blocks, stream, chk);
     }
-    if (!e) e = launch_query_major_tc(p, stream);
+    if (!e) {
+      const bool split = query_major_splits(p) > 1;
+      e = launch_query_major_tc(p, stream, split ? reinterpret_cast<float*>(ws + w.tc_m) : nullptr,
+                                split ? reinterpret_cast<float*>(ws + w.tc_acc) : nullptr);
+    }
   } else if (decode_uses_tc(p)) {
     if (grid <= 0)
       return set_cuda_error("the SM count of the current device", int(cudaErrorNoDevice));

@@ -1,9 +1,12 @@
 // Several new tokens per sequence on the tensor cores, query-major ("How Paged
 // Attention and Continuous Batching Actually Work", §Continuous batching: the
 // scheduled tokens of one request, as in a chunked prefill). A unit of work (an
-// item) is (sequence, group of HB KV heads, tile of query rows); it streams
-// those heads' blocks once for all its rows. A row is new token i of query head
-// (kv head)*G + g and sees the sequence's first L - Q + i + 1 keys.
+// item) is (sequence, group of HB KV heads, tile of query rows, split of the
+// keys); it streams its share of those heads' blocks once for all its rows. A
+// row is new token i of query head (kv head)*G + g and sees the sequence's
+// first L - Q + i + 1 keys. With several splits (small batches) each item
+// leaves fp32 partials (running maximum, sum, unnormalised O row) and a merge
+// kernel combines a row's splits, as in a split-K decode.
 //
 // The column-group decode (pa_decode_tc.cuh) puts the keys on the MMAs' M side
 // and streams them once per group of new tokens; with many new tokens each
@@ -79,8 +82,10 @@ struct QmParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   __nv_bfloat16* out;
-  int num_seqs, num_kv_heads, num_q_heads, q_len, tiles, head_groups, num_items,
+  int num_seqs, num_kv_heads, num_q_heads, q_len, tiles, head_groups, splits, num_items,
       max_blocks_per_seq, num_blocks, cap, oob_row;
+  float* part_ml;  // splits > 1: [B*Q*Hq rows][splits][m, l]
+  float* part_o;   // splits > 1: [B*Q*Hq rows][splits][128]
   float scale_log2;
   uint64_t wait_ns;
 };
@@ -88,6 +93,7 @@ struct QmParams {
 // One item as every role sees it.
 struct QmItem {
   int b, hg0, tile;  // sequence, first KV head, tile of new tokens
+  int split, c0;     // split of the keys, its first chunk
   int L;             // length after the rules (0: an empty sequence)
   int nblk, n;       // blocks the item's last row sees, chunks
   bool bad_len;      // the length broke a rule (reported once per sequence)
@@ -184,11 +190,12 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   auto item_of = [&](int j) {
     QmItem it;
     const int x = item_index(j);
-    const int per_seq = P.head_groups * P.tiles;
+    const int per_seq = P.head_groups * P.tiles * P.splits;
     const int rank = x / per_seq, rem = x % per_seq;
     it.b = ranked ? order[rank] : rank;
-    it.hg0 = rem / P.tiles * HB;
-    it.tile = rem % P.tiles;
+    it.hg0 = rem / (P.tiles * P.splits) * HB;
+    it.tile = rem / P.splits % P.tiles;
+    it.split = rem % P.splits;
     int L = P.context_lens[it.b];
     it.bad_len = L > P.cap;
     if (L > P.cap) L = P.cap;
@@ -200,7 +207,9 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     const int i_last = min(Q, (it.tile + 1) * QT) - 1;  // the item's last new token
     const int keys = L > 0 ? L - Q + i_last + 1 : 0;     // what its last row sees
     it.nblk = (keys + 15) / 16;
-    it.n = (it.nblk + NB - 1) / NB;
+    const int n_all = (it.nblk + NB - 1) / NB;  // chunks of all the splits
+    it.c0 = it.split * n_all / P.splits;
+    it.n = (it.split + 1) * n_all / P.splits - it.c0;
     return it;
   };
   auto has_item = [&](int j) { return item_index(j) < P.num_items; };
@@ -245,10 +254,10 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
         const int jj = w0 + lane;
         return (jj < P.max_blocks_per_seq && jj < nblk) ? trow[jj] : -1;
       };
-      int w0 = 0;
-      int win = window(0);
+      int w0 = it.c0 * NB;  // the split's first block
+      int win = window(w0);
       for (int c = 0; c < it.n; ++c, ++gc) {
-        if (c * NB >= w0 + 32) {
+        if ((it.c0 + c) * NB >= w0 + 32) {
           w0 += 32;
           win = window(w0);
         }
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
         }
         ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
         if (!ok) break;
-        const int jb = c * NB + u;
+        const int jb = (it.c0 + c) * NB + u;
         const int e = __shfl_sync(0xffffffffu, win, jb - w0);
         if (lane < 4 * NB) {
           int row = P.oob_row;  // past the sequence (or a bad entry): zero fill
@@ -407,13 +416,27 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           P.out +
           ((size_t(it.b) * Q + (valid ? i : 0)) * P.num_q_heads + (it.hg0 + h) * G + r0 % G) *
               QM_D;
-      if (r == 0 && it.bad_len && it.tile == 0 && it.hg0 == 0)
+      if (r == 0 && it.bad_len && it.tile == 0 && it.hg0 == 0 && it.split == 0)
         atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
-      if (it.n == 0) {  // an empty sequence: zero rows
-        if (valid)
+      // this row's partials (with several splits)
+      const size_t prow =
+          ((size_t(it.b) * Q + (valid ? i : 0)) * P.num_q_heads + (it.hg0 + h) * G + r0 % G) *
+              P.splits + it.split;
+      if (it.n == 0) {  // no keys in this split (or an empty sequence)
+        if (valid) {
+          if (P.splits == 1) {  // zero rows
 #pragma unroll
-          for (int cg = 0; cg < QM_D; cg += 8)
-            *reinterpret_cast<uint4*>(orow + cg) = make_uint4(0u, 0u, 0u, 0u);
+            for (int cg = 0; cg < QM_D; cg += 8)
+              *reinterpret_cast<uint4*>(orow + cg) = make_uint4(0u, 0u, 0u, 0u);
+          } else {  // an empty partial: weight 2^-inf = 0 in the merge
+            P.part_ml[prow * 2] = -INFINITY;
+            P.part_ml[prow * 2 + 1] = 0.0f;
+#pragma unroll
+            for (int cg = 0; cg < QM_D; cg += 4)
+              *reinterpret_cast<float4*>(P.part_o + prow * QM_D + cg) =
+                  make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
         continue;
       }
       const int L = it.L;
@@ -446,7 +469,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
 #pragma unroll
           for (int kx = 0; kx < NC; ++kx) s[kx] = __uint_as_float(raw[kx]);
         }
-        const int key0 = c * NB * 16;  // key of s[0]; s[kx] is key key0 + kx
+        const int key0 = (it.c0 + c) * NB * 16;  // key of s[0]; s[kx] is key key0 + kx
         if (!__all_sync(0xffffffffu, key0 + NC <= L_row)) {
 #pragma unroll
           for (int kx = 0; kx < NC; ++kx) s[kx] = key0 + kx < L_row ? s[kx] : -INFINITY;
@@ -492,12 +515,12 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           pw[kx / 2] = *reinterpret_cast<const uint32_t*>(&v2);
         }
         l += la + lb;
-        if ((c + 1) * NB * 16 > L) {
+        if ((it.c0 + c + 1) * NB * 16 > L) {
           // keys past the sequence in its last block may hold anything (NaN
           // included): clear their V rows so that 0 * V = 0. Thread r clears
           // row x = r % 64 of half r / 64: block x / BR, key x % 16.
           const int x = r % QM_KC, h2 = r / QM_KC;
-          if ((c * NB + x / BR) * 16 + x % 16 >= L) {
+          if (((it.c0 + c) * NB + x / BR) * 16 + x % 16 >= L) {
             uint4* vrow = reinterpret_cast<uint4*>(ring + size_t(g % QM_ST) * QM_SLOT +
                                                    QM_KV_BYTES + h2 * QM_HALF_KV + x * 128);
 #pragma unroll
@@ -528,11 +551,21 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
       if (!ok) break;
       dev::tc_fence_after();
       const float inv = l > 0.0f ? __frcp_rn(l) : 0.0f;
+      if (P.splits > 1 && valid) {
+        P.part_ml[prow * 2] = m_ref;
+        P.part_ml[prow * 2 + 1] = l;
+      }
 #pragma unroll
       for (int cg = 0; cg < QM_D; cg += 32) {
         float o[32];
         dev::tmem_ld_cols<32>(tmem + t_lane + o_col + cg, o);
-        if (valid) {
+        if (P.splits > 1) {  // the unnormalised row, relative to 2^m_ref
+          if (valid)
+#pragma unroll
+            for (int kx = 0; kx < 32; kx += 4)
+              *reinterpret_cast<float4*>(P.part_o + prow * QM_D + cg + kx) =
+                  make_float4(o[kx], o[kx + 1], o[kx + 2], o[kx + 3]);
+        } else if (valid) {
 #pragma unroll
           for (int kx = 0; kx < 32; kx += 8) {
             uint32_t w[4];
@@ -573,8 +606,43 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   }
 }
 
+// One warp per output row: the splits' partials weighted by 2^(m_s - M)
+// (M the largest reference; a split that saw no key has m = -inf), the sum
+// divided by the weighted sums.
+__global__ void __launch_bounds__(128)
+    query_major_merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
+                             __nv_bfloat16* __restrict__ out, int rows, int splits) {
+  const int row = int(blockIdx.x) * 4 + int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
+  if (row >= rows) return;
+  const float* ml = part_ml + size_t(row) * splits * 2;
+  float M = -INFINITY;
+  for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, ml[sp * 2]);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, lsum = 0.0f;
+  if (M != -INFINITY) {
+    for (int sp = 0; sp < splits; ++sp) {
+      const float m = ml[sp * 2];
+      if (m == -INFINITY) continue;
+      const float wgt = dev::fast_exp2(m - M);
+      lsum += wgt * ml[sp * 2 + 1];
+      const float4 o =
+          *reinterpret_cast<const float4*>(part_o + (size_t(row) * splits + sp) * QM_D + lane * 4);
+      acc[0] += wgt * o.x;
+      acc[1] += wgt * o.y;
+      acc[2] += wgt * o.z;
+      acc[3] += wgt * o.w;
+    }
+  }
+  const float inv = lsum > 0.0f ? __frcp_rn(lsum) : 0.0f;
+  const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&a);
+  w.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(out + size_t(row) * QM_D + lane * 4) = w;
+}
+
 template <int G, int HB>
-int launch_qm_t(const pa_decode_params* p, cudaStream_t stream) {
+int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, float* part_o) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G, HB>,
@@ -609,7 +677,11 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream) {
   P.q_len = Q;
   P.tiles = query_major_tiles(p);
   P.head_groups = H / HB;
-  P.num_items = p->num_seqs * P.head_groups * P.tiles;
+  P.splits = query_major_splits(p);
+  if (P.splits > 1 && (!part_ml || !part_o)) return int(cudaErrorInvalidValue);
+  P.part_ml = part_ml;
+  P.part_o = part_o;
+  P.num_items = p->num_seqs * P.head_groups * P.tiles * P.splits;
   P.max_blocks_per_seq = p->max_blocks_per_seq;
   P.num_blocks = p->num_blocks;
   P.cap = std::min(p->max_blocks_per_seq * 16, p->max_context_len);
@@ -620,23 +692,30 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream) {
   if (sms <= 0) return int(cudaErrorInvalidDevice);
   const dim3 grid(unsigned(std::min(P.num_items, sms)));
   query_major_kernel<G, HB><<<grid, QM_THREADS, QM_SMEM, stream>>>(tk, tv, tq, P);
+  int e = int(cudaGetLastError());
+  if (e || P.splits == 1) return e;
+  const int rows = p->num_seqs * Q * p->num_q_heads;
+  query_major_merge_kernel<<<unsigned((rows + 3) / 4), 128, 0, stream>>>(
+      part_ml, part_o, P.out, rows, P.splits);
   return int(cudaGetLastError());
 }
 
 template <int G>
-int launch_qm_g(const pa_decode_params* p, cudaStream_t stream) {
-  return query_major_heads(p) == 2 ? launch_qm_t<G, 2>(p, stream) : launch_qm_t<G, 1>(p, stream);
+int launch_qm_g(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o) {
+  return query_major_heads(p) == 2 ? launch_qm_t<G, 2>(p, stream, ml, o)
+                                   : launch_qm_t<G, 1>(p, stream, ml, o);
 }
 
 }  // namespace
 
-int launch_query_major_tc(const pa_decode_params* p, void* stream) {
+int launch_query_major_tc(const pa_decode_params* p, void* stream, float* part_ml,
+                          float* part_o) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (p->num_q_heads / p->num_kv_heads) {
-    case 1: return launch_qm_g<1>(p, s);
-    case 2: return launch_qm_g<2>(p, s);
-    case 4: return launch_qm_g<4>(p, s);
-    case 8: return launch_qm_g<8>(p, s);
+    case 1: return launch_qm_g<1>(p, s, part_ml, part_o);
+    case 2: return launch_qm_g<2>(p, s, part_ml, part_o);
+    case 4: return launch_qm_g<4>(p, s, part_ml, part_o);
+    case 8: return launch_qm_g<8>(p, s, part_ml, part_o);
     default: return int(cudaErrorInvalidValue);
   }
 }

@@ -193,17 +193,18 @@ def test_decode_workspace_size(pk):
                 max_blocks_per_seq=128, query_len=2)
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(64, 32, 128, 4, 256,
                                                                          Hkv=8, QL=2)
-    # more new tokens than one column group holds: groups as virtual sequences
+    # more new tokens than one column group holds: the query-major kernel, its
+    # keys unsplit for contexts under 4 chunks (the header only) ...
     for ql in (8, 9, 64):
         p = _params(pk, query_len=ql)
-        assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(2, 8, 128, 1, 256,
-                                                                             QL=ql)
+        assert lib.pa_decode_workspace_size(ctypes.byref(p)) == 256
+    # ... and split over up to 16 CTAs for small batches: 8 sequences x 4 head
+    # pairs = 32 units, 8 splits; partials (m, l) then O rows per (row, split)
     p = _params(pk, num_seqs=8, num_q_heads=32, num_kv_heads=8, max_context_len=2048,
                 max_blocks_per_seq=128, query_len=16)
-    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == _expected_ws(8, 32, 128, 4, 256,
-                                                                         Hkv=8, QL=16)
-    # ... unless the batch gives the query-major kernel 128 (sequence, KV head,
-    # 128-row tile) units: it splits no keys and needs the header only
+    rows = 8 * 16 * 32 * 8
+    assert lib.pa_decode_workspace_size(ctypes.byref(p)) == 256 + rows * 2 * 4 + rows * 128 * 4
+    # 64 sequences x 4 head pairs = 256 units: no split, the header only
     p.num_seqs = 64
     assert lib.pa_decode_workspace_size(ctypes.byref(p)) == 256
     p.query_len = 4  # one column group but 16 rows per KV head: query-major as well

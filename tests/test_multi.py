@@ -205,6 +205,20 @@ def test_query_major_against_the_oracle(pk, G, Hkv, QL, B):
     _check(pk, q, kc, vc, tables, lens, torch)
 
 
+@pytest.mark.parametrize("G,Hkv,QL,lens", [
+    (8, 8, 8, [4100, 2900]),               # 70B-class heads: 8 units, 16 splits
+    (4, 8, 16, [3000, 16, 700, 2049]),     # every key new; splits with no keys
+    (2, 3, 64, [1500, 2600]),              # one head per item (odd head count), two tiles
+    (1, 8, 40, [64, 5000, 333]),
+])
+def test_query_major_split_keys(pk, G, Hkv, QL, lens):
+    """Small batches: each item's keys split over CTAs, fp32 partials merged
+    by log-sum-exp weights; splits past a short sequence's keys (or past a
+    row's causal limit) contribute nothing."""
+    q, kc, vc, tables, lens, torch = _case(lens, QL, G * Hkv, Hkv, 128, seed=740 + QL + G)
+    _check(pk, q, kc, vc, tables, lens, torch)
+
+
 @pytest.mark.parametrize("G,Hkv,QL,B", [(4, 8, 8, 400), (4, 8, 64, 24), (2, 8, 24, 200)])
 def test_query_major_many_items_per_cta(pk, G, Hkv, QL, B):
     """More work items than SMs: each persistent CTA takes several in turn
