@@ -99,7 +99,7 @@ struct QmItem {
   bool bad_len;      // the length broke a rule (reported once per sequence)
 };
 
-template <int G, int HB>
+template <int G, int HB, bool SPLIT>
 __global__ void __launch_bounds__(QM_THREADS, 1)
     query_major_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -190,12 +190,13 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   auto item_of = [&](int j) {
     QmItem it;
     const int x = item_index(j);
-    const int per_seq = P.head_groups * P.tiles * P.splits;
+    const int splits = SPLIT ? P.splits : 1;
+    const int per_seq = P.head_groups * P.tiles * splits;
     const int rank = x / per_seq, rem = x % per_seq;
     it.b = ranked ? order[rank] : rank;
-    it.hg0 = rem / (P.tiles * P.splits) * HB;
-    it.tile = rem / P.splits % P.tiles;
-    it.split = rem % P.splits;
+    it.hg0 = rem / (P.tiles * splits) * HB;
+    it.tile = rem / splits % P.tiles;
+    it.split = SPLIT ? rem % splits : 0;
     int L = P.context_lens[it.b];
     it.bad_len = L > P.cap;
     if (L > P.cap) L = P.cap;
@@ -208,8 +209,8 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     const int keys = L > 0 ? L - Q + i_last + 1 : 0;     // what its last row sees
     it.nblk = (keys + 15) / 16;
     const int n_all = (it.nblk + NB - 1) / NB;  // chunks of all the splits
-    it.c0 = it.split * n_all / P.splits;
-    it.n = (it.split + 1) * n_all / P.splits - it.c0;
+    it.c0 = SPLIT ? it.split * n_all / splits : 0;
+    it.n = SPLIT ? (it.split + 1) * n_all / splits - it.c0 : n_all;
     return it;
   };
   auto has_item = [&](int j) { return item_index(j) < P.num_items; };
@@ -420,11 +421,12 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
         atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
       // this row's partials (with several splits)
       const size_t prow =
-          ((size_t(it.b) * Q + (valid ? i : 0)) * P.num_q_heads + (it.hg0 + h) * G + r0 % G) *
-              P.splits + it.split;
+          SPLIT ? ((size_t(it.b) * Q + (valid ? i : 0)) * P.num_q_heads + (it.hg0 + h) * G +
+                   r0 % G) * P.splits + it.split
+                : 0;
       if (it.n == 0) {  // no keys in this split (or an empty sequence)
         if (valid) {
-          if (P.splits == 1) {  // zero rows
+          if (!SPLIT) {  // zero rows
 #pragma unroll
             for (int cg = 0; cg < QM_D; cg += 8)
               *reinterpret_cast<uint4*>(orow + cg) = make_uint4(0u, 0u, 0u, 0u);
@@ -551,7 +553,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
       if (!ok) break;
       dev::tc_fence_after();
       const float inv = l > 0.0f ? __frcp_rn(l) : 0.0f;
-      if (P.splits > 1 && valid) {
+      if (SPLIT && valid) {
         P.part_ml[prow * 2] = m_ref;
         P.part_ml[prow * 2 + 1] = l;
       }
@@ -559,7 +561,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
       for (int cg = 0; cg < QM_D; cg += 32) {
         float o[32];
         dev::tmem_ld_cols<32>(tmem + t_lane + o_col + cg, o);
-        if (P.splits > 1) {  // the unnormalised row, relative to 2^m_ref
+        if (SPLIT) {  // the unnormalised row, relative to 2^m_ref
           if (valid)
 #pragma unroll
             for (int kx = 0; kx < 32; kx += 4)
@@ -641,11 +643,11 @@ __global__ void __launch_bounds__(128)
   *reinterpret_cast<uint2*>(out + size_t(row) * QM_D + lane * 4) = w;
 }
 
-template <int G, int HB>
+template <int G, int HB, bool SPLIT>
 int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, float* part_o) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G, HB>,
+    cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G, HB, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, QM_SMEM);
     if (e != cudaSuccess) return int(e);
     configured = true;
@@ -678,7 +680,8 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
   P.tiles = query_major_tiles(p);
   P.head_groups = H / HB;
   P.splits = query_major_splits(p);
-  if (P.splits > 1 && (!part_ml || !part_o)) return int(cudaErrorInvalidValue);
+  if ((P.splits > 1) != SPLIT || (SPLIT && (!part_ml || !part_o)))
+    return int(cudaErrorInvalidValue);
   P.part_ml = part_ml;
   P.part_o = part_o;
   P.num_items = p->num_seqs * P.head_groups * P.tiles * P.splits;
@@ -691,7 +694,7 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
   const int sms = tc_grid();
   if (sms <= 0) return int(cudaErrorInvalidDevice);
   const dim3 grid(unsigned(std::min(P.num_items, sms)));
-  query_major_kernel<G, HB><<<grid, QM_THREADS, QM_SMEM, stream>>>(tk, tv, tq, P);
+  query_major_kernel<G, HB, SPLIT><<<grid, QM_THREADS, QM_SMEM, stream>>>(tk, tv, tq, P);
   int e = int(cudaGetLastError());
   if (e || P.splits == 1) return e;
   const int rows = p->num_seqs * Q * p->num_q_heads;
@@ -702,8 +705,12 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
 
 template <int G>
 int launch_qm_g(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o) {
-  return query_major_heads(p) == 2 ? launch_qm_t<G, 2>(p, stream, ml, o)
-                                   : launch_qm_t<G, 1>(p, stream, ml, o);
+  const bool split = query_major_splits(p) > 1;
+  if (query_major_heads(p) == 2)
+    return split ? launch_qm_t<G, 2, true>(p, stream, ml, o)
+                 : launch_qm_t<G, 2, false>(p, stream, ml, o);
+  return split ? launch_qm_t<G, 1, true>(p, stream, ml, o)
+               : launch_qm_t<G, 1, false>(p, stream, ml, o);
 }
 
 }  // namespace
