@@ -201,11 +201,13 @@ static pa_status run_decode(const pa_decode_params* p, unsigned char* ws,
                                    p->num_seqs * query_len_of(p), p->num_kv_heads, p->head_dim,
                                    p->block_size, p->num_blocks, stream, chk);
     }
-    if (!e) {
-      const bool split = query_major_splits(p) > 1;
+    // the decode's set-up overlaps the write (which changes neither tables nor
+    // lengths), or the previous kernel when the caller allows it
+    const bool split = query_major_splits(p) > 1;
+    if (!e)
       e = launch_query_major_tc(p, stream, split ? reinterpret_cast<float*>(ws + w.tc_m) : nullptr,
-                                split ? reinterpret_cast<float*>(ws + w.tc_acc) : nullptr);
-    }
+                                split ? reinterpret_cast<float*>(ws + w.tc_acc) : nullptr,
+                                append != nullptr || p->overlap_prologue != 0);
   } else if (decode_uses_tc(p)) {
     if (grid <= 0)
       return set_cuda_error("the SM count of the current device", int(cudaErrorNoDevice));

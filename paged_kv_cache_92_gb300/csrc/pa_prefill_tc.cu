@@ -6,7 +6,9 @@
 // row is new token i of query head (kv head)*G + g and sees the sequence's
 // first L - Q + i + 1 keys. With several splits (small batches) each item
 // leaves fp32 partials (running maximum, sum, unnormalised O row) and a merge
-// kernel combines a row's splits, as in a split-K decode.
+// kernel combines a row's splits, as in a split-K decode. After the step's KV
+// write the kernel launches as a programmatic dependent: its set-up overlaps
+// the write, and every thread waits for it before touching the cache.
 //
 // The column-group decode (pa_decode_tc.cuh) puts the keys on the MMAs' M side
 // and streams them once per group of new tokens; with many new tokens each
@@ -95,7 +97,8 @@ struct QmItem {
   int b, hg0, tile;  // sequence, first KV head, tile of new tokens
   int split, c0;     // split of the keys, its first chunk
   int L;             // length after the rules (0: an empty sequence)
-  int nblk, n;       // blocks the item's last row sees, chunks
+  int keys;          // keys the item's last row sees
+  int nblk, n;       // blocks of those keys, chunks of this split
   bool bad_len;      // the length broke a rule (reported once per sequence)
 };
 
@@ -182,6 +185,9 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   __syncthreads();
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a programmatic dependent (after the step's KV write): nothing
+  // above touched the cache or the outputs
+  dev::griddep_wait();
 
   // The items of this CTA: pass j takes item j*grid + k (j even) or
   // j*grid + grid - 1 - k (j odd).
@@ -207,6 +213,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     it.L = L;
     const int i_last = min(Q, (it.tile + 1) * QT) - 1;  // the item's last new token
     const int keys = L > 0 ? L - Q + i_last + 1 : 0;     // what its last row sees
+    it.keys = keys;
     it.nblk = (keys + 15) / 16;
     const int n_all = (it.nblk + NB - 1) / NB;  // chunks of all the splits
     it.c0 = SPLIT ? it.split * n_all / splits : 0;
@@ -517,12 +524,14 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           pw[kx / 2] = *reinterpret_cast<const uint32_t*>(&v2);
         }
         l += la + lb;
-        if ((it.c0 + c + 1) * NB * 16 > L) {
-          // keys past the sequence in its last block may hold anything (NaN
-          // included): clear their V rows so that 0 * V = 0. Thread r clears
-          // row x = r % 64 of half r / 64: block x / BR, key x % 16.
+        if ((it.c0 + c + 1) * NB * 16 > it.keys) {
+          // keys past what the item's rows see may hold anything (NaN
+          // included): past the sequence in its last block, and new tokens
+          // of a later tile that its own item writes. Clear their V rows so
+          // that 0 * V = 0. Thread r clears row x = r % 64 of half r / 64:
+          // block x / BR, key x % 16.
           const int x = r % QM_KC, h2 = r / QM_KC;
-          if (((it.c0 + c) * NB + x / BR) * 16 + x % 16 >= L) {
+          if (((it.c0 + c) * NB + x / BR) * 16 + x % 16 >= it.keys) {
             uint4* vrow = reinterpret_cast<uint4*>(ring + size_t(g % QM_ST) * QM_SLOT +
                                                    QM_KV_BYTES + h2 * QM_HALF_KV + x * 128);
 #pragma unroll
@@ -644,7 +653,8 @@ __global__ void __launch_bounds__(128)
 }
 
 template <int G, int HB, bool SPLIT>
-int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, float* part_o) {
+int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, float* part_o,
+                bool dependent) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G, HB, SPLIT>,
@@ -693,9 +703,17 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
   P.wait_ns = p->wait_timeout_us > 0 ? uint64_t(p->wait_timeout_us) * 1000u : dev::kWaitNsLimit;
   const int sms = tc_grid();
   if (sms <= 0) return int(cudaErrorInvalidDevice);
-  const dim3 grid(unsigned(std::min(P.num_items, sms)));
-  query_major_kernel<G, HB, SPLIT><<<grid, QM_THREADS, QM_SMEM, stream>>>(tk, tv, tq, P);
-  int e = int(cudaGetLastError());
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(std::min(P.num_items, sms)));
+  cfg.blockDim = dim3(QM_THREADS);
+  cfg.dynamicSmemBytes = QM_SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int e = int(cudaLaunchKernelEx(&cfg, query_major_kernel<G, HB, SPLIT>, tk, tv, tq, P));
   if (e || P.splits == 1) return e;
   const int rows = p->num_seqs * Q * p->num_q_heads;
   query_major_merge_kernel<<<unsigned((rows + 3) / 4), 128, 0, stream>>>(
@@ -704,25 +722,25 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
 }
 
 template <int G>
-int launch_qm_g(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o) {
+int launch_qm_g(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o, bool a) {
   const bool split = query_major_splits(p) > 1;
   if (query_major_heads(p) == 2)
-    return split ? launch_qm_t<G, 2, true>(p, stream, ml, o)
-                 : launch_qm_t<G, 2, false>(p, stream, ml, o);
-  return split ? launch_qm_t<G, 1, true>(p, stream, ml, o)
-               : launch_qm_t<G, 1, false>(p, stream, ml, o);
+    return split ? launch_qm_t<G, 2, true>(p, stream, ml, o, a)
+                 : launch_qm_t<G, 2, false>(p, stream, ml, o, a);
+  return split ? launch_qm_t<G, 1, true>(p, stream, ml, o, a)
+               : launch_qm_t<G, 1, false>(p, stream, ml, o, a);
 }
 
 }  // namespace
 
 int launch_query_major_tc(const pa_decode_params* p, void* stream, float* part_ml,
-                          float* part_o) {
+                          float* part_o, bool dependent) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (p->num_q_heads / p->num_kv_heads) {
-    case 1: return launch_qm_g<1>(p, s, part_ml, part_o);
-    case 2: return launch_qm_g<2>(p, s, part_ml, part_o);
-    case 4: return launch_qm_g<4>(p, s, part_ml, part_o);
-    case 8: return launch_qm_g<8>(p, s, part_ml, part_o);
+    case 1: return launch_qm_g<1>(p, s, part_ml, part_o, dependent);
+    case 2: return launch_qm_g<2>(p, s, part_ml, part_o, dependent);
+    case 4: return launch_qm_g<4>(p, s, part_ml, part_o, dependent);
+    case 8: return launch_qm_g<8>(p, s, part_ml, part_o, dependent);
     default: return int(cudaErrorInvalidValue);
   }
 }

@@ -47,7 +47,12 @@ inline bool use_query_major(const pa_decode_params* p) {
 
 // part_ml / part_o: the workspace's partials when query_major_splits(p) > 1
 // ([B*Q*Hq][splits][2] and [B*Q*Hq][splits][128] floats), else unused.
-int launch_query_major_tc(const pa_decode_params* p, void* stream, float* part_ml, float* part_o);
+// dependent: launch as a programmatic dependent of the previous kernel (its
+// set-up overlaps that kernel; every thread waits for it before touching the
+// cache or the outputs) -- after the step's KV write, or when the caller says
+// the tables and lengths were final before the previous kernel began.
+int launch_query_major_tc(const pa_decode_params* p, void* stream, float* part_ml, float* part_o,
+                          bool dependent);
 // Its device error word shares the tensor-core decode's.
 int read_and_clear_query_major_errors(uint32_t* flags);
 

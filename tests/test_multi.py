@@ -264,12 +264,19 @@ def test_query_major_placement_invariance_bit_exact(pk):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_query_major_fused_append(pk):
-    """pa_append_decode on this path: the KV write with the slot rule, then the
+@pytest.mark.parametrize("QL,lens,G", [
+    (16, None, 4),                          # 16 sequences: two heads per item, 4 splits
+    (64, [3000, 64, 500, 65], 4),           # one head per item, two tiles, 5 splits
+    (8, [900] * 40 + [2049] * 24, 8),       # 256 items, no split
+])
+def test_query_major_fused_append(pk, QL, lens, G):
+    """pa_append_decode on this path: the KV write inside the kernel (each item
+    writes the new tokens among its keys before it loads them; the new slots
+    hold NaN before the step, so a read before the write shows), then the
     query-major decode; caches bit-exact, rows against the oracle."""
-    QL = 16
-    lens = _qm_lens(QL)
-    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case(lens, QL, 32, 8, seed=722)
+    lens = _qm_lens(QL) if lens is None else lens
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case(lens, QL, 8 * G, 8,
+                                                                 seed=722 + QL)
     kc2, vc2 = kc.clone(), vc.clone()
     out = pk.pa_append_decode(q, kc2, vc2, torch.from_numpy(tables).cuda(),
                               torch.from_numpy(lens).cuda(), int(lens.max()), kn, vn,
@@ -282,6 +289,30 @@ def test_query_major_fused_append(pk):
     assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
     want = oracle.paged_decode_multi(q.cpu(), ko, vo, tables, lens)
     harness.assert_close(harness.bf16_tensor_to_f64(out), want)
+
+
+def test_query_major_fused_append_slot_rules(pk):
+    """A slot that is not its token's is not written (PA_DEVERR_APPEND_SLOT); a
+    negative slot writes nothing; the other tokens are written, split items
+    included."""
+    QL = 16
+    q, kc, vc, tables, lens, slots, kn, vn, torch = _append_case([40, 70, 300, 2049], QL, 32, 8,
+                                                                 seed=760)
+    bad = slots.copy()
+    bad[1] = slots[1] + 1 if slots[1] % 16 != 15 else slots[1] - 1  # wrong offset
+    bad[20] = -1
+    bad[60] = slots[62]  # another token's slot
+    kc2, vc2 = kc.clone(), vc.clone()
+    pk.pa_append_decode(q, kc2, vc2, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                        int(lens.max()), kn, vn, torch.from_numpy(bad).cuda())
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() & DEVERR_APPEND_SLOT
+    written = [t for t in range(len(slots)) if t not in (1, 20, 60)]
+    ko, vo = oracle.reshape_and_cache(kn.cpu()[written], vn.cpu()[written],
+                                      oracle.bf16_bits(kc.cpu()), oracle.bf16_bits(vc.cpu()),
+                                      slots[written])
+    assert np.array_equal(oracle.bf16_bits(kc2.cpu()), ko)
+    assert np.array_equal(oracle.bf16_bits(vc2.cpu()), vo)
 
 
 def test_query_major_llama8b_layer(pk):
