@@ -185,9 +185,6 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   __syncthreads();
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // launched as a programmatic dependent (after the step's KV write): nothing
-  // above touched the cache or the outputs
-  dev::griddep_wait();
 
   // The items of this CTA: pass j takes item j*grid + k (j even) or
   // j*grid + grid - 1 - k (j odd).
@@ -222,6 +219,28 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   };
   auto has_item = [&](int j) { return item_index(j) < P.num_items; };
 
+  // Launched as a programmatic dependent (after the step's KV write, which
+  // changes neither the tables, the lengths nor q): nothing above touched the
+  // cache or the outputs, and the producer requests the first item's Q
+  // before the dependency wait.
+  int q_first = -1;  // producer lane 0: the item whose Q is already requested
+  if (warp == 4 && lane == 0) {
+    for (int j = 0; has_item(j); ++j) {
+      const QmItem it = item_of(j);
+      if (it.n == 0) continue;
+      const uint64_t pol = dev::l2_evict_first_policy();
+      dev::mbar_arrive_expect_tx(&qfull[0], QM_Q_BYTES);
+      for (int h2 = 0; h2 < 2; ++h2)
+        for (int h = 0; h < HB; ++h)
+          dev::tma_load_4d(qbuf + h2 * QM_HALF_Q + h * RPH * 128, &tm_q, h2 * 64,
+                           (it.hg0 + h) * G, it.tile * QT, it.b, &qfull[0], pol);
+      *q_issued = 1;
+      q_first = j;
+      break;
+    }
+  }
+  dev::griddep_wait();
+
   if (warp == 4) {
     // ---------------------------------------------------------- producer
     const uint64_t pol = dev::l2_evict_first_policy();
@@ -239,7 +258,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
       const QmItem it = item_of(j);
       if (it.n == 0) continue;
       const int nblk = it.nblk;
-      if (lane == 0) {
+      if (lane == 0 && j != q_first) {
         // Q of this item into buffer qi % 2 once the scores of the item that
         // used it last have completed
         const int qb = qi & 1;
