@@ -156,17 +156,25 @@ typedef struct {
                                   [num_seqs][Q][num_q_heads][head_dim], the new tokens are the
                                   last Q of each sequence's context_lens[b] (already in the cache),
                                   and query token i attends to the first context_lens[b] - Q + i + 1
-                                  of them (causal among the new tokens). The tensor-core
-                                  kernel's MMAs take the query tokens in column groups: G * Qp <= 16
-                                  columns per KV head (8 at block size 8, Qp = the group's tokens
-                                  rounded up to a power of two) and num_kv_heads * G * Qp <= 128
-                                  (64 for the 8-bit cache); a sequence with more new tokens is
-                                  decoded as several groups, each streaming the keys its last
-                                  token sees, with num_seqs * groups <= 16384. Shapes beyond
-                                  that, and the CUDA-core variant, decode each (sequence, token)
-                                  on its own with num_seqs * Q <= 65535 (else
-                                  PA_ERR_UNSUPPORTED; bf16 cache, block size 16). A sequence with
-                                  0 < context_lens[b] < Q gets zero rows and
+                                  of them (causal among the new tokens). On the tensor-core
+                                  variant with the bf16 cache, head_dim 128, block size 16 and
+                                  G in {1, 2, 4, 8}, a query-major kernel takes the new tokens
+                                  when they are more than one column group holds (below), or
+                                  when Q * G >= 16 and num_seqs * num_kv_heads * ceil(Q * G /
+                                  128) >= 128: the query rows of one or two KV heads share each
+                                  load of their keys; batches with fewer than 256 such units
+                                  split each unit's keys over CTAs and merge the partials
+                                  (workspace: pa_decode_workspace_size). Otherwise the
+                                  tensor-core kernel's MMAs take the query tokens in column
+                                  groups: G * Qp <= 16 columns per KV head (8 at block size 8,
+                                  Qp = the group's tokens rounded up to a power of two) and
+                                  num_kv_heads * G * Qp <= 128 (64 for the 8-bit cache); a
+                                  sequence with more new tokens is decoded as several groups,
+                                  each streaming the keys its last token sees, with num_seqs *
+                                  groups <= 16384. Shapes beyond that, and the CUDA-core
+                                  variant, decode each (sequence, token) on its own with
+                                  num_seqs * Q <= 65535 (else PA_ERR_UNSUPPORTED). A sequence
+                                  with 0 < context_lens[b] < Q gets zero rows and
                                   PA_DEVERR_CONTEXT_LEN. */
   int32_t wait_timeout_us;     /* tensor-core kernel: the longest one of its barrier waits may
                                   take, in microseconds; 0 = 2 s. A wait that runs out sets
