@@ -219,6 +219,26 @@ def test_query_major_split_keys(pk, G, Hkv, QL, lens):
     _check(pk, q, kc, vc, tables, lens, torch)
 
 
+@pytest.mark.parametrize("seed", range(24))
+def test_query_major_random_shapes(pk, seed):
+    """Seeded random shapes across the query-major space: G, the KV head
+    count (odd included), Q, the batch (split keys or not) and lengths from Q
+    up, some on block and chunk boundaries; the oracle's work is kept small."""
+    rng = np.random.default_rng(900 + seed)
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hkv = int(rng.choice([1, 2, 3, 4, 8]))
+    QL = int(rng.integers(3, 81))
+    B = int(rng.integers(1, 41))
+    budget = 1e8  # query rows x keys
+    lmax = max(QL + 1, min(4000, int(budget / (B * QL * G * Hkv))))
+    lens = rng.integers(QL, lmax + 1, size=B)
+    edges = [QL, QL + 1, 16 * ((QL + 15) // 16), 64 * ((QL + 63) // 64) + 1]
+    for k in range(min(B, len(edges))):
+        lens[k] = min(edges[k], lmax)
+    q, kc, vc, tables, lens, torch = _case(lens, QL, G * Hkv, Hkv, 128, seed=950 + seed)
+    _check(pk, q, kc, vc, tables, lens, torch)
+
+
 @pytest.mark.parametrize("G,Hkv,QL,B", [(4, 8, 8, 400), (4, 8, 64, 24), (2, 8, 24, 200)])
 def test_query_major_many_items_per_cta(pk, G, Hkv, QL, B):
     """More work items than SMs: each persistent CTA takes several in turn
