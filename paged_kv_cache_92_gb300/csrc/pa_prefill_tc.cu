@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_q, const QmParams P) {
   constexpr int RPH = QM_ROWS / HB;  // rows per head
-  constexpr int QT = RPH / G;        // new tokens per item
+  constexpr int QT = RPH / G;        // new tokens per tile
   constexpr int NB = 4 / HB;         // blocks per chunk
   constexpr int BR = 16 * HB;        // rows of one block's box (HB heads x 16 keys)
   constexpr int NC = 16 * NB;        // scores of a chunk per thread (its head's keys)
@@ -544,11 +544,10 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
         }
         l += la + lb;
         if ((it.c0 + c + 1) * NB * 16 > it.keys) {
-          // keys past what the item's rows see may hold anything (NaN
-          // included): past the sequence in its last block, and new tokens
-          // of a later tile that its own item writes. Clear their V rows so
-          // that 0 * V = 0. Thread r clears row x = r % 64 of half r / 64:
-          // block x / BR, key x % 16.
+          // no row of the item sees the keys from it.keys on; past the
+          // sequence, in its last block, they may hold anything (NaN
+          // included). Clear their V rows so that 0 * V = 0. Thread r clears
+          // row x = r % 64 of half r / 64: block x / BR, key x % 16.
           const int x = r % QM_KC, h2 = r / QM_KC;
           if (((it.c0 + c) * NB + x / BR) * 16 + x % 16 >= it.keys) {
             uint4* vrow = reinterpret_cast<uint4*>(ring + size_t(g % QM_ST) * QM_SLOT +
