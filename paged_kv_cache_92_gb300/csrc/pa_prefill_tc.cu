@@ -30,12 +30,13 @@
 //
 // Layout of an item's 128 rows (TMEM lanes): HB heads x RPH rows, row r0 of a
 // head being token tile*QT + r0/G, query head g = r0 % G. A chunk's 64 columns
-// are NB = 4/HB blocks x HB heads x 16 keys: one 2-D tensor-map box
-// [HB*16 rows][64 d] per block and 64-d half (the HB heads of a block are
-// adjacent in the cache), so with HB = 2 every TMA request moves 4 KiB (the
-// TMA unit spends a fixed time per request: streaming 2 KiB requests tops out
-// well below 4 KiB ones). A row's scores against the other heads' keys are
-// computed and ignored: its P is zero there.
+// are NB = 64/(BS*HB) blocks x HB heads x BS keys (BS the block size, 16 or
+// 32): one 2-D tensor-map box [HB*BS rows][64 d] per block and 64-d half (the
+// HB heads of a block are adjacent in the cache), so every TMA request moves
+// 4 KiB or more with HB = 2 or BS = 32 (the TMA unit spends a fixed time per
+// request: streaming 2 KiB requests tops out well below 4 KiB ones). A row's
+// scores against the other heads' keys are computed and ignored: its P is
+// zero there.
 #include "pa_decode_tc.cuh"
 #include "pa_query_major.h"
 
@@ -102,17 +103,17 @@ struct QmItem {
   bool bad_len;      // the length broke a rule (reported once per sequence)
 };
 
-template <int G, int HB, bool SPLIT>
+template <int G, int HB, bool SPLIT, int BS>
 __global__ void __launch_bounds__(QM_THREADS, 1)
     query_major_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_q, const QmParams P) {
   constexpr int RPH = QM_ROWS / HB;  // rows per head
   constexpr int QT = RPH / G;        // new tokens per tile
-  constexpr int NB = 4 / HB;         // blocks per chunk
-  constexpr int BR = 16 * HB;        // rows of one block's box (HB heads x 16 keys)
-  constexpr int NC = 16 * NB;        // scores of a chunk per thread (its head's keys)
-  static_assert(QT >= 1, "tile shape");
+  constexpr int BR = BS * HB;        // rows of one block's box (HB heads x BS keys)
+  constexpr int NB = QM_KC / BR;     // blocks per chunk
+  constexpr int NC = BS * NB;        // scores of a chunk per thread (its head's keys)
+  static_assert(QT >= 1 && NB >= 1 && BS % 16 == 0, "tile shape");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     const int i_last = min(Q, (it.tile + 1) * QT) - 1;  // the item's last new token
     const int keys = L > 0 ? L - Q + i_last + 1 : 0;     // what its last row sees
     it.keys = keys;
-    it.nblk = (keys + 15) / 16;
+    it.nblk = (keys + BS - 1) / BS;
     const int n_all = (it.nblk + NB - 1) / NB;  // chunks of all the splits
     it.c0 = SPLIT ? it.split * n_all / splits : 0;
     it.n = SPLIT ? (it.split + 1) * n_all / splits - it.c0 : n_all;
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           int row = P.oob_row;  // past the sequence (or a bad entry): zero fill
           if (jb < nblk) {
             if (e >= 0 && e < P.num_blocks) {
-              row = (e * P.num_kv_heads + it.hg0) * 16;
+              row = (e * P.num_kv_heads + it.hg0) * BS;
             } else if (kv == 0 && hf == 0) {
               atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
             }
@@ -477,12 +478,12 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
                                                     P.wait_ns, abort_flag));
         if (!ok) break;
         dev::tc_fence_after();
-        // this thread's scores: block u of the chunk, 16 columns at u*BR + h*16
+        // this thread's scores: block u of the chunk, BS columns at u*BR + h*BS
         float s[NC];
         {
           uint32_t raw[NC];
 #pragma unroll
-          for (int t = 0; t < NB; ++t)
+          for (int t = 0; t < NC / 16; ++t)  // 16 columns at a time
             asm volatile(
                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
                 "%10, %11, %12, %13, %14, %15}, [%16];"
@@ -492,12 +493,13 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
                   "=r"(raw[16 * t + 9]), "=r"(raw[16 * t + 10]), "=r"(raw[16 * t + 11]),
                   "=r"(raw[16 * t + 12]), "=r"(raw[16 * t + 13]), "=r"(raw[16 * t + 14]),
                   "=r"(raw[16 * t + 15])
-                : "r"(tmem + t_lane + uint32_t(g & 1) * QM_KC + uint32_t(t * BR + h * 16)));
+                : "r"(tmem + t_lane + uint32_t(g & 1) * QM_KC +
+                      uint32_t(t / (BS / 16) * BR + h * BS + t % (BS / 16) * 16)));
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
           for (int kx = 0; kx < NC; ++kx) s[kx] = __uint_as_float(raw[kx]);
         }
-        const int key0 = (it.c0 + c) * NB * 16;  // key of s[0]; s[kx] is key key0 + kx
+        const int key0 = (it.c0 + c) * NB * BS;  // key of s[0]; s[kx] is key key0 + kx
         if (!__all_sync(0xffffffffu, key0 + NC <= L_row)) {
 #pragma unroll
           for (int kx = 0; kx < NC; ++kx) s[kx] = key0 + kx < L_row ? s[kx] : -INFINITY;
@@ -543,13 +545,13 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           pw[kx / 2] = *reinterpret_cast<const uint32_t*>(&v2);
         }
         l += la + lb;
-        if ((it.c0 + c + 1) * NB * 16 > it.keys) {
+        if ((it.c0 + c + 1) * NB * BS > it.keys) {
           // no row of the item sees the keys from it.keys on; past the
           // sequence, in its last block, they may hold anything (NaN
           // included). Clear their V rows so that 0 * V = 0. Thread r clears
-          // row x = r % 64 of half r / 64: block x / BR, key x % 16.
+          // row x = r % 64 of half r / 64: block x / BR, key x % BS.
           const int x = r % QM_KC, h2 = r / QM_KC;
-          if (((it.c0 + c) * NB + x / BR) * 16 + x % 16 >= it.keys) {
+          if (((it.c0 + c) * NB + x / BR) * BS + x % BS >= it.keys) {
             uint4* vrow = reinterpret_cast<uint4*>(ring + size_t(g % QM_ST) * QM_SLOT +
                                                    QM_KV_BYTES + h2 * QM_HALF_KV + x * 128);
 #pragma unroll
@@ -557,17 +559,17 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           }
           dev::fence_async_smem();  // before the value product reads the ring
         }
-        // P[g % 2]: column m holds chunk columns 2m, 2m+1; block u's 16
-        // columns of this head are P columns (u*BR + h*16)/2 + [0, 8), the
-        // rest zero. The value product of chunk g - 2 read this buffer last.
+        // P[g % 2]: column m holds chunk columns 2m, 2m+1; block u's BS
+        // columns of this head are P columns (u*BR + h*BS)/2 + [0, BS/2),
+        // the rest zero. The value product of chunk g - 2 read this buffer last.
         if (g >= 2 && pv_done < g - 2) wait_pv(g - 2);
         if (!ok) break;
         {
           float pp[QM_KC / 2];
 #pragma unroll
           for (int m = 0; m < QM_KC / 2; ++m) {
-            const int u = 2 * m / BR, hh = 2 * m % BR / 16;  // block and head of P column m
-            pp[m] = hh == h ? __uint_as_float(pw[8 * u + m % 8]) : 0.0f;
+            const int u = 2 * m / BR, hh = 2 * m % BR / BS;  // block and head of P column m
+            pp[m] = hh == h ? __uint_as_float(pw[u * BS / 2 + m % (BS / 2)]) : 0.0f;
           }
           dev::tmem_st_cols<QM_KC / 2>(tmem + t_lane + QM_TMEM_P + uint32_t(g & 1) * 32, pp);
         }
@@ -670,22 +672,22 @@ __global__ void __launch_bounds__(128)
   *reinterpret_cast<uint2*>(out + size_t(row) * QM_D + lane * 4) = w;
 }
 
-template <int G, int HB, bool SPLIT>
+template <int G, int HB, bool SPLIT, int BS>
 int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, float* part_o,
                 bool dependent) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G, HB, SPLIT>,
+    cudaError_t e = cudaFuncSetAttribute(query_major_kernel<G, HB, SPLIT, BS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, QM_SMEM);
     if (e != cudaSuccess) return int(e);
     configured = true;
   }
   const int H = p->num_kv_heads, Q = query_len_of(p);
-  const uint64_t cache_rows = uint64_t(p->num_blocks) * H * 16;
+  const uint64_t cache_rows = uint64_t(p->num_blocks) * H * BS;
   CUtensorMap tk, tv, tq;
-  // K, V [rows][128 d]: a box of HB heads x 16 keys of one block, one 64-d half
-  int r = make_map(&tk, p->k_cache, cache_rows, QM_D, uint32_t(16 * HB));
-  if (!r) r = make_map(&tv, p->v_cache, cache_rows, QM_D, uint32_t(16 * HB));
+  // K, V [rows][128 d]: a box of HB heads x BS keys of one block, one 64-d half
+  int r = make_map(&tk, p->k_cache, cache_rows, QM_D, uint32_t(BS * HB));
+  if (!r) r = make_map(&tv, p->v_cache, cache_rows, QM_D, uint32_t(BS * HB));
   if (!r) {
     // q [B][Q][Hq][128]: box (64 d, G heads, QT tokens, 1 sequence)
     const cuuint64_t dims[4] = {uint64_t(QM_D), uint64_t(p->num_q_heads), uint64_t(Q),
@@ -715,7 +717,7 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
   P.num_items = p->num_seqs * P.head_groups * P.tiles * P.splits;
   P.max_blocks_per_seq = p->max_blocks_per_seq;
   P.num_blocks = p->num_blocks;
-  P.cap = std::min(p->max_blocks_per_seq * 16, p->max_context_len);
+  P.cap = std::min(p->max_blocks_per_seq * BS, p->max_context_len);
   P.oob_row = int(cache_rows);
   P.scale_log2 = p->scale * kLog2e;
   P.wait_ns = p->wait_timeout_us > 0 ? uint64_t(p->wait_timeout_us) * 1000u : dev::kWaitNsLimit;
@@ -731,7 +733,7 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int e = int(cudaLaunchKernelEx(&cfg, query_major_kernel<G, HB, SPLIT>, tk, tv, tq, P));
+  int e = int(cudaLaunchKernelEx(&cfg, query_major_kernel<G, HB, SPLIT, BS>, tk, tv, tq, P));
   if (e || P.splits == 1) return e;
   const int rows = p->num_seqs * Q * p->num_q_heads;
   query_major_merge_kernel<<<unsigned((rows + 3) / 4), 128, 0, stream>>>(
@@ -739,14 +741,19 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
   return int(cudaGetLastError());
 }
 
-template <int G>
-int launch_qm_g(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o, bool a) {
+template <int G, int BS>
+int launch_qm_b(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o, bool a) {
   const bool split = query_major_splits(p) > 1;
   if (query_major_heads(p) == 2)
-    return split ? launch_qm_t<G, 2, true>(p, stream, ml, o, a)
-                 : launch_qm_t<G, 2, false>(p, stream, ml, o, a);
-  return split ? launch_qm_t<G, 1, true>(p, stream, ml, o, a)
-               : launch_qm_t<G, 1, false>(p, stream, ml, o, a);
+    return split ? launch_qm_t<G, 2, true, BS>(p, stream, ml, o, a)
+                 : launch_qm_t<G, 2, false, BS>(p, stream, ml, o, a);
+  return split ? launch_qm_t<G, 1, true, BS>(p, stream, ml, o, a)
+               : launch_qm_t<G, 1, false, BS>(p, stream, ml, o, a);
+}
+template <int G>
+int launch_qm_g(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o, bool a) {
+  return p->block_size == 32 ? launch_qm_b<G, 32>(p, stream, ml, o, a)
+                             : launch_qm_b<G, 16>(p, stream, ml, o, a);
 }
 
 }  // namespace

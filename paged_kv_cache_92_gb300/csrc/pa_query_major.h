@@ -32,14 +32,15 @@ inline int query_major_splits(const pa_decode_params* p) {
   if (ns > 16) ns = 16;
   return ns < 1 ? 1 : ns;
 }
-// It takes the bf16 cache at head_dim 128 and block size 16 when the
+// It takes the bf16 cache at head_dim 128 and block size 16 or 32 when the
 // column-group decode would split the new tokens into several groups (each
 // re-reading the keys), or when a KV head has at least 16 query rows (new
 // tokens x G) and the batch gives it 128 (sequence, KV head, tile) units.
 inline bool use_query_major(const pa_decode_params* p) {
   const int g = p->num_q_heads / p->num_kv_heads;
   return p->variant == PA_DECODE_TENSOR_CORE && p->kv_dtype == PA_KV_BF16 && p->head_dim == 128 &&
-         p->block_size == 16 && query_len_of(p) > 1 && (g == 1 || g == 2 || g == 4 || g == 8) &&
+         (p->block_size == 16 || p->block_size == 32) && query_len_of(p) > 1 &&
+         (g == 1 || g == 2 || g == 4 || g == 8) &&
          (tc_n_groups(p) > 1 ||
           (query_len_of(p) * g >= 16 &&
            int64_t(p->num_seqs) * p->num_kv_heads * query_major_tiles(p) >= 128));

@@ -137,6 +137,23 @@ def test_multi_token(pk, bs, G, Hkv, QL):
     assert pk.pa_device_errors() == 0
 
 
+@pytest.mark.parametrize("G,Hkv,QL,lens", [
+    (4, 8, 8, [5000, 40, 33, 700] * 4),    # two heads per item (one 32-key block a chunk)
+    (4, 8, 64, [3000, 64, 65, 1023]),      # one head per item (two blocks a chunk), two tiles
+    (8, 8, 8, [4100, 2900]),               # keys split over CTAs
+    (2, 3, 16, [1500, 16, 2600]),          # odd KV head count
+    (4, 8, 16, [900, 31, 32, 33] * 16),    # 256 items, no split
+])
+def test_query_major_block_size_32(pk, G, Hkv, QL, lens):
+    """The query-major kernel at block size 32: boxes of HB heads x 32 keys,
+    lengths across 32-key block and chunk boundaries, every key new at L = Q."""
+    q, kc, vc, tables, lens, torch = _case(lens, G * Hkv, Hkv, 32, seed=180 + G + QL, QL=QL)
+    out = _decode(pk, q, kc, vc, tables, lens, torch)
+    ref = oracle.paged_decode_multi(q.cpu(), kc.cpu(), vc.cpu(), tables, lens)
+    harness.assert_close(harness.bf16_tensor_to_f64(out), ref)
+    assert pk.pa_device_errors() == 0
+
+
 @BLOCK_SIZES
 def test_copy_blocks_bit_exact(pk, bs):
     import torch
