@@ -682,7 +682,8 @@ def measure_multi_workloads(pk, device, steps: int = 200, launches: int = 100, w
              ("llama8b_layer_b64_q64", workloads.llama8b_layer(), 64),
              ("llama70b_long_b8_q8", workloads.llama70b_long(batch=8), 8),
              ("llama8b_high_concurrency_b256_q4", workloads.llama8b_high_concurrency(), 4),
-             ("llama70b_long_b8_q2", workloads.llama70b_long(batch=8), 2)]
+             ("llama70b_long_b8_q2", workloads.llama70b_long(batch=8), 2),
+             ("llama8b_layer_b64_bs32_q8", workloads.llama8b_layer(block_size=32), 8)]
     peak = measured_peaks()["hbm_gbs"]
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream or None
@@ -695,7 +696,8 @@ def measure_multi_workloads(pk, device, steps: int = 200, launches: int = 100, w
         B = len(lens)
         pos = (lens[:, None] - Q + np.arange(Q)[None, :]).reshape(-1)
         seq = np.repeat(np.arange(B), Q)
-        slots = (tables[seq, pos // 16].astype(np.int64) * 16 + pos % 16).astype(np.int64)
+        bs = r.block_size
+        slots = (tables[seq, pos // bs].astype(np.int64) * bs + pos % bs).astype(np.int64)
         g = torch.Generator(device="cpu").manual_seed(7)
         q = torch.randn(B, Q, Hq, D, generator=g).to(torch.bfloat16).to(device)
         kn = torch.randn(B * Q, H, D, generator=g).to(torch.bfloat16).to(device)

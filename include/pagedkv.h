@@ -157,8 +157,8 @@ typedef struct {
                                   last Q of each sequence's context_lens[b] (already in the cache),
                                   and query token i attends to the first context_lens[b] - Q + i + 1
                                   of them (causal among the new tokens). On the tensor-core
-                                  variant with the bf16 cache, head_dim 128, block size 16 and
-                                  G in {1, 2, 4, 8}, a query-major kernel takes the new tokens
+                                  variant with the bf16 cache, head_dim 128, block size 16 or 32
+                                  and G in {1, 2, 4, 8}, a query-major kernel takes the new tokens
                                   when they are more than one column group holds (below), or
                                   when Q * G >= 16 and num_seqs * num_kv_heads * ceil(Q * G /
                                   128) >= 128: the query rows of one or two KV heads share each
