@@ -637,6 +637,490 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------ two tiles per item
+// With one KV head per item and an even number of 128-row tiles per head
+// (many rows, large batches), an item takes two tiles of a head: each chunk of
+// keys is loaded once and serves both tiles' scores and value products, which
+// halves the TMA requests. Eight softmax warps (two per TMEM lane quarter: warp
+// w serves tile w / 4, lanes 32 * (w % 4) ..); TMEM holds S[tile][2] with P
+// over the first 32 columns of its S buffer, and O[tile] (512 columns), so the
+// scores of chunk g wait for the value product of chunk g - 2 of the same tile
+// and an item's first value product for its tile's previous read-out. Q of
+// both tiles (64 KiB) is one buffer, loaded once the previous item's scores
+// have completed.
+constexpr int QD_THREADS = 320;  // softmax warps 0-7, producer 8, MMA 9
+constexpr int QD_OFF_Q = 0;
+constexpr int QD_OFF_RING = QD_OFF_Q + 2 * QM_Q_BYTES;
+constexpr int QD_OFF_BARS = QD_OFF_RING + QM_ST * QM_SLOT;
+// full[ST], empty[ST], qfull, qempty, s[2][2], p[2][2], o[2][2], oempty[2], drain
+constexpr int QD_NBARS = 2 * QM_ST + 17;
+constexpr int QD_OFF_WORDS = QD_OFF_BARS + QD_NBARS * 8;
+constexpr int QD_OFF_ORDER = QD_OFF_WORDS + 64;
+constexpr int QD_SMEM = QD_OFF_ORDER + 1024 + 1024;  // + alignment slack
+static_assert(QD_SMEM <= kMaxDynSmem, "shared memory budget");
+constexpr uint32_t QD_TMEM_O = 256;  // S[t][b] at t*128 + b*64, O[t] at 256 + t*128
+
+template <int G, int BS>
+__global__ void __launch_bounds__(QD_THREADS, 1)
+    query_major_dual_kernel(const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_q, const QmParams P) {
+  constexpr int QT = QM_ROWS / G;  // new tokens per tile
+  constexpr int NB = QM_KC / BS;   // blocks per chunk
+  constexpr int NC = QM_KC;        // scores of a chunk per thread
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* qbuf = smem + QD_OFF_Q;  // tile t at t * QM_Q_BYTES
+  unsigned char* ring = smem + QD_OFF_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QD_OFF_BARS);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + QM_ST;
+  uint64_t* qfull = bars + 2 * QM_ST;  // both tiles' Q landed
+  uint64_t* qempty = qfull + 1;        // the previous item's scores completed
+  uint64_t* bar_s = qempty + 1;        // [t * 2 + c % 2] scores of chunk c, tile t
+  uint64_t* bar_p = bar_s + 4;         // [t * 2 + c % 2] P of chunk c, tile t, written
+  uint64_t* bar_o = bar_p + 4;         // [t * 2 + c % 2] value product of chunk c, tile t
+  uint64_t* oempty = bar_o + 4;        // [t] tile t's O read out
+  uint64_t* drain = oempty + 2;
+  int* words = reinterpret_cast<int*>(smem + QD_OFF_WORDS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&words[0]);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&words[1]);
+  int* issued = &words[2];    // K/V chunks requested
+  int* consumed = &words[3];  // K/V chunks whose two value products were issued
+  int* q_issued = &words[4];  // Q loads requested
+  int* q_waited = &words[5];  // Q loads seen landed
+  int* order = reinterpret_cast<int*>(smem + QD_OFF_ORDER);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Q = P.q_len;
+  const bool ranked = P.num_seqs <= QM_MAX_RANKED;
+  const int pairs = P.tiles / 2;
+
+  if (ranked) {  // sequences by decreasing length, as in query_major_kernel
+    int* lens_s = reinterpret_cast<int*>(ring);
+    for (int v = tid; v < P.num_seqs; v += QD_THREADS) lens_s[v] = P.context_lens[v];
+    __syncthreads();
+    for (int v = tid; v < P.num_seqs; v += QD_THREADS) {
+      const int Lv = lens_s[v];
+      int above = 0;
+      for (int u = 0; u < P.num_seqs; ++u) {
+        const int Lu = lens_s[u];
+        above += Lu > Lv || (Lu == Lv && u < v);
+      }
+      order[above] = v;
+    }
+    dev::fence_async_smem();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < QM_ST; ++s) {
+      dev::mbar_init(&full[s], 1);
+      dev::mbar_init(&empty[s], 1);
+    }
+    dev::mbar_init(qfull, 1);
+    dev::mbar_init(qempty, 1);
+    for (int k = 0; k < 4; ++k) {
+      dev::mbar_init(&bar_s[k], 1);
+      dev::mbar_init(&bar_p[k], 128);
+      dev::mbar_init(&bar_o[k], 1);
+    }
+    dev::mbar_init(&oempty[0], 128);
+    dev::mbar_init(&oempty[1], 128);
+    dev::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *issued = 0;
+    *consumed = 0;
+    *q_issued = 0;
+    *q_waited = 0;
+    dev::fence_barrier_init();
+  }
+  if (warp == 0) dev::tmem_alloc(tmem_slot, QM_TMEM_COLS);
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int grid = int(gridDim.x), k = int(blockIdx.x);
+  auto item_index = [&](int j) { return j * grid + ((j & 1) ? grid - 1 - k : k); };
+  auto item_of = [&](int j) {  // tile = the pair's first tile
+    QmItem it;
+    const int x = item_index(j);
+    const int per_seq = P.num_kv_heads * pairs;
+    const int rank = x / per_seq, rem = x % per_seq;
+    it.b = ranked ? order[rank] : rank;
+    it.hg0 = rem / pairs;
+    it.tile = rem % pairs * 2;
+    it.split = 0;
+    it.c0 = 0;
+    int L = P.context_lens[it.b];
+    it.bad_len = L > P.cap;
+    if (L > P.cap) L = P.cap;
+    if (L > 0 && L < Q) {
+      it.bad_len = true;
+      L = 0;
+    }
+    it.L = L;
+    const int i_last = min(Q, (it.tile + 2) * QT) - 1;  // the second tile's last new token
+    const int keys = L > 0 ? L - Q + i_last + 1 : 0;
+    it.keys = keys;
+    it.nblk = (keys + BS - 1) / BS;
+    it.n = (it.nblk + NB - 1) / NB;
+    return it;
+  };
+  auto has_item = [&](int j) { return item_index(j) < P.num_items; };
+  auto load_q = [&](const QmItem& it, uint64_t pol) {  // both tiles, by one thread
+    dev::mbar_arrive_expect_tx(qfull, 2 * QM_Q_BYTES);
+    for (int t = 0; t < 2; ++t)
+      for (int h2 = 0; h2 < 2; ++h2)
+        dev::tma_load_4d(qbuf + t * QM_Q_BYTES + h2 * QM_HALF_Q, &tm_q, h2 * 64, it.hg0 * G,
+                         (it.tile + t) * QT, it.b, qfull, pol);
+  };
+
+  int q_first = -1;  // producer lane 0: the item whose Q is already requested
+  if (warp == 8 && lane == 0) {
+    for (int j = 0; has_item(j); ++j) {
+      const QmItem it = item_of(j);
+      if (it.n == 0) continue;
+      load_q(it, dev::l2_evict_first_policy());
+      *q_issued = 1;
+      q_first = j;
+      break;
+    }
+  }
+  dev::griddep_wait();
+
+  if (warp == 8) {
+    // ---------------------------------------------------------- producer
+    const uint64_t pol = dev::l2_evict_first_policy();
+    if (lane == 0) {
+      dev::prefetch_tmap(&tm_k);
+      dev::prefetch_tmap(&tm_v);
+    }
+    const int u = (lane >> 2) % NB, hf = (lane >> 1) & 1, kv = lane & 1;
+    int gc = 0, qi = 0;
+    bool ok = true;
+    for (int j = 0; ok && has_item(j); ++j) {
+      const QmItem it = item_of(j);
+      if (it.n == 0) continue;
+      if (lane == 0 && j != q_first) {
+        // the single Q buffer, once the previous item's scores have completed
+        ok = dev::mbar_wait_sleep(qempty, uint32_t(qi - 1) & 1u, 64, P.wait_ns, abort_flag);
+        if (ok) {
+          load_q(it, pol);
+          *q_issued = qi + 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+      if (!ok) break;
+      const int32_t* trow = P.block_tables + size_t(it.b) * P.max_blocks_per_seq;
+      auto window = [&](int w0) {
+        const int jj = w0 + lane;
+        return (jj < P.max_blocks_per_seq && jj < it.nblk) ? trow[jj] : -1;
+      };
+      int w0 = 0;
+      int win = window(0);
+      for (int c = 0; c < it.n; ++c, ++gc) {
+        if (c * NB >= w0 + 32) {
+          w0 += 32;
+          win = window(w0);
+        }
+        const int slot = gc % QM_ST;
+        if (lane == 0) {
+          ok = dev::mbar_wait_sleep(&empty[slot], (uint32_t(gc / QM_ST) & 1u) ^ 1u, 64, P.wait_ns,
+                                    abort_flag);
+          if (ok) dev::mbar_arrive_expect_tx(&full[slot], QM_SLOT);
+        }
+        ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+        if (!ok) break;
+        const int jb = c * NB + u;
+        const int e = __shfl_sync(0xffffffffu, win, jb - w0);
+        if (lane < 4 * NB) {
+          int row = P.oob_row;
+          if (jb < it.nblk) {
+            if (e >= 0 && e < P.num_blocks) {
+              row = (e * P.num_kv_heads + it.hg0) * BS;
+            } else if (kv == 0 && hf == 0) {
+              atomicOr(&g_tc_errors, PA_DEVERR_TABLE_ENTRY);
+            }
+          }
+          unsigned char* dst =
+              ring + size_t(slot) * QM_SLOT + kv * QM_KV_BYTES + hf * QM_HALF_KV + u * BS * 128;
+          dev::tma_load_2d(dst, kv ? &tm_v : &tm_k, hf * 64, row, &full[slot], pol);
+        }
+        if (lane == 0) *issued = gc + 1;
+      }
+      ++qi;
+    }
+    if (!ok && lane == 0) {
+      atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      // One S cursor (both tiles' scores together) and one PV cursor per tile.
+      int js = 0, cs = 0, gs = 0, qs = 0;
+      int jv[2] = {0, 0}, cv[2] = {0, 0}, gv[2] = {0, 0}, qv[2] = {0, 0};
+      QmItem its{}, itv[2] = {};
+      auto seek = [&](int& j, int& c, QmItem& it) {
+        while (has_item(j)) {
+          it = item_of(j);
+          if (c < it.n) return true;
+          ++j;
+          c = 0;
+        }
+        return false;
+      };
+      bool s_more = seek(js, cs, its);
+      bool v_more[2] = {seek(jv[0], cv[0], itv[0]), seek(jv[1], cv[1], itv[1])};
+      bool ok = true;
+      uint64_t t_idle = 0;
+      uint32_t idle = 0;
+      auto pv_done = [&](int t, int c) {  // value product of chunk c, tile t, completed
+        return c < 0 || dev::mbar_test(&bar_o[t * 2 + (c & 1)], uint32_t(c >> 1) & 1u);
+      };
+      while (ok && (v_more[0] || v_more[1])) {
+        bool progress = false;
+        // scores of chunk gs for both tiles: it has landed, the item's Q is in,
+        // and each tile's value product of chunk gs - 2 (which read P from
+        // the same S buffer) has completed
+        if (s_more && gs <= min(gv[0], gv[1]) + 1 && pv_done(0, gs - 2) && pv_done(1, gs - 2) &&
+            (cs > 0 || dev::mbar_test(qfull, uint32_t(qs) & 1u)) &&
+            dev::mbar_test(&full[gs % QM_ST], uint32_t(gs / QM_ST) & 1u)) {
+          if (cs == 0) *q_waited = qs + 1;
+          const uint32_t kb = dev::smem_addr(ring + size_t(gs % QM_ST) * QM_SLOT);
+          dev::tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t qb = dev::smem_addr(qbuf + t * QM_Q_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < QM_D / 16; ++kk) {
+              const uint32_t h2 = kk >> 2, off = uint32_t(kk & 3) * 32;
+              dev::mma_bf16(tmem + uint32_t(t * 128 + (gs & 1) * QM_KC),
+                            dev::smem_desc(qb + h2 * QM_HALF_Q + off, 16, 1024, dev::kSwizzle128B),
+                            dev::smem_desc(kb + h2 * QM_HALF_KV + off, 16, 1024,
+                                           dev::kSwizzle128B),
+                            QM_IDESC_S, kk > 0);
+            }
+            dev::mma_commit(&bar_s[t * 2 + (gs & 1)]);
+          }
+          ++gs;
+          if (++cs == its.n) {  // the item's last scores: the Q buffer frees when they complete
+            dev::mma_commit(qempty);
+            ++qs;
+            ++js;
+            cs = 0;
+            s_more = seek(js, cs, its);
+          }
+          progress = true;
+        }
+        // the value product of chunk gv[t] of tile t once its P is written
+        // (and, on an item's first chunk, once tile t's O has been read out);
+        // a ring slot frees when both tiles' value products of its chunk are in
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int g = gv[t];
+          if (v_more[t] && g < gs &&
+              dev::mbar_test(&bar_p[t * 2 + (g & 1)], uint32_t(g >> 1) & 1u) &&
+              (cv[t] > 0 || qv[t] == 0 ||
+               dev::mbar_test(&oempty[t], uint32_t(qv[t] - 1) & 1u))) {
+            dev::tc_fence_after();
+            const uint32_t vb = dev::smem_addr(ring + size_t(g % QM_ST) * QM_SLOT + QM_KV_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < QM_KC / 16; ++kk)
+              mma_bf16_tmem_a(tmem + QD_TMEM_O + uint32_t(t * QM_D),
+                              tmem + uint32_t(t * 128 + (g & 1) * QM_KC + kk * 8),
+                              dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
+                              QM_IDESC_PV, cv[t] > 0 || kk > 0);
+            dev::mma_commit(&bar_o[t * 2 + (g & 1)]);
+            ++gv[t];
+            if (gv[1 - t] > g) {  // the other tile's value product of chunk g is in too
+              dev::mma_commit(&empty[g % QM_ST]);
+              *consumed = g + 1;
+            }
+            if (++cv[t] == itv[t].n) {
+              ++qv[t];
+              ++jv[t];
+              cv[t] = 0;
+              v_more[t] = seek(jv[t], cv[t], itv[t]);
+            }
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle = 0;
+          continue;
+        }
+        if ((++idle & 255u) != 0u) continue;
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint64_t now = dev::global_timer_ns();
+        if (idle == 256u) {
+          t_idle = now;
+        } else if (now - t_idle > P.wait_ns) {
+          ok = false;
+        }
+      }
+      if (!ok) {
+        atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      dev::mma_commit(drain);
+      (void)dev::mbar_wait(drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------- softmax
+    const int t = warp >> 2;                // tile of the item
+    const int r = (warp & 3) * 32 + lane;   // TMEM lane = row of the tile
+    const uint32_t t_lane = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t s_col = uint32_t(t * 128), o_col = QD_TMEM_O + uint32_t(t * QM_D);
+    const float sl2 = P.scale_log2;
+    int pv_done = -1, gc = 0;
+    bool ok = true;
+    auto wait_pv = [&](int kc) {  // value product of chunk kc, tile t
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_o[t * 2 + (kc & 1)], uint32_t(kc >> 1) & 1u,
+                                                  P.wait_ns, abort_flag)) &&
+           ok;
+      pv_done = kc;
+    };
+    for (int j = 0; ok && has_item(j); ++j) {
+      const QmItem it = item_of(j);
+      const int i = (it.tile + t) * QT + r / G;
+      const bool valid = i < Q;
+      __nv_bfloat16* orow =
+          P.out + ((size_t(it.b) * Q + (valid ? i : 0)) * P.num_q_heads + it.hg0 * G + r % G) * QM_D;
+      if (r == 0 && t == 0 && it.bad_len && it.tile == 0 && it.hg0 == 0)
+        atomicOr(&g_tc_errors, PA_DEVERR_CONTEXT_LEN);
+      if (it.n == 0) {  // an empty sequence: zero rows
+        if (valid)
+#pragma unroll
+          for (int cg = 0; cg < QM_D; cg += 8)
+            *reinterpret_cast<uint4*>(orow + cg) = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      const int L = it.L;
+      const int L_row = valid ? L - Q + i + 1 : 0;
+      float m_ref = -INFINITY, l = 0.0f;
+      for (int c = 0; c < it.n; ++c) {
+        const int g = gc + c;
+        ok = __all_sync(0xffffffffu, dev::mbar_wait(&bar_s[t * 2 + (g & 1)], uint32_t(g >> 1) & 1u,
+                                                    P.wait_ns, abort_flag));
+        if (!ok) break;
+        dev::tc_fence_after();
+        float s[NC];
+        dev::tmem_ld_cols<NC>(tmem + t_lane + s_col + uint32_t((g & 1) * QM_KC), s);
+        const int key0 = c * QM_KC;  // key of s[0]
+        if (!__all_sync(0xffffffffu, key0 + NC <= L_row)) {
+#pragma unroll
+          for (int kx = 0; kx < NC; ++kx) s[kx] = key0 + kx < L_row ? s[kx] : -INFINITY;
+        }
+        float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int kx = 4; kx < NC; ++kx) mx[kx & 3] = fmaxf(mx[kx & 3], s[kx]);
+        const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const bool need = cm > m_ref + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float nr = need ? cm : m_ref;
+          const float f = nr == m_ref || m_ref == -INFINITY ? 1.0f : dev::fast_exp2(m_ref - nr);
+          if (c > 0) {
+            if (pv_done < g - 1) wait_pv(g - 1);
+            if (!ok) break;
+            dev::tc_fence_after();
+#pragma unroll
+            for (int cg = 0; cg < QM_D; cg += 32) {
+              float o[32];
+              dev::tmem_ld_cols<32>(tmem + t_lane + o_col + cg, o);
+#pragma unroll
+              for (int kx = 0; kx < 32; ++kx) o[kx] *= f;
+              dev::tmem_st_cols<32>(tmem + t_lane + o_col + cg, o);
+            }
+          }
+          l *= f;
+          m_ref = nr;
+        }
+        const float nm = m_ref == -INFINITY ? 0.0f : -m_ref;
+        float pp[NC / 2];
+        float la = 0.0f, lb = 0.0f;
+#pragma unroll
+        for (int kx = 0; kx < NC; kx += 2) {
+          const float p0 = dev::fast_exp2(fmaf(s[kx], sl2, nm));
+          const float p1 = dev::fast_exp2(fmaf(s[kx + 1], sl2, nm));
+          la += p0;
+          lb += p1;
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+          pp[kx / 2] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&v2));
+        }
+        l += la + lb;
+        if ((c + 1) * QM_KC > it.keys) {
+          // no row of the item sees the keys from it.keys on (past the
+          // sequence they may hold NaN): clear their V rows, both tiles'
+          // threads alike, before either value product reads them
+          const int x = r % QM_KC, h2 = r / QM_KC;
+          if (c * QM_KC + x >= it.keys) {
+            uint4* vrow = reinterpret_cast<uint4*>(ring + size_t(g % QM_ST) * QM_SLOT +
+                                                   QM_KV_BYTES + h2 * QM_HALF_KV + x * 128);
+#pragma unroll
+            for (int kx = 0; kx < 8; ++kx) vrow[kx] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          dev::fence_async_smem();
+        }
+        // P over the first 32 columns of S[t][g % 2] (the scores are in
+        // registers); the value product of chunk g - 2, which read this
+        // buffer's last P, completed before S(g) was issued
+        dev::tmem_st_cols<NC / 2>(tmem + t_lane + s_col + uint32_t((g & 1) * QM_KC), pp);
+        dev::tc_fence_before();
+        dev::mbar_arrive(&bar_p[t * 2 + (g & 1)]);
+      }
+      if (!ok) break;
+      gc += it.n;
+      wait_pv(gc - 1);
+      if (!ok) break;
+      dev::tc_fence_after();
+      const float inv = l > 0.0f ? __frcp_rn(l) : 0.0f;
+#pragma unroll
+      for (int cg = 0; cg < QM_D; cg += 32) {
+        float o[32];
+        dev::tmem_ld_cols<32>(tmem + t_lane + o_col + cg, o);
+        if (valid) {
+#pragma unroll
+          for (int kx = 0; kx < 32; kx += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+              const __nv_bfloat162 v2 =
+                  __floats2bfloat162_rn(o[kx + 2 * q2] * inv, o[kx + 2 * q2 + 1] * inv);
+              w[q2] = *reinterpret_cast<const uint32_t*>(&v2);
+            }
+            *reinterpret_cast<uint4*>(orow + cg + kx) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      // tile t's O may take the next item
+      dev::tc_fence_before();
+      dev::mbar_arrive(&oempty[t]);
+    }
+    if (!ok && lane == 0) {
+      atomicOr(&g_tc_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    for (int c = *consumed; c < *issued; ++c)
+      (void)dev::mbar_wait(&full[c % QM_ST], uint32_t(c / QM_ST) & 1u);
+    for (int c = *q_waited; c < *q_issued; ++c) (void)dev::mbar_wait(qfull, uint32_t(c) & 1u);
+  }
+  dev::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    dev::tc_fence_after();
+    dev::tmem_dealloc(tmem, QM_TMEM_COLS);
+  }
+}
+
 // One warp per output row: the splits' partials weighted by 2^(m_s - M)
 // (M the largest reference; a split that saw no key has m = -inf), the sum
 // divided by the weighted sums.
@@ -742,13 +1226,74 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
 }
 
 template <int G, int BS>
+int launch_qd_t(const pa_decode_params* p, cudaStream_t stream, bool dependent) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(query_major_dual_kernel<G, BS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, QD_SMEM);
+    if (e != cudaSuccess) return int(e);
+    configured = true;
+  }
+  const int H = p->num_kv_heads, Q = query_len_of(p);
+  const uint64_t cache_rows = uint64_t(p->num_blocks) * H * BS;
+  CUtensorMap tk, tv, tq;
+  int r = make_map(&tk, p->k_cache, cache_rows, QM_D, uint32_t(BS));
+  if (!r) r = make_map(&tv, p->v_cache, cache_rows, QM_D, uint32_t(BS));
+  if (!r) {
+    const cuuint64_t dims[4] = {uint64_t(QM_D), uint64_t(p->num_q_heads), uint64_t(Q),
+                                uint64_t(p->num_seqs)};
+    const cuuint64_t strides[3] = {uint64_t(QM_D) * 2, uint64_t(p->num_q_heads) * QM_D * 2,
+                                   uint64_t(Q) * p->num_q_heads * QM_D * 2};
+    const cuuint32_t box[4] = {64, uint32_t(G), uint32_t(QM_ROWS / G), 1};
+    r = make_map_nd(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p->q, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (r) return r;
+  QmParams P;
+  P.block_tables = p->block_tables;
+  P.context_lens = p->context_lens;
+  P.out = static_cast<__nv_bfloat16*>(p->out);
+  P.num_seqs = p->num_seqs;
+  P.num_kv_heads = H;
+  P.num_q_heads = p->num_q_heads;
+  P.q_len = Q;
+  P.tiles = query_major_tiles(p);
+  P.head_groups = H;
+  P.splits = 1;
+  P.part_ml = nullptr;
+  P.part_o = nullptr;
+  P.num_items = p->num_seqs * H * (P.tiles / 2);
+  P.max_blocks_per_seq = p->max_blocks_per_seq;
+  P.num_blocks = p->num_blocks;
+  P.cap = std::min(p->max_blocks_per_seq * BS, p->max_context_len);
+  P.oob_row = int(cache_rows);
+  P.scale_log2 = p->scale * kLog2e;
+  P.wait_ns = p->wait_timeout_us > 0 ? uint64_t(p->wait_timeout_us) * 1000u : dev::kWaitNsLimit;
+  const int sms = tc_grid();
+  if (sms <= 0) return int(cudaErrorInvalidDevice);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(std::min(P.num_items, sms)));
+  cfg.blockDim = dim3(QD_THREADS);
+  cfg.dynamicSmemBytes = QD_SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return int(cudaLaunchKernelEx(&cfg, query_major_dual_kernel<G, BS>, tk, tv, tq, P));
+}
+
+template <int G, int BS>
 int launch_qm_b(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o, bool a) {
   const bool split = query_major_splits(p) > 1;
   if (query_major_heads(p) == 2)
     return split ? launch_qm_t<G, 2, true, BS>(p, stream, ml, o, a)
                  : launch_qm_t<G, 2, false, BS>(p, stream, ml, o, a);
-  return split ? launch_qm_t<G, 1, true, BS>(p, stream, ml, o, a)
-               : launch_qm_t<G, 1, false, BS>(p, stream, ml, o, a);
+  if (split) return launch_qm_t<G, 1, true, BS>(p, stream, ml, o, a);
+  // one head per item: an even number of tiles per head goes two tiles at a time
+  if (query_major_tiles(p) % 2 == 0) return launch_qd_t<G, BS>(p, stream, a);
+  return launch_qm_t<G, 1, false, BS>(p, stream, ml, o, a);
 }
 template <int G>
 int launch_qm_g(const pa_decode_params* p, cudaStream_t stream, float* ml, float* o, bool a) {

@@ -143,6 +143,7 @@ def test_multi_token(pk, bs, G, Hkv, QL):
     (8, 8, 8, [4100, 2900]),               # keys split over CTAs
     (2, 3, 16, [1500, 16, 2600]),          # odd KV head count
     (4, 8, 16, [900, 31, 32, 33] * 16),    # 256 items, no split
+    (4, 8, 64, [700, 64, 65, 1023] * 8),   # two tiles per item, sharing each load
 ])
 def test_query_major_block_size_32(pk, G, Hkv, QL, lens):
     """The query-major kernel at block size 32: boxes of HB heads x 32 keys,

@@ -219,6 +219,35 @@ def test_query_major_split_keys(pk, G, Hkv, QL, lens):
     _check(pk, q, kc, vc, tables, lens, torch)
 
 
+@pytest.mark.parametrize("G,Hkv,QL,B", [(4, 8, 64, 16), (8, 4, 32, 40), (1, 8, 256, 16),
+                                        (4, 3, 64, 48), (2, 8, 128, 40)])
+def test_query_major_two_tiles_per_item(pk, G, Hkv, QL, B):
+    """One KV head per item with an even number of 128-row tiles per head:
+    items of two tiles sharing each load of the keys (eight softmax warps),
+    several items per CTA."""
+    q, kc, vc, tables, lens, torch = _case(_qm_lens(QL, B), QL, G * Hkv, Hkv, 128,
+                                           seed=770 + G + QL)
+    _check(pk, q, kc, vc, tables, lens, torch)
+
+
+def test_query_major_two_tiles_short_and_empty_sequences(pk):
+    QL = 64
+    lens = _qm_lens(QL, 32)
+    lens[3], lens[5], lens[7] = 0, 40, 0  # empty, and too short for the new tokens
+    q, kc, vc, tables, lens, torch = _case(lens, QL, 32, 8, 128, seed=790)
+    out = torch.full_like(q, 7.0)
+    pk.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                 max_context_len=int(lens.max()), out=out)
+    torch.cuda.synchronize()
+    assert pk.pa_device_errors() & DEVERR_CONTEXT_LEN
+    got = harness.bf16_tensor_to_f64(out)
+    for b in (3, 5, 7):
+        assert not got[b].any()
+    keep = [b for b in range(len(lens)) if b not in (3, 5, 7)]
+    want = oracle.paged_decode_multi(q.cpu()[keep], kc.cpu(), vc.cpu(), tables[keep], lens[keep])
+    harness.assert_close(got[keep], want)
+
+
 @pytest.mark.parametrize("seed", range(24))
 def test_query_major_random_shapes(pk, seed):
     """Seeded random shapes across the query-major space: G, the KV head
