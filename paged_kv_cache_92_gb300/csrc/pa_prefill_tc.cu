@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
       bool ok = true;
       uint64_t t_idle = 0;
       uint32_t idle = 0;
+      const uint32_t idle_mask = P.wait_ns < dev::kShortWaitNs ? 0u : 255u;
       while (ok && v_more) {
         bool progress = false;
         // the scores of chunk gs: it has landed, its Q is in, and the softmax
@@ -401,14 +402,15 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           idle = 0;
           continue;
         }
-        // bounded idle: the wall clock is read every 256 polls
-        if ((++idle & 255u) != 0u) continue;
+        // bounded idle: the wall clock is read every 256 polls (every poll
+        // under a budget short enough to run out in a test)
+        if ((++idle & idle_mask) != 0u) continue;
         if (*abort_flag) {
           ok = false;
           break;
         }
         const uint64_t now = dev::global_timer_ns();
-        if (idle == 256u) {
+        if (idle == idle_mask + 1u) {
           t_idle = now;
         } else if (now - t_idle > P.wait_ns) {
           ok = false;
@@ -876,6 +878,7 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
       bool ok = true;
       uint64_t t_idle = 0;
       uint32_t idle = 0;
+      const uint32_t idle_mask = P.wait_ns < dev::kShortWaitNs ? 0u : 255u;
       auto pv_done = [&](int t, int c) {  // value product of chunk c, tile t, completed
         return c < 0 || dev::mbar_test(&bar_o[t * 2 + (c & 1)], uint32_t(c >> 1) & 1u);
       };
@@ -951,13 +954,13 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
           idle = 0;
           continue;
         }
-        if ((++idle & 255u) != 0u) continue;
+        if ((++idle & idle_mask) != 0u) continue;
         if (*abort_flag) {
           ok = false;
           break;
         }
         const uint64_t now = dev::global_timer_ns();
-        if (idle == 256u) {
+        if (idle == idle_mask + 1u) {
           t_idle = now;
         } else if (now - t_idle > P.wait_ns) {
           ok = false;

@@ -307,14 +307,16 @@ def test_bad_device_values_set_error_bits_without_faulting(pk, variant):
     assert pk.pa_device_errors() == 0
 
 
-@pytest.mark.parametrize("query_len", [1, 4])
+@pytest.mark.parametrize("query_len", [1, 3, 8])
 def test_wait_budget_exit_reports_timeout_and_leaves_the_context_usable(pk, query_len):
-    """The tensor-core kernel's bounded waits, made to run out: with a budget
+    """The tensor-core kernels' bounded waits, made to run out: with a budget
     of 1 us per barrier wait (far below a chunk's turnaround) a well-formed
     launch gives up in every CTA that holds more chunks than its ring. The
     launch must end, report PA_DEVERR_TIMEOUT, and leave the context usable:
     the next launch with the default budget, on the same buffers, matches the
-    oracle (every copy in flight had landed and the tensor memory was freed)."""
+    oracle (every copy in flight had landed and the tensor memory was freed).
+    One new token and three (12 query rows per KV head) run on the decode
+    kernel, eight on the query-major kernel."""
     import torch
 
     rng = np.random.default_rng(31)
