@@ -219,6 +219,86 @@ def test_decode_workspace_size(pk):
                                                                              QL=ql, variant=1)
 
 
+def _query_major_plan(B, Hq, Hkv, QL, mx, bs=16, variant=0, kv_dtype=0, D=128):
+    """Whether the many-token kernel takes a shape, and its key splits.
+
+    Restated from the kernel's launch rules: a KV head has QL x G query rows,
+    tiled by 128; a work item holds two KV heads when their rows fit 64 and
+    the head count is even, else one. The kernel takes bf16 head_dim 128 at
+    block size 16 or 32, G in {1, 2, 4, 8}, several new tokens, and either
+    more tokens than one column group of the column-layout decode holds
+    (16 columns per KV head, at most 128 over all KV heads, G per token) or
+    at least 16 rows per KV head with 128 (sequence, KV head, tile) units.
+    Small batches split each item's keys to reach 256 items, every split
+    at least 4 chunks of 64 / heads-per-item keys, at most 16 splits."""
+    G = Hq // Hkv
+    rows = QL * G
+    tiles = -(-rows // 128)
+    per_head = min(16, 128 // Hkv)
+    group_tokens = per_head // G if per_head >= G else 0
+    groups = -(-QL // group_tokens) if group_tokens else 0
+    takes = (variant == 0 and kv_dtype == 0 and D == 128 and bs in (16, 32) and QL > 1
+             and G in (1, 2, 4, 8)
+             and (groups > 1 or (rows >= 16 and B * Hkv * tiles >= 128)))
+    if not takes:
+        return False, 0
+    pair = 2 if rows <= 64 and Hkv % 2 == 0 else 1
+    items = B * (Hkv // pair) * tiles
+    if items >= 256:
+        return True, 1
+    chunk = 64 // pair
+    splits = min(-(-256 // items), -(-mx // chunk) // 4, 16)
+    return True, max(splits, 1)
+
+
+def test_query_major_routing_and_key_splits_over_a_spread_of_shapes(pk):
+    """The workspace the library asks for follows the many-token kernel's
+    routing and split rules: the header alone when its keys are unsplit, the
+    (m, l) pairs and the O rows of every (row, split) when they are split,
+    and the column-layout decode's workspace when the kernel does not take
+    the shape. Checked over batch sizes, head layouts (odd KV head counts
+    among them), new-token counts, block sizes and context lengths."""
+    lib = pk.load()
+    seen = {"unsplit": 0, "split": 0, "column": 0, "max_splits": 0}
+    heads = ((8, 2), (32, 8), (64, 8), (16, 8), (8, 8), (24, 3), (6, 6), (8, 1))
+    for B in (1, 2, 3, 8, 17, 64):
+        for Hq, Hkv in heads:
+            for QL in (2, 3, 4, 5, 8, 16, 33, 64, 128):
+                for bs in (16, 32):
+                    for mx in (40, 300, 2048, 32769):
+                        nb = -(-mx // bs)
+                        p = _params(pk, num_seqs=B, num_q_heads=Hq, num_kv_heads=Hkv,
+                                    query_len=QL, block_size=bs, max_context_len=mx,
+                                    max_blocks_per_seq=nb, num_blocks=B * nb)
+                        got = lib.pa_decode_workspace_size(ctypes.byref(p))
+                        qm, ns = _query_major_plan(B, Hq, Hkv, QL, mx, bs)
+                        if qm:
+                            want = 256
+                            if ns > 1:
+                                rows = B * QL * Hq * ns
+                                want += _ru(rows * 2 * 4) + _ru(rows * 128 * 4)
+                            seen["split" if ns > 1 else "unsplit"] += 1
+                            seen["max_splits"] = max(seen["max_splits"], ns)
+                            assert got == want, (B, Hq, Hkv, QL, bs, mx, ns)
+                        elif bs == 16 and Hkv in (2, 8) and Hq // Hkv in (2, 4, 8):
+                            # the column-layout tensor-core decode
+                            want = _expected_ws(B, Hq, 128, 1, 256, Hkv=Hkv, QL=QL)
+                            seen["column"] += 1
+                            assert got == want, (B, Hq, Hkv, QL, bs, mx)
+                        else:
+                            assert got > 0
+    # every branch of the rules is reached, splits up to the cap of 16
+    assert min(seen["unsplit"], seen["split"], seen["column"]) > 20
+    assert seen["max_splits"] == 16
+    # the CUDA-core variant and the 8-bit cache never take the many-token kernel
+    for kw in (dict(variant=1), dict(kv_dtype=1)):
+        p = _params(pk, num_seqs=8, num_q_heads=32, num_kv_heads=8, query_len=64,
+                    max_context_len=2048, max_blocks_per_seq=128, **kw)
+        qm, _ = _query_major_plan(8, 32, 8, 64, 2048, **kw)
+        assert not qm
+        assert lib.pa_decode_workspace_size(ctypes.byref(p)) > 256
+
+
 def test_cache_ops_reject_bad_arguments_on_the_host(pk):
     lib = pk.load()
     assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 128, 64, 10, None) == 2
