@@ -60,7 +60,8 @@ constexpr int QM_OFF_BARS = QM_OFF_RING + QM_ST * QM_SLOT;
 constexpr int QM_NBARS = 2 * QM_ST + 13;
 constexpr int QM_OFF_WORDS = QM_OFF_BARS + QM_NBARS * 8;
 constexpr int QM_OFF_ORDER = QM_OFF_WORDS + 64;      // sequence of each length rank (<= 256)
-constexpr int QM_SMEM = QM_OFF_ORDER + 1024 + 1024;  // + alignment slack
+constexpr int QM_OFF_PLAN = QM_OFF_ORDER + 1024;     // first item of each (rank, tile) (< 256)
+constexpr int QM_SMEM = QM_OFF_PLAN + 512 + 1024;    // + alignment slack
 static_assert(QM_SMEM <= kMaxDynSmem, "shared memory budget");
 constexpr int QM_MAX_RANKED = 256;
 // TMEM: S[2] at [0, 128), O[2] at [128, 384), P[2] at [384, 448)
@@ -97,6 +98,7 @@ struct QmParams {
 struct QmItem {
   int b, hg0, tile;  // sequence, first KV head, tile of new tokens
   int split, c0;     // split of the keys, its first chunk
+  int ns;            // splits of this (sequence, head group, tile)
   int L;             // length after the rules (0: an empty sequence)
   int keys;          // keys the item's last row sees
   int nblk, n;       // blocks of those keys, chunks of this split
@@ -160,6 +162,136 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     }
     dev::fence_async_smem();  // the staged lengths before the ring's first copy
   }
+
+  // The keys an item of sequence length L and tile `tile` covers: the length
+  // rules (at most the tables' capacity; a sequence shorter than its new
+  // tokens is empty) and the keys its tile's last new token sees. Returns
+  // the chunks of all its splits.
+  auto span_of = [&](int L, int tile, QmItem& it) {
+    it.bad_len = L > P.cap;
+    if (L > P.cap) L = P.cap;
+    if (L > 0 && L < Q) {  // no room for the new tokens: an empty sequence
+      it.bad_len = true;
+      L = 0;
+    }
+    it.L = L;
+    const int i_last = min(Q, (tile + 1) * QT) - 1;  // the item's last new token
+    const int keys = L > 0 ? L - Q + i_last + 1 : 0;  // what its last row sees
+    it.keys = keys;
+    it.nblk = (keys + BS - 1) / BS;
+    return (it.nblk + NB - 1) / NB;
+  };
+
+  // Split keys (fewer than 256 (sequence, head group, tile) units; the
+  // workspace holds P.splits partials per row). Two plans within that bound:
+  // every unit split P.splits ways and dealt in the snake, or one wave: each
+  // (sequence, tile) cut into pieces of at most T chunks, T the smallest that
+  // leaves every CTA at most one item. Every CTA computes both from the
+  // lengths and takes the one whose busiest CTA has fewer chunks (an item
+  // counted kItemChunks more for its start and its partials).
+  int* plan_wave = &words[6];   // the one-wave plan is in use
+  int* plan_t = &words[7];      // its T
+  int* plan_items = &words[8];  // items of the plan in use
+  uint16_t* plan_off = reinterpret_cast<uint16_t*>(smem + QM_OFF_PLAN);
+  auto wave_splits = [&](int n, int T) { return n > 0 ? min(P.splits, (n + T - 1) / T) : 1; };
+  if (SPLIT && tid == 0) {  // the uniform plan unless the comparison below picks the other
+    *plan_wave = 0;
+    *plan_items = P.num_items;
+  }
+  if (SPLIT && ranked) {  // (fewer than 256 units: at most 255 sequences, all ranked)
+    constexpr int kItemChunks = 2;
+    int* scratch = reinterpret_cast<int*>(ring);  // the staged lengths at [0, 256)
+    int* n_rt = scratch + 256;                     // chunks of each (rank, tile)
+    int* per_cta = scratch + 512;                  // the uniform plan's chunks per CTA
+    const int tiles = P.tiles, RT = P.num_seqs * tiles, cap = P.splits, hgc = P.head_groups;
+    const int grid = int(gridDim.x);
+    auto warp_max = [](int v) {
+      for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+      return v;
+    };
+    __syncthreads();  // order[] complete
+    for (int rt = tid; rt < RT; rt += QM_THREADS) {
+      QmItem tmp;
+      n_rt[rt] = span_of(scratch[order[rt / tiles]], rt % tiles, tmp);
+    }
+    for (int c = tid; c < grid; c += QM_THREADS) per_cta[c] = 0;
+    __syncthreads();
+    // uniform: item x is (rank, head group, tile, split), split fastest
+    const int per_seq = hgc * tiles * cap;
+    for (int x = tid; x < P.num_items; x += QM_THREADS) {
+      const int rem = x % per_seq, sp = rem % cap;
+      const int n = n_rt[x / per_seq * tiles + rem / cap % tiles];
+      const int sz = (sp + 1) * n / cap - sp * n / cap;
+      const int pass = x / grid, pos = x % grid;
+      if (sz > 0) atomicAdd(&per_cta[(pass & 1) ? grid - 1 - pos : pos], sz + kItemChunks);
+    }
+    __syncthreads();
+    if (warp == 0) {  // the uniform plan's busiest CTA
+      int mx = 0;
+      for (int c = lane; c < grid; c += 32) mx = max(mx, per_cta[c]);
+      mx = warp_max(mx);
+      if (lane == 0) words[9] = mx;
+    } else if (warp == 1) {  // one wave: T by bisection (the item count falls as T grows)
+      auto count = [&](int T) {
+        int c = 0;
+        for (int rt = lane; rt < RT; rt += 32) c += hgc * wave_splits(n_rt[rt], T);
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        return c;
+      };
+      int nmax = 0;
+      for (int rt = lane; rt < RT; rt += 32) nmax = max(nmax, n_rt[rt]);
+      nmax = warp_max(nmax);
+      int cost = 0x7fffffff, T = 1;
+      if (nmax > 0 && count(nmax) <= grid) {
+        int lo = 1, hi = nmax;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (count(mid) <= grid) {
+            hi = mid;
+          } else {
+            lo = mid + 1;
+          }
+        }
+        T = lo;
+        int big = 0;  // the largest piece
+        for (int rt = lane; rt < RT; rt += 32) {
+          const int n = n_rt[rt], ns = wave_splits(n, T);
+          big = max(big, (n + ns - 1) / ns);
+        }
+        cost = warp_max(big) + kItemChunks;
+      }
+      if (lane == 0) {
+        words[10] = cost;
+        *plan_t = T;
+      }
+    }
+    __syncthreads();
+    const bool wave = words[10] < words[9];
+    if (warp == 0 && wave) {  // the first item of each (rank, tile), in rank order
+      const int T = *plan_t, per = (RT + 31) / 32, r0 = lane * per;
+      int local = 0;
+      for (int i = 0; i < per; ++i)
+        if (r0 + i < RT) local += hgc * wave_splits(n_rt[r0 + i], T);
+      int incl = local;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int base = incl - local;
+      for (int i = 0; i < per; ++i) {
+        if (r0 + i < RT) {
+          plan_off[r0 + i] = uint16_t(base);
+          base += hgc * wave_splits(n_rt[r0 + i], T);
+        }
+      }
+      if (lane == 31) *plan_items = incl;
+    }
+    if (tid == 0) {
+      *plan_wave = wave ? 1 : 0;
+      if (!wave) *plan_items = P.num_items;
+    }
+    dev::fence_async_smem();  // the scratch before the ring's first copy
+  }
   if (tid == 0) {
     for (int s = 0; s < QM_ST; ++s) {
       dev::mbar_init(&full[s], 1);
@@ -194,31 +326,44 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
   auto item_of = [&](int j) {
     QmItem it;
     const int x = item_index(j);
-    const int splits = SPLIT ? P.splits : 1;
-    const int per_seq = P.head_groups * P.tiles * splits;
-    const int rank = x / per_seq, rem = x % per_seq;
-    it.b = ranked ? order[rank] : rank;
-    it.hg0 = rem / (P.tiles * splits) * HB;
-    it.tile = rem / splits % P.tiles;
-    it.split = SPLIT ? rem % splits : 0;
-    int L = P.context_lens[it.b];
-    it.bad_len = L > P.cap;
-    if (L > P.cap) L = P.cap;
-    if (L > 0 && L < Q) {  // no room for the new tokens: an empty sequence
-      it.bad_len = true;
-      L = 0;
+    const bool wave = SPLIT && *plan_wave != 0;
+    int hg = 0, sp = 0, ns = SPLIT ? P.splits : 1, rem = 0;
+    if (wave) {  // (rank, tile), then head group, then split
+      int lo = 0, hi = P.num_seqs * P.tiles - 1;  // the last (rank, tile) starting at or before x
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (int(plan_off[mid]) <= x) {
+          lo = mid;
+        } else {
+          hi = mid - 1;
+        }
+      }
+      it.b = order[lo / P.tiles];
+      it.tile = lo % P.tiles;
+      rem = x - int(plan_off[lo]);
+    } else {  // rank, then head group, then tile, then split
+      const int per_seq = P.head_groups * P.tiles * ns;
+      const int rank = x / per_seq;
+      rem = x % per_seq;
+      it.b = ranked ? order[rank] : rank;
+      hg = rem / (P.tiles * ns);
+      it.tile = rem / ns % P.tiles;
+      sp = rem % ns;
     }
-    it.L = L;
-    const int i_last = min(Q, (it.tile + 1) * QT) - 1;  // the item's last new token
-    const int keys = L > 0 ? L - Q + i_last + 1 : 0;     // what its last row sees
-    it.keys = keys;
-    it.nblk = (keys + BS - 1) / BS;
-    const int n_all = (it.nblk + NB - 1) / NB;  // chunks of all the splits
-    it.c0 = SPLIT ? it.split * n_all / splits : 0;
-    it.n = SPLIT ? (it.split + 1) * n_all / splits - it.c0 : n_all;
+    const int n_all = span_of(P.context_lens[it.b], it.tile, it);  // chunks of all the splits
+    if (wave) {
+      ns = wave_splits(n_all, *plan_t);
+      hg = rem / ns;
+      sp = rem % ns;
+    }
+    it.hg0 = hg * HB;
+    it.split = sp;
+    it.ns = ns;
+    it.c0 = SPLIT ? sp * n_all / ns : 0;
+    it.n = SPLIT ? (sp + 1) * n_all / ns - it.c0 : n_all;
     return it;
   };
-  auto has_item = [&](int j) { return item_index(j) < P.num_items; };
+  auto has_item = [&](int j) { return item_index(j) < (SPLIT ? *plan_items : P.num_items); };
 
   // Launched as a programmatic dependent (after the step's KV write, which
   // changes neither the tables, the lengths nor q): nothing above touched the
@@ -453,6 +598,11 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
           SPLIT ? ((size_t(it.b) * Q + (valid ? i : 0)) * P.num_q_heads + (it.hg0 + h) * G +
                    r0 % G) * P.splits + it.split
                 : 0;
+      // a plan with fewer splits than the workspace holds: the last split
+      // marks the row's remaining partials empty (the merge skips m = -inf)
+      if (SPLIT && valid && it.split == it.ns - 1)
+        for (int s2 = it.ns; s2 < P.splits; ++s2)
+          P.part_ml[(prow - it.split + s2) * 2] = -INFINITY;
       if (it.n == 0) {  // no keys in this split (or an empty sequence)
         if (valid) {
           if (!SPLIT) {  // zero rows
@@ -1214,7 +1364,8 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(std::min(P.num_items, sms)));
+  // split launches take every SM: the one-wave plan may cut more items
+  cfg.gridDim = dim3(unsigned(SPLIT ? sms : std::min(P.num_items, sms)));
   cfg.blockDim = dim3(QM_THREADS);
   cfg.dynamicSmemBytes = QM_SMEM;
   cfg.stream = stream;

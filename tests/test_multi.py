@@ -248,6 +248,101 @@ def test_query_major_two_tiles_short_and_empty_sequences(pk):
     harness.assert_close(got[keep], want)
 
 
+def _split_plan(lens, QL, G, Hkv, grid, BS=16):
+    """Which key-split plan the query-major kernel takes, restated from its
+    scheduling rule (test-side, so that a case can state what it exercises).
+
+    With fewer than 256 (sequence, head group, tile) units and a split bound
+    `cap` > 1 (the workspace's partials per row), the uniform plan splits
+    every unit `cap` ways and deals the items in a snake over `grid` CTAs;
+    the one-wave plan cuts each (sequence, tile) into ceil(n / T) <= cap
+    pieces, T the smallest piece length (in 64-column chunks) that leaves
+    every CTA at most one item. The kernel takes the one-wave plan when its
+    largest piece, plus 2 chunks per item, is below the uniform plan's
+    busiest CTA (each item also counted 2 chunks more)."""
+    lens = [int(x) for x in lens]
+    B, mx = len(lens), max(lens)
+    rows = QL * G
+    tiles = -(-rows // 128)
+    hb = 2 if rows <= 64 and Hkv % 2 == 0 else 1
+    NB, QT, hgc = 64 // (BS * hb), (128 // hb) // G, Hkv // hb
+    units = B * hgc * tiles
+    if units >= 256:
+        return "unsplit"
+    cap = max(1, min(-(-256 // units), -(-mx // (64 // hb)) // 4, 16))
+    if cap == 1:
+        return "unsplit"
+    n_rt = []  # chunks of each (sequence by decreasing length, tile)
+    for b in sorted(range(B), key=lambda v: (-lens[v], v)):
+        for t in range(tiles):
+            L = 0 if 0 < lens[b] < QL else lens[b]
+            keys = L - QL + min(QL, (t + 1) * QT) if L > 0 else 0
+            n_rt.append(-(-(-(-keys // BS)) // NB))
+    load = [0] * grid
+    per_seq = hgc * tiles * cap
+    for x in range(B * per_seq):
+        rem = x % per_seq
+        sp, n = rem % cap, n_rt[x // per_seq * tiles + rem // cap % tiles]
+        size = (sp + 1) * n // cap - sp * n // cap
+        p, pos = divmod(x, grid)
+        if size:
+            load[grid - 1 - pos if p & 1 else pos] += size + 2
+    pieces = lambda n, T: min(cap, -(-n // T)) if n > 0 else 1
+    count = lambda T: sum(hgc * pieces(n, T) for n in n_rt)
+    if max(n_rt) == 0 or count(max(n_rt)) > grid:
+        return "uniform"
+    T = next(T for T in range(1, max(n_rt) + 1) if count(T) <= grid)
+    wave = max(-(-n // pieces(n, T)) for n in n_rt) + 2
+    return "wave" if wave < max(load) else "uniform"
+
+
+@pytest.mark.parametrize("G,Hkv,QL,lens,plan", [
+    (8, 8, 8, [4000, 3900, 3000, 2200, 1700, 1600, 1100, 1000], "wave"),  # 70B-class heads
+    (8, 8, 8, [4100, 2000, 3500, 900], "wave"),                          # up to 16 splits
+    (4, 3, 48, [2500, 900, 1800], "wave"),         # one head per item, two tiles per head
+    (4, 8, 16, [2600, 2400, 900, 1500, 300, 2000, 1100, 700], "wave"),
+    (4, 8, 8, [1048, 1232, 159, 1236, 771, 835, 992, 520] * 4, "uniform"),  # 2 splits at most
+    (8, 8, 8, [4100, 2900], "uniform"),
+])
+def test_query_major_split_plans(pk, G, Hkv, QL, lens, plan):
+    """Split keys under both plans: every unit split the workspace's number
+    of ways, or one wave of pieces of at most T chunks, where a row may have
+    fewer splits than the workspace holds and its last split marks the rest
+    empty. The workspace is filled with 0x7f bytes first (partials of m =
+    3.4e38), so a slot left unmarked would swamp the merge."""
+    import torch
+
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert _split_plan(lens, QL, G, Hkv, 152) == plan
+    q, kc, vc, tables, lens, torch = _case(lens, QL, G * Hkv, Hkv, 128, seed=860 + QL + G)
+    p = pk.make_decode_params(q, torch.empty_like(q), kc, vc, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), max_context_len=int(lens.max()))
+    ws = torch.full((pk.pa_decode_workspace_size(p),), 0x7F, dtype=torch.uint8, device="cuda")
+    _check(pk, q, kc, vc, tables, lens, torch, workspace=ws)
+
+
+def test_query_major_one_wave_with_an_empty_sequence(pk):
+    """An empty sequence in a one-wave plan: one item with no keys, whose
+    partials (and the row's unused slots) are empty, so its rows come out
+    zero; the other rows match the oracle."""
+    import torch
+
+    lens = [3000, 0, 2500, 1200, 800, 2000]
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert _split_plan(lens, 8, 8, 8, 152) == "wave"
+    q, kc, vc, tables, lens, torch = _case(lens, 8, 64, 8, 128, seed=880)
+    p = pk.make_decode_params(q, torch.empty_like(q), kc, vc, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), max_context_len=int(lens.max()))
+    ws = torch.full((pk.pa_decode_workspace_size(p),), 0x7F, dtype=torch.uint8, device="cuda")
+    out = _decode(pk, q, kc, vc, tables, lens, torch, workspace=ws)
+    assert pk.pa_device_errors() == 0
+    got = harness.bf16_tensor_to_f64(out)
+    assert not got[1].any()
+    keep = [0, 2, 3, 4, 5]
+    want = oracle.paged_decode_multi(q.cpu()[keep], kc.cpu(), vc.cpu(), tables[keep], lens[keep])
+    harness.assert_close(got[keep], want)
+
+
 @pytest.mark.parametrize("seed", range(24))
 def test_query_major_random_shapes(pk, seed):
     """Seeded random shapes across the query-major space: G, the KV head
