@@ -489,6 +489,35 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
       const uint32_t idle_mask = P.wait_ns < dev::kShortWaitNs ? 0u : 255u;
       while (ok && v_more) {
         bool progress = false;
+        // the value product of chunk gv once its P is written (and, on an
+        // item's first chunk, once its O accumulator has been read out); it
+        // goes before the next scores when both are ready, so that its ring
+        // slot frees without waiting for them (an MMA issue blocks while the
+        // pipe is busy)
+        if (gv < gs && dev::mbar_test(&bar_p[gv & 1], uint32_t(gv >> 1) & 1u) &&
+            (cv > 0 || dev::mbar_test(&oempty[qv & 1], (uint32_t(qv >> 1) & 1u) ^ 1u))) {
+          dev::tc_fence_after();
+          const uint32_t vb = dev::smem_addr(ring + size_t(gv % QM_ST) * QM_SLOT + QM_KV_BYTES);
+          const uint32_t od = tmem + 2 * QM_KC + uint32_t(qv & 1) * QM_D;
+#pragma unroll
+          for (int kk = 0; kk < QM_KC / 16; ++kk)
+            mma_bf16_tmem_a(od, tmem + QM_TMEM_P + uint32_t(gv & 1) * 32 + uint32_t(kk * 8),
+                            // V MN-major: next 8 rows 1024 B on (SBO), second 64-d
+                            // half one half on (LBO)
+                            dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
+                            QM_IDESC_PV, cv > 0 || kk > 0);
+          dev::mma_commit(&bar_o[gv & 1]);
+          dev::mma_commit(&empty[gv % QM_ST]);
+          *consumed = gv + 1;
+          ++gv;
+          if (++cv == itv.n) {
+            ++qv;
+            ++jv;
+            cv = 0;
+            v_more = seek(jv, cv, itv);
+          }
+          progress = true;
+        }
         // the scores of chunk gs: it has landed, its Q is in, and the softmax
         // of chunk gs - 2 has read S[gs % 2] (its value product is issued)
         if (s_more && gs <= gv + 1 &&
@@ -514,32 +543,6 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
             ++js;
             cs = 0;
             s_more = seek(js, cs, its);
-          }
-          progress = true;
-        }
-        // the value product of chunk gv once its P is written (and, on an
-        // item's first chunk, once its O accumulator has been read out)
-        if (gv < gs && dev::mbar_test(&bar_p[gv & 1], uint32_t(gv >> 1) & 1u) &&
-            (cv > 0 || dev::mbar_test(&oempty[qv & 1], (uint32_t(qv >> 1) & 1u) ^ 1u))) {
-          dev::tc_fence_after();
-          const uint32_t vb = dev::smem_addr(ring + size_t(gv % QM_ST) * QM_SLOT + QM_KV_BYTES);
-          const uint32_t od = tmem + 2 * QM_KC + uint32_t(qv & 1) * QM_D;
-#pragma unroll
-          for (int kk = 0; kk < QM_KC / 16; ++kk)
-            mma_bf16_tmem_a(od, tmem + QM_TMEM_P + uint32_t(gv & 1) * 32 + uint32_t(kk * 8),
-                            // V MN-major: next 8 rows 1024 B on (SBO), second 64-d
-                            // half one half on (LBO)
-                            dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
-                            QM_IDESC_PV, cv > 0 || kk > 0);
-          dev::mma_commit(&bar_o[gv & 1]);
-          dev::mma_commit(&empty[gv % QM_ST]);
-          *consumed = gv + 1;
-          ++gv;
-          if (++cv == itv.n) {
-            ++qv;
-            ++jv;
-            cv = 0;
-            v_more = seek(jv, cv, itv);
           }
           progress = true;
         }
