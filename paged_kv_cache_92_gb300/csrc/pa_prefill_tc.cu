@@ -1037,6 +1037,41 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
       };
       while (ok && (v_more[0] || v_more[1])) {
         bool progress = false;
+        // the value product of chunk gv[t] of tile t once its P is written
+        // (and, on an item's first chunk, once tile t's O has been read out);
+        // a ring slot frees when both tiles' value products of its chunk are in.
+        // They go before the next scores when both are ready (an MMA issue
+        // blocks while the pipe is busy).
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int g = gv[t];
+          if (v_more[t] && g < gs &&
+              dev::mbar_test(&bar_p[t * 2 + (g & 1)], uint32_t(g >> 1) & 1u) &&
+              (cv[t] > 0 || qv[t] == 0 ||
+               dev::mbar_test(&oempty[t], uint32_t(qv[t] - 1) & 1u))) {
+            dev::tc_fence_after();
+            const uint32_t vb = dev::smem_addr(ring + size_t(g % QM_ST) * QM_SLOT + QM_KV_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < QM_KC / 16; ++kk)
+              mma_bf16_tmem_a(tmem + QD_TMEM_O + uint32_t(t * QM_D),
+                              tmem + uint32_t(t * 128 + (g & 1) * QM_KC + kk * 8),
+                              dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
+                              QM_IDESC_PV, cv[t] > 0 || kk > 0);
+            dev::mma_commit(&bar_o[t * 2 + (g & 1)]);
+            ++gv[t];
+            if (gv[1 - t] > g) {  // the other tile's value product of chunk g is in too
+              dev::mma_commit(&empty[g % QM_ST]);
+              *consumed = g + 1;
+            }
+            if (++cv[t] == itv[t].n) {
+              ++qv[t];
+              ++jv[t];
+              cv[t] = 0;
+              v_more[t] = seek(jv[t], cv[t], itv[t]);
+            }
+            progress = true;
+          }
+        }
         // scores of chunk gs for both tiles: it has landed, the item's Q is in,
         // and each tile's value product of chunk gs - 2 (which read P from
         // the same S buffer) has completed
@@ -1069,39 +1104,6 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
             s_more = seek(js, cs, its);
           }
           progress = true;
-        }
-        // the value product of chunk gv[t] of tile t once its P is written
-        // (and, on an item's first chunk, once tile t's O has been read out);
-        // a ring slot frees when both tiles' value products of its chunk are in
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int g = gv[t];
-          if (v_more[t] && g < gs &&
-              dev::mbar_test(&bar_p[t * 2 + (g & 1)], uint32_t(g >> 1) & 1u) &&
-              (cv[t] > 0 || qv[t] == 0 ||
-               dev::mbar_test(&oempty[t], uint32_t(qv[t] - 1) & 1u))) {
-            dev::tc_fence_after();
-            const uint32_t vb = dev::smem_addr(ring + size_t(g % QM_ST) * QM_SLOT + QM_KV_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < QM_KC / 16; ++kk)
-              mma_bf16_tmem_a(tmem + QD_TMEM_O + uint32_t(t * QM_D),
-                              tmem + uint32_t(t * 128 + (g & 1) * QM_KC + kk * 8),
-                              dev::smem_desc(vb + kk * 2048, QM_HALF_KV, 1024, dev::kSwizzle128B),
-                              QM_IDESC_PV, cv[t] > 0 || kk > 0);
-            dev::mma_commit(&bar_o[t * 2 + (g & 1)]);
-            ++gv[t];
-            if (gv[1 - t] > g) {  // the other tile's value product of chunk g is in too
-              dev::mma_commit(&empty[g % QM_ST]);
-              *consumed = g + 1;
-            }
-            if (++cv[t] == itv[t].n) {
-              ++qv[t];
-              ++jv[t];
-              cv[t] = 0;
-              v_more[t] = seek(jv[t], cv[t], itv[t]);
-            }
-            progress = true;
-          }
         }
         if (progress) {
           idle = 0;
