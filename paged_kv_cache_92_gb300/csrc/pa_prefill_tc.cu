@@ -64,6 +64,10 @@ constexpr int QM_OFF_PLAN = QM_OFF_ORDER + 1024;     // first item of each (rank
 constexpr int QM_SMEM = QM_OFF_PLAN + 512 + 1024;    // + alignment slack
 static_assert(QM_SMEM <= kMaxDynSmem, "shared memory budget");
 constexpr int QM_MAX_RANKED = 256;
+// CTAs of a split launch at most: the split plans stage 512 ints and one int
+// per CTA in the still-empty ring
+constexpr int QM_MAX_SPLIT_GRID = 4096;
+static_assert(QM_ST * QM_SLOT >= (512 + QM_MAX_SPLIT_GRID) * int(sizeof(int)), "plan scratch");
 // TMEM: S[2] at [0, 128), O[2] at [128, 384), P[2] at [384, 448)
 constexpr uint32_t QM_TMEM_COLS = 512;
 constexpr uint32_t QM_TMEM_P = 384;
@@ -1370,7 +1374,8 @@ int launch_qm_t(const pa_decode_params* p, cudaStream_t stream, float* part_ml, 
   attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   // split launches take every SM: the one-wave plan may cut more items
-  cfg.gridDim = dim3(unsigned(SPLIT ? sms : std::min(P.num_items, sms)));
+  cfg.gridDim =
+      dim3(unsigned(SPLIT ? std::min(sms, QM_MAX_SPLIT_GRID) : std::min(P.num_items, sms)));
   cfg.blockDim = dim3(QM_THREADS);
   cfg.dynamicSmemBytes = QM_SMEM;
   cfg.stream = stream;
