@@ -171,9 +171,11 @@ typedef struct {
                                   num_kv_heads * G * Qp <= 128 (64 for the 8-bit cache); a
                                   sequence with more new tokens is decoded as several groups,
                                   each streaming the keys its last token sees, with num_seqs *
-                                  groups <= 16384. Shapes beyond that, and the CUDA-core
-                                  variant, decode each (sequence, token) on its own with
-                                  num_seqs * Q <= 65535 (else PA_ERR_UNSUPPORTED). A sequence
+                                  groups <= 16384. Shapes beyond that (or with num_kv_heads
+                                  other than 1, 2, 4 and 8), and the CUDA-core variant, need
+                                  num_seqs * Q <= 65535 (else PA_ERR_UNSUPPORTED), also where
+                                  the query-major kernel takes them; off that kernel they decode
+                                  each (sequence, token) on its own. A sequence
                                   with 0 < context_lens[b] < Q gets zero rows and
                                   PA_DEVERR_CONTEXT_LEN. */
   int32_t wait_timeout_us;     /* tensor-core kernel: the longest one of its barrier waits may
